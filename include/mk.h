@@ -1,0 +1,184 @@
+/*
+ * mk.h -- C ABI of libmk: a dense Llama/Qwen-style decoder forward pass run as
+ * one persistent GB300 (sm_103a) kernel whose operators synchronise on
+ * individual tiles of the intermediate tensors.
+ *
+ * Sources of the operations:
+ *  - "MegaOps: A Kernel Overlapping Framework with PyTorch-like Modularity and
+ *    Megakernel Performance" (arXiv 2611.16248), Abstract: dependencies are
+ *    enforced on individual tiles of the intermediate tensor a producer writes
+ *    and a consumer reads; weights are prefetched while the preceding operator
+ *    runs; the comparison point is the kernel-per-operator paradigm; the models
+ *    are dense Llama3 and Qwen3, decode and prefill.
+ *  - "Lecture 112: Production Megakernels for Real-World Inference", Key
+ *    takeaways and Technical details: an on-device interpreter whose cores
+ *    atomically pop instructions from a global queue in DRAM; barriers held as
+ *    tensors; shapes, extents and barriers expressed symbolically in the
+ *    sequence length S and context length P so the work queue is built once;
+ *    memory pipelining across output tiles; the host stays out of the hot loop.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are caller-owned DEVICE memory unless a name ends in _host.
+ *    bf16 tensors are passed as raw 16-bit words; weights are [out, in]
+ *    row-major, 16-byte aligned.  The library never copies or repacks weights;
+ *    they must stay valid and unchanged while the plan lives.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on `stream`; one plan is driven by one stream at a
+ *    time.
+ *  - Return value: MK_OK or an MK_ERR_* code.  Argument errors are returned
+ *    before anything is launched.  Errors raised on the device (a wait that ran
+ *    out of time, an out-of-range token or position) are latched in a device
+ *    status word, returned by mk_status(), and every later launch on that plan
+ *    returns the latched code without launching until mk_plan_reset().
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MK_OK = 0,
+  MK_ERR_INVALID_ARG = 1, /* bad pointer, size or shape; nothing launched      */
+  MK_ERR_CUDA = 2,        /* a CUDA runtime call failed                          */
+  MK_ERR_TIMEOUT = 3,     /* a device-side wait exceeded its limit (latched)     */
+  MK_ERR_BOUNDS = 4,      /* a token/position/operand out of range (latched)     */
+  MK_ERR_UNSUPPORTED = 5, /* shape not supported by this build                   */
+  MK_ERR_NO_DEVICE = 6    /* no usable CUDA device                               */
+};
+
+enum { MK_DECODE = 0, MK_PREFILL = 1 };
+
+typedef struct mk_plan mk_plan; /* opaque, library-owned */
+
+/* Model shape.  Llama-3: qk_norm = 0.  Qwen3: qk_norm = 1 (per-head RMSNorm of
+ * q and k over head_dim, same eps, applied before RoPE).  tied_embeddings = 1
+ * makes the LM head read the embedding matrix. */
+typedef struct {
+  int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rms_eps, rope_theta;
+  int qk_norm;
+  int tied_embeddings;
+} mk_model_cfg;
+
+/* Device pointers to bf16 weights.  The per-layer fields point to HOST arrays
+ * of n_layers device pointers (copied at plan creation).  q_norm/k_norm may be
+ * NULL when qk_norm == 0; lm_head may be NULL when tied_embeddings == 1. */
+typedef struct {
+  const void *embed;      /* [vocab, hidden]                 */
+  const void *final_norm; /* [hidden]                        */
+  const void *lm_head;    /* [vocab, hidden] or NULL if tied */
+  const void *const *attn_norm; /* [hidden]                  */
+  const void *const *wq;        /* [n_q_heads*head_dim, hidden]  */
+  const void *const *wk;        /* [n_kv_heads*head_dim, hidden] */
+  const void *const *wv;        /* [n_kv_heads*head_dim, hidden] */
+  const void *const *wo;        /* [hidden, n_q_heads*head_dim]  */
+  const void *const *q_norm;    /* [head_dim] or NULL            */
+  const void *const *k_norm;    /* [head_dim] or NULL            */
+  const void *const *ffn_norm;  /* [hidden]                      */
+  const void *const *w_gate;    /* [ffn, hidden]                 */
+  const void *const *w_up;      /* [ffn, hidden]                 */
+  const void *const *w_down;    /* [hidden, ffn]                 */
+} mk_weight_ptrs;
+
+/* Build the tile DAG, the instruction queues and the barrier tensors for up to
+ * max_batch sequences of up to max_ctx cached positions (queue extents are
+ * symbolic in batch, S and P, so nothing is rebuilt when those change), and
+ * allocate the plan's device scratch (activations, barrier counters, RoPE
+ * table).  Uses the current CUDA device.  *out receives the plan. */
+int mk_plan_create(const mk_model_cfg *cfg, const mk_weight_ptrs *w, int max_batch, int max_ctx,
+                   mk_plan **out);
+void mk_plan_destroy(mk_plan *plan);
+
+/* Bytes of the KV cache the caller must allocate:
+ * bf16 [n_layers][2 (k, v)][max_batch][n_kv_heads][max_ctx][head_dim].
+ * Keys are stored after RoPE (and after the q/k norm when enabled). */
+size_t mk_kv_cache_bytes(const mk_plan *plan);
+
+/* One decode step for `batch` (1..max_batch) sequences, one persistent launch.
+ * tokens[b]: new token id of sequence b (device int32 [batch]).
+ * positions[b]: number of tokens already cached for sequence b (device int32
+ *   [batch]); the new token attends over positions[b]+1 keys and its k/v are
+ *   written to cache slot positions[b] of sequence slot b.  Must be < max_ctx.
+ * logits: device float [batch, vocab].  */
+int mk_decode_step(mk_plan *plan, const int32_t *tokens, const int32_t *positions, int batch,
+                   void *kv_cache, float *logits, void *stream);
+
+/* Same step with HOST buffers: copies tokens/positions in, runs the step, copies
+ * logits [batch, vocab] out, and waits for the stream.  Host buffers should be
+ * pinned for full speed.  Returns the device status after the wait. */
+int mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const int32_t *positions_host,
+                        int batch, void *kv_cache, float *logits_host, void *stream);
+
+/* Prefill one prompt of `len` tokens (1..max_ctx) into sequence slot 0 of the
+ * cache at positions 0..len-1, causal; writes the last token's logits
+ * (device float [vocab]). */
+int mk_prefill(mk_plan *plan, const int32_t *tokens, int len, void *kv_cache, float *logits,
+               void *stream);
+
+/* The same tile routines launched kernel-per-operator on `stream` (one launch
+ * per operator per layer, ordered by the stream), the comparison point.  mode is
+ * MK_DECODE (batch_or_len = batch, positions used) or MK_PREFILL (batch_or_len =
+ * prompt length, positions ignored).  use_graph = 1 captures the launches into
+ * a CUDA graph on first use for these pointers and replays it. */
+int mk_run_per_op(mk_plan *plan, int mode, int use_graph, const int32_t *tokens,
+                  const int32_t *positions, int batch_or_len, void *kv_cache, float *logits,
+                  void *stream);
+
+/* Wait for `stream`, then return the plan's device status word (MK_OK or the
+ * first latched MK_ERR_*). */
+int mk_status(mk_plan *plan, void *stream);
+/* Clear a latched error and the barrier counters (after a timeout). */
+int mk_plan_reset(mk_plan *plan, void *stream);
+const char *mk_status_string(int code);
+
+/* Plan facts, for tests and measurement. */
+typedef struct {
+  uint32_t n_instr_decode;  /* instructions in the decode queue            */
+  uint32_t n_instr_prefill; /* instructions in the prefill queue (0: none) */
+  uint32_t n_barriers;      /* uint32 counters in the barrier tensor       */
+  uint32_t n_launches_per_op_decode; /* kernel launches of one per-op step */
+  uint32_t n_ctas;          /* CTAs of a persistent launch                  */
+  uint32_t n_splits;        /* split-KV partitions per (sequence, kv head)  */
+  uint64_t weight_bytes;    /* bf16 weight bytes one decode step streams    */
+  uint64_t scratch_bytes;   /* device scratch owned by the plan             */
+} mk_plan_stats;
+int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
+
+/* Host-only check (no GPU needed): build the plan's queues for this shape,
+ * optionally in a seeded random topological order, and run them through a
+ * sequential simulator of the barrier counters.  Returns MK_OK if every wait is
+ * satisfied when reached and every barrier receives exactly the releases its
+ * waiters expect; fills *out (n_ctas/scratch_bytes are 0). */
+int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
+                  mk_plan_stats *out);
+
+/* Test and measurement options.  force_ctas > 0 launches that many persistent
+ * CTAs (<= the co-resident limit); queue_perm_seed != 0 rebuilds the decode
+ * queue in a seeded random topological order; trace = 1 records one 32-byte
+ * record per instruction; wait_limit_ns bounds every device-side wait
+ * (0 = default 2 s). */
+int mk_plan_set_debug(mk_plan *plan, int force_ctas, uint64_t queue_perm_seed, int trace,
+                      uint64_t wait_limit_ns);
+
+/* Test-only fault injection, made on the host: instruction `index` of the
+ * persistent queue (pop order) no longer releases its barrier, so the
+ * consumers of that barrier wait until their bounded wait gives up and the
+ * launch ends with MK_ERR_TIMEOUT latched.  The next mk_plan_set_debug()
+ * rebuilds the queue; mk_plan_reset() clears the latched error. */
+int mk_plan_debug_drop_release(mk_plan *plan, uint32_t index);
+
+/* Copy the trace of the last traced launch: records of
+ * {uint32 smid, uint32 op | layer << 8, uint64 t_begin, uint64 t_ready, uint64 t_done}
+ * (%globaltimer ns), one per instruction in pop order.  *n_records receives the
+ * count copied.  Waits for the device. */
+int mk_trace_copy(mk_plan *plan, void *host_buf, size_t bytes, size_t *n_records);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,99 @@
+"""The C ABI library loads, exports every symbol include/mk.h declares, and its
+host-only plan builder produces queues that a sequential barrier simulator
+accepts.  No GPU needed (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from tile_level_overlap_gb300 import build, mk, synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mk.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mk.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mk_[a-z_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(mk.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.mk_status_string(code)
+    assert lib.mk_status_string(0) == b"ok"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_create_without_device_reports_no_device(lib):
+    cfg = mk.model_cfg(synth.TOY_1L)
+    w = mk.mk_weight_ptrs()
+    h = ctypes.c_void_p()
+    assert lib.mk_plan_create(ctypes.byref(cfg), ctypes.byref(w), 1, 16, ctypes.byref(h)) in (
+        mk.MK_ERR_NO_DEVICE, mk.MK_ERR_INVALID_ARG)
+
+
+def _expected_weight_bytes(c):
+    qkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim * c.hidden
+    o = c.hidden * c.n_q_heads * c.head_dim
+    ffn = 3 * c.ffn * c.hidden
+    return 2 * (c.n_layers * (qkv + o + ffn) + c.vocab * c.hidden)
+
+
+@pytest.mark.parametrize("cfg,mb,mc", [
+    (synth.TOY_1L, 1, 129), (synth.TOY_1L, 8, 129), (synth.TOY_1L, 3, 17),
+    (synth.LLAMA32_1B, 1, 1025), (synth.LLAMA3_8B, 1, 4097),
+    (synth.TOY_1L.replace(qk_norm=True), 2, 64),
+])
+def test_plan_check_valid(lib, cfg, mb, mc):
+    rc, st = mk.plan_check(cfg, mb, mc)
+    assert rc == mk.MK_OK
+    assert st.weight_bytes == _expected_weight_bytes(cfg)
+    assert st.n_launches_per_op_decode == 5 * cfg.n_layers + 1
+    assert st.n_splits >= 1
+    # symbolic extents: the queue does not depend on the runtime batch or positions,
+    # only on the plan's maxima
+    rc2, st2 = mk.plan_check(cfg, mb, mc)
+    assert st2.n_instr_decode == st.n_instr_decode
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3, 4, 5])
+def test_plan_check_random_topological_orders(lib, seed):
+    rc, _ = mk.plan_check(synth.LLAMA32_1B.replace(n_layers=3), 1, 1025, seed=seed)
+    assert rc == mk.MK_OK
+    rc, _ = mk.plan_check(synth.TOY_1L, 4, 65, seed=seed)
+    assert rc == mk.MK_OK
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(head_dim=96), mk.MK_ERR_UNSUPPORTED),
+    (dict(n_q_heads=5), mk.MK_ERR_INVALID_ARG),
+    (dict(n_q_heads=6), mk.MK_ERR_UNSUPPORTED),
+    (dict(n_q_heads=48, n_kv_heads=2), mk.MK_ERR_UNSUPPORTED),
+    (dict(n_layers=0), mk.MK_ERR_INVALID_ARG),
+    (dict(hidden=260), mk.MK_ERR_UNSUPPORTED),
+])
+def test_plan_check_rejects(lib, bad, code):
+    rc, _ = mk.plan_check(synth.TOY_1L.replace(**bad), 1, 64)
+    assert rc == code
+
+
+def test_plan_check_rejects_sizes(lib):
+    assert mk.plan_check(synth.TOY_1L, 0, 64)[0] == mk.MK_ERR_INVALID_ARG
+    assert mk.plan_check(synth.TOY_1L, 1, 0)[0] == mk.MK_ERR_INVALID_ARG
+    assert mk.plan_check(synth.TOY_1L, 64, 64)[0] == mk.MK_ERR_UNSUPPORTED

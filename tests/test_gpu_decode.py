@@ -1,0 +1,219 @@
+"""Decode step on the GPU through the C ABI, against the CPU oracle.
+
+Tolerance (written here, per logits row b):
+    max_v |gpu[b, v] - oracle[b, v]| <= 2e-2 * RMS_v(oracle[b, :]).
+Bit-identity (exact) across repeated runs, persistent-CTA counts, random
+topological queue orders, and against the kernel-per-operator runner.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tile_level_overlap_gb300 import build, mk, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def _assert_rows_close(got, ref, tol=TOL):
+    got = np.asarray(got, dtype=np.float64).reshape(ref.shape)
+    for b in range(ref.shape[0]):
+        rms = np.sqrt((ref[b] ** 2).mean())
+        err = np.abs(got[b] - ref[b]).max()
+        assert err <= tol * rms, f"row {b}: max |delta| {err:.4e} > {tol} * rms {rms:.4e}"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    mk.lib()
+
+
+class Model:
+    def __init__(self, cfg, max_batch, max_ctx, seed=0):
+        self.cfg = cfg
+        self.dev = torch.device("cuda:0")
+        self.w = synth.make_weights(cfg, seed=seed, device=self.dev)
+        self.kv = synth.make_kv_cache(cfg, max_batch, max_ctx, device=self.dev)
+        self.plan = mk.Plan(cfg, self.w, max_batch, max_ctx)
+        assert self.plan.kv_cache_bytes() == self.kv.numel() * 2
+
+    def step(self, tokens, positions, per_op=False, graph=False):
+        t = torch.as_tensor(tokens, dtype=torch.int32).to(self.dev)
+        p = torch.as_tensor(positions, dtype=torch.int32).to(self.dev)
+        logits = torch.full((len(tokens), self.cfg.vocab), float("nan"), device=self.dev)
+        if per_op:
+            self.plan.run_per_op(mk.MK_DECODE, t, p, self.kv, logits, use_graph=graph)
+        else:
+            self.plan.decode_step(t, p, self.kv, logits)
+        rc = self.plan.status()
+        assert rc == mk.MK_OK, mk.lib().mk_status_string(rc)
+        return logits.cpu().numpy()
+
+    def oracle(self, tokens, positions, kv_bits=None):
+        kv_bits = synth.bf16_bits(self.kv) if kv_bits is None else kv_bits
+        return oracle.decode_step(self.cfg, synth.LazyBits(self.w), tokens, positions, kv_bits)
+
+    def close(self):
+        self.plan.close()
+        del self.w, self.kv
+        torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def toy():
+    m = Model(synth.TOY_1L, max_batch=4, max_ctx=129)
+    yield m
+    m.close()
+
+
+@pytest.mark.parametrize("pos", [0, 1, 5, 63, 64, 127, 128])
+def test_toy_decode_matches_oracle(toy, pos):
+    tokens = synth.make_tokens(1, toy.cfg.vocab, seed=pos).numpy()
+    kv_before = synth.bf16_bits(toy.kv)
+    got = toy.step(tokens, [pos])
+    ref, knew, vnew = toy.oracle(tokens, [pos], kv_before)
+    _assert_rows_close(got, ref)
+    # the step wrote the new token's (rotated) key and value into slot pos, as bf16
+    kv_after = oracle.widen_bf16(synth.bf16_bits(toy.kv))
+    k_slot = kv_after[:, 0, 0, :, pos, :]
+    v_slot = kv_after[:, 1, 0, :, pos, :]
+    np.testing.assert_allclose(k_slot, knew[:, 0], rtol=1e-2, atol=1e-2)
+    np.testing.assert_allclose(v_slot, vnew[:, 0], rtol=1e-2, atol=1e-2)
+    # nothing else in the cache changed
+    mask = np.ones(kv_after.shape[4], dtype=bool)
+    mask[pos] = False
+    np.testing.assert_array_equal(kv_after[:, :, :, :, mask], oracle.widen_bf16(kv_before)[:, :, :, :, mask])
+
+
+@pytest.mark.parametrize("positions", [[0, 64, 128], [17, 3, 100, 128], [5]])
+def test_toy_batch_ragged(toy, positions):
+    B = len(positions)
+    tokens = synth.make_tokens(B, toy.cfg.vocab, seed=B).numpy()
+    kv_before = synth.bf16_bits(toy.kv)
+    got = toy.step(tokens, positions)
+    ref, _, _ = toy.oracle(tokens, positions, kv_before)
+    _assert_rows_close(got, ref)
+
+
+def test_toy_repeat_bit_identical(toy):
+    tokens, pos = [7, 8], [100, 50]
+    first = toy.step(tokens, pos)
+    for _ in range(9):
+        np.testing.assert_array_equal(toy.step(tokens, pos), first)
+
+
+def test_toy_per_op_and_graph_bit_identical(toy):
+    tokens, pos = [11, 12, 13], [128, 0, 77]
+    mega = toy.step(tokens, pos)
+    np.testing.assert_array_equal(toy.step(tokens, pos, per_op=True), mega)
+    np.testing.assert_array_equal(toy.step(tokens, pos, per_op=True, graph=True), mega)
+    np.testing.assert_array_equal(toy.step(tokens, pos, per_op=True, graph=True), mega)
+    np.testing.assert_array_equal(toy.step(tokens, pos), mega)
+
+
+def test_toy_cta_counts_and_queue_orders(toy):
+    tokens, pos = [3, 4], [128, 9]
+    ref = toy.step(tokens, pos)
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    for ctas in [1, 2, 7, n // 2, n]:
+        toy.plan.set_debug(force_ctas=ctas)
+        np.testing.assert_array_equal(toy.step(tokens, pos), ref)
+    for seed in [1, 2, 3, 4, 5]:
+        toy.plan.set_debug(force_ctas=0, queue_perm_seed=seed)
+        np.testing.assert_array_equal(toy.step(tokens, pos), ref)
+    toy.plan.set_debug()
+
+
+def test_toy_timeout_is_reported_and_recoverable(toy):
+    tokens, pos = [3], [20]
+    ref = toy.step(tokens, pos)
+    # host-made bad plan: the first QKV tile no longer releases its barrier
+    toy.plan.set_debug(wait_limit_ns=20_000_000)
+    toy.plan.debug_drop_release(0)
+    t = torch.tensor(tokens, dtype=torch.int32, device=toy.dev)
+    p = torch.tensor(pos, dtype=torch.int32, device=toy.dev)
+    logits = torch.empty((1, toy.cfg.vocab), device=toy.dev)
+    toy.plan.decode_step(t, p, toy.kv, logits)
+    assert toy.plan.status() == mk.MK_ERR_TIMEOUT
+    with pytest.raises(mk.MkError):  # latched: nothing launches
+        toy.plan.decode_step(t, p, toy.kv, logits)
+    toy.plan.set_debug()
+    toy.plan.reset()
+    np.testing.assert_array_equal(toy.step(tokens, pos), ref)
+
+
+def test_toy_out_of_range_token_and_position(toy):
+    dev = toy.dev
+    logits = torch.empty((1, toy.cfg.vocab), device=dev)
+    for tok, pos in [(toy.cfg.vocab, 3), (-1, 3), (2, 129), (2, -5)]:
+        t = torch.tensor([tok], dtype=torch.int32, device=dev)
+        p = torch.tensor([pos], dtype=torch.int32, device=dev)
+        toy.plan.decode_step(t, p, toy.kv, logits)
+        assert toy.plan.status() == mk.MK_ERR_BOUNDS
+        toy.plan.reset()
+    toy.step([1], [1])
+
+
+def test_toy_bad_arguments_rejected_before_launch(toy):
+    dev = toy.dev
+    t = torch.zeros(5, dtype=torch.int32, device=dev)
+    p = torch.zeros(5, dtype=torch.int32, device=dev)
+    logits = torch.empty((5, toy.cfg.vocab), device=dev)
+    with pytest.raises(mk.MkError) as e:
+        toy.plan.decode_step(t, p, toy.kv, logits)  # batch 5 > max_batch 4
+    assert e.value.code == mk.MK_ERR_INVALID_ARG
+    assert mk.lib().mk_decode_step(toy.plan.h, None, None, 1, None, None, None) == mk.MK_ERR_INVALID_ARG
+
+
+def test_toy_host_buffer_entry_point(toy):
+    tokens, pos = [9, 10], [128, 1]
+    ref = toy.step(tokens, pos)
+    th = torch.tensor(tokens, dtype=torch.int32).pin_memory()
+    ph = torch.tensor(pos, dtype=torch.int32).pin_memory()
+    lh = torch.empty((2, toy.cfg.vocab), dtype=torch.float32).pin_memory()
+    assert toy.plan.decode_step_host(th, ph, toy.kv, lh) == mk.MK_OK
+    np.testing.assert_array_equal(lh.numpy(), ref)
+
+
+def test_toy_qk_norm_decode():
+    m = Model(synth.TOY_1L.replace(qk_norm=True, rms_eps=1e-6, rope_theta=1e6), 2, 65, seed=3)
+    try:
+        for tokens, pos in [([5], [64]), ([6, 7], [0, 33])]:
+            kv_before = synth.bf16_bits(m.kv)
+            got = m.step(tokens, pos)
+            ref, _, _ = m.oracle(tokens, pos, kv_before)
+            _assert_rows_close(got, ref)
+    finally:
+        m.close()
+
+
+def test_llama32_1b_decode_full_size():
+    m = Model(synth.LLAMA32_1B, 1, 1025)
+    try:
+        tokens = synth.make_tokens(1, m.cfg.vocab).numpy()
+        got = m.step(tokens, [1024])
+        ref, _, _ = m.oracle(tokens, [1024])
+        _assert_rows_close(got, ref)
+        np.testing.assert_array_equal(m.step(tokens, [1024], per_op=True), got)
+    finally:
+        m.close()
+
+
+def test_llama3_8b_decode_full_size():
+    """The benchmarked workload: 32 layers, hidden 4096, context 4096, batch 1,
+    in the persistent launch configuration the benchmark times."""
+    m = Model(synth.LLAMA3_8B, 1, 4097)
+    try:
+        tokens = synth.make_tokens(1, m.cfg.vocab).numpy()
+        kv_before = synth.bf16_bits(m.kv)
+        got = m.step(tokens, [4096])
+        ref, _, _ = m.oracle(tokens, [4096], kv_before)
+        _assert_rows_close(got, ref)
+        np.testing.assert_array_equal(m.step(tokens, [4096]), got)
+    finally:
+        m.close()

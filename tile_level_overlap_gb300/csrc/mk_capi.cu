@@ -1,0 +1,456 @@
+// C ABI of libmk (declared in include/mk.h).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+#include "mk_plan.h"
+
+namespace mk {
+int smem_bytes();
+cudaError_t kernel_setup();
+cudaError_t max_coresident(int* per_sm);
+cudaError_t launch_mega(const KParams& p, int ctas, int fast, cudaStream_t st);
+cudaError_t launch_perop(const KParams& p, uint32_t first, uint32_t count, int fast,
+                         cudaStream_t st);
+}  // namespace mk
+
+using namespace mk;
+
+struct mk_plan {
+  HostPlan hp;
+  int device = 0, n_sms = 0, max_ctas = 0;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  Instr* d_queue = nullptr;     // default topological order (per-op ranges index it)
+  Instr* d_queue_mk = nullptr;  // order popped by the persistent kernel
+  unsigned long long* d_trace = nullptr;
+  int32_t* d_tok = nullptr;     // staging for the host-buffer entry point
+  int32_t* d_pos = nullptr;
+  float* d_logits = nullptr;
+  uint32_t* d_ctl = nullptr;
+  KParams base{};
+  int force_ctas = 0, trace = 0;
+  uint64_t wait_limit_ns = 2000000000ull;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t graph = nullptr;
+  uintptr_t graph_key[6] = {0, 0, 0, 0, 0, 0};
+  size_t kv_bytes = 0;
+  int latched = 0;  // device error seen by mk_status / the host-buffer step
+};
+
+namespace {
+
+struct Bump {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  }
+};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ERR_CUDA; }
+
+#define MK_CUDA(call)                        \
+  do {                                       \
+    cudaError_t e_ = (call);                 \
+    if (e_ != cudaSuccess) return MK_ERR_CUDA; \
+  } while (0)
+
+int upload_mk_queue(mk_plan* p, uint64_t seed) {
+  const std::vector<Instr>& q = p->hp.decode;
+  if (seed == 0)
+    return cuda_err(cudaMemcpy(p->d_queue_mk, q.data(), q.size() * sizeof(Instr),
+                               cudaMemcpyHostToDevice));
+  std::vector<Instr> perm;
+  random_topological(p->hp, q, seed, &perm);
+  std::string why;
+  if (perm.size() != q.size() || simulate(p->hp, perm, &why) != MK_OK) return MK_ERR_INVALID_ARG;
+  return cuda_err(cudaMemcpy(p->d_queue_mk, perm.data(), perm.size() * sizeof(Instr),
+                             cudaMemcpyHostToDevice));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_status_string(int code) {
+  switch (code) {
+    case MK_OK: return "ok";
+    case MK_ERR_INVALID_ARG: return "invalid argument";
+    case MK_ERR_CUDA: return "CUDA runtime error";
+    case MK_ERR_TIMEOUT: return "device-side wait timed out";
+    case MK_ERR_BOUNDS: return "token, position or operand out of range";
+    case MK_ERR_UNSUPPORTED: return "shape not supported by this build";
+    case MK_ERR_NO_DEVICE: return "no CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
+                  mk_plan_stats* out) {
+  if (!cfg) return MK_ERR_INVALID_ARG;
+  HostPlan hp;
+  std::string why;
+  int rc = build_plan(*cfg, max_batch, max_ctx, &hp, &why);
+  if (rc != MK_OK) return rc;
+  std::vector<Instr> q = hp.decode;
+  if (queue_perm_seed) {
+    random_topological(hp, hp.decode, queue_perm_seed, &q);
+    if (q.size() != hp.decode.size()) return MK_ERR_INVALID_ARG;
+  }
+  rc = simulate(hp, q, &why);
+  if (out) {
+    std::memset(out, 0, sizeof(*out));
+    out->n_instr_decode = (uint32_t)hp.decode.size();
+    out->n_barriers = hp.bl.total;
+    out->n_launches_per_op_decode = (uint32_t)hp.perop_decode.size();
+    out->n_splits = (uint32_t)hp.n_splits;
+    out->weight_bytes = hp.weight_bytes;
+  }
+  return rc;
+}
+
+int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_batch, int max_ctx,
+                   mk_plan** out) {
+  if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return MK_ERR_NO_DEVICE;
+  }
+  mk_plan* p = new mk_plan();
+  std::string why;
+  int rc = build_plan(*cfg, max_batch, max_ctx, &p->hp, &why);
+  if (rc != MK_OK) {
+    delete p;
+    return rc;
+  }
+  const HostPlan& hp = p->hp;
+  const mk_model_cfg& c = hp.cfg;
+  const int L = c.n_layers;
+  // weight pointers
+  std::vector<LayerW> lw(L);
+  auto ok = [](const void* q) { return q != nullptr && aligned16(q); };
+  bool good = ok(w->embed) && ok(w->final_norm) && (c.tied_embeddings || ok(w->lm_head)) &&
+              w->attn_norm && w->wq && w->wk && w->wv && w->wo && w->ffn_norm && w->w_gate &&
+              w->w_up && w->w_down && (!c.qk_norm || (w->q_norm && w->k_norm));
+  for (int l = 0; good && l < L; ++l) {
+    LayerW& x = lw[l];
+    x.attn_norm = (const uint16_t*)w->attn_norm[l];
+    x.wq = (const uint16_t*)w->wq[l];
+    x.wk = (const uint16_t*)w->wk[l];
+    x.wv = (const uint16_t*)w->wv[l];
+    x.wo = (const uint16_t*)w->wo[l];
+    x.q_norm = c.qk_norm ? (const uint16_t*)w->q_norm[l] : nullptr;
+    x.k_norm = c.qk_norm ? (const uint16_t*)w->k_norm[l] : nullptr;
+    x.ffn_norm = (const uint16_t*)w->ffn_norm[l];
+    x.wg = (const uint16_t*)w->w_gate[l];
+    x.wu = (const uint16_t*)w->w_up[l];
+    x.wd = (const uint16_t*)w->w_down[l];
+    good = ok(x.attn_norm) && ok(x.wq) && ok(x.wk) && ok(x.wv) && ok(x.wo) && ok(x.ffn_norm) &&
+           ok(x.wg) && ok(x.wu) && ok(x.wd) && (!c.qk_norm || (ok(x.q_norm) && ok(x.k_norm)));
+  }
+  if (!good) {
+    delete p;
+    return MK_ERR_INVALID_ARG;
+  }
+
+  auto fail = [&](int code) {
+    mk_plan_destroy(p);
+    return code;
+  };
+  if (cudaGetDevice(&p->device) != cudaSuccess) return fail(MK_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&p->n_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
+    return fail(MK_ERR_CUDA);
+  if (kernel_setup() != cudaSuccess) return fail(MK_ERR_CUDA);
+  int per_sm = 0;
+  if (max_coresident(&per_sm) != cudaSuccess || per_sm < 1) return fail(MK_ERR_CUDA);
+  p->max_ctas = p->n_sms;
+
+  // one scratch allocation
+  const int H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
+  const size_t B = (size_t)max_batch;
+  Bump bm;
+  const size_t o_resid = bm.take(sizeof(float) * (2 * L + 1) * B * H);
+  const size_t o_qkv = bm.take(sizeof(float) * L * B * hp.qkv_rows);
+  const size_t o_part = bm.take(sizeof(float) * L * B * nkv * hp.n_splits * hp.rep * (d + 2));
+  const size_t o_attn = bm.take(sizeof(float) * L * B * c.n_q_heads * d);
+  const size_t o_act = bm.take(sizeof(float) * L * B * F);
+  const size_t o_bars = bm.take(sizeof(uint32_t) * hp.bl.total);
+  const size_t o_arr = bm.take(sizeof(uint32_t) * L * B * nkv);
+  const size_t o_ctl = bm.take(sizeof(uint32_t) * CTL_WORDS);
+  const size_t o_q = bm.take(sizeof(Instr) * hp.decode.size());
+  const size_t o_qmk = bm.take(sizeof(Instr) * hp.decode.size());
+  const size_t o_expr = bm.take(sizeof(uint32_t) * hp.expr.size());
+  const size_t o_rope = bm.take(sizeof(float2) * (size_t)max_ctx * (d / 2));
+  const size_t o_lw = bm.take(sizeof(LayerW) * L);
+  const size_t o_tok = bm.take(sizeof(int32_t) * B);
+  const size_t o_pos = bm.take(sizeof(int32_t) * B);
+  const size_t o_log = bm.take(sizeof(float) * B * c.vocab);
+  p->scratch_bytes = bm.off;
+  if (cudaMalloc(&p->scratch, p->scratch_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MK_ERR_CUDA);
+  }
+  uint8_t* s = (uint8_t*)p->scratch;
+  if (cudaMemset(p->scratch, 0, p->scratch_bytes) != cudaSuccess) return fail(MK_ERR_CUDA);
+
+  std::vector<float2> rope((size_t)max_ctx * (d / 2));
+  for (int pos = 0; pos < max_ctx; ++pos)
+    for (int i = 0; i < d / 2; ++i) {
+      const double inv = std::pow((double)c.rope_theta, -2.0 * i / d);
+      const double a = (double)pos * inv;
+      rope[(size_t)pos * (d / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  p->d_queue = (Instr*)(s + o_q);
+  p->d_queue_mk = (Instr*)(s + o_qmk);
+  p->d_ctl = (uint32_t*)(s + o_ctl);
+  p->d_tok = (int32_t*)(s + o_tok);
+  p->d_pos = (int32_t*)(s + o_pos);
+  p->d_logits = (float*)(s + o_log);
+  if (cudaMemcpy(s + o_q, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(s + o_qmk, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(s + o_expr, hp.expr.data(), sizeof(uint32_t) * hp.expr.size(),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(s + o_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemcpy(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(MK_ERR_CUDA);
+  if (cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+    return fail(MK_ERR_CUDA);
+
+  KParams& k = p->base;
+  std::memset(&k, 0, sizeof(k));
+  k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = nkv; k.d = d; k.F = F; k.V = c.vocab;
+  k.qk_norm = c.qk_norm; k.rep = hp.rep; k.qkv_rows = hp.qkv_rows; k.eps = c.rms_eps;
+  k.max_batch = max_batch; k.max_ctx = max_ctx; k.n_splits = hp.n_splits;
+  k.r_qkv = hp.r_qkv; k.r_o = hp.r_o; k.r_gu = hp.r_gu; k.r_down = hp.r_down; k.r_lm = hp.r_lm;
+  k.n_qkv_tiles = hp.n_qkv_tiles; k.n_o_tiles = hp.n_o_tiles; k.n_gu_tiles = hp.n_gu_tiles;
+  k.n_down_tiles = hp.n_down_tiles; k.n_lm_tiles = hp.n_lm_tiles;
+  k.embed = (const uint16_t*)w->embed;
+  k.lm = (const uint16_t*)(c.tied_embeddings ? w->embed : w->lm_head);
+  k.final_norm = (const uint16_t*)w->final_norm;
+  k.layers = (const LayerW*)(s + o_lw);
+  k.resid = (float*)(s + o_resid);
+  k.qkv = (float*)(s + o_qkv);
+  k.part = (float*)(s + o_part);
+  k.attn_out = (float*)(s + o_attn);
+  k.act = (float*)(s + o_act);
+  k.bars = (uint32_t*)(s + o_bars);
+  k.arrive = (uint32_t*)(s + o_arr);
+  k.rope = (const float2*)(s + o_rope);
+  k.ctl = p->d_ctl;
+  k.queue = p->d_queue_mk;
+  k.n_instr = (uint32_t)hp.decode.size();
+  k.expr = (const uint32_t*)(s + o_expr);
+  k.bl = hp.bl;
+  p->kv_bytes = (size_t)L * 2 * B * nkv * (size_t)max_ctx * d * 2;
+  *out = p;
+  return MK_OK;
+}
+
+void mk_plan_destroy(mk_plan* p) {
+  if (!p) return;
+  if (p->graph) cudaGraphExecDestroy(p->graph);
+  if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
+  if (p->d_trace) cudaFree(p->d_trace);
+  if (p->scratch) cudaFree(p->scratch);
+  delete p;
+}
+
+size_t mk_kv_cache_bytes(const mk_plan* p) { return p ? p->kv_bytes : 0; }
+
+int mk_plan_get_stats(const mk_plan* p, mk_plan_stats* out) {
+  if (!p || !out) return MK_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  out->n_instr_decode = (uint32_t)p->hp.decode.size();
+  out->n_barriers = p->hp.bl.total;
+  out->n_launches_per_op_decode = (uint32_t)p->hp.perop_decode.size();
+  out->n_ctas = (uint32_t)(p->force_ctas ? p->force_ctas : p->max_ctas);
+  out->n_splits = (uint32_t)p->hp.n_splits;
+  out->weight_bytes = p->hp.weight_bytes;
+  out->scratch_bytes = p->scratch_bytes;
+  return MK_OK;
+}
+
+static int check_step(mk_plan* p, const void* tokens, const void* positions, int batch,
+                      const void* kv, const void* logits) {
+  if (!p || !tokens || !positions || !kv || !logits) return MK_ERR_INVALID_ARG;
+  if (batch < 1 || batch > p->hp.max_batch) return MK_ERR_INVALID_ARG;
+  if (!aligned16(kv)) return MK_ERR_INVALID_ARG;
+  if (p->latched) return p->latched;
+  return MK_OK;
+}
+
+static KParams step_params(mk_plan* p, const int32_t* tokens, const int32_t* positions, int batch,
+                           void* kv, float* logits) {
+  KParams k = p->base;
+  k.tokens = tokens;
+  k.positions = positions;
+  k.B = batch;
+  k.S = 0;
+  k.kv = (uint16_t*)kv;
+  k.logits = logits;
+  k.mode = MODE_MEGA;
+  k.trace = p->trace ? p->d_trace : nullptr;
+  k.wait_limit_ns = p->wait_limit_ns;
+  return k;
+}
+
+int mk_decode_step(mk_plan* p, const int32_t* tokens, const int32_t* positions, int batch,
+                   void* kv, float* logits, void* stream) {
+  int rc = check_step(p, tokens, positions, batch, kv, logits);
+  if (rc != MK_OK) return rc;
+  KParams k = step_params(p, tokens, positions, batch, kv, logits);
+  const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
+  return cuda_err(launch_mega(k, ctas, p->hp.fast_b1 ? 1 : 0, (cudaStream_t)stream));
+}
+
+int mk_decode_step_host(mk_plan* p, const int32_t* tokens_host, const int32_t* positions_host,
+                        int batch, void* kv, float* logits_host, void* stream) {
+  int rc = check_step(p, tokens_host, positions_host, batch, kv, logits_host);
+  if (rc != MK_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  MK_CUDA(cudaMemcpyAsync(p->d_tok, tokens_host, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, st));
+  MK_CUDA(cudaMemcpyAsync(p->d_pos, positions_host, sizeof(int32_t) * batch, cudaMemcpyHostToDevice,
+                          st));
+  rc = mk_decode_step(p, p->d_tok, p->d_pos, batch, kv, p->d_logits, stream);
+  if (rc != MK_OK) return rc;
+  uint32_t status = 0;
+  MK_CUDA(cudaMemcpyAsync(logits_host, p->d_logits, sizeof(float) * batch * p->hp.cfg.vocab,
+                          cudaMemcpyDeviceToHost, st));
+  MK_CUDA(cudaMemcpyAsync(&status, p->d_ctl + CTL_STATUS, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                          st));
+  MK_CUDA(cudaStreamSynchronize(st));
+  if (status) p->latched = (int)status;
+  return (int)status;
+}
+
+int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits, void* stream) {
+  (void)stream;
+  if (!p || !tokens || !kv || !logits || len < 1 || len > p->hp.max_ctx) return MK_ERR_INVALID_ARG;
+  return MK_ERR_UNSUPPORTED;
+}
+
+static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
+  const int fast = p->hp.fast_b1 ? 1 : 0;
+  for (const auto& r : p->hp.perop_decode) MK_CUDA(launch_perop(k, r.first, r.second, fast, st));
+  return MK_OK;
+}
+
+int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,
+                  const int32_t* positions, int batch_or_len, void* kv, float* logits,
+                  void* stream) {
+  if (mode == MK_PREFILL) {
+    if (!p || !tokens || !kv || !logits) return MK_ERR_INVALID_ARG;
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (mode != MK_DECODE) return MK_ERR_INVALID_ARG;
+  int rc = check_step(p, tokens, positions, batch_or_len, kv, logits);
+  if (rc != MK_OK) return rc;
+  KParams k = step_params(p, tokens, positions, batch_or_len, kv, logits);
+  k.queue = p->d_queue;
+  k.trace = nullptr;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!use_graph) return launch_per_op_seq(p, k, st);
+  const uintptr_t key[6] = {(uintptr_t)tokens, (uintptr_t)positions, (uintptr_t)batch_or_len,
+                            (uintptr_t)kv, (uintptr_t)logits, (uintptr_t)mode};
+  if (!p->graph || std::memcmp(key, p->graph_key, sizeof(key)) != 0) {
+    if (p->graph) {
+      cudaGraphExecDestroy(p->graph);
+      p->graph = nullptr;
+    }
+    cudaGraph_t g = nullptr;
+    MK_CUDA(cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int lrc = launch_per_op_seq(p, k, p->cap_stream);
+    cudaError_t e = cudaStreamEndCapture(p->cap_stream, &g);
+    if (lrc != MK_OK || e != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return MK_ERR_CUDA;
+    }
+    e = cudaGraphInstantiate(&p->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      p->graph = nullptr;
+      return MK_ERR_CUDA;
+    }
+    std::memcpy(p->graph_key, key, sizeof(key));
+  }
+  return cuda_err(cudaGraphLaunch(p->graph, st));
+}
+
+int mk_status(mk_plan* p, void* stream) {
+  if (!p) return MK_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MK_ERR_CUDA;
+  uint32_t status = 0;
+  if (cudaMemcpy(&status, p->d_ctl + CTL_STATUS, sizeof(status), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return MK_ERR_CUDA;
+  if (status) p->latched = (int)status;
+  return (int)status;
+}
+
+int mk_plan_reset(mk_plan* p, void* stream) {
+  if (!p) return MK_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
+  MK_CUDA(cudaMemset(p->base.bars, 0, sizeof(uint32_t) * p->hp.bl.total));
+  MK_CUDA(cudaMemset(p->base.arrive, 0,
+                     sizeof(uint32_t) * p->hp.cfg.n_layers * p->hp.max_batch * p->hp.cfg.n_kv_heads));
+  MK_CUDA(cudaMemset(p->d_ctl, 0, sizeof(uint32_t) * CTL_WORDS));
+  MK_CUDA(cudaDeviceSynchronize());
+  p->latched = 0;
+  return MK_OK;
+}
+
+int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int trace,
+                      uint64_t wait_limit_ns) {
+  if (!p || force_ctas < 0 || force_ctas > p->max_ctas) return MK_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MK_ERR_CUDA;
+  p->force_ctas = force_ctas;
+  p->wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
+  int rc = upload_mk_queue(p, queue_perm_seed);
+  if (rc != MK_OK) return rc;
+  if (trace && !p->d_trace) {
+    if (cudaMalloc(&p->d_trace, p->hp.decode.size() * 32) != cudaSuccess) return MK_ERR_CUDA;
+    MK_CUDA(cudaMemset(p->d_trace, 0, p->hp.decode.size() * 32));
+  }
+  p->trace = trace ? 1 : 0;
+  return MK_OK;
+}
+
+int mk_plan_debug_drop_release(mk_plan* p, uint32_t index) {
+  if (!p || index >= p->hp.decode.size()) return MK_ERR_INVALID_ARG;
+  Instr in;
+  MK_CUDA(cudaDeviceSynchronize());
+  MK_CUDA(cudaMemcpy(&in, p->d_queue_mk + index, sizeof(Instr), cudaMemcpyDeviceToHost));
+  in.rel_bar = NO_BAR;
+  in.flags = 0;
+  MK_CUDA(cudaMemcpy(p->d_queue_mk + index, &in, sizeof(Instr), cudaMemcpyHostToDevice));
+  return MK_OK;
+}
+
+int mk_trace_copy(mk_plan* p, void* host_buf, size_t bytes, size_t* n_records) {
+  if (!p || !host_buf || !n_records) return MK_ERR_INVALID_ARG;
+  *n_records = 0;
+  if (!p->d_trace) return MK_ERR_INVALID_ARG;
+  MK_CUDA(cudaDeviceSynchronize());
+  size_t n = p->hp.decode.size();
+  if (bytes / 32 < n) n = bytes / 32;
+  MK_CUDA(cudaMemcpy(host_buf, p->d_trace, n * 32, cudaMemcpyDeviceToHost));
+  *n_records = n;
+  return MK_OK;
+}
+
+}  // extern "C"

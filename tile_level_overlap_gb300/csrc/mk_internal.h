@@ -1,0 +1,186 @@
+// Internal layout shared by the host plan builder and the device interpreter.
+//
+// The instruction queue, barrier tensor and symbolic-extent expressions follow
+// "Lecture 112: Production Megakernels for Real-World Inference" (Technical
+// details: an interpreter loop pops fixed-size instructions from a queue in
+// DRAM; Key takeaways: barriers are tensors partitioned along the dependency
+// dimensions, and extents are expressions in S and P so the queue is built
+// once) and the MegaOps Abstract (a consumer waits on the tiles of the
+// intermediate tensor it reads, not on the producer kernel).
+#pragma once
+#include <stdint.h>
+#include <vector_types.h>
+
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__ __forceinline__
+#else
+#define MK_HD inline
+#endif
+
+namespace mk {
+
+// ---------------------------------------------------------------- opcodes
+enum Op : uint8_t {
+  OP_NOP = 0,
+  OP_QKV = 1,   // rows of [Wq;Wk;Wv] . rmsnorm(x)               (a0 = row0, a1 = rows)
+  OP_ATTN = 2,  // split-KV decode attention                      (a0 = seq, a1 = kv head, a2 = split)
+  OP_O = 3,     // rows of Wo . attn + residual                  (a0 = row0, a1 = rows)
+  OP_GU = 4,    // rows of Wg, Wu . rmsnorm(x), SwiGLU            (a0 = row0, a1 = rows)
+  OP_DOWN = 5,  // rows of Wd . act + residual                   (a0 = row0, a1 = rows)
+  OP_LM = 6,    // rows of W_lm . rmsnorm(x)                      (a0 = row0, a1 = rows)
+  OP_COUNT = 7
+};
+
+constexpr uint32_t NO_BAR = 0xffffffffu;
+constexpr uint8_t NO_EXPR = 0xff;
+
+// Instruction flags.
+constexpr uint8_t IF_RELEASE_ON_COMBINE = 1;  // release happens once per (seq, kv head) group
+
+// One queue record, 32 bytes.
+struct Instr {
+  uint8_t op, flags;
+  uint16_t layer;
+  uint32_t a0, a1;
+  uint16_t a2;
+  uint8_t x_lo, x_hi;    // symbolic extent [lo, hi) expressions (NO_EXPR: none)
+  uint32_t wait_bar;     // first waited barrier, or NO_BAR
+  uint32_t wait_target;  // releases per step expected on each waited barrier
+  uint16_t wait_n;       // number of barriers waited on
+  uint16_t wait_stride;  // index stride between them
+  uint32_t rel_bar;      // barrier this instruction releases (+1), or NO_BAR
+};
+static_assert(sizeof(Instr) == 32, "instruction record must stay 32 bytes");
+
+// ---------------------------------------------------------------- symbolic extents
+// Tiny postfix bytecode over the runtime variables.  Word = op << 24 | imm24.
+enum XOp : uint32_t {
+  X_END = 0, X_CONST = 1, X_ARG0 = 2, X_ARG1 = 3, X_ARG2 = 4,
+  X_B = 5,    // runtime batch
+  X_S = 6,    // runtime prompt length
+  X_POS = 7,  // pop b, push positions[b]
+  X_ADD = 8, X_SUB = 9, X_MUL = 10, X_CEILDIV = 11, X_MIN = 12, X_MAX = 13
+};
+constexpr int X_MAX_WORDS = 32;  // words per expression slot
+constexpr int X_STACK = 8;
+
+MK_HD uint32_t xw(uint32_t op, uint32_t imm = 0) { return (op << 24) | (imm & 0xffffffu); }
+
+// Evaluate expression `e` (X_MAX_WORDS words).  `pos` may be null when the
+// expression does not read positions.  Out-of-range positions evaluate as 0;
+// the caller validates them separately.
+MK_HD int64_t x_eval(const uint32_t* e, const Instr& in, int B, int S, const int32_t* pos,
+                     int n_pos) {
+  int64_t st[X_STACK];
+  int sp = 0;
+  for (int i = 0; i < X_MAX_WORDS; ++i) {
+    uint32_t w = e[i];
+    uint32_t op = w >> 24;
+    int64_t imm = (int64_t)(w & 0xffffffu);
+    if (op == X_END) break;
+    switch (op) {
+      case X_CONST: st[sp++] = imm; break;
+      case X_ARG0: st[sp++] = in.a0; break;
+      case X_ARG1: st[sp++] = in.a1; break;
+      case X_ARG2: st[sp++] = in.a2; break;
+      case X_B: st[sp++] = B; break;
+      case X_S: st[sp++] = S; break;
+      case X_POS: {
+        int64_t b = st[sp - 1];
+        st[sp - 1] = (pos && b >= 0 && b < n_pos) ? (int64_t)pos[b] : 0;
+        break;
+      }
+      default: {
+        int64_t y = st[--sp];
+        int64_t x = st[sp - 1];
+        int64_t r = 0;
+        if (op == X_ADD) r = x + y;
+        else if (op == X_SUB) r = x - y;
+        else if (op == X_MUL) r = x * y;
+        else if (op == X_CEILDIV) r = y > 0 ? (x + y - 1) / y : 0;
+        else if (op == X_MIN) r = x < y ? x : y;
+        else if (op == X_MAX) r = x > y ? x : y;
+        st[sp - 1] = r;
+      }
+    }
+  }
+  return sp > 0 ? st[sp - 1] : 0;
+}
+
+// Expression slots used by the plan.
+enum XSlot : uint8_t {
+  XS_ATTN_LO = 0,  // first key of split a2 of sequence a0: min(a2*ceil((P+1)/NS), P+1)
+  XS_ATTN_HI = 1,  // one past its last key
+  XS_SEQ_LIVE = 2, // B - a0  (> 0: sequence a0 is part of this step)
+  XS_COUNT = 3
+};
+
+// ---------------------------------------------------------------- barrier tensor layout
+// One flat uint32 array.  Decode sub-tensors (all per layer):
+//   qkv[L][n_kv]   : QKV row tiles of kv group g (its q heads, k_g, v_g) done
+//   attn[L]        : (sequence, kv group) attention outputs combined
+//   o[L]           : O-projection row tiles done (residual x1 complete when full)
+//   gu[L]          : gate/up row tiles done (SwiGLU activations complete)
+//   down[L]        : down-projection row tiles done (residual x2 complete)
+//   lm[1]          : LM-head row tiles done
+struct BarLayout {
+  uint32_t qkv, attn, o, gu, down, lm, total;
+};
+
+// Control words (device uint32 array).
+enum Ctl : int {
+  CTL_HEAD = 0,     // next queue index to pop
+  CTL_EXIT = 1,     // CTAs that left the loop this launch
+  CTL_GEN = 2,      // completed persistent launches (barrier generation)
+  CTL_ABORT = 3,    // nonzero: every CTA stops popping
+  CTL_STATUS = 4,   // first latched error code
+  CTL_DETAIL = 5,   // instruction index / value that raised it
+  CTL_WORDS = 8
+};
+
+// Per-layer weight pointers as the device sees them.
+struct LayerW {
+  const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *q_norm, *k_norm, *ffn_norm, *wg, *wu, *wd;
+};
+
+enum Mode : int { MODE_MEGA = 0, MODE_PEROP = 1 };
+
+// Everything one launch needs, passed by value as a __grid_constant__ parameter.
+struct KParams {
+  // shape
+  int L, H, nq, nkv, d, F, V, qk_norm, rep, qkv_rows;
+  float eps;
+  int max_batch, max_ctx, n_splits;
+  // tiling
+  int r_qkv, r_o, r_gu, r_down, r_lm;
+  uint32_t n_qkv_tiles, n_o_tiles, n_gu_tiles, n_down_tiles, n_lm_tiles;
+  // weights
+  const uint16_t *embed, *lm, *final_norm;
+  const LayerW* layers;
+  // plan-owned scratch
+  float* resid;     // [2L+1][max_batch][H]
+  float* qkv;       // [L][max_batch][qkv_rows]
+  float* part;      // [L][max_batch][nkv][n_splits][rep][d+2]
+  float* attn_out;  // [L][max_batch][nq*d]
+  float* act;       // [L][max_batch][F]
+  uint32_t* bars;   // barrier tensor
+  uint32_t* arrive; // [L][max_batch][nkv] split arrival counters
+  const float2* rope;  // [max_ctx][d/2] (cos, sin)
+  uint32_t* ctl;
+  const Instr* queue;
+  uint32_t n_instr;
+  const uint32_t* expr;  // [XS_COUNT][X_MAX_WORDS]
+  unsigned long long* trace;  // 4 x u64 per instruction, or null
+  BarLayout bl;
+  // step
+  const int32_t* tokens;
+  const int32_t* positions;
+  int B, S;
+  uint16_t* kv;
+  float* logits;
+  int mode;
+  uint32_t perop_base;
+  unsigned long long wait_limit_ns;
+};
+
+}  // namespace mk

@@ -1,0 +1,895 @@
+// The persistent interpreter and its tile routines (sm_103a).
+//
+// One CTA per SM: a producer warp pops instructions from the global queue
+// (one atomic per instruction) and streams each instruction's dependency-free
+// operand bytes -- weight rows, or cached K/V rows -- into a shared-memory ring
+// with bulk async copies, running ahead of the consumers by up to NSTAGE
+// stages and NISLOT instructions.  Eight consumer warps take instructions in
+// pop order, wait (bounded) on the per-tile barrier counters of the tiles they
+// read, compute from the ring, store their output tile and release its
+// counter.  This is the on-device interpreter of "Lecture 112: Production
+// Megakernels for Real-World Inference" (Technical details: a loop with a
+// switch, instructions popped atomically from a queue in DRAM; memory
+// pipelining across output tiles) with the tile-level dependencies and the
+// weight prefetch across operator boundaries of the MegaOps Abstract.
+//
+// The same kernel runs kernel-per-operator (MODE_PEROP): one instruction per
+// CTA, no waits and no barrier releases; stream order replaces the counters.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mk_device.cuh"
+#include "mk_internal.h"
+#include "mk_plan.h"
+
+namespace mk {
+
+constexpr uint32_t END_SLOT = 0xffffffffu;
+constexpr int CONSUMER_BAR = 1;
+
+// Shared-memory layout (dynamic).
+struct SmemLayout {
+  static constexpr int ring = 0;
+  static constexpr int xbuf = ring + NSTAGE * STAGE_BYTES;
+  static constexpr int red = xbuf + XBUF_BYTES;            // [RMAX][BMAX_CC] floats
+  static constexpr int redw = red + RMAX * BMAX_CC * 4;    // [NW][RMAX] floats
+  static constexpr int ssw = redw + NW * RMAX * 4;         // [NW][BMAX_CC] floats
+  static constexpr int bars = ssw + NW * BMAX_CC * 4;      // mbarriers
+  static constexpr int n_mbar = 2 * NSTAGE + 2 * NISLOT;
+  static constexpr int islot = bars + n_mbar * 8;
+  static constexpr int flags = islot + NISLOT * 4;         // [8] u32
+  static constexpr int total = flags + 8 * 4;
+};
+static_assert(SmemLayout::total <= 227 * 1024, "shared memory budget");
+
+enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3 };
+
+struct Sh {
+  uint8_t* ring;
+  float* xbuf;
+  float* red;
+  float* redw;
+  float* ssw;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* ifull;
+  uint64_t* iempty;
+  volatile uint32_t* islot;
+  volatile uint32_t* flags;
+};
+
+__device__ __forceinline__ Sh sh_map(uint8_t* base) {
+  Sh s;
+  s.ring = base + SmemLayout::ring;
+  s.xbuf = reinterpret_cast<float*>(base + SmemLayout::xbuf);
+  s.red = reinterpret_cast<float*>(base + SmemLayout::red);
+  s.redw = reinterpret_cast<float*>(base + SmemLayout::redw);
+  s.ssw = reinterpret_cast<float*>(base + SmemLayout::ssw);
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + SmemLayout::bars);
+  s.full = b;
+  s.empty = b + NSTAGE;
+  s.ifull = b + 2 * NSTAGE;
+  s.iempty = b + 2 * NSTAGE + NISLOT;
+  s.islot = reinterpret_cast<volatile uint32_t*>(base + SmemLayout::islot);
+  s.flags = reinterpret_cast<volatile uint32_t*>(base + SmemLayout::flags);
+  return s;
+}
+
+// ---------------------------------------------------------------- errors
+__device__ void set_error(const KParams& P, uint32_t code, uint32_t detail) {
+  if (atomicCAS(&P.ctl[CTL_STATUS], 0u, code) == 0u) atomicExch(&P.ctl[CTL_DETAIL], detail);
+  atomicExch(&P.ctl[CTL_ABORT], 1u);
+}
+
+// Bounded mbarrier wait.  Gives up (error + false) after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(const KParams& P, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  const uint64_t limit = P.wait_limit_ns * 4ull;
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit) {
+      set_error(P, MK_ERR_TIMEOUT, 0xfffffff0u);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- operand sources
+// A tile's streamed operand: up to two regions of whole rows, each split into
+// ring stages of `rps` rows.
+struct Src {
+  const uint8_t* ptr[2];
+  uint32_t rows[2];
+  uint32_t row_bytes;
+  uint32_t rps;
+  int nreg;
+};
+
+__device__ __forceinline__ const LayerW& layer_w(const KParams& P, int l) { return P.layers[l]; }
+
+struct AttnExt {
+  bool live;
+  int pos, lo, hi, nc;  // keys [lo, hi); cached keys [lo, lo + nc)
+  bool has_new;         // this split holds the new token's key (index pos)
+};
+
+__device__ __forceinline__ AttnExt attn_extent(const KParams& P, const Instr& in) {
+  AttnExt e;
+  e.live = x_eval(P.expr + XS_SEQ_LIVE * X_MAX_WORDS, in, P.B, P.S, nullptr, 0) > 0;
+  e.pos = 0;
+  e.lo = e.hi = e.nc = 0;
+  e.has_new = false;
+  if (!e.live) return e;
+  e.pos = P.positions[in.a0];
+  if (e.pos < 0 || e.pos >= P.max_ctx) {
+    e.live = false;
+    return e;
+  }
+  e.lo = (int)x_eval(P.expr + XS_ATTN_LO * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B);
+  e.hi = (int)x_eval(P.expr + XS_ATTN_HI * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B);
+  int cend = e.hi < e.pos ? e.hi : e.pos;
+  e.nc = cend > e.lo ? cend - e.lo : 0;
+  e.has_new = e.lo <= e.pos && e.pos < e.hi;
+  return e;
+}
+
+__device__ __forceinline__ size_t kv_offset(const KParams& P, int l, int kv, int b, int g, int pos) {
+  return ((((size_t)l * 2 + kv) * P.max_batch + b) * P.nkv + g) * (size_t)P.max_ctx * P.d +
+         (size_t)pos * P.d;
+}
+
+// GEMV tile: weight matrices and K of instruction `in`.
+struct GemvDesc {
+  const uint16_t* w0;
+  const uint16_t* w1;
+  int K, rows, row0;
+};
+
+__device__ __forceinline__ GemvDesc gemv_desc(const KParams& P, const Instr& in) {
+  GemvDesc g;
+  g.w1 = nullptr;
+  g.row0 = (int)in.a0;
+  g.rows = (int)in.a1;
+  const int qd = P.nq * P.d;
+  const LayerW& W = layer_w(P, in.layer);
+  switch (in.op) {
+    case OP_QKV: {
+      int r = g.row0;
+      g.K = P.H;
+      if (r < qd) g.w0 = W.wq + (size_t)r * P.H;
+      else if (r < qd + P.nkv * P.d) g.w0 = W.wk + (size_t)(r - qd) * P.H;
+      else g.w0 = W.wv + (size_t)(r - qd - P.nkv * P.d) * P.H;
+      break;
+    }
+    case OP_O: g.K = qd; g.w0 = W.wo + (size_t)g.row0 * qd; break;
+    case OP_GU:
+      g.K = P.H;
+      g.w0 = W.wg + (size_t)g.row0 * P.H;
+      g.w1 = W.wu + (size_t)g.row0 * P.H;
+      break;
+    case OP_DOWN: g.K = P.F; g.w0 = W.wd + (size_t)g.row0 * P.F; break;
+    default: g.K = P.H; g.w0 = P.lm + (size_t)g.row0 * P.H; break;  // OP_LM
+  }
+  return g;
+}
+
+__device__ __forceinline__ Src instr_src(const KParams& P, const Instr& in) {
+  Src s;
+  s.nreg = 0;
+  s.rows[0] = s.rows[1] = 0;
+  s.ptr[0] = s.ptr[1] = nullptr;
+  if (in.op == OP_ATTN) {
+    AttnExt e = attn_extent(P, in);
+    s.row_bytes = P.d * 2;
+    s.rps = STAGE_BYTES / s.row_bytes;
+    if (e.live && e.nc > 0) {
+      s.nreg = 2;
+      s.ptr[0] = reinterpret_cast<const uint8_t*>(P.kv + kv_offset(P, in.layer, 0, in.a0, in.a1, e.lo));
+      s.ptr[1] = reinterpret_cast<const uint8_t*>(P.kv + kv_offset(P, in.layer, 1, in.a0, in.a1, e.lo));
+      s.rows[0] = s.rows[1] = (uint32_t)e.nc;
+    }
+    return s;
+  }
+  GemvDesc g = gemv_desc(P, in);
+  s.row_bytes = (uint32_t)g.K * 2;
+  s.rps = STAGE_BYTES / s.row_bytes;
+  s.nreg = g.w1 ? 2 : 1;
+  s.ptr[0] = reinterpret_cast<const uint8_t*>(g.w0);
+  s.ptr[1] = reinterpret_cast<const uint8_t*>(g.w1);
+  s.rows[0] = s.rows[1] = (uint32_t)g.rows;
+  return s;
+}
+
+__device__ __forceinline__ uint32_t src_stages(const Src& s) {
+  uint32_t n = 0;
+  for (int r = 0; r < s.nreg; ++r) n += (s.rows[r] + s.rps - 1) / s.rps;
+  return n;
+}
+
+// ---------------------------------------------------------------- producer
+__device__ void producer(const KParams& P, const Sh& S) {
+  const int lane = threadIdx.x & 31;
+  if (lane != 0) return;
+  const uint64_t policy = policy_evict_first();
+  uint32_t stage_ctr = 0, islot_ctr = 0;
+  bool first = true;
+  for (;;) {
+    uint32_t i;
+    bool end;
+    if (P.mode == MODE_MEGA) {
+      end = ld_volatile(&P.ctl[CTL_ABORT]) != 0u;
+      i = end ? END_SLOT : atomicAdd(&P.ctl[CTL_HEAD], 1u);
+      end = end || i >= P.n_instr;
+    } else {
+      i = first ? P.perop_base + blockIdx.x : END_SLOT;
+      end = !first;
+      first = false;
+    }
+    const int si = islot_ctr % NISLOT;
+    if (!mbar_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) end = true;
+    S.islot[si] = end ? END_SLOT : i;
+    mbar_arrive(&S.ifull[si]);
+    ++islot_ctr;
+    if (end) break;
+
+    const Instr in = P.queue[i];
+    const Src src = instr_src(P, in);
+    bool stuck = false;
+    for (int r = 0; r < src.nreg && !stuck; ++r) {
+      for (uint32_t row = 0; row < src.rows[r]; row += src.rps) {
+        uint32_t n = src.rows[r] - row < src.rps ? src.rows[r] - row : src.rps;
+        uint32_t bytes = n * src.row_bytes;
+        const int st = stage_ctr % NSTAGE;
+        if (!mbar_wait(P, &S.empty[st], ((stage_ctr / NSTAGE) & 1u) ^ 1u)) {
+          // the consumers stopped taking stages: issue nothing more (the
+          // consumers' own bounded waits end their loop)
+          stuck = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&S.full[st], bytes);
+        bulk_g2s(S.ring + (size_t)st * STAGE_BYTES, src.ptr[r] + (size_t)row * src.row_bytes, bytes,
+                 &S.full[st], policy);
+        ++stage_ctr;
+      }
+    }
+    if (stuck) break;
+  }
+}
+
+// ---------------------------------------------------------------- consumer helpers
+struct Ring {
+  uint32_t ctr;  // stages consumed so far
+};
+
+__device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
+  const int st = R.ctr % NSTAGE;
+  mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
+  return S.ring + (size_t)st * STAGE_BYTES;
+}
+__device__ __forceinline__ void ring_release(const Sh& S, Ring& R) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&S.empty[R.ctr % NSTAGE]);
+  ++R.ctr;
+}
+
+__device__ __forceinline__ void cbar() { named_bar(CONSUMER_BAR, NT); }
+
+// Deterministic sum over the consumer threads (fixed reduction tree).
+__device__ __forceinline__ float consumer_sum(float v, float* scratch) {
+  const int t = threadIdx.x, w = t >> 5;
+  v = warp_sum(v);
+  if ((t & 31) == 0) scratch[w] = v;
+  cbar();
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < NW; ++k) s += scratch[k];
+  cbar();
+  return s;
+}
+
+// Token id of sequence b, validated.
+__device__ __forceinline__ int token_of(const KParams& P, int b) {
+  int t = P.tokens[b];
+  if (t < 0 || t >= P.V) {
+    if (threadIdx.x == 0) set_error(P, MK_ERR_BOUNDS, (uint32_t)b);
+    t = 0;
+  }
+  return t;
+}
+
+// Activation source of a GEMV op (row-major [max_batch][K] fp32), or null when
+// it is the embedding row of the sequence's token (layer-0 QKV).
+__device__ __forceinline__ const float* gemv_x(const KParams& P, const Instr& in) {
+  const size_t bh = (size_t)P.max_batch * P.H;
+  switch (in.op) {
+    case OP_QKV: return in.layer == 0 ? nullptr : P.resid + (size_t)(2 * in.layer) * bh;
+    case OP_O: return P.attn_out + (size_t)in.layer * P.max_batch * (P.nq * P.d);
+    case OP_GU: return P.resid + (size_t)(2 * in.layer + 1) * bh;
+    case OP_DOWN: return P.act + (size_t)in.layer * P.max_batch * P.F;
+    default: return P.resid + (size_t)(2 * P.L) * bh;
+  }
+}
+__device__ __forceinline__ const uint16_t* gemv_gain(const KParams& P, const Instr& in) {
+  switch (in.op) {
+    case OP_QKV: return layer_w(P, in.layer).attn_norm;
+    case OP_GU: return layer_w(P, in.layer).ffn_norm;
+    case OP_LM: return P.final_norm;
+    default: return nullptr;
+  }
+}
+
+// Load 8 consecutive activations of sequence b starting at column c.
+__device__ __forceinline__ void load_x8(const KParams& P, const float* xs, const uint16_t* emb_row,
+                                        int b, int K, int c, float (&x)[8]) {
+  if (xs) {
+    const float4* p = reinterpret_cast<const float4*>(xs + (size_t)b * K + c);
+    float4 u = __ldcg(p), v = __ldcg(p + 1);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+  } else {
+    uint4 w = __ldg(reinterpret_cast<const uint4*>(emb_row + c));
+    widen8(w, x);
+  }
+}
+
+// ---------------------------------------------------------------- GEMV, batch 1, K = M * 8 * NT
+// Thread t owns columns 8*(t + NT*j) .. +8 for j < M and keeps them (normed)
+// in registers; every row of the tile adds into acc[row]; one multi-value warp
+// reduction and a fixed-order sum over warps per tile.
+template <int M>
+__device__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
+                          const Src& src, Ring& R) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int K = g.K;
+  const float* xs = gemv_x(P, in);
+  const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0) * P.H;
+  const uint16_t* gain = gemv_gain(P, in);
+  float xr[M][8];
+#pragma unroll
+  for (int j = 0; j < M; ++j) load_x8(P, xs, emb_row, 0, K, 8 * (t + NT * j), xr[j]);
+  if (gain) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(xr[j][e], xr[j][e], ss);
+    ss = consumer_sum(ss, S.ssw);
+    const float inv = 1.0f / sqrtf(ss / (float)K + P.eps);
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      float gw[8];
+      widen8(__ldg(reinterpret_cast<const uint4*>(gain + 8 * (t + NT * j))), gw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xr[j][e] = xr[j][e] * inv * gw[e];
+    }
+  }
+  float acc[RMAX];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+
+  const int rows0 = (int)src.rows[0];
+  const int ntot = src.nreg == 2 ? 2 * rows0 : rows0;
+  const int rps = (int)src.rps;
+  const int stages0 = (rows0 + rps - 1) / rps;
+  int cur = -1;
+  const uint8_t* stage = nullptr;
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    if (r < ntot) {
+      const int reg = r < rows0 ? 0 : 1;
+      const int rr = reg ? r - rows0 : r;
+      const int st = reg * stages0 + rr / rps;
+      if (st != cur) {
+        if (cur >= 0) ring_release(S, R);
+        stage = ring_acquire(P, S, R);
+        cur = st;
+      }
+      const uint4* row = reinterpret_cast<const uint4*>(stage + (size_t)(rr % rps) * K * 2);
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < M; ++j) a = dot8(row[t + NT * j], xr[j], a);
+      acc[r] = a;
+    }
+  }
+  if (cur >= 0) ring_release(S, R);
+
+  const float v = warp_reduce_multi<RMAX>(acc, lane);
+  if ((lane & 1) == 0) S.redw[w * RMAX + warp_multi_index<RMAX>(lane)] = v;
+  cbar();
+  if (t < ntot) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) s += S.redw[k * RMAX + t];
+    S.red[t * BMAX_CC] = s;
+  }
+  cbar();
+}
+
+// ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
+// x[B][K] (normed) staged in shared memory; one warp per (row, sequence) pair.
+__device__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
+                             const Src& src, Ring& R) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int K = g.K, B = P.B, K8 = K / 8;
+  const float* xs = gemv_x(P, in);
+  const uint16_t* gain = gemv_gain(P, in);
+  float ss[BMAX_CC];
+#pragma unroll
+  for (int b = 0; b < BMAX_CC; ++b) ss[b] = 0.f;
+  for (int idx = t; idx < B * K8; idx += NT) {
+    const int b = idx / K8, c = (idx % K8) * 8;
+    const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, b) * P.H;
+    float x[8];
+    load_x8(P, xs, emb_row, b, K, c, x);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      S.xbuf[b * K + c + e] = x[e];
+      s = fmaf(x[e], x[e], s);
+    }
+#pragma unroll
+    for (int bb = 0; bb < BMAX_CC; ++bb)
+      if (bb == b) ss[bb] += s;
+  }
+  if (gain) {
+    float inv[BMAX_CC];
+#pragma unroll
+    for (int b = 0; b < BMAX_CC; ++b)
+      inv[b] = b < B ? 1.0f / sqrtf(consumer_sum(ss[b], S.ssw) / (float)K + P.eps) : 0.f;
+    cbar();
+    for (int idx = t; idx < B * K; idx += NT) {
+      const int b = idx / K, k = idx % K;
+      float iv = 0.f;
+#pragma unroll
+      for (int bb = 0; bb < BMAX_CC; ++bb)
+        if (bb == b) iv = inv[bb];
+      const float gw = __uint_as_float((uint32_t)__ldg(gain + k) << 16);
+      S.xbuf[idx] = S.xbuf[idx] * iv * gw;
+    }
+  }
+  cbar();
+
+  int tile_row = 0;
+  for (int r = 0; r < src.nreg; ++r) {
+    for (uint32_t row = 0; row < src.rows[r]; row += src.rps) {
+      const int n = (int)(src.rows[r] - row < src.rps ? src.rows[r] - row : src.rps);
+      const uint8_t* stage = ring_acquire(P, S, R);
+      for (int p = w; p < n * B; p += NW) {
+        const int rr = p / B, b = p % B;
+        const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)rr * K * 2);
+        const float* xb = S.xbuf + b * K;
+        float a = 0.f;
+        for (int v = lane; v < K8; v += 32) a = dot8(wrow[v], xb + v * 8, a);
+        a = warp_sum(a);
+        if (lane == 0) S.red[(tile_row + rr) * BMAX_CC + b] = a;
+      }
+      ring_release(S, R);
+      tile_row += n;
+    }
+  }
+  cbar();
+}
+
+// Store a finished GEMV tile: y[r][b] is in S.red.
+__device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g) {
+  const int t = threadIdx.x, B = P.B, l = in.layer;
+  const int nout = g.rows;
+  const size_t bh = (size_t)P.max_batch * P.H;
+  for (int idx = t; idx < nout * B; idx += NT) {
+    const int r = idx / B, b = idx % B, row = g.row0 + r;
+    const float y = S.red[r * BMAX_CC + b];
+    switch (in.op) {
+      case OP_QKV:
+        P.qkv[((size_t)l * P.max_batch + b) * P.qkv_rows + row] = y;
+        break;
+      case OP_O: {
+        float prev;
+        if (l == 0) prev = __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b) * P.H + row] << 16);
+        else prev = __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
+        P.resid[(size_t)(2 * l + 1) * bh + (size_t)b * P.H + row] = prev + y;
+        break;
+      }
+      case OP_GU: {
+        const float u = S.red[(g.rows + r) * BMAX_CC + b];
+        P.act[((size_t)l * P.max_batch + b) * P.F + row] = y / (1.0f + expf(-y)) * u;
+        break;
+      }
+      case OP_DOWN: {
+        const size_t o = (size_t)b * P.H + row;
+        P.resid[(size_t)(2 * l + 2) * bh + o] = __ldcg(P.resid + (size_t)(2 * l + 1) * bh + o) + y;
+        break;
+      }
+      default:
+        P.logits[(size_t)b * P.V + row] = y;
+        break;
+    }
+  }
+}
+
+__device__ void gemv_tile(const KParams& P, const Sh& S, const Instr& in, Ring& R, bool fast) {
+  const GemvDesc g = gemv_desc(P, in);
+  const Src src = instr_src(P, in);
+  if (fast && P.B == 1) {
+    switch (g.K / FAST_K_UNIT) {
+      case 1: gemv_fast<1>(P, S, in, g, src, R); break;
+      case 2: gemv_fast<2>(P, S, in, g, src, R); break;
+      case 3: gemv_fast<3>(P, S, in, g, src, R); break;
+      case 4: gemv_fast<4>(P, S, in, g, src, R); break;
+      case 5: gemv_fast<5>(P, S, in, g, src, R); break;
+      case 6: gemv_fast<6>(P, S, in, g, src, R); break;
+      default: gemv_fast<7>(P, S, in, g, src, R); break;
+    }
+  } else {
+    gemv_generic(P, S, in, g, src, R);
+  }
+  gemv_epilogue(P, S, in, g);
+}
+
+// ---------------------------------------------------------------- decode attention (split-KV)
+// One (sequence, kv head, split): the split's cached keys stream through the
+// ring; the new token's key/value come from the QKV output (normed when q/k
+// norm is on, rotated, written to the cache by the split that holds slot pos).
+// Partial (max, sum, unnormalised o) per q head; the last split to arrive
+// combines all splits of the group in split order.
+template <int D, int REP>
+__device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32_t ii, Ring& R) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int l = in.layer, b = (int)in.a0, g = (int)in.a1, split = (int)in.a2;
+  constexpr int rep = REP;
+  const int qd = P.nq * D, NS = P.n_splits;
+  constexpr int smax = SCORE_FLOATS / REP;
+  AttnExt e = attn_extent(P, in);
+  if (t == 0 && b < P.B && !e.live) set_error(P, MK_ERR_BOUNDS, ii);  // position out of range
+  float* qs = S.xbuf;            // [rep][D]
+  float* kn = qs + 8 * 128;      // [D]
+  float* vn = kn + 128;          // [D]
+  float* sc = vn + 128;          // [rep][smax]
+  float* part = P.part + ((((size_t)l * P.max_batch + b) * P.nkv + g) * NS + split) * rep * (D + 2);
+
+  if (e.live) {
+    const float* base = P.qkv + ((size_t)l * P.max_batch + b) * P.qkv_rows;
+    for (int i = t; i < rep * D; i += NT) qs[i] = __ldcg(base + g * rep * D + i);
+    for (int i = t; i < D; i += NT) {
+      kn[i] = __ldcg(base + qd + g * D + i);
+      vn[i] = __ldcg(base + qd + P.nkv * D + g * D + i);
+    }
+    cbar();
+    if (P.qk_norm) {
+      const LayerW& W = layer_w(P, l);
+      if (w <= rep) {
+        float* u = w < rep ? qs + w * D : kn;
+        const uint16_t* gn = w < rep ? W.q_norm : W.k_norm;
+        float s = 0.f;
+        for (int i = lane; i < D; i += 32) s = fmaf(u[i], u[i], s);
+        s = warp_sum(s);
+        const float inv = 1.0f / sqrtf(s / (float)D + P.eps);
+        for (int i = lane; i < D; i += 32)
+          u[i] = u[i] * inv * __uint_as_float((uint32_t)__ldg(gn + i) << 16);
+      }
+      cbar();
+    }
+    const float2* rt = P.rope + (size_t)e.pos * (D / 2);
+    for (int i = t; i < (rep + 1) * (D / 2); i += NT) {
+      const int h = i / (D / 2), k = i % (D / 2);
+      float* u = h < rep ? qs + h * D : kn;
+      const float2 cs = __ldg(rt + k);
+      const float u1 = u[k], u2 = u[k + D / 2];
+      u[k] = u1 * cs.x - u2 * cs.y;
+      u[k + D / 2] = u2 * cs.x + u1 * cs.y;
+    }
+    cbar();
+    if (e.has_new)
+      for (int i = t; i < D; i += NT) {
+        P.kv[kv_offset(P, l, 0, b, g, e.pos) + i] = __bfloat16_as_ushort(__float2bfloat16_rn(kn[i]));
+        P.kv[kv_offset(P, l, 1, b, g, e.pos) + i] = __bfloat16_as_ushort(__float2bfloat16_rn(vn[i]));
+      }
+
+    // scores of cached keys: 8 lanes per key, lane `sub` holds element groups
+    // {sub, sub + 8, ...} of 8 (conflict-free 16-byte shared loads)
+    constexpr int G = D / 64;  // 8-element groups per lane
+    const float scale = 1.0f / sqrtf((float)D);
+    const int sub = lane & 7, quad = lane >> 3;
+    float qv[REP][G][8];
+#pragma unroll
+    for (int h = 0; h < REP; ++h)
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qv[h][gi][k] = qs[h * D + (sub + 8 * gi) * 8 + k];
+    const int kps = (int)(STAGE_BYTES / (D * 2));
+    for (int c0 = 0; c0 < e.nc; c0 += kps) {
+      const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
+      const uint8_t* stage = ring_acquire(P, S, R);
+      for (int j0 = w * 4; j0 < cnt; j0 += NW * 4) {
+        const int j = j0 + quad;
+        const bool ok = j < cnt;
+        const uint4* krow = reinterpret_cast<const uint4*>(stage + (size_t)(ok ? j : 0) * D * 2);
+        float kx[G][8];
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) widen8(krow[sub + 8 * gi], kx[gi]);
+#pragma unroll
+        for (int h = 0; h < REP; ++h) {
+          float a = 0.f;
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a = fmaf(qv[h][gi][k], kx[gi][k], a);
+          a += __shfl_xor_sync(0xffffffffu, a, 4);
+          a += __shfl_xor_sync(0xffffffffu, a, 2);
+          a += __shfl_xor_sync(0xffffffffu, a, 1);
+          if (ok && sub == 0) sc[h * smax + c0 + j] = a * scale;
+        }
+      }
+      ring_release(S, R);
+    }
+    if (e.has_new && w < rep) {
+      float a = 0.f;
+      for (int i = lane; i < D; i += 32) a = fmaf(qs[w * D + i], kn[i], a);
+      a = warp_sum(a);
+      if (lane == 0) sc[w * smax + (e.pos - e.lo)] = a * scale;
+    }
+    cbar();
+    const int n = e.hi - e.lo;
+    if (w < rep) {
+      float m = -INFINITY;
+      for (int j = lane; j < n; j += 32) m = fmaxf(m, sc[w * smax + j]);
+      m = warp_max(m);
+      float s = 0.f;
+      for (int j = lane; j < n; j += 32) {
+        const float p = expf(sc[w * smax + j] - m);
+        sc[w * smax + j] = p;
+        s += p;
+      }
+      s = warp_sum(s);
+      if (lane == 0) {
+        part[w * (D + 2) + D] = m;
+        part[w * (D + 2) + D + 1] = s;
+      }
+    }
+    cbar();
+    // o = sum_j p_j v_j: thread owns column pairs (h, 2c) for pair index t, t + NT
+    float o[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    const int npairs = rep * (D / 2);
+    for (int c0 = 0; c0 < e.nc; c0 += kps) {
+      const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
+      const uint8_t* stage = ring_acquire(P, S, R);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int pi = t + k * NT;
+        if (pi < npairs) {
+          const int h = pi / (D / 2), c = pi % (D / 2);
+          const float* ph = sc + h * smax + c0;
+          const uint32_t* vcol = reinterpret_cast<const uint32_t*>(stage) + c;
+          float a0 = o[k][0], a1 = o[k][1];
+          for (int j = 0; j < cnt; ++j) {
+            const uint32_t v2 = vcol[j * (D / 2)];
+            const float p = ph[j];
+            a0 = fmaf(p, bf_lo(v2), a0);
+            a1 = fmaf(p, bf_hi(v2), a1);
+          }
+          o[k][0] = a0;
+          o[k][1] = a1;
+        }
+      }
+      ring_release(S, R);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int pi = t + k * NT;
+      if (pi < npairs) {
+        const int h = pi / (D / 2), c = pi % (D / 2);
+        if (e.has_new) {
+          const float p = sc[h * smax + (e.pos - e.lo)];
+          o[k][0] = fmaf(p, vn[2 * c], o[k][0]);
+          o[k][1] = fmaf(p, vn[2 * c + 1], o[k][1]);
+        }
+        part[h * (D + 2) + 2 * c] = o[k][0];
+        part[h * (D + 2) + 2 * c + 1] = o[k][1];
+      }
+    }
+    // an empty split (n == 0) leaves max = -inf, sum = 0 from the softmax pass
+  }
+  cbar();
+  if (t == 0) {
+    __threadfence();
+    uint32_t* arr = P.arrive + ((size_t)l * P.max_batch + b) * P.nkv + g;
+    const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
+    const bool last = old == (uint32_t)(NS - 1);
+    if (last) *arr = 0u;  // every split of this group has arrived: reset for the next step
+    S.flags[F_LAST] = last ? 1u : 0u;
+  }
+  cbar();
+  if (S.flags[F_LAST]) {
+    if (e.live) {
+      const float* gp = P.part + (((size_t)l * P.max_batch + b) * P.nkv + g) * NS * rep * (D + 2);
+      for (int i = t; i < rep * D; i += NT) {
+        const int h = i / D, c = i % D;
+        float M = -INFINITY;
+        for (int s = 0; s < NS; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
+        float Ls = 0.f, O = 0.f;
+        for (int s = 0; s < NS; ++s) {
+          const float* ps = gp + ((size_t)s * rep + h) * (D + 2);
+          const float ms = __ldcg(ps + D);
+          const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+          Ls = fmaf(__ldcg(ps + D + 1), f, Ls);
+          O = fmaf(__ldcg(ps + c), f, O);
+        }
+        P.attn_out[((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c] = O / Ls;
+      }
+    }
+    cbar();
+    if (t == 0 && P.mode == MODE_MEGA) {
+      __threadfence();
+      red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+    }
+  }
+}
+
+__device__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, uint32_t ii, Ring& R) {
+  if (P.d == 128) {
+    switch (P.rep) {
+      case 1: attn_tile<128, 1>(P, S, in, ii, R); break;
+      case 2: attn_tile<128, 2>(P, S, in, ii, R); break;
+      case 4: attn_tile<128, 4>(P, S, in, ii, R); break;
+      default: attn_tile<128, 8>(P, S, in, ii, R); break;
+    }
+  } else {
+    switch (P.rep) {
+      case 1: attn_tile<64, 1>(P, S, in, ii, R); break;
+      case 2: attn_tile<64, 2>(P, S, in, ii, R); break;
+      case 4: attn_tile<64, 4>(P, S, in, ii, R); break;
+      default: attn_tile<64, 8>(P, S, in, ii, R); break;
+    }
+  }
+}
+
+// Drain an instruction's stages without computing (after an abort).
+__device__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
+  const uint32_t n = src_stages(instr_src(P, in));
+  for (uint32_t k = 0; k < n; ++k) {
+    ring_acquire(P, S, R);
+    ring_release(S, R);
+  }
+}
+
+// ---------------------------------------------------------------- consumer loop
+__device__ void consumer(const KParams& P, const Sh& S, bool fast) {
+  const int t = threadIdx.x;
+  Ring R{0};
+  uint32_t islot_ctr = 0;
+  const uint32_t gen = S.flags[F_GEN];
+  for (;;) {
+    const int si = islot_ctr % NISLOT;
+    // one thread takes the slot (a bounded wait); the consumer barrier hands
+    // the index to the others so that every consumer thread takes the same path
+    if (t == 0) {
+      uint32_t v = 0xffffffffu;
+      if (mbar_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u)) v = S.islot[si];
+      S.flags[F_SLOT] = v;
+    }
+    cbar();
+    const uint32_t i = S.flags[F_SLOT];
+    if ((t & 31) == 0) mbar_arrive(&S.iempty[si]);
+    ++islot_ctr;
+    if (i == END_SLOT) break;
+    const Instr in = P.queue[i];
+    const uint64_t t_begin = P.trace ? globaltimer() : 0;
+
+    // wait on the tiles this instruction reads
+    if (t == 0) {
+      uint32_t aborted = ld_volatile(&P.ctl[CTL_ABORT]) != 0u;
+      if (!aborted && P.mode == MODE_MEGA && in.wait_bar != NO_BAR) {
+        const uint32_t target = (gen + 1u) * in.wait_target;
+        const uint64_t t0 = globaltimer();
+        for (uint32_t k = 0; k < in.wait_n && !aborted;) {
+          const uint32_t* c = &P.bars[in.wait_bar + k * in.wait_stride];
+          if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
+            ++k;
+            continue;
+          }
+          if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) aborted = 1;
+          else if (globaltimer() - t0 > P.wait_limit_ns) {
+            set_error(P, MK_ERR_TIMEOUT, i);
+            aborted = 1;
+          } else {
+            __nanosleep(64);
+          }
+        }
+      }
+      S.flags[F_ABORT] = aborted;
+    }
+    cbar();
+    const uint64_t t_ready = P.trace ? globaltimer() : 0;
+    if (S.flags[F_ABORT]) {
+      drain(P, S, in, R);
+      cbar();
+      continue;
+    }
+    if (in.op == OP_ATTN) {
+      attn_dispatch(P, S, in, i, R);
+    } else {
+      gemv_tile(P, S, in, R, fast);
+      cbar();
+      if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR) {
+        __threadfence();
+        red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+      }
+    }
+    if (P.trace && t == 0) {
+      unsigned long long* tr = P.trace + (size_t)i * 4;
+      tr[0] = (unsigned long long)smid() | ((unsigned long long)(in.op | (in.layer << 8)) << 32);
+      tr[1] = t_begin;
+      tr[2] = t_ready;
+      tr[3] = globaltimer();
+    }
+    cbar();
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_constant__ KParams P,
+                                                               int fast) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Sh S = sh_map(smem);
+  const int t = threadIdx.x;
+  if (t == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], NW);
+    }
+    for (int s = 0; s < NISLOT; ++s) {
+      mbar_init(&S.ifull[s], 1);
+      mbar_init(&S.iempty[s], NW);
+    }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    S.flags[F_GEN] = P.mode == MODE_MEGA ? ld_volatile(&P.ctl[CTL_GEN]) : 0u;
+  }
+  __syncthreads();
+  if (t >= NT) producer(P, S);
+  else consumer(P, S, fast != 0);
+  __syncthreads();
+  if (t == 0 && P.mode == MODE_MEGA) {
+    __threadfence();
+    const uint32_t old = atomicAdd(&P.ctl[CTL_EXIT], 1u);
+    if (old == gridDim.x - 1) {
+      // every CTA has left its loop: rewind the queue head for the next launch
+      P.ctl[CTL_HEAD] = 0u;
+      P.ctl[CTL_EXIT] = 0u;
+      P.ctl[CTL_GEN] = S.flags[F_GEN] + 1u;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host-side launch helpers
+int smem_bytes() { return SmemLayout::total; }
+
+cudaError_t kernel_setup() {
+  return cudaFuncSetAttribute(mk_interpreter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SmemLayout::total);
+}
+
+cudaError_t max_coresident(int* per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk_interpreter, NTHREADS,
+                                                       SmemLayout::total);
+}
+
+cudaError_t launch_mega(const KParams& p, int ctas, int fast, cudaStream_t st) {
+  KParams pp = p;
+  int f = fast;
+  void* args[] = {(void*)&pp, (void*)&f};
+  return cudaLaunchCooperativeKernel((const void*)mk_interpreter, dim3(ctas), dim3(NTHREADS), args,
+                                     (size_t)SmemLayout::total, st);
+}
+
+cudaError_t launch_perop(const KParams& p, uint32_t first, uint32_t count, int fast,
+                         cudaStream_t st) {
+  KParams pp = p;
+  pp.mode = MODE_PEROP;
+  pp.perop_base = first;
+  mk_interpreter<<<count, NTHREADS, SmemLayout::total, st>>>(pp, fast);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

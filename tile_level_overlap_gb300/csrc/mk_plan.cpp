@@ -1,0 +1,340 @@
+// Host plan builder.  Turns a model shape into the tile DAG of one decode step,
+// emitted as a topological instruction queue with per-tile barrier counters.
+//
+// Following the MegaOps Abstract, each consumer waits on the tiles of the
+// intermediate tensor it reads: attention of kv group g waits only on the QKV
+// row tiles of g's heads; every other dependency of a decode step is a
+// reduction over the whole hidden vector (the RMSNorm before QKV / gate-up and
+// the input dimension of O / down), so those barriers count every producer
+// tile of the operator.  Barrier counters are never cleared: a launch of
+// generation `gen` waits for (gen + 1) * target releases
+// ("Lecture 112: Production Megakernels for Real-World Inference", Key
+// takeaways: barriers held as tensors).  Extents that depend on the batch or a
+// sequence's cached length are expressions evaluated on the device, so the
+// queue does not change with them (same source, symbolic shapes in S and P).
+#include "mk_plan.h"
+
+#include <algorithm>
+#include <cstring>
+#include <random>
+#include <unordered_map>
+
+namespace mk {
+
+namespace {
+
+int pow2_floor(int x) {
+  int p = 1;
+  while (p * 2 <= x) p *= 2;
+  return p;
+}
+
+int rows_for(long target_bytes, long row_bytes, int cap) {
+  long r = target_bytes / row_bytes;
+  if (r < 1) r = 1;
+  if (r > cap) r = cap;
+  return pow2_floor((int)r);
+}
+
+uint32_t ceil_div(uint64_t a, uint64_t b) { return (uint32_t)((a + b - 1) / b); }
+
+Instr make(Op op, int layer, uint32_t a0, uint32_t a1, uint16_t a2 = 0) {
+  Instr in;
+  std::memset(&in, 0, sizeof(in));
+  in.op = op;
+  in.layer = (uint16_t)layer;
+  in.a0 = a0;
+  in.a1 = a1;
+  in.a2 = a2;
+  in.x_lo = NO_EXPR;
+  in.x_hi = NO_EXPR;
+  in.wait_bar = NO_BAR;
+  in.rel_bar = NO_BAR;
+  return in;
+}
+
+void set_wait(Instr& in, uint32_t bar, uint32_t target, uint16_t n = 1, uint16_t stride = 1) {
+  in.wait_bar = bar;
+  in.wait_target = target;
+  in.wait_n = n;
+  in.wait_stride = stride;
+}
+
+// Postfix expression helpers.
+struct XBuild {
+  std::vector<uint32_t> w;
+  XBuild& c(uint32_t v) { w.push_back(xw(X_CONST, v)); return *this; }
+  XBuild& op(uint32_t o) { w.push_back(xw(o)); return *this; }
+};
+
+void put_expr(std::vector<uint32_t>& table, int slot, const XBuild& x) {
+  for (size_t i = 0; i < x.w.size() && i < (size_t)X_MAX_WORDS; ++i)
+    table[(size_t)slot * X_MAX_WORDS + i] = x.w[i];
+}
+
+}  // namespace
+
+int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
+               std::string* why) {
+  auto bad = [&](int code, const char* msg) {
+    if (why) *why = msg;
+    return code;
+  };
+  if (c.n_layers < 1 || c.hidden < 8 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 2 ||
+      c.ffn < 8 || c.vocab < 1)
+    return bad(MK_ERR_INVALID_ARG, "model dimensions must be positive (n_layers >= 1)");
+  if (c.n_q_heads % c.n_kv_heads) return bad(MK_ERR_INVALID_ARG, "n_q_heads % n_kv_heads != 0");
+  if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f))
+    return bad(MK_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_theta > 0");
+  if (max_batch < 1 || max_ctx < 1) return bad(MK_ERR_INVALID_ARG, "max_batch, max_ctx >= 1");
+  if (c.head_dim != 64 && c.head_dim != 128)
+    return bad(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  const int rep = c.n_q_heads / c.n_kv_heads;
+  if (rep != 1 && rep != 2 && rep != 4 && rep != 8)
+    return bad(MK_ERR_UNSUPPORTED, "query heads per kv head must be 1, 2, 4 or 8");
+  const int qd = c.n_q_heads * c.head_dim;
+  if (c.hidden % 8 || c.ffn % 8 || qd % 8)
+    return bad(MK_ERR_UNSUPPORTED, "hidden, ffn and n_q_heads*head_dim must be multiples of 8");
+  if (max_batch > BMAX_CC) return bad(MK_ERR_UNSUPPORTED, "batch above the CUDA-core decode limit");
+  const int kmax = std::max(std::max(c.hidden, c.ffn), qd);
+  const bool fast = (c.hidden % FAST_K_UNIT == 0) && (c.ffn % FAST_K_UNIT == 0) &&
+                    (qd % FAST_K_UNIT == 0) && kmax / FAST_K_UNIT <= 7;
+  // The generic path (batch > 1, or K outside the fast set) holds x[B][K] in
+  // shared memory.
+  if ((!fast || max_batch > 1) && (long)max_batch * kmax > XBUF_FLOATS)
+    return bad(MK_ERR_UNSUPPORTED,
+               "max_batch * max(K) exceeds the shared-memory activation buffer of the "
+               "CUDA-core decode path");
+  if ((long)c.head_dim * 2 > STAGE_BYTES || (long)kmax * 2 > STAGE_BYTES)
+    return bad(MK_ERR_UNSUPPORTED, "a weight row does not fit one ring stage");
+
+  HostPlan& hp = *out;
+  hp = HostPlan();
+  hp.cfg = c;
+  hp.max_batch = max_batch;
+  hp.max_ctx = max_ctx;
+  hp.rep = rep;
+  hp.qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  hp.fast_b1 = fast;
+
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
+  hp.r_qkv = std::min(rows_for(64 << 10, (long)H * 2, RMAX), d);
+  hp.r_o = rows_for(64 << 10, (long)qd * 2, RMAX);
+  hp.r_gu = rows_for(128 << 10, (long)H * 4, RMAX / 2);
+  hp.r_down = rows_for(128 << 10, (long)F * 2, RMAX);
+  hp.r_lm = rows_for(256 << 10, (long)H * 2, RMAX);
+  hp.n_qkv_tiles = hp.qkv_rows / hp.r_qkv;
+  hp.n_o_tiles = ceil_div(H, hp.r_o);
+  hp.n_gu_tiles = ceil_div(F, hp.r_gu);
+  hp.n_down_tiles = ceil_div(H, hp.r_down);
+  hp.n_lm_tiles = ceil_div(c.vocab, hp.r_lm);
+
+  // Split-KV partitions per (sequence, kv head): enough instructions to cover
+  // the SMs at batch 1, at most SCORE_FLOATS/rep keys per split, at least 32.
+  hp.split_max = SCORE_FLOATS / rep;
+  int ns = (int)ceil_div(256, (uint64_t)max_batch * nkv);
+  ns = std::max(ns, (int)ceil_div(max_ctx, hp.split_max));
+  ns = std::min(ns, (int)std::max<uint32_t>(ceil_div(max_ctx, 32), ceil_div(max_ctx, hp.split_max)));
+  ns = std::max(ns, 1);
+  hp.n_splits = ns;
+  if (hp.n_splits > 0xffff) return bad(MK_ERR_UNSUPPORTED, "too many splits");
+
+  // Barrier tensor layout.
+  BarLayout& bl = hp.bl;
+  bl.qkv = 0;
+  bl.attn = bl.qkv + L * nkv;
+  bl.o = bl.attn + L;
+  bl.gu = bl.o + L;
+  bl.down = bl.gu + L;
+  bl.lm = bl.down + L;
+  bl.total = bl.lm + 1;
+
+  // Symbolic extents.  n = P[a0] + 1 keys; chunk = ceil(n / NS).
+  hp.expr.assign((size_t)XS_COUNT * X_MAX_WORDS, 0);
+  {
+    XBuild lo;  // min(a2 * chunk, n)
+    lo.op(X_ARG2).op(X_ARG0).op(X_POS).c(1).op(X_ADD).c(ns).op(X_CEILDIV).op(X_MUL)
+        .op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
+    put_expr(hp.expr, XS_ATTN_LO, lo);
+    XBuild hi;  // min((a2 + 1) * chunk, n)
+    hi.op(X_ARG2).c(1).op(X_ADD).op(X_ARG0).op(X_POS).c(1).op(X_ADD).c(ns).op(X_CEILDIV)
+        .op(X_MUL).op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
+    put_expr(hp.expr, XS_ATTN_HI, hi);
+    XBuild live;  // B - a0
+    live.op(X_B).op(X_ARG0).op(X_SUB);
+    put_expr(hp.expr, XS_SEQ_LIVE, live);
+  }
+
+  const uint32_t per_group = (uint32_t)(rep * d + 2 * d) / hp.r_qkv;
+  auto group_of_row = [&](int row) {
+    if (row < qd) return (row / d) / rep;
+    if (row < qd + nkv * d) return (row - qd) / d;
+    return (row - qd - nkv * d) / d;
+  };
+
+  std::vector<Instr>& q = hp.decode;
+  q.clear();
+  hp.perop_decode.clear();
+  auto range_begin = [&]() { return (uint32_t)q.size(); };
+  auto range_end = [&](uint32_t b) {
+    if (q.size() > b) hp.perop_decode.push_back({b, (uint32_t)q.size() - b});
+  };
+  for (int l = 0; l < L; ++l) {
+    uint32_t b0 = range_begin();
+    for (int r = 0; r < hp.qkv_rows; r += hp.r_qkv) {
+      Instr in = make(OP_QKV, l, r, hp.r_qkv);
+      if (l > 0) set_wait(in, bl.down + l - 1, hp.n_down_tiles);
+      in.rel_bar = bl.qkv + l * nkv + group_of_row(r);
+      q.push_back(in);
+    }
+    range_end(b0);
+    b0 = range_begin();
+    for (int b = 0; b < max_batch; ++b)
+      for (int g = 0; g < nkv; ++g)
+        for (int s = 0; s < ns; ++s) {
+          Instr in = make(OP_ATTN, l, b, g, (uint16_t)s);
+          in.flags = IF_RELEASE_ON_COMBINE;
+          in.x_lo = XS_ATTN_LO;
+          in.x_hi = XS_ATTN_HI;
+          set_wait(in, bl.qkv + l * nkv + g, per_group);
+          in.rel_bar = bl.attn + l;
+          q.push_back(in);
+        }
+    range_end(b0);
+    b0 = range_begin();
+    for (int r = 0; r < H; r += hp.r_o) {
+      Instr in = make(OP_O, l, r, std::min(hp.r_o, H - r));
+      set_wait(in, bl.attn + l, (uint32_t)(max_batch * nkv));
+      in.rel_bar = bl.o + l;
+      q.push_back(in);
+    }
+    range_end(b0);
+    b0 = range_begin();
+    for (int r = 0; r < F; r += hp.r_gu) {
+      Instr in = make(OP_GU, l, r, std::min(hp.r_gu, F - r));
+      set_wait(in, bl.o + l, hp.n_o_tiles);
+      in.rel_bar = bl.gu + l;
+      q.push_back(in);
+    }
+    range_end(b0);
+    b0 = range_begin();
+    for (int r = 0; r < H; r += hp.r_down) {
+      Instr in = make(OP_DOWN, l, r, std::min(hp.r_down, H - r));
+      set_wait(in, bl.gu + l, hp.n_gu_tiles);
+      in.rel_bar = bl.down + l;
+      q.push_back(in);
+    }
+    range_end(b0);
+  }
+  uint32_t b0 = range_begin();
+  for (int r = 0; r < c.vocab; r += hp.r_lm) {
+    Instr in = make(OP_LM, L - 1, r, std::min(hp.r_lm, c.vocab - r));
+    set_wait(in, bl.down + L - 1, hp.n_down_tiles);
+    in.rel_bar = bl.lm;
+    q.push_back(in);
+  }
+  range_end(b0);
+
+  const uint64_t per_layer = (uint64_t)hp.qkv_rows * H + (uint64_t)H * qd + 3ull * F * H;
+  hp.weight_bytes = 2 * (per_layer * L + (uint64_t)c.vocab * H);
+  return MK_OK;
+}
+
+namespace {
+
+// Group key of a split-KV instruction: (layer, sequence, kv head).
+uint64_t group_key(const Instr& in) {
+  return ((uint64_t)in.layer << 40) | ((uint64_t)in.a0 << 20) | (uint64_t)in.a1;
+}
+
+// Apply `in`'s release to the counters; returns the barrier that received +1,
+// or NO_BAR.
+uint32_t apply_release(const HostPlan& hp, const Instr& in, std::vector<uint32_t>& cnt,
+                       std::unordered_map<uint64_t, int>& arrivals) {
+  if (in.rel_bar == NO_BAR) return NO_BAR;
+  if (in.flags & IF_RELEASE_ON_COMBINE) {
+    int& a = arrivals[group_key(in)];
+    if (++a < hp.n_splits) return NO_BAR;
+  }
+  cnt[in.rel_bar] += 1;
+  return in.rel_bar;
+}
+
+}  // namespace
+
+void random_topological(const HostPlan& hp, const std::vector<Instr>& q, uint64_t seed,
+                        std::vector<Instr>* out) {
+  const uint32_t nb = hp.bl.total;
+  std::vector<uint32_t> cnt(nb, 0), target(nb, 0);
+  std::vector<std::vector<uint32_t>> waiters(nb);
+  std::vector<uint32_t> unmet(q.size(), 0);
+  std::vector<uint32_t> ready;
+  for (uint32_t i = 0; i < q.size(); ++i) {
+    const Instr& in = q[i];
+    if (in.wait_bar == NO_BAR || in.wait_n == 0) {
+      ready.push_back(i);
+      continue;
+    }
+    for (uint32_t k = 0; k < in.wait_n; ++k) {
+      uint32_t b = in.wait_bar + k * in.wait_stride;
+      waiters[b].push_back(i);
+      target[b] = in.wait_target;
+      unmet[i]++;
+    }
+  }
+  std::mt19937_64 rng(seed);
+  std::unordered_map<uint64_t, int> arrivals;
+  out->clear();
+  out->reserve(q.size());
+  while (!ready.empty()) {
+    size_t pick = (size_t)(rng() % ready.size());
+    uint32_t i = ready[pick];
+    ready[pick] = ready.back();
+    ready.pop_back();
+    out->push_back(q[i]);
+    uint32_t b = apply_release(hp, q[i], cnt, arrivals);
+    if (b != NO_BAR && cnt[b] == target[b])
+      for (uint32_t w : waiters[b])
+        if (--unmet[w] == 0) ready.push_back(w);
+  }
+}
+
+int simulate(const HostPlan& hp, const std::vector<Instr>& q, std::string* why) {
+  std::vector<uint32_t> cnt(hp.bl.total, 0);
+  std::unordered_map<uint64_t, int> arrivals;
+  for (size_t i = 0; i < q.size(); ++i) {
+    const Instr& in = q[i];
+    if (in.op == OP_NOP || in.op >= OP_COUNT) {
+      if (why) *why = "unknown opcode at index " + std::to_string(i);
+      return MK_ERR_INVALID_ARG;
+    }
+    if (in.wait_bar != NO_BAR)
+      for (uint32_t k = 0; k < in.wait_n; ++k) {
+        uint32_t b = in.wait_bar + k * in.wait_stride;
+        if (b >= hp.bl.total || cnt[b] < in.wait_target) {
+          if (why)
+            *why = "instruction " + std::to_string(i) + " waits on barrier " + std::to_string(b) +
+                   " before its producers ran";
+          return MK_ERR_INVALID_ARG;
+        }
+      }
+    apply_release(hp, in, cnt, arrivals);
+  }
+  for (size_t i = 0; i < q.size(); ++i) {
+    const Instr& in = q[i];
+    if (in.wait_bar == NO_BAR) continue;
+    for (uint32_t k = 0; k < in.wait_n; ++k) {
+      uint32_t b = in.wait_bar + k * in.wait_stride;
+      if (cnt[b] != in.wait_target) {
+        if (why)
+          *why = "barrier " + std::to_string(b) + " receives " + std::to_string(cnt[b]) +
+                 " releases but instruction " + std::to_string(i) + " expects " +
+                 std::to_string(in.wait_target);
+        return MK_ERR_INVALID_ARG;
+      }
+    }
+  }
+  return MK_OK;
+}
+
+}  // namespace mk

@@ -1,0 +1,58 @@
+// Host plan builder: tile DAG -> instruction queue + barrier tensor + symbolic
+// extents, plus a sequential simulator used by the host-only checks.
+#pragma once
+#include <stdint.h>
+
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+
+namespace mk {
+
+// Kernel geometry shared by the plan builder and the kernel.
+constexpr int NW = 8;                 // consumer warps per CTA
+constexpr int NT = NW * 32;           // consumer threads
+constexpr int NTHREADS = NT + 32;     // + one producer warp
+constexpr int NSTAGE = 6;             // weight/KV ring stages
+constexpr int STAGE_BYTES = 32768;    // bytes per ring stage
+constexpr int NISLOT = 8;             // instruction slots between producer and consumers
+constexpr int RMAX = 16;              // GEMV rows per tile (both matrices of a gate/up tile)
+constexpr int BMAX_CC = 8;            // CUDA-core GEMV batch limit
+constexpr int XBUF_BYTES = 24576;     // activation / attention scratch in shared memory
+constexpr int XBUF_FLOATS = XBUF_BYTES / 4;
+constexpr int SCORE_FLOATS = 4096;    // attention scores per split (all q heads of a group)
+constexpr int FAST_K_UNIT = 8 * NT;   // K must be a multiple of this for the batch-1 fast path
+
+struct HostPlan {
+  mk_model_cfg cfg{};
+  int max_batch = 0, max_ctx = 0;
+  int rep = 0, qkv_rows = 0, n_splits = 0, split_max = 0;
+  int r_qkv = 0, r_o = 0, r_gu = 0, r_down = 0, r_lm = 0;
+  uint32_t n_qkv_tiles = 0, n_o_tiles = 0, n_gu_tiles = 0, n_down_tiles = 0, n_lm_tiles = 0;
+  bool fast_b1 = false;     // every GEMV K allows the batch-1 register path
+  BarLayout bl{};
+  std::vector<Instr> decode;                               // default topological order
+  std::vector<std::pair<uint32_t, uint32_t>> perop_decode;  // (first, count) per launch
+  std::vector<uint32_t> expr;                               // XS_COUNT * X_MAX_WORDS
+  uint64_t weight_bytes = 0;
+};
+
+// Validate the shape and build the plan.  Returns MK_OK or an MK_ERR_* code
+// with a reason in *why.
+int build_plan(const mk_model_cfg& cfg, int max_batch, int max_ctx, HostPlan* out,
+               std::string* why);
+
+// A seeded random topological order of queue `q` (Kahn's algorithm on the
+// barrier counters).  Any topological order is a valid pop order.
+void random_topological(const HostPlan& hp, const std::vector<Instr>& q, uint64_t seed,
+                        std::vector<Instr>* out);
+
+// Run `q` in order on a host model of the barrier counters.  Returns MK_OK when
+// every wait is satisfied on arrival and every waited barrier ends with exactly
+// the count its waiters expect.
+int simulate(const HostPlan& hp, const std::vector<Instr>& q, std::string* why);
+
+}  // namespace mk
