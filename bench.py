@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Decode benchmark: Llama-3-8B-shape decode step, batch 1, context 4096.
+
+One step = one whole decode step of the model (32 layers + LM head) for one
+new token, run as one persistent kernel launch through the C ABI.  Prints one
+JSON line (rank 0).  See the design doc for the metric, the roofline arithmetic and
+the input recipe.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain NumPy forward pass) on the host
+cores on a bounded sample of the same workload (a few layers + the LM head per
+step, scaled to the full layer count).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and HBM GB/s (% of ~8 TB/s), Llama-3-8B shape, batch 1, 1xGB300"
+UNIT = "tokens/s"
+CONTEXT = 4096
+BATCH = 1
+
+
+def workload_cfg():
+    from tile_level_overlap_gb300 import synth
+    return synth.LLAMA3_8B
+
+
+def algorithmic_bytes(cfg, batch, positions) -> int:
+    """Bytes one decode step must move at minimum: every weight once, the
+    cached K/V of every sequence once, the new K/V written; activations are
+    negligible (< 1 MB) and left out."""
+    H, d, F = cfg.hidden, cfg.head_dim, cfg.ffn
+    qd = cfg.n_q_heads * d
+    per_layer = (cfg.n_q_heads + 2 * cfg.n_kv_heads) * d * H + H * qd + 3 * F * H
+    weights = 2 * (cfg.n_layers * per_layer + cfg.vocab * H)
+    kv_read = sum(2 * cfg.n_layers * cfg.n_kv_heads * int(p) * d * 2 for p in positions)
+    kv_write = batch * 2 * cfg.n_layers * cfg.n_kv_heads * d * 2
+    return weights + kv_read + kv_write
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tile_level_overlap_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    e = rec.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if out.returncode == 0 and out.stdout.strip():
+                    self.rows.append([s.strip() for s in out.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        import statistics
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm: the oracle
+class OracleSample:
+    """The CPU oracle on a bounded sample of the decode step: `n_layers_sample`
+    layers + the LM head (weights drawn on the CPU with the same recipe)."""
+
+    def __init__(self, cfg, n_layers_sample: int, seed: int = 0):
+        import torch
+
+        from tile_level_overlap_gb300 import synth
+
+        torch.set_num_threads(cpu_cores())
+        self.cfg = cfg
+        self.n = n_layers_sample
+        self.sub = cfg.replace(n_layers=n_layers_sample)
+        self.w = synth.weights_as_bits(synth.make_weights(self.sub, seed=seed, device="cpu"))
+        self.kv = synth.bf16_bits(synth.make_kv_cache(self.sub, 1, CONTEXT + 1, device="cpu"))
+        self.tok = synth.make_tokens(1, cfg.vocab).numpy()
+
+    def step(self):
+        """Returns (seconds scaled to the full layer count, seconds measured)."""
+        import numpy as np
+
+        import oracle
+        from oracle import model as om
+
+        t0 = time.perf_counter()
+        oracle.decode_step(self.sub, self.w, self.tok, [CONTEXT], self.kv)
+        t_all = time.perf_counter() - t0
+        # the LM head alone, so that only the layer part is scaled
+        x = np.random.default_rng(0).normal(size=(1, self.cfg.hidden)).astype(np.float32)
+        t1 = time.perf_counter()
+        om.linear(self.w["lm_head"], om.rmsnorm(x, self.w["final_norm"], self.cfg.rms_eps))
+        t_lm = time.perf_counter() - t1
+        t_layers = max(t_all - t_lm, 1e-9)
+        return t_layers * self.cfg.n_layers / self.n + t_lm, t_all
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = workload_cfg()
+    n_s = args.ref_layers
+    sample_run = OracleSample(cfg, n_s)
+    for _ in range(args.warmup):
+        sample_run.step()
+    times, measured = [], 0.0
+    for _ in range(args.steps):
+        t, tm = sample_run.step()
+        times.append(t)
+        measured += tm
+    ms = 1e3 * sum(times) / len(times)
+    value = BATCH / (ms / 1e3)
+    sample = (f"{n_s} of {cfg.n_layers} layers + the LM head of one batch-1 decode step at context "
+              f"{CONTEXT}, per step; time scaled to {cfg.n_layers} layers")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "Llama-3-8B-shape decode, batch 1, context 4096",
+                   "weights": "bf16", "kv_cache": "bf16"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from tile_level_overlap_gb300 import mk, synth
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    cfg = workload_cfg()
+    max_ctx = CONTEXT + 1
+    w = synth.make_weights(cfg, seed=synth.SEED_WEIGHTS + rank, device=dev)
+    kv = synth.make_kv_cache(cfg, BATCH, max_ctx, device=dev)
+    plan = mk.Plan(cfg, w, BATCH, max_ctx)
+    tokens = synth.make_tokens(BATCH, cfg.vocab).to(dev)
+    positions = torch.full((BATCH,), CONTEXT, dtype=torch.int32, device=dev)
+    logits = torch.empty((BATCH, cfg.vocab), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    nbytes = algorithmic_bytes(cfg, BATCH, positions.tolist())
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+
+    def timed(fn, steps):
+        barrier()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(steps):
+                fn()
+            ev1.record(stream)
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        if pg:
+            t = torch.tensor([ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    def mega():
+        plan.decode_step(tokens, positions, kv, logits, stream=stream)
+
+    def perop():
+        plan.run_per_op(mk.MK_DECODE, tokens, positions, kv, logits, use_graph=False, stream=stream)
+
+    def perop_graph():
+        plan.run_per_op(mk.MK_DECODE, tokens, positions, kv, logits, use_graph=True, stream=stream)
+
+    for _ in range(args.warmup):
+        mega()
+    rc = plan.status(stream)
+    if rc != mk.MK_OK:
+        raise RuntimeError(f"device status {rc}")
+
+    with ClockSampler(local) as clk:
+        ms_total = timed(mega, args.steps)
+    rc = plan.status(stream)
+    if rc != mk.MK_OK:
+        raise RuntimeError(f"device status {rc}")
+    ms = ms_total / args.steps
+    value = world * BATCH * args.steps / (ms_total / 1e3)
+
+    # the same tile routines, kernel-per-operator (eager and CUDA graph)
+    for _ in range(max(1, args.warmup // 2)):
+        perop()
+        perop_graph()
+    ms_perop = timed(perop, args.steps) / args.steps
+    ms_graph = timed(perop_graph, args.steps) / args.steps
+    launches_perop = plan.stats().n_launches_per_op_decode
+
+    # end to end through the host-buffer entry point: pinned host tokens and
+    # positions in, logits out, every step
+    th = tokens.cpu().pin_memory()
+    ph = positions.cpu().pin_memory()
+    lh = torch.empty((BATCH, cfg.vocab), dtype=torch.float32).pin_memory()
+    for _ in range(2):
+        plan.decode_step_host(th, ph, kv, lh, stream=stream)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        rc = plan.decode_step_host(th, ph, kv, lh, stream=stream)
+        if rc != mk.MK_OK:
+            raise RuntimeError(f"device status {rc}")
+    e2e_s = time.perf_counter() - t0
+    if pg:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = world * BATCH * args.steps / e2e_s
+
+    # dependency-wait share from one traced step (not timed)
+    plan.set_debug(trace=True)
+    mega()
+    torch.cuda.synchronize(dev)
+    rec = plan.trace().astype(np.int64)
+    plan.set_debug(trace=False)
+    span = rec[:, 3].max() - rec[:, 1].min()
+    n_ctas = plan.stats().n_ctas
+    dep_wait = float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span) if span > 0 else None
+
+    if rank != 0:
+        return 0
+    peaks, kind = measured_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    traffic = recorded_traffic("mk_interpreter", "llama3-8b-decode-b1-ctx4096")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "Llama-3-8B-shape decode, batch 1, context 4096",
+                   "layers": cfg.n_layers, "hidden": cfg.hidden, "ffn": cfg.ffn,
+                   "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
+                   "head_dim": cfg.head_dim, "vocab": cfg.vocab, "batch": BATCH,
+                   "context": CONTEXT, "weights": "bf16", "kv_cache": "bf16",
+                   "activations": "f32",
+                   "l2": f"inputs larger than L2: {nbytes / 1e9:.2f} GB streamed per step",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "hbm_gbs": achieved,
+        "hbm_frac_of_8tbs": achieved / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_kind": kind, "kernel": "mk_interpreter",
+                     "algorithmic_bytes_per_launch": nbytes},
+        "per_op": {"ms_per_step_eager": ms_perop, "ms_per_step_graph": ms_graph,
+                   "tokens_per_s_eager": BATCH / (ms_perop / 1e3),
+                   "tokens_per_s_graph": BATCH / (ms_graph / 1e3),
+                   "launches_per_step": launches_perop,
+                   "speedup_persistent_vs_graph": ms_graph / ms},
+        "dep_wait_fraction": dep_wait,
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": 8 * BATCH,
+                "d2h_bytes_per_step": 4 * BATCH * cfg.vocab + 4},
+        "gpu_launches": args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        sample_run = OracleSample(cfg, args.ref_layers)
+        sample_run.step()
+        t = sorted(sample_run.step()[0] for _ in range(3))[1]
+        line["cpu_baseline"] = {
+            "value": BATCH / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{args.ref_layers} of {cfg.n_layers} layers + the LM head of one batch-1 "
+                      f"decode step at context {CONTEXT}, scaled to {cfg.n_layers} layers"}
+    print(json.dumps(line), flush=True)
+    plan.close()
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-layers", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -9,20 +9,13 @@
 #include "../../include/mk.h"
 #include "mk_internal.h"
 #include "mk_plan.h"
-
-namespace mk {
-int smem_bytes();
-cudaError_t kernel_setup();
-cudaError_t max_coresident(int* per_sm);
-cudaError_t launch_mega(const KParams& p, int ctas, int fast, cudaStream_t st);
-cudaError_t launch_perop(const KParams& p, uint32_t first, uint32_t count, int fast,
-                         cudaStream_t st);
-}  // namespace mk
+#include "mk_variants.h"
 
 using namespace mk;
 
 struct mk_plan {
   HostPlan hp;
+  KernelVariant kv{};
   int device = 0, n_sms = 0, max_ctas = 0;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -57,6 +50,20 @@ struct Bump {
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ERR_CUDA; }
+
+// The compiled interpreter specialisation for this shape, else the generic one.
+KernelVariant pick_variant(const HostPlan& hp) {
+  const mk_model_cfg& c = hp.cfg;
+  if (hp.fast_b1) {
+    const KernelVariant cands[] = {variant_h1_f4_d64_r4(), variant_h2_f7_d128_r4(),
+                                   variant_h2_f6_d128_r4()};
+    for (const KernelVariant& v : cands)
+      if (v.mh * FAST_K_UNIT == c.hidden && v.mf * FAST_K_UNIT == c.ffn && v.ad == c.head_dim &&
+          v.arep == hp.rep)
+        return v;
+  }
+  return variant_generic();
+}
 
 #define MK_CUDA(call)                        \
   do {                                       \
@@ -171,9 +178,10 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   if (cudaGetDevice(&p->device) != cudaSuccess) return fail(MK_ERR_CUDA);
   if (cudaDeviceGetAttribute(&p->n_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
     return fail(MK_ERR_CUDA);
-  if (kernel_setup() != cudaSuccess) return fail(MK_ERR_CUDA);
+  p->kv = pick_variant(p->hp);
+  if (p->kv.setup() != cudaSuccess) return fail(MK_ERR_CUDA);
   int per_sm = 0;
-  if (max_coresident(&per_sm) != cudaSuccess || per_sm < 1) return fail(MK_ERR_CUDA);
+  if (p->kv.occupancy(&per_sm) != cudaSuccess || per_sm < 1) return fail(MK_ERR_CUDA);
   p->max_ctas = p->n_sms;
 
   // one scratch allocation
@@ -314,7 +322,7 @@ int mk_decode_step(mk_plan* p, const int32_t* tokens, const int32_t* positions, 
   if (rc != MK_OK) return rc;
   KParams k = step_params(p, tokens, positions, batch, kv, logits);
   const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
-  return cuda_err(launch_mega(k, ctas, p->hp.fast_b1 ? 1 : 0, (cudaStream_t)stream));
+  return cuda_err(p->kv.mega(k, ctas, (cudaStream_t)stream));
 }
 
 int mk_decode_step_host(mk_plan* p, const int32_t* tokens_host, const int32_t* positions_host,
@@ -344,8 +352,7 @@ int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logi
 }
 
 static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
-  const int fast = p->hp.fast_b1 ? 1 : 0;
-  for (const auto& r : p->hp.perop_decode) MK_CUDA(launch_perop(k, r.first, r.second, fast, st));
+  for (const auto& r : p->hp.perop_decode) MK_CUDA(p->kv.perop(k, r.first, r.second, st));
   return MK_OK;
 }
 

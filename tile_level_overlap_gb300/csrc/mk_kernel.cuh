@@ -21,8 +21,12 @@
 #include "mk_device.cuh"
 #include "mk_internal.h"
 #include "mk_plan.h"
+#include "mk_variants.h"
 
 namespace mk {
+// Everything below except make_variant() has internal linkage: this header is
+// compiled once per kernel specialisation.
+namespace {
 
 constexpr uint32_t END_SLOT = 0xffffffffu;
 constexpr int CONSUMER_BAR = 1;
@@ -36,8 +40,9 @@ struct SmemLayout {
   static constexpr int ssw = redw + NW * RMAX * 4;         // [NW][BMAX_CC] floats
   static constexpr int bars = ssw + NW * BMAX_CC * 4;      // mbarriers
   static constexpr int n_mbar = 2 * NSTAGE + 2 * NISLOT;
-  static constexpr int islot = bars + n_mbar * 8;
-  static constexpr int flags = islot + NISLOT * 4;         // [8] u32
+  static constexpr int islot = bars + n_mbar * 8;          // [NISLOT] x {u32 index, pad, Instr}
+  static constexpr int islot_bytes = 48;
+  static constexpr int flags = islot + NISLOT * islot_bytes;  // [8] u32
   static constexpr int total = flags + 8 * 4;
 };
 static_assert(SmemLayout::total <= 227 * 1024, "shared memory budget");
@@ -54,9 +59,16 @@ struct Sh {
   uint64_t* empty;
   uint64_t* ifull;
   uint64_t* iempty;
-  volatile uint32_t* islot;
+  uint8_t* islot;
   volatile uint32_t* flags;
 };
+
+__device__ __forceinline__ volatile uint32_t* slot_index(const Sh& S, int si) {
+  return reinterpret_cast<volatile uint32_t*>(S.islot + si * SmemLayout::islot_bytes);
+}
+__device__ __forceinline__ Instr* slot_instr(const Sh& S, int si) {
+  return reinterpret_cast<Instr*>(S.islot + si * SmemLayout::islot_bytes + 16);
+}
 
 __device__ __forceinline__ Sh sh_map(uint8_t* base) {
   Sh s;
@@ -70,7 +82,7 @@ __device__ __forceinline__ Sh sh_map(uint8_t* base) {
   s.empty = b + NSTAGE;
   s.ifull = b + 2 * NSTAGE;
   s.iempty = b + 2 * NSTAGE + NISLOT;
-  s.islot = reinterpret_cast<volatile uint32_t*>(base + SmemLayout::islot);
+  s.islot = base + SmemLayout::islot;
   s.flags = reinterpret_cast<volatile uint32_t*>(base + SmemLayout::flags);
   return s;
 }
@@ -213,27 +225,41 @@ __device__ void producer(const KParams& P, const Sh& S) {
   if (lane != 0) return;
   const uint64_t policy = policy_evict_first();
   uint32_t stage_ctr = 0, islot_ctr = 0;
-  bool first = true;
-  for (;;) {
-    uint32_t i;
-    bool end;
+  // Pops run two instructions ahead of the one being streamed, so the latency
+  // of the queue atomic and of the record load overlaps the streaming of the
+  // current instruction.  Pop order is still this CTA's execution order.
+  uint32_t npop = 0;
+  auto pop = [&]() -> uint32_t {
+    const uint32_t k = npop++;
     if (P.mode == MODE_MEGA) {
-      end = ld_volatile(&P.ctl[CTL_ABORT]) != 0u;
-      i = end ? END_SLOT : atomicAdd(&P.ctl[CTL_HEAD], 1u);
-      end = end || i >= P.n_instr;
-    } else {
-      i = first ? P.perop_base + blockIdx.x : END_SLOT;
-      end = !first;
-      first = false;
+      if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) return END_SLOT;
+      const uint32_t i = atomicAdd(&P.ctl[CTL_HEAD], 1u);
+      return i < P.n_instr ? i : END_SLOT;
     }
+    return k == 0 ? P.perop_base + blockIdx.x : END_SLOT;
+  };
+  uint32_t ia = pop();
+  uint32_t ib = pop();
+  Instr Ia;
+  if (ia != END_SLOT) Ia = P.queue[ia];
+  for (;;) {
+    const bool end = ia == END_SLOT;
+    Instr Ib;
+    if (!end && ib != END_SLOT) Ib = P.queue[ib];
+    const uint32_t ic = (end || ib == END_SLOT) ? END_SLOT : pop();
     const int si = islot_ctr % NISLOT;
-    if (!mbar_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) end = true;
-    S.islot[si] = end ? END_SLOT : i;
+    bool posted_end = end;
+    if (!mbar_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) posted_end = true;
+    if (!posted_end) *slot_instr(S, si) = Ia;
+    *slot_index(S, si) = posted_end ? END_SLOT : ia;
     mbar_arrive(&S.ifull[si]);
     ++islot_ctr;
-    if (end) break;
+    if (posted_end) break;
 
-    const Instr in = P.queue[i];
+    const Instr in = Ia;
+    ia = ib;
+    Ia = Ib;
+    ib = ic;
     const Src src = instr_src(P, in);
     bool stuck = false;
     for (int r = 0; r < src.nreg && !stuck; ++r) {
@@ -338,14 +364,17 @@ __device__ __forceinline__ void load_x8(const KParams& P, const float* xs, const
 // in registers; every row of the tile adds into acc[row]; one multi-value warp
 // reduction and a fixed-order sum over warps per tile.
 template <int M>
-__device__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
-                          const Src& src, Ring& R) {
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int K = g.K;
+__device__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in, float (&xr)[M][8]) {
+  const int t = threadIdx.x;
+  const int K = M * FAST_K_UNIT;
   const float* xs = gemv_x(P, in);
   const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0) * P.H;
   const uint16_t* gain = gemv_gain(P, in);
-  float xr[M][8];
+  uint4 gw[M];
+  if (gain) {
+#pragma unroll
+    for (int j = 0; j < M; ++j) gw[j] = __ldg(reinterpret_cast<const uint4*>(gain + 8 * (t + NT * j)));
+  }
 #pragma unroll
   for (int j = 0; j < M; ++j) load_x8(P, xs, emb_row, 0, K, 8 * (t + NT * j), xr[j]);
   if (gain) {
@@ -358,12 +387,19 @@ __device__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in, const 
     const float inv = 1.0f / sqrtf(ss / (float)K + P.eps);
 #pragma unroll
     for (int j = 0; j < M; ++j) {
-      float gw[8];
-      widen8(__ldg(reinterpret_cast<const uint4*>(gain + 8 * (t + NT * j))), gw);
+      float g8[8];
+      widen8(gw[j], g8);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) xr[j][e] = xr[j][e] * inv * gw[e];
+      for (int e = 0; e < 8; ++e) xr[j][e] = xr[j][e] * inv * g8[e];
     }
   }
+}
+
+template <int M>
+__device__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
+                          const Src& src, Ring& R, const float (&xr)[M][8]) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int K = g.K;
   float acc[RMAX];
 #pragma unroll
   for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
@@ -471,59 +507,52 @@ __device__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, con
   cbar();
 }
 
-// Store a finished GEMV tile: y[r][b] is in S.red.
-__device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g) {
+// The residual input of an O / down tile output element (thread t owns output
+// (r, b) = (t / B, t % B)); loaded before the tile streams so that its latency
+// is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
+// (RMAX * BMAX_CC <= NT).
+__device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr& in,
+                                                   const GemvDesc& g) {
   const int t = threadIdx.x, B = P.B, l = in.layer;
-  const int nout = g.rows;
+  if (t >= g.rows * B) return 0.f;
+  const int r = t / B, b = t % B, row = g.row0 + r;
   const size_t bh = (size_t)P.max_batch * P.H;
-  for (int idx = t; idx < nout * B; idx += NT) {
-    const int r = idx / B, b = idx % B, row = g.row0 + r;
-    const float y = S.red[r * BMAX_CC + b];
-    switch (in.op) {
-      case OP_QKV:
-        P.qkv[((size_t)l * P.max_batch + b) * P.qkv_rows + row] = y;
-        break;
-      case OP_O: {
-        float prev;
-        if (l == 0) prev = __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b) * P.H + row] << 16);
-        else prev = __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
-        P.resid[(size_t)(2 * l + 1) * bh + (size_t)b * P.H + row] = prev + y;
-        break;
-      }
-      case OP_GU: {
-        const float u = S.red[(g.rows + r) * BMAX_CC + b];
-        P.act[((size_t)l * P.max_batch + b) * P.F + row] = y / (1.0f + expf(-y)) * u;
-        break;
-      }
-      case OP_DOWN: {
-        const size_t o = (size_t)b * P.H + row;
-        P.resid[(size_t)(2 * l + 2) * bh + o] = __ldcg(P.resid + (size_t)(2 * l + 1) * bh + o) + y;
-        break;
-      }
-      default:
-        P.logits[(size_t)b * P.V + row] = y;
-        break;
-    }
+  if (in.op == OP_O) {
+    if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b) * P.H + row] << 16);
+    return __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
   }
+  if (in.op == OP_DOWN) return __ldcg(P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row);
+  return 0.f;
 }
 
-__device__ void gemv_tile(const KParams& P, const Sh& S, const Instr& in, Ring& R, bool fast) {
-  const GemvDesc g = gemv_desc(P, in);
-  const Src src = instr_src(P, in);
-  if (fast && P.B == 1) {
-    switch (g.K / FAST_K_UNIT) {
-      case 1: gemv_fast<1>(P, S, in, g, src, R); break;
-      case 2: gemv_fast<2>(P, S, in, g, src, R); break;
-      case 3: gemv_fast<3>(P, S, in, g, src, R); break;
-      case 4: gemv_fast<4>(P, S, in, g, src, R); break;
-      case 5: gemv_fast<5>(P, S, in, g, src, R); break;
-      case 6: gemv_fast<6>(P, S, in, g, src, R); break;
-      default: gemv_fast<7>(P, S, in, g, src, R); break;
+// Store a finished GEMV tile: y[r][b] is in S.red; `pre` is this thread's
+// residual input from epilogue_prefetch.
+__device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
+                              float pre) {
+  const int t = threadIdx.x, B = P.B, l = in.layer;
+  if (t >= g.rows * B) return;
+  const int r = t / B, b = t % B, row = g.row0 + r;
+  const size_t bh = (size_t)P.max_batch * P.H;
+  const float y = S.red[r * BMAX_CC + b];
+  switch (in.op) {
+    case OP_QKV:
+      P.qkv[((size_t)l * P.max_batch + b) * P.qkv_rows + row] = y;
+      break;
+    case OP_O:
+      P.resid[(size_t)(2 * l + 1) * bh + (size_t)b * P.H + row] = pre + y;
+      break;
+    case OP_GU: {
+      const float u = S.red[(g.rows + r) * BMAX_CC + b];
+      P.act[((size_t)l * P.max_batch + b) * P.F + row] = y / (1.0f + expf(-y)) * u;
+      break;
     }
-  } else {
-    gemv_generic(P, S, in, g, src, R);
+    case OP_DOWN:
+      P.resid[(size_t)(2 * l + 2) * bh + (size_t)b * P.H + row] = pre + y;
+      break;
+    default:
+      P.logits[(size_t)b * P.V + row] = y;
+      break;
   }
-  gemv_epilogue(P, S, in, g);
 }
 
 // ---------------------------------------------------------------- decode attention (split-KV)
@@ -692,7 +721,6 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32
   }
   cbar();
   if (t == 0) {
-    __threadfence();
     uint32_t* arr = P.arrive + ((size_t)l * P.max_batch + b) * P.nkv + g;
     const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
     const bool last = old == (uint32_t)(NS - 1);
@@ -719,15 +747,15 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32
       }
     }
     cbar();
-    if (t == 0 && P.mode == MODE_MEGA) {
-      __threadfence();
-      red_release_gpu_add(&P.bars[in.rel_bar], 1u);
-    }
+    if (t == 0 && P.mode == MODE_MEGA) red_release_gpu_add(&P.bars[in.rel_bar], 1u);
   }
 }
 
+template <int AD, int AREP>
 __device__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, uint32_t ii, Ring& R) {
-  if (P.d == 128) {
+  if constexpr (AD != 0) {
+    attn_tile<AD, AREP>(P, S, in, ii, R);
+  } else if (P.d == 128) {
     switch (P.rep) {
       case 1: attn_tile<128, 1>(P, S, in, ii, R); break;
       case 2: attn_tile<128, 2>(P, S, in, ii, R); break;
@@ -754,26 +782,40 @@ __device__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
 }
 
 // ---------------------------------------------------------------- consumer loop
-__device__ void consumer(const KParams& P, const Sh& S, bool fast) {
+// MH, MF: K / FAST_K_UNIT of the hidden size and of the FFN size for the
+// batch-1 register path (0: the shared-memory path only).  AD, AREP: head_dim
+// and q heads per kv head of the attention tile (0: chosen at run time).
+template <int MH, int MF, int AD, int AREP>
+__device__ void consumer(const KParams& P, const Sh& S) {
   const int t = threadIdx.x;
   Ring R{0};
   uint32_t islot_ctr = 0;
   const uint32_t gen = S.flags[F_GEN];
+  constexpr int XH = MH > 0 ? MH : 1, XF = MF > 0 ? MF : 1;
+  // Normed activations stay in registers while consecutive tiles read the
+  // same vector (same operator and layer): the tag names what they hold.
+  float xh[XH][8], xf[XF][8];
+  uint32_t tag_h = 0xffffffffu, tag_f = 0xffffffffu;
+  // Last barrier (and target) thread 0 saw satisfied: counters only grow
+  // within a launch, so a repeat wait needs no new load.
+  uint32_t ok_bar = NO_BAR, ok_target = 0;
   for (;;) {
     const int si = islot_ctr % NISLOT;
     // one thread takes the slot (a bounded wait); the consumer barrier hands
-    // the index to the others so that every consumer thread takes the same path
+    // it to the others so that every consumer thread takes the same path
     if (t == 0) {
       uint32_t v = 0xffffffffu;
-      if (mbar_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u)) v = S.islot[si];
+      if (mbar_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u)) v = *slot_index(S, si);
       S.flags[F_SLOT] = v;
     }
     cbar();
     const uint32_t i = S.flags[F_SLOT];
+    Instr in;
+    if (i != END_SLOT) in = *slot_instr(S, si);
+    __syncwarp();
     if ((t & 31) == 0) mbar_arrive(&S.iempty[si]);
     ++islot_ctr;
     if (i == END_SLOT) break;
-    const Instr in = P.queue[i];
     const uint64_t t_begin = P.trace ? globaltimer() : 0;
 
     // wait on the tiles this instruction reads
@@ -781,19 +823,25 @@ __device__ void consumer(const KParams& P, const Sh& S, bool fast) {
       uint32_t aborted = ld_volatile(&P.ctl[CTL_ABORT]) != 0u;
       if (!aborted && P.mode == MODE_MEGA && in.wait_bar != NO_BAR) {
         const uint32_t target = (gen + 1u) * in.wait_target;
-        const uint64_t t0 = globaltimer();
-        for (uint32_t k = 0; k < in.wait_n && !aborted;) {
-          const uint32_t* c = &P.bars[in.wait_bar + k * in.wait_stride];
-          if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
-            ++k;
-            continue;
+        if (!(in.wait_n == 1 && in.wait_bar == ok_bar && target == ok_target)) {
+          const uint64_t t0 = globaltimer();
+          for (uint32_t k = 0; k < in.wait_n && !aborted;) {
+            const uint32_t* c = &P.bars[in.wait_bar + k * in.wait_stride];
+            if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
+              ++k;
+              continue;
+            }
+            if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) aborted = 1;
+            else if (globaltimer() - t0 > P.wait_limit_ns) {
+              set_error(P, MK_ERR_TIMEOUT, i);
+              aborted = 1;
+            } else {
+              __nanosleep(32);
+            }
           }
-          if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) aborted = 1;
-          else if (globaltimer() - t0 > P.wait_limit_ns) {
-            set_error(P, MK_ERR_TIMEOUT, i);
-            aborted = 1;
-          } else {
-            __nanosleep(64);
+          if (!aborted && in.wait_n == 1) {
+            ok_bar = in.wait_bar;
+            ok_target = target;
           }
         }
       }
@@ -807,14 +855,36 @@ __device__ void consumer(const KParams& P, const Sh& S, bool fast) {
       continue;
     }
     if (in.op == OP_ATTN) {
-      attn_dispatch(P, S, in, i, R);
+      attn_dispatch<AD, AREP>(P, S, in, i, R);
     } else {
-      gemv_tile(P, S, in, R, fast);
-      cbar();
-      if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR) {
-        __threadfence();
-        red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+      const GemvDesc g = gemv_desc(P, in);
+      const Src src = instr_src(P, in);
+      const float pre = epilogue_prefetch(P, in, g);
+      bool done = false;
+      if constexpr (MH > 0) {
+        if (P.B == 1) {
+          const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8);
+          if (in.op == OP_DOWN) {
+            if (tag != tag_f) {
+              load_x_fast<XF>(P, S, in, xf);
+              tag_f = tag;
+            }
+            gemv_fast<XF>(P, S, in, g, src, R, xf);
+          } else {
+            if (tag != tag_h) {
+              load_x_fast<XH>(P, S, in, xh);
+              tag_h = tag;
+            }
+            gemv_fast<XH>(P, S, in, g, src, R, xh);
+          }
+          done = true;
+        }
       }
+      if (!done) gemv_generic(P, S, in, g, src, R);
+      gemv_epilogue(P, S, in, g, pre);
+      cbar();
+      if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
+        red_release_gpu_add(&P.bars[in.rel_bar], 1u);
     }
     if (P.trace && t == 0) {
       unsigned long long* tr = P.trace + (size_t)i * 4;
@@ -827,8 +897,8 @@ __device__ void consumer(const KParams& P, const Sh& S, bool fast) {
   }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_constant__ KParams P,
-                                                               int fast) {
+template <int MH, int MF, int AD, int AREP>
+__global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_constant__ KParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Sh S = sh_map(smem);
   const int t = threadIdx.x;
@@ -847,7 +917,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
   }
   __syncthreads();
   if (t >= NT) producer(P, S);
-  else consumer(P, S, fast != 0);
+  else consumer<MH, MF, AD, AREP>(P, S);
   __syncthreads();
   if (t == 0 && P.mode == MODE_MEGA) {
     __threadfence();
@@ -863,33 +933,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
 }
 
 // ---------------------------------------------------------------- host-side launch helpers
-int smem_bytes() { return SmemLayout::total; }
+template <int MH, int MF, int AD, int AREP>
+struct VariantImpl {
+  static cudaError_t setup() {
+    return cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total);
+  }
+  static cudaError_t occupancy(int* per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk_interpreter<MH, MF, AD, AREP>,
+                                                         NTHREADS, SmemLayout::total);
+  }
+  static cudaError_t mega(const KParams& p, int ctas, cudaStream_t st) {
+    KParams pp = p;
+    void* args[] = {(void*)&pp};
+    return cudaLaunchCooperativeKernel((const void*)mk_interpreter<MH, MF, AD, AREP>, dim3(ctas),
+                                       dim3(NTHREADS), args, (size_t)SmemLayout::total, st);
+  }
+  static cudaError_t perop(const KParams& p, uint32_t first, uint32_t count, cudaStream_t st) {
+    KParams pp = p;
+    pp.mode = MODE_PEROP;
+    pp.perop_base = first;
+    mk_interpreter<MH, MF, AD, AREP><<<count, NTHREADS, SmemLayout::total, st>>>(pp);
+    return cudaGetLastError();
+  }
+};
 
-cudaError_t kernel_setup() {
-  return cudaFuncSetAttribute(mk_interpreter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SmemLayout::total);
-}
+}  // namespace
 
-cudaError_t max_coresident(int* per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk_interpreter, NTHREADS,
-                                                       SmemLayout::total);
-}
-
-cudaError_t launch_mega(const KParams& p, int ctas, int fast, cudaStream_t st) {
-  KParams pp = p;
-  int f = fast;
-  void* args[] = {(void*)&pp, (void*)&f};
-  return cudaLaunchCooperativeKernel((const void*)mk_interpreter, dim3(ctas), dim3(NTHREADS), args,
-                                     (size_t)SmemLayout::total, st);
-}
-
-cudaError_t launch_perop(const KParams& p, uint32_t first, uint32_t count, int fast,
-                         cudaStream_t st) {
-  KParams pp = p;
-  pp.mode = MODE_PEROP;
-  pp.perop_base = first;
-  mk_interpreter<<<count, NTHREADS, SmemLayout::total, st>>>(pp, fast);
-  return cudaGetLastError();
+template <int MH, int MF, int AD, int AREP>
+KernelVariant make_variant() {
+  using V = VariantImpl<MH, MF, AD, AREP>;
+  KernelVariant k;
+  k.mh = MH;
+  k.mf = MF;
+  k.ad = AD;
+  k.arep = AREP;
+  k.setup = &V::setup;
+  k.occupancy = &V::occupancy;
+  k.mega = &V::mega;
+  k.perop = &V::perop;
+  return k;
 }
 
 }  // namespace mk

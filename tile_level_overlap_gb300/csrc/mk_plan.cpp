@@ -15,6 +15,8 @@
 #include "mk_plan.h"
 
 #include <algorithm>
+
+#include "mk_variants.h"
 #include <cstring>
 #include <random>
 #include <unordered_map>
@@ -97,8 +99,9 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
     return bad(MK_ERR_UNSUPPORTED, "hidden, ffn and n_q_heads*head_dim must be multiples of 8");
   if (max_batch > BMAX_CC) return bad(MK_ERR_UNSUPPORTED, "batch above the CUDA-core decode limit");
   const int kmax = std::max(std::max(c.hidden, c.ffn), qd);
-  const bool fast = (c.hidden % FAST_K_UNIT == 0) && (c.ffn % FAST_K_UNIT == 0) &&
-                    (qd % FAST_K_UNIT == 0) && kmax / FAST_K_UNIT <= 7;
+  static_assert(FAST_K_UNIT == 2048, "fast-path shapes assume 8 columns x 256 threads");
+  const bool fast =
+      has_fast_variant(c.hidden, c.ffn, c.n_q_heads, c.n_kv_heads, c.head_dim);
   // The generic path (batch > 1, or K outside the fast set) holds x[B][K] in
   // shared memory.
   if ((!fast || max_batch > 1) && (long)max_batch * kmax > XBUF_FLOATS)
