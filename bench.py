@@ -130,6 +130,22 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """Max of a host float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Whole-job rate: units every rank processed / the slowest rank's time
+    (replicas: every rank runs the same per-rank work)."""
+    return world * units_per_rank / seconds_max
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -257,12 +273,7 @@ def run_ours(args):
                 fn()
             ev1.record(stream)
         barrier()
-        ms = ev0.elapsed_time(ev1)
-        if pg:
-            t = torch.tensor([ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
 
     def mega():
         plan.decode_step(tokens, positions, kv, logits, stream=stream)
@@ -285,7 +296,7 @@ def run_ours(args):
     if rc != mk.MK_OK:
         raise RuntimeError(f"device status {rc}")
     ms = ms_total / args.steps
-    value = world * BATCH * args.steps / (ms_total / 1e3)
+    value = job_throughput(BATCH * args.steps, world, ms_total / 1e3)
 
     # the same tile routines, kernel-per-operator (eager and CUDA graph)
     for _ in range(max(1, args.warmup // 2)):
@@ -308,12 +319,8 @@ def run_ours(args):
         rc = plan.decode_step_host(th, ph, kv, lh, stream=stream)
         if rc != mk.MK_OK:
             raise RuntimeError(f"device status {rc}")
-    e2e_s = time.perf_counter() - t0
-    if pg:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = world * BATCH * args.steps / e2e_s
+    e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
+    e2e = job_throughput(BATCH * args.steps, world, e2e_s)
 
     # dependency-wait share from one traced step (not timed)
     plan.set_debug(trace=True)

@@ -172,6 +172,15 @@ int mk_plan_set_debug(mk_plan *plan, int force_ctas, uint64_t queue_perm_seed, i
  * rebuilds the queue; mk_plan_reset() clears the latched error. */
 int mk_plan_debug_drop_release(mk_plan *plan, uint32_t index);
 
+/* Test-only: the tensor-core tile routine (tcgen05.mma with TMEM accumulators,
+ * TMA-fed 128-byte-swizzled operands) on one plain GEMM, synchronous:
+ *   C[M][N] (device f32) = A[M][K] (device bf16) * B[N][K]^T (device bf16),
+ * row-major, 16-byte aligned; N % 128 == 0, K % 64 == 0.  This is the
+ * contraction the batched-decode and prefill projections run ("MegaOps",
+ * Abstract: the dense Llama3/Qwen3 projections).  Returns MK_OK, an argument
+ * error, or MK_ERR_TIMEOUT if a bounded wait inside the kernel gave up. */
+int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int K, void *stream);
+
 /* Copy the trace of the last traced launch: records of
  * {uint32 smid, uint32 op | layer << 8, uint64 t_begin, uint64 t_ready, uint64 t_done}
  * (%globaltimer ns), one per instruction in pop order.  *n_records receives the

@@ -28,7 +28,7 @@ EXPORTED = [
     "mk_plan_create", "mk_plan_destroy", "mk_kv_cache_bytes", "mk_decode_step",
     "mk_decode_step_host", "mk_prefill", "mk_run_per_op", "mk_status", "mk_plan_reset",
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
-    "mk_trace_copy", "mk_plan_debug_drop_release",
+    "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16",
 ]
 
 
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
     L.mk_plan_set_debug.argtypes = [vp, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
+    L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
     _lib = L
     return L
 
