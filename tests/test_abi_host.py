@@ -22,7 +22,7 @@ def lib():
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mk_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mk_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_symbols_exported(lib):

@@ -43,11 +43,14 @@ struct SmemLayout {
   static constexpr int islot = bars + n_mbar * 8;          // [NISLOT] x {u32 index, pad, Instr}
   static constexpr int islot_bytes = 48;
   static constexpr int flags = islot + NISLOT * islot_bytes;  // [8] u32
-  static constexpr int total = flags + 8 * 4;
+  static constexpr int layers = flags + 8 * 4;             // [MAX_LAYERS] LayerW
+  static constexpr int total = layers + MAX_LAYERS * (int)sizeof(LayerW);
 };
 static_assert(SmemLayout::total <= 227 * 1024, "shared memory budget");
 
-enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3 };
+// F_STOP: set by a consumer that saw the abort word, read by the producer
+// before each pop (a shared-memory load instead of a global one).
+enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3, F_STOP = 4 };
 
 struct Sh {
   uint8_t* ring;
@@ -61,6 +64,7 @@ struct Sh {
   uint64_t* iempty;
   uint8_t* islot;
   volatile uint32_t* flags;
+  const LayerW* layers;  // copy of the per-layer weight pointers
 };
 
 __device__ __forceinline__ volatile uint32_t* slot_index(const Sh& S, int si) {
@@ -83,6 +87,7 @@ __device__ __forceinline__ Sh sh_map(uint8_t* base) {
   s.ifull = b + 2 * NSTAGE;
   s.iempty = b + 2 * NSTAGE + NISLOT;
   s.islot = base + SmemLayout::islot;
+  s.layers = reinterpret_cast<const LayerW*>(base + SmemLayout::layers);
   s.flags = reinterpret_cast<volatile uint32_t*>(base + SmemLayout::flags);
   return s;
 }
@@ -118,7 +123,15 @@ struct Src {
   int nreg;
 };
 
-__device__ __forceinline__ const LayerW& layer_w(const KParams& P, int l) { return P.layers[l]; }
+// The kernel's dynamic shared memory (every extern __shared__ array aliases it).
+extern __shared__ __align__(1024) uint8_t mk_dyn_smem[];
+
+// Per-layer weight pointers, from the copy the kernel prologue puts in shared
+// memory (no dependent global load on the producer's issue path).
+__device__ __forceinline__ const LayerW& layer_w(const KParams& P, int l) {
+  (void)P;
+  return reinterpret_cast<const LayerW*>(mk_dyn_smem + SmemLayout::layers)[l];
+}
 
 struct AttnExt {
   bool live;
@@ -232,7 +245,7 @@ __device__ void producer(const KParams& P, const Sh& S) {
   auto pop = [&]() -> uint32_t {
     const uint32_t k = npop++;
     if (P.mode == MODE_MEGA) {
-      if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) return END_SLOT;
+      if (S.flags[F_STOP]) return END_SLOT;
       const uint32_t i = atomicAdd(&P.ctl[CTL_HEAD], 1u);
       return i < P.n_instr ? i : END_SLOT;
     }
@@ -431,7 +444,9 @@ __device__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in, const 
   if (cur >= 0) ring_release(S, R);
 
   const float v = warp_reduce_multi<RMAX>(acc, lane);
-  if ((lane & 1) == 0) S.redw[w * RMAX + warp_multi_index<RMAX>(lane)] = v;
+  // after the butterfly, each group of 32 / RMAX consecutive lanes holds one total
+  constexpr int kDup = 32 / RMAX;
+  if ((lane & (kDup - 1)) == 0) S.redw[w * RMAX + warp_multi_index<RMAX>(lane)] = v;
   cbar();
   if (t < ntot) {
     float s = 0.f;
@@ -577,6 +592,15 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32
   float* part = P.part + ((((size_t)l * P.max_batch + b) * P.nkv + g) * NS + split) * rep * (D + 2);
 
   if (e.live) {
+    // RoPE factors of this thread's rotation pairs, fetched together with q/k/v
+    const float2* rt = P.rope + (size_t)e.pos * (D / 2);
+    constexpr int NROT = ((REP + 1) * (D / 2) + NT - 1) / NT;
+    float2 cs[NROT];
+#pragma unroll
+    for (int j = 0; j < NROT; ++j) {
+      const int i = t + j * NT;
+      cs[j] = i < (rep + 1) * (D / 2) ? __ldg(rt + i % (D / 2)) : make_float2(0.f, 0.f);
+    }
     const float* base = P.qkv + ((size_t)l * P.max_batch + b) * P.qkv_rows;
     for (int i = t; i < rep * D; i += NT) qs[i] = __ldcg(base + g * rep * D + i);
     for (int i = t; i < D; i += NT) {
@@ -598,14 +622,16 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32
       }
       cbar();
     }
-    const float2* rt = P.rope + (size_t)e.pos * (D / 2);
-    for (int i = t; i < (rep + 1) * (D / 2); i += NT) {
-      const int h = i / (D / 2), k = i % (D / 2);
-      float* u = h < rep ? qs + h * D : kn;
-      const float2 cs = __ldg(rt + k);
-      const float u1 = u[k], u2 = u[k + D / 2];
-      u[k] = u1 * cs.x - u2 * cs.y;
-      u[k + D / 2] = u2 * cs.x + u1 * cs.y;
+#pragma unroll
+    for (int j = 0; j < NROT; ++j) {
+      const int i = t + j * NT;
+      if (i < (rep + 1) * (D / 2)) {
+        const int h = i / (D / 2), k = i % (D / 2);
+        float* u = h < rep ? qs + h * D : kn;
+        const float u1 = u[k], u2 = u[k + D / 2];
+        u[k] = u1 * cs[j].x - u2 * cs[j].y;
+        u[k + D / 2] = u2 * cs[j].x + u1 * cs[j].y;
+      }
     }
     cbar();
     if (e.has_new)
@@ -730,20 +756,47 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32
   cbar();
   if (S.flags[F_LAST]) {
     if (e.live) {
+      // Combine the NS splits in split order: weights f_s = exp(m_s - max_s m_s)
+      // per head (staged in shared memory), o = sum_s f_s o_s / sum_s f_s l_s.
       const float* gp = P.part + (((size_t)l * P.max_batch + b) * P.nkv + g) * NS * rep * (D + 2);
+      float* fw = S.xbuf;                 // [NS][rep] weights
+      float* lw = S.xbuf + NS * rep;      // [NS][rep] partial sums
+      float* linv = lw + NS * rep;        // [rep]
+      for (int i = t; i < NS * rep; i += NT) {
+        const float* ps = gp + (size_t)i * (D + 2);
+        fw[i] = __ldcg(ps + D);
+        lw[i] = __ldcg(ps + D + 1);
+      }
+      cbar();
+      if (w < rep) {
+        float M = -INFINITY;
+        for (int s = lane; s < NS; s += 32) M = fmaxf(M, fw[s * rep + w]);
+        M = warp_max(M);
+        float Ls = 0.f;
+        for (int s = lane; s < NS; s += 32) {
+          const float ms = fw[s * rep + w];
+          const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+          fw[s * rep + w] = f;
+          Ls = fmaf(lw[s * rep + w], f, Ls);
+        }
+        Ls = warp_sum(Ls);
+        if (lane == 0) linv[w] = 1.0f / Ls;
+      }
+      cbar();
       for (int i = t; i < rep * D; i += NT) {
         const int h = i / D, c = i % D;
-        float M = -INFINITY;
-        for (int s = 0; s < NS; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
-        float Ls = 0.f, O = 0.f;
-        for (int s = 0; s < NS; ++s) {
-          const float* ps = gp + ((size_t)s * rep + h) * (D + 2);
-          const float ms = __ldcg(ps + D);
-          const float f = ms == -INFINITY ? 0.f : expf(ms - M);
-          Ls = fmaf(__ldcg(ps + D + 1), f, Ls);
-          O = fmaf(__ldcg(ps + c), f, O);
+        const float* pc = gp + (size_t)h * (D + 2) + c;
+        float O = 0.f;
+        int s = 0;
+        for (; s + 8 <= NS; s += 8) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = __ldcg(pc + (size_t)(s + u) * rep * (D + 2));
+#pragma unroll
+          for (int u = 0; u < 8; ++u) O = fmaf(v[u], fw[(s + u) * rep + h], O);
         }
-        P.attn_out[((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c] = O / Ls;
+        for (; s < NS; ++s) O = fmaf(__ldcg(pc + (size_t)s * rep * (D + 2)), fw[s * rep + h], O);
+        P.attn_out[((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c] = O * linv[h];
       }
     }
     cbar();
@@ -819,8 +872,10 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     const uint64_t t_begin = P.trace ? globaltimer() : 0;
 
     // wait on the tiles this instruction reads
+    // (the abort word is read only while spinning: a launch that never waits
+    // on an unsatisfied counter runs to completion anyway)
     if (t == 0) {
-      uint32_t aborted = ld_volatile(&P.ctl[CTL_ABORT]) != 0u;
+      uint32_t aborted = S.flags[F_STOP];
       if (!aborted && P.mode == MODE_MEGA && in.wait_bar != NO_BAR) {
         const uint32_t target = (gen + 1u) * in.wait_target;
         if (!(in.wait_n == 1 && in.wait_bar == ok_bar && target == ok_target)) {
@@ -846,6 +901,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
         }
       }
       S.flags[F_ABORT] = aborted;
+      if (aborted) S.flags[F_STOP] = 1u;  // the producer stops popping
     }
     cbar();
     const uint64_t t_ready = P.trace ? globaltimer() : 0;
@@ -893,7 +949,8 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       tr[2] = t_ready;
       tr[3] = globaltimer();
     }
-    cbar();
+    // no barrier here: the next instruction's slot and dependency barriers
+    // order every reuse of the shared scratch
   }
 }
 
@@ -914,6 +971,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
     fence_mbar_init();
     fence_proxy_async_smem();
     S.flags[F_GEN] = P.mode == MODE_MEGA ? ld_volatile(&P.ctl[CTL_GEN]) : 0u;
+    S.flags[F_STOP] = 0u;
+  }
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(P.layers);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(smem + SmemLayout::layers);
+    const int words = P.L * (int)(sizeof(LayerW) / 4);
+    for (int i = t; i < words; i += NTHREADS) dst[i] = src[i];
   }
   __syncthreads();
   if (t >= NT) producer(P, S);

@@ -89,6 +89,7 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
   if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f))
     return bad(MK_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_theta > 0");
   if (max_batch < 1 || max_ctx < 1) return bad(MK_ERR_INVALID_ARG, "max_batch, max_ctx >= 1");
+  if (c.n_layers > MAX_LAYERS) return bad(MK_ERR_UNSUPPORTED, "more layers than the kernel holds");
   if (c.head_dim != 64 && c.head_dim != 128)
     return bad(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   const int rep = c.n_q_heads / c.n_kv_heads;
@@ -121,10 +122,12 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
   hp.fast_b1 = fast;
 
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
-  hp.r_qkv = std::min(rows_for(64 << 10, (long)H * 2, RMAX), d);
-  hp.r_o = rows_for(64 << 10, (long)qd * 2, RMAX);
-  hp.r_gu = rows_for(128 << 10, (long)H * 4, RMAX / 2);
-  hp.r_down = rows_for(128 << 10, (long)F * 2, RMAX);
+  // Rows per tile: ~128-256 KB of weights per instruction amortises the
+  // per-instruction handshakes; QKV tiles stay inside one head.
+  hp.r_qkv = std::min(rows_for(128 << 10, (long)H * 2, RMAX), d);
+  hp.r_o = rows_for(128 << 10, (long)qd * 2, RMAX);
+  hp.r_gu = rows_for(256 << 10, (long)H * 4, RMAX / 2);
+  hp.r_down = rows_for(256 << 10, (long)F * 2, RMAX);
   hp.r_lm = rows_for(256 << 10, (long)H * 2, RMAX);
   hp.n_qkv_tiles = hp.qkv_rows / hp.r_qkv;
   hp.n_o_tiles = ceil_div(H, hp.r_o);
@@ -140,7 +143,8 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
   ns = std::min(ns, (int)std::max<uint32_t>(ceil_div(max_ctx, 32), ceil_div(max_ctx, hp.split_max)));
   ns = std::max(ns, 1);
   hp.n_splits = ns;
-  if (hp.n_splits > 0xffff) return bad(MK_ERR_UNSUPPORTED, "too many splits");
+  if (hp.n_splits > 0xffff || 2L * hp.n_splits * rep + rep > XBUF_FLOATS)
+    return bad(MK_ERR_UNSUPPORTED, "too many split-KV partitions for the combine buffer");
 
   // Barrier tensor layout.
   BarLayout& bl = hp.bl;

@@ -19,7 +19,8 @@ constexpr int NTHREADS = NT + 32;     // + one producer warp
 constexpr int NSTAGE = 6;             // weight/KV ring stages
 constexpr int STAGE_BYTES = 32768;    // bytes per ring stage
 constexpr int NISLOT = 8;             // instruction slots between producer and consumers
-constexpr int RMAX = 16;              // GEMV rows per tile (both matrices of a gate/up tile)
+constexpr int RMAX = 32;              // GEMV rows per tile (both matrices of a gate/up tile)
+constexpr int MAX_LAYERS = 64;        // layer pointer table kept in shared memory
 constexpr int BMAX_CC = 8;            // CUDA-core GEMV batch limit
 constexpr int XBUF_BYTES = 24576;     // activation / attention scratch in shared memory
 constexpr int XBUF_FLOATS = XBUF_BYTES / 4;
