@@ -114,6 +114,38 @@ int mk_decode_step(mk_plan *plan, const int32_t *tokens, const int32_t *position
 int mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const int32_t *positions_host,
                         int batch, void *kv_cache, float *logits_host, void *stream);
 
+/* Device memory that mk_decode_step_noalloc may use: a file-scope array of
+ * this many bytes is part of the library image, so every GPU that loads libmk
+ * holds it until the process exits. */
+#define MK_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* A decode step for callers that must not allocate device memory when they
+ * run it -- for example a serving process that handed (nearly) all device
+ * memory to its own pool and KV cache at start-up, or code running under an
+ * external memory manager that forbids new device allocations.  The paper has
+ * no counterpart: it is the persistent launch of mk_decode_step without a plan
+ * object.  The caller passes what mk_plan_create and mk_decode_step take (the
+ * model shape, the weights, the cache geometry max_batch x max_ctx, then the
+ * step's tokens, positions, KV cache and logits, same layouts).  Activations,
+ * barrier counters, the instruction queue and the RoPE table go into the
+ * static array above; nothing here calls cudaMalloc, cudaFree or any other
+ * device allocator (the queue is built in ordinary host memory and copied in).
+ *  - Shapes whose scratch exceeds MK_NOALLOC_SCRATCH_BYTES return
+ *    MK_ERR_UNSUPPORTED before any device work.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address and sets the kernel's shared-memory limit; make
+ *    that first call before any stream capture.
+ *  - All calls share the one array and find the previous call's contents;
+ *    each call clears its own counters and control words.  Calls whose work
+ *    overlaps on the GPU (several streams or threads) race on the array:
+ *    serialise them.
+ *  - Device-side errors (an out-of-range token or position) are not reported
+ *    here; the logits are then undefined.
+ * Returns MK_OK once the step is queued on `stream`. */
+int mk_decode_step_noalloc(const mk_model_cfg *cfg, const mk_weight_ptrs *w, int max_batch,
+                           int max_ctx, const int32_t *tokens, const int32_t *positions, int batch,
+                           void *kv_cache, float *logits, void *stream);
+
 /* Prefill one prompt of `len` tokens (1..max_ctx) into sequence slot 0 of the
  * cache at positions 0..len-1, causal; writes the last token's logits
  * (device float [vocab]). */

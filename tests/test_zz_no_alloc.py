@@ -1,0 +1,73 @@
+"""mk_decode_step_noalloc: the decode step for callers that cannot allocate
+device memory when they run it (their device memory is already owned by their
+own pool or by an external memory manager).  Its scratch is the library's
+static device array, so it is checked against the plan-based entry point,
+mk_decode_step, on the same inputs: logits per row within
+2e-2 * RMS(reference row), the tolerance of the other decode tests, on two
+calls in a row (the second finds the first call's leftovers in the array).
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+from tile_level_overlap_gb300 import build, mk, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    mk.lib()
+
+
+def _close(got, ref):
+    for b in range(ref.shape[0]):
+        rms = np.sqrt((ref[b] ** 2).mean())
+        assert np.abs(got[b] - ref[b]).max() <= TOL * rms
+
+
+@pytest.mark.parametrize("cfg,max_batch,max_ctx,positions", [
+    (synth.TOY_1L, 4, 129, [128, 0, 77]),
+    (synth.LLAMA32_1B, 1, 1025, [1024]),
+])
+def test_noalloc_matches_plan_entry_point(cfg, max_batch, max_ctx, positions):
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(cfg, device=dev)
+    kv = synth.make_kv_cache(cfg, max_batch, max_ctx, device=dev)
+    B = len(positions)
+    tokens = synth.make_tokens(B, cfg.vocab).to(dev)
+    pos = torch.tensor(positions, dtype=torch.int32, device=dev)
+    plan = mk.Plan(cfg, w, max_batch, max_ctx)
+    ref = torch.empty((B, cfg.vocab), device=dev)
+    plan.decode_step(tokens, pos, kv, ref)
+    assert plan.status() == mk.MK_OK
+    ref = ref.cpu().numpy()
+    plan.close()
+    for _ in range(2):
+        got = torch.full((B, cfg.vocab), float("nan"), device=dev)
+        rc = mk.decode_step_noalloc(cfg, w, max_batch, max_ctx, tokens, pos, kv, got)
+        assert rc == mk.MK_OK
+        torch.cuda.synchronize()
+        _close(got.cpu().numpy(), ref)
+    del w, kv
+    torch.cuda.empty_cache()
+
+
+def test_noalloc_rejects_shapes_beyond_its_static_scratch():
+    # The 32-layer 8B shape at a 4097-token cache needs more scratch than the
+    # static array holds; the call is refused before any device work, so every
+    # weight pointer may alias one small tensor.
+    cfg = synth.LLAMA3_8B
+    dev = torch.device("cuda:0")
+    x = torch.zeros(64, dtype=torch.bfloat16, device=dev)
+    w = {name: x for name in synth.weight_shapes(cfg)}
+    t = torch.zeros(1, dtype=torch.int32, device=dev)
+    logits = torch.empty((1, 8), device=dev)
+    assert mk.decode_step_noalloc(cfg, w, 1, 4097, t, t, x, logits) == mk.MK_ERR_UNSUPPORTED

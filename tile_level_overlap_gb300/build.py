@@ -14,7 +14,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmk.so")
 
 SOURCES = ["mk_plan.cpp", "mk_capi.cu", "mk_k_generic.cu", "mk_k_h1_f4_d64_r4.cu",
-           "mk_k_h2_f7_d128_r4.cu", "mk_k_h2_f6_d128_r4.cu", "mk_gemm.cu"]
+           "mk_k_h2_f7_d128_r4.cu", "mk_k_h2_f6_d128_r4.cu", "mk_gemm.cu", "mk_noalloc.cu"]
 HEADERS = ["mk_internal.h", "mk_plan.h", "mk_device.cuh", "mk_kernel.cuh", "mk_variants.h",
            "mk_tc.cuh", "mk_tmap.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,183 @@
+// mk_decode_step_noalloc: one decode step that never allocates device memory.
+//
+// Who needs it: callers that cannot call cudaMalloc at the moment they run a
+// step -- e.g. a serving process that hands (nearly) all device memory to its
+// own pool and KV cache up front, or code running under an external memory
+// manager that forbids new device allocations.  They still own and pass the
+// weights, the KV cache, tokens, positions and logits; everything else the
+// step needs (activations, split-KV partials, barrier counters, the
+// instruction queue, the RoPE table) lives in one file-scope device array of
+// fixed size that the library image carries.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+#include "mk_plan.h"
+#include "mk_variants.h"
+
+namespace mk {
+namespace {
+
+// The static scratch.  Every GPU that loads this library holds it until the
+// process exits.  Every call shares it and finds the previous call's contents.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MK_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+uint8_t* g_scratch_addr[kMaxDevices] = {nullptr};  // device address of the array, per device
+
+struct Take {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  }
+};
+
+KernelVariant variant_for(const HostPlan& hp) {
+  const mk_model_cfg& c = hp.cfg;
+  if (hp.fast_b1) {
+    const KernelVariant cands[] = {variant_h1_f4_d64_r4(), variant_h2_f7_d128_r4(),
+                                   variant_h2_f6_d128_r4()};
+    for (const KernelVariant& v : cands)
+      if (v.mh * FAST_K_UNIT == c.hidden && v.mf * FAST_K_UNIT == c.ffn && v.ad == c.head_dim &&
+          v.arep == hp.rep)
+        return v;
+  }
+  return variant_generic();
+}
+
+bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
+                                      int max_batch, int max_ctx, const int32_t* tokens,
+                                      const int32_t* positions, int batch, void* kv_cache,
+                                      float* logits, void* stream) {
+  if (!cfg || !w || !tokens || !positions || !kv_cache || !logits) return MK_ERR_INVALID_ARG;
+  if (batch < 1 || batch > max_batch || !al16(kv_cache)) return MK_ERR_INVALID_ARG;
+  HostPlan hp;
+  std::string why;
+  int rc = build_plan(*cfg, max_batch, max_ctx, &hp, &why);
+  if (rc != MK_OK) return rc;
+  const mk_model_cfg& c = hp.cfg;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
+  std::vector<LayerW> lw(L);
+  bool good = al16(w->embed) && al16(w->final_norm) && (c.tied_embeddings || al16(w->lm_head)) &&
+              w->attn_norm && w->wq && w->wk && w->wv && w->wo && w->ffn_norm && w->w_gate &&
+              w->w_up && w->w_down && (!c.qk_norm || (w->q_norm && w->k_norm));
+  for (int l = 0; good && l < L; ++l) {
+    LayerW& x = lw[l];
+    x.attn_norm = (const uint16_t*)w->attn_norm[l];
+    x.wq = (const uint16_t*)w->wq[l];
+    x.wk = (const uint16_t*)w->wk[l];
+    x.wv = (const uint16_t*)w->wv[l];
+    x.wo = (const uint16_t*)w->wo[l];
+    x.q_norm = c.qk_norm ? (const uint16_t*)w->q_norm[l] : nullptr;
+    x.k_norm = c.qk_norm ? (const uint16_t*)w->k_norm[l] : nullptr;
+    x.ffn_norm = (const uint16_t*)w->ffn_norm[l];
+    x.wg = (const uint16_t*)w->w_gate[l];
+    x.wu = (const uint16_t*)w->w_up[l];
+    x.wd = (const uint16_t*)w->w_down[l];
+    good = al16(x.attn_norm) && al16(x.wq) && al16(x.wk) && al16(x.wv) && al16(x.wo) &&
+           al16(x.ffn_norm) && al16(x.wg) && al16(x.wu) && al16(x.wd) &&
+           (!c.qk_norm || (al16(x.q_norm) && al16(x.k_norm)));
+  }
+  if (!good) return MK_ERR_INVALID_ARG;
+
+  // Carve the static array: the same buffers a plan allocates, one queue copy.
+  const size_t B = (size_t)max_batch;
+  Take t;
+  const size_t o_resid = t.take(sizeof(float) * (2 * L + 1) * B * H);
+  const size_t o_qkv = t.take(sizeof(float) * L * B * hp.qkv_rows);
+  const size_t o_part = t.take(sizeof(float) * L * B * nkv * hp.n_splits * hp.rep * (d + 2));
+  const size_t o_attn = t.take(sizeof(float) * L * B * c.n_q_heads * d);
+  const size_t o_act = t.take(sizeof(float) * L * B * F);
+  const size_t o_zero = t.off;  // everything from here to o_zero_end starts at zero
+  const size_t o_bars = t.take(sizeof(uint32_t) * hp.bl.total);
+  const size_t o_arr = t.take(sizeof(uint32_t) * L * B * nkv);
+  const size_t o_ctl = t.take(sizeof(uint32_t) * CTL_WORDS);
+  const size_t o_zero_end = t.off;
+  const size_t o_q = t.take(sizeof(Instr) * hp.decode.size());
+  const size_t o_expr = t.take(sizeof(uint32_t) * hp.expr.size());
+  const size_t o_rope = t.take(sizeof(float2) * (size_t)max_ctx * (d / 2));
+  const size_t o_lw = t.take(sizeof(LayerW) * L);
+  if (t.off > (size_t)MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_UNSUPPORTED;
+
+  // Per-device set-up on the first call with that device current: the array's
+  // device address and the kernel's shared-memory attribute.
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MK_ERR_CUDA;
+  const KernelVariant kv = variant_for(hp);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return MK_ERR_CUDA;
+    g_scratch_addr[dev] = (uint8_t*)ptr;
+  }
+  if (kv.setup() != cudaSuccess) return MK_ERR_CUDA;
+  int nsm = 0;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MK_ERR_CUDA;
+  uint8_t* s = g_scratch_addr[dev];
+  cudaStream_t st = (cudaStream_t)stream;
+
+  std::vector<float2> rope((size_t)max_ctx * (d / 2));
+  for (int pos = 0; pos < max_ctx; ++pos)
+    for (int i = 0; i < d / 2; ++i) {
+      const double a = (double)pos * std::pow((double)c.rope_theta, -2.0 * i / d);
+      rope[(size_t)pos * (d / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  // Copies from pageable host memory return once the source has been read.
+  if (cudaMemcpyAsync(s + o_q, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(s + o_expr, hp.expr.data(), sizeof(uint32_t) * hp.expr.size(),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(s + o_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaMemsetAsync(s + o_zero, 0, o_zero_end - o_zero, st) != cudaSuccess)
+    return MK_ERR_CUDA;
+
+  KParams k;
+  std::memset(&k, 0, sizeof(k));
+  k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = nkv; k.d = d; k.F = F; k.V = c.vocab;
+  k.qk_norm = c.qk_norm; k.rep = hp.rep; k.qkv_rows = hp.qkv_rows; k.eps = c.rms_eps;
+  k.max_batch = max_batch; k.max_ctx = max_ctx; k.n_splits = hp.n_splits;
+  k.r_qkv = hp.r_qkv; k.r_o = hp.r_o; k.r_gu = hp.r_gu; k.r_down = hp.r_down; k.r_lm = hp.r_lm;
+  k.n_qkv_tiles = hp.n_qkv_tiles; k.n_o_tiles = hp.n_o_tiles; k.n_gu_tiles = hp.n_gu_tiles;
+  k.n_down_tiles = hp.n_down_tiles; k.n_lm_tiles = hp.n_lm_tiles;
+  k.embed = (const uint16_t*)w->embed;
+  k.lm = (const uint16_t*)(c.tied_embeddings ? w->embed : w->lm_head);
+  k.final_norm = (const uint16_t*)w->final_norm;
+  k.layers = (const LayerW*)(s + o_lw);
+  k.resid = (float*)(s + o_resid);
+  k.qkv = (float*)(s + o_qkv);
+  k.part = (float*)(s + o_part);
+  k.attn_out = (float*)(s + o_attn);
+  k.act = (float*)(s + o_act);
+  k.bars = (uint32_t*)(s + o_bars);
+  k.arrive = (uint32_t*)(s + o_arr);
+  k.rope = (const float2*)(s + o_rope);
+  k.ctl = (uint32_t*)(s + o_ctl);
+  k.queue = (const Instr*)(s + o_q);
+  k.n_instr = (uint32_t)hp.decode.size();
+  k.expr = (const uint32_t*)(s + o_expr);
+  k.bl = hp.bl;
+  k.tokens = tokens;
+  k.positions = positions;
+  k.B = batch;
+  k.kv = (uint16_t*)kv_cache;
+  k.logits = logits;
+  k.mode = MODE_MEGA;
+  k.wait_limit_ns = 2000000000ull;
+  return kv.mega(k, nsm, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}

@@ -28,7 +28,7 @@ EXPORTED = [
     "mk_plan_create", "mk_plan_destroy", "mk_kv_cache_bytes", "mk_decode_step",
     "mk_decode_step_host", "mk_prefill", "mk_run_per_op", "mk_status", "mk_plan_reset",
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
-    "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16",
+    "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
 ]
 
 
@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
     L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs),
+                                         ctypes.c_int, ctypes.c_int, i32p, i32p, ctypes.c_int, vp,
+                                         f32p, vp]
     _lib = L
     return L
 
@@ -115,6 +118,36 @@ def plan_check(cfg, max_batch: int, max_ctx: int, seed: int = 0):
     st = mk_plan_stats()
     rc = lib().mk_plan_check(ctypes.byref(model_cfg(cfg)), max_batch, max_ctx, seed, ctypes.byref(st))
     return rc, st
+
+
+def weight_ptrs(cfg, weights):
+    """mk_weight_ptrs over name -> torch bf16 CUDA tensor; returns (struct,
+    keep-alive list of the pointer arrays it references)."""
+    n = cfg.n_layers
+    keep = []
+    wp = mk_weight_ptrs()
+    wp.embed = _ptr(weights["embed"])
+    wp.final_norm = _ptr(weights["final_norm"])
+    wp.lm_head = _ptr(weights["lm_head"]) if "lm_head" in weights else None
+    for k in ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "ffn_norm", "w_gate", "w_up",
+              "w_down"):
+        if all(f"layers.{l}.{k}" in weights for l in range(n)):
+            a = (ctypes.c_void_p * n)(*[_ptr(weights[f"layers.{l}.{k}"]) for l in range(n)])
+            keep.append(a)
+            setattr(wp, k, ctypes.cast(a, _PP))
+    return wp, keep
+
+
+def decode_step_noalloc(cfg, weights, max_batch: int, max_ctx: int, tokens, positions, kv, logits,
+                        stream=None) -> int:
+    """mk_decode_step_noalloc: one decode step using only the library's static
+    device scratch (no device allocation).  Returns the C status code."""
+    wp, keep = weight_ptrs(cfg, weights)
+    rc = lib().mk_decode_step_noalloc(ctypes.byref(model_cfg(cfg)), ctypes.byref(wp), max_batch,
+                                      max_ctx, _ptr(tokens), _ptr(positions), int(tokens.numel()),
+                                      _ptr(kv), _ptr(logits), _stream_ptr(stream))
+    del keep
+    return rc
 
 
 def _stream_ptr(stream) -> int:
