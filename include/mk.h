@@ -206,16 +206,21 @@ int mk_plan_debug_drop_release(mk_plan *plan, uint32_t index);
 
 /* Test-only: the tensor-core tile routine (tcgen05.mma with TMEM accumulators,
  * TMA-fed 128-byte-swizzled operands) on one plain GEMM, synchronous:
- *   C[M][N] (device f32) = A[M][K] (device bf16) * B[N][K]^T (device bf16),
- * row-major, 16-byte aligned; N % 128 == 0, K % 64 == 0.  This is the
+ *   C[M][N] (device f32) = A[M][K] (device bf16) * B^T (device bf16),
+ * row-major, 16-byte aligned; N % 128 == 0, K % 64 == 0.  b_layout 0: B is
+ * [N][K] (K contiguous, as weights are stored); b_layout 1: B is [K][N] (N
+ * contiguous, as the V cache is read by prefill attention).  This is the
  * contraction the batched-decode and prefill projections run ("MegaOps",
  * Abstract: the dense Llama3/Qwen3 projections).  Returns MK_OK, an argument
  * error, or MK_ERR_TIMEOUT if a bounded wait inside the kernel gave up. */
-int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int K, void *stream);
+int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int K, int b_layout,
+                       void *stream);
 
 /* Copy the trace of the last traced launch: records of
- * {uint32 smid, uint32 op | layer << 8, uint64 t_begin, uint64 t_ready, uint64 t_done}
- * (%globaltimer ns), one per instruction in pop order.  *n_records receives the
+ * 8 x uint64: {smid | (op | layer << 8) << 32, consumer took it, its waits were
+ * satisfied, done, producer posted it, ns spent waiting for operand stages,
+ * first operand stage ready, unused} (%globaltimer ns), 64 bytes per
+ * instruction, indexed by queue position.  *n_records receives the
  * count copied.  Waits for the device. */
 int mk_trace_copy(mk_plan *plan, void *host_buf, size_t bytes, size_t *n_records);
 

@@ -430,8 +430,8 @@ int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int 
   int rc = upload_mk_queue(p, queue_perm_seed);
   if (rc != MK_OK) return rc;
   if (trace && !p->d_trace) {
-    if (cudaMalloc(&p->d_trace, p->hp.decode.size() * 32) != cudaSuccess) return MK_ERR_CUDA;
-    MK_CUDA(cudaMemset(p->d_trace, 0, p->hp.decode.size() * 32));
+    if (cudaMalloc(&p->d_trace, p->hp.decode.size() * TRACE_WORDS * 8) != cudaSuccess) return MK_ERR_CUDA;
+    MK_CUDA(cudaMemset(p->d_trace, 0, p->hp.decode.size() * TRACE_WORDS * 8));
   }
   p->trace = trace ? 1 : 0;
   return MK_OK;
@@ -454,8 +454,8 @@ int mk_trace_copy(mk_plan* p, void* host_buf, size_t bytes, size_t* n_records) {
   if (!p->d_trace) return MK_ERR_INVALID_ARG;
   MK_CUDA(cudaDeviceSynchronize());
   size_t n = p->hp.decode.size();
-  if (bytes / 32 < n) n = bytes / 32;
-  MK_CUDA(cudaMemcpy(host_buf, p->d_trace, n * 32, cudaMemcpyDeviceToHost));
+  if (bytes / (TRACE_WORDS * 8) < n) n = bytes / (TRACE_WORDS * 8);
+  MK_CUDA(cudaMemcpy(host_buf, p->d_trace, n * TRACE_WORDS * 8, cudaMemcpyDeviceToHost));
   *n_records = n;
   return MK_OK;
 }

@@ -40,7 +40,9 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
   return true;
 }
 
-template <int BN>
+// BT: B stored [K][N] (N contiguous, the MN-major operand form), loaded as
+// BN/64 boxes of 64 N-columns x 64 K-rows placed 8 KB apart.
+template <int BN, bool BT>
 __global__ void __launch_bounds__(G_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                    float* __restrict__ C, int M, int N, int K, uint32_t* err) {
@@ -76,10 +78,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       uint8_t* st = smem + s * L::stage;
       mbar_arrive_expect_tx(&full[s], L::stage);
       tma_load_2d(st, &ta, kb * G_BK, m0, &full[s], pol);
-      tma_load_2d(st + L::a_bytes, &tb, kb * G_BK, n0, &full[s], pol);
+      if constexpr (BT) {
+#pragma unroll
+        for (int i = 0; i < BN / 64; ++i)
+          tma_load_2d(st + L::a_bytes + i * 8192, &tb, n0 + 64 * i, kb * G_BK, &full[s], pol);
+      } else {
+        tma_load_2d(st + L::a_bytes, &tb, kb * G_BK, n0, &full[s], pol);
+      }
     }
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = idesc_bf16_f32(G_BM, BN);
+    constexpr uint32_t idesc = idesc_bf16_f32(G_BM, BN, BT);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % G_STAGES;
       wait_bounded(&full[s], (kb / G_STAGES) & 1, err);
@@ -87,8 +95,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const uint32_t a0 = smem_u32(smem + s * L::stage);
       const uint32_t b0 = a0 + L::a_bytes;
 #pragma unroll
-      for (int k = 0; k < G_BK / 16; ++k)
-        tc_mma(tbase, sdesc_sw128(a0 + 32 * k), sdesc_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+      for (int k = 0; k < G_BK / 16; ++k) {
+        const uint64_t bd = BT ? sdesc_sw128_mn(b0 + 2048 * k, 8192) : sdesc_sw128(b0 + 32 * k);
+        tc_mma(tbase, sdesc_sw128(a0 + 32 * k), bd, idesc, (kb | k) != 0);
+      }
       tc_commit(&empty[s]);
     }
     tc_commit(done);
@@ -116,23 +126,23 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   }
 }
 
-template <int BN>
+template <int BN, bool BT>
 int run_gemm(const void* A, const void* B, float* C, int M, int N, int K, cudaStream_t st) {
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, G_BM) ||
-      !make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN))
-    return MK_ERR_CUDA;
+  const bool okb = BT ? make_tmap_bf16(&tb, B, (uint64_t)K, (uint64_t)N, 64)
+                      : make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, BN);
+  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, G_BM) || !okb) return MK_ERR_CUDA;
   static uint32_t* err = nullptr;
   if (!err) {
     if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return MK_ERR_CUDA;
   }
   if (cudaMemsetAsync(err, 0, sizeof(uint32_t), st) != cudaSuccess) return MK_ERR_CUDA;
   using L = GemmSmem<BN>;
-  if (cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(tc_gemm_kernel<BN, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::total) != cudaSuccess)
     return MK_ERR_CUDA;
   dim3 grid(N / BN, (M + G_BM - 1) / G_BM);
-  tc_gemm_kernel<BN><<<grid, G_THREADS, L::total, st>>>(ta, tb, C, M, N, K, err);
+  tc_gemm_kernel<BN, BT><<<grid, G_THREADS, L::total, st>>>(ta, tb, C, M, N, K, err);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_CUDA;
   uint32_t e = 0;
   if (cudaMemcpyAsync(&e, err, sizeof(e), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -145,10 +155,14 @@ int run_gemm(const void* A, const void* B, float* C, int M, int N, int K, cudaSt
 }  // namespace mk
 
 extern "C" int mk_debug_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K,
-                                  void* stream) {
+                                  int b_layout, void* stream) {
   if (!A || !B || !C || M < 1 || N < 128 || K < 64 || N % 128 || K % 64) return MK_ERR_INVALID_ARG;
   if (((uintptr_t)A | (uintptr_t)B | (uintptr_t)C) & 15u) return MK_ERR_INVALID_ARG;
+  if (b_layout != 0 && b_layout != 1) return MK_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  if (N % 256 == 0) return mk::run_gemm<256>(A, B, C, M, N, K, st);
-  return mk::run_gemm<128>(A, B, C, M, N, K, st);
+  if (b_layout == 1)
+    return N % 256 == 0 ? mk::run_gemm<256, true>(A, B, C, M, N, K, st)
+                        : mk::run_gemm<128, true>(A, B, C, M, N, K, st);
+  return N % 256 == 0 ? mk::run_gemm<256, false>(A, B, C, M, N, K, st)
+                      : mk::run_gemm<128, false>(A, B, C, M, N, K, st);
 }

@@ -266,6 +266,7 @@ __device__ void producer(const KParams& P, const Sh& S) {
     if (!posted_end) *slot_instr(S, si) = Ia;
     *slot_index(S, si) = posted_end ? END_SLOT : ia;
     mbar_arrive(&S.ifull[si]);
+    if (P.trace && !posted_end) P.trace[(size_t)ia * TRACE_WORDS + 4] = globaltimer();
     ++islot_ctr;
     if (posted_end) break;
 
@@ -298,12 +299,22 @@ __device__ void producer(const KParams& P, const Sh& S) {
 
 // ---------------------------------------------------------------- consumer helpers
 struct Ring {
-  uint32_t ctr;  // stages consumed so far
+  uint32_t ctr;           // stages consumed so far
+  uint64_t wait_ns;       // (tracing, thread 0) time spent waiting for stages
+  uint64_t first_ns;      // (tracing, thread 0) when the instruction's first stage was ready
 };
 
 __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
   const int st = R.ctr % NSTAGE;
-  mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
+  if (P.trace && threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer();
+    mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
+    const uint64_t t1 = globaltimer();
+    R.wait_ns += t1 - t0;
+    if (!R.first_ns) R.first_ns = t1;
+  } else {
+    mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
+  }
   return S.ring + (size_t)st * STAGE_BYTES;
 }
 __device__ __forceinline__ void ring_release(const Sh& S, Ring& R) {
@@ -374,10 +385,12 @@ __device__ __forceinline__ void load_x8(const KParams& P, const float* xs, const
 
 // ---------------------------------------------------------------- GEMV, batch 1, K = M * 8 * NT
 // Thread t owns columns 8*(t + NT*j) .. +8 for j < M and keeps them (normed)
-// in registers; every row of the tile adds into acc[row]; one multi-value warp
-// reduction and a fixed-order sum over warps per tile.
+// in registers; each ring stage holds RPS = 8 / M whole rows, whose per-thread
+// partial dot products are summed across the warp (multi-value butterfly) into
+// a per-warp row slot; one fixed-order sum over warps per tile.
 template <int M>
-__device__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in, float (&xr)[M][8]) {
+__device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in,
+                                            float (&xr)[M][8]) {
   const int t = threadIdx.x;
   const int K = M * FAST_K_UNIT;
   const float* xs = gemv_x(P, in);
@@ -409,44 +422,46 @@ __device__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in, floa
 }
 
 template <int M>
-__device__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
-                          const Src& src, Ring& R, const float (&xr)[M][8]) {
+__device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in,
+                                          const GemvDesc& g, const Src& src, Ring& R,
+                                          const float (&xr)[M][8]) {
+  // rows per 32 KB stage at K = M * 2048 (the plan's src.rps for these K)
+  constexpr int RPS = (8 / M) > 0 ? (8 / M) : 1;
+  constexpr int kDup = 32 / RPS;  // lanes holding the same total after the butterfly
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int K = g.K;
-  float acc[RMAX];
-#pragma unroll
-  for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-
   const int rows0 = (int)src.rows[0];
   const int ntot = src.nreg == 2 ? 2 * rows0 : rows0;
-  const int rps = (int)src.rps;
-  const int stages0 = (rows0 + rps - 1) / rps;
-  int cur = -1;
-  const uint8_t* stage = nullptr;
+  int tile_row = 0;
+#pragma unroll 1
+  for (int r = 0; r < src.nreg; ++r) {
+#pragma unroll 1
+    for (int row = 0; row < rows0; row += RPS) {
+      const int n = rows0 - row < RPS ? rows0 - row : RPS;
+      const uint8_t* stage = ring_acquire(P, S, R);
+      float acc[RPS];
 #pragma unroll
-  for (int r = 0; r < RMAX; ++r) {
-    if (r < ntot) {
-      const int reg = r < rows0 ? 0 : 1;
-      const int rr = reg ? r - rows0 : r;
-      const int st = reg * stages0 + rr / rps;
-      if (st != cur) {
-        if (cur >= 0) ring_release(S, R);
-        stage = ring_acquire(P, S, R);
-        cur = st;
+      for (int i = 0; i < RPS; ++i) {
+        float a = 0.f;
+        if (i < n) {
+          const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)i * K * 2);
+#pragma unroll
+          for (int j = 0; j < M; ++j) a = dot8(wrow[t + NT * j], xr[j], a);
+        }
+        acc[i] = a;
       }
-      const uint4* row = reinterpret_cast<const uint4*>(stage + (size_t)(rr % rps) * K * 2);
-      float a = 0.f;
-#pragma unroll
-      for (int j = 0; j < M; ++j) a = dot8(row[t + NT * j], xr[j], a);
-      acc[r] = a;
+      ring_release(S, R);
+      if constexpr (RPS == 1) {
+        const float v = warp_sum(acc[0]);
+        if (lane == 0) S.redw[w * RMAX + tile_row] = v;
+      } else {
+        const float v = warp_reduce_multi<RPS>(acc, lane);
+        const int idx = warp_multi_index<RPS>(lane);
+        if ((lane & (kDup - 1)) == 0 && idx < n) S.redw[w * RMAX + tile_row + idx] = v;
+      }
+      tile_row += n;
     }
   }
-  if (cur >= 0) ring_release(S, R);
-
-  const float v = warp_reduce_multi<RMAX>(acc, lane);
-  // after the butterfly, each group of 32 / RMAX consecutive lanes holds one total
-  constexpr int kDup = 32 / RMAX;
-  if ((lane & (kDup - 1)) == 0) S.redw[w * RMAX + warp_multi_index<RMAX>(lane)] = v;
   cbar();
   if (t < ntot) {
     float s = 0.f;
@@ -841,7 +856,7 @@ __device__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
 template <int MH, int MF, int AD, int AREP>
 __device__ void consumer(const KParams& P, const Sh& S) {
   const int t = threadIdx.x;
-  Ring R{0};
+  Ring R{0, 0, 0};
   uint32_t islot_ctr = 0;
   const uint32_t gen = S.flags[F_GEN];
   constexpr int XH = MH > 0 ? MH : 1, XF = MF > 0 ? MF : 1;
@@ -912,6 +927,18 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     }
     if (in.op == OP_ATTN) {
       attn_dispatch<AD, AREP>(P, S, in, i, R);
+      // Every GEMV after attention reloads its activations; overwriting the
+      // register copies here makes them dead during the attention tile, so
+      // attention does not have to spill around them.
+#pragma unroll
+      for (int j = 0; j < XH; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xh[j][e] = 0.f;
+#pragma unroll
+      for (int j = 0; j < XF; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xf[j][e] = 0.f;
+      tag_h = tag_f = 0xffffffffu;
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
@@ -943,12 +970,16 @@ __device__ void consumer(const KParams& P, const Sh& S) {
         red_release_gpu_add(&P.bars[in.rel_bar], 1u);
     }
     if (P.trace && t == 0) {
-      unsigned long long* tr = P.trace + (size_t)i * 4;
+      unsigned long long* tr = P.trace + (size_t)i * TRACE_WORDS;
       tr[0] = (unsigned long long)smid() | ((unsigned long long)(in.op | (in.layer << 8)) << 32);
       tr[1] = t_begin;
       tr[2] = t_ready;
       tr[3] = globaltimer();
+      tr[5] = R.wait_ns;
+      tr[6] = R.first_ns;
     }
+    R.wait_ns = 0;
+    R.first_ns = 0;
     // no barrier here: the next instruction's slot and dependency barriers
     // order every reuse of the shared scratch
   }

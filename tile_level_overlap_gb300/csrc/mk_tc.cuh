@@ -47,12 +47,27 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16: bf16 x bf16 -> f32, both
-// operands K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor of an MN-major operand (MN contiguous) with
+// 128-byte swizzle, as written by TMA boxes of 64 MN elements x R K-rows:
+// 8-K-row groups 1024 B apart, consecutive 64-element MN chunks `lbo` bytes
+// apart.  `addr` includes the K offset (multiples of 16 rows = 2048 B).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3fffu);
+  d |= (uint64_t)((lbo >> 4) & 0x3fffu) << 16;      // leading byte offset: next MN chunk
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: next 8 K-rows
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: bf16 x bf16 -> f32, M x N,
+// A K-major; B K-major, or MN-major when b_mn is set.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn = false) {
   return (1u << 4)                 // D format: f32
          | (1u << 7)               // A format: bf16
          | (1u << 10)              // B format: bf16
+         | ((b_mn ? 1u : 0u) << 16)  // B major-ness
          | ((uint32_t)(N >> 3) << 17)
          | ((uint32_t)(M >> 4) << 24);
 }
@@ -65,6 +80,30 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T for one K = 16 slice; A (M rows x 16 bf16)
+// sits in TMEM lanes 0..M-1, 8 consecutive 32-bit columns (two bf16 each,
+// lower k in the low half).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 8 consecutive 32-bit columns from registers: thread i of the warp
+// writes lane (base lane + i).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread

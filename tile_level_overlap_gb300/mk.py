@@ -88,7 +88,8 @@ def lib() -> ctypes.CDLL:
     L.mk_plan_set_debug.argtypes = [vp, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
-    L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, vp]
     L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs),
                                          ctypes.c_int, ctypes.c_int, i32p, i32p, ctypes.c_int, vp,
                                          f32p, vp]
@@ -252,8 +253,8 @@ class Plan:
         """Trace records of the last traced launch as a numpy structured array."""
         import numpy as np
         n = self.stats().n_instr_decode
-        buf = np.zeros(n * 4, dtype=np.uint64)
+        buf = np.zeros(n * 8, dtype=np.uint64)
         got = ctypes.c_size_t()
         _check(lib().mk_trace_copy(self.h, buf.ctypes.data, buf.nbytes, ctypes.byref(got)), "mk_trace_copy")
-        rec = buf[: got.value * 4].reshape(-1, 4)
+        rec = buf[: got.value * 8].reshape(-1, 8)
         return rec
