@@ -219,7 +219,7 @@ int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int
 /* Copy the trace of the last traced launch: records of
  * 8 x uint64: {smid | (op | layer << 8) << 32, consumer took it, its waits were
  * satisfied, done, producer posted it, ns spent waiting for operand stages,
- * first operand stage ready, unused} (%globaltimer ns), 64 bytes per
+ * first operand stage ready, ns the producer waited for free stages} (%globaltimer ns), 64 bytes per
  * instruction, indexed by queue position.  *n_records receives the
  * count copied.  Waits for the device. */
 int mk_trace_copy(mk_plan *plan, void *host_buf, size_t bytes, size_t *n_records);

@@ -1,0 +1,139 @@
+"""Prefill on the GPU (tensor-core tiles with tile-level dependencies) through
+the C ABI, against the CPU oracle.
+
+Tolerances (written here): last-token logits per row within
+2e-2 * RMS(oracle logits); the K/V the prefill wrote into the cache (bf16)
+within 5e-2 * RMS of the oracle's K/V (bf16 GEMM operands and bf16 storage);
+prefill(S) followed by decode(1) against the oracle's prefill(S+1) within
+2e-2 * RMS.  Kernel-per-operator prefill is bit-identical to the persistent one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tile_level_overlap_gb300 import build, mk, synth
+
+pytestmark = pytest.mark.gpu
+
+PF_SMALL = synth.ModelCfg(n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, ffn=512,
+                          vocab=1024, rms_eps=1e-5, rope_theta=1e4)
+PF_D128_QK = synth.ModelCfg(n_layers=2, hidden=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                            ffn=768, vocab=512, rms_eps=1e-6, rope_theta=1e6, qk_norm=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    mk.lib()
+
+
+def _rows_close(got, ref, tol=2e-2):
+    got = np.atleast_2d(np.asarray(got, np.float64))
+    ref = np.atleast_2d(np.asarray(ref, np.float64))
+    for b in range(ref.shape[0]):
+        rms = np.sqrt((ref[b] ** 2).mean())
+        err = np.abs(got[b] - ref[b]).max()
+        assert err <= tol * rms, f"max |delta| {err:.4e} > {tol} * rms {rms:.4e}"
+
+
+class PfModel:
+    def __init__(self, cfg, max_ctx, seed=0):
+        self.cfg = cfg
+        self.dev = torch.device("cuda:0")
+        self.w = synth.make_weights(cfg, seed=seed, device=self.dev)
+        self.kv = torch.zeros(synth.kv_cache_shape(cfg, 1, max_ctx), dtype=torch.bfloat16,
+                              device=self.dev)
+        self.plan = mk.Plan(cfg, self.w, 1, max_ctx)
+        self.max_ctx = max_ctx
+
+    def prefill(self, tokens, per_op=False, graph=False):
+        t = torch.as_tensor(tokens, dtype=torch.int32).to(self.dev)
+        logits = torch.full((self.cfg.vocab,), float("nan"), device=self.dev)
+        if per_op:
+            self.plan.run_per_op(mk.MK_PREFILL, t, None, self.kv, logits, use_graph=graph)
+        else:
+            self.plan.prefill(t, self.kv, logits)
+        rc = self.plan.status()
+        assert rc == mk.MK_OK, mk.lib().mk_status_string(rc)
+        return logits.cpu().numpy()
+
+    def decode(self, token, pos):
+        t = torch.tensor([token], dtype=torch.int32, device=self.dev)
+        p = torch.tensor([pos], dtype=torch.int32, device=self.dev)
+        logits = torch.empty((1, self.cfg.vocab), device=self.dev)
+        self.plan.decode_step(t, p, self.kv, logits)
+        assert self.plan.status() == mk.MK_OK
+        return logits.cpu().numpy()[0]
+
+    def oracle_prefill(self, tokens):
+        return oracle.prefill(self.cfg, synth.LazyBits(self.w), np.asarray(tokens))
+
+    def close(self):
+        self.plan.close()
+        del self.w, self.kv
+        torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def small():
+    m = PfModel(PF_SMALL, max_ctx=384)
+    yield m
+    m.close()
+
+
+@pytest.mark.parametrize("S", [1, 7, 128, 129, 300, 384])
+def test_prefill_matches_oracle(small, S):
+    tokens = synth.make_tokens(S, small.cfg.vocab, seed=S).numpy()
+    got = small.prefill(tokens)
+    ref, K, V = small.oracle_prefill(tokens)
+    _rows_close(got, ref)
+    kv = oracle.widen_bf16(synth.bf16_bits(small.kv))
+    for name, gpu, orc in [("K", kv[:, 0, 0, :, :S, :], K), ("V", kv[:, 1, 0, :, :S, :], V)]:
+        rms = np.sqrt((orc.astype(np.float64) ** 2).mean())
+        err = np.abs(gpu - orc).max()
+        assert err <= 5e-2 * rms, f"{name}: max |delta| {err:.3e} > 5e-2 * {rms:.3e}"
+
+
+def test_prefill_then_decode_matches_longer_prefill(small):
+    tokens = synth.make_tokens(201, small.cfg.vocab, seed=11).numpy()
+    small.prefill(tokens[:200])
+    got = small.decode(int(tokens[200]), 200)
+    ref, _, _ = small.oracle_prefill(tokens)
+    _rows_close(got, ref)
+
+
+def test_prefill_per_op_and_graph_bit_identical(small):
+    tokens = synth.make_tokens(250, small.cfg.vocab, seed=12).numpy()
+    mega = small.prefill(tokens)
+    np.testing.assert_array_equal(small.prefill(tokens), mega)
+    np.testing.assert_array_equal(small.prefill(tokens, per_op=True), mega)
+    np.testing.assert_array_equal(small.prefill(tokens, per_op=True, graph=True), mega)
+
+
+@pytest.mark.parametrize("S", [5, 256, 333])
+def test_prefill_head_dim_128_qk_norm(S):
+    m = PfModel(PF_D128_QK, max_ctx=512, seed=4)
+    try:
+        tokens = synth.make_tokens(S, m.cfg.vocab, seed=S + 1).numpy()
+        got = m.prefill(tokens)
+        ref, _, _ = m.oracle_prefill(tokens)
+        _rows_close(got, ref)
+    finally:
+        m.close()
+
+
+def test_llama3_8b_width_prefill_2048_tokens():
+    """Full Llama-3-8B widths (hidden 4096, 32/8 heads, head_dim 128, FFN
+    14336, vocab 128256) with 2 of the 32 layers, on the 2048-token prompt."""
+    cfg = synth.LLAMA3_8B.replace(n_layers=2)
+    m = PfModel(cfg, max_ctx=2049, seed=0)
+    try:
+        tokens = synth.make_tokens(2048, cfg.vocab).numpy()
+        got = m.prefill(tokens)
+        ref, _, _ = m.oracle_prefill(tokens)
+        _rows_close(got, ref)
+    finally:
+        m.close()

@@ -9,13 +9,35 @@
 #include "../../include/mk.h"
 #include "mk_internal.h"
 #include "mk_plan.h"
+#include "mk_prefill.h"
+#include "mk_tmap.h"
 #include "mk_variants.h"
 
+namespace mk {
+cudaError_t pf_setup();
+cudaError_t pf_launch_mega(const PfParams& p, int ctas, cudaStream_t st);
+cudaError_t pf_launch_perop(const PfParams& p, uint32_t first, uint32_t count, cudaStream_t st);
+}  // namespace mk
+
 using namespace mk;
+
+// Prefill state of a plan, built on the first prefill call.
+struct PrefillState {
+  bool built = false;
+  PrefillPlan pp;
+  void* mem = nullptr;
+  size_t bytes = 0;
+  PfParams base{};
+  CUtensorMap* d_tm = nullptr;          // device copy of the tensor-map table
+  std::vector<CUtensorMap> h_tm;        // host copy (source of the uploads)
+  const void* kv_mapped = nullptr;      // KV cache the table's cache map points at
+};
 
 struct mk_plan {
   HostPlan hp;
   KernelVariant kv{};
+  std::vector<LayerW> lw;  // host copy of the per-layer weight pointers
+  PrefillState pf;
   int device = 0, n_sms = 0, max_ctas = 0;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -114,9 +136,14 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
     if (q.size() != hp.decode.size()) return MK_ERR_INVALID_ARG;
   }
   rc = simulate(hp, q, &why);
+  // the prefill queue, when this shape has a prefill path
+  PrefillPlan pp;
+  const bool has_pf = build_prefill(*cfg, max_ctx, &pp, &why) == MK_OK;
+  if (rc == MK_OK && has_pf) rc = simulate_prefill(pp, pp.queue, &why);
   if (out) {
     std::memset(out, 0, sizeof(*out));
     out->n_instr_decode = (uint32_t)hp.decode.size();
+    out->n_instr_prefill = has_pf ? (uint32_t)pp.queue.size() : 0u;
     out->n_barriers = hp.bl.total;
     out->n_launches_per_op_decode = (uint32_t)hp.perop_decode.size();
     out->n_splits = (uint32_t)hp.n_splits;
@@ -233,7 +260,8 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
                  cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(s + o_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice) !=
           cudaSuccess ||
-      cudaMemcpy(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice) != cudaSuccess)
+      cudaMemcpy(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice) != cudaSuccess ||
+      (p->lw = lw, false))
     return fail(MK_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
     return fail(MK_ERR_CUDA);
@@ -274,6 +302,7 @@ void mk_plan_destroy(mk_plan* p) {
   if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
   if (p->d_trace) cudaFree(p->d_trace);
   if (p->scratch) cudaFree(p->scratch);
+  if (p->pf.mem) cudaFree(p->pf.mem);
   delete p;
 }
 
@@ -283,6 +312,14 @@ int mk_plan_get_stats(const mk_plan* p, mk_plan_stats* out) {
   if (!p || !out) return MK_ERR_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));
   out->n_instr_decode = (uint32_t)p->hp.decode.size();
+  {
+    PrefillPlan pp;
+    std::string why;
+    out->n_instr_prefill = p->pf.built ? (uint32_t)p->pf.pp.queue.size()
+                           : build_prefill(p->hp.cfg, p->hp.max_ctx, &pp, &why) == MK_OK
+                               ? (uint32_t)pp.queue.size()
+                               : 0u;
+  }
   out->n_barriers = p->hp.bl.total;
   out->n_launches_per_op_decode = (uint32_t)p->hp.perop_decode.size();
   out->n_ctas = (uint32_t)(p->force_ctas ? p->force_ctas : p->max_ctas);
@@ -345,10 +382,144 @@ int mk_decode_step_host(mk_plan* p, const int32_t* tokens_host, const int32_t* p
   return (int)status;
 }
 
+// ---------------------------------------------------------------- prefill
+// Build the prefill queue, its buffers and the tensor-map table (first call).
+static int prefill_init(mk_plan* p) {
+  PrefillState& s = p->pf;
+  if (s.built) return MK_OK;
+  std::string why;
+  int rc = build_prefill(p->hp.cfg, p->hp.max_ctx, &s.pp, &why);
+  if (rc != MK_OK) return rc;
+  if (pf_setup() != cudaSuccess) return MK_ERR_CUDA;
+  const mk_model_cfg& c = p->hp.cfg;
+  const PrefillPlan& pp = s.pp;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn;
+  const int qd = c.n_q_heads * d, kd = c.n_kv_heads * d;
+  const size_t rows = (size_t)pp.n_blocks * PF_BM;
+  const int n_maps = L * TM_PER_LAYER + AM_COUNT;
+  Bump bm;
+  const size_t o_bars = bm.take(sizeof(uint32_t) * pp.bl.total);
+  const size_t o_ctl = bm.take(sizeof(uint32_t) * CTL_WORDS);
+  const size_t o_q = bm.take(sizeof(Instr) * pp.queue.size());
+  const size_t o_expr = bm.take(sizeof(uint32_t) * pp.expr.size());
+  const size_t o_tm = bm.take(sizeof(CUtensorMap) * n_maps);
+  const size_t o_xa = bm.take(sizeof(float) * rows * H);
+  const size_t o_xb = bm.take(sizeof(float) * rows * H);
+  const size_t o_hn1 = bm.take(2 * rows * H);
+  const size_t o_hn2 = bm.take(2 * rows * H);
+  const size_t o_qb = bm.take(2 * rows * qd);
+  const size_t o_ao = bm.take(2 * rows * qd);
+  const size_t o_act = bm.take(2 * rows * F);
+  if (cudaMalloc(&s.mem, bm.off) != cudaSuccess) {
+    cudaGetLastError();
+    s.mem = nullptr;
+    return MK_ERR_CUDA;
+  }
+  s.bytes = bm.off;
+  uint8_t* b = (uint8_t*)s.mem;
+  MK_CUDA(cudaMemset(s.mem, 0, s.bytes));
+  s.d_tm = (CUtensorMap*)(b + o_tm);
+  s.h_tm.assign(n_maps, CUtensorMap{});
+  bool ok = true;
+  for (int l = 0; l < L && ok; ++l) {
+    const LayerW& w = p->lw[l];
+    CUtensorMap* t = &s.h_tm[l * TM_PER_LAYER];
+    ok = make_tmap_bf16(t + TM_WQ, w.wq, qd, H, pp.bn_qkv) &&
+         make_tmap_bf16(t + TM_WK, w.wk, kd, H, pp.bn_qkv) &&
+         make_tmap_bf16(t + TM_WV, w.wv, kd, H, pp.bn_qkv) &&
+         make_tmap_bf16(t + TM_WO, w.wo, H, qd, PF_BN) &&
+         make_tmap_bf16(t + TM_WG, w.wg, F, H, PF_BN_GU) &&
+         make_tmap_bf16(t + TM_WU, w.wu, F, H, PF_BN_GU) &&
+         make_tmap_bf16(t + TM_WD, w.wd, H, F, PF_BN);
+  }
+  CUtensorMap* a = &s.h_tm[L * TM_PER_LAYER];
+  ok = ok && make_tmap_bf16(a + AM_HN1, b + o_hn1, rows, H, PF_BM) &&
+       make_tmap_bf16(a + AM_HN2, b + o_hn2, rows, H, PF_BM) &&
+       make_tmap_bf16(a + AM_AO, b + o_ao, rows, qd, PF_BM) &&
+       make_tmap_bf16(a + AM_ACT, b + o_act, rows, F, PF_BM) &&
+       make_tmap_bf16(a + AM_Q, b + o_qb, rows, qd, PF_BM);
+  if (!ok) return MK_ERR_CUDA;
+  MK_CUDA(cudaMemcpy(b + o_q, pp.queue.data(), sizeof(Instr) * pp.queue.size(), cudaMemcpyHostToDevice));
+  MK_CUDA(cudaMemcpy(b + o_expr, pp.expr.data(), sizeof(uint32_t) * pp.expr.size(),
+                     cudaMemcpyHostToDevice));
+  MK_CUDA(cudaMemcpy(s.d_tm, s.h_tm.data(), sizeof(CUtensorMap) * n_maps, cudaMemcpyHostToDevice));
+  PfParams& k = s.base;
+  std::memset(&k, 0, sizeof(k));
+  k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = c.n_kv_heads; k.d = d; k.F = F; k.V = c.vocab;
+  k.qk_norm = c.qk_norm; k.rep = pp.rep; k.qkv_rows = pp.qkv_rows; k.bn_qkv = pp.bn_qkv;
+  k.n_blocks = pp.n_blocks; k.max_ctx = p->hp.max_ctx; k.max_batch = p->hp.max_batch;
+  k.eps = c.rms_eps;
+  k.n_qkv_n = pp.n_qkv_n; k.n_o_n = pp.n_o_n; k.n_gu_n = pp.n_gu_n; k.n_down_n = pp.n_down_n;
+  k.embed = p->base.embed;
+  k.layers = p->base.layers;
+  k.tm = s.d_tm;
+  k.xa = (float*)(b + o_xa);
+  k.xb = (float*)(b + o_xb);
+  k.hn1 = (uint16_t*)(b + o_hn1);
+  k.hn2 = (uint16_t*)(b + o_hn2);
+  k.qb = (uint16_t*)(b + o_qb);
+  k.ao = (uint16_t*)(b + o_ao);
+  k.act = (uint16_t*)(b + o_act);
+  k.rope = p->base.rope;
+  k.bars = (uint32_t*)(b + o_bars);
+  k.ctl = (uint32_t*)(b + o_ctl);
+  k.queue = (const Instr*)(b + o_q);
+  k.n_instr = (uint32_t)pp.queue.size();
+  k.expr = (const uint32_t*)(b + o_expr);
+  s.built = true;
+  return MK_OK;
+}
+
+// Point the table's cache map at this call's KV cache.
+static int prefill_bind_kv(mk_plan* p, void* kv, cudaStream_t st) {
+  PrefillState& s = p->pf;
+  if (s.kv_mapped == kv) return MK_OK;
+  const mk_model_cfg& c = p->hp.cfg;
+  const int idx = c.n_layers * TM_PER_LAYER + AM_KV;
+  const uint64_t rows = (uint64_t)c.n_layers * 2 * p->hp.max_batch * c.n_kv_heads * p->hp.max_ctx;
+  if (!make_tmap_bf16(&s.h_tm[idx], kv, rows, (uint64_t)c.head_dim, PF_BM)) return MK_ERR_CUDA;
+  MK_CUDA(cudaMemcpyAsync(s.d_tm + idx, &s.h_tm[idx], sizeof(CUtensorMap), cudaMemcpyHostToDevice, st));
+  MK_CUDA(cudaStreamSynchronize(st));
+  s.kv_mapped = kv;
+  return MK_OK;
+}
+
+static int prefill_args(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits) {
+  if (!p || !tokens || !kv || !logits || len < 1 || len > p->hp.max_ctx || !aligned16(kv))
+    return MK_ERR_INVALID_ARG;
+  if (p->latched) return p->latched;
+  return MK_OK;
+}
+
+// The LM head of the prompt's last token runs as its own per-operator launch
+// of the decode tiles after the prefill body ("Lecture 112", Practical
+// implications: a megakernel body mixed with a separate LM-head op).
+static int prefill_lm(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits,
+                      cudaStream_t st) {
+  const mk_model_cfg& c = p->hp.cfg;
+  const float* last = p->pf.base.xb + (size_t)(len - 1) * c.hidden;
+  float* dst = p->base.resid + (size_t)(2 * c.n_layers) * p->hp.max_batch * c.hidden;
+  MK_CUDA(cudaMemcpyAsync(dst, last, sizeof(float) * c.hidden, cudaMemcpyDeviceToDevice, st));
+  KParams k = step_params(p, tokens, tokens, 1, kv, logits);
+  k.queue = p->d_queue;
+  k.trace = nullptr;
+  const auto& r = p->hp.perop_decode.back();  // the LM-head tiles
+  return cuda_err(p->kv.perop(k, r.first, r.second, st));
+}
+
 int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits, void* stream) {
-  (void)stream;
-  if (!p || !tokens || !kv || !logits || len < 1 || len > p->hp.max_ctx) return MK_ERR_INVALID_ARG;
-  return MK_ERR_UNSUPPORTED;
+  int rc = prefill_args(p, tokens, len, kv, logits);
+  if (rc != MK_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = prefill_init(p)) != MK_OK || (rc = prefill_bind_kv(p, kv, st)) != MK_OK) return rc;
+  PfParams k = p->pf.base;
+  k.tokens = tokens;
+  k.S = len;
+  k.kv = (uint16_t*)kv;
+  k.mode = MODE_MEGA;
+  k.wait_limit_ns = p->wait_limit_ns;
+  MK_CUDA(pf_launch_mega(k, p->n_sms, st));
+  return prefill_lm(p, tokens, len, kv, logits, st);
 }
 
 static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
@@ -356,21 +527,37 @@ static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
   return MK_OK;
 }
 
+static int launch_per_op_prefill(mk_plan* p, const PfParams& k, void* kv, float* logits,
+                                 cudaStream_t st) {
+  for (const auto& r : p->pf.pp.perop) MK_CUDA(pf_launch_perop(k, r.first, r.second, st));
+  return prefill_lm(p, k.tokens, k.S, kv, logits, st);
+}
+
 int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,
                   const int32_t* positions, int batch_or_len, void* kv, float* logits,
                   void* stream) {
-  if (mode == MK_PREFILL) {
-    if (!p || !tokens || !kv || !logits) return MK_ERR_INVALID_ARG;
-    return MK_ERR_UNSUPPORTED;
-  }
-  if (mode != MK_DECODE) return MK_ERR_INVALID_ARG;
-  int rc = check_step(p, tokens, positions, batch_or_len, kv, logits);
-  if (rc != MK_OK) return rc;
-  KParams k = step_params(p, tokens, positions, batch_or_len, kv, logits);
-  k.queue = p->d_queue;
-  k.trace = nullptr;
   cudaStream_t st = (cudaStream_t)stream;
-  if (!use_graph) return launch_per_op_seq(p, k, st);
+  PfParams pk;
+  KParams k;
+  if (mode == MK_PREFILL) {
+    int rc = prefill_args(p, tokens, batch_or_len, kv, logits);
+    if (rc != MK_OK) return rc;
+    if ((rc = prefill_init(p)) != MK_OK || (rc = prefill_bind_kv(p, kv, st)) != MK_OK) return rc;
+    pk = p->pf.base;
+    pk.tokens = tokens;
+    pk.S = batch_or_len;
+    pk.kv = (uint16_t*)kv;
+    pk.wait_limit_ns = p->wait_limit_ns;
+    if (!use_graph) return launch_per_op_prefill(p, pk, kv, logits, st);
+  } else {
+    if (mode != MK_DECODE) return MK_ERR_INVALID_ARG;
+    int rc = check_step(p, tokens, positions, batch_or_len, kv, logits);
+    if (rc != MK_OK) return rc;
+    k = step_params(p, tokens, positions, batch_or_len, kv, logits);
+    k.queue = p->d_queue;
+    k.trace = nullptr;
+    if (!use_graph) return launch_per_op_seq(p, k, st);
+  }
   const uintptr_t key[6] = {(uintptr_t)tokens, (uintptr_t)positions, (uintptr_t)batch_or_len,
                             (uintptr_t)kv, (uintptr_t)logits, (uintptr_t)mode};
   if (!p->graph || std::memcmp(key, p->graph_key, sizeof(key)) != 0) {
@@ -380,7 +567,8 @@ int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,
     }
     cudaGraph_t g = nullptr;
     MK_CUDA(cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeThreadLocal));
-    int lrc = launch_per_op_seq(p, k, p->cap_stream);
+    int lrc = mode == MK_PREFILL ? launch_per_op_prefill(p, pk, kv, logits, p->cap_stream)
+                                 : launch_per_op_seq(p, k, p->cap_stream);
     cudaError_t e = cudaStreamEndCapture(p->cap_stream, &g);
     if (lrc != MK_OK || e != cudaSuccess) {
       if (g) cudaGraphDestroy(g);
@@ -404,6 +592,10 @@ int mk_status(mk_plan* p, void* stream) {
   if (cudaMemcpy(&status, p->d_ctl + CTL_STATUS, sizeof(status), cudaMemcpyDeviceToHost) !=
       cudaSuccess)
     return MK_ERR_CUDA;
+  if (!status && p->pf.built &&
+      cudaMemcpy(&status, p->pf.base.ctl + CTL_STATUS, sizeof(status), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return MK_ERR_CUDA;
   if (status) p->latched = (int)status;
   return (int)status;
 }
@@ -416,6 +608,10 @@ int mk_plan_reset(mk_plan* p, void* stream) {
   MK_CUDA(cudaMemset(p->base.arrive, 0,
                      sizeof(uint32_t) * p->hp.cfg.n_layers * p->hp.max_batch * p->hp.cfg.n_kv_heads));
   MK_CUDA(cudaMemset(p->d_ctl, 0, sizeof(uint32_t) * CTL_WORDS));
+  if (p->pf.built) {
+    MK_CUDA(cudaMemset(p->pf.base.bars, 0, sizeof(uint32_t) * p->pf.pp.bl.total));
+    MK_CUDA(cudaMemset(p->pf.base.ctl, 0, sizeof(uint32_t) * CTL_WORDS));
+  }
   MK_CUDA(cudaDeviceSynchronize());
   p->latched = 0;
   return MK_OK;

@@ -199,13 +199,14 @@ __device__ __forceinline__ GemvDesc gemv_desc(const KParams& P, const Instr& in)
   return g;
 }
 
-__device__ __forceinline__ Src instr_src(const KParams& P, const Instr& in) {
+// Operand source of an instruction; `e` is its attention extent (ignored for
+// GEMV tiles).
+__device__ __forceinline__ Src src_of(const KParams& P, const Instr& in, const AttnExt& e) {
   Src s;
   s.nreg = 0;
   s.rows[0] = s.rows[1] = 0;
   s.ptr[0] = s.ptr[1] = nullptr;
   if (in.op == OP_ATTN) {
-    AttnExt e = attn_extent(P, in);
     s.row_bytes = P.d * 2;
     s.rps = STAGE_BYTES / s.row_bytes;
     if (e.live && e.nc > 0) {
@@ -224,6 +225,35 @@ __device__ __forceinline__ Src instr_src(const KParams& P, const Instr& in) {
   s.ptr[1] = reinterpret_cast<const uint8_t*>(g.w1);
   s.rows[0] = s.rows[1] = (uint32_t)g.rows;
   return s;
+}
+
+__device__ __forceinline__ Src instr_src(const KParams& P, const Instr& in) {
+  AttnExt e;
+  e.live = false;
+  if (in.op == OP_ATTN) e = attn_extent(P, in);
+  return src_of(P, in, e);
+}
+
+// The attention extent travels from the producer to the consumers in the
+// instruction slot (bytes 4..15), so it is evaluated once per instruction.
+__device__ __forceinline__ void slot_put_ext(const Sh& S, int si, const AttnExt& e) {
+  int32_t* x = reinterpret_cast<int32_t*>(S.islot + si * SmemLayout::islot_bytes + 4);
+  x[0] = e.lo;
+  x[1] = e.hi;
+  x[2] = e.live ? e.pos : -1;
+}
+__device__ __forceinline__ AttnExt slot_get_ext(const Sh& S, int si) {
+  const int32_t* x = reinterpret_cast<const int32_t*>(S.islot + si * SmemLayout::islot_bytes + 4);
+  AttnExt e;
+  e.lo = x[0];
+  e.hi = x[1];
+  e.live = x[2] >= 0;
+  e.pos = e.live ? x[2] : 0;
+  const int cend = e.hi < e.pos ? e.hi : e.pos;
+  e.nc = (e.live && cend > e.lo) ? cend - e.lo : 0;
+  e.has_new = e.live && e.lo <= e.pos && e.pos < e.hi;
+  if (!e.live) e.lo = e.hi = 0;
+  return e;
 }
 
 __device__ __forceinline__ uint32_t src_stages(const Src& s) {
@@ -262,8 +292,14 @@ __device__ void producer(const KParams& P, const Sh& S) {
     const uint32_t ic = (end || ib == END_SLOT) ? END_SLOT : pop();
     const int si = islot_ctr % NISLOT;
     bool posted_end = end;
+    AttnExt ext;
+    ext.live = false;
+    if (!end && Ia.op == OP_ATTN) ext = attn_extent(P, Ia);
     if (!mbar_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) posted_end = true;
-    if (!posted_end) *slot_instr(S, si) = Ia;
+    if (!posted_end) {
+      *slot_instr(S, si) = Ia;
+      slot_put_ext(S, si, ext);
+    }
     *slot_index(S, si) = posted_end ? END_SLOT : ia;
     mbar_arrive(&S.ifull[si]);
     if (P.trace && !posted_end) P.trace[(size_t)ia * TRACE_WORDS + 4] = globaltimer();
@@ -271,28 +307,33 @@ __device__ void producer(const KParams& P, const Sh& S) {
     if (posted_end) break;
 
     const Instr in = Ia;
+    const uint32_t i_in = ia;
     ia = ib;
     Ia = Ib;
     ib = ic;
-    const Src src = instr_src(P, in);
+    const Src src = src_of(P, in, ext);
     bool stuck = false;
+    uint64_t blocked_ns = 0;  // (tracing) time spent waiting for a free stage
     for (int r = 0; r < src.nreg && !stuck; ++r) {
       for (uint32_t row = 0; row < src.rows[r]; row += src.rps) {
         uint32_t n = src.rows[r] - row < src.rps ? src.rows[r] - row : src.rps;
         uint32_t bytes = n * src.row_bytes;
         const int st = stage_ctr % NSTAGE;
+        const uint64_t tw = P.trace ? globaltimer() : 0;
         if (!mbar_wait(P, &S.empty[st], ((stage_ctr / NSTAGE) & 1u) ^ 1u)) {
           // the consumers stopped taking stages: issue nothing more (the
           // consumers' own bounded waits end their loop)
           stuck = true;
           break;
         }
+        if (P.trace) blocked_ns += globaltimer() - tw;
         mbar_arrive_expect_tx(&S.full[st], bytes);
         bulk_g2s(S.ring + (size_t)st * STAGE_BYTES, src.ptr[r] + (size_t)row * src.row_bytes, bytes,
                  &S.full[st], policy);
         ++stage_ctr;
       }
     }
+    if (P.trace) P.trace[(size_t)i_in * TRACE_WORDS + 7] = blocked_ns;
     if (stuck) break;
   }
 }
@@ -592,13 +633,13 @@ __device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, co
 // Partial (max, sum, unnormalised o) per q head; the last split to arrive
 // combines all splits of the group in split order.
 template <int D, int REP>
-__device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32_t ii, Ring& R) {
+__device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
+                          uint32_t ii, Ring& R) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int l = in.layer, b = (int)in.a0, g = (int)in.a1, split = (int)in.a2;
   constexpr int rep = REP;
   const int qd = P.nq * D, NS = P.n_splits;
   constexpr int smax = SCORE_FLOATS / REP;
-  AttnExt e = attn_extent(P, in);
   if (t == 0 && b < P.B && !e.live) set_error(P, MK_ERR_BOUNDS, ii);  // position out of range
   float* qs = S.xbuf;            // [rep][D]
   float* kn = qs + 8 * 128;      // [D]
@@ -820,22 +861,23 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, uint32
 }
 
 template <int AD, int AREP>
-__device__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, uint32_t ii, Ring& R) {
+__device__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
+                              uint32_t ii, Ring& R) {
   if constexpr (AD != 0) {
-    attn_tile<AD, AREP>(P, S, in, ii, R);
+    attn_tile<AD, AREP>(P, S, in, e, ii, R);
   } else if (P.d == 128) {
     switch (P.rep) {
-      case 1: attn_tile<128, 1>(P, S, in, ii, R); break;
-      case 2: attn_tile<128, 2>(P, S, in, ii, R); break;
-      case 4: attn_tile<128, 4>(P, S, in, ii, R); break;
-      default: attn_tile<128, 8>(P, S, in, ii, R); break;
+      case 1: attn_tile<128, 1>(P, S, in, e, ii, R); break;
+      case 2: attn_tile<128, 2>(P, S, in, e, ii, R); break;
+      case 4: attn_tile<128, 4>(P, S, in, e, ii, R); break;
+      default: attn_tile<128, 8>(P, S, in, e, ii, R); break;
     }
   } else {
     switch (P.rep) {
-      case 1: attn_tile<64, 1>(P, S, in, ii, R); break;
-      case 2: attn_tile<64, 2>(P, S, in, ii, R); break;
-      case 4: attn_tile<64, 4>(P, S, in, ii, R); break;
-      default: attn_tile<64, 8>(P, S, in, ii, R); break;
+      case 1: attn_tile<64, 1>(P, S, in, e, ii, R); break;
+      case 2: attn_tile<64, 2>(P, S, in, e, ii, R); break;
+      case 4: attn_tile<64, 4>(P, S, in, e, ii, R); break;
+      default: attn_tile<64, 8>(P, S, in, e, ii, R); break;
     }
   }
 }
@@ -879,7 +921,12 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     cbar();
     const uint32_t i = S.flags[F_SLOT];
     Instr in;
-    if (i != END_SLOT) in = *slot_instr(S, si);
+    AttnExt ext;
+    ext.live = false;
+    if (i != END_SLOT) {
+      in = *slot_instr(S, si);
+      if (in.op == OP_ATTN) ext = slot_get_ext(S, si);
+    }
     __syncwarp();
     if ((t & 31) == 0) mbar_arrive(&S.iempty[si]);
     ++islot_ctr;
@@ -926,7 +973,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       continue;
     }
     if (in.op == OP_ATTN) {
-      attn_dispatch<AD, AREP>(P, S, in, i, R);
+      attn_dispatch<AD, AREP>(P, S, in, ext, i, R);
       // Every GEMV after attention reloads its activations; overwriting the
       // register copies here makes them dead during the attention tile, so
       // attention does not have to spill around them.

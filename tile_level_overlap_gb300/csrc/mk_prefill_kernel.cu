@@ -88,15 +88,19 @@ __device__ void pf_error(const PfParams& P, uint32_t code, uint32_t detail) {
   atomicExch(&P.ctl[CTL_ABORT], 1u);
 }
 
+// Bounded mbarrier wait.  After an abort (another wait already gave up) it
+// gives up within ~10 us, so a broken launch drains quickly.
 __device__ __forceinline__ bool pf_wait(const PfParams& P, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (;;) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > P.wait_limit_ns * 4ull) {
+    const uint64_t dt = globaltimer() - t0;
+    if (dt > P.wait_limit_ns * 4ull) {
       pf_error(P, MK_ERR_TIMEOUT, 0xfffffff1u);
       return false;
     }
+    if ((it & 255u) == 0 && dt > 10000ull && ld_volatile(&P.ctl[CTL_ABORT]) != 0u) return false;
   }
 }
 
@@ -301,6 +305,13 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
       }
     }
   }
+  // Before leaving, make sure the copies this thread issued have landed
+  // (normally already consumed; after an abort some may still be in flight).
+  for (uint32_t k = 0; k < PF_NSTAGE && k < stage_ctr; ++k) {
+    const uint32_t c = stage_ctr - 1 - k;
+    pf_wait(P, &S.full[c % PF_NSTAGE], (c / PF_NSTAGE) & 1u);
+  }
+  if (qctr) pf_wait(P, S.qfull, (qctr - 1) & 1u);
 }
 
 // ---------------------------------------------------------------- tensor-core issuer
