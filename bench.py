@@ -31,6 +31,7 @@ METRIC = "decode tokens/s and HBM GB/s (% of ~8 TB/s), Llama-3-8B shape, batch 1
 UNIT = "tokens/s"
 CONTEXT = 4096
 BATCH = 1
+PREFILL_TOKENS = 2048
 
 
 def workload_cfg():
@@ -49,6 +50,18 @@ def algorithmic_bytes(cfg, batch, positions) -> int:
     kv_read = sum(2 * cfg.n_layers * cfg.n_kv_heads * int(p) * d * 2 for p in positions)
     kv_write = batch * 2 * cfg.n_layers * cfg.n_kv_heads * d * 2
     return weights + kv_read + kv_write
+
+
+def prefill_flops(cfg, S) -> float:
+    """Algorithmic FLOPs of a causal prefill of S tokens: every projection
+    (2 * S * params per layer) plus causal attention (QK^T and PV over the
+    S(S+1)/2 visible pairs per head), plus the last token's LM head."""
+    H, d, F = cfg.hidden, cfg.head_dim, cfg.ffn
+    qd = cfg.n_q_heads * d
+    per_layer_params = (cfg.n_q_heads + 2 * cfg.n_kv_heads) * d * H + H * qd + 3 * F * H
+    gemm = 2.0 * S * per_layer_params * cfg.n_layers
+    attn = 2.0 * 2.0 * qd * (S * (S + 1) / 2.0) * cfg.n_layers
+    return gemm + attn + 2.0 * cfg.vocab * H
 
 
 def measured_peaks():
@@ -332,6 +345,33 @@ def run_ours(args):
     n_ctas = plan.stats().n_ctas
     dep_wait = float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span) if span > 0 else None
 
+    # prefill of a 2048-token prompt into sequence slot 0 (after the decode
+    # timing, since it rewrites that cache slot)
+    prefill = None
+    if not args.no_prefill:
+        S = PREFILL_TOKENS
+        ptok = synth.make_tokens(S, cfg.vocab, seed=synth.SEED_TOKENS + 7).to(dev)
+        plog = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+
+        def pf():
+            plan.prefill(ptok, kv, plog, stream=stream)
+
+        for _ in range(2):
+            pf()
+        rc = plan.status(stream)
+        if rc != mk.MK_OK:
+            raise RuntimeError(f"prefill device status {rc}")
+        pf_steps = max(3, args.steps // 10)
+        ms_pf = timed(pf, pf_steps) / pf_steps
+        flops = prefill_flops(cfg, S)
+        peaks_p, kind_p = measured_peaks()
+        tf = flops / (ms_pf / 1e3) / 1e12
+        prefill = {"tokens": S, "ms": ms_pf, "tokens_per_s": S / (ms_pf / 1e3),
+                   "tflops": tf, "peak_tflops": peaks_p["bf16_tflops_sustained"],
+                   "frac_of_tensor_peak": tf / peaks_p["bf16_tflops_sustained"],
+                   "peak_kind": kind_p + " (sustained bf16)", "steps": pf_steps,
+                   "kernels_per_step": 2}
+
     if rank != 0:
         return 0
     peaks, kind = measured_peaks()
@@ -365,6 +405,7 @@ def run_ours(args):
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": 8 * BATCH,
                 "d2h_bytes_per_step": 4 * BATCH * cfg.vocab + 4},
         "gpu_launches": args.steps,
+        "prefill": prefill,
     }
     if world == 1 and not args.no_cpu_baseline:
         sample_run = OracleSample(cfg, args.ref_layers)
@@ -389,6 +430,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

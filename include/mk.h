@@ -217,10 +217,11 @@ int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int
                        void *stream);
 
 /* Copy the trace of the last traced launch: records of
- * 8 x uint64: {smid | (op | layer << 8) << 32, consumer took it, its waits were
+ * 12 x uint64: {smid | (op | layer << 8) << 32, consumer took it, its waits were
  * satisfied, done, producer posted it, ns spent waiting for operand stages,
- * first operand stage ready, ns the producer waited for free stages} (%globaltimer ns), 64 bytes per
- * instruction, indexed by queue position.  *n_records receives the
+ * first operand stage ready, ns the producer waited for free stages, last stage
+ * consumed, cross-warp reduction done, 0, 0} (%globaltimer ns; the last four
+ * for batch-1 GEMV tiles), 96 bytes per instruction, indexed by queue position.  *n_records receives the
  * count copied.  Waits for the device. */
 int mk_trace_copy(mk_plan *plan, void *host_buf, size_t bytes, size_t *n_records);
 

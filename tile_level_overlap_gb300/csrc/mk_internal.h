@@ -149,8 +149,10 @@ enum Mode : int { MODE_MEGA = 0, MODE_PEROP = 1 };
 // [0] smid | (op | layer << 8) << 32, [1] consumer took it, [2] its waits were
 // satisfied, [3] done (released), [4] producer posted it, [5] ns the consumer
 // spent waiting for ring stages, [6] first stage available, [7] ns the producer
-// spent waiting for free ring stages while streaming it.
-constexpr int TRACE_WORDS = 8;
+// spent waiting for free ring stages while streaming it, [8] (batch-1 GEMV)
+// last stage consumed, [9] (batch-1 GEMV) cross-warp reduction done, [10] and
+// [11] unused.
+constexpr int TRACE_WORDS = 12;
 
 // Everything one launch needs, passed by value as a __grid_constant__ parameter.
 struct KParams {

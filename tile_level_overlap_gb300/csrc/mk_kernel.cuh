@@ -50,7 +50,7 @@ static_assert(SmemLayout::total <= 227 * 1024, "shared memory budget");
 
 // F_STOP: set by a consumer that saw the abort word, read by the producer
 // before each pop (a shared-memory load instead of a global one).
-enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3, F_STOP = 4 };
+enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3, F_STOP = 4, F_SLOT_B = 5, F_ABORT_B = 6 };
 
 struct Sh {
   uint8_t* ring;
@@ -343,6 +343,8 @@ struct Ring {
   uint32_t ctr;           // stages consumed so far
   uint64_t wait_ns;       // (tracing, thread 0) time spent waiting for stages
   uint64_t first_ns;      // (tracing, thread 0) when the instruction's first stage was ready
+  uint64_t loop_ns;       // (tracing, thread 0) when the last stage was consumed
+  uint64_t red_ns;        // (tracing, thread 0) when the cross-warp reduction finished
 };
 
 __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
@@ -503,14 +505,20 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
       tile_row += n;
     }
   }
+  if (P.trace && t == 0) R.loop_ns = globaltimer();
   cbar();
+  if (P.trace && t == 0) R.red_ns = globaltimer();
+  // Only warp 0 finishes the tile (rows <= RMAX = 32 at batch 1): it sums the
+  // warps' partials, and the caller runs the epilogue and the release in the
+  // same warp, so the other warps move on to the next instruction.
+  if (w != 0) return;
   if (t < ntot) {
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NW; ++k) s += S.redw[k * RMAX + t];
     S.red[t * BMAX_CC] = s;
   }
-  cbar();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
@@ -898,7 +906,7 @@ __device__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
 template <int MH, int MF, int AD, int AREP>
 __device__ void consumer(const KParams& P, const Sh& S) {
   const int t = threadIdx.x;
-  Ring R{0, 0, 0};
+  Ring R{0, 0, 0, 0, 0};
   uint32_t islot_ctr = 0;
   const uint32_t gen = S.flags[F_GEN];
   constexpr int XH = MH > 0 ? MH : 1, XF = MF > 0 ? MF : 1;
@@ -911,15 +919,59 @@ __device__ void consumer(const KParams& P, const Sh& S) {
   uint32_t ok_bar = NO_BAR, ok_target = 0;
   for (;;) {
     const int si = islot_ctr % NISLOT;
-    // one thread takes the slot (a bounded wait); the consumer barrier hands
-    // it to the others so that every consumer thread takes the same path
+    // The broadcast words are double-buffered by instruction parity: warps
+    // 1..7 may still be reading this instruction's words while warp 0 (which
+    // finishes every batch-1 tile) already fills in the next instruction's.
+    const int f_slot = (islot_ctr & 1u) ? F_SLOT_B : F_SLOT;
+    const int f_abort = (islot_ctr & 1u) ? F_ABORT_B : F_ABORT;
+    // one thread takes the slot (a bounded wait)
     if (t == 0) {
       uint32_t v = 0xffffffffu;
       if (mbar_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u)) v = *slot_index(S, si);
-      S.flags[F_SLOT] = v;
+      S.flags[f_slot] = v;
+    }
+    // Thread 0 also waits on the tiles the instruction reads (the abort word is
+    // read only while spinning: a launch that never waits on an unsatisfied
+    // counter runs to completion anyway); one consumer barrier then hands the
+    // slot and the verdict to every consumer thread.
+    uint64_t t_begin = 0, t_ready = 0;
+    if (t == 0) {
+      const uint32_t iv = S.flags[f_slot];
+      uint32_t aborted = S.flags[F_STOP];
+      if (P.trace) t_begin = globaltimer();
+      if (iv != END_SLOT) {
+        const Instr& in0 = *slot_instr(S, si);
+        if (!aborted && P.mode == MODE_MEGA && in0.wait_bar != NO_BAR) {
+          const uint32_t target = (gen + 1u) * in0.wait_target;
+          if (!(in0.wait_n == 1 && in0.wait_bar == ok_bar && target == ok_target)) {
+            const uint64_t t0 = globaltimer();
+            for (uint32_t k = 0; k < in0.wait_n && !aborted;) {
+              const uint32_t* c = &P.bars[in0.wait_bar + k * in0.wait_stride];
+              if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
+                ++k;
+                continue;
+              }
+              if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) aborted = 1;
+              else if (globaltimer() - t0 > P.wait_limit_ns) {
+                set_error(P, MK_ERR_TIMEOUT, iv);
+                aborted = 1;
+              } else {
+                __nanosleep(32);
+              }
+            }
+            if (!aborted && in0.wait_n == 1) {
+              ok_bar = in0.wait_bar;
+              ok_target = target;
+            }
+          }
+        }
+      }
+      S.flags[f_abort] = aborted;
+      if (aborted) S.flags[F_STOP] = 1u;  // the producer stops popping
+      if (P.trace) t_ready = globaltimer();
     }
     cbar();
-    const uint32_t i = S.flags[F_SLOT];
+    const uint32_t i = S.flags[f_slot];
     Instr in;
     AttnExt ext;
     ext.live = false;
@@ -927,49 +979,13 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       in = *slot_instr(S, si);
       if (in.op == OP_ATTN) ext = slot_get_ext(S, si);
     }
+    const bool aborted_now = S.flags[f_abort] != 0u;
     __syncwarp();
     if ((t & 31) == 0) mbar_arrive(&S.iempty[si]);
     ++islot_ctr;
     if (i == END_SLOT) break;
-    const uint64_t t_begin = P.trace ? globaltimer() : 0;
-
-    // wait on the tiles this instruction reads
-    // (the abort word is read only while spinning: a launch that never waits
-    // on an unsatisfied counter runs to completion anyway)
-    if (t == 0) {
-      uint32_t aborted = S.flags[F_STOP];
-      if (!aborted && P.mode == MODE_MEGA && in.wait_bar != NO_BAR) {
-        const uint32_t target = (gen + 1u) * in.wait_target;
-        if (!(in.wait_n == 1 && in.wait_bar == ok_bar && target == ok_target)) {
-          const uint64_t t0 = globaltimer();
-          for (uint32_t k = 0; k < in.wait_n && !aborted;) {
-            const uint32_t* c = &P.bars[in.wait_bar + k * in.wait_stride];
-            if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
-              ++k;
-              continue;
-            }
-            if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) aborted = 1;
-            else if (globaltimer() - t0 > P.wait_limit_ns) {
-              set_error(P, MK_ERR_TIMEOUT, i);
-              aborted = 1;
-            } else {
-              __nanosleep(32);
-            }
-          }
-          if (!aborted && in.wait_n == 1) {
-            ok_bar = in.wait_bar;
-            ok_target = target;
-          }
-        }
-      }
-      S.flags[F_ABORT] = aborted;
-      if (aborted) S.flags[F_STOP] = 1u;  // the producer stops popping
-    }
-    cbar();
-    const uint64_t t_ready = P.trace ? globaltimer() : 0;
-    if (S.flags[F_ABORT]) {
+    if (aborted_now) {
       drain(P, S, in, R);
-      cbar();
       continue;
     }
     if (in.op == OP_ATTN) {
@@ -1008,13 +1024,23 @@ __device__ void consumer(const KParams& P, const Sh& S) {
             gemv_fast<XH>(P, S, in, g, src, R, xh);
           }
           done = true;
+          // warp 0 alone holds the tile's sums (gemv_fast): it stores the
+          // outputs and releases the tile's counter
+          if (t < 32) {
+            gemv_epilogue(P, S, in, g, pre);
+            __syncwarp();
+            if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
+              red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+          }
         }
       }
-      if (!done) gemv_generic(P, S, in, g, src, R);
-      gemv_epilogue(P, S, in, g, pre);
-      cbar();
-      if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
-        red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+      if (!done) {
+        gemv_generic(P, S, in, g, src, R);
+        gemv_epilogue(P, S, in, g, pre);
+        cbar();
+        if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
+          red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+      }
     }
     if (P.trace && t == 0) {
       unsigned long long* tr = P.trace + (size_t)i * TRACE_WORDS;
@@ -1024,9 +1050,13 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       tr[3] = globaltimer();
       tr[5] = R.wait_ns;
       tr[6] = R.first_ns;
+      tr[8] = R.loop_ns;
+      tr[9] = R.red_ns;
     }
     R.wait_ns = 0;
     R.first_ns = 0;
+    R.loop_ns = 0;
+    R.red_ns = 0;
     // no barrier here: the next instruction's slot and dependency barriers
     // order every reuse of the shared scratch
   }

@@ -23,6 +23,7 @@ MK_ERR_UNSUPPORTED = 5
 MK_ERR_NO_DEVICE = 6
 MK_DECODE = 0
 MK_PREFILL = 1
+TRACE_WORDS = 12  # u64 words per trace record (mk_trace_copy)
 
 EXPORTED = [
     "mk_plan_create", "mk_plan_destroy", "mk_kv_cache_bytes", "mk_decode_step",
@@ -253,8 +254,8 @@ class Plan:
         """Trace records of the last traced launch as a numpy structured array."""
         import numpy as np
         n = self.stats().n_instr_decode
-        buf = np.zeros(n * 8, dtype=np.uint64)
+        buf = np.zeros(n * TRACE_WORDS, dtype=np.uint64)
         got = ctypes.c_size_t()
         _check(lib().mk_trace_copy(self.h, buf.ctypes.data, buf.nbytes, ctypes.byref(got)), "mk_trace_copy")
-        rec = buf[: got.value * 8].reshape(-1, 8)
+        rec = buf[: got.value * TRACE_WORDS].reshape(-1, TRACE_WORDS)
         return rec
