@@ -5,6 +5,7 @@ this package.  The product path never calls it and shares no code with it.
 """
 from .model import (  # noqa: F401
     widen_bf16,
+    round_bf16,
     rmsnorm,
     rope_rotate_half,
     rope_angles,

@@ -34,7 +34,9 @@ code shared with the GPU path):
 
 Precision: every step runs in `dtype` (float32 by default, float64 for the
 pins); weights and the cache arrive as bf16 bit patterns and are widened
-exactly.  The new token's K/V stay in `dtype` (never rounded to bf16).
+exactly.  The KV cache stores bf16, so the keys and values a step produces
+enter attention rounded to bf16 (nearest, ties to even), exactly as a later
+step reads them back from the cache; kv_bf16=False keeps them in `dtype`.
 
 Parity: pinned (closed forms, invariants, library special cases and brute
 force on tiny inputs) by tests/test_oracle_pins.py.
@@ -58,6 +60,20 @@ def widen_bf16(a) -> np.ndarray:
 
 def _f(a, dtype):
     return np.asarray(widen_bf16(a), dtype=dtype)
+
+
+def round_bf16(x, dtype=np.float32) -> np.ndarray:
+    """Nearest bf16 value of x (ties to the even significand), returned in dtype.
+
+    bf16 keeps 8 significant bits over float32's exponent range: writing
+    x = m * 2^e with 0.5 <= |m| < 1, the representable neighbours are multiples
+    of 2^(e - 8); below the smallest normal (2^-126) the spacing stays 2^-133.
+    np.rint rounds halves to even, which is IEEE round-to-nearest-even.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    return (np.rint(x / q) * q).astype(dtype)
 
 
 def rmsnorm(x, w, eps, dtype=np.float32) -> np.ndarray:
@@ -167,7 +183,7 @@ def _lm_weight(cfg, w):
     return w["embed"] if _cfg(cfg, "tied_embeddings") else w["lm_head"]
 
 
-def decode_step(cfg, w, tokens, positions, kv, dtype=np.float32):
+def decode_step(cfg, w, tokens, positions, kv, dtype=np.float32, kv_bf16: bool = True):
     """One decode step for B sequences.
 
     cfg: model shape (attributes or dict keys n_layers, hidden, n_q_heads,
@@ -177,6 +193,8 @@ def decode_step(cfg, w, tokens, positions, kv, dtype=np.float32):
     tokens, positions: [B] ints; sequence b sits in cache slot b.
     kv:  [n_layers][2][max_batch][n_kv][max_ctx][d] (bf16 bits or float); only
          positions < positions[b] of slot b are read.
+    kv_bf16: the new token's key and value enter attention as the bf16 cache
+         stores them (round_bf16); False keeps them in dtype.
     Returns (logits [B, vocab], k_new [L, B, n_kv, d], v_new [L, B, n_kv, d]).
     """
     L = _cfg(cfg, "n_layers")
@@ -207,6 +225,8 @@ def decode_step(cfg, w, tokens, positions, kv, dtype=np.float32):
                 kb = rmsnorm(kb, w[p + "k_norm"], eps, dtype)
             qb = rope_rotate_half(qb, pos, theta, dtype)
             kb = rope_rotate_half(kb, pos, theta, dtype)
+            if kv_bf16:
+                kb, vb = round_bf16(kb, dtype), round_bf16(vb, dtype)
             Kb = np.concatenate([_f(kv[l, 0, b, :, :pos, :], dtype), kb[:, None, :]], axis=1)
             Vb = np.concatenate([_f(kv[l, 1, b, :, :pos, :], dtype), vb[:, None, :]], axis=1)
             o[b] = gqa_attention(qb, Kb, Vb, dtype).reshape(-1)
@@ -221,11 +241,14 @@ def decode_step(cfg, w, tokens, positions, kv, dtype=np.float32):
     return logits, k_new, v_new
 
 
-def prefill(cfg, w, tokens, dtype=np.float32, all_logits: bool = False):
+def prefill(cfg, w, tokens, dtype=np.float32, all_logits: bool = False,
+            kv_bf16: bool = True):
     """Causal forward of one prompt at positions 0..S-1.
 
     Returns (logits, K, V): logits [vocab] of the last token (or [S, vocab] when
-    all_logits), K and V [L, n_kv, S, d] (post-RoPE keys, values).
+    all_logits), K and V [L, n_kv, S, d] (post-RoPE keys, values).  With
+    kv_bf16 the keys and values are rounded to bf16 (round_bf16) before the
+    attention reads them, as a bf16 KV cache holds them.
     """
     L = _cfg(cfg, "n_layers")
     nq, nkv, d = _cfg(cfg, "n_q_heads"), _cfg(cfg, "n_kv_heads"), _cfg(cfg, "head_dim")
@@ -249,6 +272,8 @@ def prefill(cfg, w, tokens, dtype=np.float32, all_logits: bool = False):
             k = rmsnorm(k, w[p + "k_norm"], eps, dtype)
         q = rope_rotate_half(q, pos[:, None], theta, dtype)
         k = rope_rotate_half(k, pos[:, None], theta, dtype)
+        if kv_bf16:
+            k, v = round_bf16(k, dtype), round_bf16(v, dtype)
         Kl = np.ascontiguousarray(k.transpose(1, 0, 2))         # [n_kv, S, d]
         Vl = np.ascontiguousarray(v.transpose(1, 0, 2))
         K_all[l] = Kl

@@ -58,6 +58,31 @@ def test_widen_bf16_exact():
     np.testing.assert_array_equal(oracle.widen_bf16(synth.bf16_bits(t)), t.float().numpy())
 
 
+def test_round_bf16_closed_forms():
+    r = lambda v: float(oracle.round_bf16(np.float64(v), F64))
+    u = 2.0 ** -7                          # bf16 spacing in [1, 2)
+    assert r(1.0) == 1.0 and r(0.0) == 0.0 and r(-3.0) == -3.0
+    assert r(1 + u / 2) == 1.0             # tie -> even significand (1.0)
+    assert r(1 + 3 * u / 2) == 1 + 2 * u   # tie -> even significand (1 + 2u)
+    assert r(1 + u / 2 + 2 ** -30) == 1 + u
+    assert r(-(1 + u / 2 + 2 ** -30)) == -(1 + u)
+    assert r(255.9) == 256.0               # carries into the next binade
+    assert r(2.0 ** -130) == 2.0 ** -130   # subnormal range, multiple of 2^-133
+    assert r(3 * 2.0 ** -134) == 2 * 2.0 ** -133   # 1.5 quanta -> tie -> even (2)
+    assert np.isinf(r(np.inf)) and np.isnan(r(np.nan))
+
+
+def test_round_bf16_vs_torch_conversion():
+    # torch's float32 -> bfloat16 cast is round-to-nearest-even
+    g = torch.Generator().manual_seed(7)
+    x = torch.cat([torch.randn(20000, generator=g) * 10.0 ** torch.randint(-30, 30, (20000,), generator=g),
+                   torch.tensor([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8)], dtype=torch.float32)])
+    want = x.to(torch.bfloat16).float().numpy()
+    got = oracle.round_bf16(x.numpy(), np.float32)
+    np.testing.assert_array_equal(got, want)
+    assert np.all((got.view(np.uint32) & 0xFFFF) == 0)   # representable in bf16
+
+
 # ---------------------------------------------------------------- RMSNorm
 
 def test_rmsnorm_constant_vector_closed_form():
@@ -298,9 +323,10 @@ def test_zeroed_output_projections_make_layers_identity():
     np.testing.assert_allclose(logits, ref, rtol=1e-12)
 
 
-def _torch_prefill(cfg, w, tokens):
+def _torch_prefill(cfg, w, tokens, kv_bf16=False):
     """Independent float64 forward from torch library ops (F.rms_norm, complex
-    RoPE via torch.polar, F.scaled_dot_product_attention, F.silu)."""
+    RoPE via torch.polar, F.scaled_dot_product_attention, F.silu); with kv_bf16
+    the keys and values pass through torch's bfloat16 cast first."""
     T = {k: torch.from_numpy(oracle.widen_bf16(v)).double() for k, v in w.items()}
     S, d = len(tokens), cfg.head_dim
     x = T["embed"][torch.as_tensor(tokens)]
@@ -321,6 +347,9 @@ def _torch_prefill(cfg, w, tokens):
             q = F.rms_norm(q, (d,), T[p + "q_norm"], eps=cfg.rms_eps)
             k = F.rms_norm(k, (d,), T[p + "k_norm"], eps=cfg.rms_eps)
         q, k = rope(q), rope(k)
+        if kv_bf16:
+            k = k.float().to(torch.bfloat16).double()
+            v = v.float().to(torch.bfloat16).double()
         rep = cfg.n_q_heads // cfg.n_kv_heads
         o = F.scaled_dot_product_attention(q, k.repeat_interleave(rep, 0), v.repeat_interleave(rep, 0),
                                            is_causal=True)
@@ -337,8 +366,22 @@ def test_prefill_vs_torch_library_forward(qk_norm, tied):
     cfg = TINY.replace(qk_norm=qk_norm, tied_embeddings=tied)
     w = _w(cfg, seed=1)
     toks = synth.make_tokens(11, cfg.vocab).numpy()
-    got, _, _ = oracle.prefill(cfg, w, toks, F64, all_logits=True)
+    got, _, _ = oracle.prefill(cfg, w, toks, F64, all_logits=True, kv_bf16=False)
     np.testing.assert_allclose(got, _torch_prefill(cfg, w, toks), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_prefill_bf16_cache_vs_torch_library_forward(qk_norm):
+    cfg = TINY.replace(qk_norm=qk_norm)
+    w = _w(cfg, seed=1)
+    toks = synth.make_tokens(11, cfg.vocab).numpy()
+    got, K, V = oracle.prefill(cfg, w, toks, F64, all_logits=True)
+    np.testing.assert_allclose(got, _torch_prefill(cfg, w, toks, kv_bf16=True), rtol=1e-10, atol=1e-12)
+    # the K/V handed back are the stored (bf16) values
+    assert np.all((K.astype(np.float32).view(np.uint32) & 0xFFFF) == 0)
+    assert np.all((V.astype(np.float32).view(np.uint32) & 0xFFFF) == 0)
+    plain, _, _ = oracle.prefill(cfg, w, toks, F64, all_logits=True, kv_bf16=False)
+    assert np.abs(plain - got).max() > 1e-6          # the rounding is not a no-op
 
 
 @pytest.mark.parametrize("qk_norm", [False, True])
@@ -408,3 +451,16 @@ def test_float32_close_to_float64():
     a, _, _ = oracle.decode_step(cfg, w, [4, 8], [19, 3], kv, np.float32)
     b, _, _ = oracle.decode_step(cfg, w, [4, 8], [19, 3], kv, F64)
     assert np.abs(a - b).max() <= 1e-4 * np.sqrt((b ** 2).mean())
+
+
+def test_decode_new_kv_is_the_rounded_value():
+    cfg = TINY.replace(qk_norm=True)
+    w = _w(cfg, seed=8)
+    kv = synth.bf16_bits(synth.make_kv_cache(cfg, 2, 12))
+    _, kn, vn = oracle.decode_step(cfg, w, [3, 9], [11, 0], kv, F64)
+    _, kp, vp = oracle.decode_step(cfg, w, [3, 9], [11, 0], kv, F64, kv_bf16=False)
+    # layer 0 computes the same k, v either way; later layers see the rounding
+    np.testing.assert_array_equal(kn[0], oracle.round_bf16(kp[0], F64))
+    np.testing.assert_array_equal(vn[0], oracle.round_bf16(vp[0], F64))
+    assert np.all((kn.astype(np.float32).view(np.uint32) & 0xFFFF) == 0)
+    assert np.abs(kn[0] - kp[0]).max() > 0
