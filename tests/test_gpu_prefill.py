@@ -2,10 +2,14 @@
 the C ABI, against the CPU oracle.
 
 Tolerances (written here): last-token logits per row within
-2e-2 * RMS(oracle logits); the K/V the prefill wrote into the cache (bf16)
-within 5e-2 * RMS of the oracle's K/V (bf16 GEMM operands and bf16 storage);
-prefill(S) followed by decode(1) against the oracle's prefill(S+1) within
-2e-2 * RMS.  Kernel-per-operator prefill is bit-identical to the persistent one.
+2e-2 * RMS(oracle logits); the K/V the prefill wrote into the cache are bf16
+values like the oracle's (which rounds them the same way): float32 rounding
+differences move a value across a bf16 rounding boundary now and then (one
+spacing, 2^-8..2^-7 relative, more often in later layers), so each element is
+within two spacings plus 2e-2 * RMS of the oracle's, and the RMS difference is
+below 3e-3 * RMS; prefill(S) followed by decode(1) against the
+oracle's prefill(S+1) within 2e-2 * RMS.  Kernel-per-operator prefill is
+bit-identical to the persistent one.
 """
 import numpy as np
 import pytest
@@ -37,6 +41,16 @@ def _rows_close(got, ref, tol=2e-2):
         rms = np.sqrt((ref[b] ** 2).mean())
         err = np.abs(got[b] - ref[b]).max()
         assert err <= tol * rms, f"max |delta| {err:.4e} > {tol} * rms {rms:.4e}"
+
+
+def _kv_close(name, gpu, orc):
+    gpu = np.asarray(gpu, np.float64)
+    orc = np.asarray(orc, np.float64)
+    rms = np.sqrt((orc ** 2).mean())
+    bad = np.abs(gpu - orc) > 2.0 ** -6 * np.abs(orc) + 2e-2 * rms
+    assert not bad.any(), f"{name}: {bad.sum()} elements off by more than two bf16 spacings"
+    drms = np.sqrt(((gpu - orc) ** 2).mean())
+    assert drms <= 3e-3 * rms, f"{name}: rms |delta| {drms:.3e} > 3e-3 * {rms:.3e}"
 
 
 class PfModel:
@@ -92,9 +106,7 @@ def test_prefill_matches_oracle(small, S):
     _rows_close(got, ref)
     kv = oracle.widen_bf16(synth.bf16_bits(small.kv))
     for name, gpu, orc in [("K", kv[:, 0, 0, :, :S, :], K), ("V", kv[:, 1, 0, :, :S, :], V)]:
-        rms = np.sqrt((orc.astype(np.float64) ** 2).mean())
-        err = np.abs(gpu - orc).max()
-        assert err <= 5e-2 * rms, f"{name}: max |delta| {err:.3e} > 5e-2 * {rms:.3e}"
+        _kv_close(name, gpu, orc)
 
 
 def test_prefill_then_decode_matches_longer_prefill(small):
@@ -133,7 +145,10 @@ def test_llama3_8b_width_prefill_2048_tokens():
     try:
         tokens = synth.make_tokens(2048, cfg.vocab).numpy()
         got = m.prefill(tokens)
-        ref, _, _ = m.oracle_prefill(tokens)
+        ref, K, V = m.oracle_prefill(tokens)
         _rows_close(got, ref)
+        kv = oracle.widen_bf16(synth.bf16_bits(m.kv))
+        _kv_close("K", kv[:, 0, 0, :, :2048, :], K)
+        _kv_close("V", kv[:, 1, 0, :, :2048, :], V)
     finally:
         m.close()

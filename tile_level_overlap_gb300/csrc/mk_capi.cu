@@ -405,11 +405,12 @@ static int prefill_init(mk_plan* p) {
   const size_t o_tm = bm.take(sizeof(CUtensorMap) * n_maps);
   const size_t o_xa = bm.take(sizeof(float) * rows * H);
   const size_t o_xb = bm.take(sizeof(float) * rows * H);
-  const size_t o_hn1 = bm.take(2 * rows * H);
-  const size_t o_hn2 = bm.take(2 * rows * H);
-  const size_t o_qb = bm.take(2 * rows * qd);
-  const size_t o_ao = bm.take(2 * rows * qd);
-  const size_t o_act = bm.take(2 * rows * F);
+  // hi and lo bf16 planes of each tensor-core activation operand
+  const size_t o_hn1 = bm.take(4 * rows * H);
+  const size_t o_hn2 = bm.take(4 * rows * H);
+  const size_t o_qb = bm.take(4 * rows * qd);
+  const size_t o_ao = bm.take(4 * rows * qd);
+  const size_t o_act = bm.take(4 * rows * F);
   if (cudaMalloc(&s.mem, bm.off) != cudaSuccess) {
     cudaGetLastError();
     s.mem = nullptr;
@@ -433,11 +434,11 @@ static int prefill_init(mk_plan* p) {
          make_tmap_bf16(t + TM_WD, w.wd, H, F, PF_BN);
   }
   CUtensorMap* a = &s.h_tm[L * TM_PER_LAYER];
-  ok = ok && make_tmap_bf16(a + AM_HN1, b + o_hn1, rows, H, PF_BM) &&
-       make_tmap_bf16(a + AM_HN2, b + o_hn2, rows, H, PF_BM) &&
-       make_tmap_bf16(a + AM_AO, b + o_ao, rows, qd, PF_BM) &&
-       make_tmap_bf16(a + AM_ACT, b + o_act, rows, F, PF_BM) &&
-       make_tmap_bf16(a + AM_Q, b + o_qb, rows, qd, PF_BM);
+  // each map spans both planes: the lo row of token row r is r + rows
+  ok = ok && make_tmap_bf16(a + AM_HN1, b + o_hn1, 2 * rows, H, PF_BM) &&
+       make_tmap_bf16(a + AM_HN2, b + o_hn2, 2 * rows, H, PF_BM) &&
+       make_tmap_bf16(a + AM_AO, b + o_ao, 2 * rows, qd, PF_BM) &&
+       make_tmap_bf16(a + AM_ACT, b + o_act, 2 * rows, F, PF_BM);
   if (!ok) return MK_ERR_CUDA;
   MK_CUDA(cudaMemcpy(b + o_q, pp.queue.data(), sizeof(Instr) * pp.queue.size(), cudaMemcpyHostToDevice));
   MK_CUDA(cudaMemcpy(b + o_expr, pp.expr.data(), sizeof(uint32_t) * pp.expr.size(),
@@ -460,6 +461,7 @@ static int prefill_init(mk_plan* p) {
   k.qb = (uint16_t*)(b + o_qb);
   k.ao = (uint16_t*)(b + o_ao);
   k.act = (uint16_t*)(b + o_act);
+  k.plane_rows = (int)rows;
   k.rope = p->base.rope;
   k.bars = (uint32_t*)(b + o_bars);
   k.ctl = (uint32_t*)(b + o_ctl);

@@ -150,8 +150,9 @@ enum Mode : int { MODE_MEGA = 0, MODE_PEROP = 1 };
 // satisfied, [3] done (released), [4] producer posted it, [5] ns the consumer
 // spent waiting for ring stages, [6] first stage available, [7] ns the producer
 // spent waiting for free ring stages while streaming it, [8] (batch-1 GEMV)
-// last stage consumed, [9] (batch-1 GEMV) cross-warp reduction done, [10] and
-// [11] unused.
+// last stage consumed and the tile handed to the finisher warp, [9] (batch-1
+// GEMV) the finisher took it, [10] and [11] unused.  For handed-off tiles [3]
+// is written by the finisher after its release.
 constexpr int TRACE_WORDS = 12;
 
 // Everything one launch needs, passed by value as a __grid_constant__ parameter.

@@ -36,13 +36,16 @@ struct SmemLayout {
   static constexpr int ring = 0;
   static constexpr int xbuf = ring + NSTAGE * STAGE_BYTES;
   static constexpr int red = xbuf + XBUF_BYTES;            // [RMAX][BMAX_CC] floats
-  static constexpr int redw = red + RMAX * BMAX_CC * 4;    // [NW][RMAX] floats
-  static constexpr int ssw = redw + NW * RMAX * 4;         // [NW][BMAX_CC] floats
+  static constexpr int redw = red + RMAX * BMAX_CC * 4;    // [2][NW][RMAX] floats (hand-off buffers)
+  static constexpr int fin = redw + 2 * NW * RMAX * 4;     // [RMAX][BMAX_CC] floats (finisher)
+  static constexpr int ssw = fin + RMAX * BMAX_CC * 4;     // [NW][BMAX_CC] floats
   static constexpr int bars = ssw + NW * BMAX_CC * 4;      // mbarriers
-  static constexpr int n_mbar = 2 * NSTAGE + 2 * NISLOT;
+  // full, empty [NSTAGE]; ifull, iempty [NISLOT]; hfull, hempty [2]
+  static constexpr int n_mbar = 2 * NSTAGE + 2 * NISLOT + 4;
   static constexpr int islot = bars + n_mbar * 8;          // [NISLOT] x {u32 index, pad, Instr}
   static constexpr int islot_bytes = 48;
-  static constexpr int flags = islot + NISLOT * islot_bytes;  // [8] u32
+  static constexpr int hrec = islot + NISLOT * islot_bytes;  // [2] x {u32 index, pad, Instr}
+  static constexpr int flags = hrec + 2 * islot_bytes;     // [8] u32
   static constexpr int layers = flags + 8 * 4;             // [MAX_LAYERS] LayerW
   static constexpr int total = layers + MAX_LAYERS * (int)sizeof(LayerW);
 };
@@ -57,12 +60,16 @@ struct Sh {
   float* xbuf;
   float* red;
   float* redw;
+  float* fin;
   float* ssw;
   uint64_t* full;
   uint64_t* empty;
   uint64_t* ifull;
   uint64_t* iempty;
+  uint64_t* hfull;   // a batch-1 GEMV tile's per-warp sums are ready (NW arrivals)
+  uint64_t* hempty;  // the finisher has read them (1 arrival)
   uint8_t* islot;
+  uint8_t* hrec;     // the handed-off instruction (index + record) per buffer
   volatile uint32_t* flags;
   const LayerW* layers;  // copy of the per-layer weight pointers
 };
@@ -80,13 +87,17 @@ __device__ __forceinline__ Sh sh_map(uint8_t* base) {
   s.xbuf = reinterpret_cast<float*>(base + SmemLayout::xbuf);
   s.red = reinterpret_cast<float*>(base + SmemLayout::red);
   s.redw = reinterpret_cast<float*>(base + SmemLayout::redw);
+  s.fin = reinterpret_cast<float*>(base + SmemLayout::fin);
   s.ssw = reinterpret_cast<float*>(base + SmemLayout::ssw);
   uint64_t* b = reinterpret_cast<uint64_t*>(base + SmemLayout::bars);
   s.full = b;
   s.empty = b + NSTAGE;
   s.ifull = b + 2 * NSTAGE;
   s.iempty = b + 2 * NSTAGE + NISLOT;
+  s.hfull = b + 2 * NSTAGE + 2 * NISLOT;
+  s.hempty = s.hfull + 2;
   s.islot = base + SmemLayout::islot;
+  s.hrec = base + SmemLayout::hrec;
   s.layers = reinterpret_cast<const LayerW*>(base + SmemLayout::layers);
   s.flags = reinterpret_cast<volatile uint32_t*>(base + SmemLayout::flags);
   return s;
@@ -341,10 +352,10 @@ __device__ void producer(const KParams& P, const Sh& S) {
 // ---------------------------------------------------------------- consumer helpers
 struct Ring {
   uint32_t ctr;           // stages consumed so far
+  uint32_t hctr;          // batch-1 GEMV tiles handed to the finisher so far
   uint64_t wait_ns;       // (tracing, thread 0) time spent waiting for stages
   uint64_t first_ns;      // (tracing, thread 0) when the instruction's first stage was ready
-  uint64_t loop_ns;       // (tracing, thread 0) when the last stage was consumed
-  uint64_t red_ns;        // (tracing, thread 0) when the cross-warp reduction finished
+  uint64_t loop_ns;       // (tracing, thread 0) when a batch-1 GEMV tile was handed off
 };
 
 __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
@@ -464,9 +475,36 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
   }
 }
 
+// Hand-off buffers between the consumers and the finisher warp: record `hb`
+// holds the instruction whose per-warp sums sit in redw[hb].
+__device__ __forceinline__ volatile uint32_t* hrec_index(const Sh& S, int hb) {
+  return reinterpret_cast<volatile uint32_t*>(S.hrec + hb * SmemLayout::islot_bytes);
+}
+__device__ __forceinline__ Instr* hrec_instr(const Sh& S, int hb) {
+  return reinterpret_cast<Instr*>(S.hrec + hb * SmemLayout::islot_bytes + 16);
+}
+// Every consumer warp: wait until the finisher has read buffer R.hctr & 1
+// (used two hand-offs ago, so normally long free).
+__device__ __forceinline__ int handoff_acquire(const KParams& P, const Sh& S, const Ring& R) {
+  const int hb = (int)(R.hctr & 1u);
+  if ((threadIdx.x & 31) == 0) mbar_wait(P, &S.hempty[hb], ((R.hctr >> 1) & 1u) ^ 1u);
+  __syncwarp();
+  return hb;
+}
+// Every consumer warp, after its sums (and, in warp 0, the record) are written.
+__device__ __forceinline__ void handoff_commit(const Sh& S, Ring& R, int hb) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&S.hfull[hb]);
+  ++R.hctr;
+}
+
+// Batch-1 GEMV tile: streams the tile's rows and leaves one partial sum per
+// (warp, row) in a hand-off buffer; the finisher warp adds them up, runs the
+// epilogue and releases the tile, so the consumers go straight on to the next
+// instruction.
 template <int M>
 __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in,
-                                          const GemvDesc& g, const Src& src, Ring& R,
+                                          uint32_t ii, const GemvDesc& g, const Src& src, Ring& R,
                                           const float (&xr)[M][8]) {
   // rows per 32 KB stage at K = M * 2048 (the plan's src.rps for these K)
   constexpr int RPS = (8 / M) > 0 ? (8 / M) : 1;
@@ -474,7 +512,8 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int K = g.K;
   const int rows0 = (int)src.rows[0];
-  const int ntot = src.nreg == 2 ? 2 * rows0 : rows0;
+  const int hb = handoff_acquire(P, S, R);
+  float* redw = S.redw + hb * NW * RMAX;
   int tile_row = 0;
 #pragma unroll 1
   for (int r = 0; r < src.nreg; ++r) {
@@ -496,29 +535,22 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
       ring_release(S, R);
       if constexpr (RPS == 1) {
         const float v = warp_sum(acc[0]);
-        if (lane == 0) S.redw[w * RMAX + tile_row] = v;
+        if (lane == 0) redw[w * RMAX + tile_row] = v;
       } else {
         const float v = warp_reduce_multi<RPS>(acc, lane);
         const int idx = warp_multi_index<RPS>(lane);
-        if ((lane & (kDup - 1)) == 0 && idx < n) S.redw[w * RMAX + tile_row + idx] = v;
+        if ((lane & (kDup - 1)) == 0 && idx < n) redw[w * RMAX + tile_row + idx] = v;
       }
       tile_row += n;
     }
   }
-  if (P.trace && t == 0) R.loop_ns = globaltimer();
-  cbar();
-  if (P.trace && t == 0) R.red_ns = globaltimer();
-  // Only warp 0 finishes the tile (rows <= RMAX = 32 at batch 1): it sums the
-  // warps' partials, and the caller runs the epilogue and the release in the
-  // same warp, so the other warps move on to the next instruction.
-  if (w != 0) return;
-  if (t < ntot) {
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < NW; ++k) s += S.redw[k * RMAX + t];
-    S.red[t * BMAX_CC] = s;
+  if (t == 0) {
+    if (P.trace) R.loop_ns = globaltimer();
+    *hrec_instr(S, hb) = in;
+    *hrec_index(S, hb) = ii;
   }
-  __syncwarp();
+  (void)w;
+  handoff_commit(S, R, hb);
 }
 
 // ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
@@ -591,8 +623,8 @@ __device__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, con
 // is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
 // (RMAX * BMAX_CC <= NT).
 __device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr& in,
-                                                   const GemvDesc& g) {
-  const int t = threadIdx.x, B = P.B, l = in.layer;
+                                                   const GemvDesc& g, int t) {
+  const int B = P.B, l = in.layer;
   if (t >= g.rows * B) return 0.f;
   const int r = t / B, b = t % B, row = g.row0 + r;
   const size_t bh = (size_t)P.max_batch * P.H;
@@ -604,15 +636,16 @@ __device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr
   return 0.f;
 }
 
-// Store a finished GEMV tile: y[r][b] is in S.red; `pre` is this thread's
-// residual input from epilogue_prefetch.
-__device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
-                              float pre) {
-  const int t = threadIdx.x, B = P.B, l = in.layer;
+// Store a finished GEMV tile: y[r][b] is in red[r * BMAX_CC + b]; `t` is the
+// (row, sequence) slot of this thread and `pre` its residual input from
+// epilogue_prefetch.
+__device__ void gemv_epilogue(const KParams& P, const float* red, const Instr& in, const GemvDesc& g,
+                              float pre, int t) {
+  const int B = P.B, l = in.layer;
   if (t >= g.rows * B) return;
   const int r = t / B, b = t % B, row = g.row0 + r;
   const size_t bh = (size_t)P.max_batch * P.H;
-  const float y = S.red[r * BMAX_CC + b];
+  const float y = red[r * BMAX_CC + b];
   switch (in.op) {
     case OP_QKV:
       P.qkv[((size_t)l * P.max_batch + b) * P.qkv_rows + row] = y;
@@ -621,7 +654,7 @@ __device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, co
       P.resid[(size_t)(2 * l + 1) * bh + (size_t)b * P.H + row] = pre + y;
       break;
     case OP_GU: {
-      const float u = S.red[(g.rows + r) * BMAX_CC + b];
+      const float u = red[(g.rows + r) * BMAX_CC + b];
       P.act[((size_t)l * P.max_batch + b) * P.F + row] = y / (1.0f + expf(-y)) * u;
       break;
     }
@@ -634,10 +667,15 @@ __device__ void gemv_epilogue(const KParams& P, const Sh& S, const Instr& in, co
   }
 }
 
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 // ---------------------------------------------------------------- decode attention (split-KV)
 // One (sequence, kv head, split): the split's cached keys stream through the
 // ring; the new token's key/value come from the QKV output (normed when q/k
-// norm is on, rotated, written to the cache by the split that holds slot pos).
+// norm is on, rotated, rounded to bf16 like every cached entry, written to the
+// cache by the split that holds slot pos).
 // Partial (max, sum, unnormalised o) per q head; the last split to arrive
 // combines all splits of the group in split order.
 template <int D, int REP>
@@ -669,7 +707,7 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
     for (int i = t; i < rep * D; i += NT) qs[i] = __ldcg(base + g * rep * D + i);
     for (int i = t; i < D; i += NT) {
       kn[i] = __ldcg(base + qd + g * D + i);
-      vn[i] = __ldcg(base + qd + P.nkv * D + g * D + i);
+      vn[i] = round_bf16(__ldcg(base + qd + P.nkv * D + g * D + i));
     }
     cbar();
     if (P.qk_norm) {
@@ -693,8 +731,10 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
         const int h = i / (D / 2), k = i % (D / 2);
         float* u = h < rep ? qs + h * D : kn;
         const float u1 = u[k], u2 = u[k + D / 2];
-        u[k] = u1 * cs[j].x - u2 * cs[j].y;
-        u[k + D / 2] = u2 * cs[j].x + u1 * cs[j].y;
+        const float r1 = u1 * cs[j].x - u2 * cs[j].y, r2 = u2 * cs[j].x + u1 * cs[j].y;
+        // the new key enters attention as the bf16 cache stores it
+        u[k] = h < rep ? r1 : round_bf16(r1);
+        u[k + D / 2] = h < rep ? r2 : round_bf16(r2);
       }
     }
     cbar();
@@ -1005,7 +1045,6 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      const float pre = epilogue_prefetch(P, in, g);
       bool done = false;
       if constexpr (MH > 0) {
         if (P.B == 1) {
@@ -1015,28 +1054,21 @@ __device__ void consumer(const KParams& P, const Sh& S) {
               load_x_fast<XF>(P, S, in, xf);
               tag_f = tag;
             }
-            gemv_fast<XF>(P, S, in, g, src, R, xf);
+            gemv_fast<XF>(P, S, in, i, g, src, R, xf);
           } else {
             if (tag != tag_h) {
               load_x_fast<XH>(P, S, in, xh);
               tag_h = tag;
             }
-            gemv_fast<XH>(P, S, in, g, src, R, xh);
+            gemv_fast<XH>(P, S, in, i, g, src, R, xh);
           }
-          done = true;
-          // warp 0 alone holds the tile's sums (gemv_fast): it stores the
-          // outputs and releases the tile's counter
-          if (t < 32) {
-            gemv_epilogue(P, S, in, g, pre);
-            __syncwarp();
-            if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
-              red_release_gpu_add(&P.bars[in.rel_bar], 1u);
-          }
+          done = true;  // the finisher stores and releases it
         }
       }
       if (!done) {
+        const float pre = epilogue_prefetch(P, in, g, t);
         gemv_generic(P, S, in, g, src, R);
-        gemv_epilogue(P, S, in, g, pre);
+        gemv_epilogue(P, S.red, in, g, pre, t);
         cbar();
         if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
           red_release_gpu_add(&P.bars[in.rel_bar], 1u);
@@ -1047,18 +1079,59 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       tr[0] = (unsigned long long)smid() | ((unsigned long long)(in.op | (in.layer << 8)) << 32);
       tr[1] = t_begin;
       tr[2] = t_ready;
-      tr[3] = globaltimer();
+      if (!R.loop_ns) tr[3] = globaltimer();  // handed-off tiles: the finisher writes it
       tr[5] = R.wait_ns;
       tr[6] = R.first_ns;
       tr[8] = R.loop_ns;
-      tr[9] = R.red_ns;
     }
     R.wait_ns = 0;
     R.first_ns = 0;
     R.loop_ns = 0;
-    R.red_ns = 0;
     // no barrier here: the next instruction's slot and dependency barriers
     // order every reuse of the shared scratch
+  }
+  // tell the finisher that no more tiles come
+  const int hb = handoff_acquire(P, S, R);
+  if (t == 0) *hrec_index(S, hb) = END_SLOT;
+  handoff_commit(S, R, hb);
+}
+
+// ---------------------------------------------------------------- finisher warp
+// Takes the batch-1 GEMV tiles in hand-off order: adds up the consumer warps'
+// partial sums (fixed order), frees the buffer, stores the outputs (residual
+// adds, SwiGLU) and releases the tile's counter.  Its store latency and the
+// release fence stay off the consumers' path.
+__device__ void finisher(const KParams& P, const Sh& S) {
+  const int lane = threadIdx.x & 31;
+  for (uint32_t h = 0;; ++h) {
+    const int hb = (int)(h & 1u);
+    if (!mbar_wait(P, &S.hfull[hb], (h >> 1) & 1u)) break;
+    const uint32_t ii = *hrec_index(S, hb);
+    if (ii == END_SLOT) break;
+    const Instr in = *hrec_instr(S, hb);
+    const uint64_t t_take = P.trace ? globaltimer() : 0;
+    const GemvDesc g = gemv_desc(P, in);
+    const int ntot = g.w1 ? 2 * g.rows : g.rows;
+    const float* redw = S.redw + hb * NW * RMAX;
+    if (lane < ntot) {
+      float s = 0.f;
+#pragma unroll
+      for (int k = 0; k < NW; ++k) s += redw[k * RMAX + lane];
+      S.fin[lane * BMAX_CC] = s;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.hempty[hb]);
+    const float pre = epilogue_prefetch(P, in, g, lane);
+    gemv_epilogue(P, S.fin, in, g, pre, lane);
+    __syncwarp();
+    if (lane == 0) {
+      if (P.mode == MODE_MEGA && in.rel_bar != NO_BAR) red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+      if (P.trace) {
+        unsigned long long* tr = P.trace + (size_t)ii * TRACE_WORDS;
+        tr[9] = t_take;
+        tr[3] = globaltimer();
+      }
+    }
   }
 }
 
@@ -1076,6 +1149,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
       mbar_init(&S.ifull[s], 1);
       mbar_init(&S.iempty[s], NW);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.hfull[b], NW);
+      mbar_init(&S.hempty[b], 1);
+    }
     fence_mbar_init();
     fence_proxy_async_smem();
     S.flags[F_GEN] = P.mode == MODE_MEGA ? ld_volatile(&P.ctl[CTL_GEN]) : 0u;
@@ -1088,7 +1165,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
     for (int i = t; i < words; i += NTHREADS) dst[i] = src[i];
   }
   __syncthreads();
-  if (t >= NT) producer(P, S);
+  if (t >= NT + 32) finisher(P, S);
+  else if (t >= NT) producer(P, S);
   else consumer<MH, MF, AD, AREP>(P, S);
   __syncthreads();
   if (t == 0 && P.mode == MODE_MEGA) {

@@ -15,7 +15,7 @@ namespace mk {
 // Kernel geometry shared by the plan builder and the kernel.
 constexpr int NW = 8;                 // consumer warps per CTA
 constexpr int NT = NW * 32;           // consumer threads
-constexpr int NTHREADS = NT + 32;     // + one producer warp
+constexpr int NTHREADS = NT + 64;     // + one producer warp + one finisher warp
 constexpr int NSTAGE = 6;             // weight/KV ring stages
 constexpr int STAGE_BYTES = 32768;    // bytes per ring stage
 constexpr int NISLOT = 8;             // instruction slots between producer and consumers

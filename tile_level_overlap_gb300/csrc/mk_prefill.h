@@ -56,7 +56,7 @@ struct PrefillPlan {
 // then the activation maps at L * 8 + AM_*.
 enum PfWeightMap { TM_WQ = 0, TM_WK = 1, TM_WV = 2, TM_WO = 3, TM_WG = 4, TM_WU = 5, TM_WD = 6,
                    TM_PER_LAYER = 8 };
-enum PfActMap { AM_HN1 = 0, AM_HN2 = 1, AM_AO = 2, AM_ACT = 3, AM_Q = 4, AM_KV = 5, AM_COUNT = 6 };
+enum PfActMap { AM_HN1 = 0, AM_HN2 = 1, AM_AO = 2, AM_ACT = 3, AM_KV = 4, AM_COUNT = 5 };
 
 // Everything one prefill launch needs (passed by value).
 struct PfParams {
@@ -68,11 +68,16 @@ struct PfParams {
   const void* tm;           // CUtensorMap table (64-byte aligned)
   float* xa;                // residual after attention, f32 [rows][H]
   float* xb;                // residual after the FFN, f32 [rows][H]
-  uint16_t* hn1;            // bf16 RMSNorm outputs [rows][H]
+  // Tensor-core operands carried as two bf16 planes, [2][rows][cols]: the
+  // nearest bf16 (hi) and the bf16 of the remainder (lo), so hi + lo holds
+  // ~16 significant bits and an MMA pair (hi, lo) against the exact bf16
+  // weights keeps the activation's float32 precision.
+  uint16_t* hn1;            // RMSNorm outputs [2][rows][H]
   uint16_t* hn2;
-  uint16_t* qb;             // bf16 rotated queries [rows][n_q * d]
-  uint16_t* ao;             // bf16 attention outputs [rows][n_q * d]
-  uint16_t* act;            // bf16 SwiGLU outputs [rows][F]
+  uint16_t* qb;             // rotated queries [2][rows][n_q * d]
+  uint16_t* ao;             // attention outputs [2][rows][n_q * d]
+  uint16_t* act;            // SwiGLU outputs [2][rows][F]
+  int plane_rows;           // rows of one plane (token blocks x 128)
   uint16_t* kv;             // caller's KV cache (sequence slot 0 is written)
   const float2* rope;       // (cos, sin) [max_ctx][d / 2]
   uint32_t* bars;

@@ -4,13 +4,20 @@
 //  warp 0      producer: pops instructions (one atomic each), streams weight
 //              k-blocks ahead of the instruction's dependencies and activation
 //              k-blocks once they are satisfied (acquire + async-proxy fence),
-//              all with 2D TMA loads into a 4 x 48 KB ring.
+//              all with 2D TMA loads into a 3 x 64 KB ring.
 //  warp 1      tensor-core issuer: owns 512 TMEM columns (two 128 x 256 f32
 //              accumulators), issues tcgen05.mma and commits to mbarriers.
 //  warps 2-5   compute: GEMM epilogues (RoPE + K/V cache write, residual adds,
 //              SwiGLU), RMSNorm blocks, and the softmax half of causal
-//              attention (S = Q K^T and O = P V run on the tensor cores, P is
-//              written into TMEM as the A operand).
+//              attention (S = Q K^T and O = P V run on the tensor cores, Q and
+//              P are written into TMEM as the A operand).
+//
+// Precision: every activation operand of a tensor-core product is split into
+// two bf16 values, hi = bf16(x) and lo = bf16(x - hi), and multiplied as two
+// MMAs into the same float32 accumulator.  The weights are bf16 already and
+// the keys and values are the bf16 cache entries, so every product carries
+// float32-level precision; one bf16 rounding per operand would not (its error
+// grows to a few percent of the logits' RMS after two layers).
 //
 // "MegaOps" (Abstract): a consumer waits only on the tiles it reads (here:
 // attention of block m on the QKV tiles of blocks <= m, the next layer's norm
@@ -30,8 +37,10 @@
 namespace mk {
 namespace {
 
-constexpr int PF_STAGE = 48 * 1024;    // A 16 KB + B 32 KB
-constexpr int PF_NSTAGE = 4;
+// GEMM stage: A hi 16 KB | A lo 16 KB | B 32 KB.  Attention stage: K_j | V_j.
+constexpr int PF_STAGE = 64 * 1024;
+constexpr int PF_NSTAGE = 3;
+constexpr uint32_t PF_A_BYTES = PF_BM * PF_BK * 2;
 constexpr int PF_THREADS = 192;
 constexpr int PF_CBAR = 2;             // named barrier of the compute warps
 constexpr int PF_NC = 128;             // compute threads
@@ -39,10 +48,9 @@ constexpr uint32_t PF_END = 0xffffffffu;
 
 struct PfSmem {
   static constexpr int ring = 0;
-  static constexpr int qbuf = ring + PF_NSTAGE * PF_STAGE;  // 32 KB: Q of one head
-  static constexpr int bars = qbuf + 32768;
-  // full[4] empty[4] ifull[8] iempty[8] accf[2] acce[2] qfull qempty sfull pfull ofull
-  static constexpr int n_mbar = 2 * PF_NSTAGE + 2 * NISLOT + 4 + 5;
+  static constexpr int bars = ring + PF_NSTAGE * PF_STAGE;
+  // full[3] empty[3] ifull[8] iempty[8] accf[2] acce[2] qfull sfull pfull ofull
+  static constexpr int n_mbar = 2 * PF_NSTAGE + 2 * NISLOT + 4 + 4;
   static constexpr int islot = bars + n_mbar * 8;
   static constexpr int flags = islot + NISLOT * 48;          // [16] u32
   static constexpr int scratch = flags + 16 * 4;             // [128] f32
@@ -54,8 +62,7 @@ enum PfFlag { PFF_GEN = 0, PFF_SLOT = 1, PFF_ABORT = 2, PFF_TMEM = 3 };
 
 struct PfSh {
   uint8_t* ring;
-  uint8_t* qbuf;
-  uint64_t *full, *empty, *ifull, *iempty, *accf, *acce, *qfull, *qempty, *sfull, *pfull, *ofull;
+  uint64_t *full, *empty, *ifull, *iempty, *accf, *acce, *qfull, *sfull, *pfull, *ofull;
   uint8_t* islot;
   volatile uint32_t* flags;
   float* scratch;
@@ -64,7 +71,6 @@ struct PfSh {
 __device__ __forceinline__ PfSh pf_map(uint8_t* base) {
   PfSh s;
   s.ring = base + PfSmem::ring;
-  s.qbuf = base + PfSmem::qbuf;
   uint64_t* b = reinterpret_cast<uint64_t*>(base + PfSmem::bars);
   s.full = b;
   s.empty = b + PF_NSTAGE;
@@ -73,8 +79,7 @@ __device__ __forceinline__ PfSh pf_map(uint8_t* base) {
   s.accf = s.iempty + NISLOT;
   s.acce = s.accf + 2;
   s.qfull = s.acce + 2;
-  s.qempty = s.qfull + 1;
-  s.sfull = s.qempty + 1;
+  s.sfull = s.qfull + 1;
   s.pfull = s.sfull + 1;
   s.ofull = s.pfull + 1;
   s.islot = base + PfSmem::islot;
@@ -213,7 +218,7 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
   const uint64_t pol_w = policy_evict_first();  // weights: streamed
   const uint64_t pol_a = policy_evict_last();   // activations / KV: re-read by other tiles
   const uint32_t gen = S.flags[PFF_GEN];
-  uint32_t stage_ctr = 0, islot_ctr = 0, qctr = 0;
+  uint32_t stage_ctr = 0, islot_ctr = 0;
   bool first = true;
   for (;;) {
     uint32_t i;
@@ -242,67 +247,64 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
       const PfGemm g = pf_gemm(P, in);
       const int nk = g.K / PF_BK;
       const int npre = nk < PF_NSTAGE ? nk : PF_NSTAGE;
-      const uint32_t a_bytes = PF_BM * PF_BK * 2;
       const uint32_t b_bytes = (uint32_t)g.bn * PF_BK * 2;
+      const uint32_t tx = 2 * PF_A_BYTES + b_bytes;
       const uint32_t s0 = stage_ctr;
       // weights first: they depend on nothing
       for (int kb = 0; kb < npre; ++kb) {
         const int st = stage_ctr % PF_NSTAGE;
         pf_wait(P, &S.empty[st], ((stage_ctr / PF_NSTAGE) & 1u) ^ 1u);
-        uint8_t* sp = S.ring + st * PF_STAGE;
-        mbar_arrive_expect_tx(&S.full[st], a_bytes + b_bytes);
-        tma_load_2d(sp + a_bytes, tmap(P, g.b_map0), kb * PF_BK, g.b_row0, &S.full[st], pol_w);
+        uint8_t* sp = S.ring + st * PF_STAGE + 2 * PF_A_BYTES;
+        mbar_arrive_expect_tx(&S.full[st], tx);
+        tma_load_2d(sp, tmap(P, g.b_map0), kb * PF_BK, g.b_row0, &S.full[st], pol_w);
         if (g.b_map1 >= 0)
-          tma_load_2d(sp + a_bytes + g.b_rows0 * 128, tmap(P, g.b_map1), kb * PF_BK, g.b_row1,
-                      &S.full[st], pol_w);
+          tma_load_2d(sp + g.b_rows0 * 128, tmap(P, g.b_map1), kb * PF_BK, g.b_row1, &S.full[st], pol_w);
         ++stage_ctr;
       }
       // (after a timeout the loads still run -- on stale but valid memory -- so
       // that every armed stage completes and the launch can drain)
       pf_wait_deps(P, in, gen, i);
       fence_proxy_async_global();
-      const int arow = (int)in.a0 * PF_BM;
+      const int arow = (int)in.a0 * PF_BM, lrow = arow + P.plane_rows;
       for (int kb = 0; kb < npre; ++kb) {
-        const int st = (s0 + kb) % PF_NSTAGE;
-        tma_load_2d(S.ring + st * PF_STAGE, tmap(P, g.a_map), kb * PF_BK, arow, &S.full[st], pol_a);
+        uint8_t* sp = S.ring + ((s0 + kb) % PF_NSTAGE) * PF_STAGE;
+        uint64_t* fb = &S.full[(s0 + kb) % PF_NSTAGE];
+        tma_load_2d(sp, tmap(P, g.a_map), kb * PF_BK, arow, fb, pol_a);
+        tma_load_2d(sp + PF_A_BYTES, tmap(P, g.a_map), kb * PF_BK, lrow, fb, pol_a);
       }
       for (int kb = npre; kb < nk; ++kb) {
         const int st = stage_ctr % PF_NSTAGE;
         pf_wait(P, &S.empty[st], ((stage_ctr / PF_NSTAGE) & 1u) ^ 1u);
         uint8_t* sp = S.ring + st * PF_STAGE;
-        mbar_arrive_expect_tx(&S.full[st], a_bytes + b_bytes);
-        tma_load_2d(sp + a_bytes, tmap(P, g.b_map0), kb * PF_BK, g.b_row0, &S.full[st], pol_w);
+        mbar_arrive_expect_tx(&S.full[st], tx);
+        tma_load_2d(sp + 2 * PF_A_BYTES, tmap(P, g.b_map0), kb * PF_BK, g.b_row0, &S.full[st], pol_w);
         if (g.b_map1 >= 0)
-          tma_load_2d(sp + a_bytes + g.b_rows0 * 128, tmap(P, g.b_map1), kb * PF_BK, g.b_row1,
+          tma_load_2d(sp + 2 * PF_A_BYTES + g.b_rows0 * 128, tmap(P, g.b_map1), kb * PF_BK, g.b_row1,
                       &S.full[st], pol_w);
         tma_load_2d(sp, tmap(P, g.a_map), kb * PF_BK, arow, &S.full[st], pol_a);
+        tma_load_2d(sp + PF_A_BYTES, tmap(P, g.a_map), kb * PF_BK, lrow, &S.full[st], pol_a);
         ++stage_ctr;
       }
     } else if (in.op == PF_ATTN) {
       pf_wait_deps(P, in, gen, i);
       fence_proxy_async_global();
+      // one stage per key block: K_j at +0, V_j at +tile (Q goes to TMEM
+      // through the compute warps)
       const int m = (int)in.a0, gq = (int)in.a1, l = in.layer;
       const uint32_t tile = PF_BM * P.d * 2;  // one 128-row tile of d columns
       const int nbox = P.d / 64;
-      for (int h = 0; h < P.rep; ++h) {
-        pf_wait(P, S.qempty, (qctr & 1u) ^ 1u);
-        ++qctr;
-        mbar_arrive_expect_tx(S.qfull, tile);
-        for (int bx = 0; bx < nbox; ++bx)
-          tma_load_2d(S.qbuf + bx * 16384, tmap(P, am(P, AM_Q)), (gq * P.rep + h) * P.d + bx * 64,
-                      m * PF_BM, S.qfull, pol_a);
-        for (int j = 0; j <= m; ++j)
-          for (int kvsel = 0; kvsel < 2; ++kvsel) {
-            const int st = stage_ctr % PF_NSTAGE;
-            pf_wait(P, &S.empty[st], ((stage_ctr / PF_NSTAGE) & 1u) ^ 1u);
-            uint8_t* sp = S.ring + st * PF_STAGE;
-            mbar_arrive_expect_tx(&S.full[st], tile);
+      for (int h = 0; h < P.rep; ++h)
+        for (int j = 0; j <= m; ++j) {
+          const int st = stage_ctr % PF_NSTAGE;
+          pf_wait(P, &S.empty[st], ((stage_ctr / PF_NSTAGE) & 1u) ^ 1u);
+          uint8_t* sp = S.ring + st * PF_STAGE;
+          mbar_arrive_expect_tx(&S.full[st], 2 * tile);
+          for (int kvsel = 0; kvsel < 2; ++kvsel)
             for (int bx = 0; bx < nbox; ++bx)
-              tma_load_2d(sp + bx * 16384, tmap(P, am(P, AM_KV)), bx * 64,
+              tma_load_2d(sp + kvsel * tile + bx * 16384, tmap(P, am(P, AM_KV)), bx * 64,
                           kv_row(P, l, kvsel, gq) + j * PF_BM, &S.full[st], pol_a);
-            ++stage_ctr;
-          }
-      }
+          ++stage_ctr;
+        }
     }
   }
   // Before leaving, make sure the copies this thread issued have landed
@@ -311,7 +313,6 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
     const uint32_t c = stage_ctr - 1 - k;
     pf_wait(P, &S.full[c % PF_NSTAGE], (c / PF_NSTAGE) & 1u);
   }
-  if (qctr) pf_wait(P, S.qfull, (qctr - 1) & 1u);
 }
 
 // ---------------------------------------------------------------- tensor-core issuer
@@ -343,58 +344,61 @@ __device__ void pf_mma(const PfParams& P, const PfSh& S, uint32_t tbase) {
         ++stage_ctr;
         tc_fence_after();
         const uint32_t a0 = smem_u32(S.ring + st * PF_STAGE);
-        const uint32_t b0 = a0 + PF_BM * PF_BK * 2;
+        const uint32_t a1 = a0 + PF_A_BYTES, b0 = a0 + 2 * PF_A_BYTES;
 #pragma unroll
-        for (int k = 0; k < PF_BK / 16; ++k)
-          tc_mma(d, sdesc_sw128(a0 + 32 * k), sdesc_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+        for (int k = 0; k < PF_BK / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(b0 + 32 * k);
+          tc_mma(d, sdesc_sw128(a0 + 32 * k), bd, idesc, (kb | k) != 0);
+          tc_mma(d, sdesc_sw128(a1 + 32 * k), bd, idesc, true);
+        }
         tc_commit(&S.empty[st]);
       }
       tc_commit(&S.accf[ab]);
     } else if (in.op == PF_ATTN) {
-      // attention takes both accumulators: S at +0, O at +128, P at +256
+      // attention takes both accumulators: S at +0, O at +128, P hi/lo at
+      // +256/+320, Q hi/lo at +384/+448 (bf16 pairs, 16 elements per 8 columns)
       for (int b = 0; b < 2; ++b) {
         pf_wait(P, &S.acce[b], (use[b] & 1u) ^ 1u);
         ++use[b];
       }
       tc_fence_after();
       const int m = (int)in.a0;
-      const uint32_t s_t = tbase, o_t = tbase + 128, p_t = tbase + 256;
+      const uint32_t s_t = tbase, o_t = tbase + 128, p_t = tbase + 256, pl_t = tbase + 320;
+      const uint32_t q_t = tbase + 384, ql_t = tbase + 448;
       const uint32_t id_s = idesc_bf16_f32(PF_BM, PF_BM);
       const uint32_t id_o = idesc_bf16_f32(PF_BM, P.d, true);
-      const uint32_t qa = smem_u32(S.qbuf);
+      const uint32_t tile = PF_BM * P.d * 2;
       for (int h = 0; h < P.rep; ++h) {
         pf_wait(P, S.qfull, qctr & 1u);
         ++qctr;
         tc_fence_after();
         for (int j = 0; j <= m; ++j) {
           // S = Q K_j^T (K = head_dim, in 64-column atoms 16 KB apart)
-          int st = stage_ctr % PF_NSTAGE;
+          const int st = stage_ctr % PF_NSTAGE;
           pf_wait(P, &S.full[st], (stage_ctr / PF_NSTAGE) & 1u);
           ++stage_ctr;
           tc_fence_after();
           const uint32_t kb0 = smem_u32(S.ring + st * PF_STAGE);
           for (int kk = 0; kk < P.d / 16; ++kk) {
-            const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
-            tc_mma(s_t, sdesc_sw128(qa + off), sdesc_sw128(kb0 + off), id_s, kk != 0);
+            const uint64_t kd = sdesc_sw128(kb0 + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u);
+            tc_mma_ta(s_t, q_t + (uint32_t)kk * 8, kd, id_s, kk != 0);
+            tc_mma_ta(s_t, ql_t + (uint32_t)kk * 8, kd, id_s, true);
           }
-          tc_commit(&S.empty[st]);
           tc_commit(S.sfull);
           // O_j = P_j V_j (P from TMEM, V as an MN-major operand)
-          st = stage_ctr % PF_NSTAGE;
-          pf_wait(P, &S.full[st], (stage_ctr / PF_NSTAGE) & 1u);
-          ++stage_ctr;
           pf_wait(P, S.pfull, sctr & 1u);
           ++sctr;
           tc_fence_after();
-          const uint32_t vb0 = smem_u32(S.ring + st * PF_STAGE);
+          const uint32_t vb0 = kb0 + tile;
 #pragma unroll
-          for (int kk = 0; kk < PF_BM / 16; ++kk)
-            tc_mma_ta(o_t, p_t + (uint32_t)kk * 8, sdesc_sw128_mn(vb0 + (uint32_t)kk * 2048u, 16384u),
-                      id_o, kk != 0);
+          for (int kk = 0; kk < PF_BM / 16; ++kk) {
+            const uint64_t vd = sdesc_sw128_mn(vb0 + (uint32_t)kk * 2048u, 16384u);
+            tc_mma_ta(o_t, p_t + (uint32_t)kk * 8, vd, id_o, kk != 0);
+            tc_mma_ta(o_t, pl_t + (uint32_t)kk * 8, vd, id_o, true);
+          }
           tc_commit(&S.empty[st]);
           tc_commit(S.ofull);
         }
-        tc_commit(S.qempty);
       }
     }
   }
@@ -415,6 +419,25 @@ __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float (&v)[16
   b.z = pack_bf16(v[12], v[13]); b.w = pack_bf16(v[14], v[15]);
   reinterpret_cast<uint4*>(dst)[0] = a;
   reinterpret_cast<uint4*>(dst)[1] = b;
+}
+// (hi, lo) bf16 pairs of two values: hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+  hi = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+  lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
+}
+__device__ __forceinline__ void store_split8(uint16_t* hi, uint16_t* lo, const float* v) {
+  uint4 h, l;
+  split_pack(v[0], v[1], h.x, l.x);
+  split_pack(v[2], v[3], h.y, l.y);
+  split_pack(v[4], v[5], h.z, l.z);
+  split_pack(v[6], v[7], h.w, l.w);
+  *reinterpret_cast<uint4*>(hi) = h;
+  *reinterpret_cast<uint4*>(lo) = l;
+}
+__device__ __forceinline__ void store_split16(uint16_t* hi, uint16_t* lo, const float (&v)[16]) {
+  store_split8(hi, lo, v);
+  store_split8(hi + 8, lo + 8, v + 8);
 }
 __device__ __forceinline__ float bf(const uint16_t* p, int i) {
   return __uint_as_float((uint32_t)__ldg(p + i) << 16);
@@ -452,8 +475,10 @@ __device__ void pf_qkv_head(const PfParams& P, uint32_t tacc, int c0, int col, i
     }
     inv = 1.0f / sqrtf(ss / (float)d + P.eps);
   }
+  // queries: hi/lo planes (tensor-core operand); keys: the bf16 cache entry
   uint16_t* dst = is_q ? P.qb + (size_t)p * qd + col
                        : P.kv + ((size_t)kv_row(P, l, 0, (col - qd) / d) + p) * d;
+  uint16_t* dst_lo = is_q ? dst + (size_t)P.plane_rows * qd : nullptr;
   const float2* rt = P.rope + (size_t)p * half;
   for (int c = 0; c < half; c += 16) {
     float u1[16], u2[16];
@@ -474,8 +499,13 @@ __device__ void pf_qkv_head(const PfParams& P, uint32_t tacc, int c0, int col, i
       r2[e] = u2[e] * cs.x + u1[e] * cs.y;
     }
     if (live) {
-      store_bf16x16(dst + c, r1);
-      store_bf16x16(dst + c + half, r2);
+      if (is_q) {
+        store_split16(dst + c, dst_lo + c, r1);
+        store_split16(dst + c + half, dst_lo + c + half, r2);
+      } else {
+        store_bf16x16(dst + c, r1);
+        store_bf16x16(dst + c + half, r2);
+      }
     }
   }
 }
@@ -530,13 +560,14 @@ __device__ void pf_gemm_epilogue(const PfParams& P, const Instr& in, uint32_t ta
     }
     default: {  // PF_GU: columns [0,128) gate, [128,256) up
       uint16_t* dst = P.act + (size_t)p * P.F + n * PF_BN_GU;
+      uint16_t* dst_lo = dst + (size_t)P.plane_rows * P.F;
       for (int c = 0; c < PF_BN_GU; c += 16) {
         float gt[16], up[16], a[16];
         tmem_ld16(tacc + (uint32_t)c, gt);
         tmem_ld16(tacc + (uint32_t)(PF_BN_GU + c), up);
 #pragma unroll
         for (int e = 0; e < 16; ++e) a[e] = gt[e] / (1.0f + expf(-gt[e])) * up[e];
-        if (live) store_bf16x16(dst + c, a);
+        if (live) store_split16(dst + c, dst_lo + c, a);
       }
       break;
     }
@@ -587,26 +618,49 @@ __device__ void pf_norm(const PfParams& P, const Instr& in, int wc, int lane) {
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
       }
       widen8(__ldg(reinterpret_cast<const uint4*>(gain + c)), gw);
-      uint4 o;
-      o.x = pack_bf16(x[0] * inv * gw[0], x[1] * inv * gw[1]);
-      o.y = pack_bf16(x[2] * inv * gw[2], x[3] * inv * gw[3]);
-      o.z = pack_bf16(x[4] * inv * gw[4], x[5] * inv * gw[5]);
-      o.w = pack_bf16(x[6] * inv * gw[6], x[7] * inv * gw[7]);
-      *reinterpret_cast<uint4*>(dst + (size_t)p * H + c) = o;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * gw[e];
+      store_split8(dst + (size_t)p * H + c, dst + ((size_t)P.plane_rows + p) * H + c, y);
     }
   }
 }
 
-// Softmax side of one (block, kv group): per head, online softmax over key
-// blocks 0..m; O accumulates in registers (this thread's query row).
+// Softmax side of one (block, kv group).  Per head: this row's query (hi and
+// lo planes) goes into TMEM as the A operand of S = Q K^T, then an online
+// softmax runs over key blocks 0..m; P_j goes back into TMEM as (hi, lo) bf16
+// pairs for O_j = P_j V_j, and O accumulates in registers (this thread's row).
 template <int D>
 __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint32_t tbase, int row,
                         uint32_t lane_base, uint32_t& sctr) {
-  const int m = (int)in.a0, gq = (int)in.a1;
-  const int qi = m * PF_BM + row;
+  const int m = (int)in.a0, gq = (int)in.a1, lane = threadIdx.x & 31;
+  const int qi = m * PF_BM + row;  // < plane_rows: rows past the prompt are never stored
+  const int qd = P.nq * D;
   const float c = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
-  const uint32_t s_t = tbase + lane_base, o_t = tbase + 128 + lane_base, p_t = tbase + 256 + lane_base;
+  const uint32_t s_t = tbase + lane_base, o_t = tbase + 128 + lane_base;
+  const uint32_t p_t = tbase + 256 + lane_base, pl_t = tbase + 320 + lane_base;
+  const uint32_t q_t = tbase + 384 + lane_base, ql_t = tbase + 448 + lane_base;
   for (int h = 0; h < P.rep; ++h) {
+    // The previous head's (or instruction's) S products completed before its
+    // last S block was handed to these warps, so the Q columns are free.
+    const uint16_t* qh = P.qb + (size_t)qi * qd + (size_t)(gq * P.rep + h) * D;
+    const uint16_t* ql = qh + (size_t)P.plane_rows * qd;
+#pragma unroll
+    for (int c8 = 0; c8 < D / 2; c8 += 8) {
+      const uint4 a = __ldcg(reinterpret_cast<const uint4*>(qh + 2 * c8));
+      const uint4 b = __ldcg(reinterpret_cast<const uint4*>(qh + 2 * c8 + 8));
+      const uint4 e = __ldcg(reinterpret_cast<const uint4*>(ql + 2 * c8));
+      const uint4 f = __ldcg(reinterpret_cast<const uint4*>(ql + 2 * c8 + 8));
+      const uint32_t wh[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      const uint32_t wl[8] = {e.x, e.y, e.z, e.w, f.x, f.y, f.z, f.w};
+      tmem_st8(q_t + (uint32_t)c8, wh);
+      tmem_st8(ql_t + (uint32_t)c8, wl);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(S.qfull);
+
     float o[D];
 #pragma unroll
     for (int e = 0; e < D; ++e) o[e] = 0.f;
@@ -629,27 +683,9 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
       }
       const float mnew = fmaxf(mrun, mx);
       const float alpha = mrun == -INFINITY ? 0.f : exp2f(mrun - mnew);
-      // pass 2: probabilities, row sum, bf16 P into TMEM (16 keys per 8 columns)
-      float sum = 0.f;
-      uint32_t pk[PF_BM / 2];
-      for (int c0 = 0; c0 < PF_BM; c0 += 16) {
-        float s[16];
-        tmem_ld16(s_t + (uint32_t)c0, s);
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const int kj = j * PF_BM + c0 + e;
-          const bool m0 = diag && (kj > qi || kj >= P.S);
-          const bool m1 = diag && (kj + 1 > qi || kj + 1 >= P.S);
-          const float p0 = m0 ? 0.f : exp2f(s[e] * c - mnew);
-          const float p1 = m1 ? 0.f : exp2f(s[e + 1] * c - mnew);
-          sum += p0 + p1;
-          pk[(c0 + e) / 2] = pack_bf16(p0, p1);
-        }
-      }
-      lrun = lrun * alpha + sum;
-      mrun = mnew;
       if (j > 0) {
-        // O_{j-1} is ready; fold it in at the scale of block j-1
+        // O_{j-1} = P_{j-1} V_{j-1} was issued before S_j, so it is complete
+        // (and P's columns are free); fold it in at the scale of block j-1
         pf_wait(P, S.ofull, (sctr - 1) & 1u);
         tc_fence_after();
 #pragma unroll
@@ -660,18 +696,32 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
           for (int e = 0; e < 16; ++e) o[c0 + e] = o[c0 + e] * alpha_prev + v[e];
         }
       }
-      alpha_prev = alpha;
+      // pass 2: probabilities, row sum, (hi, lo) bf16 P into TMEM
+      float sum = 0.f;
+      for (int c0 = 0; c0 < PF_BM; c0 += 16) {
+        float s[16];
+        tmem_ld16(s_t + (uint32_t)c0, s);
+        uint32_t hi[8], lo[8];
 #pragma unroll
-      for (int c8 = 0; c8 < PF_BM / 2; c8 += 8) {
-        uint32_t w8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w8[e] = pk[c8 + e];
-        tmem_st8(p_t + (uint32_t)c8, w8);
+        for (int e = 0; e < 16; e += 2) {
+          const int kj = j * PF_BM + c0 + e;
+          const bool m0 = diag && (kj > qi || kj >= P.S);
+          const bool m1 = diag && (kj + 1 > qi || kj + 1 >= P.S);
+          const float p0 = m0 ? 0.f : exp2f(s[e] * c - mnew);
+          const float p1 = m1 ? 0.f : exp2f(s[e + 1] * c - mnew);
+          sum += p0 + p1;
+          split_pack(p0, p1, hi[e / 2], lo[e / 2]);
+        }
+        tmem_st8(p_t + (uint32_t)(c0 / 2), hi);
+        tmem_st8(pl_t + (uint32_t)(c0 / 2), lo);
       }
+      lrun = lrun * alpha + sum;
+      mrun = mnew;
+      alpha_prev = alpha;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(S.pfull);
+      if (lane == 0) mbar_arrive(S.pfull);
       ++sctr;
     }
     pf_wait(P, S.ofull, (sctr - 1) & 1u);
@@ -685,13 +735,14 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
       for (int e = 0; e < 16; ++e) o[c0 + e] = (o[c0 + e] * alpha_prev + v[e]) * linv;
     }
     if (qi < P.S) {
-      uint16_t* dst = P.ao + (size_t)qi * (P.nq * D) + (size_t)(gq * P.rep + h) * D;
+      uint16_t* dst = P.ao + (size_t)qi * qd + (size_t)(gq * P.rep + h) * D;
+      uint16_t* dst_lo = dst + (size_t)P.plane_rows * qd;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = o[c0 + e];
-        store_bf16x16(dst + c0, v);
+        store_split16(dst + c0, dst_lo + c0, v);
       }
     }
   }
@@ -738,6 +789,10 @@ __device__ void pf_compute(const PfParams& P, const PfSh& S, uint32_t tbase) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.acce[ab]);
       } else if (in.op == PF_ATTN) {
+        // the queries are read here with plain loads: wait for their QKV tiles
+        // (after a timeout the launch drains on stale data, as the producer does)
+        if (tc == 0) pf_wait_deps(P, in, gen, i);
+        cbar_pf();
         use[0]++;
         use[1]++;
         if (P.d == 128) pf_attn<128>(P, S, in, tbase, row, lane_base, sctr);
@@ -778,8 +833,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) mk_prefill_kernel(const __grid_
       mbar_init(&S.accf[b], 1);
       mbar_init(&S.acce[b], 4);
     }
-    mbar_init(S.qfull, 1);
-    mbar_init(S.qempty, 1);
+    mbar_init(S.qfull, 4);  // the compute warps, once the head's queries are in TMEM
     mbar_init(S.sfull, 1);
     mbar_init(S.pfull, 4);
     mbar_init(S.ofull, 1);
