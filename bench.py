@@ -7,6 +7,11 @@ JSON line (rank 0).  See the design doc for the metric, the roofline arithmetic and
 the input recipe.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload llama3-8b|llama3.2-1b] [--no-per-op] [--no-prefill]
+                  [--no-cpu-baseline]
+
+--workload llama3.2-1b (Llama-3.2-1B shape, context 1024) is a smaller case of
+the same step for profiling; the default is the headline workload.
 
 --impl reference times the CPU oracle (plain NumPy forward pass) on the host
 cores on a bounded sample of the same workload (a few layers + the LM head per
@@ -29,14 +34,24 @@ if ROOT not in sys.path:
 
 METRIC = "decode tokens/s and HBM GB/s (% of ~8 TB/s), Llama-3-8B shape, batch 1, 1xGB300"
 UNIT = "tokens/s"
-CONTEXT = 4096
 BATCH = 1
 PREFILL_TOKENS = 2048
+# name -> (shape in synth, cached context, metric, workload description, traffic key)
+WORKLOADS = {
+    "llama3-8b": ("LLAMA3_8B", 4096, METRIC, "Llama-3-8B-shape decode, batch 1, context 4096",
+                  "llama3-8b-decode-b1-ctx4096"),
+    "llama3.2-1b": ("LLAMA32_1B", 1024,
+                    "decode tokens/s and HBM GB/s, Llama-3.2-1B shape, batch 1, 1xGB300",
+                    "Llama-3.2-1B-shape decode, batch 1, context 1024",
+                    "llama3.2-1b-decode-b1-ctx1024"),
+}
 
 
-def workload_cfg():
+def workload(name):
+    """(model shape, cached context, metric, description, traffic key)."""
     from tile_level_overlap_gb300 import synth
-    return synth.LLAMA3_8B
+    shape, ctx, metric, desc, key = WORKLOADS[name]
+    return getattr(synth, shape), ctx, metric, desc, key
 
 
 def algorithmic_bytes(cfg, batch, positions) -> int:
@@ -178,7 +193,7 @@ class OracleSample:
     """The CPU oracle on a bounded sample of the decode step: `n_layers_sample`
     layers + the LM head (weights drawn on the CPU with the same recipe)."""
 
-    def __init__(self, cfg, n_layers_sample: int, seed: int = 0):
+    def __init__(self, cfg, n_layers_sample: int, context: int, seed: int = 0):
         import torch
 
         from tile_level_overlap_gb300 import synth
@@ -188,7 +203,8 @@ class OracleSample:
         self.n = n_layers_sample
         self.sub = cfg.replace(n_layers=n_layers_sample)
         self.w = synth.weights_as_bits(synth.make_weights(self.sub, seed=seed, device="cpu"))
-        self.kv = synth.bf16_bits(synth.make_kv_cache(self.sub, 1, CONTEXT + 1, device="cpu"))
+        self.context = context
+        self.kv = synth.bf16_bits(synth.make_kv_cache(self.sub, 1, context + 1, device="cpu"))
         self.tok = synth.make_tokens(1, cfg.vocab).numpy()
 
     def step(self):
@@ -199,12 +215,13 @@ class OracleSample:
         from oracle import model as om
 
         t0 = time.perf_counter()
-        oracle.decode_step(self.sub, self.w, self.tok, [CONTEXT], self.kv)
+        oracle.decode_step(self.sub, self.w, self.tok, [self.context], self.kv)
         t_all = time.perf_counter() - t0
         # the LM head alone, so that only the layer part is scaled
         x = np.random.default_rng(0).normal(size=(1, self.cfg.hidden)).astype(np.float32)
         t1 = time.perf_counter()
-        om.linear(self.w["lm_head"], om.rmsnorm(x, self.w["final_norm"], self.cfg.rms_eps))
+        lm = self.w["embed"] if self.cfg.tied_embeddings else self.w["lm_head"]
+        om.linear(lm, om.rmsnorm(x, self.w["final_norm"], self.cfg.rms_eps))
         t_lm = time.perf_counter() - t1
         t_layers = max(t_all - t_lm, 1e-9)
         return t_layers * self.cfg.n_layers / self.n + t_lm, t_all
@@ -214,9 +231,9 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    cfg = workload_cfg()
+    cfg, context, metric, wl_desc, _ = workload(args.workload)
     n_s = args.ref_layers
-    sample_run = OracleSample(cfg, n_s)
+    sample_run = OracleSample(cfg, n_s, context)
     for _ in range(args.warmup):
         sample_run.step()
     times, measured = [], 0.0
@@ -227,12 +244,12 @@ def run_reference(args):
     ms = 1e3 * sum(times) / len(times)
     value = BATCH / (ms / 1e3)
     sample = (f"{n_s} of {cfg.n_layers} layers + the LM head of one batch-1 decode step at context "
-              f"{CONTEXT}, per step; time scaled to {cfg.n_layers} layers")
+              f"{context}, per step; time scaled to {cfg.n_layers} layers")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-        "config": {"workload": "Llama-3-8B-shape decode, batch 1, context 4096",
+        "config": {"workload": wl_desc,
                    "weights": "bf16", "kv_cache": "bf16"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
@@ -260,7 +277,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    cfg = workload_cfg()
+    cfg, CONTEXT, metric, wl_desc, traffic_key = workload(args.workload)
     max_ctx = CONTEXT + 1
     w = synth.make_weights(cfg, seed=synth.SEED_WEIGHTS + rank, device=dev)
     kv = synth.make_kv_cache(cfg, BATCH, max_ctx, device=dev)
@@ -312,12 +329,18 @@ def run_ours(args):
     value = job_throughput(BATCH * args.steps, world, ms_total / 1e3)
 
     # the same tile routines, kernel-per-operator (eager and CUDA graph)
-    for _ in range(max(1, args.warmup // 2)):
-        perop()
-        perop_graph()
-    ms_perop = timed(perop, args.steps) / args.steps
-    ms_graph = timed(perop_graph, args.steps) / args.steps
-    launches_perop = plan.stats().n_launches_per_op_decode
+    per_op = None
+    if not args.no_per_op:
+        for _ in range(max(1, args.warmup // 2)):
+            perop()
+            perop_graph()
+        ms_perop = timed(perop, args.steps) / args.steps
+        ms_graph = timed(perop_graph, args.steps) / args.steps
+        per_op = {"ms_per_step_eager": ms_perop, "ms_per_step_graph": ms_graph,
+                  "tokens_per_s_eager": BATCH / (ms_perop / 1e3),
+                  "tokens_per_s_graph": BATCH / (ms_graph / 1e3),
+                  "launches_per_step": plan.stats().n_launches_per_op_decode,
+                  "speedup_persistent_vs_graph": ms_graph / ms}
 
     # end to end through the host-buffer entry point: pinned host tokens and
     # positions in, logits out, every step
@@ -376,12 +399,12 @@ def run_ours(args):
         return 0
     peaks, kind = measured_peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
-    traffic = recorded_traffic("mk_interpreter", "llama3-8b-decode-b1-ctx4096")
+    traffic = recorded_traffic("mk_interpreter", traffic_key)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "Llama-3-8B-shape decode, batch 1, context 4096",
+        "config": {"workload": wl_desc,
                    "layers": cfg.n_layers, "hidden": cfg.hidden, "ffn": cfg.ffn,
                    "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
                    "head_dim": cfg.head_dim, "vocab": cfg.vocab, "batch": BATCH,
@@ -395,11 +418,7 @@ def run_ours(args):
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_kind": kind, "kernel": "mk_interpreter",
                      "algorithmic_bytes_per_launch": nbytes},
-        "per_op": {"ms_per_step_eager": ms_perop, "ms_per_step_graph": ms_graph,
-                   "tokens_per_s_eager": BATCH / (ms_perop / 1e3),
-                   "tokens_per_s_graph": BATCH / (ms_graph / 1e3),
-                   "launches_per_step": launches_perop,
-                   "speedup_persistent_vs_graph": ms_graph / ms},
+        "per_op": per_op,
         "dep_wait_fraction": dep_wait,
         "clocks": clk.summary(),
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": 8 * BATCH,
@@ -408,7 +427,7 @@ def run_ours(args):
         "prefill": prefill,
     }
     if world == 1 and not args.no_cpu_baseline:
-        sample_run = OracleSample(cfg, args.ref_layers)
+        sample_run = OracleSample(cfg, args.ref_layers, CONTEXT)
         sample_run.step()
         t = sorted(sample_run.step()[0] for _ in range(3))[1]
         line["cpu_baseline"] = {
@@ -431,6 +450,8 @@ def main():
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-per-op", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3-8b")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

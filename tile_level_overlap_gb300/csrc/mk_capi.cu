@@ -51,6 +51,7 @@ struct mk_plan {
   KParams base{};
   int force_ctas = 0, trace = 0;
   uint64_t wait_limit_ns = 2000000000ull;
+  uint32_t l2_ahead = 0;  // L2 weight prefetch distance of the persistent decode (0: off)
   cudaStream_t cap_stream = nullptr;
   cudaGraphExec_t graph = nullptr;
   uintptr_t graph_key[6] = {0, 0, 0, 0, 0, 0};
@@ -128,7 +129,7 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
   if (!cfg) return MK_ERR_INVALID_ARG;
   HostPlan hp;
   std::string why;
-  int rc = build_plan(*cfg, max_batch, max_ctx, &hp, &why);
+  int rc = build_plan(*cfg, max_batch, max_ctx, 0, &hp, &why);
   if (rc != MK_OK) return rc;
   std::vector<Instr> q = hp.decode;
   if (queue_perm_seed) {
@@ -161,9 +162,15 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
     cudaGetLastError();
     return MK_ERR_NO_DEVICE;
   }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
   mk_plan* p = new mk_plan();
   std::string why;
-  int rc = build_plan(*cfg, max_batch, max_ctx, &p->hp, &why);
+  int rc = build_plan(*cfg, max_batch, max_ctx, sms, &p->hp, &why);
   if (rc != MK_OK) {
     delete p;
     return rc;
@@ -350,6 +357,7 @@ static KParams step_params(mk_plan* p, const int32_t* tokens, const int32_t* pos
   k.mode = MODE_MEGA;
   k.trace = p->trace ? p->d_trace : nullptr;
   k.wait_limit_ns = p->wait_limit_ns;
+  k.l2_ahead = p->l2_ahead;
   return k;
 }
 
@@ -632,6 +640,12 @@ int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int 
     MK_CUDA(cudaMemset(p->d_trace, 0, p->hp.decode.size() * TRACE_WORDS * 8));
   }
   p->trace = trace ? 1 : 0;
+  return MK_OK;
+}
+
+int mk_plan_set_l2_prefetch(mk_plan* p, uint32_t instructions_ahead) {
+  if (!p) return MK_ERR_INVALID_ARG;
+  p->l2_ahead = instructions_ahead;
   return MK_OK;
 }
 

@@ -151,8 +151,9 @@ enum Mode : int { MODE_MEGA = 0, MODE_PEROP = 1 };
 // spent waiting for ring stages, [6] first stage available, [7] ns the producer
 // spent waiting for free ring stages while streaming it, [8] (batch-1 GEMV)
 // last stage consumed and the tile handed to the finisher warp, [9] (batch-1
-// GEMV) the finisher took it, [10] and [11] unused.  For handed-off tiles [3]
-// is written by the finisher after its release.
+// GEMV) the finisher took it; for attention tiles [8]..[11] mark its phases
+// (inputs rotated, scores, softmax and P V, split arrival).  For handed-off
+// tiles [3] is written by the finisher after its release.
 constexpr int TRACE_WORDS = 12;
 
 // Everything one launch needs, passed by value as a __grid_constant__ parameter.
@@ -180,7 +181,7 @@ struct KParams {
   const Instr* queue;
   uint32_t n_instr;
   const uint32_t* expr;  // [XS_COUNT][X_MAX_WORDS]
-  unsigned long long* trace;  // 4 x u64 per instruction, or null
+  unsigned long long* trace;  // TRACE_WORDS x u64 per instruction, or null
   BarLayout bl;
   // step
   const int32_t* tokens;
@@ -191,6 +192,11 @@ struct KParams {
   int mode;
   uint32_t perop_base;
   unsigned long long wait_limit_ns;
+  // Persistent mode: when a CTA pops instruction i it also prefetches into L2
+  // the weight rows of instruction i + l2_ahead (queue order), so that weights
+  // stream from HBM while dependency waits (attention, the norms' all-to-all
+  // inputs) hold the consumers; 0 turns it off.
+  uint32_t l2_ahead;
 };
 
 }  // namespace mk

@@ -274,6 +274,19 @@ __device__ __forceinline__ uint32_t src_stages(const Src& s) {
 }
 
 // ---------------------------------------------------------------- producer
+// L2 prefetch of a GEMV instruction's weight rows (attention tiles: none; the
+// cache they read is 3.5% of a batch-1 step's bytes).
+__device__ void l2_prefetch_instr(const KParams& P, const Instr& in) {
+  if (in.op == OP_ATTN) return;
+  const GemvDesc g = gemv_desc(P, in);
+  const uint32_t bytes = (uint32_t)g.rows * (uint32_t)g.K * 2u;
+  for (int r = 0; r < (g.w1 ? 2 : 1); ++r) {
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(r ? g.w1 : g.w0);
+    for (uint32_t off = 0; off < bytes; off += 65536u)
+      l2_prefetch(base + off, bytes - off < 65536u ? bytes - off : 65536u);
+  }
+}
+
 __device__ void producer(const KParams& P, const Sh& S) {
   const int lane = threadIdx.x & 31;
   if (lane != 0) return;
@@ -296,6 +309,12 @@ __device__ void producer(const KParams& P, const Sh& S) {
   uint32_t ib = pop();
   Instr Ia;
   if (ia != END_SLOT) Ia = P.queue[ia];
+  // L2 prefetch pipeline: the record of instruction (posted + l2_ahead) is
+  // loaded in one iteration and its prefetch issued in the next, so the load
+  // latency overlaps this instruction's streaming.
+  Instr Ipf;
+  bool pf_have = false;
+  const bool pf_on = P.l2_ahead != 0u && P.mode == MODE_MEGA;
   for (;;) {
     const bool end = ia == END_SLOT;
     Instr Ib;
@@ -322,6 +341,12 @@ __device__ void producer(const KParams& P, const Sh& S) {
     ia = ib;
     Ia = Ib;
     ib = ic;
+    if (pf_on) {
+      if (pf_have) l2_prefetch_instr(P, Ipf);
+      const uint32_t j = i_in + P.l2_ahead;
+      pf_have = j < P.n_instr;
+      if (pf_have) Ipf = P.queue[j];
+    }
     const Src src = src_of(P, in, ext);
     bool stuck = false;
     uint64_t blocked_ns = 0;  // (tracing) time spent waiting for a free stage
@@ -678,6 +703,12 @@ __device__ __forceinline__ float round_bf16(float x) {
 // cache by the split that holds slot pos).
 // Partial (max, sum, unnormalised o) per q head; the last split to arrive
 // combines all splits of the group in split order.
+// (tracing) attention tile phase boundaries: trace words 8 (inputs loaded and
+// rotated), 9 (scores), 10 (softmax and P V), 11 (split arrival counted)
+__device__ __forceinline__ void attn_mark(const KParams& P, uint32_t ii, int word) {
+  if (P.trace && threadIdx.x == 0) P.trace[(size_t)ii * TRACE_WORDS + word] = globaltimer();
+}
+
 template <int D, int REP>
 __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
                           uint32_t ii, Ring& R) {
@@ -738,6 +769,7 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
       }
     }
     cbar();
+    attn_mark(P, ii, 8);
     if (e.has_new)
       for (int i = t; i < D; i += NT) {
         P.kv[kv_offset(P, l, 0, b, g, e.pos) + i] = __bfloat16_as_ushort(__float2bfloat16_rn(kn[i]));
@@ -789,6 +821,7 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
       if (lane == 0) sc[w * smax + (e.pos - e.lo)] = a * scale;
     }
     cbar();
+    attn_mark(P, ii, 9);
     const int n = e.hi - e.lo;
     if (w < rep) {
       float m = -INFINITY;
@@ -849,6 +882,7 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
     }
     // an empty split (n == 0) leaves max = -inf, sum = 0 from the softmax pass
   }
+  attn_mark(P, ii, 10);
   cbar();
   if (t == 0) {
     uint32_t* arr = P.arrive + ((size_t)l * P.max_batch + b) * P.nkv + g;
@@ -858,6 +892,7 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
     S.flags[F_LAST] = last ? 1u : 0u;
   }
   cbar();
+  attn_mark(P, ii, 11);
   if (S.flags[F_LAST]) {
     if (e.live) {
       // Combine the NS splits in split order: weights f_s = exp(m_s - max_s m_s)
@@ -866,6 +901,20 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
       float* fw = S.xbuf;                 // [NS][rep] weights
       float* lw = S.xbuf + NS * rep;      // [NS][rep] partial sums
       float* linv = lw + NS * rep;        // [rep]
+      // Each thread's (head, column) outputs: their partial values are loaded
+      // CB splits at a time, every load of a batch in flight together; the
+      // first batch goes out with the (max, sum) loads.
+      constexpr int NO = (REP * D + NT - 1) / NT;
+      constexpr int CB = NO <= 2 ? 10 : 4;
+      float v[NO][CB];
+#pragma unroll
+      for (int k = 0; k < NO; ++k) {
+        const int i = t + k * NT;
+        const float* pc = gp + (size_t)(i / D) * (D + 2) + (i % D);
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+          v[k][u] = (i < rep * D && u < NS) ? __ldcg(pc + (size_t)u * rep * (D + 2)) : 0.f;
+      }
       for (int i = t; i < NS * rep; i += NT) {
         const float* ps = gp + (size_t)i * (D + 2);
         fw[i] = __ldcg(ps + D);
@@ -887,20 +936,36 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
         if (lane == 0) linv[w] = 1.0f / Ls;
       }
       cbar();
-      for (int i = t; i < rep * D; i += NT) {
-        const int h = i / D, c = i % D;
-        const float* pc = gp + (size_t)h * (D + 2) + c;
-        float O = 0.f;
-        int s = 0;
-        for (; s + 8 <= NS; s += 8) {
-          float v[8];
+      // o = sum_s f_s o_s in split order
+      float O[NO];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = __ldcg(pc + (size_t)(s + u) * rep * (D + 2));
+      for (int k = 0; k < NO; ++k) O[k] = 0.f;
+      for (int s0 = 0; s0 < NS; s0 += CB) {
+        if (s0 > 0) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) O = fmaf(v[u], fw[(s + u) * rep + h], O);
+          for (int k = 0; k < NO; ++k) {
+            const int i = t + k * NT;
+            const float* pc = gp + (size_t)(i / D) * (D + 2) + (i % D);
+#pragma unroll
+            for (int u = 0; u < CB; ++u)
+              v[k][u] = (i < rep * D && s0 + u < NS) ? __ldcg(pc + (size_t)(s0 + u) * rep * (D + 2)) : 0.f;
+          }
         }
-        for (; s < NS; ++s) O = fmaf(__ldcg(pc + (size_t)s * rep * (D + 2)), fw[s * rep + h], O);
-        P.attn_out[((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c] = O * linv[h];
+#pragma unroll
+        for (int k = 0; k < NO; ++k) {
+          const int h = (t + k * NT) / D;
+#pragma unroll
+          for (int u = 0; u < CB; ++u)
+            if (s0 + u < NS) O[k] = fmaf(v[k][u], fw[(s0 + u) * rep + h], O[k]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NO; ++k) {
+        const int i = t + k * NT;
+        if (i < rep * D) {
+          const int h = i / D, c = i % D;
+          P.attn_out[((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c] = O[k] * linv[h];
+        }
       }
     }
     cbar();
@@ -1082,7 +1147,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       if (!R.loop_ns) tr[3] = globaltimer();  // handed-off tiles: the finisher writes it
       tr[5] = R.wait_ns;
       tr[6] = R.first_ns;
-      tr[8] = R.loop_ns;
+      if (in.op != OP_ATTN) tr[8] = R.loop_ns;
     }
     R.wait_ns = 0;
     R.first_ns = 0;

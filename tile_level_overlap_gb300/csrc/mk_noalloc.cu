@@ -65,9 +65,15 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
                                       float* logits, void* stream) {
   if (!cfg || !w || !tokens || !positions || !kv_cache || !logits) return MK_ERR_INVALID_ARG;
   if (batch < 1 || batch > max_batch || !al16(kv_cache)) return MK_ERR_INVALID_ARG;
+  int cur = 0, sms = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, cur) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
   HostPlan hp;
   std::string why;
-  int rc = build_plan(*cfg, max_batch, max_ctx, &hp, &why);
+  int rc = build_plan(*cfg, max_batch, max_ctx, sms, &hp, &why);
   if (rc != MK_OK) return rc;
   const mk_model_cfg& c = hp.cfg;
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;

@@ -76,7 +76,7 @@ void put_expr(std::vector<uint32_t>& table, int slot, const XBuild& x) {
 
 }  // namespace
 
-int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
+int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, HostPlan* out,
                std::string* why) {
   auto bad = [&](int code, const char* msg) {
     if (why) *why = msg;
@@ -135,10 +135,12 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, HostPlan* out,
   hp.n_down_tiles = ceil_div(H, hp.r_down);
   hp.n_lm_tiles = ceil_div(c.vocab, hp.r_lm);
 
-  // Split-KV partitions per (sequence, kv head): enough instructions to cover
-  // the SMs at batch 1, at most SCORE_FLOATS/rep keys per split, at least 32.
+  // Split-KV partitions per (sequence, kv head): one attention tile per SM
+  // (a single round: the phase is latency-bound, a second round doubles it),
+  // at most SCORE_FLOATS/rep keys per split, at least 32.
   hp.split_max = SCORE_FLOATS / rep;
-  int ns = (int)ceil_div(256, (uint64_t)max_batch * nkv);
+  if (n_sms <= 0) n_sms = DEFAULT_SMS;
+  int ns = n_sms / (max_batch * nkv);
   ns = std::max(ns, (int)ceil_div(max_ctx, hp.split_max));
   ns = std::min(ns, (int)std::max<uint32_t>(ceil_div(max_ctx, 32), ceil_div(max_ctx, hp.split_max)));
   ns = std::max(ns, 1);

@@ -27,6 +27,8 @@ constexpr int XBUF_FLOATS = XBUF_BYTES / 4;
 constexpr int SCORE_FLOATS = 4096;    // attention scores per split (all q heads of a group)
 constexpr int FAST_K_UNIT = 8 * NT;   // K must be a multiple of this for the batch-1 fast path
 
+constexpr int DEFAULT_SMS = 152;  // SMs of a GB300
+
 struct HostPlan {
   mk_model_cfg cfg{};
   int max_batch = 0, max_ctx = 0;
@@ -43,7 +45,9 @@ struct HostPlan {
 
 // Validate the shape and build the plan.  Returns MK_OK or an MK_ERR_* code
 // with a reason in *why.
-int build_plan(const mk_model_cfg& cfg, int max_batch, int max_ctx, HostPlan* out,
+// n_sms: SMs of the device the plan runs on (sets the split-KV count so that
+// one round of attention tiles covers the SMs); 0 = DEFAULT_SMS.
+int build_plan(const mk_model_cfg& cfg, int max_batch, int max_ctx, int n_sms, HostPlan* out,
                std::string* why);
 
 // A seeded random topological order of queue `q` (Kahn's algorithm on the
