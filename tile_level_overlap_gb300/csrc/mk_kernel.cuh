@@ -840,45 +840,65 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
       }
     }
     cbar();
-    // o = sum_j p_j v_j: thread owns column pairs (h, 2c) for pair index t, t + NT
-    float o[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    const int npairs = rep * (D / 2);
+    // o = sum_j p_j v_j.  Lane owns DPL consecutive columns, warp w a head
+    // group (HPW heads) and the keys j = kw, kw + KS, ... of each stage, so
+    // each V element is widened once for HPW heads; the KS key subsets of a
+    // head group are then added in warp order through shared memory.
+    constexpr int DPL = D / 32;                          // columns per lane
+    constexpr int HPW = REP < 4 ? REP : 4;               // heads per warp
+    constexpr int KS = NW / (REP / HPW);                 // key subsets per head group
+    static_assert(NW * HPW * D <= SCORE_FLOATS, "P V reduction buffer");
+    const int hg = w / KS, kw = w % KS;
+    float acc[HPW][DPL];
+#pragma unroll
+    for (int h = 0; h < HPW; ++h)
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) acc[h][k] = 0.f;
     for (int c0 = 0; c0 < e.nc; c0 += kps) {
       const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
       const uint8_t* stage = ring_acquire(P, S, R);
+      const float* ph = sc + (hg * HPW) * smax + c0;
+      for (int j = kw; j < cnt; j += KS) {
+        float vx[DPL];
+        if constexpr (DPL == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(stage + (size_t)j * D * 2 + lane * 8);
+          vx[0] = bf_lo(u.x); vx[1] = bf_hi(u.x); vx[2] = bf_lo(u.y); vx[3] = bf_hi(u.y);
+        } else {
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(stage + (size_t)j * D * 2 + lane * 4);
+          vx[0] = bf_lo(u); vx[1] = bf_hi(u);
+        }
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int pi = t + k * NT;
-        if (pi < npairs) {
-          const int h = pi / (D / 2), c = pi % (D / 2);
-          const float* ph = sc + h * smax + c0;
-          const uint32_t* vcol = reinterpret_cast<const uint32_t*>(stage) + c;
-          float a0 = o[k][0], a1 = o[k][1];
-          for (int j = 0; j < cnt; ++j) {
-            const uint32_t v2 = vcol[j * (D / 2)];
-            const float p = ph[j];
-            a0 = fmaf(p, bf_lo(v2), a0);
-            a1 = fmaf(p, bf_hi(v2), a1);
-          }
-          o[k][0] = a0;
-          o[k][1] = a1;
+        for (int h = 0; h < HPW; ++h) {
+          const float p = ph[h * smax + j];
+#pragma unroll
+          for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(p, vx[k], acc[h][k]);
         }
       }
       ring_release(S, R);
     }
+    // the new key's probability for this thread's outputs, read before sc is reused
+    const float p_new0 = (e.has_new && t < rep * D) ? sc[(t / D) * smax + (e.pos - e.lo)] : 0.f;
+    const float p_new1 = (e.has_new && t + NT < rep * D) ? sc[((t + NT) / D) * smax + (e.pos - e.lo)] : 0.f;
+    const float p_new2 = (e.has_new && t + 2 * NT < rep * D) ? sc[((t + 2 * NT) / D) * smax + (e.pos - e.lo)] : 0.f;
+    const float p_new3 = (e.has_new && t + 3 * NT < rep * D) ? sc[((t + 3 * NT) / D) * smax + (e.pos - e.lo)] : 0.f;
+    cbar();  // every warp is done reading the probabilities: reuse sc
+    float* red = sc;  // [NW][HPW][D]
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int pi = t + k * NT;
-      if (pi < npairs) {
-        const int h = pi / (D / 2), c = pi % (D / 2);
-        if (e.has_new) {
-          const float p = sc[h * smax + (e.pos - e.lo)];
-          o[k][0] = fmaf(p, vn[2 * c], o[k][0]);
-          o[k][1] = fmaf(p, vn[2 * c + 1], o[k][1]);
-        }
-        part[h * (D + 2) + 2 * c] = o[k][0];
-        part[h * (D + 2) + 2 * c + 1] = o[k][1];
+    for (int h = 0; h < HPW; ++h)
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) red[(w * HPW + h) * D + lane * DPL + k] = acc[h][k];
+    cbar();
+    for (int i = t, k = 0; i < rep * D; i += NT, ++k) {
+      const int h = i / D, c = i % D;
+      const int g2 = h / HPW, hh = h % HPW;
+      float o = 0.f;
+#pragma unroll
+      for (int q = 0; q < KS; ++q) o += red[((g2 * KS + q) * HPW + hh) * D + c];
+      if (e.has_new) {
+        const float pn = k == 0 ? p_new0 : k == 1 ? p_new1 : k == 2 ? p_new2 : p_new3;
+        o = fmaf(pn, vn[c], o);
       }
+      part[h * (D + 2) + c] = o;
     }
     // an empty split (n == 0) leaves max = -inf, sum = 0 from the softmax pass
   }

@@ -40,6 +40,21 @@ int rows_for(long target_bytes, long row_bytes, int cap) {
 
 uint32_t ceil_div(uint64_t a, uint64_t b) { return (uint32_t)((a + b - 1) / b); }
 
+// Rows per tile such that an operator's tiles come in whole rounds over the
+// SMs: about `target_bytes` per tile, rounded to a whole number of rounds of
+// n_sms tiles (at least one), at most `cap` rows.  An operator that waits on an
+// all-to-all input then starts with one tile per SM, which the operand ring has
+// largely prefetched during the wait, instead of a ragged second round.
+int rows_rounds(long total_rows, long row_bytes, long target_bytes, int n_sms, int cap) {
+  const double rounds_f = (double)total_rows * row_bytes / ((double)n_sms * target_bytes);
+  long rounds = (long)(rounds_f + 0.5);
+  if (rounds < 1) rounds = 1;
+  long r = (total_rows + rounds * n_sms - 1) / (rounds * n_sms);
+  if (r < 1) r = 1;
+  if (r > cap) r = cap;
+  return (int)r;
+}
+
 Instr make(Op op, int layer, uint32_t a0, uint32_t a1, uint16_t a2 = 0) {
   Instr in;
   std::memset(&in, 0, sizeof(in));
@@ -122,12 +137,13 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
   hp.fast_b1 = fast;
 
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
+  if (n_sms <= 0) n_sms = DEFAULT_SMS;
   // Rows per tile: ~128-256 KB of weights per instruction amortises the
   // per-instruction handshakes; QKV tiles stay inside one head.
   hp.r_qkv = std::min(rows_for(128 << 10, (long)H * 2, RMAX), d);
-  hp.r_o = rows_for(128 << 10, (long)qd * 2, RMAX);
-  hp.r_gu = rows_for(256 << 10, (long)H * 4, RMAX / 2);
-  hp.r_down = rows_for(256 << 10, (long)F * 2, RMAX);
+  hp.r_o = rows_rounds(H, (long)qd * 2, 256 << 10, n_sms, RMAX);
+  hp.r_gu = rows_rounds(F, (long)H * 4, 256 << 10, n_sms, RMAX / 2);
+  hp.r_down = rows_rounds(H, (long)F * 2, 256 << 10, n_sms, RMAX);
   hp.r_lm = rows_for(256 << 10, (long)H * 2, RMAX);
   hp.n_qkv_tiles = hp.qkv_rows / hp.r_qkv;
   hp.n_o_tiles = ceil_div(H, hp.r_o);
@@ -139,7 +155,6 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
   // (a single round: the phase is latency-bound, a second round doubles it),
   // at most SCORE_FLOATS/rep keys per split, at least 32.
   hp.split_max = SCORE_FLOATS / rep;
-  if (n_sms <= 0) n_sms = DEFAULT_SMS;
   int ns = n_sms / (max_batch * nkv);
   ns = std::max(ns, (int)ceil_div(max_ctx, hp.split_max));
   ns = std::min(ns, (int)std::max<uint32_t>(ceil_div(max_ctx, 32), ceil_div(max_ctx, hp.split_max)));
