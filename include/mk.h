@@ -197,16 +197,6 @@ int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t 
 int mk_plan_set_debug(mk_plan *plan, int force_ctas, uint64_t queue_perm_seed, int trace,
                       uint64_t wait_limit_ns);
 
-/* Tuning: distance, in queue positions, of the L2 weight prefetch of the
- * persistent decode step.  When a CTA pops instruction i it also issues an L2
- * prefetch of the weight rows of instruction i + instructions_ahead, so HBM
- * keeps streaming weights while tiles wait on their inputs (the pages' "prefetch
- * the next operator's weights while the current one runs", MegaOps, Abstract,
- * carried past the shared-memory ring).  0 turns it off; results do not depend
- * on it.  Applies to launches made after the call.  Returns MK_ERR_INVALID_ARG
- * for a null plan. */
-int mk_plan_set_l2_prefetch(mk_plan *plan, uint32_t instructions_ahead);
-
 /* Test-only fault injection, made on the host: instruction `index` of the
  * persistent queue (pop order) no longer releases its barrier, so the
  * consumers of that barrier wait until their bounded wait gives up and the

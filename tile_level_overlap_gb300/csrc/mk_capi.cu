@@ -51,7 +51,6 @@ struct mk_plan {
   KParams base{};
   int force_ctas = 0, trace = 0;
   uint64_t wait_limit_ns = 2000000000ull;
-  uint32_t l2_ahead = 0;  // L2 weight prefetch distance of the persistent decode (0: off)
   cudaStream_t cap_stream = nullptr;
   cudaGraphExec_t graph = nullptr;
   uintptr_t graph_key[6] = {0, 0, 0, 0, 0, 0};
@@ -357,7 +356,6 @@ static KParams step_params(mk_plan* p, const int32_t* tokens, const int32_t* pos
   k.mode = MODE_MEGA;
   k.trace = p->trace ? p->d_trace : nullptr;
   k.wait_limit_ns = p->wait_limit_ns;
-  k.l2_ahead = p->l2_ahead;
   return k;
 }
 
@@ -640,12 +638,6 @@ int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int 
     MK_CUDA(cudaMemset(p->d_trace, 0, p->hp.decode.size() * TRACE_WORDS * 8));
   }
   p->trace = trace ? 1 : 0;
-  return MK_OK;
-}
-
-int mk_plan_set_l2_prefetch(mk_plan* p, uint32_t instructions_ahead) {
-  if (!p) return MK_ERR_INVALID_ARG;
-  p->l2_ahead = instructions_ahead;
   return MK_OK;
 }
 

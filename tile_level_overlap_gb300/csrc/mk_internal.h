@@ -192,11 +192,6 @@ struct KParams {
   int mode;
   uint32_t perop_base;
   unsigned long long wait_limit_ns;
-  // Persistent mode: when a CTA pops instruction i it also prefetches into L2
-  // the weight rows of instruction i + l2_ahead (queue order), so that weights
-  // stream from HBM while dependency waits (attention, the norms' all-to-all
-  // inputs) hold the consumers; 0 turns it off.
-  uint32_t l2_ahead;
 };
 
 }  // namespace mk

@@ -274,19 +274,6 @@ __device__ __forceinline__ uint32_t src_stages(const Src& s) {
 }
 
 // ---------------------------------------------------------------- producer
-// L2 prefetch of a GEMV instruction's weight rows (attention tiles: none; the
-// cache they read is 3.5% of a batch-1 step's bytes).
-__device__ void l2_prefetch_instr(const KParams& P, const Instr& in) {
-  if (in.op == OP_ATTN) return;
-  const GemvDesc g = gemv_desc(P, in);
-  const uint32_t bytes = (uint32_t)g.rows * (uint32_t)g.K * 2u;
-  for (int r = 0; r < (g.w1 ? 2 : 1); ++r) {
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(r ? g.w1 : g.w0);
-    for (uint32_t off = 0; off < bytes; off += 65536u)
-      l2_prefetch(base + off, bytes - off < 65536u ? bytes - off : 65536u);
-  }
-}
-
 __device__ void producer(const KParams& P, const Sh& S) {
   const int lane = threadIdx.x & 31;
   if (lane != 0) return;
@@ -309,12 +296,6 @@ __device__ void producer(const KParams& P, const Sh& S) {
   uint32_t ib = pop();
   Instr Ia;
   if (ia != END_SLOT) Ia = P.queue[ia];
-  // L2 prefetch pipeline: the record of instruction (posted + l2_ahead) is
-  // loaded in one iteration and its prefetch issued in the next, so the load
-  // latency overlaps this instruction's streaming.
-  Instr Ipf;
-  bool pf_have = false;
-  const bool pf_on = P.l2_ahead != 0u && P.mode == MODE_MEGA;
   for (;;) {
     const bool end = ia == END_SLOT;
     Instr Ib;
@@ -341,12 +322,6 @@ __device__ void producer(const KParams& P, const Sh& S) {
     ia = ib;
     Ia = Ib;
     ib = ic;
-    if (pf_on) {
-      if (pf_have) l2_prefetch_instr(P, Ipf);
-      const uint32_t j = i_in + P.l2_ahead;
-      pf_have = j < P.n_instr;
-      if (pf_have) Ipf = P.queue[j];
-    }
     const Src src = src_of(P, in, ext);
     bool stuck = false;
     uint64_t blocked_ns = 0;  // (tracing) time spent waiting for a free stage
@@ -500,6 +475,24 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
   }
 }
 
+// The residual input of an O / down tile output element (thread t owns output
+// (r, b) = (t / B, t % B)); loaded before the tile streams so that its latency
+// is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
+// (RMAX * BMAX_CC <= NT).
+__device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr& in,
+                                                   const GemvDesc& g, int t) {
+  const int B = P.B, l = in.layer;
+  if (t >= g.rows * B) return 0.f;
+  const int r = t / B, b = t % B, row = g.row0 + r;
+  const size_t bh = (size_t)P.max_batch * P.H;
+  if (in.op == OP_O) {
+    if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b) * P.H + row] << 16);
+    return __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
+  }
+  if (in.op == OP_DOWN) return __ldcg(P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row);
+  return 0.f;
+}
+
 // Hand-off buffers between the consumers and the finisher warp: record `hb`
 // holds the instruction whose per-warp sums sit in redw[hb].
 __device__ __forceinline__ volatile uint32_t* hrec_index(const Sh& S, int hb) {
@@ -551,9 +544,27 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
       for (int i = 0; i < RPS; ++i) {
         float a = 0.f;
         if (i < n) {
+          // independent partial sums (one per 8-column group, two halves when
+          // there is one group), added pairwise in a fixed order: short FMA
+          // chains keep the 8 consumer warps issuing
           const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)i * K * 2);
+          constexpr int NP = M > 1 ? M : 2;
+          float pa[NP];
+          if constexpr (M == 1) {
+            const uint4 wv = wrow[t];
+            pa[0] = fmaf(bf_hi(wv.y), xr[0][3], fmaf(bf_lo(wv.y), xr[0][2],
+                    fmaf(bf_hi(wv.x), xr[0][1], bf_lo(wv.x) * xr[0][0])));
+            pa[1] = fmaf(bf_hi(wv.w), xr[0][7], fmaf(bf_lo(wv.w), xr[0][6],
+                    fmaf(bf_hi(wv.z), xr[0][5], bf_lo(wv.z) * xr[0][4])));
+          } else {
 #pragma unroll
-          for (int j = 0; j < M; ++j) a = dot8(wrow[t + NT * j], xr[j], a);
+            for (int j = 0; j < M; ++j) pa[j] = dot8(wrow[t + NT * j], xr[j], 0.f);
+          }
+#pragma unroll
+          for (int step = 1; step < NP; step *= 2)
+#pragma unroll
+            for (int j = 0; j + step < NP; j += 2 * step) pa[j] += pa[j + step];
+          a = pa[0];
         }
         acc[i] = a;
       }
@@ -580,7 +591,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
 
 // ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
 // x[B][K] (normed) staged in shared memory; one warp per (row, sequence) pair.
-__device__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
+__device__ __forceinline__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
                              const Src& src, Ring& R) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int K = g.K, B = P.B, K8 = K / 8;
@@ -643,23 +654,6 @@ __device__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, con
   cbar();
 }
 
-// The residual input of an O / down tile output element (thread t owns output
-// (r, b) = (t / B, t % B)); loaded before the tile streams so that its latency
-// is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
-// (RMAX * BMAX_CC <= NT).
-__device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr& in,
-                                                   const GemvDesc& g, int t) {
-  const int B = P.B, l = in.layer;
-  if (t >= g.rows * B) return 0.f;
-  const int r = t / B, b = t % B, row = g.row0 + r;
-  const size_t bh = (size_t)P.max_batch * P.H;
-  if (in.op == OP_O) {
-    if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b) * P.H + row] << 16);
-    return __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
-  }
-  if (in.op == OP_DOWN) return __ldcg(P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row);
-  return 0.f;
-}
 
 // Store a finished GEMV tile: y[r][b] is in red[r * BMAX_CC + b]; `t` is the
 // (row, sequence) slot of this thread and `pre` its residual input from
@@ -710,7 +704,7 @@ __device__ __forceinline__ void attn_mark(const KParams& P, uint32_t ii, int wor
 }
 
 template <int D, int REP>
-__device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
+__device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
                           uint32_t ii, Ring& R) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int l = in.layer, b = (int)in.a0, g = (int)in.a1, split = (int)in.a2;
@@ -994,7 +988,7 @@ __device__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const 
 }
 
 template <int AD, int AREP>
-__device__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
+__device__ __forceinline__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
                               uint32_t ii, Ring& R) {
   if constexpr (AD != 0) {
     attn_tile<AD, AREP>(P, S, in, e, ii, R);
@@ -1016,7 +1010,7 @@ __device__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, co
 }
 
 // Drain an instruction's stages without computing (after an abort).
-__device__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
+__device__ __forceinline__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
   const uint32_t n = src_stages(instr_src(P, in));
   for (uint32_t k = 0; k < n; ++k) {
     ring_acquire(P, S, R);

@@ -30,7 +30,6 @@ EXPORTED = [
     "mk_decode_step_host", "mk_prefill", "mk_run_per_op", "mk_status", "mk_plan_reset",
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
-    "mk_plan_set_l2_prefetch",
 ]
 
 
@@ -90,7 +89,6 @@ def lib() -> ctypes.CDLL:
     L.mk_plan_set_debug.argtypes = [vp, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
-    L.mk_plan_set_l2_prefetch.argtypes = [vp, ctypes.c_uint32]
     L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, vp]
     L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs),
@@ -248,9 +246,6 @@ class Plan:
                   wait_limit_ns: int = 0) -> None:
         _check(lib().mk_plan_set_debug(self.h, force_ctas, queue_perm_seed, int(trace), wait_limit_ns),
                "mk_plan_set_debug")
-
-    def set_l2_prefetch(self, instructions_ahead: int) -> None:
-        _check(lib().mk_plan_set_l2_prefetch(self.h, instructions_ahead), "mk_plan_set_l2_prefetch")
 
     def debug_drop_release(self, index: int) -> None:
         _check(lib().mk_plan_debug_drop_release(self.h, index), "mk_plan_debug_drop_release")
