@@ -15,9 +15,10 @@ LIB = os.path.join(PKG, "libmk.so")
 
 SOURCES = ["mk_plan.cpp", "mk_capi.cu", "mk_k_generic.cu", "mk_k_h1_f4_d64_r4.cu",
            "mk_k_h2_f7_d128_r4.cu", "mk_k_h2_f6_d128_r4.cu", "mk_gemm.cu", "mk_noalloc.cu",
-           "mk_prefill_plan.cpp", "mk_prefill_kernel.cu"]
+           "mk_prefill_plan.cpp", "mk_prefill_kernel.cu", "mk_bdecode_plan.cpp",
+           "mk_bdecode_kernel.cu"]
 HEADERS = ["mk_internal.h", "mk_plan.h", "mk_device.cuh", "mk_kernel.cuh", "mk_variants.h",
-           "mk_tc.cuh", "mk_tmap.h", "mk_prefill.h"]
+           "mk_tc.cuh", "mk_tmap.h", "mk_prefill.h", "mk_bdecode.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

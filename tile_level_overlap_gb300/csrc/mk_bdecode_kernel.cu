@@ -1,0 +1,886 @@
+// Batched decode interpreter (sm_103a): tensor-core GEMM tiles, CUDA-core
+// split-KV attention, RMSNorm blocks; one persistent CTA per SM, tile-level
+// dependencies through barrier counters (see mk_bdecode.h).
+//
+//  warp 0      producer: pops instructions (one atomic each), streams the
+//              weight k-blocks of a GEMM tile ahead of its dependencies and
+//              the activation k-blocks (hi and lo planes) once they are
+//              satisfied, or the K/V blocks of an attention split, with 2D TMA
+//              loads into a 6 x 32 KB ring.
+//  warp 1      tensor-core issuer: D[128 weight rows][N batch columns] +=
+//              W_tile * x_hi^T, then * x_lo^T, per k-step (tcgen05.mma,
+//              accumulators in TMEM, two 32-column accumulators).
+//  warps 2-5   compute: split-K partial sums, the last chunk's reduction and
+//              epilogue, RMSNorm blocks, the attention splits and their
+//              combine.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mk.h"
+#include "mk_bdecode.h"
+#include "mk_device.cuh"
+#include "mk_internal.h"
+#include "mk_plan.h"
+#include "mk_tc.cuh"
+
+namespace mk {
+namespace {
+
+constexpr int BD_STAGE = 32 * 1024;
+constexpr int BD_NSTAGE = 6;
+constexpr int BD_THREADS = 192;
+constexpr int BD_CBAR = 2;   // named barrier of the compute warps
+constexpr int BD_NC = 128;   // compute threads
+constexpr uint32_t BD_END = 0xffffffffu;
+constexpr uint32_t BD_W_BYTES = BD_M * BD_BK * 2;  // weight box(es) of a stage: 16 KB
+constexpr int BD_ACC_COLS = 32;                    // TMEM columns per accumulator
+
+struct BdSmem {
+  static constexpr int ring = 0;
+  static constexpr int scratch = ring + BD_NSTAGE * BD_STAGE;  // [128][BD_NMAX] f32
+  static constexpr int qs = scratch + BD_M * BD_NMAX * 4;      // [4][128] f32
+  static constexpr int sc = qs + 4 * 128 * 4;                  // [4][BD_KEYS] f32
+  static constexpr int hs = sc + 4 * BD_KEYS * 4;              // [4] x {m, l, alpha} + inv norms [64]
+  static constexpr int bars = hs + (16 + 64) * 4;
+  // full[6] empty[6] ifull[8] iempty[8] accf[2] acce[2]
+  static constexpr int n_mbar = 2 * BD_NSTAGE + 2 * NISLOT + 4;
+  static constexpr int islot = bars + n_mbar * 8;
+  static constexpr int flags = islot + NISLOT * 48;  // [16] u32
+  static constexpr int seq = flags + 16 * 4;         // positions[BD_NMAX], tokens[BD_NMAX]
+  static constexpr int total = seq + 2 * BD_NMAX * 4;
+};
+static_assert(BdSmem::total <= 227 * 1024, "batched decode shared memory budget");
+static_assert(BdSmem::scratch % 1024 == 0, "ring stages stay 1024-aligned");
+
+enum BdFlag { BF_GEN = 0, BF_SLOT = 1, BF_ABORT = 2, BF_TMEM = 3, BF_LAST = 4 };
+
+struct BdSh {
+  uint8_t* ring;
+  float *scratch, *qs, *sc, *hs;
+  uint64_t *full, *empty, *ifull, *iempty, *accf, *acce;
+  uint8_t* islot;
+  volatile uint32_t* flags;
+  int32_t *pos, *tok;
+};
+
+__device__ __forceinline__ BdSh bd_map(uint8_t* base) {
+  BdSh s;
+  s.ring = base + BdSmem::ring;
+  s.scratch = reinterpret_cast<float*>(base + BdSmem::scratch);
+  s.qs = reinterpret_cast<float*>(base + BdSmem::qs);
+  s.sc = reinterpret_cast<float*>(base + BdSmem::sc);
+  s.hs = reinterpret_cast<float*>(base + BdSmem::hs);
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + BdSmem::bars);
+  s.full = b;
+  s.empty = b + BD_NSTAGE;
+  s.ifull = b + 2 * BD_NSTAGE;
+  s.iempty = s.ifull + NISLOT;
+  s.accf = s.iempty + NISLOT;
+  s.acce = s.accf + 2;
+  s.islot = base + BdSmem::islot;
+  s.flags = reinterpret_cast<volatile uint32_t*>(base + BdSmem::flags);
+  s.pos = reinterpret_cast<int32_t*>(base + BdSmem::seq);
+  s.tok = s.pos + BD_NMAX;
+  return s;
+}
+
+__device__ void bd_error(const BdParams& P, uint32_t code, uint32_t detail) {
+  if (atomicCAS(&P.ctl[CTL_STATUS], 0u, code) == 0u) atomicExch(&P.ctl[CTL_DETAIL], detail);
+  atomicExch(&P.ctl[CTL_ABORT], 1u);
+}
+
+// Bounded mbarrier wait; after an abort (another wait already gave up) it
+// gives up within ~10 us so a broken launch drains.
+__device__ __forceinline__ bool bd_wait(const BdParams& P, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t dt = globaltimer() - t0;
+    if (dt > P.wait_limit_ns * 4ull) {
+      bd_error(P, MK_ERR_TIMEOUT, 0xfffffff2u);
+      return false;
+    }
+    if ((it & 255u) == 0 && dt > 10000ull && ld_volatile(&P.ctl[CTL_ABORT]) != 0u) return false;
+  }
+}
+
+// Bounded acquire-spin on the counter an instruction waits on.
+__device__ bool bd_wait_deps(const BdParams& P, const Instr& in, uint32_t gen, uint32_t idx) {
+  if (P.mode != MODE_MEGA || in.wait_bar == NO_BAR) return true;
+  const uint32_t target = (gen + 1u) * in.wait_target;
+  const uint32_t* c = &P.bars[in.wait_bar];
+  const uint64_t t0 = globaltimer();
+  while ((int32_t)(ld_acquire_gpu(c) - target) < 0) {
+    if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) return false;
+    if (globaltimer() - t0 > P.wait_limit_ns) {
+      bd_error(P, MK_ERR_TIMEOUT, idx);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+__device__ __forceinline__ const CUtensorMap* tmap(const BdParams& P, int idx) {
+  return reinterpret_cast<const CUtensorMap*>(P.tm) + idx;
+}
+__device__ __forceinline__ int gmap(const BdParams& P, int which) {
+  return P.L * BD_TM_PER_LAYER + which;
+}
+
+__device__ __forceinline__ bool is_gemm(uint8_t op) {
+  return op == BD_QKV || op == BD_O || op == BD_GU || op == BD_DOWN || op == BD_LM;
+}
+__device__ __forceinline__ bool is_norm(uint8_t op) {
+  return op == BD_NORM1 || op == BD_NORM2 || op == BD_NORMF;
+}
+
+// GEMM geometry of an instruction (row tile a0, K chunk a1).
+struct BdGemm {
+  int K;                    // full reduction length
+  int k0, nk;               // first column and 64-column steps of this chunk
+  int chunks;               // chunks of the row tile
+  int a_map, a_row;         // weight map and first row (GU: gate map; up map = a_map + 1)
+  bool gu;                  // two 64-row weight boxes (gate, up)
+  int x_map;                // activation map (hi rows [0, nb), lo rows [nb, 2 nb))
+  uint32_t tile;            // row tile within the operator (split-K partials, arrival counter)
+};
+
+__device__ __forceinline__ BdGemm bd_gemm(const BdParams& P, const Instr& in) {
+  BdGemm g;
+  const int l = in.layer, m = (int)in.a0, c = (int)in.a1;
+  const int qd = P.nq * P.d, kd = P.nkv * P.d;
+  g.gu = false;
+  switch (in.op) {
+    case BD_QKV: {
+      g.K = P.H;
+      g.chunks = (int)P.c_h;
+      g.x_map = gmap(P, TMB_HN);
+      const int r = m * BD_M;
+      if (r < qd) { g.a_map = l * BD_TM_PER_LAYER + TMB_WQ; g.a_row = r; }
+      else if (r < qd + kd) { g.a_map = l * BD_TM_PER_LAYER + TMB_WK; g.a_row = r - qd; }
+      else { g.a_map = l * BD_TM_PER_LAYER + TMB_WV; g.a_row = r - qd - kd; }
+      break;
+    }
+    case BD_O:
+      g.K = qd;
+      g.chunks = (int)P.c_q;
+      g.x_map = gmap(P, TMB_AO);
+      g.a_map = l * BD_TM_PER_LAYER + TMB_WO;
+      g.a_row = m * BD_M;
+      break;
+    case BD_GU:
+      g.K = P.H;
+      g.chunks = (int)P.c_h;
+      g.x_map = gmap(P, TMB_HN);
+      g.a_map = l * BD_TM_PER_LAYER + TMB_WG;
+      g.a_row = m * (BD_M / 2);
+      g.gu = true;
+      break;
+    case BD_DOWN:
+      g.K = P.F;
+      g.chunks = (int)P.c_f;
+      g.x_map = gmap(P, TMB_ACT);
+      g.a_map = l * BD_TM_PER_LAYER + TMB_WD;
+      g.a_row = m * BD_M;
+      break;
+    default:  // BD_LM: one chunk (its 128-row tiles are plentiful)
+      g.K = P.H;
+      g.chunks = 1;
+      g.x_map = gmap(P, TMB_HN);
+      g.a_map = gmap(P, TMB_LM);
+      g.a_row = m * BD_M;
+      break;
+  }
+  // Partial sums and arrival counters are indexed by the row tile within the
+  // operator: an operator starts only after every tile of the previous one has
+  // released, so the buffers are reused operator after operator.
+  g.tile = (uint32_t)m;
+  const int kc = g.chunks == 1 ? g.K : (g.K < BD_KC ? g.K : BD_KC);
+  g.k0 = c * kc;
+  g.nk = kc / BD_BK;
+  return g;
+}
+
+// Attention split extent: keys [lo, hi) of the positions[b] + 1 visible keys.
+struct BdAttn {
+  int lo, hi;
+  bool live;
+};
+__device__ __forceinline__ BdAttn bd_attn(const BdParams& P, const BdSh& S, const Instr& in) {
+  BdAttn e;
+  const int b = (int)in.a0, s = (int)in.a2;
+  e.live = b < P.B;
+  e.lo = e.hi = 0;
+  if (e.live) {
+    const int n = S.pos[b] + 1;
+    const int len = (n + BD_NSPLIT - 1) / BD_NSPLIT;
+    e.lo = s * len < n ? s * len : n;
+    e.hi = e.lo + len < n ? e.lo + len : n;
+  }
+  return e;
+}
+__device__ __forceinline__ int attn_blocks(const BdAttn& e) {
+  return e.hi > e.lo ? (e.hi - e.lo + BD_KEYS - 1) / BD_KEYS : 0;
+}
+// Ring stages an instruction occupies (known to every role from the record).
+__device__ __forceinline__ int bd_stages(const BdParams& P, const BdSh& S, const Instr& in) {
+  if (is_gemm(in.op)) return bd_gemm(P, in).nk;
+  if (in.op == BD_ATTN) return attn_blocks(bd_attn(P, S, in));
+  return 0;
+}
+
+__device__ __forceinline__ size_t cache_row(const BdParams& P, int l, int kv, int b, int g) {
+  return ((((size_t)l * 2 + kv) * P.max_batch + b) * P.nkv + g) * (size_t)P.max_ctx;
+}
+
+// ---------------------------------------------------------------- producer
+__device__ void bd_producer(const BdParams& P, const BdSh& S) {
+  if ((threadIdx.x & 31) != 0) return;
+  const uint64_t pol_w = policy_evict_first();  // weights: streamed once
+  const uint64_t pol_a = policy_evict_last();   // activations / KV: re-read by other tiles
+  const uint32_t gen = S.flags[BF_GEN];
+  uint32_t stage_ctr = 0, islot_ctr = 0;
+  bool first = true;
+  for (;;) {
+    uint32_t i;
+    if (P.mode == MODE_MEGA) {
+      i = ld_volatile(&P.ctl[CTL_ABORT]) ? BD_END : atomicAdd(&P.ctl[CTL_HEAD], 1u);
+      if (i >= P.n_instr) i = BD_END;
+    } else {
+      i = first ? P.perop_base + blockIdx.x : BD_END;
+      first = false;
+    }
+    const int si = islot_ctr % NISLOT;
+    bool end = i == BD_END;
+    if (!bd_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) end = true;
+    Instr in;
+    if (!end) {
+      in = P.queue[i];
+      *reinterpret_cast<Instr*>(S.islot + si * 48 + 16) = in;
+    }
+    *reinterpret_cast<volatile uint32_t*>(S.islot + si * 48) = end ? BD_END : i;
+    mbar_arrive(&S.ifull[si]);
+    ++islot_ctr;
+    if (end) break;
+
+    if (is_gemm(in.op)) {
+      const BdGemm g = bd_gemm(P, in);
+      const int npre = g.nk < BD_NSTAGE ? g.nk : BD_NSTAGE;
+      const uint32_t xb = (uint32_t)P.nb * BD_BK * 2;  // one activation plane box
+      const uint32_t tx = BD_W_BYTES + 2 * xb;
+      const uint32_t s0 = stage_ctr;
+      auto load_w = [&](uint8_t* sp, int kb, uint64_t* bar) {
+        const int x = g.k0 + kb * BD_BK;
+        if (g.gu) {
+          tma_load_2d(sp, tmap(P, g.a_map), x, g.a_row, bar, pol_w);
+          tma_load_2d(sp + BD_W_BYTES / 2, tmap(P, g.a_map + 1), x, g.a_row, bar, pol_w);
+        } else {
+          tma_load_2d(sp, tmap(P, g.a_map), x, g.a_row, bar, pol_w);
+        }
+      };
+      auto load_x = [&](uint8_t* sp, int kb, uint64_t* bar) {
+        const int x = g.k0 + kb * BD_BK;
+        tma_load_2d(sp + BD_W_BYTES, tmap(P, g.x_map), x, 0, bar, pol_a);
+        tma_load_2d(sp + BD_W_BYTES + xb, tmap(P, g.x_map), x, P.nb, bar, pol_a);
+      };
+      // weights first: they depend on nothing
+      for (int kb = 0; kb < npre; ++kb) {
+        const int st = stage_ctr % BD_NSTAGE;
+        bd_wait(P, &S.empty[st], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
+        mbar_arrive_expect_tx(&S.full[st], tx);
+        load_w(S.ring + st * BD_STAGE, kb, &S.full[st]);
+        ++stage_ctr;
+      }
+      // (after a timeout the loads still run, on stale but valid memory, so
+      // that every armed stage completes and the launch can drain)
+      bd_wait_deps(P, in, gen, i);
+      fence_proxy_async_global();
+      for (int kb = 0; kb < npre; ++kb) {
+        const int st = (s0 + kb) % BD_NSTAGE;
+        load_x(S.ring + st * BD_STAGE, kb, &S.full[st]);
+      }
+      for (int kb = npre; kb < g.nk; ++kb) {
+        const int st = stage_ctr % BD_NSTAGE;
+        bd_wait(P, &S.empty[st], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
+        mbar_arrive_expect_tx(&S.full[st], tx);
+        load_w(S.ring + st * BD_STAGE, kb, &S.full[st]);
+        load_x(S.ring + st * BD_STAGE, kb, &S.full[st]);
+        ++stage_ctr;
+      }
+    } else if (in.op == BD_ATTN) {
+      const BdAttn e = bd_attn(P, S, in);
+      const int nblk = attn_blocks(e);
+      if (nblk == 0) continue;
+      bd_wait_deps(P, in, gen, i);
+      fence_proxy_async_global();
+      const int l = in.layer, b = (int)in.a0, g = (int)in.a1;
+      const int nbox = P.d / 64;
+      const uint32_t half = BD_STAGE / 2;
+      for (int j = 0; j < nblk; ++j) {
+        const int st = stage_ctr % BD_NSTAGE;
+        bd_wait(P, &S.empty[st], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
+        uint8_t* sp = S.ring + st * BD_STAGE;
+        mbar_arrive_expect_tx(&S.full[st], 2u * BD_KEYS * P.d * 2);
+        for (int kv = 0; kv < 2; ++kv)
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(sp + kv * half + bx * (BD_KEYS * 128), tmap(P, gmap(P, TMB_KV)), bx * 64,
+                        (int)(cache_row(P, l, kv, b, g) + e.lo + j * BD_KEYS), &S.full[st], pol_a);
+        ++stage_ctr;
+      }
+    }
+  }
+  // the copies this thread issued have landed before it leaves
+  for (uint32_t k = 0; k < BD_NSTAGE && k < stage_ctr; ++k) {
+    const uint32_t c = stage_ctr - 1 - k;
+    bd_wait(P, &S.full[c % BD_NSTAGE], (c / BD_NSTAGE) & 1u);
+  }
+}
+
+// ---------------------------------------------------------------- tensor-core issuer
+__device__ void bd_mma(const BdParams& P, const BdSh& S, uint32_t tbase) {
+  if ((threadIdx.x & 31) != 0) return;
+  uint32_t islot_ctr = 0, stage_ctr = 0, use[2] = {0, 0};
+  const uint32_t idesc = idesc_bf16_f32(BD_M, P.nb);
+  const uint32_t xb = (uint32_t)P.nb * BD_BK * 2;
+  for (;;) {
+    const int si = islot_ctr % NISLOT;
+    bd_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u);
+    const uint32_t i = *reinterpret_cast<volatile uint32_t*>(S.islot + si * 48);
+    Instr in;
+    if (i != BD_END) in = *reinterpret_cast<const Instr*>(S.islot + si * 48 + 16);
+    mbar_arrive(&S.iempty[si]);
+    ++islot_ctr;
+    if (i == BD_END) break;
+    if (is_gemm(in.op)) {
+      const BdGemm g = bd_gemm(P, in);
+      const int ab = (int)((use[0] + use[1]) & 1u);
+      bd_wait(P, &S.acce[ab], (use[ab] & 1u) ^ 1u);
+      ++use[ab];
+      tc_fence_after();
+      const uint32_t d = tbase + (uint32_t)ab * BD_ACC_COLS;
+      for (int kb = 0; kb < g.nk; ++kb) {
+        const int st = stage_ctr % BD_NSTAGE;
+        bd_wait(P, &S.full[st], (stage_ctr / BD_NSTAGE) & 1u);
+        ++stage_ctr;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(S.ring + st * BD_STAGE);
+        const uint32_t bh = a0 + BD_W_BYTES, bl = bh + xb;
+#pragma unroll
+        for (int k = 0; k < BD_BK / 16; ++k) {
+          const uint64_t ad = sdesc_sw128(a0 + 32 * k);
+          tc_mma(d, ad, sdesc_sw128(bh + 32 * k), idesc, (kb | k) != 0);
+          tc_mma(d, ad, sdesc_sw128(bl + 32 * k), idesc, true);
+        }
+        tc_commit(&S.empty[st]);
+      }
+      tc_commit(&S.accf[ab]);
+    } else if (in.op == BD_ATTN) {
+      stage_ctr += (uint32_t)bd_stages(P, S, in);  // consumed by the compute warps
+    }
+  }
+}
+
+// ---------------------------------------------------------------- compute warps
+__device__ __forceinline__ void cbar_bd() { named_bar(BD_CBAR, BD_NC); }
+
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+__device__ __forceinline__ float bfw(const uint16_t* p, int i) {
+  return __uint_as_float((uint32_t)__ldg(p + i) << 16);
+}
+
+// RMSNorm of sequences [8 r, 8 r + 8) into the hi/lo planes of hn.
+__device__ void bd_norm(const BdParams& P, const BdSh& S, const Instr& in, int wc, int lane) {
+  const int l = in.layer, H = P.H;
+  const float* src;
+  const uint16_t* gain;
+  if (in.op == BD_NORM1) {
+    src = l == 0 ? nullptr : P.xb;
+    gain = P.layers[l].attn_norm;
+  } else if (in.op == BD_NORM2) {
+    src = P.xa;
+    gain = P.layers[l].ffn_norm;
+  } else {
+    src = P.xb;
+    gain = P.final_norm;
+  }
+  for (int r = wc; r < BD_RG; r += 4) {
+    const int b = (int)in.a0 * BD_RG + r;
+    if (b >= P.B) break;
+    const uint16_t* emb = nullptr;
+    if (!src) {
+      int tok = S.tok[b];
+      if (tok < 0 || tok >= P.V) {
+        if (lane == 0) bd_error(P, MK_ERR_BOUNDS, (uint32_t)b);
+        tok = 0;
+      }
+      emb = P.embed + (size_t)tok * H;
+    }
+    auto xval = [&](int c) -> float { return emb ? bfw(emb, c) : __ldcg(src + (size_t)b * H + c); };
+    float ss = 0.f;
+    for (int c = lane; c < H; c += 32) {
+      const float x = xval(c);
+      ss = fmaf(x, x, ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)H + P.eps);
+    for (int c = lane; c < H; c += 32) {
+      uint16_t hi, lo;
+      split_bf16(xval(c) * inv * bfw(gain, c), hi, lo);
+      P.hn[(size_t)b * H + c] = hi;
+      P.hn[((size_t)P.nb + b) * H + c] = lo;
+    }
+  }
+}
+
+// Epilogue of a finished GEMM row tile: y[b] is this thread's row (feature
+// 128 m + row) for sequence b.
+__device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, int row,
+                            const float (&y)[BD_NMAX]) {
+  const int l = in.layer, m = (int)in.a0, tc = threadIdx.x - 64;
+  const int B = P.B, H = P.H, d = P.d, qd = P.nq * d, kd = P.nkv * d;
+  switch (in.op) {
+    case BD_O:
+    case BD_DOWN: {
+      const int f = m * BD_M + row;
+      float* dst = in.op == BD_O ? P.xa : P.xb;
+      const float* res = in.op == BD_O ? P.xb : P.xa;
+      for (int b = 0; b < B; ++b) {
+        float r;
+        if (in.op == BD_O && l == 0) {
+          int tok = S.tok[b];
+          if (tok < 0 || tok >= P.V) tok = 0;  // reported by the layer-0 norm
+          r = bfw(P.embed + (size_t)tok * H, f);
+        } else {
+          r = __ldcg(res + (size_t)b * H + f);
+        }
+        dst[(size_t)b * H + f] = r + y[b];
+      }
+      break;
+    }
+    case BD_LM: {
+      const int f = m * BD_M + row;
+      if (f < P.V)
+        for (int b = 0; b < B; ++b) P.logits[(size_t)b * P.V + f] = y[b];
+      break;
+    }
+    case BD_GU: {
+      // rows 0..63 gate, 64..127 up (features 64 m + j)
+      for (int b = 0; b < BD_NMAX; ++b) S.scratch[row * BD_NMAX + b] = y[b];
+      cbar_bd();
+      const int j = tc & 63;
+      for (int b = tc >> 6; b < B; b += 2) {
+        const float gt = S.scratch[j * BD_NMAX + b], up = S.scratch[(64 + j) * BD_NMAX + b];
+        uint16_t hi, lo;
+        split_bf16(gt / (1.0f + expf(-gt)) * up, hi, lo);
+        const size_t o = (size_t)b * P.F + (size_t)m * (BD_M / 2) + j;
+        P.act[o] = hi;
+        P.act[o + (size_t)P.nb * P.F] = lo;
+      }
+      break;
+    }
+    default: {  // BD_QKV
+      const int f0 = m * BD_M;
+      if (f0 >= qd + kd) {  // values: straight into the cache
+        const int f = f0 + row - qd - kd, g = f / d, dim = f % d;
+        for (int b = 0; b < B; ++b)
+          P.kv[(cache_row(P, l, 1, b, g) + S.pos[b]) * d + dim] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(y[b]));
+        break;
+      }
+      for (int b = 0; b < BD_NMAX; ++b) S.scratch[row * BD_NMAX + b] = y[b];
+      cbar_bd();
+      const bool is_q = f0 < qd;
+      const int hpt = BD_M / d;  // heads in this tile
+      float* inv = S.hs + 16;    // [b][hpt] (<= 64)
+      if (P.qk_norm) {
+        for (int t = tc; t < B * hpt; t += BD_NC) {
+          const int b = t / hpt, hh = t % hpt;
+          float ss = 0.f;
+          for (int i = 0; i < d; ++i) {
+            const float v = S.scratch[(hh * d + i) * BD_NMAX + b];
+            ss = fmaf(v, v, ss);
+          }
+          inv[t] = 1.0f / sqrtf(ss / (float)d + P.eps);
+        }
+        cbar_bd();
+      }
+      const uint16_t* gn = P.qk_norm ? (is_q ? P.layers[l].q_norm : P.layers[l].k_norm) : nullptr;
+      const int half = d / 2;
+      // pair i of head hh for sequence b: thread tc takes pair index tc % 64
+      const int pi = tc & 63, hh = pi / half, i = pi % half;
+      for (int b = tc >> 6; b < B; b += 2) {
+        float u1 = S.scratch[(hh * d + i) * BD_NMAX + b];
+        float u2 = S.scratch[(hh * d + i + half) * BD_NMAX + b];
+        if (gn) {
+          const float iv = inv[b * hpt + hh];
+          u1 = u1 * iv * bfw(gn, i);
+          u2 = u2 * iv * bfw(gn, i + half);
+        }
+        const float2 cs = __ldg(P.rope + (size_t)S.pos[b] * half + i);
+        const float r1 = u1 * cs.x - u2 * cs.y, r2 = u2 * cs.x + u1 * cs.y;
+        const int f = f0 + hh * d;  // first feature of the head
+        if (is_q) {
+          P.q[(size_t)b * qd + f + i] = r1;
+          P.q[(size_t)b * qd + f + i + half] = r2;
+        } else {
+          const int g = (f - qd) / d;
+          uint16_t* kr = P.kv + (cache_row(P, l, 0, b, g) + S.pos[b]) * d;
+          kr[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r1));
+          kr[i + half] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+        }
+      }
+      break;
+    }
+  }
+}
+
+// One attention split of (sequence b, kv head g): online softmax over its key
+// blocks (K and V tiles in the ring, 128-byte swizzled rows), then the split's
+// (max, sum, unnormalised output) to global memory.  Returns the ring counter.
+template <int D>
+__device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr& in, const BdAttn& e,
+                                  uint32_t stage_ctr) {
+  const int tc = threadIdx.x - 64, lane = tc & 31, wc = tc >> 5;
+  const int b = (int)in.a0, g = (int)in.a1, s = (int)in.a2, rep = P.rep;
+  const int qd = P.nq * D;
+  const float scale = 1.0f / sqrtf((float)D);
+  float* qs = S.qs;     // [rep][D]
+  float* sc = S.sc;     // [rep][BD_KEYS]
+  float* hs = S.hs;     // [rep] x {m, l, alpha}
+  for (int t = tc; t < rep * D; t += BD_NC) qs[t] = __ldcg(P.q + (size_t)b * qd + (size_t)g * rep * D + t);
+  if (tc < rep) {
+    hs[tc * 3 + 0] = -INFINITY;
+    hs[tc * 3 + 1] = 0.f;
+    hs[tc * 3 + 2] = 0.f;
+  }
+  cbar_bd();
+  constexpr int DPL = D / 32;  // output columns per lane in P V
+  float o[DPL];
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) o[k] = 0.f;
+  const int hpt = (rep + 1) / 2;  // heads per thread in the score pass
+  const int nblk = attn_blocks(e);
+  for (int j = 0; j < nblk; ++j) {
+    const int st = stage_ctr % BD_NSTAGE;
+    bd_wait(P, &S.full[st], (stage_ctr / BD_NSTAGE) & 1u);
+    ++stage_ctr;
+    const uint8_t* kt = S.ring + st * BD_STAGE;
+    const uint8_t* vt = kt + BD_STAGE / 2;
+    // scores: thread -> key k (64 keys), heads [hh0, hh0 + hpt)
+    {
+      const int k = tc & 63, hh0 = (tc >> 6) * hpt;
+      const int key = e.lo + j * BD_KEYS + k;
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        const int bx = c8 >> 3, cc = c8 & 7;
+        const uint4 w = *reinterpret_cast<const uint4*>(kt + bx * (BD_KEYS * 128) + k * 128 +
+                                                        ((cc ^ (k & 7)) << 4));
+        float kx[8];
+        widen8(w, kx);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int h = hh0 + u;
+          if (u < hpt && h < rep) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) a[u] = fmaf(qs[h * D + c8 * 8 + t], kx[t], a[u]);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int h = hh0 + u;
+        if (u < hpt && h < rep) sc[h * BD_KEYS + k] = key < e.hi ? a[u] * scale : -INFINITY;
+      }
+    }
+    cbar_bd();
+    // online softmax: warp h owns head h
+    if (wc < rep) {
+      const float s0 = sc[wc * BD_KEYS + lane], s1 = sc[wc * BD_KEYS + lane + 32];
+      const float mx = warp_max(fmaxf(s0, s1));
+      const float m_old = hs[wc * 3 + 0];
+      const float m_new = fmaxf(m_old, mx);
+      const float alpha = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
+      const float p0 = s0 == -INFINITY ? 0.f : expf(s0 - m_new);
+      const float p1 = s1 == -INFINITY ? 0.f : expf(s1 - m_new);
+      sc[wc * BD_KEYS + lane] = p0;
+      sc[wc * BD_KEYS + lane + 32] = p1;
+      const float ps = warp_sum(p0 + p1);
+      __syncwarp();
+      if (lane == 0) {
+        hs[wc * 3 + 0] = m_new;
+        hs[wc * 3 + 1] = hs[wc * 3 + 1] * alpha + ps;
+        hs[wc * 3 + 2] = alpha;
+      }
+    }
+    cbar_bd();
+    // P V: warp h owns head h, lane the columns [DPL lane, DPL lane + DPL)
+    if (wc < rep) {
+      const float alpha = hs[wc * 3 + 2];
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) o[k] *= alpha;
+      const int col = lane * DPL, bx = col >> 6, cin = col & 63;
+      // keys past the split are skipped, not weighted by zero: the cache
+      // rows there may hold anything
+      const int kval = e.hi - (e.lo + j * BD_KEYS) < BD_KEYS ? e.hi - (e.lo + j * BD_KEYS) : BD_KEYS;
+      for (int k = 0; k < kval; ++k) {
+        const float p = sc[wc * BD_KEYS + k];
+        const uint8_t* vr = vt + bx * (BD_KEYS * 128) + k * 128 + ((((cin >> 3) ^ (k & 7))) << 4) + (cin & 7) * 2;
+        if constexpr (DPL == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(vr);
+          o[0] = fmaf(p, bf_lo(u.x), o[0]);
+          o[1] = fmaf(p, bf_hi(u.x), o[1]);
+          o[2] = fmaf(p, bf_lo(u.y), o[2]);
+          o[3] = fmaf(p, bf_hi(u.y), o[3]);
+        } else {
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
+          o[0] = fmaf(p, bf_lo(u), o[0]);
+          o[1] = fmaf(p, bf_hi(u), o[1]);
+        }
+      }
+    }
+    cbar_bd();  // every warp is done with the stage and the probabilities
+    if (tc == 0) mbar_arrive(&S.empty[st]);
+  }
+  // the split's partial: o (unnormalised), max, sum per head
+  float* part = P.apart + (((size_t)b * P.nkv + g) * BD_NSPLIT + s) * rep * (D + 2);
+  if (wc < rep) {
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) part[wc * (D + 2) + lane * DPL + k] = o[k];
+    if (lane == 0) {
+      part[wc * (D + 2) + D] = hs[wc * 3 + 0];
+      part[wc * (D + 2) + D + 1] = hs[wc * 3 + 1];
+    }
+  }
+  return stage_ctr;
+}
+
+// Combine the splits of (b, g) in split order into the hi/lo planes of ao.
+template <int D>
+__device__ void bd_attn_combine(const BdParams& P, int b, int g) {
+  const int tc = threadIdx.x - 64, rep = P.rep, qd = P.nq * D;
+  const float* gp = P.apart + ((size_t)b * P.nkv + g) * BD_NSPLIT * rep * (D + 2);
+  for (int t = tc; t < rep * D; t += BD_NC) {
+    const int h = t / D, c = t % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < BD_NSPLIT; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
+    float Lsum = 0.f, O = 0.f;
+#pragma unroll
+    for (int s = 0; s < BD_NSPLIT; ++s) {
+      const float* ps = gp + ((size_t)s * rep + h) * (D + 2);
+      const float ms = __ldcg(ps + D);
+      const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+      Lsum = fmaf(__ldcg(ps + D + 1), f, Lsum);
+      O = fmaf(__ldcg(ps + c), f, O);
+    }
+    uint16_t hi, lo;
+    split_bf16(O / Lsum, hi, lo);
+    const size_t o = (size_t)b * qd + (size_t)(g * rep + h) * D + c;
+    P.ao[o] = hi;
+    P.ao[o + (size_t)P.nb * qd] = lo;
+  }
+}
+
+__device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
+  const int wc = (threadIdx.x >> 5) - 2;  // 0..3
+  const int lane = threadIdx.x & 31;
+  const int tc = threadIdx.x - 64;
+  const int q = (threadIdx.x >> 5) & 3;   // TMEM lane quarter this warp may access
+  const int row = 32 * q + lane;
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const uint32_t gen = S.flags[BF_GEN];
+  uint32_t islot_ctr = 0, use[2] = {0, 0}, stage_ctr = 0;
+  for (;;) {
+    const int si = islot_ctr % NISLOT;
+    if (tc == 0) {
+      uint32_t v = BD_END;
+      if (bd_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u))
+        v = *reinterpret_cast<volatile uint32_t*>(S.islot + si * 48);
+      S.flags[BF_SLOT] = v;
+    }
+    cbar_bd();
+    const uint32_t i = S.flags[BF_SLOT];
+    Instr in;
+    if (i != BD_END) in = *reinterpret_cast<const Instr*>(S.islot + si * 48 + 16);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.iempty[si]);
+    ++islot_ctr;
+    if (i == BD_END) break;
+    bool release = true;
+    if (is_gemm(in.op)) {
+      const BdGemm gm = bd_gemm(P, in);
+      const int ab = (int)((use[0] + use[1]) & 1u);
+      bd_wait(P, &S.accf[ab], use[ab] & 1u);
+      ++use[ab];
+      stage_ctr += (uint32_t)gm.nk;
+      tc_fence_after();
+      float y[BD_NMAX];
+      const uint32_t t0 = tbase + (uint32_t)ab * BD_ACC_COLS + lane_base;
+      {
+        float v[16];
+        tmem_ld16(t0, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) y[k] = v[k];
+        if (P.nb > 16) {
+          tmem_ld16(t0 + 16, v);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) y[16 + k] = v[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) y[16 + k] = 0.f;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acce[ab]);
+      if (gm.chunks > 1) {
+        // split-K: publish this chunk's partial; the last chunk to arrive adds
+        // all chunks in chunk order and runs the epilogue
+        float* mine = P.part + ((size_t)gm.tile * gm.chunks + in.a1) * BD_NMAX * BD_M;
+#pragma unroll
+        for (int b = 0; b < BD_NMAX; ++b) mine[b * BD_M + row] = y[b];
+        cbar_bd();
+        if (tc == 0) {
+          uint32_t* arr = P.arrive + gm.tile;
+          const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
+          const bool last = old == (uint32_t)(gm.chunks - 1);
+          if (last) *arr = 0u;
+          S.flags[BF_LAST] = last ? 1u : 0u;
+        }
+        cbar_bd();
+        release = S.flags[BF_LAST] != 0u;
+        if (release) {
+          const float* base = P.part + (size_t)gm.tile * gm.chunks * BD_NMAX * BD_M;
+#pragma unroll
+          for (int b = 0; b < BD_NMAX; ++b) y[b] = 0.f;
+          for (int c = 0; c < gm.chunks; ++c)
+#pragma unroll
+            for (int b = 0; b < BD_NMAX; ++b)
+              y[b] += __ldcg(base + ((size_t)c * BD_NMAX + b) * BD_M + row);
+        }
+      }
+      if (release) bd_epilogue(P, S, in, row, y);
+    } else if (in.op == BD_ATTN) {
+      const BdAttn e = bd_attn(P, S, in);
+      if (!e.live) {
+        release = in.a2 == 0;  // one release per dead (b, g) group
+      } else {
+        if (tc == 0) S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+        cbar_bd();
+        if (P.d == 128) stage_ctr = bd_attn_split<128>(P, S, in, e, stage_ctr);
+        else stage_ctr = bd_attn_split<64>(P, S, in, e, stage_ctr);
+        cbar_bd();
+        if (tc == 0) {
+          uint32_t* arr = P.arrive + P.n_arrive_gemm + (size_t)in.a0 * P.nkv + in.a1;
+          const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
+          const bool last = old == (uint32_t)(BD_NSPLIT - 1);
+          if (last) *arr = 0u;
+          S.flags[BF_LAST] = last ? 1u : 0u;
+        }
+        cbar_bd();
+        release = S.flags[BF_LAST] != 0u;
+        if (release) {
+          if (P.d == 128) bd_attn_combine<128>(P, (int)in.a0, (int)in.a1);
+          else bd_attn_combine<64>(P, (int)in.a0, (int)in.a1);
+        }
+      }
+    } else if (is_norm(in.op)) {
+      if (tc == 0) S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+      cbar_bd();
+      if (!S.flags[BF_ABORT]) bd_norm(P, S, in, wc, lane);
+    }
+    fence_proxy_async_global();  // outputs are read by other CTAs' TMA loads
+    cbar_bd();
+    if (tc == 0 && release && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
+      red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+  }
+}
+
+__global__ void __launch_bounds__(BD_THREADS, 1) mk_bdecode_kernel(const __grid_constant__ BdParams P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const BdSh S = bd_map(smem);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < BD_NSTAGE; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < NISLOT; ++s) {
+      mbar_init(&S.ifull[s], 1);
+      mbar_init(&S.iempty[s], 5);  // issuer + 4 compute warps
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.accf[b], 1);
+      mbar_init(&S.acce[b], 4);
+    }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    S.flags[BF_GEN] = P.mode == MODE_MEGA ? ld_volatile(&P.ctl[CTL_GEN]) : 0u;
+  }
+  if (threadIdx.x < BD_NMAX) {
+    const bool live = (int)threadIdx.x < P.B;
+    int pos = live ? P.positions[threadIdx.x] : 0;
+    if (pos < 0 || pos >= P.max_ctx) {
+      // the new key would land outside its cache slot: report it and run the
+      // sequence at position 0 (in bounds; its result is not meaningful)
+      if (blockIdx.x == 0) bd_error(P, MK_ERR_BOUNDS, threadIdx.x);
+      pos = 0;
+    }
+    S.pos[threadIdx.x] = pos;
+    S.tok[threadIdx.x] = live ? P.tokens[threadIdx.x] : 0;
+  }
+  if (warp == 1) tmem_alloc(reinterpret_cast<uint32_t*>(const_cast<uint32_t*>(&S.flags[BF_TMEM])), 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = S.flags[BF_TMEM];
+  if (warp == 0) bd_producer(P, S);
+  else if (warp == 1) bd_mma(P, S, tbase);
+  else bd_compute(P, S, tbase);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 64);
+  }
+  if (threadIdx.x == 0 && P.mode == MODE_MEGA) {
+    __threadfence();
+    const uint32_t old = atomicAdd(&P.ctl[CTL_EXIT], 1u);
+    if (old == gridDim.x - 1) {
+      P.ctl[CTL_HEAD] = 0u;
+      P.ctl[CTL_EXIT] = 0u;
+      P.ctl[CTL_GEN] = S.flags[BF_GEN] + 1u;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t bd_setup() {
+  return cudaFuncSetAttribute(mk_bdecode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              BdSmem::total);
+}
+cudaError_t bd_launch_mega(const BdParams& p, int ctas, cudaStream_t st) {
+  BdParams pp = p;
+  void* args[] = {(void*)&pp};
+  return cudaLaunchCooperativeKernel((const void*)mk_bdecode_kernel, dim3(ctas), dim3(BD_THREADS), args,
+                                     (size_t)BdSmem::total, st);
+}
+cudaError_t bd_launch_perop(const BdParams& p, uint32_t first, uint32_t count, cudaStream_t st) {
+  BdParams pp = p;
+  pp.mode = MODE_PEROP;
+  pp.perop_base = first;
+  mk_bdecode_kernel<<<count, BD_THREADS, BdSmem::total, st>>>(pp);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

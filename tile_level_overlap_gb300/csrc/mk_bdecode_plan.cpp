@@ -1,0 +1,240 @@
+// Host plan of the tensor-core batched decode queue (see mk_bdecode.h).
+// Every GEMM row tile is released once, by the last of its K chunks to
+// arrive; every (sequence, kv head) attention group once, by the last of its
+// splits.  Waiters count those releases.
+#include <algorithm>
+#include <cstring>
+#include <map>
+
+#include "mk_bdecode.h"
+#include "mk_plan.h"
+
+namespace mk {
+
+namespace {
+
+Instr bd_make(uint8_t op, int layer, uint32_t a0, uint32_t a1, uint16_t a2 = 0) {
+  Instr in;
+  std::memset(&in, 0, sizeof(in));
+  in.op = op;
+  in.layer = (uint16_t)layer;
+  in.a0 = a0;
+  in.a1 = a1;
+  in.a2 = a2;
+  in.x_lo = NO_EXPR;
+  in.x_hi = NO_EXPR;
+  in.wait_bar = NO_BAR;
+  in.rel_bar = NO_BAR;
+  return in;
+}
+
+void bd_wait(Instr& in, uint32_t bar, uint32_t target) {
+  in.wait_bar = bar;
+  in.wait_target = target;
+  in.wait_n = 1;
+  in.wait_stride = 1;
+}
+
+uint32_t chunks(int K) { return (uint32_t)((K + BD_KC - 1) / BD_KC); }
+
+}  // namespace
+
+int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, BdPlan* out, std::string* why) {
+  auto bad = [&](int code, const char* msg) {
+    if (why) *why = msg;
+    return code;
+  };
+  if (c.n_layers < 1 || c.n_layers > MAX_LAYERS || c.hidden < 64 || c.n_q_heads < 1 ||
+      c.n_kv_heads < 1 || c.ffn < 64 || c.vocab < 1 || max_ctx < 2)
+    return bad(MK_ERR_INVALID_ARG, "bad model dimensions or context");
+  if (c.n_q_heads % c.n_kv_heads) return bad(MK_ERR_INVALID_ARG, "n_q_heads % n_kv_heads != 0");
+  if (max_batch < 1 || max_batch > BD_NMAX)
+    return bad(MK_ERR_UNSUPPORTED, "tensor-core decode takes 1..32 sequences");
+  if (c.head_dim != 64 && c.head_dim != 128)
+    return bad(MK_ERR_UNSUPPORTED, "tensor-core decode head_dim must be 64 or 128");
+  const int rep = c.n_q_heads / c.n_kv_heads;
+  if (rep > 4) return bad(MK_ERR_UNSUPPORTED, "tensor-core decode takes at most 4 q heads per kv head");
+  const int qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+  if (c.hidden % BD_M || qd % BD_M || kd % BD_M || c.ffn % (BD_M / 2) || c.hidden % BD_BK ||
+      c.ffn % BD_BK || qd % BD_BK)
+    return bad(MK_ERR_UNSUPPORTED,
+               "tensor-core decode needs hidden, n_q*d, n_kv*d % 128 == 0 and ffn % 64 == 0");
+  auto chunk_ok = [](int K) { return K <= BD_KC ? true : K % BD_KC == 0; };
+  if (!chunk_ok(c.hidden) || !chunk_ok(qd) || !chunk_ok(c.ffn))
+    return bad(MK_ERR_UNSUPPORTED, "K dimensions above 1024 must be multiples of 1024");
+  BdPlan& bp = *out;
+  bp = BdPlan();
+  bp.cfg = c;
+  bp.max_batch = max_batch;
+  bp.max_ctx = max_ctx;
+  bp.nb = max_batch <= 16 ? 16 : 32;
+  bp.rep = rep;
+  bp.qkv_rows = qd + 2 * kd;
+  bp.n_rg = (max_batch + BD_RG - 1) / BD_RG;
+  bp.n_qkv_m = (uint32_t)(bp.qkv_rows / BD_M);
+  bp.n_o_m = (uint32_t)(c.hidden / BD_M);
+  bp.n_gu_m = (uint32_t)(c.ffn / (BD_M / 2));
+  bp.n_down_m = (uint32_t)(c.hidden / BD_M);
+  bp.n_lm_m = (uint32_t)((c.vocab + BD_M - 1) / BD_M);
+  bp.c_h = chunks(c.hidden);
+  bp.c_q = chunks(qd);
+  bp.c_f = chunks(c.ffn);
+
+  const int L = c.n_layers, nkv = c.n_kv_heads;
+  BdBars& b = bp.bl;
+  b.norm1 = 0;
+  b.qkv = b.norm1 + L;
+  b.attn = b.qkv + L;
+  b.o = b.attn + L;
+  b.norm2 = b.o + L;
+  b.gu = b.norm2 + L;
+  b.down = b.gu + L;
+  b.normf = b.down + L;
+  b.lm = b.normf + 1;
+  b.total = b.lm + 1;
+
+  std::vector<Instr>& q = bp.queue;
+  auto begin = [&]() { return (uint32_t)q.size(); };
+  auto end = [&](uint32_t s) {
+    if (q.size() > s) bp.perop.push_back({s, (uint32_t)q.size() - s});
+  };
+  auto gemm = [&](uint8_t op, int l, uint32_t nm, uint32_t nc, uint32_t wbar, uint32_t wtarget,
+                  uint32_t rbar) {
+    const uint32_t s = begin();
+    for (uint32_t m = 0; m < nm; ++m)
+      for (uint32_t ch = 0; ch < nc; ++ch) {
+        Instr in = bd_make(op, l, m, ch);
+        bd_wait(in, wbar, wtarget);
+        in.rel_bar = rbar;
+        q.push_back(in);
+      }
+    end(s);
+  };
+  auto norm = [&](uint8_t op, int l, uint32_t wbar, uint32_t wtarget, uint32_t rbar) {
+    const uint32_t s = begin();
+    for (int r = 0; r < bp.n_rg; ++r) {
+      Instr in = bd_make(op, l, (uint32_t)r, 0);
+      if (wbar != NO_BAR) bd_wait(in, wbar, wtarget);
+      in.rel_bar = rbar;
+      q.push_back(in);
+    }
+    end(s);
+  };
+  for (int l = 0; l < L; ++l) {
+    norm(BD_NORM1, l, l > 0 ? b.down + l - 1 : NO_BAR, bp.n_down_m, b.norm1 + l);
+    gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, b.norm1 + l, (uint32_t)bp.n_rg, b.qkv + l);
+    {
+      const uint32_t s = begin();
+      for (int bb = 0; bb < max_batch; ++bb)
+        for (int g = 0; g < nkv; ++g)
+          for (int sp = 0; sp < BD_NSPLIT; ++sp) {
+            Instr in = bd_make(BD_ATTN, l, (uint32_t)bb, (uint32_t)g, (uint16_t)sp);
+            bd_wait(in, b.qkv + l, bp.n_qkv_m);
+            in.rel_bar = b.attn + l;
+            q.push_back(in);
+          }
+      end(s);
+    }
+    gemm(BD_O, l, bp.n_o_m, bp.c_q, b.attn + l, (uint32_t)(max_batch * nkv), b.o + l);
+    norm(BD_NORM2, l, b.o + l, bp.n_o_m, b.norm2 + l);
+    gemm(BD_GU, l, bp.n_gu_m, bp.c_h, b.norm2 + l, (uint32_t)bp.n_rg, b.gu + l);
+    gemm(BD_DOWN, l, bp.n_down_m, bp.c_f, b.gu + l, bp.n_gu_m, b.down + l);
+  }
+  norm(BD_NORMF, L - 1, b.down + L - 1, bp.n_down_m, b.normf);
+  gemm(BD_LM, L - 1, bp.n_lm_m, 1, b.normf, (uint32_t)bp.n_rg, b.lm);
+  return MK_OK;
+}
+
+// Sequential check of a queue order: every wait is satisfied when reached and
+// every barrier ends with exactly the releases its waiters expect.  A GEMM row
+// tile releases once when its last chunk arrives; an attention group once
+// when its last split arrives.
+int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string* why) {
+  std::vector<uint32_t> cnt(bp.bl.total, 0);
+  std::map<uint64_t, uint32_t> arrived;
+  auto group_size = [&](const Instr& in) -> uint32_t {
+    switch (in.op) {
+      case BD_QKV: case BD_GU: return bp.c_h;
+      case BD_O: return bp.c_q;
+      case BD_DOWN: return bp.c_f;
+      case BD_ATTN: return BD_NSPLIT;
+      default: return 1;
+    }
+  };
+  for (size_t i = 0; i < q.size(); ++i) {
+    const Instr& in = q[i];
+    if (in.op < BD_NORM1 || in.op > BD_LM) {
+      if (why) *why = "unknown batched-decode opcode at " + std::to_string(i);
+      return MK_ERR_INVALID_ARG;
+    }
+    if (in.wait_bar != NO_BAR && (in.wait_bar >= bp.bl.total || cnt[in.wait_bar] < in.wait_target)) {
+      if (why) *why = "batched-decode instruction " + std::to_string(i) + " waits before its producers";
+      return MK_ERR_INVALID_ARG;
+    }
+    if (in.rel_bar == NO_BAR) continue;
+    const uint32_t gs = group_size(in);
+    if (gs == 1) {
+      cnt[in.rel_bar] += 1;
+      continue;
+    }
+    const uint64_t key = ((uint64_t)in.op << 56) | ((uint64_t)in.layer << 40) |
+                         (in.op == BD_ATTN ? ((uint64_t)in.a0 << 20 | in.a1) : (uint64_t)in.a0);
+    if (++arrived[key] == gs) cnt[in.rel_bar] += 1;
+  }
+  for (size_t i = 0; i < q.size(); ++i) {
+    const Instr& in = q[i];
+    if (in.wait_bar != NO_BAR && cnt[in.wait_bar] != in.wait_target) {
+      if (why) *why = "batched-decode barrier count mismatch at instruction " + std::to_string(i);
+      return MK_ERR_INVALID_ARG;
+    }
+  }
+  return MK_OK;
+}
+
+// A seeded random topological order of the queue (for schedule-invariance
+// tests): repeatedly takes a random instruction whose wait is satisfied.
+void random_order_bdecode(const BdPlan& bp, uint64_t seed, std::vector<Instr>* out) {
+  const std::vector<Instr>& q = bp.queue;
+  out->clear();
+  std::vector<uint32_t> cnt(bp.bl.total, 0);
+  std::vector<std::vector<uint32_t>> waiters(bp.bl.total);
+  std::vector<uint32_t> ready;
+  for (uint32_t i = 0; i < q.size(); ++i) {
+    if (q[i].wait_bar == NO_BAR) ready.push_back(i);
+    else waiters[q[i].wait_bar].push_back(i);
+  }
+  std::map<uint64_t, uint32_t> arrived;
+  auto group_size = [&](const Instr& in) -> uint32_t {
+    switch (in.op) {
+      case BD_QKV: case BD_GU: return bp.c_h;
+      case BD_O: return bp.c_q;
+      case BD_DOWN: return bp.c_f;
+      case BD_ATTN: return BD_NSPLIT;
+      default: return 1;
+    }
+  };
+  uint64_t x = seed * 0x9E3779B97F4A7C15ull + 1;
+  while (!ready.empty()) {
+    x ^= x << 13; x ^= x >> 7; x ^= x << 17;
+    const size_t k = (size_t)(x % ready.size());
+    const uint32_t i = ready[k];
+    ready[k] = ready.back();
+    ready.pop_back();
+    const Instr& in = q[i];
+    out->push_back(in);
+    if (in.rel_bar == NO_BAR) continue;
+    const uint32_t gs = group_size(in);
+    bool fire = gs == 1;
+    if (!fire) {
+      const uint64_t key = ((uint64_t)in.op << 56) | ((uint64_t)in.layer << 40) |
+                           (in.op == BD_ATTN ? ((uint64_t)in.a0 << 20 | in.a1) : (uint64_t)in.a0);
+      fire = ++arrived[key] == gs;
+    }
+    if (!fire) continue;
+    const uint32_t c = ++cnt[in.rel_bar];
+    for (uint32_t w : waiters[in.rel_bar])
+      if (q[w].wait_target == c) ready.push_back(w);
+  }
+}
+
+}  // namespace mk

@@ -1,12 +1,14 @@
 // C ABI of libmk (declared in include/mk.h).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <string>
 #include <vector>
 
 #include "../../include/mk.h"
+#include "mk_bdecode.h"
 #include "mk_internal.h"
 #include "mk_plan.h"
 #include "mk_prefill.h"
@@ -33,8 +35,24 @@ struct PrefillState {
   const void* kv_mapped = nullptr;      // KV cache the table's cache map points at
 };
 
+// Tensor-core batched decode state of a plan (shapes whose batch the CUDA-core
+// decode path does not take).
+struct BdState {
+  bool on = false;
+  BdPlan bp;
+  void* mem = nullptr;
+  CUtensorMap* d_tm = nullptr;
+  std::vector<CUtensorMap> h_tm;
+  const void* kv_mapped = nullptr;
+  Instr* d_queue = nullptr;
+  BdParams base{};
+  size_t arrive_words = 0;
+};
+
 struct mk_plan {
-  HostPlan hp;
+  HostPlan hp;  // CUDA-core decode plan (batch 1 only when bd.on: it serves the prefill's LM head)
+  BdState bd;
+  int max_batch = 0;  // sequences a decode step may carry (the caller's)
   KernelVariant kv{};
   std::vector<LayerW> lw;  // host copy of the per-layer weight pointers
   PrefillState pf;
@@ -106,6 +124,134 @@ int upload_mk_queue(mk_plan* p, uint64_t seed) {
                              cudaMemcpyHostToDevice));
 }
 
+// ---------------------------------------------------------------- batched decode (tensor cores)
+// Buffers, tensor maps and launch parameters of the tensor-core batched path.
+int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
+  BdState& s = p->bd;
+  const BdPlan& bp = s.bp;
+  if (bd_setup() != cudaSuccess) return MK_ERR_CUDA;
+  const mk_model_cfg& c = bp.cfg;
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
+  const int qd = c.n_q_heads * d, kd = nkv * d, NB = bp.nb;
+  // split-K partials of the operator with the most (row tile, chunk) pairs
+  const size_t pairs = std::max({(size_t)bp.n_qkv_m * bp.c_h, (size_t)bp.n_o_m * bp.c_q,
+                                 (size_t)bp.n_gu_m * bp.c_h, (size_t)bp.n_down_m * bp.c_f});
+  const uint32_t max_m = std::max({bp.n_qkv_m, bp.n_o_m, bp.n_gu_m, bp.n_down_m, bp.n_lm_m});
+  const int n_maps = L * BD_TM_PER_LAYER + TMB_COUNT;
+  Bump bm;
+  const size_t o_bars = bm.take(sizeof(uint32_t) * bp.bl.total);
+  const size_t o_ctl = bm.take(sizeof(uint32_t) * CTL_WORDS);
+  const size_t o_q = bm.take(sizeof(Instr) * bp.queue.size());
+  const size_t o_qmk = bm.take(sizeof(Instr) * bp.queue.size());
+  const size_t o_tm = bm.take(sizeof(CUtensorMap) * n_maps);
+  const size_t o_xa = bm.take(sizeof(float) * NB * H);
+  const size_t o_xb = bm.take(sizeof(float) * NB * H);
+  const size_t o_hn = bm.take(4 * (size_t)NB * H);
+  const size_t o_ao = bm.take(4 * (size_t)NB * qd);
+  const size_t o_act = bm.take(4 * (size_t)NB * F);
+  const size_t o_qv = bm.take(sizeof(float) * NB * qd);
+  const size_t o_part = bm.take(sizeof(float) * pairs * BD_NMAX * BD_M);
+  const size_t o_apart = bm.take(sizeof(float) * bp.max_batch * nkv * BD_NSPLIT * bp.rep * (d + 2));
+  s.arrive_words = (size_t)max_m + (size_t)bp.max_batch * nkv;
+  const size_t o_arr = bm.take(sizeof(uint32_t) * s.arrive_words);
+  if (cudaMalloc(&s.mem, bm.off) != cudaSuccess) {
+    cudaGetLastError();
+    s.mem = nullptr;
+    return MK_ERR_CUDA;
+  }
+  p->scratch_bytes += bm.off;
+  uint8_t* b = (uint8_t*)s.mem;
+  MK_CUDA(cudaMemset(s.mem, 0, bm.off));
+  MK_CUDA(cudaMemcpy(b + o_q, bp.queue.data(), sizeof(Instr) * bp.queue.size(), cudaMemcpyHostToDevice));
+  MK_CUDA(cudaMemcpy(b + o_qmk, bp.queue.data(), sizeof(Instr) * bp.queue.size(), cudaMemcpyHostToDevice));
+  s.d_queue = (Instr*)(b + o_q);
+  s.d_tm = (CUtensorMap*)(b + o_tm);
+  s.h_tm.assign(n_maps, CUtensorMap{});
+  bool ok = true;
+  for (int l = 0; l < L && ok; ++l) {
+    const LayerW& x = p->lw[l];
+    CUtensorMap* t = &s.h_tm[l * BD_TM_PER_LAYER];
+    ok = make_tmap_bf16(t + TMB_WQ, x.wq, qd, H, BD_M) && make_tmap_bf16(t + TMB_WK, x.wk, kd, H, BD_M) &&
+         make_tmap_bf16(t + TMB_WV, x.wv, kd, H, BD_M) && make_tmap_bf16(t + TMB_WO, x.wo, H, qd, BD_M) &&
+         make_tmap_bf16(t + TMB_WG, x.wg, F, H, BD_M / 2) &&
+         make_tmap_bf16(t + TMB_WU, x.wu, F, H, BD_M / 2) && make_tmap_bf16(t + TMB_WD, x.wd, H, F, BD_M);
+  }
+  CUtensorMap* gm = &s.h_tm[L * BD_TM_PER_LAYER];
+  const void* lm = c.tied_embeddings ? w->embed : w->lm_head;
+  ok = ok && make_tmap_bf16(gm + TMB_LM, lm, c.vocab, H, BD_M) &&
+       make_tmap_bf16(gm + TMB_HN, b + o_hn, 2 * NB, H, NB) &&
+       make_tmap_bf16(gm + TMB_AO, b + o_ao, 2 * NB, qd, NB) &&
+       make_tmap_bf16(gm + TMB_ACT, b + o_act, 2 * NB, F, NB);
+  if (!ok) return MK_ERR_CUDA;
+  MK_CUDA(cudaMemcpy(s.d_tm, s.h_tm.data(), sizeof(CUtensorMap) * n_maps, cudaMemcpyHostToDevice));
+  BdParams& k = s.base;
+  std::memset(&k, 0, sizeof(k));
+  k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = nkv; k.d = d; k.F = F; k.V = c.vocab;
+  k.qk_norm = c.qk_norm; k.rep = bp.rep; k.qkv_rows = bp.qkv_rows; k.max_ctx = bp.max_ctx;
+  k.max_batch = bp.max_batch; k.nb = NB; k.n_rg = bp.n_rg; k.eps = c.rms_eps;
+  k.n_qkv_m = bp.n_qkv_m; k.n_o_m = bp.n_o_m; k.n_gu_m = bp.n_gu_m; k.n_down_m = bp.n_down_m;
+  k.n_lm_m = bp.n_lm_m; k.c_h = bp.c_h; k.c_q = bp.c_q; k.c_f = bp.c_f;
+  k.embed = (const uint16_t*)w->embed;
+  k.final_norm = (const uint16_t*)w->final_norm;
+  k.layers = p->base.layers;
+  k.tm = s.d_tm;
+  k.xa = (float*)(b + o_xa);
+  k.xb = (float*)(b + o_xb);
+  k.hn = (uint16_t*)(b + o_hn);
+  k.ao = (uint16_t*)(b + o_ao);
+  k.act = (uint16_t*)(b + o_act);
+  k.q = (float*)(b + o_qv);
+  k.part = (float*)(b + o_part);
+  k.apart = (float*)(b + o_apart);
+  k.arrive = (uint32_t*)(b + o_arr);
+  k.n_arrive_gemm = max_m;
+  k.rope = p->base.rope;
+  k.bars = (uint32_t*)(b + o_bars);
+  k.ctl = (uint32_t*)(b + o_ctl);
+  k.queue = (const Instr*)(b + o_qmk);
+  k.n_instr = (uint32_t)bp.queue.size();
+  return MK_OK;
+}
+
+// Point the table's cache map at this call's KV cache.
+int bd_bind_kv(mk_plan* p, void* kv, cudaStream_t st) {
+  BdState& s = p->bd;
+  if (s.kv_mapped == kv) return MK_OK;
+  const mk_model_cfg& c = s.bp.cfg;
+  const int idx = c.n_layers * BD_TM_PER_LAYER + TMB_KV;
+  const uint64_t rows = (uint64_t)c.n_layers * 2 * p->max_batch * c.n_kv_heads * s.bp.max_ctx;
+  if (!make_tmap_bf16(&s.h_tm[idx], kv, rows, (uint64_t)c.head_dim, BD_KEYS)) return MK_ERR_CUDA;
+  MK_CUDA(cudaMemcpyAsync(s.d_tm + idx, &s.h_tm[idx], sizeof(CUtensorMap), cudaMemcpyHostToDevice, st));
+  MK_CUDA(cudaStreamSynchronize(st));
+  s.kv_mapped = kv;
+  return MK_OK;
+}
+
+BdParams bd_params(mk_plan* p, const int32_t* tokens, const int32_t* positions, int batch, void* kv,
+                   float* logits) {
+  BdParams k = p->bd.base;
+  k.tokens = tokens;
+  k.positions = positions;
+  k.B = batch;
+  k.kv = (uint16_t*)kv;
+  k.logits = logits;
+  k.mode = MODE_MEGA;
+  k.wait_limit_ns = p->wait_limit_ns;
+  return k;
+}
+
+int bd_upload_queue(mk_plan* p, uint64_t seed) {
+  BdState& s = p->bd;
+  std::vector<Instr> q = s.bp.queue;
+  if (seed) {
+    random_order_bdecode(s.bp, seed, &q);
+    std::string why;
+    if (q.size() != s.bp.queue.size() || simulate_bdecode(s.bp, q, &why) != MK_OK) return MK_ERR_INVALID_ARG;
+  }
+  return cuda_err(cudaMemcpy(const_cast<Instr*>(s.base.queue), q.data(), q.size() * sizeof(Instr),
+                             cudaMemcpyHostToDevice));
+}
+
 }  // namespace
 
 extern "C" {
@@ -129,6 +275,22 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
   HostPlan hp;
   std::string why;
   int rc = build_plan(*cfg, max_batch, max_ctx, 0, &hp, &why);
+  if (rc == MK_ERR_UNSUPPORTED && max_batch > 1) {
+    BdPlan bp;
+    if (build_bdecode(*cfg, max_batch, max_ctx, &bp, &why) != MK_OK) return rc;
+    std::vector<Instr> q = bp.queue;
+    if (queue_perm_seed) random_order_bdecode(bp, queue_perm_seed, &q);
+    if (q.size() != bp.queue.size()) return MK_ERR_INVALID_ARG;
+    rc = simulate_bdecode(bp, q, &why);
+    if (out) {
+      std::memset(out, 0, sizeof(*out));
+      out->n_instr_decode = (uint32_t)bp.queue.size();
+      out->n_barriers = bp.bl.total;
+      out->n_launches_per_op_decode = (uint32_t)bp.perop.size();
+      out->n_splits = BD_NSPLIT;
+    }
+    return rc;
+  }
   if (rc != MK_OK) return rc;
   std::vector<Instr> q = hp.decode;
   if (queue_perm_seed) {
@@ -169,7 +331,15 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   }
   mk_plan* p = new mk_plan();
   std::string why;
+  p->max_batch = max_batch;
   int rc = build_plan(*cfg, max_batch, max_ctx, sms, &p->hp, &why);
+  if (rc == MK_ERR_UNSUPPORTED && max_batch > 1 &&
+      build_bdecode(*cfg, max_batch, max_ctx, &p->bd.bp, &why) == MK_OK) {
+    // the batch goes to the tensor-core path; the CUDA-core plan keeps one
+    // sequence for the prefill's LM head
+    p->bd.on = true;
+    rc = build_plan(*cfg, 1, max_ctx, sms, &p->hp, &why);
+  }
   if (rc != MK_OK) {
     delete p;
     return rc;
@@ -219,7 +389,7 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
 
   // one scratch allocation
   const int H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
-  const size_t B = (size_t)max_batch;
+  const size_t B = (size_t)hp.max_batch;
   Bump bm;
   const size_t o_resid = bm.take(sizeof(float) * (2 * L + 1) * B * H);
   const size_t o_qkv = bm.take(sizeof(float) * L * B * hp.qkv_rows);
@@ -234,9 +404,9 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   const size_t o_expr = bm.take(sizeof(uint32_t) * hp.expr.size());
   const size_t o_rope = bm.take(sizeof(float2) * (size_t)max_ctx * (d / 2));
   const size_t o_lw = bm.take(sizeof(LayerW) * L);
-  const size_t o_tok = bm.take(sizeof(int32_t) * B);
-  const size_t o_pos = bm.take(sizeof(int32_t) * B);
-  const size_t o_log = bm.take(sizeof(float) * B * c.vocab);
+  const size_t o_tok = bm.take(sizeof(int32_t) * max_batch);
+  const size_t o_pos = bm.take(sizeof(int32_t) * max_batch);
+  const size_t o_log = bm.take(sizeof(float) * max_batch * c.vocab);
   p->scratch_bytes = bm.off;
   if (cudaMalloc(&p->scratch, p->scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -276,7 +446,7 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   std::memset(&k, 0, sizeof(k));
   k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = nkv; k.d = d; k.F = F; k.V = c.vocab;
   k.qk_norm = c.qk_norm; k.rep = hp.rep; k.qkv_rows = hp.qkv_rows; k.eps = c.rms_eps;
-  k.max_batch = max_batch; k.max_ctx = max_ctx; k.n_splits = hp.n_splits;
+  k.max_batch = hp.max_batch; k.max_ctx = max_ctx; k.n_splits = hp.n_splits;
   k.r_qkv = hp.r_qkv; k.r_o = hp.r_o; k.r_gu = hp.r_gu; k.r_down = hp.r_down; k.r_lm = hp.r_lm;
   k.n_qkv_tiles = hp.n_qkv_tiles; k.n_o_tiles = hp.n_o_tiles; k.n_gu_tiles = hp.n_gu_tiles;
   k.n_down_tiles = hp.n_down_tiles; k.n_lm_tiles = hp.n_lm_tiles;
@@ -297,7 +467,8 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   k.n_instr = (uint32_t)hp.decode.size();
   k.expr = (const uint32_t*)(s + o_expr);
   k.bl = hp.bl;
-  p->kv_bytes = (size_t)L * 2 * B * nkv * (size_t)max_ctx * d * 2;
+  p->kv_bytes = (size_t)L * 2 * max_batch * nkv * (size_t)max_ctx * d * 2;
+  if (p->bd.on && (rc = bd_init(p, w)) != MK_OK) return fail(rc);
   *out = p;
   return MK_OK;
 }
@@ -309,6 +480,7 @@ void mk_plan_destroy(mk_plan* p) {
   if (p->d_trace) cudaFree(p->d_trace);
   if (p->scratch) cudaFree(p->scratch);
   if (p->pf.mem) cudaFree(p->pf.mem);
+  if (p->bd.mem) cudaFree(p->bd.mem);
   delete p;
 }
 
@@ -332,13 +504,19 @@ int mk_plan_get_stats(const mk_plan* p, mk_plan_stats* out) {
   out->n_splits = (uint32_t)p->hp.n_splits;
   out->weight_bytes = p->hp.weight_bytes;
   out->scratch_bytes = p->scratch_bytes;
+  if (p->bd.on) {
+    out->n_instr_decode = (uint32_t)p->bd.bp.queue.size();
+    out->n_barriers = p->bd.bp.bl.total;
+    out->n_launches_per_op_decode = (uint32_t)p->bd.bp.perop.size();
+    out->n_splits = BD_NSPLIT;
+  }
   return MK_OK;
 }
 
 static int check_step(mk_plan* p, const void* tokens, const void* positions, int batch,
                       const void* kv, const void* logits) {
   if (!p || !tokens || !positions || !kv || !logits) return MK_ERR_INVALID_ARG;
-  if (batch < 1 || batch > p->hp.max_batch) return MK_ERR_INVALID_ARG;
+  if (batch < 1 || batch > p->max_batch) return MK_ERR_INVALID_ARG;
   if (!aligned16(kv)) return MK_ERR_INVALID_ARG;
   if (p->latched) return p->latched;
   return MK_OK;
@@ -363,8 +541,13 @@ int mk_decode_step(mk_plan* p, const int32_t* tokens, const int32_t* positions, 
                    void* kv, float* logits, void* stream) {
   int rc = check_step(p, tokens, positions, batch, kv, logits);
   if (rc != MK_OK) return rc;
-  KParams k = step_params(p, tokens, positions, batch, kv, logits);
   const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
+  if (p->bd.on) {
+    if ((rc = bd_bind_kv(p, kv, (cudaStream_t)stream)) != MK_OK) return rc;
+    return cuda_err(bd_launch_mega(bd_params(p, tokens, positions, batch, kv, logits), ctas,
+                                   (cudaStream_t)stream));
+  }
+  KParams k = step_params(p, tokens, positions, batch, kv, logits);
   return cuda_err(p->kv.mega(k, ctas, (cudaStream_t)stream));
 }
 
@@ -381,8 +564,8 @@ int mk_decode_step_host(mk_plan* p, const int32_t* tokens_host, const int32_t* p
   uint32_t status = 0;
   MK_CUDA(cudaMemcpyAsync(logits_host, p->d_logits, sizeof(float) * batch * p->hp.cfg.vocab,
                           cudaMemcpyDeviceToHost, st));
-  MK_CUDA(cudaMemcpyAsync(&status, p->d_ctl + CTL_STATUS, sizeof(uint32_t), cudaMemcpyDeviceToHost,
-                          st));
+  MK_CUDA(cudaMemcpyAsync(&status, (p->bd.on ? p->bd.base.ctl : p->d_ctl) + CTL_STATUS,
+                          sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
   MK_CUDA(cudaStreamSynchronize(st));
   if (status) p->latched = (int)status;
   return (int)status;
@@ -454,7 +637,7 @@ static int prefill_init(mk_plan* p) {
   std::memset(&k, 0, sizeof(k));
   k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = c.n_kv_heads; k.d = d; k.F = F; k.V = c.vocab;
   k.qk_norm = c.qk_norm; k.rep = pp.rep; k.qkv_rows = pp.qkv_rows; k.bn_qkv = pp.bn_qkv;
-  k.n_blocks = pp.n_blocks; k.max_ctx = p->hp.max_ctx; k.max_batch = p->hp.max_batch;
+  k.n_blocks = pp.n_blocks; k.max_ctx = p->hp.max_ctx; k.max_batch = p->max_batch;
   k.eps = c.rms_eps;
   k.n_qkv_n = pp.n_qkv_n; k.n_o_n = pp.n_o_n; k.n_gu_n = pp.n_gu_n; k.n_down_n = pp.n_down_n;
   k.embed = p->base.embed;
@@ -484,7 +667,7 @@ static int prefill_bind_kv(mk_plan* p, void* kv, cudaStream_t st) {
   if (s.kv_mapped == kv) return MK_OK;
   const mk_model_cfg& c = p->hp.cfg;
   const int idx = c.n_layers * TM_PER_LAYER + AM_KV;
-  const uint64_t rows = (uint64_t)c.n_layers * 2 * p->hp.max_batch * c.n_kv_heads * p->hp.max_ctx;
+  const uint64_t rows = (uint64_t)c.n_layers * 2 * p->max_batch * c.n_kv_heads * p->hp.max_ctx;
   if (!make_tmap_bf16(&s.h_tm[idx], kv, rows, (uint64_t)c.head_dim, PF_BM)) return MK_ERR_CUDA;
   MK_CUDA(cudaMemcpyAsync(s.d_tm + idx, &s.h_tm[idx], sizeof(CUtensorMap), cudaMemcpyHostToDevice, st));
   MK_CUDA(cudaStreamSynchronize(st));
@@ -535,6 +718,13 @@ static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
   return MK_OK;
 }
 
+static int launch_per_op_bd(mk_plan* p, const BdParams& k, cudaStream_t st) {
+  BdParams kk = k;
+  kk.queue = p->bd.d_queue;  // per-operator ranges index the default order
+  for (const auto& r : p->bd.bp.perop) MK_CUDA(bd_launch_perop(kk, r.first, r.second, st));
+  return MK_OK;
+}
+
 static int launch_per_op_prefill(mk_plan* p, const PfParams& k, void* kv, float* logits,
                                  cudaStream_t st) {
   for (const auto& r : p->pf.pp.perop) MK_CUDA(pf_launch_perop(k, r.first, r.second, st));
@@ -547,6 +737,7 @@ int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,
   cudaStream_t st = (cudaStream_t)stream;
   PfParams pk;
   KParams k;
+  BdParams bk;
   if (mode == MK_PREFILL) {
     int rc = prefill_args(p, tokens, batch_or_len, kv, logits);
     if (rc != MK_OK) return rc;
@@ -561,10 +752,15 @@ int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,
     if (mode != MK_DECODE) return MK_ERR_INVALID_ARG;
     int rc = check_step(p, tokens, positions, batch_or_len, kv, logits);
     if (rc != MK_OK) return rc;
+    if (p->bd.on) {
+      if ((rc = bd_bind_kv(p, kv, st)) != MK_OK) return rc;
+      bk = bd_params(p, tokens, positions, batch_or_len, kv, logits);
+      if (!use_graph) return launch_per_op_bd(p, bk, st);
+    }
     k = step_params(p, tokens, positions, batch_or_len, kv, logits);
     k.queue = p->d_queue;
     k.trace = nullptr;
-    if (!use_graph) return launch_per_op_seq(p, k, st);
+    if (!use_graph && !p->bd.on) return launch_per_op_seq(p, k, st);
   }
   const uintptr_t key[6] = {(uintptr_t)tokens, (uintptr_t)positions, (uintptr_t)batch_or_len,
                             (uintptr_t)kv, (uintptr_t)logits, (uintptr_t)mode};
@@ -576,7 +772,8 @@ int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,
     cudaGraph_t g = nullptr;
     MK_CUDA(cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeThreadLocal));
     int lrc = mode == MK_PREFILL ? launch_per_op_prefill(p, pk, kv, logits, p->cap_stream)
-                                 : launch_per_op_seq(p, k, p->cap_stream);
+              : p->bd.on        ? launch_per_op_bd(p, bk, p->cap_stream)
+                                : launch_per_op_seq(p, k, p->cap_stream);
     cudaError_t e = cudaStreamEndCapture(p->cap_stream, &g);
     if (lrc != MK_OK || e != cudaSuccess) {
       if (g) cudaGraphDestroy(g);
@@ -604,6 +801,10 @@ int mk_status(mk_plan* p, void* stream) {
       cudaMemcpy(&status, p->pf.base.ctl + CTL_STATUS, sizeof(status), cudaMemcpyDeviceToHost) !=
           cudaSuccess)
     return MK_ERR_CUDA;
+  if (!status && p->bd.on &&
+      cudaMemcpy(&status, p->bd.base.ctl + CTL_STATUS, sizeof(status), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return MK_ERR_CUDA;
   if (status) p->latched = (int)status;
   return (int)status;
 }
@@ -620,6 +821,11 @@ int mk_plan_reset(mk_plan* p, void* stream) {
     MK_CUDA(cudaMemset(p->pf.base.bars, 0, sizeof(uint32_t) * p->pf.pp.bl.total));
     MK_CUDA(cudaMemset(p->pf.base.ctl, 0, sizeof(uint32_t) * CTL_WORDS));
   }
+  if (p->bd.on) {
+    MK_CUDA(cudaMemset(p->bd.base.bars, 0, sizeof(uint32_t) * p->bd.bp.bl.total));
+    MK_CUDA(cudaMemset(p->bd.base.ctl, 0, sizeof(uint32_t) * CTL_WORDS));
+    MK_CUDA(cudaMemset(p->bd.base.arrive, 0, sizeof(uint32_t) * p->bd.arrive_words));
+  }
   MK_CUDA(cudaDeviceSynchronize());
   p->latched = 0;
   return MK_OK;
@@ -631,7 +837,7 @@ int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int 
   if (cudaDeviceSynchronize() != cudaSuccess) return MK_ERR_CUDA;
   p->force_ctas = force_ctas;
   p->wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
-  int rc = upload_mk_queue(p, queue_perm_seed);
+  int rc = p->bd.on ? bd_upload_queue(p, queue_perm_seed) : upload_mk_queue(p, queue_perm_seed);
   if (rc != MK_OK) return rc;
   if (trace && !p->d_trace) {
     if (cudaMalloc(&p->d_trace, p->hp.decode.size() * TRACE_WORDS * 8) != cudaSuccess) return MK_ERR_CUDA;
@@ -643,6 +849,7 @@ int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int 
 
 int mk_plan_debug_drop_release(mk_plan* p, uint32_t index) {
   if (!p || index >= p->hp.decode.size()) return MK_ERR_INVALID_ARG;
+  if (p->bd.on) return MK_ERR_UNSUPPORTED;
   Instr in;
   MK_CUDA(cudaDeviceSynchronize());
   MK_CUDA(cudaMemcpy(&in, p->d_queue_mk + index, sizeof(Instr), cudaMemcpyDeviceToHost));
