@@ -34,24 +34,37 @@ if ROOT not in sys.path:
 
 METRIC = "decode tokens/s and HBM GB/s (% of ~8 TB/s), Llama-3-8B shape, batch 1, 1xGB300"
 UNIT = "tokens/s"
-BATCH = 1
 PREFILL_TOKENS = 2048
-# name -> (shape in synth, cached context, metric, workload description, traffic key)
+# name -> (shape in synth, batch, largest cached context, smallest (ragged
+# contexts U[lo, ctx], seeded) or None (all at ctx), metric, description,
+# traffic key)
 WORKLOADS = {
-    "llama3-8b": ("LLAMA3_8B", 4096, METRIC, "Llama-3-8B-shape decode, batch 1, context 4096",
-                  "llama3-8b-decode-b1-ctx4096"),
-    "llama3.2-1b": ("LLAMA32_1B", 1024,
+    "llama3-8b": ("LLAMA3_8B", 1, 4096, None, METRIC,
+                  "Llama-3-8B-shape decode, batch 1, context 4096", "llama3-8b-decode-b1-ctx4096"),
+    "llama3.2-1b": ("LLAMA32_1B", 1, 1024, None,
                     "decode tokens/s and HBM GB/s, Llama-3.2-1B shape, batch 1, 1xGB300",
                     "Llama-3.2-1B-shape decode, batch 1, context 1024",
                     "llama3.2-1b-decode-b1-ctx1024"),
+    "llama3-8b-b8": ("LLAMA3_8B", 8, 4096, None,
+                     "decode tokens/s and HBM GB/s, Llama-3-8B shape, batch 8, 1xGB300",
+                     "Llama-3-8B-shape decode, batch 8, context 4096 each",
+                     "llama3-8b-decode-b8-ctx4096"),
+    "qwen3-8b-b32": ("QWEN3_8B", 32, 2048, 512,
+                     "decode tokens/s and HBM GB/s, Qwen3-8B shape, batch 32, 1xGB300",
+                     "Qwen3-8B-shape decode, batch 32, contexts U[512, 2048] (seeded)",
+                     "qwen3-8b-decode-b32-ragged"),
 }
 
 
 def workload(name):
-    """(model shape, cached context, metric, description, traffic key)."""
+    """(model shape, batch, positions [batch], metric, description, traffic key)."""
     from tile_level_overlap_gb300 import synth
-    shape, ctx, metric, desc, key = WORKLOADS[name]
-    return getattr(synth, shape), ctx, metric, desc, key
+    shape, batch, ctx, lo, metric, desc, key = WORKLOADS[name]
+    if lo is None:
+        positions = [ctx] * batch
+    else:
+        positions = [int(v) for v in synth.make_contexts(batch, lo, ctx)]
+    return getattr(synth, shape), batch, positions, metric, desc, key
 
 
 def algorithmic_bytes(cfg, batch, positions) -> int:
@@ -202,7 +215,7 @@ class OracleSample:
     """The CPU oracle on a bounded sample of the decode step: `n_layers_sample`
     layers + the LM head (weights drawn on the CPU with the same recipe)."""
 
-    def __init__(self, cfg, n_layers_sample: int, context: int, seed: int = 0):
+    def __init__(self, cfg, n_layers_sample: int, positions, seed: int = 0):
         import torch
 
         from tile_level_overlap_gb300 import synth
@@ -212,9 +225,10 @@ class OracleSample:
         self.n = n_layers_sample
         self.sub = cfg.replace(n_layers=n_layers_sample)
         self.w = synth.weights_as_bits(synth.make_weights(self.sub, seed=seed, device="cpu"))
-        self.context = context
-        self.kv = synth.bf16_bits(synth.make_kv_cache(self.sub, 1, context + 1, device="cpu"))
-        self.tok = synth.make_tokens(1, cfg.vocab).numpy()
+        self.positions = list(positions)
+        self.kv = synth.bf16_bits(synth.make_kv_cache(self.sub, len(self.positions),
+                                                      max(self.positions) + 1, device="cpu"))
+        self.tok = synth.make_tokens(len(self.positions), cfg.vocab).numpy()
 
     def step(self):
         """Returns (seconds scaled to the full layer count, seconds measured)."""
@@ -224,10 +238,10 @@ class OracleSample:
         from oracle import model as om
 
         t0 = time.perf_counter()
-        oracle.decode_step(self.sub, self.w, self.tok, [self.context], self.kv)
+        oracle.decode_step(self.sub, self.w, self.tok, self.positions, self.kv)
         t_all = time.perf_counter() - t0
         # the LM head alone, so that only the layer part is scaled
-        x = np.random.default_rng(0).normal(size=(1, self.cfg.hidden)).astype(np.float32)
+        x = np.random.default_rng(0).normal(size=(len(self.positions), self.cfg.hidden)).astype(np.float32)
         t1 = time.perf_counter()
         lm = self.w["embed"] if self.cfg.tied_embeddings else self.w["lm_head"]
         om.linear(lm, om.rmsnorm(x, self.w["final_norm"], self.cfg.rms_eps))
@@ -240,9 +254,9 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    cfg, context, metric, wl_desc, _ = workload(args.workload)
+    cfg, batch, positions, metric, wl_desc, _ = workload(args.workload)
     n_s = args.ref_layers
-    sample_run = OracleSample(cfg, n_s, context)
+    sample_run = OracleSample(cfg, n_s, positions)
     for _ in range(args.warmup):
         sample_run.step()
     times, measured = [], 0.0
@@ -251,9 +265,9 @@ def run_reference(args):
         times.append(t)
         measured += tm
     ms = 1e3 * sum(times) / len(times)
-    value = BATCH / (ms / 1e3)
-    sample = (f"{n_s} of {cfg.n_layers} layers + the LM head of one batch-1 decode step at context "
-              f"{context}, per step; time scaled to {cfg.n_layers} layers")
+    value = batch / (ms / 1e3)
+    sample = (f"{n_s} of {cfg.n_layers} layers + the LM head of one batch-{batch} decode step "
+              f"({wl_desc}), per step; time scaled to {cfg.n_layers} layers")
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -286,13 +300,14 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    cfg, CONTEXT, metric, wl_desc, traffic_key = workload(args.workload)
+    cfg, BATCH, pos_list, metric, wl_desc, traffic_key = workload(args.workload)
+    CONTEXT = max(pos_list)
     max_ctx = CONTEXT + 1
     w = synth.make_weights(cfg, seed=synth.SEED_WEIGHTS + rank, device=dev)
     kv = synth.make_kv_cache(cfg, BATCH, max_ctx, device=dev)
     plan = mk.Plan(cfg, w, BATCH, max_ctx)
     tokens = synth.make_tokens(BATCH, cfg.vocab).to(dev)
-    positions = torch.full((BATCH,), CONTEXT, dtype=torch.int32, device=dev)
+    positions = torch.tensor(pos_list, dtype=torch.int32, device=dev)
     logits = torch.empty((BATCH, cfg.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     nbytes = algorithmic_bytes(cfg, BATCH, positions.tolist())
@@ -367,15 +382,18 @@ def run_ours(args):
     e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
     e2e = job_throughput(BATCH * args.steps, world, e2e_s)
 
-    # dependency-wait share from one traced step (not timed)
-    plan.set_debug(trace=True)
-    mega()
-    torch.cuda.synchronize(dev)
-    rec = plan.trace().astype(np.int64)
-    plan.set_debug(trace=False)
-    span = rec[:, 3].max() - rec[:, 1].min()
-    n_ctas = plan.stats().n_ctas
-    dep_wait = float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span) if span > 0 else None
+    # dependency-wait share from one traced step (not timed; the CUDA-core
+    # batch-1 path records the trace)
+    dep_wait = None
+    if BATCH == 1:
+        plan.set_debug(trace=True)
+        mega()
+        torch.cuda.synchronize(dev)
+        rec = plan.trace().astype(np.int64)
+        plan.set_debug(trace=False)
+        span = rec[:, 3].max() - rec[:, 1].min()
+        n_ctas = plan.stats().n_ctas
+        dep_wait = float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span) if span > 0 else None
 
     # prefill of a 2048-token prompt into sequence slot 0 (after the decode
     # timing, since it rewrites that cache slot)
@@ -408,7 +426,7 @@ def run_ours(args):
         return 0
     peaks, kind = measured_peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
-    traffic = recorded_traffic("mk_interpreter", traffic_key)
+    traffic = recorded_traffic("mk_interpreter", traffic_key) if plan.stats().decode_path == 0 else None
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -417,7 +435,10 @@ def run_ours(args):
                    "layers": cfg.n_layers, "hidden": cfg.hidden, "ffn": cfg.ffn,
                    "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
                    "head_dim": cfg.head_dim, "vocab": cfg.vocab, "batch": BATCH,
-                   "context": CONTEXT, "weights": "bf16", "kv_cache": "bf16",
+                   "context": CONTEXT if BATCH == 1 else pos_list,
+                   "path": "tensor-core persistent" if plan.stats().decode_path == 1
+                           else "cuda-core persistent",
+                   "weights": "bf16", "kv_cache": "bf16",
                    "activations": "f32",
                    "l2": f"inputs larger than L2: {nbytes / 1e9:.2f} GB streamed per step",
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -425,7 +446,8 @@ def run_ours(args):
         "hbm_frac_of_8tbs": achieved / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "peak_kind": kind, "kernel": "mk_interpreter",
+                     "peak_kind": kind,
+                     "kernel": "mk_bdecode_kernel" if plan.stats().decode_path == 1 else "mk_interpreter",
                      "algorithmic_bytes_per_launch": nbytes},
         "per_op": per_op,
         "dep_wait_fraction": dep_wait,
@@ -436,13 +458,13 @@ def run_ours(args):
         "prefill": prefill,
     }
     if world == 1 and not args.no_cpu_baseline:
-        sample_run = OracleSample(cfg, args.ref_layers, CONTEXT)
+        sample_run = OracleSample(cfg, args.ref_layers, pos_list)
         sample_run.step()
         t = sorted(sample_run.step()[0] for _ in range(3))[1]
         line["cpu_baseline"] = {
             "value": BATCH / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{args.ref_layers} of {cfg.n_layers} layers + the LM head of one batch-1 "
-                      f"decode step at context {CONTEXT}, scaled to {cfg.n_layers} layers"}
+            "sample": f"{args.ref_layers} of {cfg.n_layers} layers + the LM head of one batch-{BATCH} "
+                      f"decode step ({wl_desc}), scaled to {cfg.n_layers} layers"}
     print(json.dumps(line), flush=True)
     plan.close()
     if pg:

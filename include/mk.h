@@ -178,6 +178,9 @@ typedef struct {
   uint32_t n_splits;        /* split-KV partitions per (sequence, kv head)  */
   uint64_t weight_bytes;    /* bf16 weight bytes one decode step streams    */
   uint64_t scratch_bytes;   /* device scratch owned by the plan             */
+  uint32_t decode_path;     /* 0: CUDA-core decode interpreter; 1: tensor-core
+                               batched decode (batches the former does not
+                               take, up to 32 sequences)                     */
 } mk_plan_stats;
 int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
 
@@ -216,13 +219,19 @@ int mk_plan_debug_drop_release(mk_plan *plan, uint32_t index);
 int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int K, int b_layout,
                        void *stream);
 
-/* Copy the trace of the last traced launch: records of
- * 12 x uint64: {smid | (op | layer << 8) << 32, consumer took it, its waits were
- * satisfied, done, producer posted it, ns spent waiting for operand stages,
- * first operand stage ready, ns the producer waited for free stages, last stage
- * consumed, cross-warp reduction done, 0, 0} (%globaltimer ns; the last four
- * for batch-1 GEMV tiles), 96 bytes per instruction, indexed by queue position.  *n_records receives the
- * count copied.  Waits for the device. */
+/* Copy the trace of the last traced launch (mk_plan_set_debug(trace = 1)):
+ * 12 x uint64 per instruction (96 bytes), indexed by queue position, times in
+ * %globaltimer ns.  CUDA-core decode: {smid | (op | layer << 8) << 32, consumer
+ * took it, its waits were satisfied, done, producer posted it, ns spent waiting
+ * for operand stages, first operand stage ready, ns the producer waited for free
+ * stages, then for batch-1 GEMV tiles: last stage consumed (attention: inputs
+ * rotated), finisher took it (attention: scores done), attention: softmax and
+ * P V done, split arrival counted}.  Tensor-core batched decode
+ * (mk_plan_stats.decode_path = 1): {smid | (op | layer << 8) << 32, compute
+ * warps took it, inputs ready (GEMM: accumulator full; otherwise dependencies
+ * met), done, producer posted it, producer's dependency wait met, producer
+ * issued its last stage, first MMA issued, last MMA committed, 0, 0, 0}.
+ * *n_records receives the count copied.  Waits for the device. */
 int mk_trace_copy(mk_plan *plan, void *host_buf, size_t bytes, size_t *n_records);
 
 #ifdef __cplusplus

@@ -63,7 +63,7 @@ class BModel:
         self.max_batch = max_batch
         assert self.plan.kv_cache_bytes() == self.kv.numel() * 2
         # the batch exceeds what the CUDA-core path takes: tensor-core plan
-        assert self.plan.stats().n_splits == 4
+        assert self.plan.stats().decode_path == 1
 
     def step(self, tokens, positions, per_op=False, graph=False):
         t = torch.as_tensor(tokens, dtype=torch.int32).to(self.dev)

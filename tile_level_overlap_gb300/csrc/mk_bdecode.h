@@ -5,8 +5,13 @@
 // on-device interpreter popping instructions from a queue in DRAM).
 //
 // Per layer:
-//   NORM1(r) -> QKV(m, c) -> ATTN(b, g, s) -> O(m, c) -> NORM2(r) -> GU(m, c) -> DOWN(m, c)
-// then NORMF(r) -> LM(m) after the last layer.  GEMM tiles put 128 weight
+//   QKV(m, c) -> ATTN(b, g, s) -> O(m, c) -> GU(m, c) -> DOWN(m, c)
+// then LM(m) after the last layer (NORM1(r) before layer 0 only).  The RMSNorms
+// are folded into the GEMMs next to them: an O or down tile also writes its
+// columns of x * gain (the next norm's input times its gain) and the tile's
+// sums of x^2 per sequence; the next projection multiplies x * gain by the
+// weights and scales its outputs by 1 / rms, which the projection's linearity
+// in each row makes equal to projecting the normed row.  GEMM tiles put 128 weight
 // rows (m) on the tcgen05 M side and the batch (padded to N = 16 or 32
 // columns) on the N side, over one K chunk (c) of at most BD_KC columns; the
 // last chunk of a row tile to arrive adds the chunks' partial sums in chunk
@@ -27,7 +32,7 @@
 namespace mk {
 
 enum BdOp : uint8_t {
-  BD_NORM1 = 40,  // RMSNorm(attn) of sequences [8 r, 8 r + 8)          (a0 = r)
+  BD_NORM1 = 40,  // layer-0 RMSNorm input of sequences [8 r, 8 r + 8)  (a0 = r)
   BD_QKV = 41,    // [q|k|v] rows [128 m, +128) over K chunk c            (a0 = m, a1 = c)
   BD_ATTN = 42,   // split s of (sequence b, kv head g)                   (a0 = b, a1 = g, a2 = s)
   BD_O = 43,      // O rows of row tile m, chunk c; + residual
@@ -42,7 +47,7 @@ constexpr int BD_M = 128;       // weight rows per GEMM tile (tcgen05 M)
 constexpr int BD_BK = 64;       // reduction depth per ring stage (one 128-byte swizzle atom)
 constexpr int BD_NMAX = 32;     // most sequences per step (tcgen05 N)
 constexpr int BD_KC = 1024;     // K chunk of a split-K tile
-constexpr int BD_RG = 8;        // sequences per RMSNorm instruction
+constexpr int BD_RG = 8;        // sequences per RMSNorm instruction (one compute warp each)
 constexpr int BD_KEYS = 64;     // cached keys per attention stage
 constexpr int BD_NSPLIT = 4;    // attention splits per (sequence, kv head)
 
@@ -82,6 +87,8 @@ struct BdParams {
   uint16_t* ao;             // attention output, hi/lo planes [2][nb][n_q d]
   uint16_t* act;            // SwiGLU output, hi/lo planes [2][nb][F]
   float* q;                 // rotated (normed) queries [nb][n_q d]
+  float* ss1;               // sums of x^2 per (row tile, sequence) for the next QKV / LM [tiles][BD_NMAX]
+  float* ss2;               // the same for the gate/up projection [tiles][BD_NMAX]
   float* part;              // split-K partial sums [row tile][chunk][BD_NMAX][128] of one operator
   float* apart;             // attention split partials [nb][n_kv][BD_NSPLIT][rep][d + 2]
   uint32_t* arrive;         // arrival counters: [row tiles of one operator] then [max_batch * n_kv]
@@ -99,6 +106,12 @@ struct BdParams {
   int mode;
   uint32_t perop_base;
   unsigned long long wait_limit_ns;
+  // TRACE_WORDS x u64 per instruction (queue index), or null: [0] smid | (op |
+  // layer << 8) << 32, [1] compute warps took it, [2] inputs ready (GEMM:
+  // accumulator full; attention / norm: dependencies met), [3] done, [4]
+  // producer posted it, [5] producer's dependency wait met, [6] producer
+  // issued its last stage, [7] first MMA issued, [8] last MMA committed.
+  unsigned long long* trace;
 };
 
 // Shapes the tensor-core batched path takes (MK_OK) or why not.

@@ -10,9 +10,10 @@
 //  warp 1      tensor-core issuer: D[128 weight rows][N batch columns] +=
 //              W_tile * x_hi^T, then * x_lo^T, per k-step (tcgen05.mma,
 //              accumulators in TMEM, two 32-column accumulators).
-//  warps 2-5   compute: split-K partial sums, the last chunk's reduction and
-//              epilogue, RMSNorm blocks, the attention splits and their
-//              combine.
+//  warps 2-9   compute: split-K partial sums, the last chunk's reduction and
+//              epilogue (the two warps of a TMEM lane quarter take 16 batch
+//              columns each), the layer-0 RMSNorm, the attention splits and
+//              their combine.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,9 +30,9 @@ namespace {
 
 constexpr int BD_STAGE = 32 * 1024;
 constexpr int BD_NSTAGE = 6;
-constexpr int BD_THREADS = 192;
+constexpr int BD_THREADS = 320;
 constexpr int BD_CBAR = 2;   // named barrier of the compute warps
-constexpr int BD_NC = 128;   // compute threads
+constexpr int BD_NC = 256;   // compute threads (8 warps: two per TMEM lane quarter)
 constexpr uint32_t BD_END = 0xffffffffu;
 constexpr uint32_t BD_W_BYTES = BD_M * BD_BK * 2;  // weight box(es) of a stage: 16 KB
 constexpr int BD_ACC_COLS = 32;                    // TMEM columns per accumulator
@@ -42,7 +43,8 @@ struct BdSmem {
   static constexpr int qs = scratch + BD_M * BD_NMAX * 4;      // [4][128] f32
   static constexpr int sc = qs + 4 * 128 * 4;                  // [4][BD_KEYS] f32
   static constexpr int hs = sc + 4 * BD_KEYS * 4;              // [4] x {m, l, alpha} + inv norms [64]
-  static constexpr int bars = hs + (16 + 64) * 4;
+  static constexpr int rinv = hs + (16 + 64) * 4;             // [BD_NMAX] 1 / rms per sequence
+  static constexpr int bars = rinv + BD_NMAX * 4;
   // full[6] empty[6] ifull[8] iempty[8] accf[2] acce[2]
   static constexpr int n_mbar = 2 * BD_NSTAGE + 2 * NISLOT + 4;
   static constexpr int islot = bars + n_mbar * 8;
@@ -57,7 +59,7 @@ enum BdFlag { BF_GEN = 0, BF_SLOT = 1, BF_ABORT = 2, BF_TMEM = 3, BF_LAST = 4 };
 
 struct BdSh {
   uint8_t* ring;
-  float *scratch, *qs, *sc, *hs;
+  float *scratch, *qs, *sc, *hs, *rinv;
   uint64_t *full, *empty, *ifull, *iempty, *accf, *acce;
   uint8_t* islot;
   volatile uint32_t* flags;
@@ -71,6 +73,7 @@ __device__ __forceinline__ BdSh bd_map(uint8_t* base) {
   s.qs = reinterpret_cast<float*>(base + BdSmem::qs);
   s.sc = reinterpret_cast<float*>(base + BdSmem::sc);
   s.hs = reinterpret_cast<float*>(base + BdSmem::hs);
+  s.rinv = reinterpret_cast<float*>(base + BdSmem::rinv);
   uint64_t* b = reinterpret_cast<uint64_t*>(base + BdSmem::bars);
   s.full = b;
   s.empty = b + BD_NSTAGE;
@@ -121,6 +124,10 @@ __device__ bool bd_wait_deps(const BdParams& P, const Instr& in, uint32_t gen, u
     __nanosleep(64);
   }
   return true;
+}
+
+__device__ __forceinline__ void bd_mark(const BdParams& P, uint32_t i, int word) {
+  if (P.trace) P.trace[(size_t)i * TRACE_WORDS + word] = globaltimer();
 }
 
 __device__ __forceinline__ const CUtensorMap* tmap(const BdParams& P, int idx) {
@@ -243,23 +250,38 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
   const uint64_t pol_a = policy_evict_last();   // activations / KV: re-read by other tiles
   const uint32_t gen = S.flags[BF_GEN];
   uint32_t stage_ctr = 0, islot_ctr = 0;
-  bool first = true;
-  for (;;) {
-    uint32_t i;
+  uint32_t npop = 0;
+  // Pops run one instruction ahead of the one being streamed, so the latency
+  // of the queue atomic and of the record load overlaps the current
+  // instruction's copies.  Pop order is still this CTA's execution order.
+  auto pop = [&]() -> uint32_t {
+    const uint32_t k = npop++;
     if (P.mode == MODE_MEGA) {
-      i = ld_volatile(&P.ctl[CTL_ABORT]) ? BD_END : atomicAdd(&P.ctl[CTL_HEAD], 1u);
-      if (i >= P.n_instr) i = BD_END;
-    } else {
-      i = first ? P.perop_base + blockIdx.x : BD_END;
-      first = false;
+      if (ld_volatile(&P.ctl[CTL_ABORT])) return BD_END;
+      const uint32_t v = atomicAdd(&P.ctl[CTL_HEAD], 1u);
+      return v < P.n_instr ? v : BD_END;
+    }
+    return k == 0 ? P.perop_base + blockIdx.x : BD_END;
+  };
+  uint32_t inext = pop();
+  Instr Inext;
+  if (inext != BD_END) Inext = P.queue[inext];
+  // last counter (and target) seen satisfied: counters only grow within a
+  // launch, so repeated waits on it need no new load
+  uint32_t ok_bar = NO_BAR, ok_target = 0;
+  for (;;) {
+    const uint32_t i = inext;
+    const Instr in = Inext;
+    if (i != BD_END) {
+      inext = pop();
+      if (inext != BD_END) Inext = P.queue[inext];
     }
     const int si = islot_ctr % NISLOT;
     bool end = i == BD_END;
     if (!bd_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) end = true;
-    Instr in;
     if (!end) {
-      in = P.queue[i];
       *reinterpret_cast<Instr*>(S.islot + si * 48 + 16) = in;
+      bd_mark(P, i, 4);
     }
     *reinterpret_cast<volatile uint32_t*>(S.islot + si * 48) = end ? BD_END : i;
     mbar_arrive(&S.ifull[si]);
@@ -296,8 +318,15 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
       }
       // (after a timeout the loads still run, on stale but valid memory, so
       // that every armed stage completes and the launch can drain)
-      bd_wait_deps(P, in, gen, i);
-      fence_proxy_async_global();
+      const uint32_t target = (gen + 1u) * in.wait_target;
+      if (!(in.wait_bar == ok_bar && target == ok_target)) {
+        if (bd_wait_deps(P, in, gen, i)) {
+          ok_bar = in.wait_bar;
+          ok_target = target;
+        }
+        fence_proxy_async_global();
+      }
+      bd_mark(P, i, 5);
       for (int kb = 0; kb < npre; ++kb) {
         const int st = (s0 + kb) % BD_NSTAGE;
         load_x(S.ring + st * BD_STAGE, kb, &S.full[st]);
@@ -310,6 +339,7 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
         load_x(S.ring + st * BD_STAGE, kb, &S.full[st]);
         ++stage_ctr;
       }
+      bd_mark(P, i, 6);
     } else if (in.op == BD_ATTN) {
       const BdAttn e = bd_attn(P, S, in);
       const int nblk = attn_blocks(e);
@@ -361,6 +391,7 @@ __device__ void bd_mma(const BdParams& P, const BdSh& S, uint32_t tbase) {
       ++use[ab];
       tc_fence_after();
       const uint32_t d = tbase + (uint32_t)ab * BD_ACC_COLS;
+      bd_mark(P, i, 7);
       for (int kb = 0; kb < g.nk; ++kb) {
         const int st = stage_ctr % BD_NSTAGE;
         bd_wait(P, &S.full[st], (stage_ctr / BD_NSTAGE) & 1u);
@@ -377,6 +408,7 @@ __device__ void bd_mma(const BdParams& P, const BdSh& S, uint32_t tbase) {
         tc_commit(&S.empty[st]);
       }
       tc_commit(&S.accf[ab]);
+      bd_mark(P, i, 8);
     } else if (in.op == BD_ATTN) {
       stage_ctr += (uint32_t)bd_stages(P, S, in);  // consumed by the compute warps
     }
@@ -395,54 +427,88 @@ __device__ __forceinline__ float bfw(const uint16_t* p, int i) {
   return __uint_as_float((uint32_t)__ldg(p + i) << 16);
 }
 
-// RMSNorm of sequences [8 r, 8 r + 8) into the hi/lo planes of hn.
+// Layer 0's input norm, sequences [BD_RG r, BD_RG r + BD_RG): the embedding
+// row times the attention-norm gain into the hi/lo planes of hn, and the row's
+// sum of squares into ss1 slot 0 (the QKV epilogue scales by 1 / rms).  One
+// warp per sequence, 8 consecutive columns per lane and step.
 __device__ void bd_norm(const BdParams& P, const BdSh& S, const Instr& in, int wc, int lane) {
-  const int l = in.layer, H = P.H;
-  const float* src;
-  const uint16_t* gain;
-  if (in.op == BD_NORM1) {
-    src = l == 0 ? nullptr : P.xb;
-    gain = P.layers[l].attn_norm;
-  } else if (in.op == BD_NORM2) {
-    src = P.xa;
-    gain = P.layers[l].ffn_norm;
-  } else {
-    src = P.xb;
-    gain = P.final_norm;
+  const int H = P.H;
+  const uint16_t* gain = P.layers[0].attn_norm;
+  const int b = (int)in.a0 * BD_RG + wc;
+  if (wc >= BD_RG || b >= P.B) return;
+  int tok = S.tok[b];
+  if (tok < 0 || tok >= P.V) {
+    if (lane == 0) bd_error(P, MK_ERR_BOUNDS, (uint32_t)b);
+    tok = 0;
   }
-  for (int r = wc; r < BD_RG; r += 4) {
-    const int b = (int)in.a0 * BD_RG + r;
-    if (b >= P.B) break;
-    const uint16_t* emb = nullptr;
-    if (!src) {
-      int tok = S.tok[b];
-      if (tok < 0 || tok >= P.V) {
-        if (lane == 0) bd_error(P, MK_ERR_BOUNDS, (uint32_t)b);
-        tok = 0;
-      }
-      emb = P.embed + (size_t)tok * H;
+  const uint16_t* emb = P.embed + (size_t)tok * H;
+  float ss = 0.f;
+  for (int c = lane * 8; c < H; c += 256) {
+    float x[8], gw[8];
+    widen8(__ldg(reinterpret_cast<const uint4*>(emb + c)), x);
+    widen8(__ldg(reinterpret_cast<const uint4*>(gain + c)), gw);
+    uint16_t hi[8], lo[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ss = fmaf(x[e], x[e], ss);
+      split_bf16(x[e] * gw[e], hi[e], lo[e]);
     }
-    auto xval = [&](int c) -> float { return emb ? bfw(emb, c) : __ldcg(src + (size_t)b * H + c); };
-    float ss = 0.f;
-    for (int c = lane; c < H; c += 32) {
-      const float x = xval(c);
-      ss = fmaf(x, x, ss);
-    }
-    ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss / (float)H + P.eps);
-    for (int c = lane; c < H; c += 32) {
-      uint16_t hi, lo;
-      split_bf16(xval(c) * inv * bfw(gain, c), hi, lo);
-      P.hn[(size_t)b * H + c] = hi;
-      P.hn[((size_t)P.nb + b) * H + c] = lo;
-    }
+    uint4 h, o;
+    h.x = hi[0] | ((uint32_t)hi[1] << 16); h.y = hi[2] | ((uint32_t)hi[3] << 16);
+    h.z = hi[4] | ((uint32_t)hi[5] << 16); h.w = hi[6] | ((uint32_t)hi[7] << 16);
+    o.x = lo[0] | ((uint32_t)lo[1] << 16); o.y = lo[2] | ((uint32_t)lo[3] << 16);
+    o.z = lo[4] | ((uint32_t)lo[5] << 16); o.w = lo[6] | ((uint32_t)lo[7] << 16);
+    *reinterpret_cast<uint4*>(P.hn + (size_t)b * H + c) = h;
+    *reinterpret_cast<uint4*>(P.hn + ((size_t)P.nb + b) * H + c) = o;
   }
+  ss = warp_sum(ss);
+  if (lane == 0) P.ss1[b] = ss;
 }
 
-// Epilogue of a finished GEMM row tile: y[b] is this thread's row (feature
-// 128 m + row) for sequence b.
+// 1 / rms of every live sequence from the per-tile sums of squares (tile
+// order), into S.rinv.  All compute threads call it (it ends with a barrier).
+__device__ void bd_rms_inv(const BdParams& P, const BdSh& S, const float* ss, int nslots) {
+  const int tc = threadIdx.x - 64;
+  if (tc < P.B) {
+    float t = 0.f;
+    for (int k = 0; k < nslots; ++k) t += __ldcg(ss + (size_t)k * BD_NMAX + tc);
+    S.rinv[tc] = 1.0f / sqrtf(t / (float)P.H + P.eps);
+  }
+  cbar_bd();
+}
+
+// The next norm's input for this thread's feature f of row tile m: x * gain
+// into the hi/lo planes of hn, and the tile's sum of squares per sequence
+// (rows in order) into ss[m].  All compute threads call it.
+__device__ void bd_norm_out(const BdParams& P, const BdSh& S, int m, int row, int b0, const float (&x)[16],
+                            const uint16_t* gain, float* ss) {
+  const int tc = threadIdx.x - 64, H = P.H, f = m * BD_M + row;
+  const float gw = bfw(gain, f);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int b = b0 + k;
+    if (b < P.B) {
+      uint16_t hi, lo;
+      split_bf16(x[k] * gw, hi, lo);
+      P.hn[(size_t)b * H + f] = hi;
+      P.hn[((size_t)P.nb + b) * H + f] = lo;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) S.scratch[row * BD_NMAX + b0 + k] = x[k] * x[k];
+  cbar_bd();
+  if (tc < P.B) {
+    float t = 0.f;
+    for (int r = 0; r < BD_M; ++r) t += S.scratch[r * BD_NMAX + tc];
+    ss[(size_t)m * BD_NMAX + tc] = t;
+  }
+  cbar_bd();
+}
+
+// Epilogue of a finished GEMM row tile: y[k] is this thread's row (feature
+// 128 m + row) for sequence b0 + k.
 __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, int row,
-                            const float (&y)[BD_NMAX]) {
+                            int b0, const float (&y)[16]) {
   const int l = in.layer, m = (int)in.a0, tc = threadIdx.x - 64;
   const int B = P.B, H = P.H, d = P.d, qd = P.nq * d, kd = P.nkv * d;
   switch (in.op) {
@@ -451,31 +517,49 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
       const int f = m * BD_M + row;
       float* dst = in.op == BD_O ? P.xa : P.xb;
       const float* res = in.op == BD_O ? P.xb : P.xa;
-      for (int b = 0; b < B; ++b) {
-        float r;
-        if (in.op == BD_O && l == 0) {
-          int tok = S.tok[b];
-          if (tok < 0 || tok >= P.V) tok = 0;  // reported by the layer-0 norm
-          r = bfw(P.embed + (size_t)tok * H, f);
-        } else {
-          r = __ldcg(res + (size_t)b * H + f);
+      float x[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int b = b0 + k;
+        float r = 0.f;
+        if (b < B) {
+          if (in.op == BD_O && l == 0) {
+            int tok = S.tok[b];
+            if (tok < 0 || tok >= P.V) tok = 0;  // reported by the layer-0 norm
+            r = bfw(P.embed + (size_t)tok * H, f);
+          } else {
+            r = __ldcg(res + (size_t)b * H + f);
+          }
         }
-        dst[(size_t)b * H + f] = r + y[b];
+        x[k] = b < B ? r + y[k] : 0.f;
+        if (b < B) dst[(size_t)b * H + f] = x[k];
       }
+      // the next norm's input: the FFN norm after O, the next layer's
+      // attention norm (or the final norm) after down
+      const uint16_t* gain = in.op == BD_O ? P.layers[l].ffn_norm
+                           : l + 1 < P.L  ? P.layers[l + 1].attn_norm
+                                          : P.final_norm;
+      bd_norm_out(P, S, m, row, b0, x, gain, in.op == BD_O ? P.ss2 : P.ss1);
       break;
     }
     case BD_LM: {
+      bd_rms_inv(P, S, P.ss1, (int)P.n_down_m);
       const int f = m * BD_M + row;
-      if (f < P.V)
-        for (int b = 0; b < B; ++b) P.logits[(size_t)b * P.V + f] = y[b];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (f < P.V && b0 + k < B) P.logits[(size_t)(b0 + k) * P.V + f] = y[k] * S.rinv[b0 + k];
       break;
     }
     case BD_GU: {
-      // rows 0..63 gate, 64..127 up (features 64 m + j)
-      for (int b = 0; b < BD_NMAX; ++b) S.scratch[row * BD_NMAX + b] = y[b];
+      // rows 0..63 gate, 64..127 up (features 64 m + j), both scaled by the
+      // FFN norm's 1 / rms
+      bd_rms_inv(P, S, P.ss2, (int)P.n_o_m);
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        S.scratch[row * BD_NMAX + b0 + k] = b0 + k < B ? y[k] * S.rinv[b0 + k] : 0.f;
       cbar_bd();
       const int j = tc & 63;
-      for (int b = tc >> 6; b < B; b += 2) {
+      for (int b = tc >> 6; b < B; b += BD_NC / 64) {
         const float gt = S.scratch[j * BD_NMAX + b], up = S.scratch[(64 + j) * BD_NMAX + b];
         uint16_t hi, lo;
         split_bf16(gt / (1.0f + expf(-gt)) * up, hi, lo);
@@ -486,15 +570,23 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
       break;
     }
     default: {  // BD_QKV
+      // the attention norm's 1 / rms (layer 0: one full-row sum per sequence)
+      bd_rms_inv(P, S, P.ss1, l == 0 ? 1 : (int)P.n_down_m);
       const int f0 = m * BD_M;
       if (f0 >= qd + kd) {  // values: straight into the cache
         const int f = f0 + row - qd - kd, g = f / d, dim = f % d;
-        for (int b = 0; b < B; ++b)
-          P.kv[(cache_row(P, l, 1, b, g) + S.pos[b]) * d + dim] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(y[b]));
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int b = b0 + k;
+          if (b < B)
+            P.kv[(cache_row(P, l, 1, b, g) + S.pos[b]) * d + dim] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(y[k] * S.rinv[b]));
+        }
         break;
       }
-      for (int b = 0; b < BD_NMAX; ++b) S.scratch[row * BD_NMAX + b] = y[b];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        S.scratch[row * BD_NMAX + b0 + k] = b0 + k < B ? y[k] * S.rinv[b0 + k] : 0.f;
       cbar_bd();
       const bool is_q = f0 < qd;
       const int hpt = BD_M / d;  // heads in this tile
@@ -515,7 +607,7 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
       const int half = d / 2;
       // pair i of head hh for sequence b: thread tc takes pair index tc % 64
       const int pi = tc & 63, hh = pi / half, i = pi % half;
-      for (int b = tc >> 6; b < B; b += 2) {
+      for (int b = tc >> 6; b < B; b += BD_NC / 64) {
         float u1 = S.scratch[(hh * d + i) * BD_NMAX + b];
         float u2 = S.scratch[(hh * d + i + half) * BD_NMAX + b];
         if (gn) {
@@ -544,28 +636,51 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
 // One attention split of (sequence b, kv head g): online softmax over its key
 // blocks (K and V tiles in the ring, 128-byte swizzled rows), then the split's
 // (max, sum, unnormalised output) to global memory.  Returns the ring counter.
+//  scores  8 lanes per key (lane `sub` holds 8-column groups sub, sub + 8),
+//          q in registers, a three-level shuffle per head; warp w takes keys
+//          [8 w, 8 w + 8) of the block.
+//  P V     warp w the same 8 keys for every head, lane the columns
+//          [DPL lane, DPL lane + DPL): each V element is widened once for all
+//          heads; the eight warps' partial outputs are added once per split.
 template <int D>
 __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr& in, const BdAttn& e,
                                   uint32_t stage_ctr) {
   const int tc = threadIdx.x - 64, lane = tc & 31, wc = tc >> 5;
   const int b = (int)in.a0, g = (int)in.a1, s = (int)in.a2, rep = P.rep;
   const int qd = P.nq * D;
+  constexpr int G = D / 64;    // 8-column groups per lane in the score pass
+  constexpr int DPL = D / 32;  // output columns per lane in P V
   const float scale = 1.0f / sqrtf((float)D);
-  float* qs = S.qs;     // [rep][D]
-  float* sc = S.sc;     // [rep][BD_KEYS]
-  float* hs = S.hs;     // [rep] x {m, l, alpha}
-  for (int t = tc; t < rep * D; t += BD_NC) qs[t] = __ldcg(P.q + (size_t)b * qd + (size_t)g * rep * D + t);
+  float* sc = S.sc;  // [rep][BD_KEYS]
+  float* hs = S.hs;  // [rep] x {m, l, alpha}
+  const int sub = lane & 7, quad = lane >> 3;
+  float qv[4][G][8];
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      if (h < rep) {
+        const float* qp = P.q + (size_t)b * qd + (size_t)(g * rep + h) * D + (sub + 8 * gi) * 8;
+        const float4 u = __ldcg(reinterpret_cast<const float4*>(qp));
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(qp + 4));
+        qv[h][gi][0] = u.x; qv[h][gi][1] = u.y; qv[h][gi][2] = u.z; qv[h][gi][3] = u.w;
+        qv[h][gi][4] = v.x; qv[h][gi][5] = v.y; qv[h][gi][6] = v.z; qv[h][gi][7] = v.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) qv[h][gi][t] = 0.f;
+      }
+    }
   if (tc < rep) {
     hs[tc * 3 + 0] = -INFINITY;
     hs[tc * 3 + 1] = 0.f;
     hs[tc * 3 + 2] = 0.f;
   }
-  cbar_bd();
-  constexpr int DPL = D / 32;  // output columns per lane in P V
-  float o[DPL];
+  float acc[4][DPL];
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) o[k] = 0.f;
-  const int hpt = (rep + 1) / 2;  // heads per thread in the score pass
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[h][k] = 0.f;
+  cbar_bd();
   const int nblk = attn_blocks(e);
   for (int j = 0; j < nblk; ++j) {
     const int st = stage_ctr % BD_NSTAGE;
@@ -573,31 +688,26 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     ++stage_ctr;
     const uint8_t* kt = S.ring + st * BD_STAGE;
     const uint8_t* vt = kt + BD_STAGE / 2;
-    // scores: thread -> key k (64 keys), heads [hh0, hh0 + hpt)
-    {
-      const int k = tc & 63, hh0 = (tc >> 6) * hpt;
-      const int key = e.lo + j * BD_KEYS + k;
-      float a[4] = {0.f, 0.f, 0.f, 0.f};
+    const int base = e.lo + j * BD_KEYS;
 #pragma unroll
-      for (int c8 = 0; c8 < D / 8; ++c8) {
-        const int bx = c8 >> 3, cc = c8 & 7;
-        const uint4 w = *reinterpret_cast<const uint4*>(kt + bx * (BD_KEYS * 128) + k * 128 +
-                                                        ((cc ^ (k & 7)) << 4));
-        float kx[8];
-        widen8(w, kx);
+    for (int pass = 0; pass < 2; ++pass) {
+      const int k = wc * 8 + pass * 4 + quad;
+      float kx[G][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int h = hh0 + u;
-          if (u < hpt && h < rep) {
+      for (int gi = 0; gi < G; ++gi)
+        widen8(*reinterpret_cast<const uint4*>(kt + gi * (BD_KEYS * 128) + k * 128 + ((sub ^ (k & 7)) << 4)),
+               kx[gi]);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) a[u] = fmaf(qs[h * D + c8 * 8 + t], kx[t], a[u]);
-          }
-        }
-      }
+      for (int h = 0; h < 4; ++h) {
+        float a = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int h = hh0 + u;
-        if (u < hpt && h < rep) sc[h * BD_KEYS + k] = key < e.hi ? a[u] * scale : -INFINITY;
+        for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+          for (int t = 0; t < 8; ++t) a = fmaf(qv[h][gi][t], kx[gi][t], a);
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        if (sub == 0 && h < rep) sc[h * BD_KEYS + k] = base + k < e.hi ? a * scale : -INFINITY;
       }
     }
     cbar_bd();
@@ -621,43 +731,60 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
       }
     }
     cbar_bd();
-    // P V: warp h owns head h, lane the columns [DPL lane, DPL lane + DPL)
-    if (wc < rep) {
-      const float alpha = hs[wc * 3 + 2];
+    // P V over this warp's 16 keys (keys past the split are skipped, not
+    // weighted by zero: the cache rows there may hold anything)
+    {
 #pragma unroll
-      for (int k = 0; k < DPL; ++k) o[k] *= alpha;
+      for (int h = 0; h < 4; ++h) {
+        const float alpha = h < rep ? hs[h * 3 + 2] : 0.f;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[h][k] *= alpha;
+      }
       const int col = lane * DPL, bx = col >> 6, cin = col & 63;
-      // keys past the split are skipped, not weighted by zero: the cache
-      // rows there may hold anything
-      const int kval = e.hi - (e.lo + j * BD_KEYS) < BD_KEYS ? e.hi - (e.lo + j * BD_KEYS) : BD_KEYS;
-      for (int k = 0; k < kval; ++k) {
-        const float p = sc[wc * BD_KEYS + k];
+      const int k0 = wc * 8;
+      const int k1 = e.hi - base < k0 + 8 ? e.hi - base : k0 + 8;
+      for (int k = k0; k < k1; ++k) {
         const uint8_t* vr = vt + bx * (BD_KEYS * 128) + k * 128 + ((((cin >> 3) ^ (k & 7))) << 4) + (cin & 7) * 2;
+        float vx[DPL];
         if constexpr (DPL == 4) {
           const uint2 u = *reinterpret_cast<const uint2*>(vr);
-          o[0] = fmaf(p, bf_lo(u.x), o[0]);
-          o[1] = fmaf(p, bf_hi(u.x), o[1]);
-          o[2] = fmaf(p, bf_lo(u.y), o[2]);
-          o[3] = fmaf(p, bf_hi(u.y), o[3]);
+          vx[0] = bf_lo(u.x); vx[1] = bf_hi(u.x); vx[2] = bf_lo(u.y); vx[3] = bf_hi(u.y);
         } else {
           const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
-          o[0] = fmaf(p, bf_lo(u), o[0]);
-          o[1] = fmaf(p, bf_hi(u), o[1]);
+          vx[0] = bf_lo(u); vx[1] = bf_hi(u);
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          if (h < rep) {
+            const float p = sc[h * BD_KEYS + k];
+#pragma unroll
+            for (int t = 0; t < DPL; ++t) acc[h][t] = fmaf(p, vx[t], acc[h][t]);
+          }
         }
       }
     }
     cbar_bd();  // every warp is done with the stage and the probabilities
     if (tc == 0) mbar_arrive(&S.empty[st]);
   }
-  // the split's partial: o (unnormalised), max, sum per head
-  float* part = P.apart + (((size_t)b * P.nkv + g) * BD_NSPLIT + s) * rep * (D + 2);
-  if (wc < rep) {
+  // add the eight warps' partial outputs (warp order), then the split's
+  // partial: o (unnormalised), max, sum per head
+  float* red = S.scratch;  // [8 warps][4 heads][D]
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) part[wc * (D + 2) + lane * DPL + k] = o[k];
-    if (lane == 0) {
-      part[wc * (D + 2) + D] = hs[wc * 3 + 0];
-      part[wc * (D + 2) + D + 1] = hs[wc * 3 + 1];
-    }
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) red[(wc * 4 + h) * D + lane * DPL + k] = acc[h][k];
+  cbar_bd();
+  float* part = P.apart + (((size_t)b * P.nkv + g) * BD_NSPLIT + s) * rep * (D + 2);
+  for (int t = tc; t < rep * D; t += BD_NC) {
+    const int h = t / D, c = t % D;
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) o += red[(w * 4 + h) * D + c];
+    part[h * (D + 2) + c] = o;
+  }
+  if (tc < rep) {
+    part[tc * (D + 2) + D] = hs[tc * 3 + 0];
+    part[tc * (D + 2) + D + 1] = hs[tc * 3 + 1];
   }
   return stage_ctr;
 }
@@ -690,7 +817,7 @@ __device__ void bd_attn_combine(const BdParams& P, int b, int g) {
 }
 
 __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
-  const int wc = (threadIdx.x >> 5) - 2;  // 0..3
+  const int wc = (threadIdx.x >> 5) - 2;  // compute warp 0..7
   const int lane = threadIdx.x & 31;
   const int tc = threadIdx.x - 64;
   const int q = (threadIdx.x >> 5) & 3;   // TMEM lane quarter this warp may access
@@ -714,6 +841,12 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
     if (lane == 0) mbar_arrive(&S.iempty[si]);
     ++islot_ctr;
     if (i == BD_END) break;
+    if (tc == 0) {
+      bd_mark(P, i, 1);
+      if (P.trace)
+        P.trace[(size_t)i * TRACE_WORDS] =
+            (unsigned long long)smid() | ((unsigned long long)(in.op | (in.layer << 8)) << 32);
+    }
     bool release = true;
     if (is_gemm(in.op)) {
       const BdGemm gm = bd_gemm(P, in);
@@ -722,22 +855,11 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
       ++use[ab];
       stage_ctr += (uint32_t)gm.nk;
       tc_fence_after();
-      float y[BD_NMAX];
-      const uint32_t t0 = tbase + (uint32_t)ab * BD_ACC_COLS + lane_base;
-      {
-        float v[16];
-        tmem_ld16(t0, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) y[k] = v[k];
-        if (P.nb > 16) {
-          tmem_ld16(t0 + 16, v);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) y[16 + k] = v[k];
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) y[16 + k] = 0.f;
-        }
-      }
+      if (tc == 0) bd_mark(P, i, 2);
+      // batch columns [b0, b0 + 16) of this thread's row (feature)
+      const int b0 = 16 * (wc >> 2);
+      float y[16];
+      tmem_ld16(tbase + (uint32_t)ab * BD_ACC_COLS + lane_base + (uint32_t)b0, y);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.acce[ab]);
@@ -746,7 +868,7 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
         // all chunks in chunk order and runs the epilogue
         float* mine = P.part + ((size_t)gm.tile * gm.chunks + in.a1) * BD_NMAX * BD_M;
 #pragma unroll
-        for (int b = 0; b < BD_NMAX; ++b) mine[b * BD_M + row] = y[b];
+        for (int k = 0; k < 16; ++k) mine[(b0 + k) * BD_M + row] = y[k];
         cbar_bd();
         if (tc == 0) {
           uint32_t* arr = P.arrive + gm.tile;
@@ -760,20 +882,23 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
         if (release) {
           const float* base = P.part + (size_t)gm.tile * gm.chunks * BD_NMAX * BD_M;
 #pragma unroll
-          for (int b = 0; b < BD_NMAX; ++b) y[b] = 0.f;
+          for (int k = 0; k < 16; ++k) y[k] = 0.f;
           for (int c = 0; c < gm.chunks; ++c)
 #pragma unroll
-            for (int b = 0; b < BD_NMAX; ++b)
-              y[b] += __ldcg(base + ((size_t)c * BD_NMAX + b) * BD_M + row);
+            for (int k = 0; k < 16; ++k)
+              y[k] += __ldcg(base + ((size_t)c * BD_NMAX + b0 + k) * BD_M + row);
         }
       }
-      if (release) bd_epilogue(P, S, in, row, y);
+      if (release) bd_epilogue(P, S, in, row, b0, y);
     } else if (in.op == BD_ATTN) {
       const BdAttn e = bd_attn(P, S, in);
       if (!e.live) {
         release = in.a2 == 0;  // one release per dead (b, g) group
       } else {
-        if (tc == 0) S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+        if (tc == 0) {
+          S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+          bd_mark(P, i, 2);
+        }
         cbar_bd();
         if (P.d == 128) stage_ctr = bd_attn_split<128>(P, S, in, e, stage_ctr);
         else stage_ctr = bd_attn_split<64>(P, S, in, e, stage_ctr);
@@ -793,7 +918,10 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
         }
       }
     } else if (is_norm(in.op)) {
-      if (tc == 0) S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+      if (tc == 0) {
+        S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+        bd_mark(P, i, 2);
+      }
       cbar_bd();
       if (!S.flags[BF_ABORT]) bd_norm(P, S, in, wc, lane);
     }
@@ -801,6 +929,7 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
     cbar_bd();
     if (tc == 0 && release && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
       red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+    if (tc == 0) bd_mark(P, i, 3);
   }
 }
 
@@ -815,11 +944,11 @@ __global__ void __launch_bounds__(BD_THREADS, 1) mk_bdecode_kernel(const __grid_
     }
     for (int s = 0; s < NISLOT; ++s) {
       mbar_init(&S.ifull[s], 1);
-      mbar_init(&S.iempty[s], 5);  // issuer + 4 compute warps
+      mbar_init(&S.iempty[s], 9);  // issuer + 8 compute warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.accf[b], 1);
-      mbar_init(&S.acce[b], 4);
+      mbar_init(&S.acce[b], 8);
     }
     fence_mbar_init();
     fence_proxy_async_smem();

@@ -120,9 +120,12 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, BdPlan* out
     }
     end(s);
   };
+  // layer 0's input norm is its own instruction (the embedding rows); every
+  // later norm is folded into the O / down epilogues (see mk_bdecode.h)
+  norm(BD_NORM1, 0, NO_BAR, 0, b.norm1);
   for (int l = 0; l < L; ++l) {
-    norm(BD_NORM1, l, l > 0 ? b.down + l - 1 : NO_BAR, bp.n_down_m, b.norm1 + l);
-    gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, b.norm1 + l, (uint32_t)bp.n_rg, b.qkv + l);
+    if (l == 0) gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, b.norm1, (uint32_t)bp.n_rg, b.qkv + l);
+    else gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, b.down + l - 1, bp.n_down_m, b.qkv + l);
     {
       const uint32_t s = begin();
       for (int bb = 0; bb < max_batch; ++bb)
@@ -136,12 +139,10 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, BdPlan* out
       end(s);
     }
     gemm(BD_O, l, bp.n_o_m, bp.c_q, b.attn + l, (uint32_t)(max_batch * nkv), b.o + l);
-    norm(BD_NORM2, l, b.o + l, bp.n_o_m, b.norm2 + l);
-    gemm(BD_GU, l, bp.n_gu_m, bp.c_h, b.norm2 + l, (uint32_t)bp.n_rg, b.gu + l);
+    gemm(BD_GU, l, bp.n_gu_m, bp.c_h, b.o + l, bp.n_o_m, b.gu + l);
     gemm(BD_DOWN, l, bp.n_down_m, bp.c_f, b.gu + l, bp.n_gu_m, b.down + l);
   }
-  norm(BD_NORMF, L - 1, b.down + L - 1, bp.n_down_m, b.normf);
-  gemm(BD_LM, L - 1, bp.n_lm_m, 1, b.normf, (uint32_t)bp.n_rg, b.lm);
+  gemm(BD_LM, L - 1, bp.n_lm_m, 1, b.down + L - 1, bp.n_down_m, b.lm);
   return MK_OK;
 }
 

@@ -150,6 +150,8 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   const size_t o_ao = bm.take(4 * (size_t)NB * qd);
   const size_t o_act = bm.take(4 * (size_t)NB * F);
   const size_t o_qv = bm.take(sizeof(float) * NB * qd);
+  const size_t o_ss1 = bm.take(sizeof(float) * std::max<uint32_t>(bp.n_down_m, 1) * BD_NMAX);
+  const size_t o_ss2 = bm.take(sizeof(float) * bp.n_o_m * BD_NMAX);
   const size_t o_part = bm.take(sizeof(float) * pairs * BD_NMAX * BD_M);
   const size_t o_apart = bm.take(sizeof(float) * bp.max_batch * nkv * BD_NSPLIT * bp.rep * (d + 2));
   s.arrive_words = (size_t)max_m + (size_t)bp.max_batch * nkv;
@@ -201,6 +203,8 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   k.ao = (uint16_t*)(b + o_ao);
   k.act = (uint16_t*)(b + o_act);
   k.q = (float*)(b + o_qv);
+  k.ss1 = (float*)(b + o_ss1);
+  k.ss2 = (float*)(b + o_ss2);
   k.part = (float*)(b + o_part);
   k.apart = (float*)(b + o_apart);
   k.arrive = (uint32_t*)(b + o_arr);
@@ -237,6 +241,7 @@ BdParams bd_params(mk_plan* p, const int32_t* tokens, const int32_t* positions, 
   k.logits = logits;
   k.mode = MODE_MEGA;
   k.wait_limit_ns = p->wait_limit_ns;
+  k.trace = p->trace ? p->d_trace : nullptr;
   return k;
 }
 
@@ -288,6 +293,7 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
       out->n_barriers = bp.bl.total;
       out->n_launches_per_op_decode = (uint32_t)bp.perop.size();
       out->n_splits = BD_NSPLIT;
+      out->decode_path = 1;
     }
     return rc;
   }
@@ -509,6 +515,7 @@ int mk_plan_get_stats(const mk_plan* p, mk_plan_stats* out) {
     out->n_barriers = p->bd.bp.bl.total;
     out->n_launches_per_op_decode = (uint32_t)p->bd.bp.perop.size();
     out->n_splits = BD_NSPLIT;
+    out->decode_path = 1;
   }
   return MK_OK;
 }
@@ -839,9 +846,10 @@ int mk_plan_set_debug(mk_plan* p, int force_ctas, uint64_t queue_perm_seed, int 
   p->wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000ull;
   int rc = p->bd.on ? bd_upload_queue(p, queue_perm_seed) : upload_mk_queue(p, queue_perm_seed);
   if (rc != MK_OK) return rc;
+  const size_t n_rec = p->bd.on ? p->bd.bp.queue.size() : p->hp.decode.size();
   if (trace && !p->d_trace) {
-    if (cudaMalloc(&p->d_trace, p->hp.decode.size() * TRACE_WORDS * 8) != cudaSuccess) return MK_ERR_CUDA;
-    MK_CUDA(cudaMemset(p->d_trace, 0, p->hp.decode.size() * TRACE_WORDS * 8));
+    if (cudaMalloc(&p->d_trace, n_rec * TRACE_WORDS * 8) != cudaSuccess) return MK_ERR_CUDA;
+    MK_CUDA(cudaMemset(p->d_trace, 0, n_rec * TRACE_WORDS * 8));
   }
   p->trace = trace ? 1 : 0;
   return MK_OK;
@@ -864,7 +872,7 @@ int mk_trace_copy(mk_plan* p, void* host_buf, size_t bytes, size_t* n_records) {
   *n_records = 0;
   if (!p->d_trace) return MK_ERR_INVALID_ARG;
   MK_CUDA(cudaDeviceSynchronize());
-  size_t n = p->hp.decode.size();
+  size_t n = p->bd.on ? p->bd.bp.queue.size() : p->hp.decode.size();
   if (bytes / (TRACE_WORDS * 8) < n) n = bytes / (TRACE_WORDS * 8);
   MK_CUDA(cudaMemcpy(host_buf, p->d_trace, n * TRACE_WORDS * 8, cudaMemcpyDeviceToHost));
   *n_records = n;

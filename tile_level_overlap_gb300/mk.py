@@ -54,7 +54,8 @@ class mk_plan_stats(ctypes.Structure):
     _fields_ = [("n_instr_decode", ctypes.c_uint32), ("n_instr_prefill", ctypes.c_uint32),
                 ("n_barriers", ctypes.c_uint32), ("n_launches_per_op_decode", ctypes.c_uint32),
                 ("n_ctas", ctypes.c_uint32), ("n_splits", ctypes.c_uint32),
-                ("weight_bytes", ctypes.c_uint64), ("scratch_bytes", ctypes.c_uint64)]
+                ("weight_bytes", ctypes.c_uint64), ("scratch_bytes", ctypes.c_uint64),
+                ("decode_path", ctypes.c_uint32)]
 
 
 _lib = None
