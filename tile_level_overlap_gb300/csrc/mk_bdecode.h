@@ -49,7 +49,7 @@ constexpr int BD_NMAX = 32;     // most sequences per step (tcgen05 N)
 constexpr int BD_KC = 1024;     // K chunk of a split-K tile
 constexpr int BD_RG = 8;        // sequences per RMSNorm instruction (one compute warp each)
 constexpr int BD_KEYS = 64;     // cached keys per attention stage
-constexpr int BD_NSPLIT = 4;    // attention splits per (sequence, kv head)
+constexpr int BD_NSPLIT_MAX = 8;  // attention splits per (sequence, kv head), at most
 
 // Barrier sub-tensors: one counter per layer and operator.
 struct BdBars {
@@ -59,6 +59,7 @@ struct BdBars {
 struct BdPlan {
   mk_model_cfg cfg{};
   int max_batch = 0, max_ctx = 0, nb = 0;  // nb: batch columns (16 or 32)
+  int nsplit = 0;  // attention splits per (sequence, kv head)
   int rep = 0, qkv_rows = 0, n_rg = 0;
   uint32_t n_qkv_m = 0, n_o_m = 0, n_gu_m = 0, n_down_m = 0, n_lm_m = 0;  // row tiles
   uint32_t c_h = 0, c_q = 0, c_f = 0;  // K chunks for K = H, n_q*d, F
@@ -74,7 +75,7 @@ enum BdMap { TMB_WQ = 0, TMB_WK = 1, TMB_WV = 2, TMB_WO = 3, TMB_WG = 4, TMB_WU 
 enum BdGlobalMap { TMB_LM = 0, TMB_HN = 1, TMB_AO = 2, TMB_ACT = 3, TMB_KV = 4, TMB_COUNT = 5 };
 
 struct BdParams {
-  int L, H, nq, nkv, d, F, V, qk_norm, rep, qkv_rows, max_ctx, max_batch, nb, n_rg;
+  int L, H, nq, nkv, d, F, V, qk_norm, rep, qkv_rows, max_ctx, max_batch, nb, n_rg, nsplit;
   float eps;
   uint32_t n_qkv_m, n_o_m, n_gu_m, n_down_m, n_lm_m, c_h, c_q, c_f;
   const uint16_t* embed;
@@ -90,7 +91,7 @@ struct BdParams {
   float* ss1;               // sums of x^2 per (row tile, sequence) for the next QKV / LM [tiles][BD_NMAX]
   float* ss2;               // the same for the gate/up projection [tiles][BD_NMAX]
   float* part;              // split-K partial sums [row tile][chunk][BD_NMAX][128] of one operator
-  float* apart;             // attention split partials [nb][n_kv][BD_NSPLIT][rep][d + 2]
+  float* apart;             // attention split partials [max_batch][n_kv][nsplit][rep][d + 2]
   uint32_t* arrive;         // arrival counters: [row tiles of one operator] then [max_batch * n_kv]
   uint32_t n_arrive_gemm;   // row-tile counters (the attention ones follow)
   uint16_t* kv;             // caller's KV cache
@@ -110,12 +111,15 @@ struct BdParams {
   // layer << 8) << 32, [1] compute warps took it, [2] inputs ready (GEMM:
   // accumulator full; attention / norm: dependencies met), [3] done, [4]
   // producer posted it, [5] producer's dependency wait met, [6] producer
-  // issued its last stage, [7] first MMA issued, [8] last MMA committed.
+  // issued its last stage, [7] first MMA issued, [8] last MMA committed;
+  // attention splits: [9] first key block ready, [10] last key block done.
   unsigned long long* trace;
 };
 
 // Shapes the tensor-core batched path takes (MK_OK) or why not.
-int build_bdecode(const mk_model_cfg& cfg, int max_batch, int max_ctx, BdPlan* out, std::string* why);
+// n_sms: SMs of the device (sets the attention split count); 0 = DEFAULT_SMS.
+int build_bdecode(const mk_model_cfg& cfg, int max_batch, int max_ctx, int n_sms, BdPlan* out,
+                  std::string* why);
 int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string* why);
 void random_order_bdecode(const BdPlan& bp, uint64_t seed, std::vector<Instr>* out);
 

@@ -223,7 +223,7 @@ __device__ __forceinline__ BdAttn bd_attn(const BdParams& P, const BdSh& S, cons
   e.lo = e.hi = 0;
   if (e.live) {
     const int n = S.pos[b] + 1;
-    const int len = (n + BD_NSPLIT - 1) / BD_NSPLIT;
+    const int len = (n + P.nsplit - 1) / P.nsplit;
     e.lo = s * len < n ? s * len : n;
     e.hi = e.lo + len < n ? e.lo + len : n;
   }
@@ -346,6 +346,7 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
       if (nblk == 0) continue;
       bd_wait_deps(P, in, gen, i);
       fence_proxy_async_global();
+      bd_mark(P, i, 5);
       const int l = in.layer, b = (int)in.a0, g = (int)in.a1;
       const int nbox = P.d / 64;
       const uint32_t half = BD_STAGE / 2;
@@ -360,6 +361,7 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
                         (int)(cache_row(P, l, kv, b, g) + e.lo + j * BD_KEYS), &S.full[st], pol_a);
         ++stage_ctr;
       }
+      bd_mark(P, i, 6);
     }
   }
   // the copies this thread issued have landed before it leaves
@@ -644,7 +646,7 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
 //          heads; the eight warps' partial outputs are added once per split.
 template <int D>
 __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr& in, const BdAttn& e,
-                                  uint32_t stage_ctr) {
+                                  uint32_t stage_ctr, uint32_t idx) {
   const int tc = threadIdx.x - 64, lane = tc & 31, wc = tc >> 5;
   const int b = (int)in.a0, g = (int)in.a1, s = (int)in.a2, rep = P.rep;
   const int qd = P.nq * D;
@@ -686,6 +688,7 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     const int st = stage_ctr % BD_NSTAGE;
     bd_wait(P, &S.full[st], (stage_ctr / BD_NSTAGE) & 1u);
     ++stage_ctr;
+    if (j == 0 && tc == 0) bd_mark(P, idx, 9);
     const uint8_t* kt = S.ring + st * BD_STAGE;
     const uint8_t* vt = kt + BD_STAGE / 2;
     const int base = e.lo + j * BD_KEYS;
@@ -766,6 +769,7 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     cbar_bd();  // every warp is done with the stage and the probabilities
     if (tc == 0) mbar_arrive(&S.empty[st]);
   }
+  if (tc == 0) bd_mark(P, idx, 10);
   // add the eight warps' partial outputs (warp order), then the split's
   // partial: o (unnormalised), max, sum per head
   float* red = S.scratch;  // [8 warps][4 heads][D]
@@ -774,7 +778,7 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
 #pragma unroll
     for (int k = 0; k < DPL; ++k) red[(wc * 4 + h) * D + lane * DPL + k] = acc[h][k];
   cbar_bd();
-  float* part = P.apart + (((size_t)b * P.nkv + g) * BD_NSPLIT + s) * rep * (D + 2);
+  float* part = P.apart + (((size_t)b * P.nkv + g) * P.nsplit + s) * rep * (D + 2);
   for (int t = tc; t < rep * D; t += BD_NC) {
     const int h = t / D, c = t % D;
     float o = 0.f;
@@ -793,15 +797,13 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
 template <int D>
 __device__ void bd_attn_combine(const BdParams& P, int b, int g) {
   const int tc = threadIdx.x - 64, rep = P.rep, qd = P.nq * D;
-  const float* gp = P.apart + ((size_t)b * P.nkv + g) * BD_NSPLIT * rep * (D + 2);
+  const float* gp = P.apart + ((size_t)b * P.nkv + g) * P.nsplit * rep * (D + 2);
   for (int t = tc; t < rep * D; t += BD_NC) {
     const int h = t / D, c = t % D;
     float M = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < BD_NSPLIT; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
+    for (int s = 0; s < P.nsplit; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
     float Lsum = 0.f, O = 0.f;
-#pragma unroll
-    for (int s = 0; s < BD_NSPLIT; ++s) {
+    for (int s = 0; s < P.nsplit; ++s) {
       const float* ps = gp + ((size_t)s * rep + h) * (D + 2);
       const float ms = __ldcg(ps + D);
       const float f = ms == -INFINITY ? 0.f : expf(ms - M);
@@ -900,13 +902,13 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
           bd_mark(P, i, 2);
         }
         cbar_bd();
-        if (P.d == 128) stage_ctr = bd_attn_split<128>(P, S, in, e, stage_ctr);
-        else stage_ctr = bd_attn_split<64>(P, S, in, e, stage_ctr);
+        if (P.d == 128) stage_ctr = bd_attn_split<128>(P, S, in, e, stage_ctr, i);
+        else stage_ctr = bd_attn_split<64>(P, S, in, e, stage_ctr, i);
         cbar_bd();
         if (tc == 0) {
           uint32_t* arr = P.arrive + P.n_arrive_gemm + (size_t)in.a0 * P.nkv + in.a1;
           const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
-          const bool last = old == (uint32_t)(BD_NSPLIT - 1);
+          const bool last = old == (uint32_t)(P.nsplit - 1);
           if (last) *arr = 0u;
           S.flags[BF_LAST] = last ? 1u : 0u;
         }

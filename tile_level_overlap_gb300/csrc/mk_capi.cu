@@ -153,7 +153,7 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   const size_t o_ss1 = bm.take(sizeof(float) * std::max<uint32_t>(bp.n_down_m, 1) * BD_NMAX);
   const size_t o_ss2 = bm.take(sizeof(float) * bp.n_o_m * BD_NMAX);
   const size_t o_part = bm.take(sizeof(float) * pairs * BD_NMAX * BD_M);
-  const size_t o_apart = bm.take(sizeof(float) * bp.max_batch * nkv * BD_NSPLIT * bp.rep * (d + 2));
+  const size_t o_apart = bm.take(sizeof(float) * bp.max_batch * nkv * bp.nsplit * bp.rep * (d + 2));
   s.arrive_words = (size_t)max_m + (size_t)bp.max_batch * nkv;
   const size_t o_arr = bm.take(sizeof(uint32_t) * s.arrive_words);
   if (cudaMalloc(&s.mem, bm.off) != cudaSuccess) {
@@ -190,7 +190,7 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   std::memset(&k, 0, sizeof(k));
   k.L = L; k.H = H; k.nq = c.n_q_heads; k.nkv = nkv; k.d = d; k.F = F; k.V = c.vocab;
   k.qk_norm = c.qk_norm; k.rep = bp.rep; k.qkv_rows = bp.qkv_rows; k.max_ctx = bp.max_ctx;
-  k.max_batch = bp.max_batch; k.nb = NB; k.n_rg = bp.n_rg; k.eps = c.rms_eps;
+  k.max_batch = bp.max_batch; k.nb = NB; k.n_rg = bp.n_rg; k.nsplit = bp.nsplit; k.eps = c.rms_eps;
   k.n_qkv_m = bp.n_qkv_m; k.n_o_m = bp.n_o_m; k.n_gu_m = bp.n_gu_m; k.n_down_m = bp.n_down_m;
   k.n_lm_m = bp.n_lm_m; k.c_h = bp.c_h; k.c_q = bp.c_q; k.c_f = bp.c_f;
   k.embed = (const uint16_t*)w->embed;
@@ -282,7 +282,7 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
   int rc = build_plan(*cfg, max_batch, max_ctx, 0, &hp, &why);
   if (rc == MK_ERR_UNSUPPORTED && max_batch > 1) {
     BdPlan bp;
-    if (build_bdecode(*cfg, max_batch, max_ctx, &bp, &why) != MK_OK) return rc;
+    if (build_bdecode(*cfg, max_batch, max_ctx, 0, &bp, &why) != MK_OK) return rc;
     std::vector<Instr> q = bp.queue;
     if (queue_perm_seed) random_order_bdecode(bp, queue_perm_seed, &q);
     if (q.size() != bp.queue.size()) return MK_ERR_INVALID_ARG;
@@ -292,7 +292,7 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
       out->n_instr_decode = (uint32_t)bp.queue.size();
       out->n_barriers = bp.bl.total;
       out->n_launches_per_op_decode = (uint32_t)bp.perop.size();
-      out->n_splits = BD_NSPLIT;
+      out->n_splits = (uint32_t)bp.nsplit;
       out->decode_path = 1;
     }
     return rc;
@@ -340,7 +340,7 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   p->max_batch = max_batch;
   int rc = build_plan(*cfg, max_batch, max_ctx, sms, &p->hp, &why);
   if (rc == MK_ERR_UNSUPPORTED && max_batch > 1 &&
-      build_bdecode(*cfg, max_batch, max_ctx, &p->bd.bp, &why) == MK_OK) {
+      build_bdecode(*cfg, max_batch, max_ctx, sms, &p->bd.bp, &why) == MK_OK) {
     // the batch goes to the tensor-core path; the CUDA-core plan keeps one
     // sequence for the prefill's LM head
     p->bd.on = true;
@@ -514,7 +514,7 @@ int mk_plan_get_stats(const mk_plan* p, mk_plan_stats* out) {
     out->n_instr_decode = (uint32_t)p->bd.bp.queue.size();
     out->n_barriers = p->bd.bp.bl.total;
     out->n_launches_per_op_decode = (uint32_t)p->bd.bp.perop.size();
-    out->n_splits = BD_NSPLIT;
+    out->n_splits = (uint32_t)p->bd.bp.nsplit;
     out->decode_path = 1;
   }
   return MK_OK;
