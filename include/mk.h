@@ -194,8 +194,8 @@ int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t 
 
 /* Test and measurement options.  force_ctas > 0 launches that many persistent
  * CTAs (<= the co-resident limit); queue_perm_seed != 0 rebuilds the decode
- * queue in a seeded random topological order; trace = 1 records one 32-byte
- * record per instruction; wait_limit_ns bounds every device-side wait
+ * queue in a seeded random topological order; trace = 1 records one 128-byte
+ * record per instruction (mk_trace_copy); wait_limit_ns bounds every device-side wait
  * (0 = default 2 s). */
 int mk_plan_set_debug(mk_plan *plan, int force_ctas, uint64_t queue_perm_seed, int trace,
                       uint64_t wait_limit_ns);
@@ -220,17 +220,22 @@ int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int
                        void *stream);
 
 /* Copy the trace of the last traced launch (mk_plan_set_debug(trace = 1)):
- * 12 x uint64 per instruction (96 bytes), indexed by queue position, times in
+ * 16 x uint64 per instruction (128 bytes), indexed by queue position, times in
  * %globaltimer ns.  CUDA-core decode: {smid | (op | layer << 8) << 32, consumer
  * took it, its waits were satisfied, done, producer posted it, ns spent waiting
  * for operand stages, first operand stage ready, ns the producer waited for free
- * stages, then for batch-1 GEMV tiles: last stage consumed (attention: inputs
- * rotated), finisher took it (attention: scores done), attention: softmax and
- * P V done, split arrival counted}.  Tensor-core batched decode
- * (mk_plan_stats.decode_path = 1): {smid | (op | layer << 8) << 32, compute
- * warps took it, inputs ready (GEMM: accumulator full; otherwise dependencies
- * met), done, producer posted it, producer's dependency wait met, producer
- * issued its last stage, first MMA issued, last MMA committed, 0, 0, 0}.
+ * stages, then for GEMV tiles: last stage consumed (batch-1 tiles), finisher
+ * took it (batch-1 tiles), instruction reached every consumer warp, hand-off
+ * buffer free (batch-1 tiles); for attention tiles: inputs rotated, scores
+ * done, softmax and P V done, split arrival counted; then consumer loop top
+ * before the instruction was taken, and for batch-1 GEMV tiles: consumer warp
+ * 7 reached the hand-off, finisher added the partial sums, consumer warp 0
+ * finished the hand-off}.  Tensor-core batched
+ * decode (mk_plan_stats.decode_path = 1): {smid | (op | layer << 8) << 32,
+ * compute warps took it, inputs ready (GEMM: accumulator full; otherwise
+ * dependencies met), done, producer posted it, producer's dependency wait met,
+ * producer issued its last stage, first MMA issued, last MMA committed, then
+ * for attention splits: first key block ready, last key block done; 0 x 5}.
  * *n_records receives the count copied.  Waits for the device. */
 int mk_trace_copy(mk_plan *plan, void *host_buf, size_t bytes, size_t *n_records);
 

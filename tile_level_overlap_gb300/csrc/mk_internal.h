@@ -154,7 +154,7 @@ enum Mode : int { MODE_MEGA = 0, MODE_PEROP = 1 };
 // GEMV) the finisher took it; for attention tiles [8]..[11] mark its phases
 // (inputs rotated, scores, softmax and P V, split arrival).  For handed-off
 // tiles [3] is written by the finisher after its release.
-constexpr int TRACE_WORDS = 12;
+constexpr int TRACE_WORDS = 16;
 
 // Everything one launch needs, passed by value as a __grid_constant__ parameter.
 struct KParams {

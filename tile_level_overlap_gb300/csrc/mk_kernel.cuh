@@ -279,9 +279,13 @@ __device__ void producer(const KParams& P, const Sh& S) {
   if (lane != 0) return;
   const uint64_t policy = policy_evict_first();
   uint32_t stage_ctr = 0, islot_ctr = 0;
-  // Pops run two instructions ahead of the one being streamed, so the latency
-  // of the queue atomic and of the record load overlaps the streaming of the
-  // current instruction.  Pop order is still this CTA's execution order.
+  // An instruction is popped only once the ring has a free stage for its first
+  // operand block, i.e. when this CTA can start streaming it.  A CTA whose
+  // consumers wait on a dependency therefore holds at most the one instruction
+  // it is prefetching, and the rest of a dependency-gated operator goes to the
+  // CTAs that reach it first instead of queueing behind the waiting one.  The
+  // pop and record latency overlap the consumers' work on the stages already
+  // in the ring.
   uint32_t npop = 0;
   auto pop = [&]() -> uint32_t {
     const uint32_t k = npop++;
@@ -292,36 +296,28 @@ __device__ void producer(const KParams& P, const Sh& S) {
     }
     return k == 0 ? P.perop_base + blockIdx.x : END_SLOT;
   };
-  uint32_t ia = pop();
-  uint32_t ib = pop();
-  Instr Ia;
-  if (ia != END_SLOT) Ia = P.queue[ia];
   for (;;) {
-    const bool end = ia == END_SLOT;
-    Instr Ib;
-    if (!end && ib != END_SLOT) Ib = P.queue[ib];
-    const uint32_t ic = (end || ib == END_SLOT) ? END_SLOT : pop();
+    const bool room = mbar_wait(P, &S.empty[stage_ctr % NSTAGE], ((stage_ctr / NSTAGE) & 1u) ^ 1u);
+    const uint32_t i_in = room ? pop() : END_SLOT;
+    const bool end = i_in == END_SLOT;
+    Instr in;
+    if (!end) in = P.queue[i_in];
     const int si = islot_ctr % NISLOT;
     bool posted_end = end;
     AttnExt ext;
     ext.live = false;
-    if (!end && Ia.op == OP_ATTN) ext = attn_extent(P, Ia);
+    if (!end && in.op == OP_ATTN) ext = attn_extent(P, in);
     if (!mbar_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) posted_end = true;
     if (!posted_end) {
-      *slot_instr(S, si) = Ia;
+      *slot_instr(S, si) = in;
       slot_put_ext(S, si, ext);
     }
-    *slot_index(S, si) = posted_end ? END_SLOT : ia;
+    *slot_index(S, si) = posted_end ? END_SLOT : i_in;
     mbar_arrive(&S.ifull[si]);
-    if (P.trace && !posted_end) P.trace[(size_t)ia * TRACE_WORDS + 4] = globaltimer();
+    if (P.trace && !posted_end) P.trace[(size_t)i_in * TRACE_WORDS + 4] = globaltimer();
     ++islot_ctr;
     if (posted_end) break;
 
-    const Instr in = Ia;
-    const uint32_t i_in = ia;
-    ia = ib;
-    Ia = Ib;
-    ib = ic;
     const Src src = src_of(P, in, ext);
     bool stuck = false;
     uint64_t blocked_ns = 0;  // (tracing) time spent waiting for a free stage
@@ -356,6 +352,8 @@ struct Ring {
   uint64_t wait_ns;       // (tracing, thread 0) time spent waiting for stages
   uint64_t first_ns;      // (tracing, thread 0) when the instruction's first stage was ready
   uint64_t loop_ns;       // (tracing, thread 0) when a batch-1 GEMV tile was handed off
+  uint64_t cbar_ns;       // (tracing, thread 0) when the instruction reached every consumer warp
+  uint64_t hacq_ns;       // (tracing, thread 0) when the hand-off buffer was free
 };
 
 __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
@@ -519,74 +517,92 @@ __device__ __forceinline__ void handoff_commit(const Sh& S, Ring& R, int hb) {
 // Batch-1 GEMV tile: streams the tile's rows and leaves one partial sum per
 // (warp, row) in a hand-off buffer; the finisher warp adds them up, runs the
 // epilogue and releases the tile, so the consumers go straight on to the next
-// instruction.
+// instruction.  Software-pipelined by one stage: a stage's loads are issued,
+// then the warp reduction of the previous stage's row sums, then this stage's
+// FMAs, so the shuffle chain overlaps the shared-memory latency instead of
+// following it; the loop body stays small (one stage).
 template <int M>
 __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in,
                                           uint32_t ii, const GemvDesc& g, const Src& src, Ring& R,
                                           const float (&xr)[M][8]) {
-  // rows per 32 KB stage at K = M * 2048 (the plan's src.rps for these K)
-  constexpr int RPS = (8 / M) > 0 ? (8 / M) : 1;
-  constexpr int kDup = 32 / RPS;  // lanes holding the same total after the butterfly
+  constexpr int RPS = fast_rps(M);  // whole rows per 32 KB stage at K = M * 2048
+  constexpr int kDup = 32 / RPS;    // lanes holding the same total after the reduction
+  constexpr int NP = M > 1 ? M : 2;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int K = g.K;
   const int rows0 = (int)src.rows[0];
+  const int nst = ((rows0 + RPS - 1) / RPS) * src.nreg;
   const int hb = handoff_acquire(P, S, R);
+  if (P.trace && t == 0) R.hacq_ns = globaltimer();
   float* redw = S.redw + hb * NW * RMAX;
-  int tile_row = 0;
+  const int idx = warp_multi_index<RPS>(lane);
+  const bool writer = (lane & (kDup - 1)) == 0;
+  float prev[RPS];
+#pragma unroll
+  for (int i = 0; i < RPS; ++i) prev[i] = 0.f;
+  int prev_row = 0, prev_n = 0;  // tile row and row count of the sums in prev
+  int srow = 0, reg = 0;         // first row of the next stage in its region
 #pragma unroll 1
-  for (int r = 0; r < src.nreg; ++r) {
-#pragma unroll 1
-    for (int row = 0; row < rows0; row += RPS) {
-      const int n = rows0 - row < RPS ? rows0 - row : RPS;
-      const uint8_t* stage = ring_acquire(P, S, R);
-      float acc[RPS];
+  for (int s = 0; s < nst; ++s) {
+    const int n = rows0 - srow < RPS ? rows0 - srow : RPS;
+    const int st = R.ctr % NSTAGE;
+    const uint8_t* stage = ring_acquire(P, S, R);
+    uint4 wv[RPS][M];
 #pragma unroll
-      for (int i = 0; i < RPS; ++i) {
-        float a = 0.f;
-        if (i < n) {
-          // independent partial sums (one per 8-column group, two halves when
-          // there is one group), added pairwise in a fixed order: short FMA
-          // chains keep the 8 consumer warps issuing
-          const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)i * K * 2);
-          constexpr int NP = M > 1 ? M : 2;
-          float pa[NP];
-          if constexpr (M == 1) {
-            const uint4 wv = wrow[t];
-            pa[0] = fmaf(bf_hi(wv.y), xr[0][3], fmaf(bf_lo(wv.y), xr[0][2],
-                    fmaf(bf_hi(wv.x), xr[0][1], bf_lo(wv.x) * xr[0][0])));
-            pa[1] = fmaf(bf_hi(wv.w), xr[0][7], fmaf(bf_lo(wv.w), xr[0][6],
-                    fmaf(bf_hi(wv.z), xr[0][5], bf_lo(wv.z) * xr[0][4])));
-          } else {
+    for (int i = 0; i < RPS; ++i)
 #pragma unroll
-            for (int j = 0; j < M; ++j) pa[j] = dot8(wrow[t + NT * j], xr[j], 0.f);
-          }
-#pragma unroll
-          for (int step = 1; step < NP; step *= 2)
-#pragma unroll
-            for (int j = 0; j + step < NP; j += 2 * step) pa[j] += pa[j + step];
-          a = pa[0];
-        }
-        acc[i] = a;
-      }
-      ring_release(S, R);
-      if constexpr (RPS == 1) {
-        const float v = warp_sum(acc[0]);
-        if (lane == 0) redw[w * RMAX + tile_row] = v;
-      } else {
-        const float v = warp_reduce_multi<RPS>(acc, lane);
-        const int idx = warp_multi_index<RPS>(lane);
-        if ((lane & (kDup - 1)) == 0 && idx < n) redw[w * RMAX + tile_row + idx] = v;
-      }
-      tile_row += n;
+      for (int j = 0; j < M; ++j)
+        wv[i][j] = reinterpret_cast<const uint4*>(stage + (size_t)i * K * 2)[t + NT * j];
+    // the previous stage's sums while the loads are in flight
+    {
+      const float v = warp_reduce_multi<RPS>(prev, lane);
+      if (writer && idx < prev_n) redw[w * RMAX + prev_row + idx] = v;
     }
+#pragma unroll
+    for (int i = 0; i < RPS; ++i) {
+      // independent partial sums (one per 8-column group, two halves when
+      // there is one group), added pairwise in a fixed order.  Rows past the
+      // region's end read stale stage bytes into sums that are never stored.
+      float pa[NP];
+      if constexpr (M == 1) {
+        const uint4 q = wv[i][0];
+        pa[0] = fmaf(bf_hi(q.y), xr[0][3], fmaf(bf_lo(q.y), xr[0][2],
+                fmaf(bf_hi(q.x), xr[0][1], bf_lo(q.x) * xr[0][0])));
+        pa[1] = fmaf(bf_hi(q.w), xr[0][7], fmaf(bf_lo(q.w), xr[0][6],
+                fmaf(bf_hi(q.z), xr[0][5], bf_lo(q.z) * xr[0][4])));
+      } else {
+#pragma unroll
+        for (int j = 0; j < M; ++j) pa[j] = dot8(wv[i][j], xr[j], 0.f);
+      }
+#pragma unroll
+      for (int step = 1; step < NP; step *= 2)
+#pragma unroll
+        for (int j = 0; j + step < NP; j += 2 * step) pa[j] += pa[j + step];
+      prev[i] = pa[0];
+    }
+    __syncwarp();
+    mbar_arrive_if(&S.empty[st], lane == 0);
+    ++R.ctr;
+    prev_row = reg * rows0 + srow;
+    prev_n = n;
+    srow += RPS;
+    if (srow >= rows0) {
+      srow = 0;
+      ++reg;
+    }
+  }
+  {
+    const float v = warp_reduce_multi<RPS>(prev, lane);
+    if (writer && idx < prev_n) redw[w * RMAX + prev_row + idx] = v;
   }
   if (t == 0) {
     if (P.trace) R.loop_ns = globaltimer();
     *hrec_instr(S, hb) = in;
     *hrec_index(S, hb) = ii;
   }
-  (void)w;
+  if (P.trace && t == NT - 32) P.trace[(size_t)ii * TRACE_WORDS + 13] = globaltimer();
   handoff_commit(S, R, hb);
+  if (P.trace && t == 0) P.trace[(size_t)ii * TRACE_WORDS + 15] = globaltimer();
 }
 
 // ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
@@ -1025,7 +1041,7 @@ __device__ __forceinline__ void drain(const KParams& P, const Sh& S, const Instr
 template <int MH, int MF, int AD, int AREP>
 __device__ void consumer(const KParams& P, const Sh& S) {
   const int t = threadIdx.x;
-  Ring R{0, 0, 0, 0, 0};
+  Ring R{0, 0, 0, 0, 0, 0, 0};
   uint32_t islot_ctr = 0;
   const uint32_t gen = S.flags[F_GEN];
   constexpr int XH = MH > 0 ? MH : 1, XF = MF > 0 ? MF : 1;
@@ -1043,6 +1059,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     // finishes every batch-1 tile) already fills in the next instruction's.
     const int f_slot = (islot_ctr & 1u) ? F_SLOT_B : F_SLOT;
     const int f_abort = (islot_ctr & 1u) ? F_ABORT_B : F_ABORT;
+    const uint64_t t_top = (P.trace && t == 0) ? globaltimer() : 0;
     // one thread takes the slot (a bounded wait)
     if (t == 0) {
       uint32_t v = 0xffffffffu;
@@ -1090,6 +1107,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       if (P.trace) t_ready = globaltimer();
     }
     cbar();
+    if (P.trace && t == 0) R.cbar_ns = globaltimer();
     const uint32_t i = S.flags[f_slot];
     Instr in;
     AttnExt ext;
@@ -1161,11 +1179,17 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       if (!R.loop_ns) tr[3] = globaltimer();  // handed-off tiles: the finisher writes it
       tr[5] = R.wait_ns;
       tr[6] = R.first_ns;
-      if (in.op != OP_ATTN) tr[8] = R.loop_ns;
+      if (in.op != OP_ATTN) {
+        tr[8] = R.loop_ns;
+        tr[10] = R.cbar_ns;
+        tr[11] = R.hacq_ns;
+      }
+      tr[12] = t_top;
     }
     R.wait_ns = 0;
     R.first_ns = 0;
     R.loop_ns = 0;
+    R.hacq_ns = 0;
     // no barrier here: the next instruction's slot and dependency barriers
     // order every reuse of the shared scratch
   }
@@ -1200,6 +1224,7 @@ __device__ void finisher(const KParams& P, const Sh& S) {
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.hempty[hb]);
+    if (P.trace && lane == 0) P.trace[(size_t)ii * TRACE_WORDS + 14] = globaltimer();
     const float pre = epilogue_prefetch(P, in, g, lane);
     gemv_epilogue(P, S.fin, in, g, pre, lane);
     __syncwarp();

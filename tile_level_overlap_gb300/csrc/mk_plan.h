@@ -26,6 +26,8 @@ constexpr int XBUF_BYTES = 24576;     // activation / attention scratch in share
 constexpr int XBUF_FLOATS = XBUF_BYTES / 4;
 constexpr int SCORE_FLOATS = 4096;    // attention scores per split (all q heads of a group)
 constexpr int FAST_K_UNIT = 8 * NT;   // K must be a multiple of this for the batch-1 fast path
+// Batch-1 fast path at K = m * FAST_K_UNIT: whole weight rows per ring stage.
+MK_HD constexpr int fast_rps(int m) { return m >= 8 ? 1 : 8 / m; }
 
 constexpr int DEFAULT_SMS = 152;  // SMs of a GB300
 

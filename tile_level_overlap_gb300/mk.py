@@ -23,7 +23,7 @@ MK_ERR_UNSUPPORTED = 5
 MK_ERR_NO_DEVICE = 6
 MK_DECODE = 0
 MK_PREFILL = 1
-TRACE_WORDS = 12  # u64 words per trace record (mk_trace_copy)
+TRACE_WORDS = 16  # u64 words per trace record (mk_trace_copy)
 
 EXPORTED = [
     "mk_plan_create", "mk_plan_destroy", "mk_kv_cache_bytes", "mk_decode_step",
