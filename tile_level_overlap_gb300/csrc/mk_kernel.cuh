@@ -1045,10 +1045,12 @@ __device__ void consumer(const KParams& P, const Sh& S) {
   uint32_t islot_ctr = 0;
   const uint32_t gen = S.flags[F_GEN];
   constexpr int XH = MH > 0 ? MH : 1, XF = MF > 0 ? MF : 1;
-  // Normed activations stay in registers while consecutive tiles read the
-  // same vector (same operator and layer): the tag names what they hold.
-  float xh[XH][8], xf[XF][8];
-  uint32_t tag_h = 0xffffffffu, tag_f = 0xffffffffu;
+  constexpr int XM = XH > XF ? XH : XF;
+  // The activation vector stays in registers while consecutive tiles read it
+  // (same operator and layer): the tag names what it holds.  One array serves
+  // both widths (every operator change reloads it anyway).
+  float xr[XM][8];
+  uint32_t tag_x = 0xffffffffu;
   // Last barrier (and target) thread 0 saw satisfied: counters only grow
   // within a launch, so a repeat wait needs no new load.
   uint32_t ok_bar = NO_BAR, ok_target = 0;
@@ -1131,14 +1133,10 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       // register copies here makes them dead during the attention tile, so
       // attention does not have to spill around them.
 #pragma unroll
-      for (int j = 0; j < XH; ++j)
+      for (int j = 0; j < XM; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xh[j][e] = 0.f;
-#pragma unroll
-      for (int j = 0; j < XF; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xf[j][e] = 0.f;
-      tag_h = tag_f = 0xffffffffu;
+        for (int e = 0; e < 8; ++e) xr[j][e] = 0.f;
+      tag_x = 0xffffffffu;
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
@@ -1147,15 +1145,17 @@ __device__ void consumer(const KParams& P, const Sh& S) {
         if (P.B == 1) {
           const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8);
           if (in.op == OP_DOWN) {
-            if (tag != tag_f) {
+            auto& xf = *reinterpret_cast<float(*)[XF][8]>(&xr);
+            if (tag != tag_x) {
               load_x_fast<XF>(P, S, in, xf);
-              tag_f = tag;
+              tag_x = tag;
             }
             gemv_fast<XF>(P, S, in, i, g, src, R, xf);
           } else {
-            if (tag != tag_h) {
+            auto& xh = *reinterpret_cast<float(*)[XH][8]>(&xr);
+            if (tag != tag_x) {
               load_x_fast<XH>(P, S, in, xh);
-              tag_h = tag;
+              tag_x = tag;
             }
             gemv_fast<XH>(P, S, in, i, g, src, R, xh);
           }
