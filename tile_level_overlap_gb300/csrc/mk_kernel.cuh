@@ -346,15 +346,19 @@ __device__ void producer(const KParams& P, const Sh& S) {
 }
 
 // ---------------------------------------------------------------- consumer helpers
+// Tracing (thread 0 only) writes each timestamp into the instruction's record
+// when it is taken, so no timestamp stays live in registers across a tile.
 struct Ring {
-  uint32_t ctr;           // stages consumed so far
-  uint32_t hctr;          // batch-1 GEMV tiles handed to the finisher so far
-  uint64_t wait_ns;       // (tracing, thread 0) time spent waiting for stages
-  uint64_t first_ns;      // (tracing, thread 0) when the instruction's first stage was ready
-  uint64_t loop_ns;       // (tracing, thread 0) when a batch-1 GEMV tile was handed off
-  uint64_t cbar_ns;       // (tracing, thread 0) when the instruction reached every consumer warp
-  uint64_t hacq_ns;       // (tracing, thread 0) when the hand-off buffer was free
+  uint32_t ctr;      // stages consumed so far
+  uint32_t hctr;     // batch-1 GEMV tiles handed to the finisher so far
+  uint32_t cur;      // (tracing) queue index of the instruction being run
+  uint32_t wait_ns;  // (tracing) time spent waiting for stages in this instruction
+  bool first_done;   // (tracing) its first stage was recorded
+  bool handed;       // a batch-1 GEMV tile went to the finisher (which records "done")
 };
+__device__ __forceinline__ void trace_mark(const KParams& P, uint32_t ii, int word) {
+  P.trace[(size_t)ii * TRACE_WORDS + word] = globaltimer();
+}
 
 __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
   const int st = R.ctr % NSTAGE;
@@ -362,8 +366,11 @@ __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const S
     const uint64_t t0 = globaltimer();
     mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
     const uint64_t t1 = globaltimer();
-    R.wait_ns += t1 - t0;
-    if (!R.first_ns) R.first_ns = t1;
+    R.wait_ns += (uint32_t)(t1 - t0);
+    if (!R.first_done) {
+      P.trace[(size_t)R.cur * TRACE_WORDS + 6] = t1;
+      R.first_done = true;
+    }
   } else {
     mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
   }
@@ -473,6 +480,20 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
   }
 }
 
+// The down projection's input (the SwiGLU output: no norm, no gain, never the
+// embedding), loaded without the general form's gain registers.
+template <int M>
+__device__ __forceinline__ void load_x_plain(const float* xs, float (&xr)[M][8]) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    const float4* p = reinterpret_cast<const float4*>(xs + 8 * (t + NT * j));
+    const float4 u = __ldcg(p), v = __ldcg(p + 1);
+    xr[j][0] = u.x; xr[j][1] = u.y; xr[j][2] = u.z; xr[j][3] = u.w;
+    xr[j][4] = v.x; xr[j][5] = v.y; xr[j][6] = v.z; xr[j][7] = v.w;
+  }
+}
+
 // The residual input of an O / down tile output element (thread t owns output
 // (r, b) = (t / B, t % B)); loaded before the tile streams so that its latency
 // is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
@@ -533,7 +554,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   const int rows0 = (int)src.rows[0];
   const int nst = ((rows0 + RPS - 1) / RPS) * src.nreg;
   const int hb = handoff_acquire(P, S, R);
-  if (P.trace && t == 0) R.hacq_ns = globaltimer();
+  if (P.trace && t == 0) trace_mark(P, ii, 11);
   float* redw = S.redw + hb * NW * RMAX;
   const int idx = warp_multi_index<RPS>(lane);
   const bool writer = (lane & (kDup - 1)) == 0;
@@ -596,13 +617,14 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
     if (writer && idx < prev_n) redw[w * RMAX + prev_row + idx] = v;
   }
   if (t == 0) {
-    if (P.trace) R.loop_ns = globaltimer();
+    if (P.trace) trace_mark(P, ii, 8);
     *hrec_instr(S, hb) = in;
     *hrec_index(S, hb) = ii;
   }
-  if (P.trace && t == NT - 32) P.trace[(size_t)ii * TRACE_WORDS + 13] = globaltimer();
+  if (P.trace && t == NT - 32) trace_mark(P, ii, 13);
   handoff_commit(S, R, hb);
-  if (P.trace && t == 0) P.trace[(size_t)ii * TRACE_WORDS + 15] = globaltimer();
+  R.handed = true;
+  if (P.trace && t == 0) trace_mark(P, ii, 15);
 }
 
 // ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
@@ -1041,7 +1063,7 @@ __device__ __forceinline__ void drain(const KParams& P, const Sh& S, const Instr
 template <int MH, int MF, int AD, int AREP>
 __device__ void consumer(const KParams& P, const Sh& S) {
   const int t = threadIdx.x;
-  Ring R{0, 0, 0, 0, 0, 0, 0};
+  Ring R{0, 0, 0, 0, false, false};
   uint32_t islot_ctr = 0;
   const uint32_t gen = S.flags[F_GEN];
   constexpr int XH = MH > 0 ? MH : 1, XF = MF > 0 ? MF : 1;
@@ -1072,11 +1094,10 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     // read only while spinning: a launch that never waits on an unsatisfied
     // counter runs to completion anyway); one consumer barrier then hands the
     // slot and the verdict to every consumer thread.
-    uint64_t t_begin = 0, t_ready = 0;
     if (t == 0) {
       const uint32_t iv = S.flags[f_slot];
       uint32_t aborted = S.flags[F_STOP];
-      if (P.trace) t_begin = globaltimer();
+      const uint64_t t_begin = P.trace ? globaltimer() : 0;
       if (iv != END_SLOT) {
         const Instr& in0 = *slot_instr(S, si);
         if (!aborted && P.mode == MODE_MEGA && in0.wait_bar != NO_BAR) {
@@ -1106,10 +1127,16 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       }
       S.flags[f_abort] = aborted;
       if (aborted) S.flags[F_STOP] = 1u;  // the producer stops popping
-      if (P.trace) t_ready = globaltimer();
+      if (P.trace && iv != END_SLOT) {
+        unsigned long long* tr = P.trace + (size_t)iv * TRACE_WORDS;
+        tr[12] = t_top;
+        tr[1] = t_begin;
+        tr[2] = globaltimer();
+        R.cur = iv;
+      }
     }
     cbar();
-    if (P.trace && t == 0) R.cbar_ns = globaltimer();
+    if (P.trace && t == 0 && S.flags[f_slot] != END_SLOT) trace_mark(P, R.cur, 10);
     const uint32_t i = S.flags[f_slot];
     Instr in;
     AttnExt ext;
@@ -1147,7 +1174,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
           if (in.op == OP_DOWN) {
             auto& xf = *reinterpret_cast<float(*)[XF][8]>(&xr);
             if (tag != tag_x) {
-              load_x_fast<XF>(P, S, in, xf);
+              load_x_plain<XF>(gemv_x(P, in), xf);
               tag_x = tag;
             }
             gemv_fast<XF>(P, S, in, i, g, src, R, xf);
@@ -1174,22 +1201,12 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     if (P.trace && t == 0) {
       unsigned long long* tr = P.trace + (size_t)i * TRACE_WORDS;
       tr[0] = (unsigned long long)smid() | ((unsigned long long)(in.op | (in.layer << 8)) << 32);
-      tr[1] = t_begin;
-      tr[2] = t_ready;
-      if (!R.loop_ns) tr[3] = globaltimer();  // handed-off tiles: the finisher writes it
+      if (!R.handed) tr[3] = globaltimer();  // handed-off tiles: the finisher writes it
       tr[5] = R.wait_ns;
-      tr[6] = R.first_ns;
-      if (in.op != OP_ATTN) {
-        tr[8] = R.loop_ns;
-        tr[10] = R.cbar_ns;
-        tr[11] = R.hacq_ns;
-      }
-      tr[12] = t_top;
     }
     R.wait_ns = 0;
-    R.first_ns = 0;
-    R.loop_ns = 0;
-    R.hacq_ns = 0;
+    R.first_done = false;
+    R.handed = false;
     // no barrier here: the next instruction's slot and dependency barriers
     // order every reuse of the shared scratch
   }
