@@ -957,7 +957,7 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
       // CB splits at a time, every load of a batch in flight together; the
       // first batch goes out with the (max, sum) loads.
       constexpr int NO = (REP * D + NT - 1) / NT;
-      constexpr int CB = NO <= 2 ? 10 : 4;
+      constexpr int CB = NO <= 1 ? 32 : NO <= 2 ? 20 : 8;
       float v[NO][CB];
 #pragma unroll
       for (int k = 0; k < NO; ++k) {
@@ -1154,7 +1154,29 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       drain(P, S, in, R);
       continue;
     }
-    if (in.op == OP_ATTN) {
+    // The batch-1 GEMV tiles (most instructions) come first in the code, so
+    // their dispatch path stays short and contiguous; the finisher stores and
+    // releases them.
+    if (MH > 0 && P.B == 1 && in.op != OP_ATTN) {
+      const GemvDesc g = gemv_desc(P, in);
+      const Src src = instr_src(P, in);
+      const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8);
+      if (in.op != OP_DOWN) {
+        auto& xh = *reinterpret_cast<float(*)[XH][8]>(&xr);
+        if (tag != tag_x) {
+          load_x_fast<XH>(P, S, in, xh);
+          tag_x = tag;
+        }
+        gemv_fast<XH>(P, S, in, i, g, src, R, xh);
+      } else {
+        auto& xf = *reinterpret_cast<float(*)[XF][8]>(&xr);
+        if (tag != tag_x) {
+          load_x_plain<XF>(gemv_x(P, in), xf);
+          tag_x = tag;
+        }
+        gemv_fast<XF>(P, S, in, i, g, src, R, xf);
+      }
+    } else if (in.op == OP_ATTN) {
       attn_dispatch<AD, AREP>(P, S, in, ext, i, R);
       // Every GEMV after attention reloads its activations; overwriting the
       // register copies here makes them dead during the attention tile, so
@@ -1167,36 +1189,12 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      bool done = false;
-      if constexpr (MH > 0) {
-        if (P.B == 1) {
-          const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8);
-          if (in.op == OP_DOWN) {
-            auto& xf = *reinterpret_cast<float(*)[XF][8]>(&xr);
-            if (tag != tag_x) {
-              load_x_plain<XF>(gemv_x(P, in), xf);
-              tag_x = tag;
-            }
-            gemv_fast<XF>(P, S, in, i, g, src, R, xf);
-          } else {
-            auto& xh = *reinterpret_cast<float(*)[XH][8]>(&xr);
-            if (tag != tag_x) {
-              load_x_fast<XH>(P, S, in, xh);
-              tag_x = tag;
-            }
-            gemv_fast<XH>(P, S, in, i, g, src, R, xh);
-          }
-          done = true;  // the finisher stores and releases it
-        }
-      }
-      if (!done) {
-        const float pre = epilogue_prefetch(P, in, g, t);
-        gemv_generic(P, S, in, g, src, R);
-        gemv_epilogue(P, S.red, in, g, pre, t);
-        cbar();
-        if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
-          red_release_gpu_add(&P.bars[in.rel_bar], 1u);
-      }
+      const float pre = epilogue_prefetch(P, in, g, t);
+      gemv_generic(P, S, in, g, src, R);
+      gemv_epilogue(P, S.red, in, g, pre, t);
+      cbar();
+      if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
+        red_release_gpu_add(&P.bars[in.rel_bar], 1u);
     }
     if (P.trace && t == 0) {
       unsigned long long* tr = P.trace + (size_t)i * TRACE_WORDS;
