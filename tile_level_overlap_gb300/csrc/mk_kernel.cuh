@@ -37,7 +37,8 @@ struct SmemLayout {
   static constexpr int xbuf = ring + NSTAGE * STAGE_BYTES;
   static constexpr int red = xbuf + XBUF_BYTES;            // [RMAX][BMAX_CC] floats
   static constexpr int redw = red + RMAX * BMAX_CC * 4;    // [2][NW][RMAX] floats (hand-off buffers)
-  static constexpr int fin = redw + 2 * NW * RMAX * 4;     // [RMAX][BMAX_CC] floats (finisher)
+  static constexpr int hpre = redw + 2 * NW * RMAX * 4;    // [2][RMAX] floats (hand-off residual inputs)
+  static constexpr int fin = hpre + 2 * RMAX * 4;          // [RMAX][BMAX_CC] floats (finisher)
   static constexpr int ssw = fin + RMAX * BMAX_CC * 4;     // [NW][BMAX_CC] floats
   static constexpr int bars = ssw + NW * BMAX_CC * 4;      // mbarriers
   // full, empty [NSTAGE]; ifull, iempty [NISLOT]; hfull, hempty [2]
@@ -60,6 +61,7 @@ struct Sh {
   float* xbuf;
   float* red;
   float* redw;
+  float* hpre;
   float* fin;
   float* ssw;
   uint64_t* full;
@@ -87,6 +89,7 @@ __device__ __forceinline__ Sh sh_map(uint8_t* base) {
   s.xbuf = reinterpret_cast<float*>(base + SmemLayout::xbuf);
   s.red = reinterpret_cast<float*>(base + SmemLayout::red);
   s.redw = reinterpret_cast<float*>(base + SmemLayout::redw);
+  s.hpre = reinterpret_cast<float*>(base + SmemLayout::hpre);
   s.fin = reinterpret_cast<float*>(base + SmemLayout::fin);
   s.ssw = reinterpret_cast<float*>(base + SmemLayout::ssw);
   uint64_t* b = reinterpret_cast<uint64_t*>(base + SmemLayout::bars);
@@ -555,6 +558,9 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   const int nst = ((rows0 + RPS - 1) / RPS) * src.nreg;
   const int hb = handoff_acquire(P, S, R);
   if (P.trace && t == 0) trace_mark(P, ii, 11);
+  // the residual input of the tile's outputs (O, down), loaded now so that its
+  // latency hides behind the stages; the finisher takes it from the hand-off
+  const float pre = epilogue_prefetch(P, in, g, t);
   float* redw = S.redw + hb * NW * RMAX;
   const int idx = warp_multi_index<RPS>(lane);
   const bool writer = (lane & (kDup - 1)) == 0;
@@ -616,6 +622,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
     const float v = warp_reduce_multi<RPS>(prev, lane);
     if (writer && idx < prev_n) redw[w * RMAX + prev_row + idx] = v;
   }
+  if (t < RMAX) S.hpre[hb * RMAX + t] = pre;
   if (t == 0) {
     if (P.trace) trace_mark(P, ii, 8);
     *hrec_instr(S, hb) = in;
@@ -1237,10 +1244,10 @@ __device__ void finisher(const KParams& P, const Sh& S) {
       for (int k = 0; k < NW; ++k) s += redw[k * RMAX + lane];
       S.fin[lane * BMAX_CC] = s;
     }
+    const float pre = S.hpre[hb * RMAX + lane];
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.hempty[hb]);
     if (P.trace && lane == 0) P.trace[(size_t)ii * TRACE_WORDS + 14] = globaltimer();
-    const float pre = epilogue_prefetch(P, in, g, lane);
     gemv_epilogue(P, S.fin, in, g, pre, lane);
     __syncwarp();
     if (lane == 0) {
