@@ -251,9 +251,9 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
   const uint32_t gen = S.flags[BF_GEN];
   uint32_t stage_ctr = 0, islot_ctr = 0;
   uint32_t npop = 0;
-  // Pops run one instruction ahead of the one being streamed, so the latency
-  // of the queue atomic and of the record load overlaps the current
-  // instruction's copies.  Pop order is still this CTA's execution order.
+  // An instruction is popped only once a ring stage is free, i.e. when this
+  // CTA can start streaming it: a CTA whose current tile waits on a
+  // dependency does not also claim the next tile ahead of CTAs that are free.
   auto pop = [&]() -> uint32_t {
     const uint32_t k = npop++;
     if (P.mode == MODE_MEGA) {
@@ -263,19 +263,14 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
     }
     return k == 0 ? P.perop_base + blockIdx.x : BD_END;
   };
-  uint32_t inext = pop();
-  Instr Inext;
-  if (inext != BD_END) Inext = P.queue[inext];
   // last counter (and target) seen satisfied: counters only grow within a
   // launch, so repeated waits on it need no new load
   uint32_t ok_bar = NO_BAR, ok_target = 0;
   for (;;) {
-    const uint32_t i = inext;
-    const Instr in = Inext;
-    if (i != BD_END) {
-      inext = pop();
-      if (inext != BD_END) Inext = P.queue[inext];
-    }
+    const bool room = bd_wait(P, &S.empty[stage_ctr % BD_NSTAGE], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
+    const uint32_t i = room ? pop() : BD_END;
+    Instr in;
+    if (i != BD_END) in = P.queue[i];
     const int si = islot_ctr % NISLOT;
     bool end = i == BD_END;
     if (!bd_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) end = true;
