@@ -83,6 +83,14 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
   }
 
   std::vector<Instr>& q = pp.queue;
+  // GEMM tiles go group by group of PF_BLOCK_GROUP token blocks, and within a
+  // group weight tile by weight tile, so the blocks of a group read each
+  // weight tile from L2 right after the first of them brought it in.
+  auto grouped = [&](uint32_t nn, auto&& emit) {
+    for (int mg = 0; mg < NB; mg += PF_BLOCK_GROUP)
+      for (uint32_t n = 0; n < nn; ++n)
+        for (int m = mg; m < NB && m < mg + PF_BLOCK_GROUP; ++m) emit(m, n);
+  };
   auto begin = [&]() { return (uint32_t)q.size(); };
   auto end = [&](uint32_t s) {
     if (q.size() > s) pp.perop.push_back({s, (uint32_t)q.size() - s});
@@ -102,16 +110,15 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
     }
     end(s);
     s = begin();
-    for (int m = 0; m < NB; ++m)
-      for (uint32_t n = 0; n < pp.n_qkv_n; ++n) {
-        Instr in = pf_make(PF_QKV, l, m, n);
-        in.wait_bar = bar(b.norm1, l, m);
-        in.wait_target = 1;
-        in.wait_n = 1;
-        in.wait_stride = 1;
-        in.rel_bar = bar(b.qkv, l, m);
-        q.push_back(in);
-      }
+    grouped(pp.n_qkv_n, [&](int m, uint32_t n) {
+      Instr in = pf_make(PF_QKV, l, m, n);
+      in.wait_bar = bar(b.norm1, l, m);
+      in.wait_target = 1;
+      in.wait_n = 1;
+      in.wait_stride = 1;
+      in.rel_bar = bar(b.qkv, l, m);
+      q.push_back(in);
+    });
     end(s);
     s = begin();
     for (int m = 0; m < NB; ++m)
@@ -126,16 +133,15 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
       }
     end(s);
     s = begin();
-    for (int m = 0; m < NB; ++m)
-      for (uint32_t n = 0; n < pp.n_o_n; ++n) {
-        Instr in = pf_make(PF_O, l, m, n);
-        in.wait_bar = bar(b.attn, l, m);
-        in.wait_target = (uint32_t)nkv;
-        in.wait_n = 1;
-        in.wait_stride = 1;
-        in.rel_bar = bar(b.o, l, m);
-        q.push_back(in);
-      }
+    grouped(pp.n_o_n, [&](int m, uint32_t n) {
+      Instr in = pf_make(PF_O, l, m, n);
+      in.wait_bar = bar(b.attn, l, m);
+      in.wait_target = (uint32_t)nkv;
+      in.wait_n = 1;
+      in.wait_stride = 1;
+      in.rel_bar = bar(b.o, l, m);
+      q.push_back(in);
+    });
     end(s);
     s = begin();
     for (int m = 0; m < NB; ++m) {
@@ -149,28 +155,26 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
     }
     end(s);
     s = begin();
-    for (int m = 0; m < NB; ++m)
-      for (uint32_t n = 0; n < pp.n_gu_n; ++n) {
-        Instr in = pf_make(PF_GU, l, m, n);
-        in.wait_bar = bar(b.norm2, l, m);
-        in.wait_target = 1;
-        in.wait_n = 1;
-        in.wait_stride = 1;
-        in.rel_bar = bar(b.gu, l, m);
-        q.push_back(in);
-      }
+    grouped(pp.n_gu_n, [&](int m, uint32_t n) {
+      Instr in = pf_make(PF_GU, l, m, n);
+      in.wait_bar = bar(b.norm2, l, m);
+      in.wait_target = 1;
+      in.wait_n = 1;
+      in.wait_stride = 1;
+      in.rel_bar = bar(b.gu, l, m);
+      q.push_back(in);
+    });
     end(s);
     s = begin();
-    for (int m = 0; m < NB; ++m)
-      for (uint32_t n = 0; n < pp.n_down_n; ++n) {
-        Instr in = pf_make(PF_DOWN, l, m, n);
-        in.wait_bar = bar(b.gu, l, m);
-        in.wait_target = pp.n_gu_n;
-        in.wait_n = 1;
-        in.wait_stride = 1;
-        in.rel_bar = bar(b.down, l, m);
-        q.push_back(in);
-      }
+    grouped(pp.n_down_n, [&](int m, uint32_t n) {
+      Instr in = pf_make(PF_DOWN, l, m, n);
+      in.wait_bar = bar(b.gu, l, m);
+      in.wait_target = pp.n_gu_n;
+      in.wait_n = 1;
+      in.wait_stride = 1;
+      in.rel_bar = bar(b.down, l, m);
+      q.push_back(in);
+    });
     end(s);
   }
   return MK_OK;
