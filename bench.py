@@ -365,6 +365,18 @@ def run_ours(args):
                   "tokens_per_s_graph": BATCH / (ms_graph / 1e3),
                   "launches_per_step": plan.stats().n_launches_per_op_decode,
                   "speedup_persistent_vs_graph": ms_graph / ms}
+        # mixed composition: persistent layers, then the LM head as its own
+        # kernel-per-operator launch ("One Megakernel is Not Enough")
+        plan.set_lm_mode(mk.MK_LM_SEPARATE)
+        for _ in range(max(1, args.warmup // 2)):
+            mega()
+        ms_mixed = timed(mega, args.steps) / args.steps
+        plan.set_lm_mode(mk.MK_LM_FUSED)
+        rc = plan.status(stream)
+        if rc != mk.MK_OK:
+            raise RuntimeError(f"device status {rc}")
+        per_op["ms_per_step_lm_separate"] = ms_mixed
+        per_op["speedup_fused_vs_lm_separate"] = ms_mixed / ms
 
     # end to end through the host-buffer entry point: pinned host tokens and
     # positions in, logits out, every step

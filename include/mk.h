@@ -192,6 +192,19 @@ int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
 int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
                   mk_plan_stats *out);
 
+/* Composition of the decode step ("One Megakernel is Not Enough", Abstract:
+ * one megakernel is not always the fastest; Lecture 112 summary, Practical
+ * implications: the LM head may stay a separate operator).
+ * MK_LM_FUSED (default): one persistent launch runs every tile of the step,
+ * the LM head included.  MK_LM_SEPARATE: the persistent launch runs the
+ * layers, then the LM-head tiles run as one kernel-per-operator launch on the
+ * same stream (stream order replaces their counter waits).  Results are
+ * bit-identical in both modes.  Applies to mk_decode_step and
+ * mk_decode_step_host calls made after it; returns MK_ERR_INVALID_ARG for a
+ * null plan or an unknown mode. */
+enum { MK_LM_FUSED = 0, MK_LM_SEPARATE = 1 };
+int mk_plan_set_lm_mode(mk_plan *plan, int mode);
+
 /* Test and measurement options.  force_ctas > 0 launches that many persistent
  * CTAs (<= the co-resident limit); queue_perm_seed != 0 rebuilds the decode
  * queue in a seeded random topological order; trace = 1 records one 128-byte

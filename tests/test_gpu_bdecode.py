@@ -140,6 +140,11 @@ def test_small_bit_identical_runs_ctas_orders_and_per_op(small):
         small.plan.set_debug()
     np.testing.assert_array_equal(small.step(tokens, positions, per_op=True), ref)
     np.testing.assert_array_equal(small.step(tokens, positions, per_op=True, graph=True), ref)
+    try:
+        small.plan.set_lm_mode(mk.MK_LM_SEPARATE)
+        np.testing.assert_array_equal(small.step(tokens, positions), ref)
+    finally:
+        small.plan.set_lm_mode(mk.MK_LM_FUSED)
 
 
 def test_head_dim_128_qk_norm_batched():

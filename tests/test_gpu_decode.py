@@ -116,6 +116,24 @@ def test_toy_per_op_and_graph_bit_identical(toy):
     np.testing.assert_array_equal(toy.step(tokens, pos), mega)
 
 
+def test_toy_lm_separate_bit_identical(toy):
+    """The LM head as its own kernel-per-operator launch after the persistent
+    layers gives the same logits as the all-in-one step."""
+    tokens, pos = [21, 22, 23], [64, 1, 120]
+    fused = toy.step(tokens, pos)
+    try:
+        toy.plan.set_lm_mode(mk.MK_LM_SEPARATE)
+        np.testing.assert_array_equal(toy.step(tokens, pos), fused)
+        toy.plan.set_debug(queue_perm_seed=5)
+        np.testing.assert_array_equal(toy.step(tokens, pos), fused)
+    finally:
+        toy.plan.set_lm_mode(mk.MK_LM_FUSED)
+        toy.plan.set_debug()
+    np.testing.assert_array_equal(toy.step(tokens, pos), fused)
+    with pytest.raises(mk.MkError):
+        toy.plan.set_lm_mode(7)
+
+
 def test_toy_cta_counts_and_queue_orders(toy):
     tokens, pos = [3, 4], [128, 9]
     ref = toy.step(tokens, pos)
@@ -200,6 +218,8 @@ def test_llama32_1b_decode_full_size():
         ref, _, _ = m.oracle(tokens, [1024])
         _assert_rows_close(got, ref)
         np.testing.assert_array_equal(m.step(tokens, [1024], per_op=True), got)
+        m.plan.set_lm_mode(mk.MK_LM_SEPARATE)
+        np.testing.assert_array_equal(m.step(tokens, [1024]), got)
     finally:
         m.close()
 

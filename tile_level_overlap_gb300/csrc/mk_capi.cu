@@ -68,6 +68,7 @@ struct mk_plan {
   uint32_t* d_ctl = nullptr;
   KParams base{};
   int force_ctas = 0, trace = 0;
+  int lm_separate = 0;  // MK_LM_SEPARATE: the LM head runs as its own kernel-per-op launch
   uint64_t wait_limit_ns = 2000000000ull;
   cudaStream_t cap_stream = nullptr;
   cudaGraphExec_t graph = nullptr;
@@ -549,13 +550,37 @@ int mk_decode_step(mk_plan* p, const int32_t* tokens, const int32_t* positions, 
   int rc = check_step(p, tokens, positions, batch, kv, logits);
   if (rc != MK_OK) return rc;
   const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
+  cudaStream_t st = (cudaStream_t)stream;
+  // MK_LM_SEPARATE: the persistent launch stops before the LM-head tiles (the
+  // last instructions of every topological order: each waits on all of the
+  // last down projection), which then run as one kernel-per-operator launch.
   if (p->bd.on) {
-    if ((rc = bd_bind_kv(p, kv, (cudaStream_t)stream)) != MK_OK) return rc;
-    return cuda_err(bd_launch_mega(bd_params(p, tokens, positions, batch, kv, logits), ctas,
-                                   (cudaStream_t)stream));
+    if ((rc = bd_bind_kv(p, kv, st)) != MK_OK) return rc;
+    BdParams k = bd_params(p, tokens, positions, batch, kv, logits);
+    if (!p->lm_separate) return cuda_err(bd_launch_mega(k, ctas, st));
+    const auto& r = p->bd.bp.perop.back();  // the LM-head tiles
+    k.n_instr -= r.second;
+    MK_CUDA(bd_launch_mega(k, ctas, st));
+    k.n_instr += r.second;
+    k.queue = p->bd.d_queue;  // per-operator ranges index the default order
+    k.trace = nullptr;
+    return cuda_err(bd_launch_perop(k, r.first, r.second, st));
   }
   KParams k = step_params(p, tokens, positions, batch, kv, logits);
-  return cuda_err(p->kv.mega(k, ctas, (cudaStream_t)stream));
+  if (!p->lm_separate) return cuda_err(p->kv.mega(k, ctas, st));
+  const auto& r = p->hp.perop_decode.back();  // the LM-head tiles
+  k.n_instr -= r.second;
+  MK_CUDA(p->kv.mega(k, ctas, st));
+  k.n_instr += r.second;
+  k.queue = p->d_queue;
+  k.trace = nullptr;
+  return cuda_err(p->kv.perop(k, r.first, r.second, st));
+}
+
+int mk_plan_set_lm_mode(mk_plan* p, int mode) {
+  if (!p || (mode != MK_LM_FUSED && mode != MK_LM_SEPARATE)) return MK_ERR_INVALID_ARG;
+  p->lm_separate = mode == MK_LM_SEPARATE;
+  return MK_OK;
 }
 
 int mk_decode_step_host(mk_plan* p, const int32_t* tokens_host, const int32_t* positions_host,

@@ -23,6 +23,7 @@ MK_ERR_UNSUPPORTED = 5
 MK_ERR_NO_DEVICE = 6
 MK_DECODE = 0
 MK_PREFILL = 1
+MK_LM_FUSED, MK_LM_SEPARATE = 0, 1
 TRACE_WORDS = 16  # u64 words per trace record (mk_trace_copy)
 
 EXPORTED = [
@@ -30,6 +31,7 @@ EXPORTED = [
     "mk_decode_step_host", "mk_prefill", "mk_run_per_op", "mk_status", "mk_plan_reset",
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
+    "mk_plan_set_lm_mode",
 ]
 
 
@@ -88,6 +90,7 @@ def lib() -> ctypes.CDLL:
     L.mk_plan_check.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.c_int, ctypes.c_int,
                                 ctypes.c_uint64, ctypes.POINTER(mk_plan_stats)]
     L.mk_plan_set_debug.argtypes = [vp, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64]
+    L.mk_plan_set_lm_mode.argtypes = [vp, ctypes.c_int]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
     L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -247,6 +250,11 @@ class Plan:
                   wait_limit_ns: int = 0) -> None:
         _check(lib().mk_plan_set_debug(self.h, force_ctas, queue_perm_seed, int(trace), wait_limit_ns),
                "mk_plan_set_debug")
+
+    def set_lm_mode(self, mode: int) -> None:
+        """MK_LM_FUSED: the LM head inside the persistent step; MK_LM_SEPARATE:
+        the layers persistent, then the LM head as a kernel-per-operator launch."""
+        _check(lib().mk_plan_set_lm_mode(self.h, mode), "mk_plan_set_lm_mode")
 
     def debug_drop_release(self, index: int) -> None:
         _check(lib().mk_plan_debug_drop_release(self.h, index), "mk_plan_debug_drop_release")
