@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "decode tokens/s and HBM GB/s (% of ~8 TB/s), Llama-3-8B shape, batch 1, 1xGB300"
 UNIT = "tokens/s"
 PREFILL_TOKENS = 2048
+MULTI_STEPS = 8  # tokens per launch of the multi-step greedy decode leg
 # name -> (shape in synth, batch, largest cached context, smallest (ragged
 # contexts U[lo, ctx], seeded) or None (all at ctx), metric, description,
 # traffic key)
@@ -407,6 +408,36 @@ def run_ours(args):
         n_ctas = plan.stats().n_ctas
         dep_wait = float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span) if span > 0 else None
 
+    # greedy decode of MULTI_STEPS tokens per launch (mk_decode_steps, batch
+    # 1): positions CONTEXT - MULTI_STEPS .. CONTEXT - 1 so the steps fit the
+    # cache; tokens chosen on the device, the host out of the loop
+    multi = None
+    if BATCH == 1 and CONTEXT > MULTI_STEPS:
+        p0 = torch.tensor([CONTEXT - MULTI_STEPS], dtype=torch.int32, device=dev)
+        out_tok = torch.empty(MULTI_STEPS, dtype=torch.int32, device=dev)
+        lg1 = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+
+        def multi_step():
+            plan.decode_steps(tokens, p0, MULTI_STEPS, kv, out_tok, lg1, stream=stream)
+
+        try:
+            multi_step()
+        except mk.MkError as e:
+            if e.code != mk.MK_ERR_UNSUPPORTED:
+                raise
+        else:
+            for _ in range(max(1, args.warmup // 2)):
+                multi_step()
+            launches = max(1, args.steps // MULTI_STEPS)
+            ms_launch = timed(multi_step, launches) / launches
+            rc = plan.status(stream)
+            if rc != mk.MK_OK:
+                raise RuntimeError(f"device status {rc}")
+            multi = {"steps_per_launch": MULTI_STEPS, "launches": launches,
+                     "ms_per_token": ms_launch / MULTI_STEPS,
+                     "tokens_per_s": MULTI_STEPS / (ms_launch / 1e3),
+                     "positions": [CONTEXT - MULTI_STEPS, CONTEXT - 1]}
+
     # prefill of a 2048-token prompt into sequence slot 0 (after the decode
     # timing, since it rewrites that cache slot)
     prefill = None
@@ -468,6 +499,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": 4 * BATCH * cfg.vocab + 4},
         "gpu_launches": args.steps,
         "prefill": prefill,
+        "multi_step": multi,
     }
     if world == 1 and not args.no_cpu_baseline:
         sample_run = OracleSample(cfg, args.ref_layers, pos_list)

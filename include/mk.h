@@ -192,6 +192,28 @@ int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
 int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
                   mk_plan_stats *out);
 
+/* Greedy decode of n_steps tokens of one sequence in ONE persistent launch
+ * (the host stays out of the loop: "Lecture 112" summary, Practical
+ * implications).  Step s (0 <= s < n_steps) is the decode step of
+ * mk_decode_step at position position[0] + s; step 0 reads token[0], every
+ * later step the token the previous step chose: the index of the largest
+ * logit (the smallest index among equal logits), computed on the device from
+ * the LM-head tiles as they finish.  The queue runs n_steps times with barrier
+ * generations per step; the layer-0 projection of step s + 1 waits on every
+ * LM-head tile of step s.
+ *   token       device int32 [1]      first input token
+ *   position    device int32 [1]      tokens already cached (index of token)
+ *   n_steps     1 .. 64               position[0] + n_steps <= max_ctx, else
+ *                                     MK_ERR_BOUNDS is latched
+ *   out_tokens  device int32 [n_steps] out_tokens[s] = the token step s chose
+ *   logits      device float [V]      the last step's logits
+ * Cache slots position[0] .. position[0] + n_steps - 1 are written.  Batch-1
+ * plans of the CUDA-core path with the batch-1 register kernel only (other
+ * plans: MK_ERR_UNSUPPORTED); the caller's buffers follow mk_decode_step's
+ * rules.  Asynchronous on `stream`. */
+int mk_decode_steps(mk_plan *plan, const int32_t *token, const int32_t *position, int n_steps,
+                    void *kv_cache, int32_t *out_tokens, float *logits, void *stream);
+
 /* Composition of the decode step ("One Megakernel is Not Enough", Abstract:
  * one megakernel is not always the fastest; Lecture 112 summary, Practical
  * implications: the LM head may stay a separate operator).

@@ -237,3 +237,60 @@ def test_llama3_8b_decode_full_size():
         np.testing.assert_array_equal(m.step(tokens, [4096]), got)
     finally:
         m.close()
+
+
+def test_multi_step_greedy_decode():
+    """mk_decode_steps: n greedy steps in one launch equal n single steps fed
+    the argmax of each step's logits (same tile arithmetic: bit-identical
+    logits and cache); each chosen token is a maximum of the oracle's logits
+    for that step within the tolerance (teacher-forced with the chosen tokens),
+    and the last step's logits match the oracle's."""
+    cfg = synth.LLAMA32_1B.replace(n_layers=2)
+    n, pos0 = 5, 250
+    m = Model(cfg, 1, 300, seed=6)
+    try:
+        kv0 = m.kv.clone()
+        tok0 = synth.make_tokens(1, cfg.vocab, seed=31)
+        t = tok0.to(m.dev)
+        p = torch.tensor([pos0], dtype=torch.int32, device=m.dev)
+        out = torch.full((n,), -1, dtype=torch.int32, device=m.dev)
+        lg = torch.full((cfg.vocab,), float("nan"), device=m.dev)
+        m.plan.decode_steps(t, p, n, m.kv, out, lg)
+        assert m.plan.status() == mk.MK_OK
+        chosen = out.cpu().numpy()
+        multi_logits = lg.cpu().numpy()
+        kv_multi = m.kv.clone()
+        # the same steps one launch each, the argmax taken on the host
+        m.kv.copy_(kv0)
+        tok = int(tok0[0])
+        ref_tokens = []
+        for s in range(n):
+            got = m.step([tok], [pos0 + s])[0]
+            tok = int(np.argmax(got))  # first index among equal maxima
+            ref_tokens.append(tok)
+        np.testing.assert_array_equal(chosen, np.array(ref_tokens, dtype=np.int32))
+        np.testing.assert_array_equal(multi_logits, got)
+        assert torch.equal(m.kv, kv_multi)
+        # oracle, teacher-forced with the chosen tokens, its own cache appends
+        kvb = synth.bf16_bits(kv0)
+        w = synth.LazyBits(m.w)
+        tok = int(tok0[0])
+        for s in range(n):
+            ref, knew, vnew = oracle.decode_step(cfg, w, [tok], [pos0 + s], kvb)
+            row = ref[0]
+            rms = np.sqrt((row ** 2).mean())
+            assert row[chosen[s]] >= row.max() - 2 * TOL * rms, f"step {s}: token {chosen[s]} is not a maximum"
+            kb = torch.from_numpy(np.ascontiguousarray(knew[:, 0])).to(torch.bfloat16).view(torch.int16).numpy()
+            vb = torch.from_numpy(np.ascontiguousarray(vnew[:, 0])).to(torch.bfloat16).view(torch.int16).numpy()
+            kvb[:, 0, 0, :, pos0 + s, :] = kb.view(kvb.dtype)
+            kvb[:, 1, 0, :, pos0 + s, :] = vb.view(kvb.dtype)
+            tok = int(chosen[s])
+        _assert_rows_close(multi_logits[None, :], ref[None, :])
+        # past the end of the cache: latched bounds error, nothing else
+        m.plan.reset()
+        p2 = torch.tensor([300 - 2], dtype=torch.int32, device=m.dev)
+        m.plan.decode_steps(t, p2, 3, m.kv, out, lg)
+        assert m.plan.status() == mk.MK_ERR_BOUNDS
+        m.plan.reset()
+    finally:
+        m.close()

@@ -66,6 +66,7 @@ struct mk_plan {
   int32_t* d_pos = nullptr;
   float* d_logits = nullptr;
   uint32_t* d_ctl = nullptr;
+  uint8_t* d_msteps = nullptr;  // multi-step decode words (16 bytes per step)
   KParams base{};
   int force_ctas = 0, trace = 0;
   int lm_separate = 0;  // MK_LM_SEPARATE: the LM head runs as its own kernel-per-op launch
@@ -414,6 +415,9 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   const size_t o_tok = bm.take(sizeof(int32_t) * max_batch);
   const size_t o_pos = bm.take(sizeof(int32_t) * max_batch);
   const size_t o_log = bm.take(sizeof(float) * max_batch * c.vocab);
+  // multi-step decode: per step the packed maximum (u64), the finished LM
+  // tiles and the chosen token, cleared together before each such launch
+  const size_t o_msteps = bm.take(16 * MAX_DECODE_STEPS);
   p->scratch_bytes = bm.off;
   if (cudaMalloc(&p->scratch, p->scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -472,6 +476,8 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   k.ctl = p->d_ctl;
   k.queue = p->d_queue_mk;
   k.n_instr = (uint32_t)hp.decode.size();
+  k.n_steps = 1;
+  p->d_msteps = s + o_msteps;
   k.expr = (const uint32_t*)(s + o_expr);
   k.bl = hp.bl;
   p->kv_bytes = (size_t)L * 2 * max_batch * nkv * (size_t)max_ctx * d * 2;
@@ -575,6 +581,23 @@ int mk_decode_step(mk_plan* p, const int32_t* tokens, const int32_t* positions, 
   k.queue = p->d_queue;
   k.trace = nullptr;
   return cuda_err(p->kv.perop(k, r.first, r.second, st));
+}
+
+int mk_decode_steps(mk_plan* p, const int32_t* token, const int32_t* position, int n_steps,
+                    void* kv, int32_t* out_tokens, float* logits, void* stream) {
+  int rc = check_step(p, token, position, 1, kv, logits);
+  if (rc != MK_OK) return rc;
+  if (!out_tokens || n_steps < 1 || n_steps > (int)MAX_DECODE_STEPS) return MK_ERR_INVALID_ARG;
+  if (p->bd.on || !p->hp.fast_b1) return MK_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
+  KParams k = step_params(p, token, position, 1, kv, logits);
+  k.n_steps = (uint32_t)n_steps;
+  k.argmax = reinterpret_cast<unsigned long long*>(p->d_msteps);
+  k.lm_done = reinterpret_cast<uint32_t*>(p->d_msteps + 8 * MAX_DECODE_STEPS);
+  k.out_tokens = out_tokens;
+  MK_CUDA(cudaMemsetAsync(p->d_msteps, 0, 16 * MAX_DECODE_STEPS, st));
+  return cuda_err(p->kv.mega_steps(k, ctas, st));
 }
 
 int mk_plan_set_lm_mode(mk_plan* p, int mode) {

@@ -67,10 +67,11 @@ constexpr int X_STACK = 8;
 MK_HD uint32_t xw(uint32_t op, uint32_t imm = 0) { return (op << 24) | (imm & 0xffffffu); }
 
 // Evaluate expression `e` (X_MAX_WORDS words).  `pos` may be null when the
-// expression does not read positions.  Out-of-range positions evaluate as 0;
-// the caller validates them separately.
+// expression does not read positions; X_POS reads pos[b] + pos_add (the step
+// index of a multi-step launch).  Out-of-range positions evaluate as 0; the
+// caller validates them separately.
 MK_HD int64_t x_eval(const uint32_t* e, const Instr& in, int B, int S, const int32_t* pos,
-                     int n_pos) {
+                     int n_pos, int pos_add = 0) {
   int64_t st[X_STACK];
   int sp = 0;
   for (int i = 0; i < X_MAX_WORDS; ++i) {
@@ -87,7 +88,7 @@ MK_HD int64_t x_eval(const uint32_t* e, const Instr& in, int B, int S, const int
       case X_S: st[sp++] = S; break;
       case X_POS: {
         int64_t b = st[sp - 1];
-        st[sp - 1] = (pos && b >= 0 && b < n_pos) ? (int64_t)pos[b] : 0;
+        st[sp - 1] = (pos && b >= 0 && b < n_pos) ? (int64_t)pos[b] + pos_add : 0;
         break;
       }
       default: {
@@ -192,6 +193,20 @@ struct KParams {
   int mode;
   uint32_t perop_base;
   unsigned long long wait_limit_ns;
+  // Multi-step greedy decode (batch 1): the queue runs n_steps times in one
+  // launch; step s reads positions + s and, for s > 0, the token step s - 1
+  // chose.  Per step: the packed (ordered logit, inverted index) maximum over
+  // the LM-head tiles, the count of finished LM tiles, the chosen token.
+  // n_steps = 1 and null pointers for a single step.
+  uint32_t n_steps;
+  unsigned long long* argmax;  // [n_steps], zero before the launch
+  uint32_t* lm_done;           // [n_steps], zero before the launch
+  int32_t* out_tokens;         // [n_steps]
 };
+
+// Slot words carry the queue index in the low 24 bits and the step of a
+// multi-step launch above them.
+constexpr uint32_t SLOT_INDEX_BITS = 24;
+constexpr uint32_t MAX_DECODE_STEPS = 64;
 
 }  // namespace mk

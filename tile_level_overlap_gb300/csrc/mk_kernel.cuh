@@ -153,20 +153,20 @@ struct AttnExt {
   bool has_new;         // this split holds the new token's key (index pos)
 };
 
-__device__ __forceinline__ AttnExt attn_extent(const KParams& P, const Instr& in) {
+__device__ __forceinline__ AttnExt attn_extent(const KParams& P, const Instr& in, uint32_t step = 0) {
   AttnExt e;
   e.live = x_eval(P.expr + XS_SEQ_LIVE * X_MAX_WORDS, in, P.B, P.S, nullptr, 0) > 0;
   e.pos = 0;
   e.lo = e.hi = e.nc = 0;
   e.has_new = false;
   if (!e.live) return e;
-  e.pos = P.positions[in.a0];
+  e.pos = P.positions[in.a0] + (int)step;
   if (e.pos < 0 || e.pos >= P.max_ctx) {
     e.live = false;
     return e;
   }
-  e.lo = (int)x_eval(P.expr + XS_ATTN_LO * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B);
-  e.hi = (int)x_eval(P.expr + XS_ATTN_HI * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B);
+  e.lo = (int)x_eval(P.expr + XS_ATTN_LO * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step);
+  e.hi = (int)x_eval(P.expr + XS_ATTN_HI * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step);
   int cend = e.hi < e.pos ? e.hi : e.pos;
   e.nc = cend > e.lo ? cend - e.lo : 0;
   e.has_new = e.lo <= e.pos && e.pos < e.hi;
@@ -277,6 +277,9 @@ __device__ __forceinline__ uint32_t src_stages(const Src& s) {
 }
 
 // ---------------------------------------------------------------- producer
+// MS: the multi-step kernel (mk_decode_steps); the single-step kernel keeps
+// the step at 0 at compile time.
+template <bool MS>
 __device__ void producer(const KParams& P, const Sh& S) {
   const int lane = threadIdx.x & 31;
   if (lane != 0) return;
@@ -289,33 +292,37 @@ __device__ void producer(const KParams& P, const Sh& S) {
   // CTAs that reach it first instead of queueing behind the waiting one.  The
   // pop and record latency overlap the consumers' work on the stages already
   // in the ring.
+  // A multi-step launch runs the queue n_steps times: pop g is instruction
+  // g % n_instr of step g / n_instr.
   uint32_t npop = 0;
   auto pop = [&]() -> uint32_t {
     const uint32_t k = npop++;
     if (P.mode == MODE_MEGA) {
       if (S.flags[F_STOP]) return END_SLOT;
-      const uint32_t i = atomicAdd(&P.ctl[CTL_HEAD], 1u);
-      return i < P.n_instr ? i : END_SLOT;
+      const uint32_t g = atomicAdd(&P.ctl[CTL_HEAD], 1u);
+      return g < P.n_instr * (MS ? P.n_steps : 1u) ? g : END_SLOT;
     }
     return k == 0 ? P.perop_base + blockIdx.x : END_SLOT;
   };
   for (;;) {
     const bool room = mbar_wait(P, &S.empty[stage_ctr % NSTAGE], ((stage_ctr / NSTAGE) & 1u) ^ 1u);
-    const uint32_t i_in = room ? pop() : END_SLOT;
-    const bool end = i_in == END_SLOT;
+    const uint32_t g_in = room ? pop() : END_SLOT;
+    const bool end = g_in == END_SLOT;
+    const uint32_t step = (MS && !end) ? g_in / P.n_instr : 0u;
+    const uint32_t i_in = end ? END_SLOT : g_in - step * P.n_instr;
     Instr in;
     if (!end) in = P.queue[i_in];
     const int si = islot_ctr % NISLOT;
     bool posted_end = end;
     AttnExt ext;
     ext.live = false;
-    if (!end && in.op == OP_ATTN) ext = attn_extent(P, in);
+    if (!end && in.op == OP_ATTN) ext = attn_extent(P, in, step);
     if (!mbar_wait(P, &S.iempty[si], ((islot_ctr / NISLOT) & 1u) ^ 1u)) posted_end = true;
     if (!posted_end) {
       *slot_instr(S, si) = in;
       slot_put_ext(S, si, ext);
     }
-    *slot_index(S, si) = posted_end ? END_SLOT : i_in;
+    *slot_index(S, si) = posted_end ? END_SLOT : (i_in | (step << SLOT_INDEX_BITS));
     mbar_arrive(&S.ifull[si]);
     if (P.trace && !posted_end) P.trace[(size_t)i_in * TRACE_WORDS + 4] = globaltimer();
     ++islot_ctr;
@@ -400,9 +407,12 @@ __device__ __forceinline__ float consumer_sum(float v, float* scratch) {
   return s;
 }
 
-// Token id of sequence b, validated.
-__device__ __forceinline__ int token_of(const KParams& P, int b) {
-  int t = P.tokens[b];
+// Token id of sequence b, validated: the caller's for step 0 of a launch, for
+// a later step of a multi-step launch the one the previous step chose (the
+// index in its packed maximum, read after its LM tiles all finished).
+__device__ __forceinline__ int token_of(const KParams& P, int b, uint32_t step = 0) {
+  int t = step == 0 ? P.tokens[b]
+                    : (int)(0xffffffffu - (uint32_t)__ldcg(P.argmax + (step - 1)));
   if (t < 0 || t >= P.V) {
     if (threadIdx.x == 0) set_error(P, MK_ERR_BOUNDS, (uint32_t)b);
     t = 0;
@@ -452,11 +462,11 @@ __device__ __forceinline__ void load_x8(const KParams& P, const float* xs, const
 // a per-warp row slot; one fixed-order sum over warps per tile.
 template <int M>
 __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in,
-                                            float (&xr)[M][8]) {
+                                            float (&xr)[M][8], uint32_t step) {
   const int t = threadIdx.x;
   const int K = M * FAST_K_UNIT;
   const float* xs = gemv_x(P, in);
-  const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0) * P.H;
+  const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0, step) * P.H;
   const uint16_t* gain = gemv_gain(P, in);
   uint4 gw[M];
   if (gain) {
@@ -502,13 +512,13 @@ __device__ __forceinline__ void load_x_plain(const float* xs, float (&xr)[M][8])
 // is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
 // (RMAX * BMAX_CC <= NT).
 __device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr& in,
-                                                   const GemvDesc& g, int t) {
+                                                   const GemvDesc& g, int t, uint32_t step = 0) {
   const int B = P.B, l = in.layer;
   if (t >= g.rows * B) return 0.f;
   const int r = t / B, b = t % B, row = g.row0 + r;
   const size_t bh = (size_t)P.max_batch * P.H;
   if (in.op == OP_O) {
-    if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b) * P.H + row] << 16);
+    if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b, step) * P.H + row] << 16);
     return __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
   }
   if (in.op == OP_DOWN) return __ldcg(P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row);
@@ -519,6 +529,9 @@ __device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr
 // holds the instruction whose per-warp sums sit in redw[hb].
 __device__ __forceinline__ volatile uint32_t* hrec_index(const Sh& S, int hb) {
   return reinterpret_cast<volatile uint32_t*>(S.hrec + hb * SmemLayout::islot_bytes);
+}
+__device__ __forceinline__ volatile uint32_t* hrec_step(const Sh& S, int hb) {
+  return reinterpret_cast<volatile uint32_t*>(S.hrec + hb * SmemLayout::islot_bytes + 4);
 }
 __device__ __forceinline__ Instr* hrec_instr(const Sh& S, int hb) {
   return reinterpret_cast<Instr*>(S.hrec + hb * SmemLayout::islot_bytes + 16);
@@ -545,10 +558,10 @@ __device__ __forceinline__ void handoff_commit(const Sh& S, Ring& R, int hb) {
 // then the warp reduction of the previous stage's row sums, then this stage's
 // FMAs, so the shuffle chain overlaps the shared-memory latency instead of
 // following it; the loop body stays small (one stage).
-template <int M>
+template <int M, bool MS>
 __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in,
-                                          uint32_t ii, const GemvDesc& g, const Src& src, Ring& R,
-                                          const float (&xr)[M][8]) {
+                                          uint32_t ii, uint32_t step, const GemvDesc& g, const Src& src,
+                                          Ring& R, const float (&xr)[M][8]) {
   constexpr int RPS = fast_rps(M);  // whole rows per 32 KB stage at K = M * 2048
   constexpr int kDup = 32 / RPS;    // lanes holding the same total after the reduction
   constexpr int NP = M > 1 ? M : 2;
@@ -560,7 +573,8 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   if (P.trace && t == 0) trace_mark(P, ii, 11);
   // the residual input of the tile's outputs (O, down), loaded now so that its
   // latency hides behind the stages; the finisher takes it from the hand-off
-  const float pre = epilogue_prefetch(P, in, g, t);
+  const float pre = epilogue_prefetch(P, in, g, t, step);
+  if (MS && t == 0) *hrec_step(S, hb) = step;  // the buffer is this tile's from here on
   float* redw = S.redw + hb * NW * RMAX;
   const int idx = warp_multi_index<RPS>(lane);
   const bool writer = (lane & (kDup - 1)) == 0;
@@ -1055,8 +1069,9 @@ __device__ __forceinline__ void attn_dispatch(const KParams& P, const Sh& S, con
 }
 
 // Drain an instruction's stages without computing (after an abort).
-__device__ __forceinline__ void drain(const KParams& P, const Sh& S, const Instr& in, Ring& R) {
-  const uint32_t n = src_stages(instr_src(P, in));
+__device__ __forceinline__ void drain(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
+                                      Ring& R) {
+  const uint32_t n = src_stages(src_of(P, in, e));
   for (uint32_t k = 0; k < n; ++k) {
     ring_acquire(P, S, R);
     ring_release(S, R);
@@ -1067,7 +1082,7 @@ __device__ __forceinline__ void drain(const KParams& P, const Sh& S, const Instr
 // MH, MF: K / FAST_K_UNIT of the hidden size and of the FFN size for the
 // batch-1 register path (0: the shared-memory path only).  AD, AREP: head_dim
 // and q heads per kv head of the attention tile (0: chosen at run time).
-template <int MH, int MF, int AD, int AREP>
+template <int MH, int MF, int AD, int AREP, bool MS>
 __device__ void consumer(const KParams& P, const Sh& S) {
   const int t = threadIdx.x;
   Ring R{0, 0, 0, 0, false, false};
@@ -1102,13 +1117,31 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     // counter runs to completion anyway); one consumer barrier then hands the
     // slot and the verdict to every consumer thread.
     if (t == 0) {
-      const uint32_t iv = S.flags[f_slot];
+      const uint32_t sv = S.flags[f_slot];
+      const uint32_t iv = (!MS || sv == END_SLOT) ? sv : sv & ((1u << SLOT_INDEX_BITS) - 1u);
+      const uint32_t step0 = (!MS || sv == END_SLOT) ? 0u : sv >> SLOT_INDEX_BITS;
       uint32_t aborted = S.flags[F_STOP];
       const uint64_t t_begin = P.trace ? globaltimer() : 0;
       if (iv != END_SLOT) {
         const Instr& in0 = *slot_instr(S, si);
+        // a later step of a multi-step launch starts from the token the
+        // previous step chose: the layer-0 projection waits for all of that
+        // step's LM-head tiles
+        if (MS && !aborted && step0 > 0 && in0.op == OP_QKV && in0.layer == 0) {
+          const uint64_t t0 = globaltimer();
+          while ((int32_t)(ld_acquire_gpu(P.lm_done + (step0 - 1)) - P.n_lm_tiles) < 0) {
+            if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) {
+              aborted = 1;
+            } else if (globaltimer() - t0 > P.wait_limit_ns) {
+              set_error(P, MK_ERR_TIMEOUT, iv);
+              aborted = 1;
+            }
+            if (aborted) break;
+            __nanosleep(32);
+          }
+        }
         if (!aborted && P.mode == MODE_MEGA && in0.wait_bar != NO_BAR) {
-          const uint32_t target = (gen + 1u) * in0.wait_target;
+          const uint32_t target = (gen + step0 + 1u) * in0.wait_target;
           if (!(in0.wait_n == 1 && in0.wait_bar == ok_bar && target == ok_target)) {
             const uint64_t t0 = globaltimer();
             for (uint32_t k = 0; k < in0.wait_n && !aborted;) {
@@ -1144,7 +1177,9 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     }
     cbar();
     if (P.trace && t == 0 && S.flags[f_slot] != END_SLOT) trace_mark(P, R.cur, 10);
-    const uint32_t i = S.flags[f_slot];
+    const uint32_t slotv = S.flags[f_slot];
+    const uint32_t i = (!MS || slotv == END_SLOT) ? slotv : slotv & ((1u << SLOT_INDEX_BITS) - 1u);
+    const uint32_t step = (!MS || slotv == END_SLOT) ? 0u : slotv >> SLOT_INDEX_BITS;
     Instr in;
     AttnExt ext;
     ext.live = false;
@@ -1158,7 +1193,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     ++islot_ctr;
     if (i == END_SLOT) break;
     if (aborted_now) {
-      drain(P, S, in, R);
+      drain(P, S, in, ext, R);
       continue;
     }
     // The batch-1 GEMV tiles (most instructions) come first in the code, so
@@ -1167,21 +1202,21 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     if (MH > 0 && P.B == 1 && in.op != OP_ATTN) {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8);
+      const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8) | (step << 24);
       if (in.op != OP_DOWN) {
         auto& xh = *reinterpret_cast<float(*)[XH][8]>(&xr);
         if (tag != tag_x) {
-          load_x_fast<XH>(P, S, in, xh);
+          load_x_fast<XH>(P, S, in, xh, step);
           tag_x = tag;
         }
-        gemv_fast<XH>(P, S, in, i, g, src, R, xh);
+        gemv_fast<XH, MS>(P, S, in, i, step, g, src, R, xh);
       } else {
         auto& xf = *reinterpret_cast<float(*)[XF][8]>(&xr);
         if (tag != tag_x) {
           load_x_plain<XF>(gemv_x(P, in), xf);
           tag_x = tag;
         }
-        gemv_fast<XF>(P, S, in, i, g, src, R, xf);
+        gemv_fast<XF, MS>(P, S, in, i, step, g, src, R, xf);
       }
     } else if (in.op == OP_ATTN) {
       attn_dispatch<AD, AREP>(P, S, in, ext, i, R);
@@ -1221,11 +1256,41 @@ __device__ void consumer(const KParams& P, const Sh& S) {
   handoff_commit(S, R, hb);
 }
 
+// ---------------------------------------------------------------- greedy choice
+// A logit and its vocabulary row packed so that the unsigned maximum picks the
+// largest logit and, among equal logits, the smallest row: the float's bits
+// mapped to an order-preserving unsigned word, then the row inverted.
+__device__ __forceinline__ unsigned long long argmax_key(float y, uint32_t row) {
+  const uint32_t u = __float_as_uint(y);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (0xffffffffu - row);
+}
+
+// One LM-head tile of a multi-step launch (finisher warp, batch 1): fold the
+// tile's logits into the step's maximum, count the tile; the last tile of the
+// step stores the chosen token.
+__device__ void lm_tile_choose(const KParams& P, const GemvDesc& g, uint32_t step, int lane) {
+  unsigned long long key = 0;
+  if (lane < g.rows) key = argmax_key(P.logits[g.row0 + lane], (uint32_t)(g.row0 + lane));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+    key = other > key ? other : key;
+  }
+  if (lane == 0) {
+    atomicMax(P.argmax + step, key);
+    const uint32_t old = atom_add_acq_rel_gpu(P.lm_done + step, 1u);
+    if (old + 1u == P.n_lm_tiles)
+      P.out_tokens[step] = (int32_t)(0xffffffffu - (uint32_t)__ldcg(P.argmax + step));
+  }
+}
+
 // ---------------------------------------------------------------- finisher warp
 // Takes the batch-1 GEMV tiles in hand-off order: adds up the consumer warps'
 // partial sums (fixed order), frees the buffer, stores the outputs (residual
 // adds, SwiGLU) and releases the tile's counter.  Its store latency and the
 // release fence stay off the consumers' path.
+template <bool MS>
 __device__ void finisher(const KParams& P, const Sh& S) {
   const int lane = threadIdx.x & 31;
   for (uint32_t h = 0;; ++h) {
@@ -1245,11 +1310,13 @@ __device__ void finisher(const KParams& P, const Sh& S) {
       S.fin[lane * BMAX_CC] = s;
     }
     const float pre = S.hpre[hb * RMAX + lane];
+    const uint32_t step = MS ? *hrec_step(S, hb) : 0u;
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.hempty[hb]);
     if (P.trace && lane == 0) P.trace[(size_t)ii * TRACE_WORDS + 14] = globaltimer();
     gemv_epilogue(P, S.fin, in, g, pre, lane);
     __syncwarp();
+    if (MS && in.op == OP_LM) lm_tile_choose(P, g, step, lane);
     if (lane == 0) {
       if (P.mode == MODE_MEGA && in.rel_bar != NO_BAR) red_release_gpu_add(&P.bars[in.rel_bar], 1u);
       if (P.trace) {
@@ -1261,7 +1328,7 @@ __device__ void finisher(const KParams& P, const Sh& S) {
   }
 }
 
-template <int MH, int MF, int AD, int AREP>
+template <int MH, int MF, int AD, int AREP, bool MS>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_constant__ KParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Sh S = sh_map(smem);
@@ -1291,9 +1358,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
     for (int i = t; i < words; i += NTHREADS) dst[i] = src[i];
   }
   __syncthreads();
-  if (t >= NT + 32) finisher(P, S);
-  else if (t >= NT) producer(P, S);
-  else consumer<MH, MF, AD, AREP>(P, S);
+  if (t >= NT + 32) finisher<MS>(P, S);
+  else if (t >= NT) producer<MS>(P, S);
+  else consumer<MH, MF, AD, AREP, MS>(P, S);
   __syncthreads();
   if (t == 0 && P.mode == MODE_MEGA) {
     __threadfence();
@@ -1302,7 +1369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
       // every CTA has left its loop: rewind the queue head for the next launch
       P.ctl[CTL_HEAD] = 0u;
       P.ctl[CTL_EXIT] = 0u;
-      P.ctl[CTL_GEN] = S.flags[F_GEN] + 1u;
+      P.ctl[CTL_GEN] = S.flags[F_GEN] + (MS ? P.n_steps : 1u);
       __threadfence();
     }
   }
@@ -1312,24 +1379,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
 template <int MH, int MF, int AD, int AREP>
 struct VariantImpl {
   static cudaError_t setup() {
-    return cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP>,
+    cudaError_t e = cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total);
+    if (e != cudaSuccess || MH == 0) return e;
+    return cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total);
   }
   static cudaError_t occupancy(int* per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk_interpreter<MH, MF, AD, AREP>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk_interpreter<MH, MF, AD, AREP, false>,
                                                          NTHREADS, SmemLayout::total);
   }
   static cudaError_t mega(const KParams& p, int ctas, cudaStream_t st) {
     KParams pp = p;
     void* args[] = {(void*)&pp};
-    return cudaLaunchCooperativeKernel((const void*)mk_interpreter<MH, MF, AD, AREP>, dim3(ctas),
+    return cudaLaunchCooperativeKernel((const void*)mk_interpreter<MH, MF, AD, AREP, false>, dim3(ctas),
+                                       dim3(NTHREADS), args, (size_t)SmemLayout::total, st);
+  }
+  // the multi-step kernel (mk_decode_steps; batch-1 register path only)
+  static cudaError_t mega_steps(const KParams& p, int ctas, cudaStream_t st) {
+    if (MH == 0) return cudaErrorNotSupported;
+    KParams pp = p;
+    void* args[] = {(void*)&pp};
+    return cudaLaunchCooperativeKernel((const void*)mk_interpreter<MH, MF, AD, AREP, MH != 0>, dim3(ctas),
                                        dim3(NTHREADS), args, (size_t)SmemLayout::total, st);
   }
   static cudaError_t perop(const KParams& p, uint32_t first, uint32_t count, cudaStream_t st) {
     KParams pp = p;
     pp.mode = MODE_PEROP;
     pp.perop_base = first;
-    mk_interpreter<MH, MF, AD, AREP><<<count, NTHREADS, SmemLayout::total, st>>>(pp);
+    mk_interpreter<MH, MF, AD, AREP, false><<<count, NTHREADS, SmemLayout::total, st>>>(pp);
     return cudaGetLastError();
   }
 };
@@ -1347,6 +1425,7 @@ KernelVariant make_variant() {
   k.setup = &V::setup;
   k.occupancy = &V::occupancy;
   k.mega = &V::mega;
+  k.mega_steps = &V::mega_steps;
   k.perop = &V::perop;
   return k;
 }

@@ -185,5 +185,6 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   k.logits = logits;
   k.mode = MODE_MEGA;
   k.wait_limit_ns = 2000000000ull;
+  k.n_steps = 1;
   return kv.mega(k, nsm, st) == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }

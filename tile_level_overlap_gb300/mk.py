@@ -31,7 +31,7 @@ EXPORTED = [
     "mk_decode_step_host", "mk_prefill", "mk_run_per_op", "mk_status", "mk_plan_reset",
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
-    "mk_plan_set_lm_mode",
+    "mk_plan_set_lm_mode", "mk_decode_steps",
 ]
 
 
@@ -91,6 +91,7 @@ def lib() -> ctypes.CDLL:
                                 ctypes.c_uint64, ctypes.POINTER(mk_plan_stats)]
     L.mk_plan_set_debug.argtypes = [vp, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64]
     L.mk_plan_set_lm_mode.argtypes = [vp, ctypes.c_int]
+    L.mk_decode_steps.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
     L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -223,6 +224,14 @@ class Plan:
     def decode_step(self, tokens, positions, kv, logits, stream=None) -> None:
         _check(lib().mk_decode_step(self.h, _ptr(tokens), _ptr(positions), int(tokens.numel()),
                                     _ptr(kv), _ptr(logits), _stream_ptr(stream)), "mk_decode_step")
+
+    def decode_steps(self, token, position, n_steps: int, kv, out_tokens, logits, stream=None) -> None:
+        """mk_decode_steps: n_steps greedy decode steps of one sequence in one
+        launch (device tensors: token [1], position [1], out_tokens [n_steps],
+        logits [V])."""
+        _check(lib().mk_decode_steps(self.h, _ptr(token), _ptr(position), int(n_steps), _ptr(kv),
+                                     _ptr(out_tokens), _ptr(logits), _stream_ptr(stream)),
+               "mk_decode_steps")
 
     def decode_step_host(self, tokens, positions, kv, logits, stream=None) -> int:
         """tokens/positions/logits are CPU tensors (pinned for speed)."""
