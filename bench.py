@@ -464,6 +464,24 @@ def run_ours(args):
                    "frac_of_tensor_peak": tf / peaks_p["bf16_tflops_sustained"],
                    "peak_kind": kind_p + " (sustained bf16)", "steps": pf_steps,
                    "kernels_per_step": 2}
+        # the same prompt with the logits of every token (final norm and LM
+        # head as tensor-core tiles inside the one persistent launch)
+        pall = torch.empty((S, cfg.vocab), dtype=torch.float32, device=dev)
+
+        def pf_all():
+            plan.prefill_logits(ptok, kv, pall, stream=stream)
+
+        pf_all()
+        rc = plan.status(stream)
+        if rc != mk.MK_OK:
+            raise RuntimeError(f"prefill device status {rc}")
+        ms_all = timed(pf_all, pf_steps) / pf_steps
+        flops_all = flops + 2.0 * (S - 1) * cfg.vocab * cfg.hidden
+        tf_all = flops_all / (ms_all / 1e3) / 1e12
+        prefill["all_token_logits"] = {
+            "ms": ms_all, "tokens_per_s": S / (ms_all / 1e3), "tflops": tf_all,
+            "frac_of_tensor_peak": tf_all / peaks_p["bf16_tflops_sustained"], "kernels_per_step": 1}
+        del pall
 
     if rank != 0:
         return 0

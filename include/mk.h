@@ -192,6 +192,18 @@ int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
 int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
                   mk_plan_stats *out);
 
+/* Prefill with the logits of EVERY prompt token (SURVEY.md-listed variant of
+ * the prefill: "MegaOps", Abstract, prefill of the dense Llama3/Qwen3
+ * decoders).  Same as mk_prefill, except that the final RMSNorm and the LM
+ * head run for all len tokens inside the same persistent launch, as
+ * tensor-core GEMM tiles (128 tokens x 256 vocabulary rows) that wait on the
+ * last layer's tiles of their own 128-token block.
+ *   logits  device float [len][V], row-major, caller-owned; row i = the
+ *           logits after token i (row len - 1 = mk_prefill's logits).
+ * Errors as mk_prefill. */
+int mk_prefill_logits(mk_plan *plan, const int32_t *tokens, int len, void *kv_cache, float *logits,
+                      void *stream);
+
 /* Greedy decode of n_steps tokens of one sequence in ONE persistent launch
  * (the host stays out of the loop: "Lecture 112" summary, Practical
  * implications).  Step s (0 <= s < n_steps) is the decode step of

@@ -152,3 +152,57 @@ def test_llama3_8b_width_prefill_2048_tokens():
         _kv_close("V", kv[:, 1, 0, :, :2048, :], V)
     finally:
         m.close()
+
+
+def _prefill_logits(m, tokens):
+    t = torch.as_tensor(tokens, dtype=torch.int32).to(m.dev)
+    logits = torch.full((len(tokens), m.cfg.vocab), float("nan"), device=m.dev)
+    m.plan.prefill_logits(t, m.kv, logits)
+    rc = m.plan.status()
+    assert rc == mk.MK_OK, mk.lib().mk_status_string(rc)
+    return logits.cpu().numpy()
+
+
+@pytest.mark.parametrize("S", [1, 130, 300])
+def test_prefill_all_token_logits(small, S):
+    """Every row of mk_prefill_logits against the oracle's all-token logits;
+    the cache as mk_prefill writes it; repeat runs bit-identical."""
+    tokens = synth.make_tokens(S, small.cfg.vocab, seed=S + 40).numpy()
+    got = _prefill_logits(small, tokens)
+    ref, K, V = oracle.prefill(small.cfg, synth.LazyBits(small.w), tokens, all_logits=True)
+    _rows_close(got, ref)
+    kv = oracle.widen_bf16(synth.bf16_bits(small.kv))
+    _kv_close("K", kv[:, 0, 0, :, :S, :], K)
+    _kv_close("V", kv[:, 1, 0, :, :S, :], V)
+    np.testing.assert_array_equal(_prefill_logits(small, tokens), got)
+    # the last-token entry point still gives its own (CUDA-core) last row
+    _rows_close(small.prefill(tokens)[None, :], ref[-1:])
+
+
+def test_prefill_all_token_logits_ragged_vocab():
+    """A vocabulary that is not a multiple of the 256-row LM tile."""
+    cfg = PF_SMALL.replace(vocab=1000)
+    m = PfModel(cfg, max_ctx=200, seed=2)
+    try:
+        tokens = synth.make_tokens(150, cfg.vocab, seed=3).numpy()
+        got = _prefill_logits(m, tokens)
+        ref, _, _ = oracle.prefill(cfg, synth.LazyBits(m.w), tokens, all_logits=True)
+        _rows_close(got, ref)
+    finally:
+        m.close()
+
+
+def test_llama3_8b_width_prefill_all_token_logits_sampled():
+    """Llama-3-8B widths, 2 layers, 2048 tokens: sampled rows of the all-token
+    logits against the oracle's last-token logits of the prompt's prefixes
+    (row r depends on tokens 0..r only)."""
+    cfg = synth.LLAMA3_8B.replace(n_layers=2)
+    m = PfModel(cfg, max_ctx=2049, seed=0)
+    try:
+        tokens = synth.make_tokens(2048, cfg.vocab).numpy()
+        got = _prefill_logits(m, tokens)
+        for r in [0, 129, 2047]:
+            ref, _, _ = oracle.prefill(cfg, synth.LazyBits(m.w), tokens[:r + 1])
+            _rows_close(got[r:r + 1], ref[None, :])
+    finally:
+        m.close()

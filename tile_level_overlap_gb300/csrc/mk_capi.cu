@@ -682,7 +682,8 @@ static int prefill_init(mk_plan* p) {
   ok = ok && make_tmap_bf16(a + AM_HN1, b + o_hn1, 2 * rows, H, PF_BM) &&
        make_tmap_bf16(a + AM_HN2, b + o_hn2, 2 * rows, H, PF_BM) &&
        make_tmap_bf16(a + AM_AO, b + o_ao, 2 * rows, qd, PF_BM) &&
-       make_tmap_bf16(a + AM_ACT, b + o_act, 2 * rows, F, PF_BM);
+       make_tmap_bf16(a + AM_ACT, b + o_act, 2 * rows, F, PF_BM) &&
+       make_tmap_bf16(a + AM_LMW, p->base.lm, (uint64_t)c.vocab, H, PF_BN);
   if (!ok) return MK_ERR_CUDA;
   MK_CUDA(cudaMemcpy(b + o_q, pp.queue.data(), sizeof(Instr) * pp.queue.size(), cudaMemcpyHostToDevice));
   MK_CUDA(cudaMemcpy(b + o_expr, pp.expr.data(), sizeof(uint32_t) * pp.expr.size(),
@@ -696,6 +697,7 @@ static int prefill_init(mk_plan* p) {
   k.eps = c.rms_eps;
   k.n_qkv_n = pp.n_qkv_n; k.n_o_n = pp.n_o_n; k.n_gu_n = pp.n_gu_n; k.n_down_n = pp.n_down_n;
   k.embed = p->base.embed;
+  k.final_norm = p->base.final_norm;
   k.layers = p->base.layers;
   k.tm = s.d_tm;
   k.xa = (float*)(b + o_xa);
@@ -710,7 +712,7 @@ static int prefill_init(mk_plan* p) {
   k.bars = (uint32_t*)(b + o_bars);
   k.ctl = (uint32_t*)(b + o_ctl);
   k.queue = (const Instr*)(b + o_q);
-  k.n_instr = (uint32_t)pp.queue.size();
+  k.n_instr = pp.n_body;  // the all-token logits entry point runs the rest too
   k.expr = (const uint32_t*)(b + o_expr);
   s.built = true;
   return MK_OK;
@@ -768,6 +770,25 @@ int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logi
   return prefill_lm(p, tokens, len, kv, logits, st);
 }
 
+int mk_prefill_logits(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits,
+                      void* stream) {
+  int rc = prefill_args(p, tokens, len, kv, logits);
+  if (rc != MK_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = prefill_init(p)) != MK_OK || (rc = prefill_bind_kv(p, kv, st)) != MK_OK) return rc;
+  PfParams k = p->pf.base;
+  k.tokens = tokens;
+  k.S = len;
+  k.kv = (uint16_t*)kv;
+  k.logits = logits;
+  k.n_instr = (uint32_t)p->pf.pp.queue.size();  // the body, the final norms, the LM head
+  const PfBars& bl = p->pf.pp.bl;
+  MK_CUDA(cudaMemsetAsync(k.bars + bl.normf, 0, sizeof(uint32_t) * (bl.total - bl.normf), st));
+  k.mode = MODE_MEGA;
+  k.wait_limit_ns = p->wait_limit_ns;
+  return cuda_err(pf_launch_mega(k, p->n_sms, st));
+}
+
 static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
   for (const auto& r : p->hp.perop_decode) MK_CUDA(p->kv.perop(k, r.first, r.second, st));
   return MK_OK;
@@ -782,7 +803,10 @@ static int launch_per_op_bd(mk_plan* p, const BdParams& k, cudaStream_t st) {
 
 static int launch_per_op_prefill(mk_plan* p, const PfParams& k, void* kv, float* logits,
                                  cudaStream_t st) {
-  for (const auto& r : p->pf.pp.perop) MK_CUDA(pf_launch_perop(k, r.first, r.second, st));
+  for (uint32_t j = 0; j < p->pf.pp.n_perop_body; ++j) {
+    const auto& r = p->pf.pp.perop[j];
+    MK_CUDA(pf_launch_perop(k, r.first, r.second, st));
+  }
   return prefill_lm(p, k.tokens, k.S, kv, logits, st);
 }
 

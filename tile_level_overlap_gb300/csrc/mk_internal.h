@@ -36,6 +36,9 @@ constexpr uint8_t NO_EXPR = 0xff;
 
 // Instruction flags.
 constexpr uint8_t IF_RELEASE_ON_COMBINE = 1;  // release happens once per (seq, kv head) group
+// The waited counter is cleared before every launch that runs this
+// instruction (it is not released by every launch): absolute target.
+constexpr uint8_t IF_ABS_TARGET = 2;
 
 // One queue record, 32 bytes.
 struct Instr {

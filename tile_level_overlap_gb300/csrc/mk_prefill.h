@@ -25,6 +25,8 @@ enum PfOp : uint8_t {
   PF_NORM2 = 20,  // RMSNorm of a block before the FFN                  (a0 = block)
   PF_GU = 21,     // gate/up columns n (128 + 128) of a block, SwiGLU   (a0 = block, a1 = n)
   PF_DOWN = 22,   // down columns n of a block + residual               (a0 = block, a1 = n)
+  PF_NORMF = 23,  // final RMSNorm of a block (all-token logits only)    (a0 = block)
+  PF_LM = 24,     // LM-head columns n of a block -> f32 logits         (a0 = block, a1 = n)
 };
 
 constexpr int PF_BM = 128;   // tokens per block (tcgen05 M)
@@ -37,17 +39,20 @@ constexpr int PXS_BLOCK_LIVE = 0;
 constexpr int PF_BLOCK_GROUP = 4;  // token blocks that share each weight tile in the queue order
 constexpr int PXS_COUNT = 1;
 
-// Barrier sub-tensors, each [L][n_blocks].
+// Barrier sub-tensors, each [L][n_blocks]; normf and lm are [n_blocks].
 struct PfBars {
-  uint32_t norm1, qkv, attn, o, norm2, gu, down, total;
+  uint32_t norm1, qkv, attn, o, norm2, gu, down, normf, lm, total;
 };
 
 struct PrefillPlan {
   mk_model_cfg cfg{};
   int max_ctx = 0, n_blocks = 0, rep = 0, qkv_rows = 0;
   int bn_qkv = 0;  // 256, or 128 when a head group does not fill 256 columns
-  uint32_t n_qkv_n = 0, n_o_n = 0, n_gu_n = 0, n_down_n = 0;
+  uint32_t n_qkv_n = 0, n_o_n = 0, n_gu_n = 0, n_down_n = 0, n_lm_n = 0;
   PfBars bl{};
+  // queue[0, n_body): the prompt's layers; queue[n_body, size): the final
+  // norm and the LM head of every token (run only for all-token logits)
+  uint32_t n_body = 0, n_perop_body = 0;  // (and the per-operator ranges of the body)
   std::vector<Instr> queue;                                // topological
   std::vector<std::pair<uint32_t, uint32_t>> perop;        // (first, count) per launch
   std::vector<uint32_t> expr;                              // PXS_COUNT * X_MAX_WORDS
@@ -57,7 +62,7 @@ struct PrefillPlan {
 // then the activation maps at L * 8 + AM_*.
 enum PfWeightMap { TM_WQ = 0, TM_WK = 1, TM_WV = 2, TM_WO = 3, TM_WG = 4, TM_WU = 5, TM_WD = 6,
                    TM_PER_LAYER = 8 };
-enum PfActMap { AM_HN1 = 0, AM_HN2 = 1, AM_AO = 2, AM_ACT = 3, AM_KV = 4, AM_COUNT = 5 };
+enum PfActMap { AM_HN1 = 0, AM_HN2 = 1, AM_AO = 2, AM_ACT = 3, AM_KV = 4, AM_LMW = 5, AM_COUNT = 6 };
 
 // Everything one prefill launch needs (passed by value).
 struct PfParams {
@@ -65,6 +70,8 @@ struct PfParams {
   float eps;
   uint32_t n_qkv_n, n_o_n, n_gu_n, n_down_n;
   const uint16_t* embed;
+  const uint16_t* final_norm;
+  float* logits;            // all-token logits [S][V] (PF_LM tiles), or null
   const LayerW* layers;     // device array [L]
   const void* tm;           // CUtensorMap table (64-byte aligned)
   float* xa;                // residual after attention, f32 [rows][H]

@@ -122,7 +122,7 @@ __device__ __forceinline__ bool pf_live(const PfParams& P, const Instr& in) {
 // false (abort) on timeout or when another CTA aborted.
 __device__ bool pf_wait_deps(const PfParams& P, const Instr& in, uint32_t gen, uint32_t idx) {
   if (P.mode != MODE_MEGA || in.wait_bar == NO_BAR) return true;
-  const uint32_t target = (gen + 1u) * in.wait_target;
+  const uint32_t target = (in.flags & IF_ABS_TARGET) ? in.wait_target : (gen + 1u) * in.wait_target;
   const uint64_t t0 = globaltimer();
   for (uint32_t k = 0; k < in.wait_n;) {
     const uint32_t* c = &P.bars[in.wait_bar + k * in.wait_stride];
@@ -141,7 +141,7 @@ __device__ bool pf_wait_deps(const PfParams& P, const Instr& in, uint32_t gen, u
 }
 
 __device__ __forceinline__ bool is_gemm(uint8_t op) {
-  return op == PF_QKV || op == PF_O || op == PF_GU || op == PF_DOWN;
+  return op == PF_QKV || op == PF_O || op == PF_GU || op == PF_DOWN || op == PF_LM;
 }
 
 // GEMM geometry of an instruction.
@@ -178,6 +178,14 @@ __device__ __forceinline__ PfGemm pf_gemm(const PfParams& P, const Instr& in) {
       }
       break;
     }
+    case PF_LM:
+      g.K = P.H;
+      g.a_map = am(P, AM_HN1);
+      g.bn = PF_BN;
+      g.b_map0 = am(P, AM_LMW);
+      g.b_row0 = n * PF_BN;
+      g.b_rows0 = PF_BN;
+      break;
     case PF_O:
       g.K = qd;
       g.a_map = am(P, AM_AO);
@@ -558,6 +566,20 @@ __device__ void pf_gemm_epilogue(const PfParams& P, const Instr& in, uint32_t ta
       }
       break;
     }
+    case PF_LM: {  // logits of token p, vocabulary rows [256 n, 256 n + 256) (< V)
+      const int col0 = n * PF_BN;
+      float* dst = P.logits + (size_t)p * P.V + col0;
+      for (int c = 0; c < PF_BN; c += 16) {
+        float v[16];
+        tmem_ld16(tacc + (uint32_t)c, v);
+        if (live) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (col0 + c + e < P.V) dst[c + e] = v[e];
+        }
+      }
+      break;
+    }
     default: {  // PF_GU: columns [0,128) gate, [128,256) up
       uint16_t* dst = P.act + (size_t)p * P.F + n * PF_BN_GU;
       uint16_t* dst_lo = dst + (size_t)P.plane_rows * P.F;
@@ -577,10 +599,13 @@ __device__ void pf_gemm_epilogue(const PfParams& P, const Instr& in, uint32_t ta
 // RMSNorm of one 128-token block: warp w handles rows w, w + 4, ...
 __device__ void pf_norm(const PfParams& P, const Instr& in, int wc, int lane) {
   const int l = in.layer, m = (int)in.a0, H = P.H;
+  // NORM1 (and the final norm, PF_NORMF) read the residual after the FFN and
+  // write the hn1 planes; NORM2 reads the residual after attention
   const bool first = in.op == PF_NORM1;
-  const float* src = first ? P.xb : P.xa;
-  const uint16_t* gain = first ? P.layers[l].attn_norm : P.layers[l].ffn_norm;
-  uint16_t* dst = first ? P.hn1 : P.hn2;
+  const bool fin = in.op == PF_NORMF;
+  const float* src = (first || fin) ? P.xb : P.xa;
+  const uint16_t* gain = fin ? P.final_norm : first ? P.layers[l].attn_norm : P.layers[l].ffn_norm;
+  uint16_t* dst = (first || fin) ? P.hn1 : P.hn2;
   for (int r = wc; r < PF_BM; r += 4) {
     const int p = m * PF_BM + r;
     if (p >= P.S) break;

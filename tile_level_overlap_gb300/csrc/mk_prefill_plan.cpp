@@ -57,6 +57,7 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
   pp.n_o_n = (uint32_t)(c.hidden / PF_BN);
   pp.n_gu_n = (uint32_t)(c.ffn / PF_BN_GU);
   pp.n_down_n = (uint32_t)(c.hidden / PF_BN);
+  pp.n_lm_n = (uint32_t)((c.vocab + PF_BN - 1) / PF_BN);
 
   const int L = c.n_layers, NB = pp.n_blocks, nkv = c.n_kv_heads;
   PfBars& b = pp.bl;
@@ -68,7 +69,9 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
   b.norm2 = b.o + per;
   b.gu = b.norm2 + per;
   b.down = b.gu + per;
-  b.total = b.down + per;
+  b.normf = b.down + per;
+  b.lm = b.normf + (uint32_t)NB;
+  b.total = b.lm + (uint32_t)NB;
   auto bar = [&](uint32_t base, int l, int m) { return base + (uint32_t)(l * NB + m); };
 
   pp.expr.assign((size_t)PXS_COUNT * X_MAX_WORDS, 0);
@@ -177,6 +180,35 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
     });
     end(s);
   }
+  pp.n_body = (uint32_t)q.size();
+  pp.n_perop_body = (uint32_t)pp.perop.size();
+  // all-token logits: the final norm of every block, then the LM head (the
+  // tensor-core GEMM of the normed rows with the [V][H] weights)
+  uint32_t s = begin();
+  for (int m = 0; m < NB; ++m) {
+    Instr in = pf_make(PF_NORMF, L - 1, m, 0);
+    in.wait_bar = bar(b.down, L - 1, m);
+    in.wait_target = pp.n_down_n;
+    in.wait_n = 1;
+    in.wait_stride = 1;
+    in.rel_bar = b.normf + (uint32_t)m;
+    q.push_back(in);
+  }
+  end(s);
+  s = begin();
+  // (the normf and lm counters are released only by launches that run this
+  // tail: they are cleared before each such launch and waited on absolutely)
+  grouped(pp.n_lm_n, [&](int m, uint32_t n) {
+    Instr in = pf_make(PF_LM, L - 1, m, n);
+    in.flags = IF_ABS_TARGET;
+    in.wait_bar = b.normf + (uint32_t)m;
+    in.wait_target = 1;
+    in.wait_n = 1;
+    in.wait_stride = 1;
+    in.rel_bar = b.lm + (uint32_t)m;
+    q.push_back(in);
+  });
+  end(s);
   return MK_OK;
 }
 
@@ -184,7 +216,7 @@ int simulate_prefill(const PrefillPlan& pp, const std::vector<Instr>& q, std::st
   std::vector<uint32_t> cnt(pp.bl.total, 0);
   for (size_t i = 0; i < q.size(); ++i) {
     const Instr& in = q[i];
-    if (in.op < PF_NORM1 || in.op > PF_DOWN) {
+    if (in.op < PF_NORM1 || in.op > PF_LM) {
       if (why) *why = "unknown prefill opcode at " + std::to_string(i);
       return MK_ERR_INVALID_ARG;
     }
