@@ -48,7 +48,7 @@ constexpr int BD_BK = 64;       // reduction depth per ring stage (one 128-byte 
 constexpr int BD_NMAX = 32;     // most sequences per step (tcgen05 N)
 constexpr int BD_KC = 1024;     // K chunk of a split-K tile
 constexpr int BD_RG = 8;        // sequences per RMSNorm instruction (one compute warp each)
-constexpr int BD_KEYS = 64;     // cached keys per attention stage
+constexpr int BD_KEYS = 128;    // cached keys per attention block (K in one ring stage, V in the next)
 constexpr int BD_NSPLIT_MAX = 8;  // attention splits per (sequence, kv head), at most
 
 // Barrier sub-tensors: one counter per layer and operator.

@@ -235,7 +235,7 @@ __device__ __forceinline__ int attn_blocks(const BdAttn& e) {
 // Ring stages an instruction occupies (known to every role from the record).
 __device__ __forceinline__ int bd_stages(const BdParams& P, const BdSh& S, const Instr& in) {
   if (is_gemm(in.op)) return bd_gemm(P, in).nk;
-  if (in.op == BD_ATTN) return attn_blocks(bd_attn(P, S, in));
+  if (in.op == BD_ATTN) return 2 * attn_blocks(bd_attn(P, S, in));
   return 0;
 }
 
@@ -344,18 +344,17 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
       bd_mark(P, i, 5);
       const int l = in.layer, b = (int)in.a0, g = (int)in.a1;
       const int nbox = P.d / 64;
-      const uint32_t half = BD_STAGE / 2;
-      for (int j = 0; j < nblk; ++j) {
-        const int st = stage_ctr % BD_NSTAGE;
-        bd_wait(P, &S.empty[st], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
-        uint8_t* sp = S.ring + st * BD_STAGE;
-        mbar_arrive_expect_tx(&S.full[st], 2u * BD_KEYS * P.d * 2);
-        for (int kv = 0; kv < 2; ++kv)
+      for (int j = 0; j < nblk; ++j)
+        for (int kv = 0; kv < 2; ++kv) {  // the block's K into one stage, its V into the next
+          const int st = stage_ctr % BD_NSTAGE;
+          bd_wait(P, &S.empty[st], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
+          uint8_t* sp = S.ring + st * BD_STAGE;
+          mbar_arrive_expect_tx(&S.full[st], (uint32_t)BD_KEYS * P.d * 2);
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sp + kv * half + bx * (BD_KEYS * 128), tmap(P, gmap(P, TMB_KV)), bx * 64,
+            tma_load_2d(sp + bx * (BD_KEYS * 128), tmap(P, gmap(P, TMB_KV)), bx * 64,
                         (int)(cache_row(P, l, kv, b, g) + e.lo + j * BD_KEYS), &S.full[st], pol_a);
-        ++stage_ctr;
-      }
+          ++stage_ctr;
+        }
       bd_mark(P, i, 6);
     }
   }
@@ -681,15 +680,15 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
   const int nblk = attn_blocks(e);
   for (int j = 0; j < nblk; ++j) {
     const int st = stage_ctr % BD_NSTAGE;
+    const int st_v = (stage_ctr + 1) % BD_NSTAGE;
     bd_wait(P, &S.full[st], (stage_ctr / BD_NSTAGE) & 1u);
-    ++stage_ctr;
     if (j == 0 && tc == 0) bd_mark(P, idx, 9);
     const uint8_t* kt = S.ring + st * BD_STAGE;
-    const uint8_t* vt = kt + BD_STAGE / 2;
+    const uint8_t* vt = S.ring + st_v * BD_STAGE;
     const int base = e.lo + j * BD_KEYS;
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-      const int k = wc * 8 + pass * 4 + quad;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int k = wc * 16 + pass * 4 + quad;
       float kx[G][8];
 #pragma unroll
       for (int gi = 0; gi < G; ++gi)
@@ -711,16 +710,24 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     cbar_bd();
     // online softmax: warp h owns head h
     if (wc < rep) {
-      const float s0 = sc[wc * BD_KEYS + lane], s1 = sc[wc * BD_KEYS + lane + 32];
-      const float mx = warp_max(fmaxf(s0, s1));
+      float sv[BD_KEYS / 32];
+#pragma unroll
+      for (int u = 0; u < BD_KEYS / 32; ++u) sv[u] = sc[wc * BD_KEYS + lane + 32 * u];
+      float mx = sv[0];
+#pragma unroll
+      for (int u = 1; u < BD_KEYS / 32; ++u) mx = fmaxf(mx, sv[u]);
+      mx = warp_max(mx);
       const float m_old = hs[wc * 3 + 0];
       const float m_new = fmaxf(m_old, mx);
       const float alpha = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
-      const float p0 = s0 == -INFINITY ? 0.f : expf(s0 - m_new);
-      const float p1 = s1 == -INFINITY ? 0.f : expf(s1 - m_new);
-      sc[wc * BD_KEYS + lane] = p0;
-      sc[wc * BD_KEYS + lane + 32] = p1;
-      const float ps = warp_sum(p0 + p1);
+      float psum = 0.f;
+#pragma unroll
+      for (int u = 0; u < BD_KEYS / 32; ++u) {
+        const float pv = sv[u] == -INFINITY ? 0.f : expf(sv[u] - m_new);
+        sc[wc * BD_KEYS + lane + 32 * u] = pv;
+        psum += pv;
+      }
+      const float ps = warp_sum(psum);
       __syncwarp();
       if (lane == 0) {
         hs[wc * 3 + 0] = m_new;
@@ -739,8 +746,10 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
         for (int k = 0; k < DPL; ++k) acc[h][k] *= alpha;
       }
       const int col = lane * DPL, bx = col >> 6, cin = col & 63;
-      const int k0 = wc * 8;
-      const int k1 = e.hi - base < k0 + 8 ? e.hi - base : k0 + 8;
+      const int k0 = wc * (BD_KEYS / 8);
+      const int k1 = e.hi - base < k0 + BD_KEYS / 8 ? e.hi - base : k0 + BD_KEYS / 8;
+      // the block's values are in the next stage
+      bd_wait(P, &S.full[st_v], ((stage_ctr + 1) / BD_NSTAGE) & 1u);
       for (int k = k0; k < k1; ++k) {
         const uint8_t* vr = vt + bx * (BD_KEYS * 128) + k * 128 + ((((cin >> 3) ^ (k & 7))) << 4) + (cin & 7) * 2;
         float vx[DPL];
@@ -761,8 +770,12 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
         }
       }
     }
-    cbar_bd();  // every warp is done with the stage and the probabilities
-    if (tc == 0) mbar_arrive(&S.empty[st]);
+    cbar_bd();  // every warp is done with the stages and the probabilities
+    if (tc == 0) {
+      mbar_arrive(&S.empty[st]);
+      mbar_arrive(&S.empty[st_v]);
+    }
+    stage_ctr += 2;
   }
   if (tc == 0) bd_mark(P, idx, 10);
   // add the eight warps' partial outputs (warp order), then the split's
