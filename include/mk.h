@@ -192,6 +192,20 @@ int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
 int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
                   mk_plan_stats *out);
 
+/* Prefill of `batch` prompts (SURVEY.md-listed variant of the prefill):
+ * prompt b (tokens[b * stride .. b * stride + lens[b])) goes to sequence slot
+ * b of the cache and its last token's logits to logits[b].  Each prompt runs
+ * as mk_prefill does (one persistent launch of the prompt's tiles, then its
+ * LM-head tiles), the prompts back to back on `stream`.
+ *   tokens  device int32 [batch][stride]
+ *   lens    HOST int32 [batch], 1 <= lens[b] <= min(stride, max_ctx)
+ *   batch   1 .. max_batch of the plan
+ *   logits  device float [batch][V]
+ * Argument errors: MK_ERR_INVALID_ARG (nothing launched); device errors are
+ * latched as for mk_prefill. */
+int mk_prefill_batch(mk_plan *plan, const int32_t *tokens, const int32_t *lens, int batch,
+                     int stride, void *kv_cache, float *logits, void *stream);
+
 /* Prefill with the logits of EVERY prompt token (SURVEY.md-listed variant of
  * the prefill: "MegaOps", Abstract, prefill of the dense Llama3/Qwen3
  * decoders).  Same as mk_prefill, except that the final RMSNorm and the LM

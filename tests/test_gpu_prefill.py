@@ -206,3 +206,46 @@ def test_llama3_8b_width_prefill_all_token_logits_sampled():
             _rows_close(got[r:r + 1], ref[None, :])
     finally:
         m.close()
+
+
+def test_prefill_batch_slots():
+    """mk_prefill_batch: three prompts of different lengths into cache slots
+    0..2: each slot's keys/values and last-token logits against the oracle,
+    then one batched decode step over the three slots against the oracle's
+    prefill of each prompt plus the decoded token."""
+    cfg = PF_SMALL
+    m = PfModel(cfg, max_ctx=320, seed=8)
+    try:
+        m.kv = torch.zeros(synth.kv_cache_shape(cfg, 3, 320), dtype=torch.bfloat16, device=m.dev)
+        m.plan.close()
+        m.plan = mk.Plan(cfg, m.w, 3, 320)
+        lens = [200, 7, 129]
+        stride = 256
+        toks = np.zeros((3, stride), dtype=np.int32)
+        seqs = [synth.make_tokens(n, cfg.vocab, seed=50 + b).numpy() for b, n in enumerate(lens)]
+        for b, sq in enumerate(seqs):
+            toks[b, :len(sq)] = sq
+        t = torch.from_numpy(toks).to(m.dev)
+        lg = torch.full((3, cfg.vocab), float("nan"), device=m.dev)
+        m.plan.prefill_batch(t, lens, m.kv, lg)
+        assert m.plan.status() == mk.MK_OK
+        got = lg.cpu().numpy()
+        kv = oracle.widen_bf16(synth.bf16_bits(m.kv))
+        for b, sq in enumerate(seqs):
+            ref, K, V = oracle.prefill(cfg, synth.LazyBits(m.w), sq)
+            _rows_close(got[b:b + 1], ref[None, :])
+            _kv_close(f"K{b}", kv[:, 0, b, :, :lens[b], :], K)
+            _kv_close(f"V{b}", kv[:, 1, b, :, :lens[b], :], V)
+        nxt = synth.make_tokens(3, cfg.vocab, seed=60).numpy()
+        dl = torch.empty((3, cfg.vocab), device=m.dev)
+        m.plan.decode_step(torch.from_numpy(nxt.astype(np.int32)).to(m.dev),
+                           torch.tensor(lens, dtype=torch.int32, device=m.dev), m.kv, dl)
+        assert m.plan.status() == mk.MK_OK
+        dec = dl.cpu().numpy()
+        for b, sq in enumerate(seqs):
+            ref, _, _ = oracle.prefill(cfg, synth.LazyBits(m.w), np.concatenate([sq, nxt[b:b + 1]]))
+            _rows_close(dec[b:b + 1], ref[None, :])
+        with pytest.raises(mk.MkError):
+            m.plan.prefill_batch(t, [200, 0, 5], m.kv, lg)
+    finally:
+        m.close()

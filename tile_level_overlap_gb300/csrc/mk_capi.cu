@@ -770,6 +770,34 @@ int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logi
   return prefill_lm(p, tokens, len, kv, logits, st);
 }
 
+int mk_prefill_batch(mk_plan* p, const int32_t* tokens, const int32_t* lens, int batch, int stride,
+                     void* kv, float* logits, void* stream) {
+  if (!p || !tokens || !lens || !kv || !logits || batch < 1 || batch > p->max_batch ||
+      stride < 1 || !aligned16(kv))
+    return MK_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b)
+    if (lens[b] < 1 || lens[b] > p->hp.max_ctx || lens[b] > stride) return MK_ERR_INVALID_ARG;
+  if (p->latched) return p->latched;
+  cudaStream_t st = (cudaStream_t)stream;
+  int rc;
+  if ((rc = prefill_init(p)) != MK_OK || (rc = prefill_bind_kv(p, kv, st)) != MK_OK) return rc;
+  const int V = p->hp.cfg.vocab;
+  for (int b = 0; b < batch; ++b) {
+    // one persistent launch per prompt, into its own cache slot, then its
+    // last token's LM head
+    PfParams k = p->pf.base;
+    k.tokens = tokens + (size_t)b * stride;
+    k.S = lens[b];
+    k.slot = b;
+    k.kv = (uint16_t*)kv;
+    k.mode = MODE_MEGA;
+    k.wait_limit_ns = p->wait_limit_ns;
+    MK_CUDA(pf_launch_mega(k, p->n_sms, st));
+    if ((rc = prefill_lm(p, k.tokens, lens[b], kv, logits + (size_t)b * V, st)) != MK_OK) return rc;
+  }
+  return MK_OK;
+}
+
 int mk_prefill_logits(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits,
                       void* stream) {
   int rc = prefill_args(p, tokens, len, kv, logits);

@@ -86,7 +86,8 @@ struct PfParams {
   uint16_t* ao;             // attention outputs [2][rows][n_q * d]
   uint16_t* act;            // SwiGLU outputs [2][rows][F]
   int plane_rows;           // rows of one plane (token blocks x 128)
-  uint16_t* kv;             // caller's KV cache (sequence slot 0 is written)
+  uint16_t* kv;             // caller's KV cache
+  int slot;                 // the sequence slot this prompt's keys and values go to
   const float2* rope;       // (cos, sin) [max_ctx][d / 2]
   uint32_t* bars;
   uint32_t* ctl;

@@ -217,7 +217,7 @@ __device__ __forceinline__ PfGemm pf_gemm(const PfParams& P, const Instr& in) {
 }
 
 __device__ __forceinline__ int kv_row(const PfParams& P, int l, int kv, int g) {
-  return (((l * 2 + kv) * P.max_batch + 0) * P.nkv + g) * P.max_ctx;
+  return (((l * 2 + kv) * P.max_batch + P.slot) * P.nkv + g) * P.max_ctx;
 }
 
 // ---------------------------------------------------------------- producer

@@ -31,7 +31,7 @@ EXPORTED = [
     "mk_decode_step_host", "mk_prefill", "mk_run_per_op", "mk_status", "mk_plan_reset",
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
-    "mk_plan_set_lm_mode", "mk_decode_steps", "mk_prefill_logits",
+    "mk_plan_set_lm_mode", "mk_decode_steps", "mk_prefill_logits", "mk_prefill_batch",
 ]
 
 
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
     L.mk_plan_set_lm_mode.argtypes = [vp, ctypes.c_int]
     L.mk_decode_steps.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp]
     L.mk_prefill_logits.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp]
+    L.mk_prefill_batch.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int,
+                                   vp, vp, vp]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
     L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -242,6 +244,14 @@ class Plan:
     def prefill(self, tokens, kv, logits, stream=None) -> None:
         _check(lib().mk_prefill(self.h, _ptr(tokens), int(tokens.numel()), _ptr(kv), _ptr(logits),
                                 _stream_ptr(stream)), "mk_prefill")
+
+    def prefill_batch(self, tokens, lens, kv, logits, stream=None) -> None:
+        """mk_prefill_batch: tokens device [batch, stride], lens a list of
+        prompt lengths, logits device [batch, V]; prompt b to cache slot b."""
+        n = len(lens)
+        arr = (ctypes.c_int32 * n)(*[int(v) for v in lens])
+        _check(lib().mk_prefill_batch(self.h, _ptr(tokens), arr, n, int(tokens.shape[1]), _ptr(kv),
+                                      _ptr(logits), _stream_ptr(stream)), "mk_prefill_batch")
 
     def prefill_logits(self, tokens, kv, logits, stream=None) -> None:
         """mk_prefill_logits: the prompt's logits for every token, [len, V]."""
