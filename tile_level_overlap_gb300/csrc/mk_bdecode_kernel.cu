@@ -750,6 +750,7 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
       const int k1 = e.hi - base < k0 + BD_KEYS / 8 ? e.hi - base : k0 + BD_KEYS / 8;
       // the block's values are in the next stage
       bd_wait(P, &S.full[st_v], ((stage_ctr + 1) / BD_NSTAGE) & 1u);
+#pragma unroll 4
       for (int k = k0; k < k1; ++k) {
         const uint8_t* vr = vt + bx * (BD_KEYS * 128) + k * 128 + ((((cin >> 3) ^ (k & 7))) << 4) + (cin & 7) * 2;
         float vx[DPL];

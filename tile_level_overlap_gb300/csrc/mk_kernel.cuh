@@ -911,6 +911,7 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
       const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
       const uint8_t* stage = ring_acquire(P, S, R);
       const float* ph = sc + (hg * HPW) * smax + c0;
+#pragma unroll 4
       for (int j = kw; j < cnt; j += KS) {
         float vx[DPL];
         if constexpr (DPL == 4) {
