@@ -694,18 +694,24 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
       for (int gi = 0; gi < G; ++gi)
         widen8(*reinterpret_cast<const uint4*>(kt + gi * (BD_KEYS * 128) + k * 128 + ((sub ^ (k & 7)) << 4)),
                kx[gi]);
+      // per head two partial sums (the two halves of the lane's elements),
+      // then one multi-value sum over the key's 8 lanes for the four heads
+      float a[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        float a = 0.f;
+        float pa[2] = {0.f, 0.f};
 #pragma unroll
         for (int gi = 0; gi < G; ++gi)
 #pragma unroll
-          for (int t = 0; t < 8; ++t) a = fmaf(qv[h][gi][t], kx[gi][t], a);
-        a += __shfl_xor_sync(0xffffffffu, a, 4);
-        a += __shfl_xor_sync(0xffffffffu, a, 2);
-        a += __shfl_xor_sync(0xffffffffu, a, 1);
-        if (sub == 0 && h < rep) sc[h * BD_KEYS + k] = base + k < e.hi ? a * scale : -INFINITY;
+          for (int t = 0; t < 8; ++t) {
+            const int half = (gi * 8 + t) >= 4 * G;
+            pa[half] = fmaf(qv[h][gi][t], kx[gi][t], pa[half]);
+          }
+        a[h] = pa[0] + pa[1];
       }
+      const float tot = sum8_multi4(a, lane);
+      const int hh = (sub >> 1) & 3;
+      if ((sub & 1) == 0 && hh < rep) sc[hh * BD_KEYS + k] = base + k < e.hi ? tot * scale : -INFINITY;
     }
     cbar_bd();
     // online softmax: warp h owns head h
