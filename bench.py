@@ -438,6 +438,30 @@ def run_ours(args):
                      "tokens_per_s": MULTI_STEPS / (ms_launch / 1e3),
                      "positions": [CONTEXT - MULTI_STEPS, CONTEXT - 1]}
 
+    # chunked prefill mixed with decode (tensor-core batched plans): the last
+    # half of the columns become a prompt chunk of one slot (consecutive
+    # positions before that slot's context), the rest decode as before
+    mixed = None
+    if plan.stats().decode_path == 1 and BATCH >= 4:
+        half = BATCH // 2
+        cslot = BATCH - 1
+        cpos = pos_list[cslot] - half
+        slots_m = torch.tensor(list(range(BATCH - half)) + [cslot] * half, dtype=torch.int32, device=dev)
+        pos_m = torch.tensor(pos_list[:BATCH - half] + [cpos + i for i in range(half)],
+                             dtype=torch.int32, device=dev)
+
+        def mixed_step():
+            plan.decode_step_slots(tokens, pos_m, slots_m, kv, logits, stream=stream)
+
+        for _ in range(max(1, args.warmup // 2)):
+            mixed_step()
+        ms_mixed = timed(mixed_step, args.steps) / args.steps
+        rc = plan.status(stream)
+        if rc != mk.MK_OK:
+            raise RuntimeError(f"device status {rc}")
+        mixed = {"decode_columns": BATCH - half, "chunk_tokens": half, "ms_per_step": ms_mixed,
+                 "tokens_per_s": BATCH / (ms_mixed / 1e3)}
+
     # prefill of a 2048-token prompt into sequence slot 0 (after the decode
     # timing, since it rewrites that cache slot)
     prefill = None
@@ -518,6 +542,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "prefill": prefill,
         "multi_step": multi,
+        "mixed_chunk": mixed,
     }
     if world == 1 and not args.no_cpu_baseline:
         sample_run = OracleSample(cfg, args.ref_layers, pos_list)

@@ -218,6 +218,27 @@ int mk_prefill_batch(mk_plan *plan, const int32_t *tokens, const int32_t *lens, 
 int mk_prefill_logits(mk_plan *plan, const int32_t *tokens, int len, void *kv_cache, float *logits,
                       void *stream);
 
+/* Chunked prefill mixed with decode in ONE persistent launch ("Lecture 112"
+ * summary, Key takeaways: one queue with symbolic extents serves both; the
+ * MegaOps Abstract's decode and prefill of the same decoder).  A decode step
+ * whose columns name their cache slot: column c is the token tokens[c] of the
+ * sequence in slot slots[c] at position positions[c].  Several columns of one
+ * slot at consecutive positions are a prompt chunk: every column's key and
+ * value are in the cache before any column's attention reads it (the
+ * attention tiles wait on the whole projection), so column c attends to the
+ * slot's keys 0..positions[c], its own chunk's earlier tokens included.
+ * Columns of other slots are ordinary decode steps.
+ *   slots   device int32 [batch], 0 <= slots[c] < max_batch (else
+ *           MK_ERR_BOUNDS is latched); no two columns may share
+ *           (slot, position)
+ *   tokens, positions, batch, kv_cache, logits: as mk_decode_step (logits
+ *           [batch][V]: every column's, the chunk's included)
+ * Plans of the tensor-core batched path only (mk_plan_stats.decode_path = 1;
+ * others: MK_ERR_UNSUPPORTED). */
+int mk_decode_step_slots(mk_plan *plan, const int32_t *tokens, const int32_t *positions,
+                         const int32_t *slots, int batch, void *kv_cache, float *logits,
+                         void *stream);
+
 /* Greedy decode of n_steps tokens of one sequence in ONE persistent launch
  * (the host stays out of the loop: "Lecture 112" summary, Practical
  * implications).  Step s (0 <= s < n_steps) is the decode step of

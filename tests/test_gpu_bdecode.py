@@ -190,3 +190,51 @@ def test_qwen3_8b_width_batch32_ragged():
         m.check(tokens, positions)
     finally:
         m.close()
+
+
+def test_prompt_chunk_mixed_with_decode(small):
+    """mk_decode_step_slots: a 6-token prompt chunk of slot 0 (positions
+    p0..p0+5) and decode tokens of slots 1..5 in one persistent launch.  The
+    oracle runs the chunk token by token (each step appending its key/value)
+    and the decode columns as one step on the cache before the launch."""
+    cfg = small.cfg
+    p0, chunk = 150, 6
+    dec_slots = [1, 2, 3, 4, 5]
+    dec_pos = [10, 299, 0, 77, 128]
+    toks = synth.make_tokens(chunk + len(dec_slots), cfg.vocab, seed=91).numpy()
+    slots = np.array([0] * chunk + dec_slots, dtype=np.int32)
+    pos = np.array([p0 + i for i in range(chunk)] + dec_pos, dtype=np.int32)
+    kv_before = synth.bf16_bits(small.kv)
+    n = len(toks)
+    lg = torch.full((n, cfg.vocab), float("nan"), device=small.dev)
+    small.plan.decode_step_slots(torch.from_numpy(toks.astype(np.int32)).to(small.dev),
+                                 torch.from_numpy(pos).to(small.dev),
+                                 torch.from_numpy(slots).to(small.dev), small.kv, lg)
+    rc = small.plan.status()
+    assert rc == mk.MK_OK, mk.lib().mk_status_string(rc)
+    got = lg.cpu().numpy()
+    w = synth.LazyBits(small.w)
+    # the chunk, token by token, on slot 0's cache
+    kv0 = kv_before[:, :, 0:1].copy()
+    for i in range(chunk):
+        ref, knew, vnew = oracle.decode_step(cfg, w, toks[i:i + 1], [p0 + i], kv0)
+        _rows_close(got[i:i + 1], ref)
+        kb = torch.from_numpy(np.ascontiguousarray(knew[:, 0])).to(torch.bfloat16).view(torch.int16).numpy()
+        vb = torch.from_numpy(np.ascontiguousarray(vnew[:, 0])).to(torch.bfloat16).view(torch.int16).numpy()
+        kv0[:, 0, 0, :, p0 + i, :] = kb.view(kv0.dtype)
+        kv0[:, 1, 0, :, p0 + i, :] = vb.view(kv0.dtype)
+    after = oracle.widen_bf16(synth.bf16_bits(small.kv))
+    np.testing.assert_allclose(after[:, :, 0, :, p0:p0 + chunk], oracle.widen_bf16(kv0)[:, :, 0, :, p0:p0 + chunk],
+                               rtol=2.0 ** -6, atol=2e-2)
+    # the decode columns: one step of slots 1..5 (sequence b in slot b)
+    kvd = kv_before[:, :, 1:6].copy()
+    ref, _, _ = oracle.decode_step(cfg, w, toks[chunk:], dec_pos, kvd)
+    _rows_close(got[chunk:], ref)
+    # a slot outside the plan latches a bounds error
+    small.plan.reset()
+    bad = torch.tensor([0, 12], dtype=torch.int32, device=small.dev)
+    small.plan.decode_step_slots(torch.tensor([1, 2], dtype=torch.int32, device=small.dev),
+                                 torch.tensor([5, 6], dtype=torch.int32, device=small.dev), bad,
+                                 small.kv, lg[:2])
+    assert small.plan.status() == mk.MK_ERR_BOUNDS
+    small.plan.reset()

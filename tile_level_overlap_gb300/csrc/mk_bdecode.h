@@ -102,6 +102,7 @@ struct BdParams {
   uint32_t n_instr;
   const int32_t* tokens;
   const int32_t* positions;
+  const int32_t* slots;     // [B] cache slot of each column, or null (column b uses slot b)
   float* logits;            // [B][V]
   int B;
   int mode;

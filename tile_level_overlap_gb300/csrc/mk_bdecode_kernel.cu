@@ -49,8 +49,8 @@ struct BdSmem {
   static constexpr int n_mbar = 2 * BD_NSTAGE + 2 * NISLOT + 4;
   static constexpr int islot = bars + n_mbar * 8;
   static constexpr int flags = islot + NISLOT * 48;  // [16] u32
-  static constexpr int seq = flags + 16 * 4;         // positions[BD_NMAX], tokens[BD_NMAX]
-  static constexpr int total = seq + 2 * BD_NMAX * 4;
+  static constexpr int seq = flags + 16 * 4;         // positions, tokens, cache slots [BD_NMAX] each
+  static constexpr int total = seq + 3 * BD_NMAX * 4;
 };
 static_assert(BdSmem::total <= 227 * 1024, "batched decode shared memory budget");
 static_assert(BdSmem::scratch % 1024 == 0, "ring stages stay 1024-aligned");
@@ -63,7 +63,7 @@ struct BdSh {
   uint64_t *full, *empty, *ifull, *iempty, *accf, *acce;
   uint8_t* islot;
   volatile uint32_t* flags;
-  int32_t *pos, *tok;
+  int32_t *pos, *tok, *slot;
 };
 
 __device__ __forceinline__ BdSh bd_map(uint8_t* base) {
@@ -85,6 +85,7 @@ __device__ __forceinline__ BdSh bd_map(uint8_t* base) {
   s.flags = reinterpret_cast<volatile uint32_t*>(base + BdSmem::flags);
   s.pos = reinterpret_cast<int32_t*>(base + BdSmem::seq);
   s.tok = s.pos + BD_NMAX;
+  s.slot = s.tok + BD_NMAX;
   return s;
 }
 
@@ -239,8 +240,9 @@ __device__ __forceinline__ int bd_stages(const BdParams& P, const BdSh& S, const
   return 0;
 }
 
-__device__ __forceinline__ size_t cache_row(const BdParams& P, int l, int kv, int b, int g) {
-  return ((((size_t)l * 2 + kv) * P.max_batch + b) * P.nkv + g) * (size_t)P.max_ctx;
+// First cache row of (layer l, K or V, cache slot, kv head g).
+__device__ __forceinline__ size_t cache_row(const BdParams& P, int l, int kv, int slot, int g) {
+  return ((((size_t)l * 2 + kv) * P.max_batch + slot) * P.nkv + g) * (size_t)P.max_ctx;
 }
 
 // ---------------------------------------------------------------- producer
@@ -352,7 +354,7 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
           mbar_arrive_expect_tx(&S.full[st], (uint32_t)BD_KEYS * P.d * 2);
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(sp + bx * (BD_KEYS * 128), tmap(P, gmap(P, TMB_KV)), bx * 64,
-                        (int)(cache_row(P, l, kv, b, g) + e.lo + j * BD_KEYS), &S.full[st], pol_a);
+                        (int)(cache_row(P, l, kv, S.slot[b], g) + e.lo + j * BD_KEYS), &S.full[st], pol_a);
           ++stage_ctr;
         }
       bd_mark(P, i, 6);
@@ -575,7 +577,7 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
         for (int k = 0; k < 16; ++k) {
           const int b = b0 + k;
           if (b < B)
-            P.kv[(cache_row(P, l, 1, b, g) + S.pos[b]) * d + dim] =
+            P.kv[(cache_row(P, l, 1, S.slot[b], g) + S.pos[b]) * d + dim] =
                 __bfloat16_as_ushort(__float2bfloat16_rn(y[k] * S.rinv[b]));
         }
         break;
@@ -619,7 +621,7 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
           P.q[(size_t)b * qd + f + i + half] = r2;
         } else {
           const int g = (f - qd) / d;
-          uint16_t* kr = P.kv + (cache_row(P, l, 0, b, g) + S.pos[b]) * d;
+          uint16_t* kr = P.kv + (cache_row(P, l, 0, S.slot[b], g) + S.pos[b]) * d;
           kr[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r1));
           kr[i + half] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
         }
@@ -980,8 +982,16 @@ __global__ void __launch_bounds__(BD_THREADS, 1) mk_bdecode_kernel(const __grid_
       if (blockIdx.x == 0) bd_error(P, MK_ERR_BOUNDS, threadIdx.x);
       pos = 0;
     }
+    // the column's cache slot: its own index, or the caller's map (several
+    // columns of one slot at consecutive positions: a prompt chunk)
+    int slot = !live ? 0 : P.slots ? P.slots[threadIdx.x] : (int)threadIdx.x;
+    if (slot < 0 || slot >= P.max_batch) {
+      if (blockIdx.x == 0) bd_error(P, MK_ERR_BOUNDS, threadIdx.x);
+      slot = 0;
+    }
     S.pos[threadIdx.x] = pos;
     S.tok[threadIdx.x] = live ? P.tokens[threadIdx.x] : 0;
+    S.slot[threadIdx.x] = slot;
   }
   if (warp == 1) tmem_alloc(reinterpret_cast<uint32_t*>(const_cast<uint32_t*>(&S.flags[BF_TMEM])), 64);
   tc_fence_before();

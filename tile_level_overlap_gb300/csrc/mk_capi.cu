@@ -600,6 +600,20 @@ int mk_decode_steps(mk_plan* p, const int32_t* token, const int32_t* position, i
   return cuda_err(p->kv.mega_steps(k, ctas, st));
 }
 
+int mk_decode_step_slots(mk_plan* p, const int32_t* tokens, const int32_t* positions,
+                         const int32_t* slots, int batch, void* kv, float* logits, void* stream) {
+  int rc = check_step(p, tokens, positions, batch, kv, logits);
+  if (rc != MK_OK) return rc;
+  if (!slots) return MK_ERR_INVALID_ARG;
+  if (!p->bd.on) return MK_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
+  if ((rc = bd_bind_kv(p, kv, st)) != MK_OK) return rc;
+  BdParams k = bd_params(p, tokens, positions, batch, kv, logits);
+  k.slots = slots;
+  return cuda_err(bd_launch_mega(k, ctas, st));
+}
+
 int mk_plan_set_lm_mode(mk_plan* p, int mode) {
   if (!p || (mode != MK_LM_FUSED && mode != MK_LM_SEPARATE)) return MK_ERR_INVALID_ARG;
   p->lm_separate = mode == MK_LM_SEPARATE;

@@ -32,6 +32,7 @@ EXPORTED = [
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
     "mk_plan_set_lm_mode", "mk_decode_steps", "mk_prefill_logits", "mk_prefill_batch",
+    "mk_decode_step_slots",
 ]
 
 
@@ -93,6 +94,7 @@ def lib() -> ctypes.CDLL:
     L.mk_plan_set_lm_mode.argtypes = [vp, ctypes.c_int]
     L.mk_decode_steps.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp]
     L.mk_prefill_logits.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp]
+    L.mk_decode_step_slots.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, vp]
     L.mk_prefill_batch.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int,
                                    vp, vp, vp]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
@@ -235,6 +237,13 @@ class Plan:
         _check(lib().mk_decode_steps(self.h, _ptr(token), _ptr(position), int(n_steps), _ptr(kv),
                                      _ptr(out_tokens), _ptr(logits), _stream_ptr(stream)),
                "mk_decode_steps")
+
+    def decode_step_slots(self, tokens, positions, slots, kv, logits, stream=None) -> None:
+        """mk_decode_step_slots: column c is tokens[c] of cache slot slots[c] at
+        positions[c] (a prompt chunk = several columns of one slot)."""
+        _check(lib().mk_decode_step_slots(self.h, _ptr(tokens), _ptr(positions), _ptr(slots),
+                                          int(tokens.numel()), _ptr(kv), _ptr(logits),
+                                          _stream_ptr(stream)), "mk_decode_step_slots")
 
     def decode_step_host(self, tokens, positions, kv, logits, stream=None) -> int:
         """tokens/positions/logits are CPU tensors (pinned for speed)."""
