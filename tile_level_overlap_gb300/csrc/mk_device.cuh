@@ -129,6 +129,18 @@ __device__ __forceinline__ float dot8(const uint4 w, const float* x, float a) {
   return a;
 }
 
+// Warp-level tensor-core product c += A (16 x 16, rows g and g + 8 held as
+// a0..a3) x B (16 x 8, b0..b1), bf16 operands, f32 accumulators; the standard
+// m16n8k16 fragment layout (lane = 4 g + t).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Sums of four values over the 8 lanes of an aligned lane group (xor 4, 2, 1),
 // as a multi-value butterfly: 4 shuffles instead of 12.  Afterwards the lane
 // holds the total of value ((lane & 7) >> 1), in both lanes of each pair.

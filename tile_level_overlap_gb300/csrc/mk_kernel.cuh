@@ -829,43 +829,96 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
         P.kv[kv_offset(P, l, 1, b, g, e.pos) + i] = __bfloat16_as_ushort(__float2bfloat16_rn(vn[i]));
       }
 
-    // scores of cached keys: 8 lanes per key, lane `sub` holds element groups
-    // {sub, sub + 8, ...} of 8 (conflict-free 16-byte shared loads)
-    constexpr int G = D / 64;  // 8-element groups per lane
     const float scale = 1.0f / sqrtf((float)D);
-    const int sub = lane & 7, quad = lane >> 3;
-    float qv[REP][G][8];
-#pragma unroll
-    for (int h = 0; h < REP; ++h)
-#pragma unroll
-      for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) qv[h][gi][k] = qs[h * D + (sub + 8 * gi) * 8 + k];
     const int kps = (int)(STAGE_BYTES / (D * 2));
-    for (int c0 = 0; c0 < e.nc; c0 += kps) {
-      const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
-      const uint8_t* stage = ring_acquire(P, S, R);
-      for (int j0 = w * 4; j0 < cnt; j0 += NW * 4) {
-        const int j = j0 + quad;
-        const bool ok = j < cnt;
-        const uint4* krow = reinterpret_cast<const uint4*>(stage + (size_t)(ok ? j : 0) * D * 2);
-        float kx[G][8];
+    if constexpr (REP <= 4) {
+      // Scores of cached keys on the tensor cores, 8 keys per m16n8k16 product
+      // per warp: A rows r < REP hold q of head r rounded to bf16, rows REP..
+      // 2 REP - 1 the bf16 of its remainder (hi + lo keeps q's float32
+      // precision against the exact bf16 keys), the other rows zero.  The
+      // reduction index is permuted so that lane t's four values of k-step
+      // 2 s + u are dimensions 32 s + 8 t + 4 u .. + 3: one 16-byte load per key
+      // row gives two k-steps of B.
+      constexpr int KSTEPS = D / 16;
+      const int g = lane >> 2, tq = lane & 3;
+      uint32_t af[KSTEPS][2];
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi) widen8(krow[sub + 8 * gi], kx[gi]);
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int base = 32 * (ks >> 1) + 8 * tq + 4 * (ks & 1);
 #pragma unroll
-        for (int h = 0; h < REP; ++h) {
-          float a = 0.f;
+        for (int r = 0; r < 2; ++r) {
+          uint32_t hv[2];
 #pragma unroll
-          for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a = fmaf(qv[h][gi][k], kx[gi][k], a);
-          a += __shfl_xor_sync(0xffffffffu, a, 4);
-          a += __shfl_xor_sync(0xffffffffu, a, 2);
-          a += __shfl_xor_sync(0xffffffffu, a, 1);
-          if (ok && sub == 0) sc[h * smax + c0 + j] = a * scale;
+          for (int x = 0; x < 2; ++x) {
+            const float qf = g < 2 * REP ? qs[(g % REP) * D + base + 2 * r + x] : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(qf);
+            const __nv_bfloat16 v = g < REP ? hi : __float2bfloat16_rn(qf - __bfloat162float(hi));
+            hv[x] = (uint32_t)__bfloat16_as_ushort(v);
+          }
+          af[ks][r] = hv[0] | (hv[1] << 16);
         }
       }
-      ring_release(S, R);
+      for (int c0 = 0; c0 < e.nc; c0 += kps) {
+        const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
+        const uint8_t* stage = ring_acquire(P, S, R);
+        const int nblk = (cnt + 7) >> 3;
+        for (int nb = w; nb < nblk; nb += NW) {
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint8_t* row = stage + (size_t)(nb * 8 + g) * D * 2 + tq * 16;
+#pragma unroll
+          for (int s2 = 0; s2 < KSTEPS / 2; ++s2) {
+            const uint4 kk = *reinterpret_cast<const uint4*>(row + s2 * 64);
+            mma_bf16_16816(c, af[2 * s2][0], 0u, af[2 * s2][1], 0u, kk.x, kk.y);
+            mma_bf16_16816(c, af[2 * s2 + 1][0], 0u, af[2 * s2 + 1][1], 0u, kk.z, kk.w);
+          }
+          // row g (hi) + row g + REP (lo): lanes 4 REP apart
+          const float s0 = c[0] + __shfl_xor_sync(0xffffffffu, c[0], 4 * REP);
+          const float s1 = c[1] + __shfl_xor_sync(0xffffffffu, c[1], 4 * REP);
+          const int j = nb * 8 + 2 * tq;
+          if (g < REP) {
+            if (j < cnt) sc[g * smax + c0 + j] = s0 * scale;
+            if (j + 1 < cnt) sc[g * smax + c0 + j + 1] = s1 * scale;
+          }
+        }
+        ring_release(S, R);
+      }
+    } else {
+      // scores of cached keys: 8 lanes per key, lane `sub` holds element groups
+      // {sub, sub + 8, ...} of 8 (conflict-free 16-byte shared loads)
+      constexpr int G = D / 64;  // 8-element groups per lane
+      const int sub = lane & 7, quad = lane >> 3;
+      float qv[REP][G][8];
+#pragma unroll
+      for (int h = 0; h < REP; ++h)
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) qv[h][gi][k] = qs[h * D + (sub + 8 * gi) * 8 + k];
+      for (int c0 = 0; c0 < e.nc; c0 += kps) {
+        const int cnt = e.nc - c0 < kps ? e.nc - c0 : kps;
+        const uint8_t* stage = ring_acquire(P, S, R);
+        for (int j0 = w * 4; j0 < cnt; j0 += NW * 4) {
+          const int j = j0 + quad;
+          const bool ok = j < cnt;
+          const uint4* krow = reinterpret_cast<const uint4*>(stage + (size_t)(ok ? j : 0) * D * 2);
+          float kx[G][8];
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) widen8(krow[sub + 8 * gi], kx[gi]);
+#pragma unroll
+          for (int h = 0; h < REP; ++h) {
+            float a = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+              for (int k = 0; k < 8; ++k) a = fmaf(qv[h][gi][k], kx[gi][k], a);
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            if (ok && sub == 0) sc[h * smax + c0 + j] = a * scale;
+          }
+        }
+        ring_release(S, R);
+      }
     }
     if (e.has_new && w < rep) {
       float a = 0.f;
