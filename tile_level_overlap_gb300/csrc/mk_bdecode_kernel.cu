@@ -646,28 +646,37 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
   const int tc = threadIdx.x - 64, lane = tc & 31, wc = tc >> 5;
   const int b = (int)in.a0, g = (int)in.a1, s = (int)in.a2, rep = P.rep;
   const int qd = P.nq * D;
-  constexpr int G = D / 64;    // 8-column groups per lane in the score pass
   constexpr int DPL = D / 32;  // output columns per lane in P V
   const float scale = 1.0f / sqrtf((float)D);
   float* sc = S.sc;  // [rep][BD_KEYS]
   float* hs = S.hs;  // [rep] x {m, l, alpha}
-  const int sub = lane & 7, quad = lane >> 3;
-  float qv[4][G][8];
+  // Scores on the tensor cores, 8 keys per m16n8k16 product: A rows r < rep
+  // hold q of head r rounded to bf16, rows rep .. 2 rep - 1 the bf16 of its
+  // remainder (hi + lo keeps q's float32 precision against the exact bf16
+  // keys), the other rows zero.  The reduction index is permuted so that lane
+  // t's four values of k-step 2 s + u are dimensions 32 s + 8 t + 4 u .. + 3:
+  // one 16-byte load per key row gives two k-steps of B.
+  constexpr int KSTEPS = D / 16;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int hq = gq < rep ? gq : gq - rep;
+  uint32_t af[KSTEPS][2];
 #pragma unroll
-  for (int h = 0; h < 4; ++h)
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gq < 2 * rep)
+      u = __ldcg(reinterpret_cast<const float4*>(P.q + (size_t)b * qd + (size_t)(g * rep + hq) * D +
+                                                 32 * (ks >> 1) + 8 * tq + 4 * (ks & 1)));
+    const float f[4] = {u.x, u.y, u.z, u.w};
+    uint32_t hv[4];
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-      if (h < rep) {
-        const float* qp = P.q + (size_t)b * qd + (size_t)(g * rep + h) * D + (sub + 8 * gi) * 8;
-        const float4 u = __ldcg(reinterpret_cast<const float4*>(qp));
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(qp + 4));
-        qv[h][gi][0] = u.x; qv[h][gi][1] = u.y; qv[h][gi][2] = u.z; qv[h][gi][3] = u.w;
-        qv[h][gi][4] = v.x; qv[h][gi][5] = v.y; qv[h][gi][6] = v.z; qv[h][gi][7] = v.w;
-      } else {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) qv[h][gi][t] = 0.f;
-      }
+    for (int x = 0; x < 4; ++x) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(f[x]);
+      const __nv_bfloat16 v = gq < rep ? hi : __float2bfloat16_rn(f[x] - __bfloat162float(hi));
+      hv[x] = (uint32_t)__bfloat16_as_ushort(v);
     }
+    af[ks][0] = hv[0] | (hv[1] << 16);
+    af[ks][1] = hv[2] | (hv[3] << 16);
+  }
   if (tc < rep) {
     hs[tc * 3 + 0] = -INFINITY;
     hs[tc * 3 + 1] = 0.f;
@@ -689,31 +698,27 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     const uint8_t* vt = S.ring + st_v * BD_STAGE;
     const int base = e.lo + j * BD_KEYS;
 #pragma unroll
-    for (int pass = 0; pass < 4; ++pass) {
-      const int k = wc * 16 + pass * 4 + quad;
-      float kx[G][8];
+    for (int nn = 0; nn < 2; ++nn) {
+      // keys 16 wc + 8 nn .. + 7: row gq of this product; the K block is
+      // [D / 64 halves][BD_KEYS][64] with 16-byte chunk c of key k at c ^ (k & 7)
+      const int kr = wc * 16 + nn * 8 + gq;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int gi = 0; gi < G; ++gi)
-        widen8(*reinterpret_cast<const uint4*>(kt + gi * (BD_KEYS * 128) + k * 128 + ((sub ^ (k & 7)) << 4)),
-               kx[gi]);
-      // per head two partial sums (the two halves of the lane's elements),
-      // then one multi-value sum over the key's 8 lanes for the four heads
-      float a[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float pa[2] = {0.f, 0.f};
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int half = (gi * 8 + t) >= 4 * G;
-            pa[half] = fmaf(qv[h][gi][t], kx[gi][t], pa[half]);
-          }
-        a[h] = pa[0] + pa[1];
+      for (int s2 = 0; s2 < KSTEPS / 2; ++s2) {
+        const int chunk = 4 * (s2 & 1) + tq;
+        const uint4 kk = *reinterpret_cast<const uint4*>(kt + (s2 >> 1) * (BD_KEYS * 128) + kr * 128 +
+                                                         ((chunk ^ (kr & 7)) << 4));
+        mma_bf16_16816(c, af[2 * s2][0], 0u, af[2 * s2][1], 0u, kk.x, kk.y);
+        mma_bf16_16816(c, af[2 * s2 + 1][0], 0u, af[2 * s2 + 1][1], 0u, kk.z, kk.w);
       }
-      const float tot = sum8_multi4(a, lane);
-      const int hh = (sub >> 1) & 3;
-      if ((sub & 1) == 0 && hh < rep) sc[hh * BD_KEYS + k] = base + k < e.hi ? tot * scale : -INFINITY;
+      // row gq (hi) + row gq + rep (lo): lanes 4 rep apart
+      const float s0 = c[0] + __shfl_xor_sync(0xffffffffu, c[0], 4 * rep);
+      const float s1 = c[1] + __shfl_xor_sync(0xffffffffu, c[1], 4 * rep);
+      const int k = wc * 16 + nn * 8 + 2 * tq;
+      if (gq < rep) {
+        sc[gq * BD_KEYS + k] = base + k < e.hi ? s0 * scale : -INFINITY;
+        sc[gq * BD_KEYS + k + 1] = base + k + 1 < e.hi ? s1 * scale : -INFINITY;
+      }
     }
     cbar_bd();
     // online softmax: warp h owns head h
