@@ -210,6 +210,24 @@ def test_toy_qk_norm_decode():
         m.close()
 
 
+@pytest.mark.parametrize("nq,nkv,d", [(4, 4, 64), (8, 1, 64), (4, 2, 128), (4, 1, 128), (8, 8, 128)])
+def test_head_layouts_decode(nq, nkv, d):
+    """1, 8, 2 and 4 query heads per kv head at both head sizes: the attention
+    tile's tensor-core score rows (q of each head as bf16 hi and lo rows) for up
+    to 4 heads and its CUDA-core scores for 8, at positions whose splits end
+    inside an 8-key product (a few keys per split)."""
+    cfg = synth.TOY_1L.replace(n_q_heads=nq, n_kv_heads=nkv, head_dim=d)
+    m = Model(cfg, 2, 200, seed=5)
+    try:
+        for tokens, pos in [([3], [0]), ([9], [101]), ([4, 11], [157, 38]), ([2, 8], [199, 7])]:
+            kv_before = synth.bf16_bits(m.kv)
+            got = m.step(tokens, pos)
+            ref, _, _ = m.oracle(tokens, pos, kv_before)
+            _assert_rows_close(got, ref)
+    finally:
+        m.close()
+
+
 def test_llama32_1b_decode_full_size():
     m = Model(synth.LLAMA32_1B, 1, 1025)
     try:
