@@ -3,8 +3,9 @@
 
 One step = one whole decode step of the model (32 layers + LM head) for one
 new token, run as one persistent kernel launch through the C ABI.  Prints one
-JSON line (rank 0).  See the design doc for the metric, the roofline arithmetic and
-the input recipe.
+JSON line (rank 0): tokens/s of the persistent step, its HBM bytes per second
+against the measured copy bandwidth (algorithmic bytes: every weight once plus
+the cached and new K/V), and the comparison legs.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload llama3-8b|llama3.2-1b] [--no-per-op] [--no-prefill]

@@ -192,7 +192,8 @@ int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
 int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t queue_perm_seed,
                   mk_plan_stats *out);
 
-/* Prefill of `batch` prompts (SURVEY.md-listed variant of the prefill):
+/* Prefill of `batch` prompts ("MegaOps", Abstract: prefill of the dense
+ * Llama3/Qwen3 decoders, here for several prompts):
  * prompt b (tokens[b * stride .. b * stride + lens[b])) goes to sequence slot
  * b of the cache and its last token's logits to logits[b].  Each prompt runs
  * as mk_prefill does (one persistent launch of the prompt's tiles, then its
@@ -206,9 +207,8 @@ int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t 
 int mk_prefill_batch(mk_plan *plan, const int32_t *tokens, const int32_t *lens, int batch,
                      int stride, void *kv_cache, float *logits, void *stream);
 
-/* Prefill with the logits of EVERY prompt token (SURVEY.md-listed variant of
- * the prefill: "MegaOps", Abstract, prefill of the dense Llama3/Qwen3
- * decoders).  Same as mk_prefill, except that the final RMSNorm and the LM
+/* Prefill with the logits of EVERY prompt token ("MegaOps", Abstract:
+ * prefill of the dense Llama3/Qwen3 decoders).  Same as mk_prefill, except that the final RMSNorm and the LM
  * head run for all len tokens inside the same persistent launch, as
  * tensor-core GEMM tiles (128 tokens x 256 vocabulary rows) that wait on the
  * last layer's tiles of their own 128-token block.

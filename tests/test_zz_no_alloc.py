@@ -3,8 +3,9 @@ device memory when they run it (their device memory is already owned by their
 own pool or by an external memory manager).  Its scratch is the library's
 static device array, so it is checked against the plan-based entry point,
 mk_decode_step, on the same inputs: logits per row within
-2e-2 * RMS(reference row), the tolerance of the other decode tests, on two
-calls in a row (the second finds the first call's leftovers in the array).
+2e-2 * RMS(reference row), the tolerance of the other decode tests, and
+bit-identical (the same plan, kernel and queue run in both), on two calls in a
+row (the second finds the first call's leftovers in the array).
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test."""
@@ -55,19 +56,25 @@ def test_noalloc_matches_plan_entry_point(cfg, max_batch, max_ctx, positions):
         rc = mk.decode_step_noalloc(cfg, w, max_batch, max_ctx, tokens, pos, kv, got)
         assert rc == mk.MK_OK
         torch.cuda.synchronize()
-        _close(got.cpu().numpy(), ref)
+        got = got.cpu().numpy()
+        _close(got, ref)
+        np.testing.assert_array_equal(got, ref)
     del w, kv
     torch.cuda.empty_cache()
 
 
 def test_noalloc_rejects_shapes_beyond_its_static_scratch():
-    # The 32-layer 8B shape at a 4097-token cache needs more scratch than the
-    # static array holds; the call is refused before any device work, so every
-    # weight pointer may alias one small tensor.
+    # A 65536-token cache at head_dim 128: its RoPE table alone (one (cos, sin)
+    # float pair per position and rotation pair) is larger than the static
+    # array, whatever the SM count or the tiling, so the call is refused before
+    # any device work and every weight pointer may alias one small tensor.
     cfg = synth.LLAMA3_8B
+    max_ctx = 1 << 16
+    rope_bytes = max_ctx * (cfg.head_dim // 2) * 8
+    assert rope_bytes > mk.MK_NOALLOC_SCRATCH_BYTES
     dev = torch.device("cuda:0")
     x = torch.zeros(64, dtype=torch.bfloat16, device=dev)
     w = {name: x for name in synth.weight_shapes(cfg)}
     t = torch.zeros(1, dtype=torch.int32, device=dev)
     logits = torch.empty((1, 8), device=dev)
-    assert mk.decode_step_noalloc(cfg, w, 1, 4097, t, t, x, logits) == mk.MK_ERR_UNSUPPORTED
+    assert mk.decode_step_noalloc(cfg, w, 1, max_ctx, t, t, x, logits) == mk.MK_ERR_UNSUPPORTED

@@ -54,7 +54,10 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   if (c.head_dim != 64 && c.head_dim != 128)
     return bad(MK_ERR_UNSUPPORTED, "tensor-core decode head_dim must be 64 or 128");
   const int rep = c.n_q_heads / c.n_kv_heads;
-  if (rep > 4) return bad(MK_ERR_UNSUPPORTED, "tensor-core decode takes at most 4 q heads per kv head");
+  // the tensor-core attention scores pair q row g (hi) with row g + rep (lo)
+  // by a lane xor of 4 * rep: rep must be a power of two
+  if (rep != 1 && rep != 2 && rep != 4)
+    return bad(MK_ERR_UNSUPPORTED, "tensor-core decode takes 1, 2 or 4 q heads per kv head");
   const int qd = c.n_q_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
   if (c.hidden % BD_M || qd % BD_M || kd % BD_M || c.ffn % (BD_M / 2) || c.hidden % BD_BK ||
       c.ffn % BD_BK || qd % BD_BK)

@@ -25,6 +25,7 @@ MK_DECODE = 0
 MK_PREFILL = 1
 MK_LM_FUSED, MK_LM_SEPARATE = 0, 1
 TRACE_WORDS = 16  # u64 words per trace record (mk_trace_copy)
+MK_NOALLOC_SCRATCH_BYTES = 16 << 20  # static device scratch of mk_decode_step_noalloc
 
 EXPORTED = [
     "mk_plan_create", "mk_plan_destroy", "mk_kv_cache_bytes", "mk_decode_step",
