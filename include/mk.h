@@ -181,8 +181,21 @@ typedef struct {
   uint32_t decode_path;     /* 0: CUDA-core decode interpreter; 1: tensor-core
                                batched decode (batches the former does not
                                take, up to 32 sequences)                     */
+  uint64_t queue_hash;      /* FNV-1a hash of the decode queue as the device
+                               holds it (mk_plan_get_stats only; reading it
+                               back waits for the device)                    */
 } mk_plan_stats;
 int mk_plan_get_stats(const mk_plan *plan, mk_plan_stats *out);
+
+/* Test-only: mk_plan_create for a device of n_sms SMs (1 .. the current
+ * device's count; 0 = the device's own): the plan's projection tiling is cut
+ * for n_sms SMs and its persistent launches use n_sms CTAs.  Results must not
+ * depend on it ("MegaOps", Abstract: scheduling changes only when independent
+ * tiles run, not what they compute); schedule-invariance tests compare plans
+ * built for several counts.  Errors as mk_plan_create; n_sms above the device's
+ * count is MK_ERR_INVALID_ARG. */
+int mk_plan_create_for_sms(const mk_model_cfg *cfg, const mk_weight_ptrs *w, int max_batch,
+                           int max_ctx, int n_sms, mk_plan **out);
 
 /* Host-only check (no GPU needed): build the plan's queues for this shape,
  * optionally in a seeded random topological order, and run them through a

@@ -55,6 +55,11 @@ def _expected_weight_bytes(c):
     return 2 * (c.n_layers * (qkv + o + ffn) + c.vocab * c.hidden)
 
 
+def _keys_per_split(head_dim):
+    # the model constant of the decode attention tiling (mk_plan.h)
+    return 216 if head_dim >= 128 else 64
+
+
 @pytest.mark.parametrize("cfg,mb,mc", [
     (synth.TOY_1L, 1, 129), (synth.TOY_1L, 8, 129), (synth.TOY_1L, 3, 17),
     (synth.LLAMA32_1B, 1, 1025), (synth.LLAMA3_8B, 1, 4097),
@@ -64,12 +69,33 @@ def test_plan_check_valid(lib, cfg, mb, mc):
     rc, st = mk.plan_check(cfg, mb, mc)
     assert rc == mk.MK_OK
     assert st.weight_bytes == _expected_weight_bytes(cfg)
-    assert st.n_launches_per_op_decode == 5 * cfg.n_layers + 1
-    assert st.n_splits >= 1
-    # symbolic extents: the queue does not depend on the runtime batch or positions,
-    # only on the plan's maxima
-    rc2, st2 = mk.plan_check(cfg, mb, mc)
-    assert st2.n_instr_decode == st.n_instr_decode
+    ns = -(-mc // _keys_per_split(cfg.head_dim))
+    assert st.n_splits == ns
+    # per layer: QKV, the attention splits, the combining splits (when a group
+    # has more than one split), O, gate/up, down; then the LM head
+    assert st.n_launches_per_op_decode == (5 + (ns > 1)) * cfg.n_layers + 1
+
+
+@pytest.mark.parametrize("cfg,mc", [(synth.TOY_1L, 129), (synth.LLAMA32_1B, 1025),
+                                    (synth.LLAMA3_8B, 4097), (synth.TOY_1L, 2000)])
+def test_split_tiling_independent_of_max_batch(lib, cfg, mc):
+    """The split-KV tiling is fixed keys per split (a model constant): the
+    split count is ceil(max_ctx / KPS) whatever max_batch is, and only the
+    attention part of the queue grows with max_batch (one set of splits per
+    sequence slot)."""
+    kps = _keys_per_split(cfg.head_dim)
+    counts = {}
+    for mb in (1, 2, 3):
+        if mb * max(cfg.hidden, cfg.ffn) > 6144 and mb > 1:
+            continue  # beyond the CUDA-core path's shared-memory activation buffer
+        rc, st = mk.plan_check(cfg, mb, mc)
+        assert rc == mk.MK_OK
+        assert st.n_splits == -(-mc // kps)
+        counts[mb] = st.n_instr_decode
+    for mb in counts:
+        if mb > 1:
+            per_slot = cfg.n_layers * cfg.n_kv_heads * -(-mc // kps)
+            assert counts[mb] - counts[1] == (mb - 1) * per_slot
 
 
 @pytest.mark.parametrize("seed", [1, 2, 3, 4, 5])

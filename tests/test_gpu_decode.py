@@ -147,6 +147,65 @@ def test_toy_cta_counts_and_queue_orders(toy):
     toy.plan.set_debug()
 
 
+def test_queue_unchanged_by_steps(toy):
+    """Symbolic extents: one queue serves every batch and position -- the
+    device queue hashes the same before and after steps at several batches
+    and positions, and the hash does see the queue (a permuted order changes
+    it)."""
+    h0 = toy.plan.stats().queue_hash
+    for tokens, pos in [([1], [0]), ([2, 3], [5, 128]), ([4, 5, 6, 7], [1, 2, 3, 4]), ([9], [128])]:
+        toy.step(tokens, pos)
+        assert toy.plan.stats().queue_hash == h0
+    toy.plan.set_debug(queue_perm_seed=3)
+    assert toy.plan.stats().queue_hash != h0
+    toy.plan.set_debug()
+    assert toy.plan.stats().queue_hash == h0
+
+
+def _sm_counts():
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    return sorted({n, min(n, 132), min(n, 100)}, reverse=True)
+
+
+@pytest.mark.parametrize("cfg,max_ctx,positions,batches", [
+    (synth.TOY_1L, 300, [0, 63, 64, 250, 299], (1, 4)),
+    (synth.LLAMA32_1B.replace(n_layers=2), 1025, [1024, 300, 7], (1,)),
+])
+def test_bits_independent_of_sm_count_and_max_batch(cfg, max_ctx, positions, batches):
+    """Schedule invariance beyond one plan: plans tiled and launched for 152,
+    132 and 100 SMs, and with room for 1 or 4 sequences (the same CUDA-core
+    path), give bit-identical logits for the same sequence in slot 0 (the
+    split-KV tiling is a fixed number of keys per split, a model constant)."""
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(cfg, seed=11, device=dev)
+    kv1 = synth.make_kv_cache(cfg, 1, max_ctx, device=dev)
+    ref = {}
+    try:
+        for mb in batches:
+            kv = synth.make_kv_cache(cfg, mb, max_ctx, device=dev)
+            for sms in _sm_counts():
+                # every plan starts from the same cache (each step writes its
+                # slot, which later positions of the sequence read)
+                kv[:, :, 0].copy_(kv1[:, :, 0])
+                plan = mk.Plan(cfg, w, mb, max_ctx, n_sms=sms)
+                assert plan.stats().decode_path == 0
+                for p in positions:
+                    t = synth.make_tokens(1, cfg.vocab, seed=p).to(dev)
+                    pp = torch.tensor([p], dtype=torch.int32, device=dev)
+                    lg = torch.empty((1, cfg.vocab), device=dev)
+                    plan.decode_step(t, pp, kv, lg)
+                    assert plan.status() == mk.MK_OK
+                    got = lg.cpu().numpy()
+                    if p in ref:
+                        np.testing.assert_array_equal(got, ref[p], err_msg=f"max_batch {mb}, {sms} SMs, pos {p}")
+                    else:
+                        ref[p] = got
+                plan.close()
+    finally:
+        del w, kv1
+        torch.cuda.empty_cache()
+
+
 def test_toy_timeout_is_reported_and_recoverable(toy):
     tokens, pos = [3], [20]
     ref = toy.step(tokens, pos)
@@ -253,6 +312,15 @@ def test_llama3_8b_decode_full_size():
         ref, _, _ = m.oracle(tokens, [4096], kv_before)
         _assert_rows_close(got, ref)
         np.testing.assert_array_equal(m.step(tokens, [4096]), got)
+        # the same step tiled and launched for 100 SMs: bit-identical
+        plan100 = mk.Plan(m.cfg, m.w, 1, 4097, n_sms=min(100, _sm_counts()[0]))
+        t = torch.as_tensor(tokens, dtype=torch.int32).to(m.dev)
+        p = torch.tensor([4096], dtype=torch.int32, device=m.dev)
+        lg = torch.empty((1, m.cfg.vocab), device=m.dev)
+        plan100.decode_step(t, p, m.kv, lg)
+        assert plan100.status() == mk.MK_OK
+        np.testing.assert_array_equal(lg.cpu().numpy(), got)
+        plan100.close()
     finally:
         m.close()
 

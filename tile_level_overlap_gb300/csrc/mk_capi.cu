@@ -59,6 +59,7 @@ struct mk_plan {
   int device = 0, n_sms = 0, max_ctas = 0;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
+  size_t tagged_bytes = 0;      // the tagged intermediate tensors at the scratch's start
   Instr* d_queue = nullptr;     // default topological order (per-op ranges index it)
   Instr* d_queue_mk = nullptr;  // order popped by the persistent kernel
   unsigned long long* d_trace = nullptr;
@@ -324,7 +325,12 @@ int mk_plan_check(const mk_model_cfg* cfg, int max_batch, int max_ctx, uint64_t 
 
 int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_batch, int max_ctx,
                    mk_plan** out) {
-  if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
+  return mk_plan_create_for_sms(cfg, w, max_batch, max_ctx, 0, out);
+}
+
+int mk_plan_create_for_sms(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_batch,
+                           int max_ctx, int n_sms, mk_plan** out) {
+  if (!cfg || !w || !out || n_sms < 0) return MK_ERR_INVALID_ARG;
   *out = nullptr;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
@@ -337,6 +343,8 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
+  if (n_sms > sms) return MK_ERR_INVALID_ARG;
+  if (n_sms > 0) sms = n_sms;  // tile the plan, and launch it, as on a device with n_sms SMs
   mk_plan* p = new mk_plan();
   std::string why;
   p->max_batch = max_batch;
@@ -387,31 +395,21 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
     return code;
   };
   if (cudaGetDevice(&p->device) != cudaSuccess) return fail(MK_ERR_CUDA);
-  if (cudaDeviceGetAttribute(&p->n_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
-    return fail(MK_ERR_CUDA);
+  p->n_sms = sms;
   p->kv = pick_variant(p->hp);
   if (p->kv.setup() != cudaSuccess) return fail(MK_ERR_CUDA);
   int per_sm = 0;
   if (p->kv.occupancy(&per_sm) != cudaSuccess || per_sm < 1) return fail(MK_ERR_CUDA);
   p->max_ctas = p->n_sms;
 
-  // one scratch allocation
+  // one scratch allocation: the decode layout (shared with the no-allocation
+  // entry point), then a second copy of the queue, the host-buffer staging and
+  // the multi-step words
   const int H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
-  const size_t B = (size_t)hp.max_batch;
+  const DecodeScratch ds = decode_scratch(hp);
   Bump bm;
-  const size_t o_resid = bm.take(sizeof(float) * (2 * L + 1) * B * H);
-  const size_t o_qkv = bm.take(sizeof(float) * L * B * hp.qkv_rows);
-  const size_t o_part = bm.take(sizeof(float) * L * B * nkv * hp.n_splits * hp.rep * (d + 2));
-  const size_t o_attn = bm.take(sizeof(float) * L * B * c.n_q_heads * d);
-  const size_t o_act = bm.take(sizeof(float) * L * B * F);
-  const size_t o_bars = bm.take(sizeof(uint32_t) * hp.bl.total);
-  const size_t o_arr = bm.take(sizeof(uint32_t) * L * B * nkv);
-  const size_t o_ctl = bm.take(sizeof(uint32_t) * CTL_WORDS);
-  const size_t o_q = bm.take(sizeof(Instr) * hp.decode.size());
+  bm.off = ds.total;
   const size_t o_qmk = bm.take(sizeof(Instr) * hp.decode.size());
-  const size_t o_expr = bm.take(sizeof(uint32_t) * hp.expr.size());
-  const size_t o_rope = bm.take(sizeof(float2) * (size_t)max_ctx * (d / 2));
-  const size_t o_lw = bm.take(sizeof(LayerW) * L);
   const size_t o_tok = bm.take(sizeof(int32_t) * max_batch);
   const size_t o_pos = bm.take(sizeof(int32_t) * max_batch);
   const size_t o_log = bm.take(sizeof(float) * max_batch * c.vocab);
@@ -419,12 +417,14 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   // tiles and the chosen token, cleared together before each such launch
   const size_t o_msteps = bm.take(16 * MAX_DECODE_STEPS);
   p->scratch_bytes = bm.off;
+  p->tagged_bytes = ds.tagged_end;
   if (cudaMalloc(&p->scratch, p->scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
     return fail(MK_ERR_CUDA);
   }
   uint8_t* s = (uint8_t*)p->scratch;
   if (cudaMemset(p->scratch, 0, p->scratch_bytes) != cudaSuccess) return fail(MK_ERR_CUDA);
+  const size_t o_q = ds.o_q, o_expr = ds.o_expr, o_rope = ds.o_rope, o_lw = ds.o_lw;
 
   std::vector<float2> rope((size_t)max_ctx * (d / 2));
   for (int pos = 0; pos < max_ctx; ++pos)
@@ -435,7 +435,7 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
     }
   p->d_queue = (Instr*)(s + o_q);
   p->d_queue_mk = (Instr*)(s + o_qmk);
-  p->d_ctl = (uint32_t*)(s + o_ctl);
+  p->d_ctl = (uint32_t*)(s + ds.o_ctl);
   p->d_tok = (int32_t*)(s + o_tok);
   p->d_pos = (int32_t*)(s + o_pos);
   p->d_logits = (float*)(s + o_log);
@@ -465,13 +465,13 @@ int mk_plan_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int max_bat
   k.lm = (const uint16_t*)(c.tied_embeddings ? w->embed : w->lm_head);
   k.final_norm = (const uint16_t*)w->final_norm;
   k.layers = (const LayerW*)(s + o_lw);
-  k.resid = (float*)(s + o_resid);
-  k.qkv = (float*)(s + o_qkv);
-  k.part = (float*)(s + o_part);
-  k.attn_out = (float*)(s + o_attn);
-  k.act = (float*)(s + o_act);
-  k.bars = (uint32_t*)(s + o_bars);
-  k.arrive = (uint32_t*)(s + o_arr);
+  k.resid = (u64*)(s + ds.o_resid);
+  k.qkv = (u64*)(s + ds.o_qkv);
+  k.part = (u64*)(s + ds.o_part);
+  k.attn_out = (u64*)(s + ds.o_attn);
+  k.act = (u64*)(s + ds.o_act);
+  k.kps = hp.kps;
+  k.bars = (uint32_t*)(s + ds.o_bars);
   k.rope = (const float2*)(s + o_rope);
   k.ctl = p->d_ctl;
   k.queue = p->d_queue_mk;
@@ -514,6 +514,19 @@ int mk_plan_get_stats(const mk_plan* p, mk_plan_stats* out) {
   out->n_barriers = p->hp.bl.total;
   out->n_launches_per_op_decode = (uint32_t)p->hp.perop_decode.size();
   out->n_ctas = (uint32_t)(p->force_ctas ? p->force_ctas : p->max_ctas);
+  {
+    // FNV-1a over the decode queue as the device holds it (the order the
+    // persistent kernel pops)
+    const Instr* dq = p->bd.on ? p->bd.base.queue : p->d_queue_mk;
+    const size_t n = p->bd.on ? p->bd.bp.queue.size() : p->hp.decode.size();
+    std::vector<uint8_t> q(n * sizeof(Instr));
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(q.data(), dq, q.size(), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return MK_ERR_CUDA;
+    uint64_t h = 1469598103934665603ull;
+    for (uint8_t v : q) h = (h ^ v) * 1099511628211ull;
+    out->queue_hash = h;
+  }
   out->n_splits = (uint32_t)p->hp.n_splits;
   out->weight_bytes = p->hp.weight_bytes;
   out->scratch_bytes = p->scratch_bytes;
@@ -580,7 +593,7 @@ int mk_decode_step(mk_plan* p, const int32_t* tokens, const int32_t* positions, 
   k.n_instr += r.second;
   k.queue = p->d_queue;
   k.trace = nullptr;
-  return cuda_err(p->kv.perop(k, r.first, r.second, st));
+  return cuda_err(p->kv.perop(k, r.first, r.second, p->max_ctas, st));
 }
 
 int mk_decode_steps(mk_plan* p, const int32_t* token, const int32_t* position, int n_steps,
@@ -760,13 +773,17 @@ static int prefill_lm(mk_plan* p, const int32_t* tokens, int len, void* kv, floa
                       cudaStream_t st) {
   const mk_model_cfg& c = p->hp.cfg;
   const float* last = p->pf.base.xb + (size_t)(len - 1) * c.hidden;
-  float* dst = p->base.resid + (size_t)(2 * c.n_layers) * p->hp.max_batch * c.hidden;
-  MK_CUDA(cudaMemcpyAsync(dst, last, sizeof(float) * c.hidden, cudaMemcpyDeviceToDevice, st));
+  u64* dst = p->base.resid + (size_t)(2 * c.n_layers) * p->hp.max_batch * c.hidden;
+  // the floats into the low halves of the tagged words (the kernel-per-operator
+  // LM tiles read them without a tag check; their tags stay stale for any
+  // later persistent launch, which waits for its own writes)
+  MK_CUDA(cudaMemcpy2DAsync(dst, sizeof(u64), last, sizeof(float), sizeof(float), c.hidden,
+                            cudaMemcpyDeviceToDevice, st));
   KParams k = step_params(p, tokens, tokens, 1, kv, logits);
   k.queue = p->d_queue;
   k.trace = nullptr;
   const auto& r = p->hp.perop_decode.back();  // the LM-head tiles
-  return cuda_err(p->kv.perop(k, r.first, r.second, st));
+  return cuda_err(p->kv.perop(k, r.first, r.second, p->max_ctas, st));
 }
 
 int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits, void* stream) {
@@ -832,7 +849,7 @@ int mk_prefill_logits(mk_plan* p, const int32_t* tokens, int len, void* kv, floa
 }
 
 static int launch_per_op_seq(mk_plan* p, const KParams& k, cudaStream_t st) {
-  for (const auto& r : p->hp.perop_decode) MK_CUDA(p->kv.perop(k, r.first, r.second, st));
+  for (const auto& r : p->hp.perop_decode) MK_CUDA(p->kv.perop(k, r.first, r.second, p->max_ctas, st));
   return MK_OK;
 }
 
@@ -935,9 +952,10 @@ int mk_plan_reset(mk_plan* p, void* stream) {
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MK_ERR_CUDA;
   MK_CUDA(cudaMemset(p->base.bars, 0, sizeof(uint32_t) * p->hp.bl.total));
-  MK_CUDA(cudaMemset(p->base.arrive, 0,
-                     sizeof(uint32_t) * p->hp.cfg.n_layers * p->hp.max_batch * p->hp.cfg.n_kv_heads));
   MK_CUDA(cudaMemset(p->d_ctl, 0, sizeof(uint32_t) * CTL_WORDS));
+  // the launch counter restarts at 0: clear every tagged word, so that no
+  // stale word carries a tag a later launch expects
+  MK_CUDA(cudaMemset(p->scratch, 0, p->tagged_bytes));
   if (p->pf.built) {
     MK_CUDA(cudaMemset(p->pf.base.bars, 0, sizeof(uint32_t) * p->pf.pp.bl.total));
     MK_CUDA(cudaMemset(p->pf.base.ctl, 0, sizeof(uint32_t) * CTL_WORDS));
@@ -975,8 +993,7 @@ int mk_plan_debug_drop_release(mk_plan* p, uint32_t index) {
   Instr in;
   MK_CUDA(cudaDeviceSynchronize());
   MK_CUDA(cudaMemcpy(&in, p->d_queue_mk + index, sizeof(Instr), cudaMemcpyDeviceToHost));
-  in.rel_bar = NO_BAR;
-  in.flags = 0;
+  in.flags |= IF_NO_PUBLISH;
   MK_CUDA(cudaMemcpy(p->d_queue_mk + index, &in, sizeof(Instr), cudaMemcpyHostToDevice));
   return MK_OK;
 }

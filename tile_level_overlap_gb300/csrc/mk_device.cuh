@@ -3,6 +3,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "mk_internal.h"
+
 namespace mk {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -98,6 +100,33 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tagged words
+// An element of an intermediate tensor of the decode step is one 64-bit word:
+// the float in the low half, the tag of the launch step that wrote it in the
+// high half.  An aligned 64-bit access is single-copy atomic, so a reader that
+// sees the tag it expects also sees the value stored with it: each word is its
+// own barrier (a barrier tensor partitioned down to single elements), and the
+// writer needs no fence and no counter release after its stores.  (u64 is
+// declared in mk_internal.h.)
+
+__device__ __forceinline__ u64 tag_word(float v, uint32_t tag) {
+  return ((u64)tag << 32) | (u64)__float_as_uint(v);
+}
+__device__ __forceinline__ float tag_val(u64 w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint32_t tag_of(u64 w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ void st_tagged(u64* p, float v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(tag_word(v, tag)) : "memory");
+}
+__device__ __forceinline__ u64 ld_tagged(const u64* p) {
+  u64 w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+// Two consecutive words (16-byte aligned); each is read atomically.
+__device__ __forceinline__ void ld_tagged2(const u64* p, u64& a, u64& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 // Named barrier among `n` threads (id 0 is __syncthreads).

@@ -19,6 +19,8 @@
 
 namespace mk {
 
+typedef unsigned long long u64;  // a tagged word (mk_device.cuh)
+
 // ---------------------------------------------------------------- opcodes
 enum Op : uint8_t {
   OP_NOP = 0,
@@ -35,10 +37,17 @@ constexpr uint32_t NO_BAR = 0xffffffffu;
 constexpr uint8_t NO_EXPR = 0xff;
 
 // Instruction flags.
-constexpr uint8_t IF_RELEASE_ON_COMBINE = 1;  // release happens once per (seq, kv head) group
+// Decode attention: this split also combines every split of its (sequence, kv
+// head) group (the last split of the group in every topological order: it
+// waits on the others' partials).
+constexpr uint8_t IF_COMBINE = 1;
 // The waited counter is cleared before every launch that runs this
 // instruction (it is not released by every launch): absolute target.
 constexpr uint8_t IF_ABS_TARGET = 2;
+// Test-only fault injection (decode interpreter): the instruction stores its
+// outputs under a tag no reader expects, so its consumers' bounded waits run
+// out.
+constexpr uint8_t IF_NO_PUBLISH = 4;
 
 // One queue record, 32 bytes.
 struct Instr {
@@ -113,8 +122,8 @@ MK_HD int64_t x_eval(const uint32_t* e, const Instr& in, int B, int S, const int
 
 // Expression slots used by the plan.
 enum XSlot : uint8_t {
-  XS_ATTN_LO = 0,  // first key of split a2 of sequence a0: min(a2*ceil((P+1)/NS), P+1)
-  XS_ATTN_HI = 1,  // one past its last key
+  XS_ATTN_LO = 0,  // first key of split a2 of sequence a0: min(a2 * KPS, P + 1)
+  XS_ATTN_HI = 1,  // one past its last key: min((a2 + 1) * KPS, P + 1)
   XS_SEQ_LIVE = 2, // B - a0  (> 0: sequence a0 is part of this step)
   XS_COUNT = 3
 };
@@ -122,13 +131,15 @@ enum XSlot : uint8_t {
 // ---------------------------------------------------------------- barrier tensor layout
 // One flat uint32 array.  Decode sub-tensors (all per layer):
 //   qkv[L][n_kv]   : QKV row tiles of kv group g (its q heads, k_g, v_g) done
+//   split[L][max_batch][n_kv] : the splits of a (sequence, kv group) other
+//                    than its combining split done
 //   attn[L]        : (sequence, kv group) attention outputs combined
 //   o[L]           : O-projection row tiles done (residual x1 complete when full)
 //   gu[L]          : gate/up row tiles done (SwiGLU activations complete)
 //   down[L]        : down-projection row tiles done (residual x2 complete)
 //   lm[1]          : LM-head row tiles done
 struct BarLayout {
-  uint32_t qkv, attn, o, gu, down, lm, total;
+  uint32_t qkv, split, attn, o, gu, down, lm, total;
 };
 
 // Control words (device uint32 array).
@@ -172,14 +183,15 @@ struct KParams {
   // weights
   const uint16_t *embed, *lm, *final_norm;
   const LayerW* layers;
-  // plan-owned scratch
-  float* resid;     // [2L+1][max_batch][H]
-  float* qkv;       // [L][max_batch][qkv_rows]
-  float* part;      // [L][max_batch][nkv][n_splits][rep][d+2]
-  float* attn_out;  // [L][max_batch][nq*d]
-  float* act;       // [L][max_batch][F]
-  uint32_t* bars;   // barrier tensor
-  uint32_t* arrive; // [L][max_batch][nkv] split arrival counters
+  // plan-owned scratch: the intermediate tensors are tagged words (the float
+  // and the tag of the launch step that wrote it; see mk_device.cuh)
+  u64* resid;     // [2L+1][max_batch][H]
+  u64* qkv;       // [L][max_batch][qkv_rows]
+  u64* part;      // [L][max_batch][nkv][n_splits][rep][d+2]
+  u64* attn_out;  // [L][max_batch][nq*d]
+  u64* act;       // [L][max_batch][F]
+  int kps;          // keys per attention split (a model constant)
+  uint32_t* bars;   // barrier tensor (host simulation; the kernel reads tags)
   const float2* rope;  // [max_ctx][d/2] (cos, sin)
   uint32_t* ctl;
   const Instr* queue;
@@ -194,7 +206,7 @@ struct KParams {
   uint16_t* kv;
   float* logits;
   int mode;
-  uint32_t perop_base;
+  uint32_t perop_base, perop_count;  // kernel-per-operator: the operator's queue range
   unsigned long long wait_limit_ns;
   // Multi-step greedy decode (batch 1): the queue runs n_steps times in one
   // launch; step s reads positions + s and, for s > 0, the token step s - 1

@@ -13,8 +13,9 @@
 // pipelining across output tiles) with the tile-level dependencies and the
 // weight prefetch across operator boundaries of the MegaOps Abstract.
 //
-// The same kernel runs kernel-per-operator (MODE_PEROP): one instruction per
-// CTA, no waits and no barrier releases; stream order replaces the counters.
+// The same kernel runs kernel-per-operator (MODE_PEROP): one launch per
+// operator, its tiles split statically over at most one CTA per SM, no tag
+// checks; stream order replaces them.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -124,6 +125,45 @@ __device__ __forceinline__ bool mbar_wait(const KParams& P, uint64_t* bar, uint3
       return false;
     }
   }
+}
+
+// Bounded poll on tagged words.  `load` reads this thread's words and returns
+// true once every tag it read is the expected one (always true for tag 0:
+// kernel-per-operator launches, where stream order makes every input ready).
+// Retries until it succeeds, the launch is aborted (abort word, or a local
+// stop), or the wait limit passes (MK_ERR_TIMEOUT, detail = `detail`).  On
+// failure it raises the CTA's stop flag and returns false; the caller still
+// finishes its tile on whatever it read, so the ring protocol stays intact,
+// and the next instruction is drained.
+template <class F>
+__device__ __forceinline__ bool poll_until(const KParams& P, const Sh& S, F&& load, uint32_t detail) {
+  if (load()) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    __nanosleep(32);
+    const uint32_t ab = ld_volatile(&P.ctl[CTL_ABORT]);  // in flight with the loads
+    if (load()) return true;
+    if (ab != 0u || S.flags[F_STOP] != 0u) {
+      S.flags[F_STOP] = 1u;
+      return false;
+    }
+    if (globaltimer() - t0 > P.wait_limit_ns) {
+      set_error(P, MK_ERR_TIMEOUT, detail);
+      S.flags[F_STOP] = 1u;
+      return false;
+    }
+  }
+}
+
+// Tag a launch step expects on its inputs and writes on its outputs: a fresh
+// value per (launch, step) in the persistent mode, 0 (no checks) in the
+// kernel-per-operator mode.  IF_NO_PUBLISH (test-only) stores under 0, which no
+// persistent reader expects.
+__device__ __forceinline__ uint32_t step_tag(const KParams& P, uint32_t gen, uint32_t step) {
+  return P.mode == MODE_MEGA ? gen + step + 1u : 0u;
+}
+__device__ __forceinline__ uint32_t pub_tag(const Instr& in, uint32_t tag) {
+  return (in.flags & IF_NO_PUBLISH) ? 0u : tag;
 }
 
 // ---------------------------------------------------------------- operand sources
@@ -302,7 +342,11 @@ __device__ void producer(const KParams& P, const Sh& S) {
       const uint32_t g = atomicAdd(&P.ctl[CTL_HEAD], 1u);
       return g < P.n_instr * (MS ? P.n_steps : 1u) ? g : END_SLOT;
     }
-    return k == 0 ? P.perop_base + blockIdx.x : END_SLOT;
+    // kernel-per-operator: CTA c runs tiles c, c + grid, ... of the
+    // operator (a static split, no atomics), so a CTA loads the operator's
+    // input activations once, as in the persistent launch
+    const uint32_t j = k * gridDim.x + blockIdx.x;
+    return j < P.perop_count ? P.perop_base + j : END_SLOT;
   };
   for (;;) {
     const bool room = mbar_wait(P, &S.empty[stage_ctr % NSTAGE], ((stage_ctr / NSTAGE) & 1u) ^ 1u);
@@ -420,9 +464,9 @@ __device__ __forceinline__ int token_of(const KParams& P, int b, uint32_t step =
   return t;
 }
 
-// Activation source of a GEMV op (row-major [max_batch][K] fp32), or null when
-// it is the embedding row of the sequence's token (layer-0 QKV).
-__device__ __forceinline__ const float* gemv_x(const KParams& P, const Instr& in) {
+// Activation source of a GEMV op (row-major [max_batch][K] tagged words), or
+// null when it is the embedding row of the sequence's token (layer-0 QKV).
+__device__ __forceinline__ const u64* gemv_x(const KParams& P, const Instr& in) {
   const size_t bh = (size_t)P.max_batch * P.H;
   switch (in.op) {
     case OP_QKV: return in.layer == 0 ? nullptr : P.resid + (size_t)(2 * in.layer) * bh;
@@ -441,14 +485,29 @@ __device__ __forceinline__ const uint16_t* gemv_gain(const KParams& P, const Ins
   }
 }
 
-// Load 8 consecutive activations of sequence b starting at column c.
-__device__ __forceinline__ void load_x8(const KParams& P, const float* xs, const uint16_t* emb_row,
-                                        int b, int K, int c, float (&x)[8]) {
+// Read 8 consecutive tagged words (64-byte aligned) into x; true when every
+// tag is `tag` (or tag is 0).
+__device__ __forceinline__ bool ld_tagged8(const u64* p, uint32_t tag, float (&x)[8]) {
+  u64 w[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) ld_tagged2(p + 2 * k, w[2 * k], w[2 * k + 1]);
+  uint32_t bad = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    x[k] = tag_val(w[k]);
+    bad |= tag_of(w[k]) ^ tag;
+  }
+  return tag == 0u || bad == 0u;
+}
+
+// Load 8 consecutive activations of sequence b starting at column c (a bounded
+// poll on their tags), or widen them from the embedding row.
+__device__ __forceinline__ void load_x8(const KParams& P, const Sh& S, const u64* xs,
+                                        const uint16_t* emb_row, int b, int K, int c, uint32_t tag,
+                                        float (&x)[8]) {
   if (xs) {
-    const float4* p = reinterpret_cast<const float4*>(xs + (size_t)b * K + c);
-    float4 u = __ldcg(p), v = __ldcg(p + 1);
-    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
-    x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+    const u64* p = xs + (size_t)b * K + c;
+    poll_until(P, S, [&]() { return ld_tagged8(p, tag, x); }, 0xfffffff1u);
   } else {
     uint4 w = __ldg(reinterpret_cast<const uint4*>(emb_row + c));
     widen8(w, x);
@@ -462,10 +521,10 @@ __device__ __forceinline__ void load_x8(const KParams& P, const float* xs, const
 // a per-warp row slot; one fixed-order sum over warps per tile.
 template <int M>
 __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in,
-                                            float (&xr)[M][8], uint32_t step) {
+                                            float (&xr)[M][8], uint32_t step, uint32_t tag) {
   const int t = threadIdx.x;
-  const int K = M * FAST_K_UNIT;
-  const float* xs = gemv_x(P, in);
+  constexpr int K = M * FAST_K_UNIT;
+  const u64* xs = gemv_x(P, in);
   const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0, step) * P.H;
   const uint16_t* gain = gemv_gain(P, in);
   uint4 gw[M];
@@ -473,8 +532,21 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
 #pragma unroll
     for (int j = 0; j < M; ++j) gw[j] = __ldg(reinterpret_cast<const uint4*>(gain + 8 * (t + NT * j)));
   }
+  if (xs) {
+    // every word of this thread's columns in flight at once, one tag check
+    poll_until(P, S, [&]() {
+      bool ok = true;
 #pragma unroll
-  for (int j = 0; j < M; ++j) load_x8(P, xs, emb_row, 0, K, 8 * (t + NT * j), xr[j]);
+      for (int j = 0; j < M; ++j) ok &= ld_tagged8(xs + 8 * (t + NT * j), tag, xr[j]);
+      return ok;
+    }, 0xfffffff2u);
+  } else {
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(emb_row + 8 * (t + NT * j)));
+      widen8(w, xr[j]);
+    }
+  }
   if (gain) {
     float ss = 0.f;
 #pragma unroll
@@ -496,33 +568,52 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
 // The down projection's input (the SwiGLU output: no norm, no gain, never the
 // embedding), loaded without the general form's gain registers.
 template <int M>
-__device__ __forceinline__ void load_x_plain(const float* xs, float (&xr)[M][8]) {
+__device__ __forceinline__ void load_x_plain(const KParams& P, const Sh& S, const u64* xs,
+                                             float (&xr)[M][8], uint32_t tag) {
   const int t = threadIdx.x;
+  // two halves, so that the tag halves of the words in flight do not push
+  // the register-resident activations out
+  constexpr int MA = (M + 1) / 2;
+  poll_until(P, S, [&]() {
+    bool ok = true;
 #pragma unroll
-  for (int j = 0; j < M; ++j) {
-    const float4* p = reinterpret_cast<const float4*>(xs + 8 * (t + NT * j));
-    const float4 u = __ldcg(p), v = __ldcg(p + 1);
-    xr[j][0] = u.x; xr[j][1] = u.y; xr[j][2] = u.z; xr[j][3] = u.w;
-    xr[j][4] = v.x; xr[j][5] = v.y; xr[j][6] = v.z; xr[j][7] = v.w;
-  }
+    for (int j = 0; j < MA; ++j) ok &= ld_tagged8(xs + 8 * (t + NT * j), tag, xr[j]);
+    return ok;
+  }, 0xfffffff3u);
+  poll_until(P, S, [&]() {
+    bool ok = true;
+#pragma unroll
+    for (int j = MA; j < M; ++j) ok &= ld_tagged8(xs + 8 * (t + NT * j), tag, xr[j]);
+    return ok;
+  }, 0xfffffff3u);
 }
 
 // The residual input of an O / down tile output element (thread t owns output
 // (r, b) = (t / B, t % B)); loaded before the tile streams so that its latency
 // is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
 // (RMAX * BMAX_CC <= NT).
-__device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Instr& in,
-                                                   const GemvDesc& g, int t, uint32_t step = 0) {
+__device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Sh& S, const Instr& in,
+                                                   const GemvDesc& g, int t, uint32_t tag,
+                                                   uint32_t step = 0) {
   const int B = P.B, l = in.layer;
   if (t >= g.rows * B) return 0.f;
   const int r = t / B, b = t % B, row = g.row0 + r;
   const size_t bh = (size_t)P.max_batch * P.H;
+  const u64* src = nullptr;
   if (in.op == OP_O) {
     if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b, step) * P.H + row] << 16);
-    return __ldcg(P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row);
+    src = P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row;
+  } else if (in.op == OP_DOWN) {
+    src = P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row;
+  } else {
+    return 0.f;
   }
-  if (in.op == OP_DOWN) return __ldcg(P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row);
-  return 0.f;
+  u64 w = 0;
+  poll_until(P, S, [&]() {
+    w = ld_tagged(src);
+    return tag == 0u || tag_of(w) == tag;
+  }, 0xfffffff4u);
+  return tag_val(w);
 }
 
 // Hand-off buffers between the consumers and the finisher warp: record `hb`
@@ -560,8 +651,8 @@ __device__ __forceinline__ void handoff_commit(const Sh& S, Ring& R, int hb) {
 // following it; the loop body stays small (one stage).
 template <int M, bool MS>
 __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const Instr& in,
-                                          uint32_t ii, uint32_t step, const GemvDesc& g, const Src& src,
-                                          Ring& R, const float (&xr)[M][8]) {
+                                          uint32_t ii, uint32_t step, uint32_t tag, const GemvDesc& g,
+                                          const Src& src, Ring& R, const float (&xr)[M][8]) {
   constexpr int RPS = fast_rps(M);  // whole rows per 32 KB stage at K = M * 2048
   constexpr int kDup = 32 / RPS;    // lanes holding the same total after the reduction
   constexpr int NP = M > 1 ? M : 2;
@@ -573,7 +664,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   if (P.trace && t == 0) trace_mark(P, ii, 11);
   // the residual input of the tile's outputs (O, down), loaded now so that its
   // latency hides behind the stages; the finisher takes it from the hand-off
-  const float pre = epilogue_prefetch(P, in, g, t, step);
+  const float pre = epilogue_prefetch(P, S, in, g, t, tag, step);
   if (MS && t == 0) *hrec_step(S, hb) = step;  // the buffer is this tile's from here on
   float* redw = S.redw + hb * NW * RMAX;
   const int idx = warp_multi_index<RPS>(lane);
@@ -651,10 +742,10 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
 // ---------------------------------------------------------------- GEMV, any K, batch <= BMAX_CC
 // x[B][K] (normed) staged in shared memory; one warp per (row, sequence) pair.
 __device__ __forceinline__ void gemv_generic(const KParams& P, const Sh& S, const Instr& in, const GemvDesc& g,
-                             const Src& src, Ring& R) {
+                             const Src& src, Ring& R, uint32_t tag) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int K = g.K, B = P.B, K8 = K / 8;
-  const float* xs = gemv_x(P, in);
+  const u64* xs = gemv_x(P, in);
   const uint16_t* gain = gemv_gain(P, in);
   float ss[BMAX_CC];
 #pragma unroll
@@ -663,7 +754,7 @@ __device__ __forceinline__ void gemv_generic(const KParams& P, const Sh& S, cons
     const int b = idx / K8, c = (idx % K8) * 8;
     const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, b) * P.H;
     float x[8];
-    load_x8(P, xs, emb_row, b, K, c, x);
+    load_x8(P, S, xs, emb_row, b, K, c, tag, x);
     float s = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -717,8 +808,10 @@ __device__ __forceinline__ void gemv_generic(const KParams& P, const Sh& S, cons
 // Store a finished GEMV tile: y[r][b] is in red[r * BMAX_CC + b]; `t` is the
 // (row, sequence) slot of this thread and `pre` its residual input from
 // epilogue_prefetch.
+// Outputs are stored as tagged words under `ptag` (the logits as plain floats):
+// their consumers poll the tags, so no fence or counter release follows.
 __device__ void gemv_epilogue(const KParams& P, const float* red, const Instr& in, const GemvDesc& g,
-                              float pre, int t) {
+                              float pre, int t, uint32_t ptag) {
   const int B = P.B, l = in.layer;
   if (t >= g.rows * B) return;
   const int r = t / B, b = t % B, row = g.row0 + r;
@@ -726,18 +819,18 @@ __device__ void gemv_epilogue(const KParams& P, const float* red, const Instr& i
   const float y = red[r * BMAX_CC + b];
   switch (in.op) {
     case OP_QKV:
-      P.qkv[((size_t)l * P.max_batch + b) * P.qkv_rows + row] = y;
+      st_tagged(P.qkv + ((size_t)l * P.max_batch + b) * P.qkv_rows + row, y, ptag);
       break;
     case OP_O:
-      P.resid[(size_t)(2 * l + 1) * bh + (size_t)b * P.H + row] = pre + y;
+      st_tagged(P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row, pre + y, ptag);
       break;
     case OP_GU: {
       const float u = red[(g.rows + r) * BMAX_CC + b];
-      P.act[((size_t)l * P.max_batch + b) * P.F + row] = y / (1.0f + expf(-y)) * u;
+      st_tagged(P.act + ((size_t)l * P.max_batch + b) * P.F + row, y / (1.0f + expf(-y)) * u, ptag);
       break;
     }
     case OP_DOWN:
-      P.resid[(size_t)(2 * l + 2) * bh + (size_t)b * P.H + row] = pre + y;
+      st_tagged(P.resid + (size_t)(2 * l + 2) * bh + (size_t)b * P.H + row, pre + y, ptag);
       break;
     default:
       P.logits[(size_t)b * P.V + row] = y;
@@ -754,30 +847,35 @@ __device__ __forceinline__ float round_bf16(float x) {
 // ring; the new token's key/value come from the QKV output (normed when q/k
 // norm is on, rotated, rounded to bf16 like every cached entry, written to the
 // cache by the split that holds slot pos).
-// Partial (max, sum, unnormalised o) per q head; the last split to arrive
-// combines all splits of the group in split order.
+// Partial (max, sum, unnormalised o) per q head, stored as tagged words.  The
+// group's last split (IF_COMBINE) then polls every live split's partial and
+// combines them in split order; a split past the sequence's keys holds none
+// and does nothing unless it is that combining split.
 // (tracing) attention tile phase boundaries: trace words 8 (inputs loaded and
-// rotated), 9 (scores), 10 (softmax and P V), 11 (split arrival counted)
+// rotated), 9 (scores), 10 (softmax and P V), 11 (partials of the group ready,
+// combining split only)
 __device__ __forceinline__ void attn_mark(const KParams& P, uint32_t ii, int word) {
   if (P.trace && threadIdx.x == 0) P.trace[(size_t)ii * TRACE_WORDS + word] = globaltimer();
 }
 
 template <int D, int REP>
 __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
-                          uint32_t ii, Ring& R) {
+                          uint32_t ii, uint32_t tag, Ring& R) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int l = in.layer, b = (int)in.a0, g = (int)in.a1, split = (int)in.a2;
   constexpr int rep = REP;
   const int qd = P.nq * D, NS = P.n_splits;
   constexpr int smax = SCORE_FLOATS / REP;
+  const uint32_t ptag = pub_tag(in, tag);
   if (t == 0 && b < P.B && !e.live) set_error(P, MK_ERR_BOUNDS, ii);  // position out of range
   float* qs = S.xbuf;            // [rep][D]
   float* kn = qs + 8 * 128;      // [D]
   float* vn = kn + 128;          // [D]
   float* sc = vn + 128;          // [rep][smax]
-  float* part = P.part + ((((size_t)l * P.max_batch + b) * P.nkv + g) * NS + split) * rep * (D + 2);
+  u64* part = P.part + ((((size_t)l * P.max_batch + b) * P.nkv + g) * NS + split) * rep * (D + 2);
+  const int n = e.hi - e.lo;     // keys of this split (0: past the sequence's keys)
 
-  if (e.live) {
+  if (e.live && n > 0) {
     // RoPE factors of this thread's rotation pairs, fetched together with q/k/v
     const float2* rt = P.rope + (size_t)e.pos * (D / 2);
     constexpr int NROT = ((REP + 1) * (D / 2) + NT - 1) / NT;
@@ -787,13 +885,36 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
       const int i = t + j * NT;
       cs[j] = i < (rep + 1) * (D / 2) ? __ldg(rt + i % (D / 2)) : make_float2(0.f, 0.f);
     }
-    const float* base = P.qkv + ((size_t)l * P.max_batch + b) * P.qkv_rows;
-    for (int i = t; i < rep * D; i += NT) qs[i] = __ldcg(base + g * rep * D + i);
-    for (int i = t; i < D; i += NT) {
-      kn[i] = __ldcg(base + qd + g * D + i);
-      vn[i] = round_bf16(__ldcg(base + qd + P.nkv * D + g * D + i));
+    // q of the group's heads, k and v: a bounded poll on their tags
+    {
+      const u64* base = P.qkv + ((size_t)l * P.max_batch + b) * P.qkv_rows;
+      constexpr int NQ = ((REP + 2) * D + NT - 1) / NT;
+      u64 wq[NQ];
+      poll_until(P, S, [&]() {
+        uint32_t bad = 0;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          const int i = t + j * NT;
+          if (i < (REP + 2) * D) {
+            const u64* src = i < REP * D       ? base + g * REP * D + i
+                             : i < (REP + 1) * D ? base + qd + g * D + (i - REP * D)
+                                                 : base + qd + P.nkv * D + g * D + (i - (REP + 1) * D);
+            wq[j] = ld_tagged(src);
+            bad |= tag_of(wq[j]) ^ tag;
+          }
+        }
+        return tag == 0u || bad == 0u;
+      }, ii);
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        const int i = t + j * NT;
+        if (i < REP * D) qs[i] = tag_val(wq[j]);
+        else if (i < (REP + 1) * D) kn[i - REP * D] = tag_val(wq[j]);
+        else if (i < (REP + 2) * D) vn[i - (REP + 1) * D] = round_bf16(tag_val(wq[j]));
+      }
     }
     cbar();
+    if (P.trace && t == 0) trace_mark(P, ii, 2);
     if (P.qk_norm) {
       const LayerW& W = layer_w(P, l);
       if (w <= rep) {
@@ -928,7 +1049,10 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
     }
     cbar();
     attn_mark(P, ii, 9);
-    const int n = e.hi - e.lo;
+    // (max, sum) of head w stay in lane 0 of warp w until the partial's
+    // outputs are stored: they are stored last, so a combining split that
+    // sees them finds the outputs written too (normally; it checks their tags)
+    float m_h = -INFINITY, s_h = 0.f;
     if (w < rep) {
       float m = -INFINITY;
       for (int j = lane; j < n; j += 32) m = fmaxf(m, sc[w * smax + j]);
@@ -940,10 +1064,8 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
         s += p;
       }
       s = warp_sum(s);
-      if (lane == 0) {
-        part[w * (D + 2) + D] = m;
-        part[w * (D + 2) + D + 1] = s;
-      }
+      m_h = m;
+      s_h = s;
     }
     cbar();
     // o = sum_j p_j v_j.  Lane owns DPL consecutive columns, warp w a head
@@ -1005,119 +1127,129 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
         const float pn = k == 0 ? p_new0 : k == 1 ? p_new1 : k == 2 ? p_new2 : p_new3;
         o = fmaf(pn, vn[c], o);
       }
-      part[h * (D + 2) + c] = o;
+      st_tagged(part + h * (D + 2) + c, o, ptag);
     }
-    // an empty split (n == 0) leaves max = -inf, sum = 0 from the softmax pass
+    cbar();  // every output of the partial is stored
+    if (w < rep && lane == 0) {
+      st_tagged(part + w * (D + 2) + D, m_h, ptag);
+      st_tagged(part + w * (D + 2) + D + 1, s_h, ptag);
+    }
+    attn_mark(P, ii, 10);
+  } else if (P.trace && t == 0) {
+    trace_mark(P, ii, 2);
   }
-  attn_mark(P, ii, 10);
-  cbar();
-  if (t == 0) {
-    uint32_t* arr = P.arrive + ((size_t)l * P.max_batch + b) * P.nkv + g;
-    const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
-    const bool last = old == (uint32_t)(NS - 1);
-    if (last) *arr = 0u;  // every split of this group has arrived: reset for the next step
-    S.flags[F_LAST] = last ? 1u : 0u;
-  }
-  cbar();
-  attn_mark(P, ii, 11);
-  if (S.flags[F_LAST]) {
-    if (e.live) {
-      // Combine the NS splits in split order: weights f_s = exp(m_s - max_s m_s)
-      // per head (staged in shared memory), o = sum_s f_s o_s / sum_s f_s l_s.
-      const float* gp = P.part + (((size_t)l * P.max_batch + b) * P.nkv + g) * NS * rep * (D + 2);
-      float* fw = S.xbuf;                 // [NS][rep] weights
-      float* lw = S.xbuf + NS * rep;      // [NS][rep] partial sums
-      float* linv = lw + NS * rep;        // [rep]
-      // Each thread's (head, column) outputs: their partial values are loaded
-      // CB splits at a time, every load of a batch in flight together; the
-      // first batch goes out with the (max, sum) loads.
-      constexpr int NO = (REP * D + NT - 1) / NT;
-      constexpr int CB = NO <= 1 ? 32 : NO <= 2 ? 20 : 8;
-      float v[NO][CB];
+  if ((in.flags & IF_COMBINE) && e.live) {
+    // Combine the group's live splits (those holding keys: ceil((pos + 1) /
+    // KPS) of them) in split order: weights f_s = exp(m_s - max_s m_s) per
+    // head (staged in shared memory), o = sum_s f_s o_s / sum_s f_s l_s.  Every
+    // partial is a bounded poll on its tags.
+    const int nl = (e.pos + P.kps) / P.kps;  // ceil((pos + 1) / KPS)
+    const u64* gp = P.part + (((size_t)l * P.max_batch + b) * P.nkv + g) * NS * rep * (D + 2);
+    cbar();  // the scratch in xbuf is free (this split's own work is done)
+    float* fw = S.xbuf;                 // [nl][rep] weights
+    float* lw = S.xbuf + NS * rep;      // [nl][rep] partial sums
+    float* linv = lw + NS * rep;        // [rep]
+    // This thread's (head, column) outputs: their partial values are read CB
+    // splits at a time (every load of a batch in flight together); the first
+    // batch goes out once every split's (max, sum) is in, so its round trip
+    // overlaps the weights' computation, and is checked afterwards.
+    constexpr int NO = (REP * D + NT - 1) / NT;
+    constexpr int CB = NO <= 1 ? 16 : NO <= 2 ? 20 : 8;
+    float v[NO][CB];
+    auto load_batch = [&](int s0) {
+      uint32_t bad = 0;
 #pragma unroll
       for (int k = 0; k < NO; ++k) {
         const int i = t + k * NT;
-        const float* pc = gp + (size_t)(i / D) * (D + 2) + (i % D);
+        const u64* pc = gp + (size_t)(i / D) * (D + 2) + (i % D);
 #pragma unroll
-        for (int u = 0; u < CB; ++u)
-          v[k][u] = (i < rep * D && u < NS) ? __ldcg(pc + (size_t)u * rep * (D + 2)) : 0.f;
-      }
-      for (int i = t; i < NS * rep; i += NT) {
-        const float* ps = gp + (size_t)i * (D + 2);
-        fw[i] = __ldcg(ps + D);
-        lw[i] = __ldcg(ps + D + 1);
-      }
-      cbar();
-      if (w < rep) {
-        float M = -INFINITY;
-        for (int s = lane; s < NS; s += 32) M = fmaxf(M, fw[s * rep + w]);
-        M = warp_max(M);
-        float Ls = 0.f;
-        for (int s = lane; s < NS; s += 32) {
-          const float ms = fw[s * rep + w];
-          const float f = ms == -INFINITY ? 0.f : expf(ms - M);
-          fw[s * rep + w] = f;
-          Ls = fmaf(lw[s * rep + w], f, Ls);
-        }
-        Ls = warp_sum(Ls);
-        if (lane == 0) linv[w] = 1.0f / Ls;
-      }
-      cbar();
-      // o = sum_s f_s o_s in split order
-      float O[NO];
-#pragma unroll
-      for (int k = 0; k < NO; ++k) O[k] = 0.f;
-      for (int s0 = 0; s0 < NS; s0 += CB) {
-        if (s0 > 0) {
-#pragma unroll
-          for (int k = 0; k < NO; ++k) {
-            const int i = t + k * NT;
-            const float* pc = gp + (size_t)(i / D) * (D + 2) + (i % D);
-#pragma unroll
-            for (int u = 0; u < CB; ++u)
-              v[k][u] = (i < rep * D && s0 + u < NS) ? __ldcg(pc + (size_t)(s0 + u) * rep * (D + 2)) : 0.f;
+        for (int u = 0; u < CB; ++u) {
+          if (i < rep * D && s0 + u < nl) {
+            const u64 wv = ld_tagged(pc + (size_t)(s0 + u) * rep * (D + 2));
+            v[k][u] = tag_val(wv);
+            bad |= tag_of(wv) ^ tag;
+          } else {
+            v[k][u] = 0.f;
           }
         }
-#pragma unroll
-        for (int k = 0; k < NO; ++k) {
-          const int h = (t + k * NT) / D;
-#pragma unroll
-          for (int u = 0; u < CB; ++u)
-            if (s0 + u < NS) O[k] = fmaf(v[k][u], fw[(s0 + u) * rep + h], O[k]);
-        }
       }
-#pragma unroll
-      for (int k = 0; k < NO; ++k) {
-        const int i = t + k * NT;
-        if (i < rep * D) {
-          const int h = i / D, c = i % D;
-          P.attn_out[((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c] = O[k] * linv[h];
-        }
-      }
+      return bad;
+    };
+    for (int i = t; i < nl * rep; i += NT) {
+      const u64* ps = gp + (size_t)i * (D + 2) + D;
+      u64 mw = 0, lw2 = 0;
+      poll_until(P, S, [&]() {
+        ld_tagged2(ps, mw, lw2);
+        return tag == 0u || ((tag_of(mw) ^ tag) | (tag_of(lw2) ^ tag)) == 0u;
+      }, ii);
+      fw[i] = tag_val(mw);
+      lw[i] = tag_val(lw2);
     }
     cbar();
-    if (t == 0 && P.mode == MODE_MEGA) red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+    attn_mark(P, ii, 11);
+    const uint32_t bad0 = load_batch(0);
+    if (w < rep) {
+      float M = -INFINITY;
+      for (int s = lane; s < nl; s += 32) M = fmaxf(M, fw[s * rep + w]);
+      M = warp_max(M);
+      float Ls = 0.f;
+      for (int s = lane; s < nl; s += 32) {
+        const float ms = fw[s * rep + w];
+        const float f = ms == -INFINITY ? 0.f : expf(ms - M);
+        fw[s * rep + w] = f;
+        Ls = fmaf(lw[s * rep + w], f, Ls);
+      }
+      Ls = warp_sum(Ls);
+      if (lane == 0) linv[w] = 1.0f / Ls;
+    }
+    cbar();
+    // o = sum_s f_s o_s in split order
+    float O[NO];
+#pragma unroll
+    for (int k = 0; k < NO; ++k) O[k] = 0.f;
+    for (int s0 = 0; s0 < nl; s0 += CB) {
+      if (s0 > 0 || (tag != 0u && bad0 != 0u))
+        poll_until(P, S, [&]() { return load_batch(s0) == 0u || tag == 0u; }, ii);
+#pragma unroll
+      for (int k = 0; k < NO; ++k) {
+        const int h = (t + k * NT) / D;
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+          if (s0 + u < nl) O[k] = fmaf(v[k][u], fw[(s0 + u) * rep + h], O[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NO; ++k) {
+      const int i = t + k * NT;
+      if (i < rep * D) {
+        const int h = i / D, c = i % D;
+        st_tagged(P.attn_out + ((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c,
+                  O[k] * linv[h], ptag);
+      }
+    }
   }
+  // no barrier here: the next instruction's slot hand-off orders every reuse
+  // of the shared scratch
 }
 
 template <int AD, int AREP>
 __device__ __forceinline__ void attn_dispatch(const KParams& P, const Sh& S, const Instr& in, const AttnExt& e,
-                              uint32_t ii, Ring& R) {
+                              uint32_t ii, uint32_t tag, Ring& R) {
   if constexpr (AD != 0) {
-    attn_tile<AD, AREP>(P, S, in, e, ii, R);
+    attn_tile<AD, AREP>(P, S, in, e, ii, tag, R);
   } else if (P.d == 128) {
     switch (P.rep) {
-      case 1: attn_tile<128, 1>(P, S, in, e, ii, R); break;
-      case 2: attn_tile<128, 2>(P, S, in, e, ii, R); break;
-      case 4: attn_tile<128, 4>(P, S, in, e, ii, R); break;
-      default: attn_tile<128, 8>(P, S, in, e, ii, R); break;
+      case 1: attn_tile<128, 1>(P, S, in, e, ii, tag, R); break;
+      case 2: attn_tile<128, 2>(P, S, in, e, ii, tag, R); break;
+      case 4: attn_tile<128, 4>(P, S, in, e, ii, tag, R); break;
+      default: attn_tile<128, 8>(P, S, in, e, ii, tag, R); break;
     }
   } else {
     switch (P.rep) {
-      case 1: attn_tile<64, 1>(P, S, in, e, ii, R); break;
-      case 2: attn_tile<64, 2>(P, S, in, e, ii, R); break;
-      case 4: attn_tile<64, 4>(P, S, in, e, ii, R); break;
-      default: attn_tile<64, 8>(P, S, in, e, ii, R); break;
+      case 1: attn_tile<64, 1>(P, S, in, e, ii, tag, R); break;
+      case 2: attn_tile<64, 2>(P, S, in, e, ii, tag, R); break;
+      case 4: attn_tile<64, 4>(P, S, in, e, ii, tag, R); break;
+      default: attn_tile<64, 8>(P, S, in, e, ii, tag, R); break;
     }
   }
 }
@@ -1149,9 +1281,6 @@ __device__ void consumer(const KParams& P, const Sh& S) {
   // both widths (every operator change reloads it anyway).
   float xr[XM][8];
   uint32_t tag_x = 0xffffffffu;
-  // Last barrier (and target) thread 0 saw satisfied: counters only grow
-  // within a launch, so a repeat wait needs no new load.
-  uint32_t ok_bar = NO_BAR, ok_target = 0;
   for (;;) {
     const int si = islot_ctr % NISLOT;
     // The broadcast words are double-buffered by instruction parity: warps
@@ -1160,28 +1289,23 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     const int f_slot = (islot_ctr & 1u) ? F_SLOT_B : F_SLOT;
     const int f_abort = (islot_ctr & 1u) ? F_ABORT_B : F_ABORT;
     const uint64_t t_top = (P.trace && t == 0) ? globaltimer() : 0;
-    // one thread takes the slot (a bounded wait)
+    // One thread takes the slot (a bounded wait) and hands it, with the stop
+    // verdict, to every consumer thread through one consumer barrier.  The
+    // tiles' dependencies are not waited on here: each tile polls the tags of
+    // the words it reads (poll_until).  Only the multi-step launch keeps one
+    // counter wait: a later step's layer-0 projection starts from the token
+    // the previous step chose, once all of that step's LM-head tiles counted.
     if (t == 0) {
       uint32_t v = 0xffffffffu;
       if (mbar_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u)) v = *slot_index(S, si);
       S.flags[f_slot] = v;
-    }
-    // Thread 0 also waits on the tiles the instruction reads (the abort word is
-    // read only while spinning: a launch that never waits on an unsatisfied
-    // counter runs to completion anyway); one consumer barrier then hands the
-    // slot and the verdict to every consumer thread.
-    if (t == 0) {
-      const uint32_t sv = S.flags[f_slot];
-      const uint32_t iv = (!MS || sv == END_SLOT) ? sv : sv & ((1u << SLOT_INDEX_BITS) - 1u);
-      const uint32_t step0 = (!MS || sv == END_SLOT) ? 0u : sv >> SLOT_INDEX_BITS;
+      const uint32_t iv = (!MS || v == END_SLOT) ? v : v & ((1u << SLOT_INDEX_BITS) - 1u);
+      const uint32_t step0 = (!MS || v == END_SLOT) ? 0u : v >> SLOT_INDEX_BITS;
       uint32_t aborted = S.flags[F_STOP];
       const uint64_t t_begin = P.trace ? globaltimer() : 0;
-      if (iv != END_SLOT) {
+      if (MS && iv != END_SLOT && !aborted && step0 > 0) {
         const Instr& in0 = *slot_instr(S, si);
-        // a later step of a multi-step launch starts from the token the
-        // previous step chose: the layer-0 projection waits for all of that
-        // step's LM-head tiles
-        if (MS && !aborted && step0 > 0 && in0.op == OP_QKV && in0.layer == 0) {
+        if (in0.op == OP_QKV && in0.layer == 0) {
           const uint64_t t0 = globaltimer();
           while ((int32_t)(ld_acquire_gpu(P.lm_done + (step0 - 1)) - P.n_lm_tiles) < 0) {
             if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) {
@@ -1194,30 +1318,6 @@ __device__ void consumer(const KParams& P, const Sh& S) {
             __nanosleep(32);
           }
         }
-        if (!aborted && P.mode == MODE_MEGA && in0.wait_bar != NO_BAR) {
-          const uint32_t target = (gen + step0 + 1u) * in0.wait_target;
-          if (!(in0.wait_n == 1 && in0.wait_bar == ok_bar && target == ok_target)) {
-            const uint64_t t0 = globaltimer();
-            for (uint32_t k = 0; k < in0.wait_n && !aborted;) {
-              const uint32_t* c = &P.bars[in0.wait_bar + k * in0.wait_stride];
-              if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
-                ++k;
-                continue;
-              }
-              if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) aborted = 1;
-              else if (globaltimer() - t0 > P.wait_limit_ns) {
-                set_error(P, MK_ERR_TIMEOUT, iv);
-                aborted = 1;
-              } else {
-                __nanosleep(32);
-              }
-            }
-            if (!aborted && in0.wait_n == 1) {
-              ok_bar = in0.wait_bar;
-              ok_target = target;
-            }
-          }
-        }
       }
       S.flags[f_abort] = aborted;
       if (aborted) S.flags[F_STOP] = 1u;  // the producer stops popping
@@ -1225,7 +1325,6 @@ __device__ void consumer(const KParams& P, const Sh& S) {
         unsigned long long* tr = P.trace + (size_t)iv * TRACE_WORDS;
         tr[12] = t_top;
         tr[1] = t_begin;
-        tr[2] = globaltimer();
         R.cur = iv;
       }
     }
@@ -1250,30 +1349,33 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       drain(P, S, in, ext, R);
       continue;
     }
+    const uint32_t tag = step_tag(P, gen, step);
     // The batch-1 GEMV tiles (most instructions) come first in the code, so
     // their dispatch path stays short and contiguous; the finisher stores and
-    // releases them.
+    // publishes them.
     if (MH > 0 && P.B == 1 && in.op != OP_ATTN) {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      const uint32_t tag = (uint32_t)in.op | ((uint32_t)in.layer << 8) | (step << 24);
+      const uint32_t xtag = (uint32_t)in.op | ((uint32_t)in.layer << 8) | (step << 24);
       if (in.op != OP_DOWN) {
         auto& xh = *reinterpret_cast<float(*)[XH][8]>(&xr);
-        if (tag != tag_x) {
-          load_x_fast<XH>(P, S, in, xh, step);
-          tag_x = tag;
+        if (xtag != tag_x) {
+          load_x_fast<XH>(P, S, in, xh, step, tag);
+          tag_x = xtag;
         }
-        gemv_fast<XH, MS>(P, S, in, i, step, g, src, R, xh);
+        if (P.trace && t == 0) trace_mark(P, i, 2);
+        gemv_fast<XH, MS>(P, S, in, i, step, tag, g, src, R, xh);
       } else {
         auto& xf = *reinterpret_cast<float(*)[XF][8]>(&xr);
-        if (tag != tag_x) {
-          load_x_plain<XF>(gemv_x(P, in), xf);
-          tag_x = tag;
+        if (xtag != tag_x) {
+          load_x_plain<XF>(P, S, gemv_x(P, in), xf, tag);
+          tag_x = xtag;
         }
-        gemv_fast<XF, MS>(P, S, in, i, step, g, src, R, xf);
+        if (P.trace && t == 0) trace_mark(P, i, 2);
+        gemv_fast<XF, MS>(P, S, in, i, step, tag, g, src, R, xf);
       }
     } else if (in.op == OP_ATTN) {
-      attn_dispatch<AD, AREP>(P, S, in, ext, i, R);
+      attn_dispatch<AD, AREP>(P, S, in, ext, i, tag, R);
       // Every GEMV after attention reloads its activations; overwriting the
       // register copies here makes them dead during the attention tile, so
       // attention does not have to spill around them.
@@ -1285,12 +1387,10 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      const float pre = epilogue_prefetch(P, in, g, t);
-      gemv_generic(P, S, in, g, src, R);
-      gemv_epilogue(P, S.red, in, g, pre, t);
-      cbar();
-      if (t == 0 && P.mode == MODE_MEGA && in.rel_bar != NO_BAR)
-        red_release_gpu_add(&P.bars[in.rel_bar], 1u);
+      const float pre = epilogue_prefetch(P, S, in, g, t, tag);
+      gemv_generic(P, S, in, g, src, R, tag);
+      if (P.trace && t == 0) trace_mark(P, i, 2);
+      gemv_epilogue(P, S.red, in, g, pre, t, pub_tag(in, tag));
     }
     if (P.trace && t == 0) {
       unsigned long long* tr = P.trace + (size_t)i * TRACE_WORDS;
@@ -1301,7 +1401,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     R.wait_ns = 0;
     R.first_done = false;
     R.handed = false;
-    // no barrier here: the next instruction's slot and dependency barriers
+    // no barrier here: the next instruction's slot and the tiles' own barriers
     // order every reuse of the shared scratch
   }
   // tell the finisher that no more tiles come
@@ -1341,12 +1441,14 @@ __device__ void lm_tile_choose(const KParams& P, const GemvDesc& g, uint32_t ste
 
 // ---------------------------------------------------------------- finisher warp
 // Takes the batch-1 GEMV tiles in hand-off order: adds up the consumer warps'
-// partial sums (fixed order), frees the buffer, stores the outputs (residual
-// adds, SwiGLU) and releases the tile's counter.  Its store latency and the
-// release fence stay off the consumers' path.
+// partial sums (fixed order), frees the buffer and stores the outputs
+// (residual adds, SwiGLU) as tagged words, which publishes them: the
+// consumers poll the tags, so no fence or counter release follows and the
+// store latency stays off the consumers' path.
 template <bool MS>
 __device__ void finisher(const KParams& P, const Sh& S) {
   const int lane = threadIdx.x & 31;
+  const uint32_t gen = S.flags[F_GEN];
   for (uint32_t h = 0;; ++h) {
     const int hb = (int)(h & 1u);
     if (!mbar_wait(P, &S.hfull[hb], (h >> 1) & 1u)) break;
@@ -1368,11 +1470,10 @@ __device__ void finisher(const KParams& P, const Sh& S) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.hempty[hb]);
     if (P.trace && lane == 0) P.trace[(size_t)ii * TRACE_WORDS + 14] = globaltimer();
-    gemv_epilogue(P, S.fin, in, g, pre, lane);
+    gemv_epilogue(P, S.fin, in, g, pre, lane, pub_tag(in, step_tag(P, gen, step)));
     __syncwarp();
     if (MS && in.op == OP_LM) lm_tile_choose(P, g, step, lane);
     if (lane == 0) {
-      if (P.mode == MODE_MEGA && in.rel_bar != NO_BAR) red_release_gpu_add(&P.bars[in.rel_bar], 1u);
       if (P.trace) {
         unsigned long long* tr = P.trace + (size_t)ii * TRACE_WORDS;
         tr[9] = t_take;
@@ -1457,11 +1558,14 @@ struct VariantImpl {
     return cudaLaunchCooperativeKernel((const void*)mk_interpreter<MH, MF, AD, AREP, MH != 0>, dim3(ctas),
                                        dim3(NTHREADS), args, (size_t)SmemLayout::total, st);
   }
-  static cudaError_t perop(const KParams& p, uint32_t first, uint32_t count, cudaStream_t st) {
+  // one launch of an operator's `count` tiles on at most `ctas` CTAs
+  static cudaError_t perop(const KParams& p, uint32_t first, uint32_t count, int ctas, cudaStream_t st) {
     KParams pp = p;
     pp.mode = MODE_PEROP;
     pp.perop_base = first;
-    mk_interpreter<MH, MF, AD, AREP, false><<<count, NTHREADS, SmemLayout::total, st>>>(pp);
+    pp.perop_count = count;
+    const uint32_t grid = count < (uint32_t)ctas ? count : (uint32_t)ctas;
+    mk_interpreter<MH, MF, AD, AREP, false><<<grid, NTHREADS, SmemLayout::total, st>>>(pp);
     return cudaGetLastError();
   }
 };

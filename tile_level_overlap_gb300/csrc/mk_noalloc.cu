@@ -30,15 +30,6 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MK_NOALLOC_SCRATCH_BY
 constexpr int kMaxDevices = 64;
 uint8_t* g_scratch_addr[kMaxDevices] = {nullptr};  // device address of the array, per device
 
-struct Take {
-  size_t off = 0;
-  size_t take(size_t bytes) {
-    size_t o = off;
-    off += (bytes + 255) & ~(size_t)255;
-    return o;
-  }
-};
-
 KernelVariant variant_for(const HostPlan& hp) {
   const mk_model_cfg& c = hp.cfg;
   if (hp.fast_b1) {
@@ -100,24 +91,10 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   }
   if (!good) return MK_ERR_INVALID_ARG;
 
-  // Carve the static array: the same buffers a plan allocates, one queue copy.
-  const size_t B = (size_t)max_batch;
-  Take t;
-  const size_t o_resid = t.take(sizeof(float) * (2 * L + 1) * B * H);
-  const size_t o_qkv = t.take(sizeof(float) * L * B * hp.qkv_rows);
-  const size_t o_part = t.take(sizeof(float) * L * B * nkv * hp.n_splits * hp.rep * (d + 2));
-  const size_t o_attn = t.take(sizeof(float) * L * B * c.n_q_heads * d);
-  const size_t o_act = t.take(sizeof(float) * L * B * F);
-  const size_t o_zero = t.off;  // everything from here to o_zero_end starts at zero
-  const size_t o_bars = t.take(sizeof(uint32_t) * hp.bl.total);
-  const size_t o_arr = t.take(sizeof(uint32_t) * L * B * nkv);
-  const size_t o_ctl = t.take(sizeof(uint32_t) * CTL_WORDS);
-  const size_t o_zero_end = t.off;
-  const size_t o_q = t.take(sizeof(Instr) * hp.decode.size());
-  const size_t o_expr = t.take(sizeof(uint32_t) * hp.expr.size());
-  const size_t o_rope = t.take(sizeof(float2) * (size_t)max_ctx * (d / 2));
-  const size_t o_lw = t.take(sizeof(LayerW) * L);
-  if (t.off > (size_t)MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_UNSUPPORTED;
+  // Carve the static array: the decode layout a plan allocates (one queue copy).
+  const DecodeScratch ds = decode_scratch(hp);
+  if (ds.total > (size_t)MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_UNSUPPORTED;
+  const size_t o_q = ds.o_q, o_expr = ds.o_expr, o_rope = ds.o_rope, o_lw = ds.o_lw;
 
   // Per-device set-up on the first call with that device current: the array's
   // device address and the kernel's shared-memory attribute.
@@ -150,7 +127,11 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
                       st) != cudaSuccess ||
       cudaMemcpyAsync(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice, st) !=
           cudaSuccess ||
-      cudaMemsetAsync(s + o_zero, 0, o_zero_end - o_zero, st) != cudaSuccess)
+      // every call restarts the launch counter at 0, so the tagged
+      // intermediate tensors, the counters and the control words all start
+      // at zero (no word left by an earlier call, of any shape, carries a tag
+      // this call expects)
+      cudaMemsetAsync(s, 0, ds.zero_end, st) != cudaSuccess)
     return MK_ERR_CUDA;
 
   KParams k;
@@ -165,15 +146,15 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   k.lm = (const uint16_t*)(c.tied_embeddings ? w->embed : w->lm_head);
   k.final_norm = (const uint16_t*)w->final_norm;
   k.layers = (const LayerW*)(s + o_lw);
-  k.resid = (float*)(s + o_resid);
-  k.qkv = (float*)(s + o_qkv);
-  k.part = (float*)(s + o_part);
-  k.attn_out = (float*)(s + o_attn);
-  k.act = (float*)(s + o_act);
-  k.bars = (uint32_t*)(s + o_bars);
-  k.arrive = (uint32_t*)(s + o_arr);
+  k.resid = (u64*)(s + ds.o_resid);
+  k.qkv = (u64*)(s + ds.o_qkv);
+  k.part = (u64*)(s + ds.o_part);
+  k.attn_out = (u64*)(s + ds.o_attn);
+  k.act = (u64*)(s + ds.o_act);
+  k.kps = hp.kps;
+  k.bars = (uint32_t*)(s + ds.o_bars);
   k.rope = (const float2*)(s + o_rope);
-  k.ctl = (uint32_t*)(s + o_ctl);
+  k.ctl = (uint32_t*)(s + ds.o_ctl);
   k.queue = (const Instr*)(s + o_q);
   k.n_instr = (uint32_t)hp.decode.size();
   k.expr = (const uint32_t*)(s + o_expr);

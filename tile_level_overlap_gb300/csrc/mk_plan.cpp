@@ -6,12 +6,15 @@
 // row tiles of g's heads; every other dependency of a decode step is a
 // reduction over the whole hidden vector (the RMSNorm before QKV / gate-up and
 // the input dimension of O / down), so those barriers count every producer
-// tile of the operator.  Barrier counters are never cleared: a launch of
-// generation `gen` waits for (gen + 1) * target releases
-// ("Lecture 112: Production Megakernels for Real-World Inference", Key
-// takeaways: barriers held as tensors).  Extents that depend on the batch or a
-// sequence's cached length are expressions evaluated on the device, so the
-// queue does not change with them (same source, symbolic shapes in S and P).
+// tile of the operator ("Lecture 112: Production Megakernels for Real-World
+// Inference", Key takeaways: barriers held as tensors).  The counters define
+// the DAG that the host simulator and the random topological orders check;
+// on the device the decode interpreter enforces the same dependencies through
+// the tag each element of an intermediate tensor carries (mk_device.cuh), a
+// barrier tensor partitioned down to single elements.  Extents that depend on
+// the batch or a sequence's cached length are expressions evaluated on the
+// device, so the queue does not change with them (same source, symbolic
+// shapes in S and P).
 #include "mk_plan.h"
 
 #include <algorithm>
@@ -19,7 +22,6 @@
 #include "mk_variants.h"
 #include <cstring>
 #include <random>
-#include <unordered_map>
 
 namespace mk {
 
@@ -151,38 +153,40 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
   hp.n_down_tiles = ceil_div(H, hp.r_down);
   hp.n_lm_tiles = ceil_div(c.vocab, hp.r_lm);
 
-  // Split-KV partitions per (sequence, kv head): one attention tile per SM
-  // (a single round: the phase is latency-bound, a second round doubles it),
-  // at most SCORE_FLOATS/rep keys per split, at least 32.
+  // Split-KV partitions per (sequence, kv head): a fixed number of keys per
+  // split (a model constant, keys_per_split), so which keys each partial
+  // holds -- and with it every bit of the result -- depends only on the model
+  // and the sequence's cached length, never on the device's SM count or the
+  // plan's max_batch.  The queue holds ceil(max_ctx / KPS) splits per group;
+  // splits past a sequence's keys are empty and cost one pop.
+  hp.kps = keys_per_split(d);
   hp.split_max = SCORE_FLOATS / rep;
-  int ns = n_sms / (max_batch * nkv);
-  ns = std::max(ns, (int)ceil_div(max_ctx, hp.split_max));
-  ns = std::min(ns, (int)std::max<uint32_t>(ceil_div(max_ctx, 32), ceil_div(max_ctx, hp.split_max)));
-  ns = std::max(ns, 1);
+  if (hp.kps > hp.split_max) return bad(MK_ERR_UNSUPPORTED, "keys per split above the score buffer");
+  const int ns = std::max(1, (int)ceil_div(max_ctx, hp.kps));
   hp.n_splits = ns;
   if (hp.n_splits > 0xffff || 2L * hp.n_splits * rep + rep > XBUF_FLOATS)
-    return bad(MK_ERR_UNSUPPORTED, "too many split-KV partitions for the combine buffer");
+    return bad(MK_ERR_UNSUPPORTED, "max_ctx needs more split-KV partitions than the combine buffer holds");
 
   // Barrier tensor layout.
   BarLayout& bl = hp.bl;
   bl.qkv = 0;
-  bl.attn = bl.qkv + L * nkv;
+  bl.split = bl.qkv + L * nkv;
+  bl.attn = bl.split + L * max_batch * nkv;
   bl.o = bl.attn + L;
   bl.gu = bl.o + L;
   bl.down = bl.gu + L;
   bl.lm = bl.down + L;
   bl.total = bl.lm + 1;
 
-  // Symbolic extents.  n = P[a0] + 1 keys; chunk = ceil(n / NS).
+  // Symbolic extents.  n = P[a0] + 1 keys; split a2 holds keys
+  // [a2 * KPS, (a2 + 1) * KPS) clipped to n.
   hp.expr.assign((size_t)XS_COUNT * X_MAX_WORDS, 0);
   {
-    XBuild lo;  // min(a2 * chunk, n)
-    lo.op(X_ARG2).op(X_ARG0).op(X_POS).c(1).op(X_ADD).c(ns).op(X_CEILDIV).op(X_MUL)
-        .op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
+    XBuild lo;  // min(a2 * KPS, n)
+    lo.op(X_ARG2).c(hp.kps).op(X_MUL).op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
     put_expr(hp.expr, XS_ATTN_LO, lo);
-    XBuild hi;  // min((a2 + 1) * chunk, n)
-    hi.op(X_ARG2).c(1).op(X_ADD).op(X_ARG0).op(X_POS).c(1).op(X_ADD).c(ns).op(X_CEILDIV)
-        .op(X_MUL).op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
+    XBuild hi;  // min((a2 + 1) * KPS, n)
+    hi.op(X_ARG2).c(1).op(X_ADD).c(hp.kps).op(X_MUL).op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
     put_expr(hp.expr, XS_ATTN_HI, hi);
     XBuild live;  // B - a0
     live.op(X_B).op(X_ARG0).op(X_SUB);
@@ -213,17 +217,34 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
     }
     range_end(b0);
     b0 = range_begin();
+    // The last split of each (sequence, kv head) group also combines the
+    // group's partials: it waits on the other splits (its own inputs are
+    // ready once they are, since they waited on the same QKV tiles).  The
+    // combining splits of a layer follow all its other splits, so the
+    // kernel-per-operator runner launches them as their own operator.
     for (int b = 0; b < max_batch; ++b)
       for (int g = 0; g < nkv; ++g)
-        for (int s = 0; s < ns; ++s) {
+        for (int s = 0; s + 1 < ns; ++s) {
           Instr in = make(OP_ATTN, l, b, g, (uint16_t)s);
-          in.flags = IF_RELEASE_ON_COMBINE;
           in.x_lo = XS_ATTN_LO;
           in.x_hi = XS_ATTN_HI;
           set_wait(in, bl.qkv + l * nkv + g, per_group);
-          in.rel_bar = bl.attn + l;
+          in.rel_bar = bl.split + ((uint32_t)l * max_batch + b) * nkv + g;
           q.push_back(in);
         }
+    range_end(b0);
+    b0 = range_begin();
+    for (int b = 0; b < max_batch; ++b)
+      for (int g = 0; g < nkv; ++g) {
+        Instr in = make(OP_ATTN, l, b, g, (uint16_t)(ns - 1));
+        in.x_lo = XS_ATTN_LO;
+        in.x_hi = XS_ATTN_HI;
+        in.flags = IF_COMBINE;
+        if (ns > 1) set_wait(in, bl.split + ((uint32_t)l * max_batch + b) * nkv + g, (uint32_t)(ns - 1));
+        else set_wait(in, bl.qkv + l * nkv + g, per_group);
+        in.rel_bar = bl.attn + l;
+        q.push_back(in);
+      }
     range_end(b0);
     b0 = range_begin();
     for (int r = 0; r < H; r += hp.r_o) {
@@ -264,22 +285,41 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
   return MK_OK;
 }
 
-namespace {
-
-// Group key of a split-KV instruction: (layer, sequence, kv head).
-uint64_t group_key(const Instr& in) {
-  return ((uint64_t)in.layer << 40) | ((uint64_t)in.a0 << 20) | (uint64_t)in.a1;
+DecodeScratch decode_scratch(const HostPlan& hp) {
+  const mk_model_cfg& c = hp.cfg;
+  const size_t L = (size_t)c.n_layers, B = (size_t)hp.max_batch, H = (size_t)c.hidden;
+  const size_t d = (size_t)c.head_dim, nkv = (size_t)c.n_kv_heads;
+  const size_t w = sizeof(unsigned long long);  // one tagged word per element
+  DecodeScratch x{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  x.o_resid = take(w * (2 * L + 1) * B * H);
+  x.o_qkv = take(w * L * B * hp.qkv_rows);
+  x.o_part = take(w * L * B * nkv * hp.n_splits * hp.rep * (d + 2));
+  x.o_attn = take(w * L * B * c.n_q_heads * d);
+  x.o_act = take(w * L * B * c.ffn);
+  x.tagged_end = off;
+  x.o_bars = take(sizeof(uint32_t) * hp.bl.total);
+  x.o_ctl = take(sizeof(uint32_t) * CTL_WORDS);
+  x.zero_end = off;
+  x.o_q = take(sizeof(Instr) * hp.decode.size());
+  x.o_expr = take(sizeof(uint32_t) * hp.expr.size());
+  x.o_rope = take(sizeof(float2) * (size_t)hp.max_ctx * (d / 2));
+  x.o_lw = take(sizeof(LayerW) * L);
+  x.total = off;
+  return x;
 }
+
+namespace {
 
 // Apply `in`'s release to the counters; returns the barrier that received +1,
 // or NO_BAR.
-uint32_t apply_release(const HostPlan& hp, const Instr& in, std::vector<uint32_t>& cnt,
-                       std::unordered_map<uint64_t, int>& arrivals) {
+uint32_t apply_release(const Instr& in, std::vector<uint32_t>& cnt) {
   if (in.rel_bar == NO_BAR) return NO_BAR;
-  if (in.flags & IF_RELEASE_ON_COMBINE) {
-    int& a = arrivals[group_key(in)];
-    if (++a < hp.n_splits) return NO_BAR;
-  }
   cnt[in.rel_bar] += 1;
   return in.rel_bar;
 }
@@ -307,7 +347,6 @@ void random_topological(const HostPlan& hp, const std::vector<Instr>& q, uint64_
     }
   }
   std::mt19937_64 rng(seed);
-  std::unordered_map<uint64_t, int> arrivals;
   out->clear();
   out->reserve(q.size());
   while (!ready.empty()) {
@@ -316,7 +355,7 @@ void random_topological(const HostPlan& hp, const std::vector<Instr>& q, uint64_
     ready[pick] = ready.back();
     ready.pop_back();
     out->push_back(q[i]);
-    uint32_t b = apply_release(hp, q[i], cnt, arrivals);
+    uint32_t b = apply_release(q[i], cnt);
     if (b != NO_BAR && cnt[b] == target[b])
       for (uint32_t w : waiters[b])
         if (--unmet[w] == 0) ready.push_back(w);
@@ -325,7 +364,6 @@ void random_topological(const HostPlan& hp, const std::vector<Instr>& q, uint64_
 
 int simulate(const HostPlan& hp, const std::vector<Instr>& q, std::string* why) {
   std::vector<uint32_t> cnt(hp.bl.total, 0);
-  std::unordered_map<uint64_t, int> arrivals;
   for (size_t i = 0; i < q.size(); ++i) {
     const Instr& in = q[i];
     if (in.op == OP_NOP || in.op >= OP_COUNT) {
@@ -342,7 +380,7 @@ int simulate(const HostPlan& hp, const std::vector<Instr>& q, std::string* why) 
           return MK_ERR_INVALID_ARG;
         }
       }
-    apply_release(hp, in, cnt, arrivals);
+    apply_release(in, cnt);
   }
   for (size_t i = 0; i < q.size(); ++i) {
     const Instr& in = q[i];

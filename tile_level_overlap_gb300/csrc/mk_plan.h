@@ -31,10 +31,18 @@ MK_HD constexpr int fast_rps(int m) { return m >= 8 ? 1 : 8 / m; }
 
 constexpr int DEFAULT_SMS = 152;  // SMs of a GB300
 
+// Keys per decode-attention split, a constant of the model shape (head_dim):
+// 216 keys at head_dim 128 and 64 keys at head_dim 64, so that 4096 and 1024
+// cached keys with 8 kv heads (the Llama-3-8B and Llama-3.2-1B decode shapes)
+// give about one attention tile per SM of a 152-SM GB300 (the phase is
+// latency-bound: a second round of tiles doubles it).  Multiples of 8 (one
+// tensor-core score product).
+MK_HD constexpr int keys_per_split(int head_dim) { return head_dim >= 128 ? 216 : 64; }
+
 struct HostPlan {
   mk_model_cfg cfg{};
   int max_batch = 0, max_ctx = 0;
-  int rep = 0, qkv_rows = 0, n_splits = 0, split_max = 0;
+  int rep = 0, qkv_rows = 0, n_splits = 0, split_max = 0, kps = 0;
   int r_qkv = 0, r_o = 0, r_gu = 0, r_down = 0, r_lm = 0;
   uint32_t n_qkv_tiles = 0, n_o_tiles = 0, n_gu_tiles = 0, n_down_tiles = 0, n_lm_tiles = 0;
   bool fast_b1 = false;     // every GEMV K allows the batch-1 register path
@@ -47,10 +55,25 @@ struct HostPlan {
 
 // Validate the shape and build the plan.  Returns MK_OK or an MK_ERR_* code
 // with a reason in *why.
-// n_sms: SMs of the device the plan runs on (sets the split-KV count so that
-// one round of attention tiles covers the SMs); 0 = DEFAULT_SMS.
+// n_sms: SMs of the device the plan runs on (sets the row tiling of the
+// projections in whole rounds over the SMs; results do not depend on it);
+// 0 = DEFAULT_SMS.
 int build_plan(const mk_model_cfg& cfg, int max_batch, int max_ctx, int n_sms, HostPlan* out,
                std::string* why);
+
+// Device scratch of a decode plan: offsets into one allocation (256-byte
+// aligned), shared by mk_plan_create and mk_decode_step_noalloc.  The tagged
+// intermediate tensors ([o_resid, tagged_end)) must be zero before the first
+// launch and whenever the launch counter (CTL_GEN) is cleared, so that no
+// stale word carries a tag a later launch expects; the barrier counters and
+// control words follow them ([o_bars, zero_end) must start at zero too).
+struct DecodeScratch {
+  size_t o_resid, o_qkv, o_part, o_attn, o_act, tagged_end;
+  size_t o_bars, o_ctl, zero_end;
+  size_t o_q, o_expr, o_rope, o_lw;
+  size_t total;
+};
+DecodeScratch decode_scratch(const HostPlan& hp);
 
 // A seeded random topological order of queue `q` (Kahn's algorithm on the
 // barrier counters).  Any topological order is a valid pop order.

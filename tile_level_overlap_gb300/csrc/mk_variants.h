@@ -15,7 +15,7 @@ struct KernelVariant {
   cudaError_t (*occupancy)(int* per_sm);
   cudaError_t (*mega)(const KParams& p, int ctas, cudaStream_t st);
   cudaError_t (*mega_steps)(const KParams& p, int ctas, cudaStream_t st);  // mk_decode_steps
-  cudaError_t (*perop)(const KParams& p, uint32_t first, uint32_t count, cudaStream_t st);
+  cudaError_t (*perop)(const KParams& p, uint32_t first, uint32_t count, int ctas, cudaStream_t st);
 };
 
 // Shapes with a batch-1 register-path specialisation (K = M * 2048).

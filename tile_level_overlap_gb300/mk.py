@@ -33,7 +33,7 @@ EXPORTED = [
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
     "mk_plan_set_lm_mode", "mk_decode_steps", "mk_prefill_logits", "mk_prefill_batch",
-    "mk_decode_step_slots",
+    "mk_decode_step_slots", "mk_plan_create_for_sms",
 ]
 
 
@@ -59,7 +59,7 @@ class mk_plan_stats(ctypes.Structure):
                 ("n_barriers", ctypes.c_uint32), ("n_launches_per_op_decode", ctypes.c_uint32),
                 ("n_ctas", ctypes.c_uint32), ("n_splits", ctypes.c_uint32),
                 ("weight_bytes", ctypes.c_uint64), ("scratch_bytes", ctypes.c_uint64),
-                ("decode_path", ctypes.c_uint32)]
+                ("decode_path", ctypes.c_uint32), ("queue_hash", ctypes.c_uint64)]
 
 
 _lib = None
@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
     vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
     L.mk_plan_create.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs),
                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)]
+    L.mk_plan_create_for_sms.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs),
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)]
     L.mk_plan_destroy.argtypes = [vp]
     L.mk_plan_destroy.restype = None
     L.mk_kv_cache_bytes.argtypes = [vp]
@@ -179,7 +181,10 @@ class Plan:
     produced by synth.make_weights).  Keeps references so the weights outlive
     the plan."""
 
-    def __init__(self, cfg, weights: Dict[str, "object"], max_batch: int, max_ctx: int):
+    def __init__(self, cfg, weights: Dict[str, "object"], max_batch: int, max_ctx: int,
+                 n_sms: int = 0):
+        """n_sms > 0 (test-only): tile and launch the plan as on a device with
+        that many SMs (mk_plan_create_for_sms)."""
         L = lib()
         self.cfg = cfg
         self.max_batch = max_batch
@@ -202,8 +207,8 @@ class Plan:
         for k, a in self._arrays.items():
             setattr(wp, k, ctypes.cast(a, _PP) if a is not None else None)
         h = ctypes.c_void_p()
-        _check(L.mk_plan_create(ctypes.byref(model_cfg(cfg)), ctypes.byref(wp), max_batch, max_ctx,
-                                ctypes.byref(h)), "mk_plan_create")
+        _check(L.mk_plan_create_for_sms(ctypes.byref(model_cfg(cfg)), ctypes.byref(wp), max_batch,
+                                        max_ctx, int(n_sms), ctypes.byref(h)), "mk_plan_create")
         self.h = h
 
     def close(self):
