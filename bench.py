@@ -15,8 +15,8 @@ the cached and new K/V), and the comparison legs.
 the same step for profiling; the default is the headline workload.
 
 --impl reference times the CPU oracle (plain NumPy forward pass) on the host
-cores on a bounded sample of the same workload (a few layers + the LM head per
-step, scaled to the full layer count).
+cores: one whole decode step of the same workload per step (--ref-layers N
+times N layers + the LM head instead, scaled to the full layer count).
 """
 from __future__ import annotations
 
@@ -37,6 +37,8 @@ METRIC = "decode tokens/s and HBM GB/s (% of ~8 TB/s), Llama-3-8B shape, batch 1
 UNIT = "tokens/s"
 PREFILL_TOKENS = 2048
 MULTI_STEPS = 8  # tokens per launch of the multi-step greedy decode leg
+DEP_WAIT_STEPS = 5  # traced steps the dependency-wait share is averaged over
+BATCHED_LEGS = ("llama3-8b-b8", "qwen3-8b-b32")
 # name -> (shape in synth, batch, largest cached context, smallest (ragged
 # contexts U[lo, ctx], seeded) or None (all at ctx), metric, description,
 # traffic key)
@@ -214,26 +216,40 @@ def cpu_cores() -> int:
 
 # ---------------------------------------------------------------- reference arm: the oracle
 class OracleSample:
-    """The CPU oracle on a bounded sample of the decode step: `n_layers_sample`
-    layers + the LM head (weights drawn on the CPU with the same recipe)."""
+    """The CPU oracle on the decode step: `n_layers_sample` layers + the LM
+    head per step (0 or the model's depth = the whole model, no scaling).
+    Weights are the caller's tensors copied to the host, else drawn with the
+    same recipe (on the GPU when one is present, for speed)."""
 
-    def __init__(self, cfg, n_layers_sample: int, positions, seed: int = 0):
+    def __init__(self, cfg, n_layers_sample: int, positions, weights=None, seed: int = 0):
         import torch
 
         from tile_level_overlap_gb300 import synth
 
         torch.set_num_threads(cpu_cores())
         self.cfg = cfg
-        self.n = n_layers_sample
-        self.sub = cfg.replace(n_layers=n_layers_sample)
-        self.w = synth.weights_as_bits(synth.make_weights(self.sub, seed=seed, device="cpu"))
+        self.n = cfg.n_layers if n_layers_sample <= 0 else min(n_layers_sample, cfg.n_layers)
+        self.sub = cfg.replace(n_layers=self.n)
+        if weights is None:
+            dev = "cuda" if torch.cuda.is_available() else "cpu"
+            weights = synth.make_weights(self.sub, seed=seed, device=dev)
+        names = synth.weight_shapes(self.sub)
+        self.w = {k: synth.bf16_bits(weights[k]) for k in names}
         self.positions = list(positions)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
         self.kv = synth.bf16_bits(synth.make_kv_cache(self.sub, len(self.positions),
-                                                      max(self.positions) + 1, device="cpu"))
+                                                      max(self.positions) + 1, device=dev))
         self.tok = synth.make_tokens(len(self.positions), cfg.vocab).numpy()
 
+    def describe(self, wl_desc: str, batch: int) -> str:
+        if self.n == self.cfg.n_layers:
+            return (f"one whole batch-{batch} decode step ({wl_desc}): all {self.cfg.n_layers} layers "
+                    f"+ the LM head, per step")
+        return (f"{self.n} of {self.cfg.n_layers} layers + the LM head of one batch-{batch} decode step "
+                f"({wl_desc}), per step; time scaled to {self.cfg.n_layers} layers")
+
     def step(self):
-        """Returns (seconds scaled to the full layer count, seconds measured)."""
+        """Returns (seconds for the whole model, seconds measured)."""
         import numpy as np
 
         import oracle
@@ -242,6 +258,8 @@ class OracleSample:
         t0 = time.perf_counter()
         oracle.decode_step(self.sub, self.w, self.tok, self.positions, self.kv)
         t_all = time.perf_counter() - t0
+        if self.n == self.cfg.n_layers:
+            return t_all, t_all
         # the LM head alone, so that only the layer part is scaled
         x = np.random.default_rng(0).normal(size=(len(self.positions), self.cfg.hidden)).astype(np.float32)
         t1 = time.perf_counter()
@@ -257,8 +275,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg, batch, positions, metric, wl_desc, _ = workload(args.workload)
-    n_s = args.ref_layers
-    sample_run = OracleSample(cfg, n_s, positions)
+    sample_run = OracleSample(cfg, args.ref_layers, positions)
     for _ in range(args.warmup):
         sample_run.step()
     times, measured = [], 0.0
@@ -268,8 +285,6 @@ def run_reference(args):
         measured += tm
     ms = 1e3 * sum(times) / len(times)
     value = batch / (ms / 1e3)
-    sample = (f"{n_s} of {cfg.n_layers} layers + the LM head of one batch-{batch} decode step "
-              f"({wl_desc}), per step; time scaled to {cfg.n_layers} layers")
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -277,7 +292,7 @@ def run_reference(args):
         "config": {"workload": wl_desc,
                    "weights": "bf16", "kv_cache": "bf16"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample_run.describe(wl_desc, batch)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -319,17 +334,20 @@ def run_ours(args):
         if pg:
             pg.barrier()
 
-    def timed(fn, steps):
+    def timed(fn, steps, per_step=None):
+        """Total ms of `steps` calls (max over ranks), one CUDA event pair per
+        step on the launching stream; per-step ms into `per_step` if given."""
         barrier()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(steps):
+            evs[0].record(stream)
+            for i in range(steps):
                 fn()
-            ev1.record(stream)
+                evs[i + 1].record(stream)
         barrier()
-        return max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
+        if per_step is not None:
+            per_step.extend(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+        return max_over_ranks(evs[0].elapsed_time(evs[-1]), pg, dev)
 
     def mega():
         plan.decode_step(tokens, positions, kv, logits, stream=stream)
@@ -346,8 +364,9 @@ def run_ours(args):
     if rc != mk.MK_OK:
         raise RuntimeError(f"device status {rc}")
 
+    step_ms = []
     with ClockSampler(local) as clk:
-        ms_total = timed(mega, args.steps)
+        ms_total = timed(mega, args.steps, step_ms)
     rc = plan.status(stream)
     if rc != mk.MK_OK:
         raise RuntimeError(f"device status {rc}")
@@ -396,18 +415,25 @@ def run_ours(args):
     e2e_s = max_over_ranks(time.perf_counter() - t0, pg, dev)
     e2e = job_throughput(BATCH * args.steps, world, e2e_s)
 
-    # dependency-wait share from one traced step (not timed; the CUDA-core
-    # batch-1 path records the trace)
+    # dependency-wait share from traced steps (not timed; the CUDA-core
+    # batch-1 path records the trace): per step, the time consumers spent from
+    # taking an instruction until its inputs were ready, over CTAs x span
     dep_wait = None
     if BATCH == 1:
         plan.set_debug(trace=True)
-        mega()
-        torch.cuda.synchronize(dev)
-        rec = plan.trace().astype(np.int64)
+        fr = []
+        for _ in range(DEP_WAIT_STEPS):
+            mega()
+            torch.cuda.synchronize(dev)
+            rec = plan.trace().astype(np.int64)
+            span = rec[:, 3].max() - rec[:, 1].min()
+            n_ctas = plan.stats().n_ctas
+            if span > 0:
+                fr.append(float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span))
         plan.set_debug(trace=False)
-        span = rec[:, 3].max() - rec[:, 1].min()
-        n_ctas = plan.stats().n_ctas
-        dep_wait = float((rec[:, 2] - rec[:, 1]).sum()) / float(n_ctas * span) if span > 0 else None
+        if fr:
+            dep_wait = {"mean": float(np.mean(fr)), "min": float(np.min(fr)),
+                        "max": float(np.max(fr)), "steps": len(fr)}
 
     # greedy decode of MULTI_STEPS tokens per launch (mk_decode_steps, batch
     # 1): positions CONTEXT - MULTI_STEPS .. CONTEXT - 1 so the steps fit the
@@ -508,21 +534,32 @@ def run_ours(args):
             "frac_of_tensor_peak": tf_all / peaks_p["bf16_tflops_sustained"], "kernels_per_step": 1}
         del pall
 
+    # batched decode on the tensor-core path (the Llama-3-8B batch-8 and
+    # Qwen3-8B batch-32 ragged workloads), each with its own roofline
+    batched = None
+    decode_path = plan.stats().decode_path
+    if not args.no_batched and world == 1:
+        plan.close()
+        del w, kv
+        torch.cuda.empty_cache()
+        batched = {name: batched_leg(name, dev, stream, timed, args) for name in BATCHED_LEGS}
+
     if rank != 0:
         return 0
     peaks, kind = measured_peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
-    traffic = recorded_traffic("mk_interpreter", traffic_key) if plan.stats().decode_path == 0 else None
+    traffic = recorded_traffic("mk_interpreter", traffic_key) if decode_path == 0 else None
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "ms_per_step_stats": step_stats(step_ms),
         "config": {"workload": wl_desc,
                    "layers": cfg.n_layers, "hidden": cfg.hidden, "ffn": cfg.ffn,
                    "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
                    "head_dim": cfg.head_dim, "vocab": cfg.vocab, "batch": BATCH,
                    "context": CONTEXT if BATCH == 1 else pos_list,
-                   "path": "tensor-core persistent" if plan.stats().decode_path == 1
+                   "path": "tensor-core persistent" if decode_path == 1
                            else "cuda-core persistent",
                    "weights": "bf16", "kv_cache": "bf16",
                    "activations": "f32",
@@ -533,7 +570,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_kind": kind,
-                     "kernel": "mk_bdecode_kernel" if plan.stats().decode_path == 1 else "mk_interpreter",
+                     "kernel": "mk_bdecode_kernel" if decode_path == 1 else "mk_interpreter",
                      "algorithmic_bytes_per_launch": nbytes},
         "per_op": per_op,
         "dep_wait_fraction": dep_wait,
@@ -544,20 +581,102 @@ def run_ours(args):
         "prefill": prefill,
         "multi_step": multi,
         "mixed_chunk": mixed,
+        "batched": batched,
     }
     if world == 1 and not args.no_cpu_baseline:
-        sample_run = OracleSample(cfg, args.ref_layers, pos_list)
+        # the oracle as it stands on the host cores: the whole decode step of
+        # the same workload (same weights, copied to the host), median of 3
+        sample_run = OracleSample(cfg, args.ref_layers, pos_list,
+                                  weights=None if batched is not None else w)
         sample_run.step()
         t = sorted(sample_run.step()[0] for _ in range(3))[1]
         line["cpu_baseline"] = {
             "value": BATCH / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{args.ref_layers} of {cfg.n_layers} layers + the LM head of one batch-{BATCH} "
-                      f"decode step ({wl_desc}), scaled to {cfg.n_layers} layers"}
+            "sample": sample_run.describe(wl_desc, BATCH) + " (median of 3)"}
     print(json.dumps(line), flush=True)
-    plan.close()
+    if batched is None:
+        plan.close()
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+def step_stats(ms_list):
+    """Median, p10, p90 and mean of per-step times (ms)."""
+    import numpy as np
+    a = np.asarray(ms_list, dtype=np.float64)
+    if a.size == 0:
+        return None
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "mean": float(a.mean()), "n": int(a.size)}
+
+
+def batched_leg(name, dev, stream, timed, args):
+    """One batched-decode workload: the persistent step (per-step times and
+    roofline), the same tile routines kernel-per-operator in a CUDA graph, and
+    a prompt chunk mixed with decode columns."""
+    import torch
+
+    from tile_level_overlap_gb300 import mk, synth
+
+    cfg, batch, pos_list, metric, desc, _ = workload(name)
+    max_ctx = max(pos_list) + 1
+    w = synth.make_weights(cfg, device=dev)
+    kv = synth.make_kv_cache(cfg, batch, max_ctx, device=dev)
+    plan = mk.Plan(cfg, w, batch, max_ctx)
+    tokens = synth.make_tokens(batch, cfg.vocab).to(dev)
+    positions = torch.tensor(pos_list, dtype=torch.int32, device=dev)
+    logits = torch.empty((batch, cfg.vocab), dtype=torch.float32, device=dev)
+
+    def mega():
+        plan.decode_step(tokens, positions, kv, logits, stream=stream)
+
+    def graph():
+        plan.run_per_op(mk.MK_DECODE, tokens, positions, kv, logits, use_graph=True, stream=stream)
+
+    for _ in range(args.warmup):
+        mega()
+    per = []
+    ms = timed(mega, args.steps, per) / args.steps
+    for _ in range(max(1, args.warmup // 2)):
+        graph()
+    ms_graph = timed(graph, args.steps) / args.steps
+    # a prompt chunk of the last slot (half the columns, consecutive positions
+    # before its context) mixed with decode tokens of the other slots
+    half = batch // 2
+    cslot = batch - 1
+    cpos = pos_list[cslot] - half
+    slots_m = torch.tensor(list(range(batch - half)) + [cslot] * half, dtype=torch.int32, device=dev)
+    pos_m = torch.tensor(pos_list[:batch - half] + [cpos + i for i in range(half)], dtype=torch.int32,
+                         device=dev)
+
+    def mixed():
+        plan.decode_step_slots(tokens, pos_m, slots_m, kv, logits, stream=stream)
+
+    for _ in range(max(1, args.warmup // 2)):
+        mixed()
+    ms_mixed = timed(mixed, args.steps) / args.steps
+    rc = plan.status(stream)
+    if rc != mk.MK_OK:
+        raise RuntimeError(f"{name}: device status {rc}")
+    peaks, kind = measured_peaks()
+    nbytes = algorithmic_bytes(cfg, batch, pos_list)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    out = {"workload": desc, "metric": metric, "batch": batch,
+           "path": "tensor-core persistent" if plan.stats().decode_path == 1 else "cuda-core persistent",
+           "ms_per_step": ms, "ms_per_step_stats": step_stats(per),
+           "tokens_per_s": batch / (ms / 1e3),
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "peak_kind": kind,
+                        "kernel": "mk_bdecode_kernel" if plan.stats().decode_path == 1 else "mk_interpreter",
+                        "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+           "per_op_graph_ms_per_step": ms_graph, "speedup_persistent_vs_graph": ms_graph / ms,
+           "mixed_chunk": {"decode_columns": batch - half, "chunk_tokens": half, "ms_per_step": ms_mixed,
+                           "tokens_per_s": batch / (ms_mixed / 1e3)}}
+    plan.close()
+    del w, kv
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -566,10 +685,13 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--ref-layers", type=int, default=2)
+    ap.add_argument("--ref-layers", type=int, default=0,
+                    help="oracle layers per reference step (0: the whole model)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-per-op", action="store_true")
+    ap.add_argument("--no-batched", action="store_true",
+                    help="skip the batch-8 and batch-32 tensor-core decode legs")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3-8b")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,6 +1,8 @@
 // The persistent interpreter and its tile routines (sm_103a).
 //
-// One CTA per SM: a producer warp pops instructions from the global queue
+// One CTA per SM (12 warps: 8 consumer warps, a producer warp, a finisher warp
+// and two idle warps that complete the third warpgroup, whose registers go to
+// the consumers): a producer warp pops instructions from the global queue
 // (one atomic per instruction) and streams each instruction's dependency-free
 // operand bytes -- weight rows, or cached K/V rows -- into a shared-memory ring
 // with bulk async copies, running ahead of the consumers by up to NSTAGE
@@ -519,12 +521,19 @@ __device__ __forceinline__ void load_x8(const KParams& P, const Sh& S, const u64
 // in registers; each ring stage holds RPS = 8 / M whole rows, whose per-thread
 // partial dot products are summed across the warp (multi-value butterfly) into
 // a per-warp row slot; one fixed-order sum over warps per tile.
-template <int M>
+template <int M, bool MS>
 __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const Instr& in,
                                             float (&xr)[M][8], uint32_t step, uint32_t tag) {
   const int t = threadIdx.x;
   constexpr int K = M * FAST_K_UNIT;
   const u64* xs = gemv_x(P, in);
+  // a later step of a multi-step launch starts from the token the previous
+  // step chose: the layer-0 projection waits until all of that step's LM-head
+  // tiles counted (their packed maximum is then final)
+  if (MS && !xs && step > 0)
+    poll_until(P, S, [&]() {
+      return (int32_t)(ld_acquire_gpu(P.lm_done + (step - 1)) - P.n_lm_tiles) >= 0;
+    }, 0xfffffff5u);
   const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0, step) * P.H;
   const uint16_t* gain = gemv_gain(P, in);
   uint4 gw[M];
@@ -589,30 +598,41 @@ __device__ __forceinline__ void load_x_plain(const KParams& P, const Sh& S, cons
 }
 
 // The residual input of an O / down tile output element (thread t owns output
-// (r, b) = (t / B, t % B)); loaded before the tile streams so that its latency
-// is hidden.  Every (row, sequence) pair of a tile maps to one consumer thread
-// (RMAX * BMAX_CC <= NT).
-__device__ __forceinline__ float epilogue_prefetch(const KParams& P, const Sh& S, const Instr& in,
-                                                   const GemvDesc& g, int t, uint32_t tag,
-                                                   uint32_t step = 0) {
+// (r, b) = (t / B, t % B)): its word is read before the tile streams, so that
+// the read's latency hides behind the stages, and its tag is checked after
+// them (epilogue_resolve).  Every (row, sequence) pair of a tile maps to one
+// consumer thread (RMAX * BMAX_CC <= NT).
+// The tagged word of output (r, b)'s residual input, or null (no residual, or
+// the embedding row in layer 0).
+__device__ __forceinline__ const u64* residual_src(const KParams& P, const Instr& in, const GemvDesc& g,
+                                                   int t) {
   const int B = P.B, l = in.layer;
-  if (t >= g.rows * B) return 0.f;
+  if (t >= g.rows * B) return nullptr;
   const int r = t / B, b = t % B, row = g.row0 + r;
   const size_t bh = (size_t)P.max_batch * P.H;
-  const u64* src = nullptr;
-  if (in.op == OP_O) {
-    if (l == 0) return __uint_as_float((uint32_t)P.embed[(size_t)token_of(P, b, step) * P.H + row] << 16);
-    src = P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row;
-  } else if (in.op == OP_DOWN) {
-    src = P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row;
-  } else {
-    return 0.f;
+  if (in.op == OP_O && l > 0) return P.resid + (size_t)(2 * l) * bh + (size_t)b * P.H + row;
+  if (in.op == OP_DOWN) return P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row;
+  return nullptr;
+}
+__device__ __forceinline__ u64 epilogue_prefetch(const KParams& P, const Instr& in, const GemvDesc& g,
+                                                 int t, uint32_t step = 0) {
+  if (in.op == OP_O && in.layer == 0 && t < g.rows * P.B) {
+    const int r = t / P.B, b = t % P.B;
+    return (u64)((uint32_t)P.embed[(size_t)token_of(P, b, step) * P.H + g.row0 + r] << 16);
   }
-  u64 w = 0;
-  poll_until(P, S, [&]() {
-    w = ld_tagged(src);
-    return tag == 0u || tag_of(w) == tag;
-  }, 0xfffffff4u);
+  const u64* src = residual_src(P, in, g, t);
+  return src ? ld_tagged(src) : 0ull;
+}
+// The residual input's value, once its tag is the expected one (a bounded poll
+// when the early read found it stale).
+__device__ __forceinline__ float epilogue_resolve(const KParams& P, const Sh& S, const Instr& in,
+                                                  const GemvDesc& g, int t, u64 w, uint32_t tag) {
+  const u64* src = residual_src(P, in, g, t);
+  if (src && tag != 0u && tag_of(w) != tag)
+    poll_until(P, S, [&]() {
+      w = ld_tagged(src);
+      return tag_of(w) == tag;
+    }, 0xfffffff4u);
   return tag_val(w);
 }
 
@@ -664,7 +684,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   if (P.trace && t == 0) trace_mark(P, ii, 11);
   // the residual input of the tile's outputs (O, down), loaded now so that its
   // latency hides behind the stages; the finisher takes it from the hand-off
-  const float pre = epilogue_prefetch(P, S, in, g, t, tag, step);
+  const u64 pre_w = epilogue_prefetch(P, in, g, t, step);
   if (MS && t == 0) *hrec_step(S, hb) = step;  // the buffer is this tile's from here on
   float* redw = S.redw + hb * NW * RMAX;
   const int idx = warp_multi_index<RPS>(lane);
@@ -727,7 +747,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
     const float v = warp_reduce_multi<RPS>(prev, lane);
     if (writer && idx < prev_n) redw[w * RMAX + prev_row + idx] = v;
   }
-  if (t < RMAX) S.hpre[hb * RMAX + t] = pre;
+  if (t < RMAX) S.hpre[hb * RMAX + t] = epilogue_resolve(P, S, in, g, t, pre_w, tag);
   if (t == 0) {
     if (P.trace) trace_mark(P, ii, 8);
     *hrec_instr(S, hb) = in;
@@ -1290,35 +1310,17 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     const int f_abort = (islot_ctr & 1u) ? F_ABORT_B : F_ABORT;
     const uint64_t t_top = (P.trace && t == 0) ? globaltimer() : 0;
     // One thread takes the slot (a bounded wait) and hands it, with the stop
-    // verdict, to every consumer thread through one consumer barrier.  The
-    // tiles' dependencies are not waited on here: each tile polls the tags of
-    // the words it reads (poll_until).  Only the multi-step launch keeps one
-    // counter wait: a later step's layer-0 projection starts from the token
-    // the previous step chose, once all of that step's LM-head tiles counted.
+    // verdict, to every consumer thread through one consumer barrier (which
+    // also keeps the warps of a tile in step, so the ring's stages are freed
+    // together).  The tiles' dependencies are not waited on here: each tile
+    // polls the tags of the words it reads (poll_until).
     if (t == 0) {
       uint32_t v = 0xffffffffu;
       if (mbar_wait(P, &S.ifull[si], (islot_ctr / NISLOT) & 1u)) v = *slot_index(S, si);
       S.flags[f_slot] = v;
       const uint32_t iv = (!MS || v == END_SLOT) ? v : v & ((1u << SLOT_INDEX_BITS) - 1u);
-      const uint32_t step0 = (!MS || v == END_SLOT) ? 0u : v >> SLOT_INDEX_BITS;
-      uint32_t aborted = S.flags[F_STOP];
+      const uint32_t aborted = S.flags[F_STOP];
       const uint64_t t_begin = P.trace ? globaltimer() : 0;
-      if (MS && iv != END_SLOT && !aborted && step0 > 0) {
-        const Instr& in0 = *slot_instr(S, si);
-        if (in0.op == OP_QKV && in0.layer == 0) {
-          const uint64_t t0 = globaltimer();
-          while ((int32_t)(ld_acquire_gpu(P.lm_done + (step0 - 1)) - P.n_lm_tiles) < 0) {
-            if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) {
-              aborted = 1;
-            } else if (globaltimer() - t0 > P.wait_limit_ns) {
-              set_error(P, MK_ERR_TIMEOUT, iv);
-              aborted = 1;
-            }
-            if (aborted) break;
-            __nanosleep(32);
-          }
-        }
-      }
       S.flags[f_abort] = aborted;
       if (aborted) S.flags[F_STOP] = 1u;  // the producer stops popping
       if (P.trace && iv != END_SLOT) {
@@ -1360,7 +1362,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
       if (in.op != OP_DOWN) {
         auto& xh = *reinterpret_cast<float(*)[XH][8]>(&xr);
         if (xtag != tag_x) {
-          load_x_fast<XH>(P, S, in, xh, step, tag);
+          load_x_fast<XH, MS>(P, S, in, xh, step, tag);
           tag_x = xtag;
         }
         if (P.trace && t == 0) trace_mark(P, i, 2);
@@ -1387,10 +1389,10 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      const float pre = epilogue_prefetch(P, S, in, g, t, tag);
+      const u64 pre_w = epilogue_prefetch(P, in, g, t);
       gemv_generic(P, S, in, g, src, R, tag);
       if (P.trace && t == 0) trace_mark(P, i, 2);
-      gemv_epilogue(P, S.red, in, g, pre, t, pub_tag(in, tag));
+      gemv_epilogue(P, S.red, in, g, epilogue_resolve(P, S, in, g, t, pre_w, tag), t, pub_tag(in, tag));
     }
     if (P.trace && t == 0) {
       unsigned long long* tr = P.trace + (size_t)i * TRACE_WORDS;
@@ -1513,9 +1515,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
     for (int i = t; i < words; i += NTHREADS) dst[i] = src[i];
   }
   __syncthreads();
-  if (t >= NT + 32) finisher<MS>(P, S);
-  else if (t >= NT) producer<MS>(P, S);
-  else consumer<MH, MF, AD, AREP, MS>(P, S);
+  // Register split: the launch gives every thread the same count (168 at 12
+  // warps); the producer/finisher warpgroup (warps 8-11: producer, finisher,
+  // two idle warps) gives most of its share to the two consumer warpgroups.
+  // Shares: 8 consumer warps x 224 + 4 warps x 56 = 12 warps x 168 per thread.
+  if (t >= NT) {
+    setmaxnreg_dec<SPLIT_REGS_SIDE>();
+    if (t < NT + 32) producer<MS>(P, S);
+    else if (t < NT + 64) finisher<MS>(P, S);
+  } else {
+    setmaxnreg_inc<SPLIT_REGS_CONSUMER>();
+    consumer<MH, MF, AD, AREP, MS>(P, S);
+  }
   __syncthreads();
   if (t == 0 && P.mode == MODE_MEGA) {
     __threadfence();
@@ -1531,14 +1542,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
 }
 
 // ---------------------------------------------------------------- host-side launch helpers
+// The register split (setmaxnreg) adds up only if the launch gives each thread
+// exactly LAUNCH_REGS registers; with fewer, the consumer warps' increase
+// could never be granted, so such a build is refused instead of launched.
+template <class K>
+cudaError_t check_launch_regs(K kernel) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+  if (e != cudaSuccess) return e;
+  return a.numRegs == LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 template <int MH, int MF, int AD, int AREP>
 struct VariantImpl {
   static cudaError_t setup() {
     cudaError_t e = cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total);
+    if (e == cudaSuccess) e = check_launch_regs(mk_interpreter<MH, MF, AD, AREP, false>);
     if (e != cudaSuccess || MH == 0) return e;
-    return cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total);
+    e = cudaFuncSetAttribute(mk_interpreter<MH, MF, AD, AREP, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total);
+    if (e == cudaSuccess) e = check_launch_regs(mk_interpreter<MH, MF, AD, AREP, true>);
+    return e;
   }
   static cudaError_t occupancy(int* per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, mk_interpreter<MH, MF, AD, AREP, false>,

@@ -15,7 +15,16 @@ namespace mk {
 // Kernel geometry shared by the plan builder and the kernel.
 constexpr int NW = 8;                 // consumer warps per CTA
 constexpr int NT = NW * 32;           // consumer threads
-constexpr int NTHREADS = NT + 64;     // + one producer warp + one finisher warp
+constexpr int NTHREADS = NT + 128;    // + producer warp, finisher warp, two idle warps
+// Registers per thread after the kernel's setmaxnreg split (the launch gives
+// 168 to each of the 12 warps: 65536 / (3 warps per SM sub-partition x 32 x
+// 4), rounded down to 8).  The two consumer warpgroups take 224, the
+// producer/finisher warpgroup keeps 56: 8 x 224 + 4 x 56 = 12 x 168.
+constexpr int LAUNCH_REGS = 168;
+constexpr int SPLIT_REGS_CONSUMER = 224;
+constexpr int SPLIT_REGS_SIDE = 56;
+static_assert(8 * SPLIT_REGS_CONSUMER + 4 * SPLIT_REGS_SIDE == 12 * LAUNCH_REGS,
+              "register split must add up to the launch's registers");
 constexpr int NSTAGE = 6;             // weight/KV ring stages
 constexpr int STAGE_BYTES = 32768;    // bytes per ring stage
 constexpr int NISLOT = 8;             // instruction slots between producer and consumers
