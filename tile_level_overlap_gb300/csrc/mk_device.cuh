@@ -169,6 +169,30 @@ __device__ __forceinline__ float dot8(const uint4 w, const float* x, float a) {
   return a;
 }
 
+// Packed f32 pairs (sm_100 fma.rn.f32x2: two independent fp32 FMAs, each
+// rounded once, in one instruction).  A pair is a u64: element 0 in the low
+// word.
+__device__ __forceinline__ u64 pack_f32x2(float lo, float hi) {
+  return ((u64)__float_as_uint(hi) << 32) | (u64)__float_as_uint(lo);
+}
+__device__ __forceinline__ u64 fma_f32x2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// acc + (w's 8 bf16, as (even, odd) pairs) * x pairs: four packed FMAs, the
+// even columns accumulating in the low lane, the odd ones in the high lane.
+__device__ __forceinline__ u64 dot8_x2(const uint4 w, const u64 (&x)[4], u64 acc) {
+  acc = fma_f32x2(((u64)(w.x & 0xffff0000u) << 32) | (u64)(w.x << 16), x[0], acc);
+  acc = fma_f32x2(((u64)(w.y & 0xffff0000u) << 32) | (u64)(w.y << 16), x[1], acc);
+  acc = fma_f32x2(((u64)(w.z & 0xffff0000u) << 32) | (u64)(w.z << 16), x[2], acc);
+  acc = fma_f32x2(((u64)(w.w & 0xffff0000u) << 32) | (u64)(w.w << 16), x[3], acc);
+  return acc;
+}
+__device__ __forceinline__ float pair_sum(u64 p) {
+  return __uint_as_float((uint32_t)p) + __uint_as_float((uint32_t)(p >> 32));
+}
+
 // Warp-level tensor-core product c += A (16 x 16, rows g and g + 8 held as
 // a0..a3) x B (16 x 8, b0..b1), bf16 operands, f32 accumulators; the standard
 // m16n8k16 fragment layout (lane = 4 g + t).

@@ -416,11 +416,12 @@ __device__ __forceinline__ void trace_mark(const KParams& P, uint32_t ii, int wo
   P.trace[(size_t)ii * TRACE_WORDS + word] = globaltimer();
 }
 
-__device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
-  const int st = R.ctr % NSTAGE;
+// Wait for ring stage number `c` (a running count) and return it.
+__device__ __forceinline__ const uint8_t* ring_wait(const KParams& P, const Sh& S, Ring& R, uint32_t c) {
+  const int st = c % NSTAGE;
   if (P.trace && threadIdx.x == 0) {
     const uint64_t t0 = globaltimer();
-    mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
+    mbar_wait(P, &S.full[st], (c / NSTAGE) & 1u);
     const uint64_t t1 = globaltimer();
     R.wait_ns += (uint32_t)(t1 - t0);
     if (!R.first_done) {
@@ -428,9 +429,12 @@ __device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const S
       R.first_done = true;
     }
   } else {
-    mbar_wait(P, &S.full[st], (R.ctr / NSTAGE) & 1u);
+    mbar_wait(P, &S.full[st], (c / NSTAGE) & 1u);
   }
   return S.ring + (size_t)st * STAGE_BYTES;
+}
+__device__ __forceinline__ const uint8_t* ring_acquire(const KParams& P, const Sh& S, Ring& R) {
+  return ring_wait(P, S, R, R.ctr);
 }
 __device__ __forceinline__ void ring_release(const Sh& S, Ring& R) {
   __syncwarp();
@@ -675,7 +679,6 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
                                           const Src& src, Ring& R, const float (&xr)[M][8]) {
   constexpr int RPS = fast_rps(M);  // whole rows per 32 KB stage at K = M * 2048
   constexpr int kDup = 32 / RPS;    // lanes holding the same total after the reduction
-  constexpr int NP = M > 1 ? M : 2;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int K = g.K;
   const int rows0 = (int)src.rows[0];
@@ -687,6 +690,12 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   const u64 pre_w = epilogue_prefetch(P, in, g, t, step);
   if (MS && t == 0) *hrec_step(S, hb) = step;  // the buffer is this tile's from here on
   float* redw = S.redw + hb * NW * RMAX;
+  // the activations as packed (even, odd) column pairs for fma.rn.f32x2
+  u64 xp[M][4];
+#pragma unroll
+  for (int j = 0; j < M; ++j)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) xp[j][k] = pack_f32x2(xr[j][2 * k], xr[j][2 * k + 1]);
   const int idx = warp_multi_index<RPS>(lane);
   const bool writer = (lane & (kDup - 1)) == 0;
   float prev[RPS];
@@ -712,25 +721,15 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
     }
 #pragma unroll
     for (int i = 0; i < RPS; ++i) {
-      // independent partial sums (one per 8-column group, two halves when
-      // there is one group), added pairwise in a fixed order.  Rows past the
-      // region's end read stale stage bytes into sums that are never stored.
-      float pa[NP];
-      if constexpr (M == 1) {
-        const uint4 q = wv[i][0];
-        pa[0] = fmaf(bf_hi(q.y), xr[0][3], fmaf(bf_lo(q.y), xr[0][2],
-                fmaf(bf_hi(q.x), xr[0][1], bf_lo(q.x) * xr[0][0])));
-        pa[1] = fmaf(bf_hi(q.w), xr[0][7], fmaf(bf_lo(q.w), xr[0][6],
-                fmaf(bf_hi(q.z), xr[0][5], bf_lo(q.z) * xr[0][4])));
-      } else {
+      // Packed products: each bf16 pair of a weight word times the matching
+      // pair of activations in one fma.rn.f32x2 (even and odd columns in the
+      // two lanes of the accumulator pair), per 8-column group; the lanes and
+      // the groups are added in a fixed order.  Rows past the region's end
+      // read stale stage bytes into sums that are never stored.
+      u64 acc = dot8_x2(wv[i][0], xp[0], 0ull);
 #pragma unroll
-        for (int j = 0; j < M; ++j) pa[j] = dot8(wv[i][j], xr[j], 0.f);
-      }
-#pragma unroll
-      for (int step = 1; step < NP; step *= 2)
-#pragma unroll
-        for (int j = 0; j + step < NP; j += 2 * step) pa[j] += pa[j + step];
-      prev[i] = pa[0];
+      for (int j = 1; j < M; ++j) acc = dot8_x2(wv[i][j], xp[j], acc);
+      prev[i] = pair_sum(acc);
     }
     __syncwarp();
     mbar_arrive_if(&S.empty[st], lane == 0);
