@@ -1422,11 +1422,13 @@ __device__ __forceinline__ unsigned long long argmax_key(float y, uint32_t row) 
 }
 
 // One LM-head tile of a multi-step launch (finisher warp, batch 1): fold the
-// tile's logits into the step's maximum, count the tile; the last tile of the
-// step stores the chosen token.
-__device__ void lm_tile_choose(const KParams& P, const GemvDesc& g, uint32_t step, int lane) {
+// tile's logits (lane r holds row r's in `y`) into the step's maximum, count
+// the tile; the last tile of the step stores the chosen token.  Runs before
+// the tile's logits are stored (only the launch's last step stores them), so
+// the counting atomic's release has no logits stores to wait for.
+__device__ void lm_tile_choose(const KParams& P, const GemvDesc& g, uint32_t step, int lane, float y) {
   unsigned long long key = 0;
-  if (lane < g.rows) key = argmax_key(P.logits[g.row0 + lane], (uint32_t)(g.row0 + lane));
+  if (lane < g.rows) key = argmax_key(y, (uint32_t)(g.row0 + lane));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
@@ -1471,9 +1473,15 @@ __device__ void finisher(const KParams& P, const Sh& S) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.hempty[hb]);
     if (P.trace && lane == 0) P.trace[(size_t)ii * TRACE_WORDS + 14] = globaltimer();
-    gemv_epilogue(P, S.fin, in, g, pre, lane, pub_tag(in, step_tag(P, gen, step)));
+    if (MS && in.op == OP_LM) {
+      // greedy choice from the registers; the logits of steps before the
+      // launch's last are not returned, so they are not stored
+      lm_tile_choose(P, g, step, lane, S.fin[lane * BMAX_CC]);
+      if (step + 1u == P.n_steps) gemv_epilogue(P, S.fin, in, g, pre, lane, 0u);
+    } else {
+      gemv_epilogue(P, S.fin, in, g, pre, lane, pub_tag(in, step_tag(P, gen, step)));
+    }
     __syncwarp();
-    if (MS && in.op == OP_LM) lm_tile_choose(P, g, step, lane);
     if (lane == 0) {
       if (P.trace) {
         unsigned long long* tr = P.trace + (size_t)ii * TRACE_WORDS;
