@@ -39,6 +39,7 @@ PREFILL_TOKENS = 2048
 MULTI_STEPS = 8  # tokens per launch of the multi-step greedy decode leg
 DEP_WAIT_STEPS = 5  # traced steps the dependency-wait share is averaged over
 BATCHED_LEGS = ("llama3-8b-b8", "qwen3-8b-b32")
+BATCH_PREFILL_PROMPTS, BATCH_PREFILL_TOKENS = 4, 512  # the several-prompt prefill leg
 # name -> (shape in synth, batch, largest cached context, smallest (ragged
 # contexts U[lo, ctx], seeded) or None (all at ctx), metric, description,
 # traffic key)
@@ -659,6 +660,37 @@ def batched_leg(name, dev, stream, timed, args):
     rc = plan.status(stream)
     if rc != mk.MK_OK:
         raise RuntimeError(f"{name}: device status {rc}")
+    # several prompts prefilled in one launch (each weight tile streamed once
+    # for all of them) against one launch per prompt
+    batch_prefill = None
+    if batch >= BATCH_PREFILL_PROMPTS:
+        n_p = BATCH_PREFILL_PROMPTS
+        ptoks = synth.make_tokens(n_p * BATCH_PREFILL_TOKENS, cfg.vocab, seed=synth.SEED_TOKENS + 11)
+        ptoks = ptoks.view(n_p, BATCH_PREFILL_TOKENS).to(dev)
+        lens = [BATCH_PREFILL_TOKENS] * n_p
+        plog = torch.empty((n_p, cfg.vocab), dtype=torch.float32, device=dev)
+
+        def one_launch():
+            plan.prefill_batch(ptoks, lens, kv, plog, stream=stream)
+
+        def per_prompt():
+            for b in range(n_p):
+                plan.prefill_batch(ptoks[b:b + 1], lens[:1], kv, plog[b:b + 1], stream=stream)
+
+        one_launch()
+        per_prompt()
+        pf_steps = max(3, args.steps // 10)
+        ms_one = timed(one_launch, pf_steps) / pf_steps
+        ms_each = timed(per_prompt, pf_steps) / pf_steps
+        rc = plan.status(stream)
+        if rc != mk.MK_OK:
+            raise RuntimeError(f"{name}: batch prefill device status {rc}")
+        ntok = n_p * BATCH_PREFILL_TOKENS
+        batch_prefill = {"prompts": n_p, "tokens_each": BATCH_PREFILL_TOKENS,
+                         "ms_one_launch": ms_one, "ms_one_launch_per_prompt": ms_each,
+                         "tokens_per_s_one_launch": ntok / (ms_one / 1e3),
+                         "tokens_per_s_per_prompt": ntok / (ms_each / 1e3),
+                         "speedup": ms_each / ms_one}
     peaks, kind = measured_peaks()
     nbytes = algorithmic_bytes(cfg, batch, pos_list)
     achieved = nbytes / (ms / 1e3) / 1e9
@@ -672,7 +704,8 @@ def batched_leg(name, dev, stream, timed, args):
                         "algorithmic_bytes_per_launch": nbytes, "traffic": None},
            "per_op_graph_ms_per_step": ms_graph, "speedup_persistent_vs_graph": ms_graph / ms,
            "mixed_chunk": {"decode_columns": batch - half, "chunk_tokens": half, "ms_per_step": ms_mixed,
-                           "tokens_per_s": batch / (ms_mixed / 1e3)}}
+                           "tokens_per_s": batch / (ms_mixed / 1e3)},
+           "batch_prefill": batch_prefill}
     plan.close()
     del w, kv
     torch.cuda.empty_cache()

@@ -208,9 +208,16 @@ int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t 
 /* Prefill of `batch` prompts ("MegaOps", Abstract: prefill of the dense
  * Llama3/Qwen3 decoders, here for several prompts):
  * prompt b (tokens[b * stride .. b * stride + lens[b])) goes to sequence slot
- * b of the cache and its last token's logits to logits[b].  Each prompt runs
- * as mk_prefill does (one persistent launch of the prompt's tiles, then its
- * LM-head tiles), the prompts back to back on `stream`.
+ * b of the cache and its last token's logits to logits[b].  The prompts'
+ * 128-token blocks go end to end into ONE persistent launch of the prefill
+ * queue ("Lecture 112" summary, Key takeaways: one queue whose extents are
+ * symbolic), so every weight tile is streamed once for all of them: a table
+ * gives each block its cache slot, its prompt's first block, length and
+ * token offset (RoPE positions, cache rows and causal attention stay within
+ * the prompt).  When the blocks exceed the plan's context (sum over b of
+ * ceil(lens[b] / 128) > ceil(max_ctx / 128)), consecutive prompts are packed
+ * into as few such launches as fit.  Then each prompt's last token runs its
+ * LM-head tiles.  Results are bit-identical to prompt-by-prompt calls.
  *   tokens  device int32 [batch][stride]
  *   lens    HOST int32 [batch], 1 <= lens[b] <= min(stride, max_ctx)
  *   batch   1 .. max_batch of the plan

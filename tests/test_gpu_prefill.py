@@ -208,17 +208,20 @@ def test_llama3_8b_width_prefill_all_token_logits_sampled():
         m.close()
 
 
-def test_prefill_batch_slots():
+@pytest.mark.parametrize("max_ctx", [320, 700])
+def test_prefill_batch_slots(max_ctx):
     """mk_prefill_batch: three prompts of different lengths into cache slots
     0..2: each slot's keys/values and last-token logits against the oracle,
     then one batched decode step over the three slots against the oracle's
-    prefill of each prompt plus the decoded token."""
+    prefill of each prompt plus the decoded token.  With a 700-token context
+    all five 128-token blocks share one launch; with 320 (three blocks per
+    launch) the first two prompts share one and the third has its own."""
     cfg = PF_SMALL
-    m = PfModel(cfg, max_ctx=320, seed=8)
+    m = PfModel(cfg, max_ctx=max_ctx, seed=8)
     try:
-        m.kv = torch.zeros(synth.kv_cache_shape(cfg, 3, 320), dtype=torch.bfloat16, device=m.dev)
+        m.kv = torch.zeros(synth.kv_cache_shape(cfg, 3, max_ctx), dtype=torch.bfloat16, device=m.dev)
         m.plan.close()
-        m.plan = mk.Plan(cfg, m.w, 3, 320)
+        m.plan = mk.Plan(cfg, m.w, 3, max_ctx)
         lens = [200, 7, 129]
         stride = 256
         toks = np.zeros((3, stride), dtype=np.int32)
@@ -249,3 +252,39 @@ def test_prefill_batch_slots():
             m.plan.prefill_batch(t, [200, 0, 5], m.kv, lg)
     finally:
         m.close()
+
+
+def test_prefill_batch_bit_identical_to_single_prompts():
+    """One launch over three prompts (their blocks end to end in the
+    activation planes) computes every row as the prompt's own launch does:
+    logits and cache entries bit-identical to three one-prompt calls (head_dim
+    128 with q/k norm)."""
+    cfg = PF_D128_QK
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(cfg, seed=9, device=dev)
+    plan = mk.Plan(cfg, w, 3, 700)
+    try:
+        lens = [300, 5, 256]
+        stride = 320
+        toks = np.zeros((3, stride), dtype=np.int32)
+        seqs = [synth.make_tokens(n, cfg.vocab, seed=70 + b).numpy() for b, n in enumerate(lens)]
+        for b, sq in enumerate(seqs):
+            toks[b, :len(sq)] = sq
+        kv = torch.zeros(synth.kv_cache_shape(cfg, 3, 700), dtype=torch.bfloat16, device=dev)
+        lg = torch.full((3, cfg.vocab), float("nan"), device=dev)
+        plan.prefill_batch(torch.from_numpy(toks).to(dev), lens, kv, lg)
+        assert plan.status() == mk.MK_OK
+        got = lg.cpu().numpy()
+        for b, sq in enumerate(seqs):
+            kv1 = torch.zeros_like(kv)
+            lg1 = torch.full((1, cfg.vocab), float("nan"), device=dev)
+            one = np.zeros((1, stride), dtype=np.int32)
+            one[0, :len(sq)] = sq
+            plan.prefill_batch(torch.from_numpy(one).to(dev), [lens[b]], kv1, lg1)
+            assert plan.status() == mk.MK_OK
+            np.testing.assert_array_equal(got[b], lg1.cpu().numpy()[0])
+            assert torch.equal(kv[:, :, b, :, :lens[b]], kv1[:, :, 0, :, :lens[b]])
+    finally:
+        plan.close()
+        del w
+        torch.cuda.empty_cache()

@@ -33,6 +33,7 @@ struct PrefillState {
   CUtensorMap* d_tm = nullptr;          // device copy of the tensor-map table
   std::vector<CUtensorMap> h_tm;        // host copy (source of the uploads)
   const void* kv_mapped = nullptr;      // KV cache the table's cache map points at
+  int4* d_blk = nullptr;                // block table of a several-prompt launch [n_blocks]
 };
 
 // Tensor-core batched decode state of a plan (shapes whose batch the CUDA-core
@@ -682,6 +683,7 @@ static int prefill_init(mk_plan* p) {
   const size_t o_qb = bm.take(4 * rows * qd);
   const size_t o_ao = bm.take(4 * rows * qd);
   const size_t o_act = bm.take(4 * rows * F);
+  const size_t o_blk = bm.take(sizeof(int4) * pp.n_blocks);
   if (cudaMalloc(&s.mem, bm.off) != cudaSuccess) {
     cudaGetLastError();
     s.mem = nullptr;
@@ -691,6 +693,7 @@ static int prefill_init(mk_plan* p) {
   uint8_t* b = (uint8_t*)s.mem;
   MK_CUDA(cudaMemset(s.mem, 0, s.bytes));
   s.d_tm = (CUtensorMap*)(b + o_tm);
+  s.d_blk = (int4*)(b + o_blk);
   s.h_tm.assign(n_maps, CUtensorMap{});
   bool ok = true;
   for (int l = 0; l < L && ok; ++l) {
@@ -769,10 +772,10 @@ static int prefill_args(mk_plan* p, const int32_t* tokens, int len, void* kv, fl
 // The LM head of the prompt's last token runs as its own per-operator launch
 // of the decode tiles after the prefill body ("Lecture 112", Practical
 // implications: a megakernel body mixed with a separate LM-head op).
-static int prefill_lm(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits,
+static int prefill_lm(mk_plan* p, const int32_t* tokens, int last_row, void* kv, float* logits,
                       cudaStream_t st) {
   const mk_model_cfg& c = p->hp.cfg;
-  const float* last = p->pf.base.xb + (size_t)(len - 1) * c.hidden;
+  const float* last = p->pf.base.xb + (size_t)last_row * c.hidden;
   u64* dst = p->base.resid + (size_t)(2 * c.n_layers) * p->hp.max_batch * c.hidden;
   // the floats into the low halves of the tagged words (the kernel-per-operator
   // LM tiles read them without a tag check; their tags stay stale for any
@@ -798,7 +801,7 @@ int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logi
   k.mode = MODE_MEGA;
   k.wait_limit_ns = p->wait_limit_ns;
   MK_CUDA(pf_launch_mega(k, p->n_sms, st));
-  return prefill_lm(p, tokens, len, kv, logits, st);
+  return prefill_lm(p, tokens, len - 1, kv, logits, st);
 }
 
 int mk_prefill_batch(mk_plan* p, const int32_t* tokens, const int32_t* lens, int batch, int stride,
@@ -813,18 +816,40 @@ int mk_prefill_batch(mk_plan* p, const int32_t* tokens, const int32_t* lens, int
   int rc;
   if ((rc = prefill_init(p)) != MK_OK || (rc = prefill_bind_kv(p, kv, st)) != MK_OK) return rc;
   const int V = p->hp.cfg.vocab;
-  for (int b = 0; b < batch; ++b) {
-    // one persistent launch per prompt, into its own cache slot, then its
-    // last token's LM head
+  const int cap = p->pf.pp.n_blocks;  // token blocks one launch holds
+  // The prompts' 128-token blocks go end to end into the launch's activation
+  // planes (as many prompts per launch as fit: all of them when their blocks
+  // fit the plan's context), so every weight tile streams once per launch for
+  // all of its prompts; then each prompt's last token gets its LM head.
+  for (int b0 = 0; b0 < batch;) {
+    std::vector<int4> tab;
+    int b1 = b0;
+    while (b1 < batch) {
+      const int nb = (lens[b1] + PF_BM - 1) / PF_BM;
+      if (!tab.empty() && (int)tab.size() + nb > cap) break;
+      const int first = (int)tab.size();
+      for (int m = 0; m < nb; ++m) tab.push_back(make_int4(b1, first, lens[b1], b1 * stride));
+      ++b1;
+    }
+    // (a pageable source: the copy has read it when the call returns)
+    MK_CUDA(cudaMemcpyAsync(p->pf.d_blk, tab.data(), sizeof(int4) * tab.size(), cudaMemcpyHostToDevice,
+                            st));
     PfParams k = p->pf.base;
-    k.tokens = tokens + (size_t)b * stride;
-    k.S = lens[b];
-    k.slot = b;
+    k.tokens = tokens;
+    k.S = (int)tab.size() * PF_BM;
+    k.blk = p->pf.d_blk;
     k.kv = (uint16_t*)kv;
     k.mode = MODE_MEGA;
     k.wait_limit_ns = p->wait_limit_ns;
     MK_CUDA(pf_launch_mega(k, p->n_sms, st));
-    if ((rc = prefill_lm(p, k.tokens, lens[b], kv, logits + (size_t)b * V, st)) != MK_OK) return rc;
+    int blk0 = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int row = blk0 * PF_BM + lens[b] - 1;
+      if ((rc = prefill_lm(p, tokens + (size_t)b * stride, row, kv, logits + (size_t)b * V, st)) != MK_OK)
+        return rc;
+      blk0 += (lens[b] + PF_BM - 1) / PF_BM;
+    }
+    b0 = b1;
   }
   return MK_OK;
 }
@@ -866,7 +891,7 @@ static int launch_per_op_prefill(mk_plan* p, const PfParams& k, void* kv, float*
     const auto& r = p->pf.pp.perop[j];
     MK_CUDA(pf_launch_perop(k, r.first, r.second, st));
   }
-  return prefill_lm(p, k.tokens, k.S, kv, logits, st);
+  return prefill_lm(p, k.tokens, k.S - 1, kv, logits, st);
 }
 
 int mk_run_per_op(mk_plan* p, int mode, int use_graph, const int32_t* tokens,

@@ -88,6 +88,12 @@ struct PfParams {
   int plane_rows;           // rows of one plane (token blocks x 128)
   uint16_t* kv;             // caller's KV cache
   int slot;                 // the sequence slot this prompt's keys and values go to
+  // Several prompts in one launch (mk_prefill_batch): their 128-token blocks
+  // lie end to end in the activation planes, and block j of the launch is
+  // described by blk[j] = {cache slot, the prompt's first block, the prompt's
+  // length, the prompt's offset in `tokens`}; S = the blocks x 128.  Null for
+  // one prompt (slot `slot`, block j = the prompt's block j, length S).
+  const int4* blk;
   const float2* rope;       // (cos, sin) [max_ctx][d / 2]
   uint32_t* bars;
   uint32_t* ctl;

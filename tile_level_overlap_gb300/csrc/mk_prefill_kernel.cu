@@ -216,8 +216,41 @@ __device__ __forceinline__ PfGemm pf_gemm(const PfParams& P, const Instr& in) {
   return g;
 }
 
-__device__ __forceinline__ int kv_row(const PfParams& P, int l, int kv, int g) {
-  return (((l * 2 + kv) * P.max_batch + P.slot) * P.nkv + g) * P.max_ctx;
+__device__ __forceinline__ int kv_row(const PfParams& P, int l, int kv, int g, int slot) {
+  return (((l * 2 + kv) * P.max_batch + slot) * P.nkv + g) * P.max_ctx;
+}
+
+// Where plane row p of the launch belongs: its prompt's cache slot, its
+// position in the prompt, the prompt's length, its index in `tokens`, and
+// whether it holds a token (rows past a prompt's end pad its last block).
+struct PfRow {
+  int slot, pos, len, tok;
+  bool live;
+};
+__device__ __forceinline__ PfRow pf_row(const PfParams& P, int p) {
+  PfRow r;
+  if (!P.blk) {
+    r.slot = P.slot;
+    r.pos = p;
+    r.len = P.S;
+    r.tok = p;
+  } else {
+    const int4 b = P.blk[p / PF_BM];
+    r.slot = b.x;
+    r.pos = p - b.y * PF_BM;
+    r.len = b.z;
+    r.tok = b.w + r.pos;
+  }
+  r.live = r.pos < r.len;
+  return r;
+}
+// First block of the prompt that block m belongs to (its causal key blocks
+// are first .. m).
+__device__ __forceinline__ int pf_first_block(const PfParams& P, int m) {
+  return P.blk ? P.blk[m].y : 0;
+}
+__device__ __forceinline__ int pf_block_slot(const PfParams& P, int m) {
+  return P.blk ? P.blk[m].x : P.slot;
 }
 
 // ---------------------------------------------------------------- producer
@@ -299,10 +332,11 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
       // one stage per key block: K_j at +0, V_j at +tile (Q goes to TMEM
       // through the compute warps)
       const int m = (int)in.a0, gq = (int)in.a1, l = in.layer;
+      const int first = pf_first_block(P, m), slot = pf_block_slot(P, m);
       const uint32_t tile = PF_BM * P.d * 2;  // one 128-row tile of d columns
       const int nbox = P.d / 64;
       for (int h = 0; h < P.rep; ++h)
-        for (int j = 0; j <= m; ++j) {
+        for (int j = first; j <= m; ++j) {
           const int st = stage_ctr % PF_NSTAGE;
           pf_wait(P, &S.empty[st], ((stage_ctr / PF_NSTAGE) & 1u) ^ 1u);
           uint8_t* sp = S.ring + st * PF_STAGE;
@@ -310,7 +344,7 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
           for (int kvsel = 0; kvsel < 2; ++kvsel)
             for (int bx = 0; bx < nbox; ++bx)
               tma_load_2d(sp + kvsel * tile + bx * 16384, tmap(P, am(P, AM_KV)), bx * 64,
-                          kv_row(P, l, kvsel, gq) + j * PF_BM, &S.full[st], pol_a);
+                          kv_row(P, l, kvsel, gq, slot) + (j - first) * PF_BM, &S.full[st], pol_a);
           ++stage_ctr;
         }
     }
@@ -370,7 +404,7 @@ __device__ void pf_mma(const PfParams& P, const PfSh& S, uint32_t tbase) {
         ++use[b];
       }
       tc_fence_after();
-      const int m = (int)in.a0;
+      const int m = (int)in.a0, first = pf_first_block(P, m);
       const uint32_t s_t = tbase, o_t = tbase + 128, p_t = tbase + 256, pl_t = tbase + 320;
       const uint32_t q_t = tbase + 384, ql_t = tbase + 448;
       const uint32_t id_s = idesc_bf16_f32(PF_BM, PF_BM);
@@ -380,7 +414,7 @@ __device__ void pf_mma(const PfParams& P, const PfSh& S, uint32_t tbase) {
         pf_wait(P, S.qfull, qctr & 1u);
         ++qctr;
         tc_fence_after();
-        for (int j = 0; j <= m; ++j) {
+        for (int j = first; j <= m; ++j) {
           // S = Q K_j^T (K = head_dim, in 64-column atoms 16 KB apart)
           const int st = stage_ctr % PF_NSTAGE;
           pf_wait(P, &S.full[st], (stage_ctr / PF_NSTAGE) & 1u);
@@ -454,14 +488,15 @@ __device__ __forceinline__ float bf(const uint16_t* p, int i) {
 // QKV epilogue of one head: columns [c0, c0 + d) of the tile accumulator.
 // The TMEM loads run on every thread of the warp; only live rows store.
 __device__ void pf_qkv_head(const PfParams& P, uint32_t tacc, int c0, int col, int p, int l,
-                            bool live) {
+                            const PfRow& pr) {
+  const bool live = pr.live;
   const int d = P.d, qd = P.nq * d, kd = P.nkv * d;
   const LayerW& W = P.layers[l];
   const bool is_v = col >= qd + kd;
   const int half = d / 2;
   if (is_v) {
     const int g = (col - qd - kd) / d;
-    uint16_t* dst = P.kv + ((size_t)kv_row(P, l, 1, g) + p) * d;
+    uint16_t* dst = P.kv + ((size_t)kv_row(P, l, 1, g, pr.slot) + pr.pos) * d;
     for (int c = 0; c < d; c += 16) {
       float v[16];
       tmem_ld16(tacc + (uint32_t)(c0 + c), v);
@@ -485,9 +520,9 @@ __device__ void pf_qkv_head(const PfParams& P, uint32_t tacc, int c0, int col, i
   }
   // queries: hi/lo planes (tensor-core operand); keys: the bf16 cache entry
   uint16_t* dst = is_q ? P.qb + (size_t)p * qd + col
-                       : P.kv + ((size_t)kv_row(P, l, 0, (col - qd) / d) + p) * d;
+                       : P.kv + ((size_t)kv_row(P, l, 0, (col - qd) / d, pr.slot) + pr.pos) * d;
   uint16_t* dst_lo = is_q ? dst + (size_t)P.plane_rows * qd : nullptr;
-  const float2* rt = P.rope + (size_t)p * half;
+  const float2* rt = P.rope + (size_t)(pr.live ? pr.pos : 0) * half;
   for (int c = 0; c < half; c += 16) {
     float u1[16], u2[16];
     tmem_ld16(tacc + (uint32_t)(c0 + c), u1);
@@ -522,12 +557,13 @@ __device__ void pf_qkv_head(const PfParams& P, uint32_t tacc, int c0, int col, i
 // rows past the prompt are computed on a clamped row and not stored.
 __device__ void pf_gemm_epilogue(const PfParams& P, const Instr& in, uint32_t tacc, int p_row) {
   const int l = in.layer, n = (int)in.a1;
-  const bool live = p_row < P.S;
+  const PfRow pr = pf_row(P, p_row);
+  const bool live = pr.live;
   const int p = live ? p_row : 0;  // dead rows read row 0's inputs and store nothing
   switch (in.op) {
     case PF_QKV: {
       const int base = n * P.bn_qkv;
-      for (int c0 = 0; c0 < P.bn_qkv; c0 += P.d) pf_qkv_head(P, tacc, c0, base + c0, p, l, live);
+      for (int c0 = 0; c0 < P.bn_qkv; c0 += P.d) pf_qkv_head(P, tacc, c0, base + c0, p, l, pr);
       break;
     }
     case PF_O:
@@ -537,7 +573,7 @@ __device__ void pf_gemm_epilogue(const PfParams& P, const Instr& in, uint32_t ta
       const float* res = in.op == PF_O ? P.xb : P.xa;
       const uint16_t* emb = nullptr;
       if (in.op == PF_O && l == 0) {
-        int tok = P.tokens[p];
+        int tok = P.tokens[live ? pr.tok : 0];
         if (tok < 0 || tok >= P.V) tok = 0;
         emb = P.embed + (size_t)tok * P.H + col0;
       }
@@ -608,10 +644,11 @@ __device__ void pf_norm(const PfParams& P, const Instr& in, int wc, int lane) {
   uint16_t* dst = (first || fin) ? P.hn1 : P.hn2;
   for (int r = wc; r < PF_BM; r += 4) {
     const int p = m * PF_BM + r;
-    if (p >= P.S) break;
+    const PfRow pr = pf_row(P, p);
+    if (!pr.live) break;
     const uint16_t* emb = nullptr;
     if (first && l == 0) {
-      int tok = P.tokens[p];
+      int tok = P.tokens[pr.tok];
       if (tok < 0 || tok >= P.V) {
         if (lane == 0) pf_error(P, MK_ERR_BOUNDS, (uint32_t)p);
         tok = 0;
@@ -660,6 +697,11 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
                         uint32_t lane_base, uint32_t& sctr) {
   const int m = (int)in.a0, gq = (int)in.a1, lane = threadIdx.x & 31;
   const int qi = m * PF_BM + row;  // < plane_rows: rows past the prompt are never stored
+  // positions within the prompt: this row's, and the keys' from the prompt's
+  // first block
+  const PfRow pr = pf_row(P, qi);
+  const int first = pf_first_block(P, m);
+  const int qpos = pr.pos, klen = pr.len;
   const int qd = P.nq * D;
   const float c = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
   const uint32_t s_t = tbase + lane_base, o_t = tbase + 128 + lane_base;
@@ -690,7 +732,7 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
 #pragma unroll
     for (int e = 0; e < D; ++e) o[e] = 0.f;
     float mrun = -INFINITY, lrun = 0.f, alpha_prev = 0.f;
-    for (int j = 0; j <= m; ++j) {
+    for (int j = first; j <= m; ++j) {
       pf_wait(P, S.sfull, sctr & 1u);
       tc_fence_after();
       const bool diag = j == m;
@@ -701,14 +743,14 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
         tmem_ld16(s_t + (uint32_t)c0, s);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int kj = j * PF_BM + c0 + e;
-          const bool masked = diag && (kj > qi || kj >= P.S);
+          const int kj = (j - first) * PF_BM + c0 + e;
+          const bool masked = diag && (kj > qpos || kj >= klen);
           if (!masked) mx = fmaxf(mx, s[e] * c);
         }
       }
       const float mnew = fmaxf(mrun, mx);
       const float alpha = mrun == -INFINITY ? 0.f : exp2f(mrun - mnew);
-      if (j > 0) {
+      if (j > first) {
         // O_{j-1} = P_{j-1} V_{j-1} was issued before S_j, so it is complete
         // (and P's columns are free); fold it in at the scale of block j-1
         pf_wait(P, S.ofull, (sctr - 1) & 1u);
@@ -729,9 +771,9 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
         uint32_t hi[8], lo[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          const int kj = j * PF_BM + c0 + e;
-          const bool m0 = diag && (kj > qi || kj >= P.S);
-          const bool m1 = diag && (kj + 1 > qi || kj + 1 >= P.S);
+          const int kj = (j - first) * PF_BM + c0 + e;
+          const bool m0 = diag && (kj > qpos || kj >= klen);
+          const bool m1 = diag && (kj + 1 > qpos || kj + 1 >= klen);
           const float p0 = m0 ? 0.f : exp2f(s[e] * c - mnew);
           const float p1 = m1 ? 0.f : exp2f(s[e + 1] * c - mnew);
           sum += p0 + p1;
@@ -759,7 +801,7 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
 #pragma unroll
       for (int e = 0; e < 16; ++e) o[c0 + e] = (o[c0 + e] * alpha_prev + v[e]) * linv;
     }
-    if (qi < P.S) {
+    if (pr.live) {
       uint16_t* dst = P.ao + (size_t)qi * qd + (size_t)(gq * P.rep + h) * D;
       uint16_t* dst_lo = dst + (size_t)P.plane_rows * qd;
 #pragma unroll
