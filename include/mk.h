@@ -227,6 +227,25 @@ int mk_plan_check(const mk_model_cfg *cfg, int max_batch, int max_ctx, uint64_t 
 int mk_prefill_batch(mk_plan *plan, const int32_t *tokens, const int32_t *lens, int batch,
                      int stride, void *kv_cache, float *logits, void *stream);
 
+/* Chunked prefill mixed with decode in the tensor-core prefill kernel
+ * ("Lecture 112" summary, Key takeaways: one queue with symbolic extents
+ * serves both; "MegaOps", Abstract: decode and prefill of the same decoder).
+ * Chunk i is chunks[4 i .. 4 i + 3] = {slot, pos0, len, tok}: `len` tokens
+ * (tokens[tok .. tok + len), device int32) of the sequence in cache slot
+ * `slot`, at cache positions pos0 .. pos0 + len - 1, the positions below pos0
+ * already cached.  A decode token is a chunk of length 1; a prompt's
+ * continuation a longer one.  The chunks' 128-token blocks share one
+ * persistent launch (as for mk_prefill_batch): every row attends to its
+ * sequence's keys 0 .. its own position (the cached ones and its chunk's
+ * earlier ones) and writes its key and value to the cache.  logits[i]
+ * (device float [n][V]) receives the logits after chunk i's last token.
+ *   chunks  HOST int32 [n][4]; 0 <= slot < max_batch, len >= 1,
+ *           pos0 + len <= max_ctx; a later chunk of a slot must start where
+ *           the slot's previous chunk ends (else MK_ERR_INVALID_ARG)
+ * Errors as mk_prefill. */
+int mk_prefill_chunks(mk_plan *plan, const int32_t *tokens, const int32_t *chunks, int n,
+                      void *kv_cache, float *logits, void *stream);
+
 /* Prefill with the logits of EVERY prompt token ("MegaOps", Abstract:
  * prefill of the dense Llama3/Qwen3 decoders).  Same as mk_prefill, except that the final RMSNorm and the LM
  * head run for all len tokens inside the same persistent launch, as

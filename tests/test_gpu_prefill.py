@@ -288,3 +288,54 @@ def test_prefill_batch_bit_identical_to_single_prompts():
         plan.close()
         del w
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("max_ctx", [320, 512])
+def test_prefill_chunks_mixed_with_decode(max_ctx):
+    """mk_prefill_chunks: the tensor-core prefill kernel running a prompt
+    continuation and decode tokens together -- 130 tokens of slot 0 at cache
+    positions 150..279 (not aligned to 128 positions, crossing a key-block
+    boundary) and one decode token each for slots 1 and 2 -- after the three
+    prompts were prefilled.  Each chunk's last logits against the oracle's
+    prefill of the whole sequence; the cache entries the chunks wrote against
+    the oracle's keys and values.  With a 512-token context all four 128-token
+    blocks share one launch; with 320 the packing needs two."""
+    cfg = PF_SMALL
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(cfg, seed=12, device=dev)
+    plan = mk.Plan(cfg, w, 3, max_ctx)
+    try:
+        kv = torch.zeros(synth.kv_cache_shape(cfg, 3, max_ctx), dtype=torch.bfloat16, device=dev)
+        lens = [150, 40, 90]
+        stride = 160
+        prompts = [synth.make_tokens(n, cfg.vocab, seed=80 + b).numpy() for b, n in enumerate(lens)]
+        toks = np.zeros((3, stride), dtype=np.int32)
+        for b, sq in enumerate(prompts):
+            toks[b, :len(sq)] = sq
+        lg = torch.empty((3, cfg.vocab), device=dev)
+        plan.prefill_batch(torch.from_numpy(toks).to(dev), lens, kv, lg)
+        assert plan.status() == mk.MK_OK
+        cont = synth.make_tokens(130, cfg.vocab, seed=90).numpy()
+        dec = synth.make_tokens(2, cfg.vocab, seed=91).numpy()
+        ctoks = np.concatenate([cont, dec]).astype(np.int32)
+        chunks = [(0, 150, 130, 0), (1, 40, 1, 130), (2, 90, 1, 131)]
+        clg = torch.full((3, cfg.vocab), float("nan"), device=dev)
+        plan.prefill_chunks(torch.from_numpy(ctoks).to(dev), chunks, kv, clg)
+        assert plan.status() == mk.MK_OK
+        got = clg.cpu().numpy()
+        cache = oracle.widen_bf16(synth.bf16_bits(kv))
+        seqs = [np.concatenate([prompts[0], cont]), np.concatenate([prompts[1], dec[:1]]),
+                np.concatenate([prompts[2], dec[1:]])]
+        for b, sq in enumerate(seqs):
+            ref, K, V = oracle.prefill(cfg, synth.LazyBits(w), sq)
+            _rows_close(got[b:b + 1], ref[None, :])
+            p0, n = chunks[b][1], chunks[b][2]
+            _kv_close(f"K{b}", cache[:, 0, b, :, p0:p0 + n, :], K[:, :, p0:p0 + n, :])
+            _kv_close(f"V{b}", cache[:, 1, b, :, p0:p0 + n, :], V[:, :, p0:p0 + n, :])
+        # a chunk that does not continue its slot's previous chunk is refused
+        with pytest.raises(mk.MkError):
+            plan.prefill_chunks(torch.from_numpy(ctoks).to(dev), [(0, 10, 5, 0), (0, 20, 5, 5)], kv, clg)
+    finally:
+        plan.close()
+        del w
+        torch.cuda.empty_cache()

@@ -804,32 +804,34 @@ int mk_prefill(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logi
   return prefill_lm(p, tokens, len - 1, kv, logits, st);
 }
 
-int mk_prefill_batch(mk_plan* p, const int32_t* tokens, const int32_t* lens, int batch, int stride,
-                     void* kv, float* logits, void* stream) {
-  if (!p || !tokens || !lens || !kv || !logits || batch < 1 || batch > p->max_batch ||
-      stride < 1 || !aligned16(kv))
-    return MK_ERR_INVALID_ARG;
-  for (int b = 0; b < batch; ++b)
-    if (lens[b] < 1 || lens[b] > p->hp.max_ctx || lens[b] > stride) return MK_ERR_INVALID_ARG;
-  if (p->latched) return p->latched;
-  cudaStream_t st = (cudaStream_t)stream;
+// One prefill chunk: `len` tokens of the sequence in cache slot `slot`,
+// taking cache positions pos0 .. pos0 + len - 1 (positions below pos0 already
+// cached), its tokens at tokens[tok .. tok + len).
+struct PfChunk {
+  int slot, pos0, len, tok;
+};
+
+// The chunks' 128-token blocks go end to end into the launch's activation
+// planes (as many chunks per launch as fit the plan's context), so every
+// weight tile streams once per launch for all of them; then each chunk's last
+// token runs its LM head into logits[i].
+static int prefill_chunks(mk_plan* p, const int32_t* tokens, const std::vector<PfChunk>& ch, void* kv,
+                          float* logits, cudaStream_t st) {
   int rc;
   if ((rc = prefill_init(p)) != MK_OK || (rc = prefill_bind_kv(p, kv, st)) != MK_OK) return rc;
   const int V = p->hp.cfg.vocab;
   const int cap = p->pf.pp.n_blocks;  // token blocks one launch holds
-  // The prompts' 128-token blocks go end to end into the launch's activation
-  // planes (as many prompts per launch as fit: all of them when their blocks
-  // fit the plan's context), so every weight tile streams once per launch for
-  // all of its prompts; then each prompt's last token gets its LM head.
-  for (int b0 = 0; b0 < batch;) {
+  const int n = (int)ch.size();
+  for (int c0 = 0; c0 < n;) {
     std::vector<int4> tab;
-    int b1 = b0;
-    while (b1 < batch) {
-      const int nb = (lens[b1] + PF_BM - 1) / PF_BM;
+    int c1 = c0;
+    while (c1 < n) {
+      const int nb = (ch[c1].len + PF_BM - 1) / PF_BM;
       if (!tab.empty() && (int)tab.size() + nb > cap) break;
       const int first = (int)tab.size();
-      for (int m = 0; m < nb; ++m) tab.push_back(make_int4(b1, first, lens[b1], b1 * stride));
-      ++b1;
+      for (int m = 0; m < nb; ++m)
+        tab.push_back(make_int4(ch[c1].slot | (first << 16), ch[c1].pos0, ch[c1].len, ch[c1].tok));
+      ++c1;
     }
     // (a pageable source: the copy has read it when the call returns)
     MK_CUDA(cudaMemcpyAsync(p->pf.d_blk, tab.data(), sizeof(int4) * tab.size(), cudaMemcpyHostToDevice,
@@ -843,15 +845,48 @@ int mk_prefill_batch(mk_plan* p, const int32_t* tokens, const int32_t* lens, int
     k.wait_limit_ns = p->wait_limit_ns;
     MK_CUDA(pf_launch_mega(k, p->n_sms, st));
     int blk0 = 0;
-    for (int b = b0; b < b1; ++b) {
-      const int row = blk0 * PF_BM + lens[b] - 1;
-      if ((rc = prefill_lm(p, tokens + (size_t)b * stride, row, kv, logits + (size_t)b * V, st)) != MK_OK)
-        return rc;
-      blk0 += (lens[b] + PF_BM - 1) / PF_BM;
+    for (int c = c0; c < c1; ++c) {
+      const int row = blk0 * PF_BM + ch[c].len - 1;
+      if ((rc = prefill_lm(p, tokens, row, kv, logits + (size_t)c * V, st)) != MK_OK) return rc;
+      blk0 += (ch[c].len + PF_BM - 1) / PF_BM;
     }
-    b0 = b1;
+    c0 = c1;
   }
   return MK_OK;
+}
+
+int mk_prefill_batch(mk_plan* p, const int32_t* tokens, const int32_t* lens, int batch, int stride,
+                     void* kv, float* logits, void* stream) {
+  if (!p || !tokens || !lens || !kv || !logits || batch < 1 || batch > p->max_batch ||
+      stride < 1 || !aligned16(kv))
+    return MK_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b)
+    if (lens[b] < 1 || lens[b] > p->hp.max_ctx || lens[b] > stride) return MK_ERR_INVALID_ARG;
+  if (p->latched) return p->latched;
+  std::vector<PfChunk> ch(batch);
+  for (int b = 0; b < batch; ++b) ch[b] = PfChunk{b, 0, lens[b], b * stride};
+  return prefill_chunks(p, tokens, ch, kv, logits, (cudaStream_t)stream);
+}
+
+int mk_prefill_chunks(mk_plan* p, const int32_t* tokens, const int32_t* chunks, int n, void* kv,
+                      float* logits, void* stream) {
+  if (!p || !tokens || !chunks || !kv || !logits || n < 1 || !aligned16(kv)) return MK_ERR_INVALID_ARG;
+  std::vector<PfChunk> ch(n);
+  for (int i = 0; i < n; ++i) {
+    ch[i] = PfChunk{chunks[4 * i], chunks[4 * i + 1], chunks[4 * i + 2], chunks[4 * i + 3]};
+    const PfChunk& c = ch[i];
+    if (c.slot < 0 || c.slot >= p->max_batch || c.pos0 < 0 || c.len < 1 || c.tok < 0 ||
+        (long)c.pos0 + c.len > p->hp.max_ctx)
+      return MK_ERR_INVALID_ARG;
+    // a later chunk of the same slot continues the slot's previous chunk
+    for (int j = i - 1; j >= 0; --j)
+      if (ch[j].slot == c.slot) {
+        if (ch[j].pos0 + ch[j].len != c.pos0) return MK_ERR_INVALID_ARG;
+        break;
+      }
+  }
+  if (p->latched) return p->latched;
+  return prefill_chunks(p, tokens, ch, kv, logits, (cudaStream_t)stream);
 }
 
 int mk_prefill_logits(mk_plan* p, const int32_t* tokens, int len, void* kv, float* logits,

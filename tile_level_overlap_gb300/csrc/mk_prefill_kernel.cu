@@ -220,37 +220,44 @@ __device__ __forceinline__ int kv_row(const PfParams& P, int l, int kv, int g, i
   return (((l * 2 + kv) * P.max_batch + slot) * P.nkv + g) * P.max_ctx;
 }
 
-// Where plane row p of the launch belongs: its prompt's cache slot, its
-// position in the prompt, the prompt's length, its index in `tokens`, and
-// whether it holds a token (rows past a prompt's end pad its last block).
+// The chunk that block m of the launch belongs to: its cache slot, its first
+// block in the launch, the cache position of its first token, its length and
+// its first token's index in `tokens`.  One prompt (no table): slot `slot`,
+// position 0, length S.
+struct PfBlk {
+  int slot, first, pos0, len, tok;
+};
+__device__ __forceinline__ PfBlk pf_blk(const PfParams& P, int m) {
+  if (!P.blk) return PfBlk{P.slot, 0, 0, P.S, 0};
+  const int4 b = P.blk[m];
+  return PfBlk{b.x & 0xffff, b.x >> 16, b.y, b.z, b.w};
+}
+// Where plane row p of the launch belongs: its chunk's cache slot, its cache
+// position, the end of its chunk's keys, its index in `tokens`, and whether it
+// holds a token (rows past a chunk's end pad its last block).
 struct PfRow {
-  int slot, pos, len, tok;
+  int slot, pos, kend, tok;
   bool live;
 };
 __device__ __forceinline__ PfRow pf_row(const PfParams& P, int p) {
-  PfRow r;
-  if (!P.blk) {
-    r.slot = P.slot;
-    r.pos = p;
-    r.len = P.S;
-    r.tok = p;
-  } else {
-    const int4 b = P.blk[p / PF_BM];
-    r.slot = b.x;
-    r.pos = p - b.y * PF_BM;
-    r.len = b.z;
-    r.tok = b.w + r.pos;
-  }
-  r.live = r.pos < r.len;
-  return r;
+  const PfBlk b = pf_blk(P, p / PF_BM);
+  const int r = p - b.first * PF_BM;  // row within the chunk
+  PfRow w;
+  w.slot = b.slot;
+  w.pos = b.pos0 + r;
+  w.kend = b.pos0 + b.len;
+  w.tok = b.tok + r;
+  w.live = r < b.len;
+  return w;
 }
-// First block of the prompt that block m belongs to (its causal key blocks
-// are first .. m).
-__device__ __forceinline__ int pf_first_block(const PfParams& P, int m) {
-  return P.blk ? P.blk[m].y : 0;
-}
-__device__ __forceinline__ int pf_block_slot(const PfParams& P, int m) {
-  return P.blk ? P.blk[m].x : P.slot;
+// Key blocks (128 cache positions each, from position 0) that block m's rows
+// attend to: up to its last live row's position (causal; keys before the
+// chunk come from the cache, the chunk's own from its QKV tiles).
+__device__ __forceinline__ int pf_key_blocks(const PfParams& P, int m) {
+  const PfBlk b = pf_blk(P, m);
+  const int r0 = (m - b.first) * PF_BM;
+  const int last = (b.len < r0 + PF_BM ? b.len : r0 + PF_BM) - 1;
+  return (b.pos0 + last) / PF_BM + 1;
 }
 
 // ---------------------------------------------------------------- producer
@@ -332,11 +339,11 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
       // one stage per key block: K_j at +0, V_j at +tile (Q goes to TMEM
       // through the compute warps)
       const int m = (int)in.a0, gq = (int)in.a1, l = in.layer;
-      const int first = pf_first_block(P, m), slot = pf_block_slot(P, m);
+      const int nkb = pf_key_blocks(P, m), slot = pf_blk(P, m).slot;
       const uint32_t tile = PF_BM * P.d * 2;  // one 128-row tile of d columns
       const int nbox = P.d / 64;
       for (int h = 0; h < P.rep; ++h)
-        for (int j = first; j <= m; ++j) {
+        for (int j = 0; j < nkb; ++j) {
           const int st = stage_ctr % PF_NSTAGE;
           pf_wait(P, &S.empty[st], ((stage_ctr / PF_NSTAGE) & 1u) ^ 1u);
           uint8_t* sp = S.ring + st * PF_STAGE;
@@ -344,7 +351,7 @@ __device__ void pf_producer(const PfParams& P, const PfSh& S) {
           for (int kvsel = 0; kvsel < 2; ++kvsel)
             for (int bx = 0; bx < nbox; ++bx)
               tma_load_2d(sp + kvsel * tile + bx * 16384, tmap(P, am(P, AM_KV)), bx * 64,
-                          kv_row(P, l, kvsel, gq, slot) + (j - first) * PF_BM, &S.full[st], pol_a);
+                          kv_row(P, l, kvsel, gq, slot) + j * PF_BM, &S.full[st], pol_a);
           ++stage_ctr;
         }
     }
@@ -404,7 +411,7 @@ __device__ void pf_mma(const PfParams& P, const PfSh& S, uint32_t tbase) {
         ++use[b];
       }
       tc_fence_after();
-      const int m = (int)in.a0, first = pf_first_block(P, m);
+      const int nkb = pf_key_blocks(P, (int)in.a0);
       const uint32_t s_t = tbase, o_t = tbase + 128, p_t = tbase + 256, pl_t = tbase + 320;
       const uint32_t q_t = tbase + 384, ql_t = tbase + 448;
       const uint32_t id_s = idesc_bf16_f32(PF_BM, PF_BM);
@@ -414,7 +421,7 @@ __device__ void pf_mma(const PfParams& P, const PfSh& S, uint32_t tbase) {
         pf_wait(P, S.qfull, qctr & 1u);
         ++qctr;
         tc_fence_after();
-        for (int j = first; j <= m; ++j) {
+        for (int j = 0; j < nkb; ++j) {
           // S = Q K_j^T (K = head_dim, in 64-column atoms 16 KB apart)
           const int st = stage_ctr % PF_NSTAGE;
           pf_wait(P, &S.full[st], (stage_ctr / PF_NSTAGE) & 1u);
@@ -697,11 +704,11 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
                         uint32_t lane_base, uint32_t& sctr) {
   const int m = (int)in.a0, gq = (int)in.a1, lane = threadIdx.x & 31;
   const int qi = m * PF_BM + row;  // < plane_rows: rows past the prompt are never stored
-  // positions within the prompt: this row's, and the keys' from the prompt's
-  // first block
+  // cache positions: this row's, and the end of its chunk's keys; key block j
+  // holds positions 128 j .. 128 j + 127
   const PfRow pr = pf_row(P, qi);
-  const int first = pf_first_block(P, m);
-  const int qpos = pr.pos, klen = pr.len;
+  const int nkb = pf_key_blocks(P, m);
+  const int qpos = pr.pos, klen = pr.kend;
   const int qd = P.nq * D;
   const float c = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
   const uint32_t s_t = tbase + lane_base, o_t = tbase + 128 + lane_base;
@@ -732,10 +739,12 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
 #pragma unroll
     for (int e = 0; e < D; ++e) o[e] = 0.f;
     float mrun = -INFINITY, lrun = 0.f, alpha_prev = 0.f;
-    for (int j = first; j <= m; ++j) {
+    for (int j = 0; j < nkb; ++j) {
       pf_wait(P, S.sfull, sctr & 1u);
       tc_fence_after();
-      const bool diag = j == m;
+      // the blocks that can hold keys past this row (the causal diagonal of a
+      // chunk not aligned to 128 positions may cross two of them)
+      const bool diag = (j + 1) * PF_BM > qpos || (j + 1) * PF_BM > klen;
       // pass 1: row max of the scaled scores
       float mx = -INFINITY;
       for (int c0 = 0; c0 < PF_BM; c0 += 16) {
@@ -743,14 +752,14 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
         tmem_ld16(s_t + (uint32_t)c0, s);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int kj = (j - first) * PF_BM + c0 + e;
+          const int kj = j * PF_BM + c0 + e;
           const bool masked = diag && (kj > qpos || kj >= klen);
           if (!masked) mx = fmaxf(mx, s[e] * c);
         }
       }
       const float mnew = fmaxf(mrun, mx);
       const float alpha = mrun == -INFINITY ? 0.f : exp2f(mrun - mnew);
-      if (j > first) {
+      if (j > 0) {
         // O_{j-1} = P_{j-1} V_{j-1} was issued before S_j, so it is complete
         // (and P's columns are free); fold it in at the scale of block j-1
         pf_wait(P, S.ofull, (sctr - 1) & 1u);
@@ -771,7 +780,7 @@ __device__ void pf_attn(const PfParams& P, const PfSh& S, const Instr& in, uint3
         uint32_t hi[8], lo[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          const int kj = (j - first) * PF_BM + c0 + e;
+          const int kj = j * PF_BM + c0 + e;
           const bool m0 = diag && (kj > qpos || kj >= klen);
           const bool m1 = diag && (kj + 1 > qpos || kj + 1 >= klen);
           const float p0 = m0 ? 0.f : exp2f(s[e] * c - mnew);

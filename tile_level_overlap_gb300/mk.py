@@ -33,7 +33,7 @@ EXPORTED = [
     "mk_status_string", "mk_plan_get_stats", "mk_plan_check", "mk_plan_set_debug",
     "mk_trace_copy", "mk_plan_debug_drop_release", "mk_debug_gemm_bf16", "mk_decode_step_noalloc",
     "mk_plan_set_lm_mode", "mk_decode_steps", "mk_prefill_logits", "mk_prefill_batch",
-    "mk_decode_step_slots", "mk_plan_create_for_sms",
+    "mk_decode_step_slots", "mk_plan_create_for_sms", "mk_prefill_chunks",
 ]
 
 
@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
     L.mk_decode_step_slots.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, vp]
     L.mk_prefill_batch.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int,
                                    vp, vp, vp]
+    L.mk_prefill_chunks.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, vp, vp, vp]
     L.mk_trace_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mk_plan_debug_drop_release.argtypes = [vp, ctypes.c_uint32]
     L.mk_debug_gemm_bf16.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -267,6 +268,15 @@ class Plan:
         arr = (ctypes.c_int32 * n)(*[int(v) for v in lens])
         _check(lib().mk_prefill_batch(self.h, _ptr(tokens), arr, n, int(tokens.shape[1]), _ptr(kv),
                                       _ptr(logits), _stream_ptr(stream)), "mk_prefill_batch")
+
+    def prefill_chunks(self, tokens, chunks, kv, logits, stream=None) -> None:
+        """mk_prefill_chunks: tokens device int32 [*], chunks a list of (slot,
+        pos0, len, token offset), logits device [n, V]."""
+        n = len(chunks)
+        flat = [int(v) for c in chunks for v in c]
+        arr = (ctypes.c_int32 * (4 * n))(*flat)
+        _check(lib().mk_prefill_chunks(self.h, _ptr(tokens), arr, n, _ptr(kv), _ptr(logits),
+                                       _stream_ptr(stream)), "mk_prefill_chunks")
 
     def prefill_logits(self, tokens, kv, logits, stream=None) -> None:
         """mk_prefill_logits: the prompt's logits for every token, [len, V]."""
