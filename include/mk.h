@@ -133,8 +133,15 @@ int mk_decode_step_host(mk_plan *plan, const int32_t *tokens_host, const int32_t
  *  - Shapes whose scratch exceeds MK_NOALLOC_SCRATCH_BYTES return
  *    MK_ERR_UNSUPPORTED before any device work.
  *  - The first call on a device (with that device current) looks up the
- *    array's device address and sets the kernel's shared-memory limit; make
- *    that first call before any stream capture.
+ *    array's device address and sets the kernel's shared-memory limit.
+ *  - A call on a stream that is being captured into a graph returns
+ *    MK_ERR_INVALID_ARG before any device work (the call copies host data
+ *    that a replayed graph would read after it is gone).
+ *  - The host-side plan and RoPE table are kept from the previous call with
+ *    the same (shape, max_batch, max_ctx, device SM count), and the array's
+ *    queue, bytecode, RoPE table and layer table are re-copied only when the
+ *    previous call on the device left another shape's (or other weights') in
+ *    it; repeated calls with one shape cost a memset and the launch.
  *  - All calls share the one array and find the previous call's contents;
  *    each call clears its own counters and control words.  Calls whose work
  *    overlaps on the GPU (several streams or threads) race on the array:

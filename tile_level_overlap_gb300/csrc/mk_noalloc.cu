@@ -12,6 +12,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -45,6 +46,31 @@ KernelVariant variant_for(const HostPlan& hp) {
 
 bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
+// The host-side work of a call depends only on (shape, max_batch, max_ctx,
+// SM count): the plan build and the RoPE table are kept from the previous call
+// with the same key, and the queue, bytecode and RoPE table are copied into
+// the static array only when the array does not already hold them (calls are
+// serialised by contract, so the last upload per device is what it holds).
+struct NoallocKey {
+  mk_model_cfg cfg;
+  int max_batch, max_ctx, sms;
+  bool same(const NoallocKey& o) const {
+    return std::memcmp(&cfg, &o.cfg, sizeof(cfg)) == 0 && max_batch == o.max_batch &&
+           max_ctx == o.max_ctx && sms == o.sms;
+  }
+};
+struct NoallocHost {
+  bool valid = false;
+  NoallocKey key{};
+  HostPlan hp;
+  std::vector<float2> rope;
+};
+std::mutex g_mu;
+NoallocHost g_host;                            // last plan built (any device)
+NoallocKey g_resident[kMaxDevices];            // the shape each device's array holds
+bool g_resident_valid[kMaxDevices] = {false};
+std::vector<LayerW> g_resident_lw[kMaxDevices];  // the layer table it holds
+
 }  // namespace
 }  // namespace mk
 
@@ -56,16 +82,47 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
                                       float* logits, void* stream) {
   if (!cfg || !w || !tokens || !positions || !kv_cache || !logits) return MK_ERR_INVALID_ARG;
   if (batch < 1 || batch > max_batch || !al16(kv_cache)) return MK_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  // The copies below read host memory that this library owns and rewrites: a
+  // captured graph would replay them later, so a capturing stream is refused.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return MK_ERR_INVALID_ARG;
   int cur = 0, sms = 0;
   if (cudaGetDevice(&cur) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, cur) != cudaSuccess) {
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
-  HostPlan hp;
-  std::string why;
-  int rc = build_plan(*cfg, max_batch, max_ctx, sms, &hp, &why);
-  if (rc != MK_OK) return rc;
+  NoallocKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.cfg = *cfg;
+  key.max_batch = max_batch;
+  key.max_ctx = max_ctx;
+  key.sms = sms;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_host.valid || !g_host.key.same(key)) {
+    g_host.valid = false;
+    std::string why;
+    const int rc = build_plan(*cfg, max_batch, max_ctx, sms, &g_host.hp, &why);
+    if (rc != MK_OK) return rc;
+    if (decode_scratch(g_host.hp).total > (size_t)MK_NOALLOC_SCRATCH_BYTES)
+      return MK_ERR_UNSUPPORTED;  // before the RoPE table is computed
+    const int hd = g_host.hp.cfg.head_dim;
+    g_host.rope.assign((size_t)max_ctx * (hd / 2), make_float2(0.f, 0.f));
+    for (int pos = 0; pos < max_ctx; ++pos)
+      for (int i = 0; i < hd / 2; ++i) {
+        const double a = (double)pos * std::pow((double)g_host.hp.cfg.rope_theta, -2.0 * i / hd);
+        g_host.rope[(size_t)pos * (hd / 2) + i] =
+            make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    g_host.key = key;
+    g_host.valid = true;
+  }
+  const HostPlan& hp = g_host.hp;
   const mk_model_cfg& c = hp.cfg;
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
   std::vector<LayerW> lw(L);
@@ -110,29 +167,36 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   int nsm = 0;
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MK_ERR_CUDA;
   uint8_t* s = g_scratch_addr[dev];
-  cudaStream_t st = (cudaStream_t)stream;
 
-  std::vector<float2> rope((size_t)max_ctx * (d / 2));
-  for (int pos = 0; pos < max_ctx; ++pos)
-    for (int i = 0; i < d / 2; ++i) {
-      const double a = (double)pos * std::pow((double)c.rope_theta, -2.0 * i / d);
-      rope[(size_t)pos * (d / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
-    }
-  // Copies from pageable host memory return once the source has been read.
-  if (cudaMemcpyAsync(s + o_q, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
-                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(s + o_expr, hp.expr.data(), sizeof(uint32_t) * hp.expr.size(),
-                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(s + o_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice,
-                      st) != cudaSuccess ||
-      cudaMemcpyAsync(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess ||
-      // every call restarts the launch counter at 0, so the tagged
-      // intermediate tensors, the counters and the control words all start
-      // at zero (no word left by an earlier call, of any shape, carries a tag
-      // this call expects)
-      cudaMemsetAsync(s, 0, ds.zero_end, st) != cudaSuccess)
-    return MK_ERR_CUDA;
+  // The queue, bytecode and RoPE table go in only when this device's array
+  // holds another shape's (pageable copies return once the source is read),
+  // the layer table only when the weights moved.  Every call clears the tagged
+  // intermediate tensors, the counters and the control words: the launch
+  // counter restarts at 0, so no word left by an earlier call, of any shape,
+  // carries a tag this call expects.
+  const std::vector<float2>& rope = g_host.rope;
+  if (!(g_resident_valid[dev] && g_resident[dev].same(key))) {
+    g_resident_valid[dev] = false;
+    g_resident_lw[dev].clear();
+    if (cudaMemcpyAsync(s + o_q, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(s + o_expr, hp.expr.data(), sizeof(uint32_t) * hp.expr.size(),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(s + o_rope, rope.data(), sizeof(float2) * rope.size(),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MK_ERR_CUDA;
+    g_resident[dev] = key;
+    g_resident_valid[dev] = true;
+  }
+  if (g_resident_lw[dev].size() != lw.size() ||
+      std::memcmp(g_resident_lw[dev].data(), lw.data(), sizeof(LayerW) * lw.size()) != 0) {
+    g_resident_lw[dev].clear();
+    if (cudaMemcpyAsync(s + o_lw, lw.data(), sizeof(LayerW) * L, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return MK_ERR_CUDA;
+    g_resident_lw[dev] = lw;
+  }
+  if (cudaMemsetAsync(s, 0, ds.zero_end, st) != cudaSuccess) return MK_ERR_CUDA;
 
   KParams k;
   std::memset(&k, 0, sizeof(k));
