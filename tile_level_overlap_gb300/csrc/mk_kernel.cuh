@@ -7,9 +7,12 @@
 // operand bytes -- weight rows, or cached K/V rows -- into a shared-memory ring
 // with bulk async copies, running ahead of the consumers by up to NSTAGE
 // stages and NISLOT instructions.  Eight consumer warps take instructions in
-// pop order, wait (bounded) on the per-tile barrier counters of the tiles they
-// read, compute from the ring, store their output tile and release its
-// counter.  This is the on-device interpreter of "Lecture 112: Production
+// pop order, compute from the ring, and read their other inputs with a
+// bounded poll on the tag each element of an intermediate tensor carries (the
+// launch step that wrote it), so a tile waits on exactly the elements it
+// reads; a finisher warp adds the consumers' partial sums of a batch-1 GEMV
+// tile and stores its outputs under the step's tag, which publishes them
+// without a fence or counter.  This is the on-device interpreter of "Lecture 112: Production
 // Megakernels for Real-World Inference" (Technical details: a loop with a
 // switch, instructions popped atomically from a queue in DRAM; memory
 // pipelining across output tiles) with the tile-level dependencies and the
