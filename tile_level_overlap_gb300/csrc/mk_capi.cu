@@ -425,7 +425,7 @@ int mk_plan_create_for_sms(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int
   }
   uint8_t* s = (uint8_t*)p->scratch;
   if (cudaMemset(p->scratch, 0, p->scratch_bytes) != cudaSuccess) return fail(MK_ERR_CUDA);
-  const size_t o_q = ds.o_q, o_expr = ds.o_expr, o_rope = ds.o_rope, o_lw = ds.o_lw;
+  const size_t o_q = ds.o_q, o_rope = ds.o_rope, o_lw = ds.o_lw;
 
   std::vector<float2> rope((size_t)max_ctx * (d / 2));
   for (int pos = 0; pos < max_ctx; ++pos)
@@ -443,8 +443,6 @@ int mk_plan_create_for_sms(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int
   if (cudaMemcpy(s + o_q, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
                  cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(s + o_qmk, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
-                 cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(s + o_expr, hp.expr.data(), sizeof(uint32_t) * hp.expr.size(),
                  cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(s + o_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice) !=
           cudaSuccess ||
@@ -479,7 +477,7 @@ int mk_plan_create_for_sms(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int
   k.n_instr = (uint32_t)hp.decode.size();
   k.n_steps = 1;
   p->d_msteps = s + o_msteps;
-  k.expr = (const uint32_t*)(s + o_expr);
+  std::memcpy(k.xw, hp.expr.data(), sizeof(k.xw));
   k.bl = hp.bl;
   p->kv_bytes = (size_t)L * 2 * max_batch * nkv * (size_t)max_ctx * d * 2;
   if (p->bd.on && (rc = bd_init(p, w)) != MK_OK) return fail(rc);
@@ -673,7 +671,6 @@ static int prefill_init(mk_plan* p) {
   const size_t o_bars = bm.take(sizeof(uint32_t) * pp.bl.total);
   const size_t o_ctl = bm.take(sizeof(uint32_t) * CTL_WORDS);
   const size_t o_q = bm.take(sizeof(Instr) * pp.queue.size());
-  const size_t o_expr = bm.take(sizeof(uint32_t) * pp.expr.size());
   const size_t o_tm = bm.take(sizeof(CUtensorMap) * n_maps);
   const size_t o_xa = bm.take(sizeof(float) * rows * H);
   const size_t o_xb = bm.take(sizeof(float) * rows * H);
@@ -716,8 +713,6 @@ static int prefill_init(mk_plan* p) {
        make_tmap_bf16(a + AM_LMW, p->base.lm, (uint64_t)c.vocab, H, PF_BN);
   if (!ok) return MK_ERR_CUDA;
   MK_CUDA(cudaMemcpy(b + o_q, pp.queue.data(), sizeof(Instr) * pp.queue.size(), cudaMemcpyHostToDevice));
-  MK_CUDA(cudaMemcpy(b + o_expr, pp.expr.data(), sizeof(uint32_t) * pp.expr.size(),
-                     cudaMemcpyHostToDevice));
   MK_CUDA(cudaMemcpy(s.d_tm, s.h_tm.data(), sizeof(CUtensorMap) * n_maps, cudaMemcpyHostToDevice));
   PfParams& k = s.base;
   std::memset(&k, 0, sizeof(k));
@@ -743,7 +738,7 @@ static int prefill_init(mk_plan* p) {
   k.ctl = (uint32_t*)(b + o_ctl);
   k.queue = (const Instr*)(b + o_q);
   k.n_instr = pp.n_body;  // the all-token logits entry point runs the rest too
-  k.expr = (const uint32_t*)(b + o_expr);
+  std::memcpy(k.xw, pp.expr.data(), sizeof(k.xw));
   s.built = true;
   return MK_OK;
 }

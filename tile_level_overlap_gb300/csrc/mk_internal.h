@@ -74,50 +74,55 @@ enum XOp : uint32_t {
   X_ADD = 8, X_SUB = 9, X_MUL = 10, X_CEILDIV = 11, X_MIN = 12, X_MAX = 13
 };
 constexpr int X_MAX_WORDS = 32;  // words per expression slot
-constexpr int X_STACK = 8;
+constexpr int X_STACK = 4;  // evaluation stack depth (x_eval; checked when a plan is built)
 
 MK_HD uint32_t xw(uint32_t op, uint32_t imm = 0) { return (op << 24) | (imm & 0xffffffu); }
 
 // Evaluate expression `e` (X_MAX_WORDS words).  `pos` may be null when the
 // expression does not read positions; X_POS reads pos[b] + pos_add (the step
-// index of a multi-step launch).  Out-of-range positions evaluate as 0; the
-// caller validates them separately.
+// index of a multi-step launch), or `known_pos` + pos_add without a load when
+// b == known_b (a position the caller already holds).  Out-of-range positions
+// evaluate as 0; the caller validates them separately.
 MK_HD int64_t x_eval(const uint32_t* e, const Instr& in, int B, int S, const int32_t* pos,
-                     int n_pos, int pos_add = 0) {
-  int64_t st[X_STACK];
+                     int n_pos, int pos_add = 0, int known_b = -1, int known_pos = 0) {
+  // 32-bit values (extents and positions stay below 2^24) in X_STACK
+  // registers (a shift register) rather than a local array: on the device a
+  // dynamically indexed array goes to local memory, whose round trips under
+  // load made an evaluation take microseconds.
+  int32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
   int sp = 0;
   for (int i = 0; i < X_MAX_WORDS; ++i) {
-    uint32_t w = e[i];
-    uint32_t op = w >> 24;
-    int64_t imm = (int64_t)(w & 0xffffffu);
+    const uint32_t w = e[i];
+    const uint32_t op = w >> 24;
+    const int32_t imm = (int32_t)(w & 0xffffffu);
     if (op == X_END) break;
-    switch (op) {
-      case X_CONST: st[sp++] = imm; break;
-      case X_ARG0: st[sp++] = in.a0; break;
-      case X_ARG1: st[sp++] = in.a1; break;
-      case X_ARG2: st[sp++] = in.a2; break;
-      case X_B: st[sp++] = B; break;
-      case X_S: st[sp++] = S; break;
-      case X_POS: {
-        int64_t b = st[sp - 1];
-        st[sp - 1] = (pos && b >= 0 && b < n_pos) ? (int64_t)pos[b] + pos_add : 0;
-        break;
-      }
-      default: {
-        int64_t y = st[--sp];
-        int64_t x = st[sp - 1];
-        int64_t r = 0;
-        if (op == X_ADD) r = x + y;
-        else if (op == X_SUB) r = x - y;
-        else if (op == X_MUL) r = x * y;
-        else if (op == X_CEILDIV) r = y > 0 ? (x + y - 1) / y : 0;
-        else if (op == X_MIN) r = x < y ? x : y;
-        else if (op == X_MAX) r = x > y ? x : y;
-        st[sp - 1] = r;
-      }
+    if (op <= X_S) {  // a push
+      const int32_t v = op == X_CONST  ? imm
+                        : op == X_ARG0 ? (int32_t)in.a0
+                        : op == X_ARG1 ? (int32_t)in.a1
+                        : op == X_ARG2 ? (int32_t)in.a2
+                        : op == X_B    ? (int32_t)B
+                                       : (int32_t)S;
+      s3 = s2; s2 = s1; s1 = s0; s0 = v;
+      ++sp;
+    } else if (op == X_POS) {  // top b -> positions[b]
+      const int32_t b = s0;
+      s0 = b == known_b && b >= 0 ? (int32_t)known_pos + pos_add
+           : (pos && b >= 0 && b < n_pos) ? (int32_t)pos[b] + pos_add : 0;
+    } else {  // a binary operator: second from top (x) op top (y)
+      const int32_t y = s0, x = s1;
+      int32_t r = 0;
+      if (op == X_ADD) r = x + y;
+      else if (op == X_SUB) r = x - y;
+      else if (op == X_MUL) r = x * y;
+      else if (op == X_CEILDIV) r = y > 0 ? (x + y - 1) / y : 0;
+      else if (op == X_MIN) r = x < y ? x : y;
+      else if (op == X_MAX) r = x > y ? x : y;
+      s0 = r; s1 = s2; s2 = s3;
+      --sp;
     }
   }
-  return sp > 0 ? st[sp - 1] : 0;
+  return sp > 0 ? s0 : 0;
 }
 
 // Expression slots used by the plan.
@@ -196,7 +201,12 @@ struct KParams {
   uint32_t* ctl;
   const Instr* queue;
   uint32_t n_instr;
-  const uint32_t* expr;  // [XS_COUNT][X_MAX_WORDS]
+  // the plan's expressions [XS_COUNT][X_MAX_WORDS], held in the launch's
+  // parameter block: the producer evaluates them for every attention
+  // instruction it pops, and reads from the constant cache keep that
+  // evaluation off the memory system (from global memory its dependent word
+  // loads took several microseconds per instruction under the weight stream)
+  uint32_t xw[XS_COUNT * X_MAX_WORDS];
   unsigned long long* trace;  // TRACE_WORDS x u64 per instruction, or null
   BarLayout bl;
   // step
@@ -218,6 +228,7 @@ struct KParams {
   uint32_t* lm_done;           // [n_steps], zero before the launch
   int32_t* out_tokens;         // [n_steps]
 };
+static_assert(sizeof(KParams) <= 4096, "kernel parameter block limit");
 
 // Slot words carry the queue index in the low 24 bits and the step of a
 // multi-step launch above them.

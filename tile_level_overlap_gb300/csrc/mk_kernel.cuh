@@ -200,18 +200,21 @@ struct AttnExt {
 
 __device__ __forceinline__ AttnExt attn_extent(const KParams& P, const Instr& in, uint32_t step = 0) {
   AttnExt e;
-  e.live = x_eval(P.expr + XS_SEQ_LIVE * X_MAX_WORDS, in, P.B, P.S, nullptr, 0) > 0;
+  e.live = x_eval(P.xw + XS_SEQ_LIVE * X_MAX_WORDS, in, P.B, P.S, nullptr, 0) > 0;
   e.pos = 0;
   e.lo = e.hi = e.nc = 0;
   e.has_new = false;
   if (!e.live) return e;
-  e.pos = P.positions[in.a0] + (int)step;
+  const int p0 = P.positions[in.a0];
+  e.pos = p0 + (int)step;
   if (e.pos < 0 || e.pos >= P.max_ctx) {
     e.live = false;
     return e;
   }
-  e.lo = (int)x_eval(P.expr + XS_ATTN_LO * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step);
-  e.hi = (int)x_eval(P.expr + XS_ATTN_HI * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step);
+  e.lo = (int)x_eval(P.xw + XS_ATTN_LO * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step,
+                     (int)in.a0, p0);
+  e.hi = (int)x_eval(P.xw + XS_ATTN_HI * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step,
+                     (int)in.a0, p0);
   int cend = e.hi < e.pos ? e.hi : e.pos;
   e.nc = cend > e.lo ? cend - e.lo : 0;
   e.has_new = e.lo <= e.pos && e.pos < e.hi;
@@ -340,6 +343,9 @@ __device__ void producer(const KParams& P, const Sh& S) {
   // A multi-step launch runs the queue n_steps times: pop g is instruction
   // g % n_instr of step g / n_instr.
   uint32_t npop = 0;
+  // multi-step: the step of pop g is g / n_instr; a CTA's pops increase, so
+  // the step is tracked by comparison instead of a division per pop
+  uint32_t step_cur = 0, step_base = 0;
   auto pop = [&]() -> uint32_t {
     const uint32_t k = npop++;
     if (P.mode == MODE_MEGA) {
@@ -357,8 +363,14 @@ __device__ void producer(const KParams& P, const Sh& S) {
     const bool room = mbar_wait(P, &S.empty[stage_ctr % NSTAGE], ((stage_ctr / NSTAGE) & 1u) ^ 1u);
     const uint32_t g_in = room ? pop() : END_SLOT;
     const bool end = g_in == END_SLOT;
-    const uint32_t step = (MS && !end) ? g_in / P.n_instr : 0u;
-    const uint32_t i_in = end ? END_SLOT : g_in - step * P.n_instr;
+    if (MS && !end) {
+      while (g_in - step_base >= P.n_instr) {
+        ++step_cur;
+        step_base += P.n_instr;
+      }
+    }
+    const uint32_t step = MS ? step_cur : 0u;
+    const uint32_t i_in = end ? END_SLOT : g_in - (MS ? step_base : 0u);
     Instr in;
     if (!end) in = P.queue[i_in];
     const int si = islot_ctr % NISLOT;
@@ -1513,6 +1525,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
       mbar_init(&S.hfull[b], NW);
       mbar_init(&S.hempty[b], 1);
     }
+
     fence_mbar_init();
     fence_proxy_async_smem();
     S.flags[F_GEN] = P.mode == MODE_MEGA ? ld_volatile(&P.ctl[CTL_GEN]) : 0u;
@@ -1533,6 +1546,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
     setmaxnreg_dec<SPLIT_REGS_SIDE>();
     if (t < NT + 32) producer<MS>(P, S);
     else if (t < NT + 64) finisher<MS>(P, S);
+
   } else {
     setmaxnreg_inc<SPLIT_REGS_CONSUMER>();
     consumer<MH, MF, AD, AREP, MS>(P, S);

@@ -151,7 +151,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   // Carve the static array: the decode layout a plan allocates (one queue copy).
   const DecodeScratch ds = decode_scratch(hp);
   if (ds.total > (size_t)MK_NOALLOC_SCRATCH_BYTES) return MK_ERR_UNSUPPORTED;
-  const size_t o_q = ds.o_q, o_expr = ds.o_expr, o_rope = ds.o_rope, o_lw = ds.o_lw;
+  const size_t o_q = ds.o_q, o_rope = ds.o_rope, o_lw = ds.o_lw;
 
   // Per-device set-up on the first call with that device current: the array's
   // device address and the kernel's shared-memory attribute.
@@ -179,8 +179,6 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
     g_resident_valid[dev] = false;
     g_resident_lw[dev].clear();
     if (cudaMemcpyAsync(s + o_q, hp.decode.data(), sizeof(Instr) * hp.decode.size(),
-                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(s + o_expr, hp.expr.data(), sizeof(uint32_t) * hp.expr.size(),
                         cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(s + o_rope, rope.data(), sizeof(float2) * rope.size(),
                         cudaMemcpyHostToDevice, st) != cudaSuccess)
@@ -221,7 +219,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   k.ctl = (uint32_t*)(s + ds.o_ctl);
   k.queue = (const Instr*)(s + o_q);
   k.n_instr = (uint32_t)hp.decode.size();
-  k.expr = (const uint32_t*)(s + o_expr);
+  std::memcpy(k.xw, hp.expr.data(), sizeof(k.xw));
   k.bl = hp.bl;
   k.tokens = tokens;
   k.positions = positions;

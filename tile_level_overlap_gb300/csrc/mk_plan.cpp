@@ -79,16 +79,31 @@ void set_wait(Instr& in, uint32_t bar, uint32_t target, uint16_t n = 1, uint16_t
   in.wait_stride = stride;
 }
 
-// Postfix expression helpers.
+// Postfix expression helpers.  `depth` tracks the evaluation stack, which
+// x_eval holds in X_STACK registers.
 struct XBuild {
   std::vector<uint32_t> w;
-  XBuild& c(uint32_t v) { w.push_back(xw(X_CONST, v)); return *this; }
-  XBuild& op(uint32_t o) { w.push_back(xw(o)); return *this; }
+  int sp = 0, depth = 0;
+  XBuild& c(uint32_t v) { return push(xw(X_CONST, v)); }
+  XBuild& op(uint32_t o) {
+    if (o <= X_S) return push(xw(o));
+    w.push_back(xw(o));
+    if (o != X_POS) --sp;  // binary operators pop two, push one
+    return *this;
+  }
+  XBuild& push(uint32_t word) {
+    w.push_back(word);
+    depth = ++sp > depth ? sp : depth;
+    return *this;
+  }
 };
 
-void put_expr(std::vector<uint32_t>& table, int slot, const XBuild& x) {
-  for (size_t i = 0; i < x.w.size() && i < (size_t)X_MAX_WORDS; ++i)
-    table[(size_t)slot * X_MAX_WORDS + i] = x.w[i];
+// Store an expression in its slot; false when it does not fit the slot's
+// words or the evaluation stack.
+bool put_expr(std::vector<uint32_t>& table, int slot, const XBuild& x) {
+  if (x.w.size() >= (size_t)X_MAX_WORDS || x.depth > X_STACK) return false;
+  for (size_t i = 0; i < x.w.size(); ++i) table[(size_t)slot * X_MAX_WORDS + i] = x.w[i];
+  return true;
 }
 
 }  // namespace
@@ -184,13 +199,14 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
   {
     XBuild lo;  // min(a2 * KPS, n)
     lo.op(X_ARG2).c(hp.kps).op(X_MUL).op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
-    put_expr(hp.expr, XS_ATTN_LO, lo);
+    bool fits = put_expr(hp.expr, XS_ATTN_LO, lo);
     XBuild hi;  // min((a2 + 1) * KPS, n)
     hi.op(X_ARG2).c(1).op(X_ADD).c(hp.kps).op(X_MUL).op(X_ARG0).op(X_POS).c(1).op(X_ADD).op(X_MIN);
-    put_expr(hp.expr, XS_ATTN_HI, hi);
+    fits = put_expr(hp.expr, XS_ATTN_HI, hi) && fits;
     XBuild live;  // B - a0
     live.op(X_B).op(X_ARG0).op(X_SUB);
-    put_expr(hp.expr, XS_SEQ_LIVE, live);
+    fits = put_expr(hp.expr, XS_SEQ_LIVE, live) && fits;
+    if (!fits) return bad(MK_ERR_UNSUPPORTED, "extent expression exceeds the evaluator");
   }
 
   const uint32_t per_group = (uint32_t)(rep * d + 2 * d) / hp.r_qkv;
@@ -307,7 +323,6 @@ DecodeScratch decode_scratch(const HostPlan& hp) {
   x.o_ctl = take(sizeof(uint32_t) * CTL_WORDS);
   x.zero_end = off;
   x.o_q = take(sizeof(Instr) * hp.decode.size());
-  x.o_expr = take(sizeof(uint32_t) * hp.expr.size());
   x.o_rope = take(sizeof(float2) * (size_t)hp.max_ctx * (d / 2));
   x.o_lw = take(sizeof(LayerW) * L);
   x.total = off;

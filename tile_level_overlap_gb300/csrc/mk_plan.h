@@ -79,7 +79,7 @@ int build_plan(const mk_model_cfg& cfg, int max_batch, int max_ctx, int n_sms, H
 struct DecodeScratch {
   size_t o_resid, o_qkv, o_part, o_attn, o_act, tagged_end;
   size_t o_bars, o_ctl, zero_end;
-  size_t o_q, o_expr, o_rope, o_lw;
+  size_t o_q, o_rope, o_lw;
   size_t total;
 };
 DecodeScratch decode_scratch(const HostPlan& hp);

@@ -88,24 +88,29 @@ struct PfParams {
   int plane_rows;           // rows of one plane (token blocks x 128)
   uint16_t* kv;             // caller's KV cache
   int slot;                 // the sequence slot this prompt's keys and values go to
-  // Several prompts in one launch (mk_prefill_batch): their 128-token blocks
-  // lie end to end in the activation planes, and block j of the launch is
-  // described by blk[j] = {cache slot, the prompt's first block, the prompt's
-  // length, the prompt's offset in `tokens`}; S = the blocks x 128.  Null for
-  // one prompt (slot `slot`, block j = the prompt's block j, length S).
+  // Several prompts or chunks in one launch (mk_prefill_batch,
+  // mk_prefill_chunks): their 128-token blocks lie end to end in the
+  // activation planes, and block j of the launch is described by
+  // blk[j] = {cache slot | the chunk's first block << 16, the chunk's first
+  // position, its length, its first token's offset in `tokens`}; S = the
+  // blocks x 128.  Null for one prompt (slot `slot`, positions from 0, block j
+  // = the prompt's block j, length S).
   const int4* blk;
   const float2* rope;       // (cos, sin) [max_ctx][d / 2]
   uint32_t* bars;
   uint32_t* ctl;
   const Instr* queue;
   uint32_t n_instr;
-  const uint32_t* expr;
+  // the plan's expressions [PXS_COUNT][X_MAX_WORDS], in the launch's parameter
+  // block (read through the constant cache on the producer's path)
+  uint32_t xw[PXS_COUNT * X_MAX_WORDS];
   const int32_t* tokens;
   int S;
   int mode;
   uint32_t perop_base;
   unsigned long long wait_limit_ns;
 };
+static_assert(sizeof(PfParams) <= 4096, "kernel parameter block limit");
 
 int build_prefill(const mk_model_cfg& cfg, int max_ctx, PrefillPlan* out, std::string* why);
 int simulate_prefill(const PrefillPlan& pp, const std::vector<Instr>& q, std::string* why);

@@ -115,7 +115,7 @@ __device__ __forceinline__ const CUtensorMap* tmap(const PfParams& P, int idx) {
 __device__ __forceinline__ int am(const PfParams& P, int which) { return P.L * TM_PER_LAYER + which; }
 
 __device__ __forceinline__ bool pf_live(const PfParams& P, const Instr& in) {
-  return x_eval(P.expr + PXS_BLOCK_LIVE * X_MAX_WORDS, in, 1, P.S, nullptr, 0) > 0;
+  return x_eval(P.xw + PXS_BLOCK_LIVE * X_MAX_WORDS, in, 1, P.S, nullptr, 0) > 0;
 }
 
 // Bounded acquire-spin on every barrier an instruction waits on.  Returns
