@@ -106,6 +106,26 @@ def test_plan_check_random_topological_orders(lib, seed):
     assert rc == mk.MK_OK
 
 
+@pytest.mark.parametrize("cfg,mb,mc", [
+    (synth.LLAMA3_8B.replace(n_layers=2), 8, 4097),
+    (synth.QWEN3_8B.replace(n_layers=2), 32, 2049),
+    (synth.ModelCfg(n_layers=2, hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, ffn=3072,
+                    vocab=1000, rms_eps=1e-5, rope_theta=1e4), 12, 300),
+    (synth.ModelCfg(n_layers=2, hidden=512, n_q_heads=8, n_kv_heads=8, head_dim=64, ffn=768,
+                    vocab=1000, rms_eps=1e-5, rope_theta=1e4), 20, 200),
+])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_batched_plan_check_random_orders(lib, cfg, mb, mc, seed):
+    """The tensor-core batched-decode queue and random topological orders of
+    it pass the host simulator: every wait (including the O chunks' waits on
+    their kv groups and the down chunks' waits on their gate/up row tiles) is
+    met when reached, and every barrier ends with exactly the releases its
+    waiters expect."""
+    rc, st = mk.plan_check(cfg, mb, mc, seed=seed)
+    assert rc == mk.MK_OK
+    assert st.decode_path == 1
+
+
 @pytest.mark.parametrize("bad,code", [
     (dict(head_dim=96), mk.MK_ERR_UNSUPPORTED),
     (dict(n_q_heads=5), mk.MK_ERR_INVALID_ARG),

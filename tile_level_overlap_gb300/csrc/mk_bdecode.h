@@ -118,7 +118,7 @@ struct BdParams {
 };
 
 // Shapes the tensor-core batched path takes (MK_OK) or why not.
-// n_sms: SMs of the device (sets the attention split count); 0 = DEFAULT_SMS.
+// n_sms: SMs of the device (not used: the attention split count is fixed).
 int build_bdecode(const mk_model_cfg& cfg, int max_batch, int max_ctx, int n_sms, BdPlan* out,
                   std::string* why);
 int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string* why);

@@ -110,13 +110,18 @@ __device__ __forceinline__ bool bd_wait(const BdParams& P, uint64_t* bar, uint32
   }
 }
 
-// Bounded acquire-spin on the counter an instruction waits on.
+// Bounded acquire-spin on the counters an instruction waits on: wait_n
+// counters, wait_stride apart, each to wait_target releases per step.
 __device__ bool bd_wait_deps(const BdParams& P, const Instr& in, uint32_t gen, uint32_t idx) {
   if (P.mode != MODE_MEGA || in.wait_bar == NO_BAR) return true;
   const uint32_t target = (gen + 1u) * in.wait_target;
-  const uint32_t* c = &P.bars[in.wait_bar];
   const uint64_t t0 = globaltimer();
-  while ((int32_t)(ld_acquire_gpu(c) - target) < 0) {
+  for (uint32_t k = 0; k < in.wait_n;) {
+    const uint32_t* c = &P.bars[in.wait_bar + k * in.wait_stride];
+    if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) {
+      ++k;
+      continue;
+    }
     if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u) return false;
     if (globaltimer() - t0 > P.wait_limit_ns) {
       bd_error(P, MK_ERR_TIMEOUT, idx);
@@ -267,7 +272,7 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
   };
   // last counter (and target) seen satisfied: counters only grow within a
   // launch, so repeated waits on it need no new load
-  uint32_t ok_bar = NO_BAR, ok_target = 0;
+  uint32_t ok_bar = NO_BAR, ok_target = 0, ok_n = 0;
   for (;;) {
     const bool room = bd_wait(P, &S.empty[stage_ctr % BD_NSTAGE], ((stage_ctr / BD_NSTAGE) & 1u) ^ 1u);
     const uint32_t i = room ? pop() : BD_END;
@@ -316,10 +321,11 @@ __device__ void bd_producer(const BdParams& P, const BdSh& S) {
       // (after a timeout the loads still run, on stale but valid memory, so
       // that every armed stage completes and the launch can drain)
       const uint32_t target = (gen + 1u) * in.wait_target;
-      if (!(in.wait_bar == ok_bar && target == ok_target)) {
+      if (!(in.wait_bar == ok_bar && target == ok_target && in.wait_n == ok_n)) {
         if (bd_wait_deps(P, in, gen, i)) {
           ok_bar = in.wait_bar;
           ok_target = target;
+          ok_n = in.wait_n;
         }
         fence_proxy_async_global();
       }

@@ -1,7 +1,15 @@
 // Host plan of the tensor-core batched decode queue (see mk_bdecode.h).
 // Every GEMM row tile is released once, by the last of its K chunks to
 // arrive; every (sequence, kv head) attention group once, by the last of its
-// splits.  Waiters count those releases.
+// splits.  Waiters count those releases.  Where a consumer's K chunk reads
+// only some producer tiles, it waits on just those (barriers partitioned
+// along the dependency dimension, "Lecture 112: Production Megakernels for
+// Real-World Inference", Key takeaways): a down-projection chunk of 1024
+// SwiGLU columns on the 16 gate/up row tiles that write them, an
+// O-projection chunk of 1024 attention-output columns on the kv groups whose
+// heads those are.  The RMSNorm-folded projections (QKV, gate/up) scale their
+// outputs by 1 / rms of the whole input row, so they wait on every producer
+// row tile.
 #include <algorithm>
 #include <cstring>
 #include <map>
@@ -28,10 +36,10 @@ Instr bd_make(uint8_t op, int layer, uint32_t a0, uint32_t a1, uint16_t a2 = 0) 
   return in;
 }
 
-void bd_wait(Instr& in, uint32_t bar, uint32_t target) {
+void bd_wait(Instr& in, uint32_t bar, uint32_t target, uint16_t n = 1) {
   in.wait_bar = bar;
   in.wait_target = target;
-  in.wait_n = 1;
+  in.wait_n = n;
   in.wait_stride = 1;
 }
 
@@ -91,14 +99,18 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   bp.c_f = chunks(c.ffn);
 
   const int L = c.n_layers, nkv = c.n_kv_heads;
+  // kv groups per 1024-column chunk of the attention output, gate/up row
+  // tiles (64 SwiGLU columns each) per 1024-column chunk of the FFN
+  const uint32_t g_per_c = qd <= BD_KC ? (uint32_t)nkv : (uint32_t)(BD_KC / (rep * c.head_dim));
+  const uint32_t gu_per_c = c.ffn <= BD_KC ? bp.n_gu_m : (uint32_t)(BD_KC / (BD_M / 2));
   BdBars& b = bp.bl;
   b.norm1 = 0;
   b.qkv = b.norm1 + L;
-  b.attn = b.qkv + L;
-  b.o = b.attn + L;
+  b.attn = b.qkv + L;                      // [L][n_kv]
+  b.o = b.attn + L * nkv;
   b.norm2 = b.o + L;
-  b.gu = b.norm2 + L;
-  b.down = b.gu + L;
+  b.gu = b.norm2 + L;                      // [L][c_f]
+  b.down = b.gu + L * bp.c_f;
   b.normf = b.down + L;
   b.lm = b.normf + 1;
   b.total = b.lm + 1;
@@ -108,18 +120,26 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   auto end = [&](uint32_t s) {
     if (q.size() > s) bp.perop.push_back({s, (uint32_t)q.size() - s});
   };
-  auto gemm = [&](uint8_t op, int l, uint32_t nm, uint32_t nc, uint32_t wbar, uint32_t wtarget,
-                  uint32_t rbar) {
+  // wait(ch): first barrier, count and per-barrier target of chunk ch;
+  // rel(m): the barrier row tile m releases
+  struct Wait {
+    uint32_t bar, target;
+    uint16_t n;
+  };
+  auto gemm = [&](uint8_t op, int l, uint32_t nm, uint32_t nc, auto&& wait, auto&& rel) {
     const uint32_t s = begin();
     for (uint32_t m = 0; m < nm; ++m)
       for (uint32_t ch = 0; ch < nc; ++ch) {
         Instr in = bd_make(op, l, m, ch);
-        bd_wait(in, wbar, wtarget);
-        in.rel_bar = rbar;
+        const Wait w = wait(ch);
+        bd_wait(in, w.bar, w.target, w.n);
+        in.rel_bar = rel(m);
         q.push_back(in);
       }
     end(s);
   };
+  auto all = [](uint32_t bar, uint32_t target) { return [=](uint32_t) { return Wait{bar, target, 1}; }; };
+  auto one = [](uint32_t bar) { return [=](uint32_t) { return bar; }; };
   auto norm = [&](uint8_t op, int l, uint32_t wbar, uint32_t wtarget, uint32_t rbar) {
     const uint32_t s = begin();
     for (int r = 0; r < bp.n_rg; ++r) {
@@ -134,25 +154,39 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   // later norm is folded into the O / down epilogues (see mk_bdecode.h)
   norm(BD_NORM1, 0, NO_BAR, 0, b.norm1);
   for (int l = 0; l < L; ++l) {
-    if (l == 0) gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, b.norm1, (uint32_t)bp.n_rg, b.qkv + l);
-    else gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, b.down + l - 1, bp.n_down_m, b.qkv + l);
+    if (l == 0) gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, all(b.norm1, (uint32_t)bp.n_rg), one(b.qkv + l));
+    else gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, all(b.down + l - 1, bp.n_down_m), one(b.qkv + l));
     {
+      // kv group by kv group (every sequence of a group, then the next
+      // group): the first groups finish first, and the O chunks that read
+      // only their heads start while the later groups are still running
       const uint32_t s = begin();
-      for (int bb = 0; bb < max_batch; ++bb)
-        for (int g = 0; g < nkv; ++g)
+      for (int g = 0; g < nkv; ++g)
+        for (int bb = 0; bb < max_batch; ++bb)
           for (int sp = 0; sp < bp.nsplit; ++sp) {
             Instr in = bd_make(BD_ATTN, l, (uint32_t)bb, (uint32_t)g, (uint16_t)sp);
             bd_wait(in, b.qkv + l, bp.n_qkv_m);
-            in.rel_bar = b.attn + l;
+            in.rel_bar = b.attn + l * nkv + g;
             q.push_back(in);
           }
       end(s);
     }
-    gemm(BD_O, l, bp.n_o_m, bp.c_q, b.attn + l, (uint32_t)(max_batch * nkv), b.o + l);
-    gemm(BD_GU, l, bp.n_gu_m, bp.c_h, b.o + l, bp.n_o_m, b.gu + l);
-    gemm(BD_DOWN, l, bp.n_down_m, bp.c_f, b.gu + l, bp.n_gu_m, b.down + l);
+    // O chunk ch: the kv groups of its 1024 attention-output columns, every
+    // sequence of each
+    gemm(BD_O, l, bp.n_o_m, bp.c_q,
+         [&](uint32_t ch) {
+           return Wait{b.attn + l * nkv + ch * g_per_c, (uint32_t)max_batch, (uint16_t)g_per_c};
+         },
+         one(b.o + l));
+    // gate/up row tile m writes SwiGLU columns [64 m, 64 m + 64)
+    gemm(BD_GU, l, bp.n_gu_m, bp.c_h, all(b.o + l, bp.n_o_m),
+         [&](uint32_t m) { return b.gu + l * bp.c_f + m / gu_per_c; });
+    // down chunk ch: the gate/up row tiles of its 1024 SwiGLU columns
+    gemm(BD_DOWN, l, bp.n_down_m, bp.c_f,
+         [&](uint32_t ch) { return Wait{b.gu + l * bp.c_f + ch, gu_per_c, 1}; },
+         one(b.down + l));
   }
-  gemm(BD_LM, L - 1, bp.n_lm_m, 1, b.down + L - 1, bp.n_down_m, b.lm);
+  gemm(BD_LM, L - 1, bp.n_lm_m, 1, all(b.down + L - 1, bp.n_down_m), one(b.lm));
   return MK_OK;
 }
 
@@ -178,9 +212,14 @@ int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string*
       if (why) *why = "unknown batched-decode opcode at " + std::to_string(i);
       return MK_ERR_INVALID_ARG;
     }
-    if (in.wait_bar != NO_BAR && (in.wait_bar >= bp.bl.total || cnt[in.wait_bar] < in.wait_target)) {
-      if (why) *why = "batched-decode instruction " + std::to_string(i) + " waits before its producers";
-      return MK_ERR_INVALID_ARG;
+    if (in.wait_bar != NO_BAR) {
+      for (uint32_t k = 0; k < in.wait_n; ++k) {
+        const uint32_t wb = in.wait_bar + k * in.wait_stride;
+        if (wb >= bp.bl.total || cnt[wb] < in.wait_target) {
+          if (why) *why = "batched-decode instruction " + std::to_string(i) + " waits before its producers";
+          return MK_ERR_INVALID_ARG;
+        }
+      }
     }
     if (in.rel_bar == NO_BAR) continue;
     const uint32_t gs = group_size(in);
@@ -194,10 +233,12 @@ int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string*
   }
   for (size_t i = 0; i < q.size(); ++i) {
     const Instr& in = q[i];
-    if (in.wait_bar != NO_BAR && cnt[in.wait_bar] != in.wait_target) {
-      if (why) *why = "batched-decode barrier count mismatch at instruction " + std::to_string(i);
-      return MK_ERR_INVALID_ARG;
-    }
+    if (in.wait_bar == NO_BAR) continue;
+    for (uint32_t k = 0; k < in.wait_n; ++k)
+      if (cnt[in.wait_bar + k * in.wait_stride] != in.wait_target) {
+        if (why) *why = "batched-decode barrier count mismatch at instruction " + std::to_string(i);
+        return MK_ERR_INVALID_ARG;
+      }
   }
   return MK_OK;
 }
@@ -209,10 +250,14 @@ void random_order_bdecode(const BdPlan& bp, uint64_t seed, std::vector<Instr>* o
   out->clear();
   std::vector<uint32_t> cnt(bp.bl.total, 0);
   std::vector<std::vector<uint32_t>> waiters(bp.bl.total);
-  std::vector<uint32_t> ready;
+  std::vector<uint32_t> ready, pending(q.size(), 0);  // pending: barriers not yet at target
   for (uint32_t i = 0; i < q.size(); ++i) {
-    if (q[i].wait_bar == NO_BAR) ready.push_back(i);
-    else waiters[q[i].wait_bar].push_back(i);
+    if (q[i].wait_bar == NO_BAR) {
+      ready.push_back(i);
+      continue;
+    }
+    pending[i] = q[i].wait_n;
+    for (uint32_t k = 0; k < q[i].wait_n; ++k) waiters[q[i].wait_bar + k * q[i].wait_stride].push_back(i);
   }
   std::map<uint64_t, uint32_t> arrived;
   auto group_size = [&](const Instr& in) -> uint32_t {
@@ -244,7 +289,7 @@ void random_order_bdecode(const BdPlan& bp, uint64_t seed, std::vector<Instr>* o
     if (!fire) continue;
     const uint32_t c = ++cnt[in.rel_bar];
     for (uint32_t w : waiters[in.rel_bar])
-      if (q[w].wait_target == c) ready.push_back(w);
+      if (q[w].wait_target == c && --pending[w] == 0) ready.push_back(w);
   }
 }
 
