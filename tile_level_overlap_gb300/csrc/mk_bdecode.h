@@ -90,10 +90,21 @@ struct BdParams {
   float* q;                 // rotated (normed) queries [nb][n_q d]
   float* ss1;               // sums of x^2 per (row tile, sequence) for the next QKV / LM [tiles][BD_NMAX]
   float* ss2;               // the same for the gate/up projection [tiles][BD_NMAX]
-  float* part;              // split-K partial sums [row tile][chunk][BD_NMAX][128] of one operator
+  // split-K partial sums [slot = row tile x chunks + chunk][BD_NMAX][128] in
+  // two regions that operators alternate between: O and down in the first,
+  // QKV and gate/up in the second from slot part_b.  A chunk may start while
+  // the previous operator's row tiles are still summing their chunks (its
+  // wait covers only the tiles it reads), never while the one before that
+  // is, so neighbours must not share a region.
+  float* part;
+  uint32_t part_b;
   float* apart;             // attention split partials [max_batch][n_kv][nsplit][rep][d + 2]
-  uint32_t* arrive;         // arrival counters: [row tiles of one operator] then [max_batch * n_kv]
-  uint32_t n_arrive_gemm;   // row-tile counters (the attention ones follow)
+  // arrival counters: row tiles of the first region's operator, of the
+  // second's from arrive_b, then [max_batch * n_kv] attention groups from
+  // n_arrive_gemm
+  uint32_t* arrive;
+  uint32_t arrive_b;
+  uint32_t n_arrive_gemm;
   uint16_t* kv;             // caller's KV cache
   const float2* rope;       // (cos, sin) [max_ctx][d / 2]
   uint32_t* bars;

@@ -158,7 +158,8 @@ struct BdGemm {
   int a_map, a_row;         // weight map and first row (GU: gate map; up map = a_map + 1)
   bool gu;                  // two 64-row weight boxes (gate, up)
   int x_map;                // activation map (hi rows [0, nb), lo rows [nb, 2 nb))
-  uint32_t tile;            // row tile within the operator (split-K partials, arrival counter)
+  uint32_t pslot;           // first split-K partial slot of the row tile
+  uint32_t arr;             // its arrival counter
 };
 
 __device__ __forceinline__ BdGemm bd_gemm(const BdParams& P, const Instr& in) {
@@ -208,9 +209,13 @@ __device__ __forceinline__ BdGemm bd_gemm(const BdParams& P, const Instr& in) {
       break;
   }
   // Partial sums and arrival counters are indexed by the row tile within the
-  // operator: an operator starts only after every tile of the previous one has
-  // released, so the buffers are reused operator after operator.
-  g.tile = (uint32_t)m;
+  // operator, in one of two regions: O and down in the first, QKV and gate/up
+  // in the second.  A chunk can start while row tiles of the operator before
+  // it still sum their chunks (it waits only on the tiles it reads), but not
+  // while the operator before that one does, so alternating regions suffice.
+  const bool rb = in.op == BD_QKV || in.op == BD_GU;
+  g.pslot = (rb ? P.part_b : 0u) + (uint32_t)(m * g.chunks);
+  g.arr = (rb ? P.arrive_b : 0u) + (uint32_t)m;
   const int kc = g.chunks == 1 ? g.K : (g.K < BD_KC ? g.K : BD_KC);
   g.k0 = c * kc;
   g.nk = kc / BD_BK;
@@ -896,12 +901,12 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
       if (gm.chunks > 1) {
         // split-K: publish this chunk's partial; the last chunk to arrive adds
         // all chunks in chunk order and runs the epilogue
-        float* mine = P.part + ((size_t)gm.tile * gm.chunks + in.a1) * BD_NMAX * BD_M;
+        float* mine = P.part + ((size_t)gm.pslot + in.a1) * BD_NMAX * BD_M;
 #pragma unroll
         for (int k = 0; k < 16; ++k) mine[(b0 + k) * BD_M + row] = y[k];
         cbar_bd();
         if (tc == 0) {
-          uint32_t* arr = P.arrive + gm.tile;
+          uint32_t* arr = P.arrive + gm.arr;
           const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
           const bool last = old == (uint32_t)(gm.chunks - 1);
           if (last) *arr = 0u;
@@ -910,7 +915,7 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
         cbar_bd();
         release = S.flags[BF_LAST] != 0u;
         if (release) {
-          const float* base = P.part + (size_t)gm.tile * gm.chunks * BD_NMAX * BD_M;
+          const float* base = P.part + (size_t)gm.pslot * BD_NMAX * BD_M;
 #pragma unroll
           for (int k = 0; k < 16; ++k) y[k] = 0.f;
           for (int c = 0; c < gm.chunks; ++c)

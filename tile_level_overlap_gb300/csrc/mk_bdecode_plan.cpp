@@ -7,9 +7,12 @@
 // Real-World Inference", Key takeaways): a down-projection chunk of 1024
 // SwiGLU columns on the 16 gate/up row tiles that write them, an
 // O-projection chunk of 1024 attention-output columns on the kv groups whose
-// heads those are.  The RMSNorm-folded projections (QKV, gate/up) scale their
-// outputs by 1 / rms of the whole input row, so they wait on every producer
-// row tile.
+// heads those are, a QKV or gate/up chunk of 1024 hidden features on the 8
+// down or O row tiles that write them.  The RMSNorm-folded projections scale
+// their outputs by 1 / rms of the whole row, which needs every producer row
+// tile: their epilogue runs in the last chunk of the row tile to arrive, when
+// all chunks have passed their waits, so together they have covered every
+// producer tile.
 #include <algorithm>
 #include <cstring>
 #include <map>
@@ -103,15 +106,17 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   // tiles (64 SwiGLU columns each) per 1024-column chunk of the FFN
   const uint32_t g_per_c = qd <= BD_KC ? (uint32_t)nkv : (uint32_t)(BD_KC / (rep * c.head_dim));
   const uint32_t gu_per_c = c.ffn <= BD_KC ? bp.n_gu_m : (uint32_t)(BD_KC / (BD_M / 2));
+  // O / down row tiles (128 hidden features each) per 1024-feature chunk
+  const uint32_t h_per_c = c.hidden <= BD_KC ? bp.n_down_m : (uint32_t)(BD_KC / BD_M);
   BdBars& b = bp.bl;
   b.norm1 = 0;
   b.qkv = b.norm1 + L;
   b.attn = b.qkv + L;                      // [L][n_kv]
-  b.o = b.attn + L * nkv;
-  b.norm2 = b.o + L;
+  b.o = b.attn + L * nkv;                  // [L][c_h]
+  b.norm2 = b.o + L * bp.c_h;
   b.gu = b.norm2 + L;                      // [L][c_f]
-  b.down = b.gu + L * bp.c_f;
-  b.normf = b.down + L;
+  b.down = b.gu + L * bp.c_f;              // [L][c_h]
+  b.normf = b.down + L * bp.c_h;
   b.lm = b.normf + 1;
   b.total = b.lm + 1;
 
@@ -155,7 +160,10 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   norm(BD_NORM1, 0, NO_BAR, 0, b.norm1);
   for (int l = 0; l < L; ++l) {
     if (l == 0) gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, all(b.norm1, (uint32_t)bp.n_rg), one(b.qkv + l));
-    else gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, all(b.down + l - 1, bp.n_down_m), one(b.qkv + l));
+    else
+      gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h,
+           [&](uint32_t ch) { return Wait{b.down + (l - 1) * bp.c_h + ch, h_per_c, 1}; },
+           one(b.qkv + l));
     {
       // kv group by kv group (every sequence of a group, then the next
       // group): the first groups finish first, and the O chunks that read
@@ -177,16 +185,21 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
          [&](uint32_t ch) {
            return Wait{b.attn + l * nkv + ch * g_per_c, (uint32_t)max_batch, (uint16_t)g_per_c};
          },
-         one(b.o + l));
-    // gate/up row tile m writes SwiGLU columns [64 m, 64 m + 64)
-    gemm(BD_GU, l, bp.n_gu_m, bp.c_h, all(b.o + l, bp.n_o_m),
+         [&](uint32_t m) { return b.o + l * bp.c_h + m / h_per_c; });
+    // gate/up chunk ch: the O row tiles of its 1024 hidden features; row
+    // tile m writes SwiGLU columns [64 m, 64 m + 64)
+    gemm(BD_GU, l, bp.n_gu_m, bp.c_h,
+         [&](uint32_t ch) { return Wait{b.o + l * bp.c_h + ch, h_per_c, 1}; },
          [&](uint32_t m) { return b.gu + l * bp.c_f + m / gu_per_c; });
     // down chunk ch: the gate/up row tiles of its 1024 SwiGLU columns
     gemm(BD_DOWN, l, bp.n_down_m, bp.c_f,
          [&](uint32_t ch) { return Wait{b.gu + l * bp.c_f + ch, gu_per_c, 1}; },
-         one(b.down + l));
+         [&](uint32_t m) { return b.down + l * bp.c_h + m / h_per_c; });
   }
-  gemm(BD_LM, L - 1, bp.n_lm_m, 1, all(b.down + L - 1, bp.n_down_m), one(b.lm));
+  // the LM head is not split over K: every down row tile of the last layer
+  gemm(BD_LM, L - 1, bp.n_lm_m, 1,
+       [&](uint32_t) { return Wait{b.down + (L - 1) * bp.c_h, h_per_c, (uint16_t)bp.c_h}; },
+       one(b.lm));
   return MK_OK;
 }
 

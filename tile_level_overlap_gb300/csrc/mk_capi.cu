@@ -137,10 +137,11 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   const mk_model_cfg& c = bp.cfg;
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
   const int qd = c.n_q_heads * d, kd = nkv * d, NB = bp.nb;
-  // split-K partials of the operator with the most (row tile, chunk) pairs
-  const size_t pairs = std::max({(size_t)bp.n_qkv_m * bp.c_h, (size_t)bp.n_o_m * bp.c_q,
-                                 (size_t)bp.n_gu_m * bp.c_h, (size_t)bp.n_down_m * bp.c_f});
-  const uint32_t max_m = std::max({bp.n_qkv_m, bp.n_o_m, bp.n_gu_m, bp.n_down_m, bp.n_lm_m});
+  // split-K partials and arrival counters in two regions: O and down in the
+  // first, QKV and gate/up in the second (neighbouring operators overlap)
+  const size_t pairs_a = std::max((size_t)bp.n_o_m * bp.c_q, (size_t)bp.n_down_m * bp.c_f);
+  const size_t pairs_b = std::max((size_t)bp.n_qkv_m * bp.c_h, (size_t)bp.n_gu_m * bp.c_h);
+  const uint32_t m_a = std::max(bp.n_o_m, bp.n_down_m), m_b = std::max(bp.n_qkv_m, bp.n_gu_m);
   const int n_maps = L * BD_TM_PER_LAYER + TMB_COUNT;
   Bump bm;
   const size_t o_bars = bm.take(sizeof(uint32_t) * bp.bl.total);
@@ -156,9 +157,9 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   const size_t o_qv = bm.take(sizeof(float) * NB * qd);
   const size_t o_ss1 = bm.take(sizeof(float) * std::max<uint32_t>(bp.n_down_m, 1) * BD_NMAX);
   const size_t o_ss2 = bm.take(sizeof(float) * bp.n_o_m * BD_NMAX);
-  const size_t o_part = bm.take(sizeof(float) * pairs * BD_NMAX * BD_M);
+  const size_t o_part = bm.take(sizeof(float) * (pairs_a + pairs_b) * BD_NMAX * BD_M);
   const size_t o_apart = bm.take(sizeof(float) * bp.max_batch * nkv * bp.nsplit * bp.rep * (d + 2));
-  s.arrive_words = (size_t)max_m + (size_t)bp.max_batch * nkv;
+  s.arrive_words = (size_t)m_a + m_b + (size_t)bp.max_batch * nkv;
   const size_t o_arr = bm.take(sizeof(uint32_t) * s.arrive_words);
   if (cudaMalloc(&s.mem, bm.off) != cudaSuccess) {
     cudaGetLastError();
@@ -212,7 +213,9 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   k.part = (float*)(b + o_part);
   k.apart = (float*)(b + o_apart);
   k.arrive = (uint32_t*)(b + o_arr);
-  k.n_arrive_gemm = max_m;
+  k.part_b = (uint32_t)pairs_a;
+  k.arrive_b = m_a;
+  k.n_arrive_gemm = m_a + m_b;
   k.rope = p->base.rope;
   k.bars = (uint32_t*)(b + o_bars);
   k.ctl = (uint32_t*)(b + o_ctl);
