@@ -192,28 +192,26 @@ def test_qwen3_8b_width_batch32_ragged():
         m.close()
 
 
-def test_prompt_chunk_mixed_with_decode(small):
-    """mk_decode_step_slots: a 6-token prompt chunk of slot 0 (positions
-    p0..p0+5) and decode tokens of slots 1..5 in one persistent launch.  The
-    oracle runs the chunk token by token (each step appending its key/value)
-    and the decode columns as one step on the cache before the launch."""
-    cfg = small.cfg
-    p0, chunk = 150, 6
-    dec_slots = [1, 2, 3, 4, 5]
-    dec_pos = [10, 299, 0, 77, 128]
-    toks = synth.make_tokens(chunk + len(dec_slots), cfg.vocab, seed=91).numpy()
+def _chunk_with_decode(m, p0, chunk, dec_slots, dec_pos, seed):
+    """mk_decode_step_slots: a prompt chunk of slot 0 (positions p0 ..
+    p0 + chunk - 1) and decode tokens of other slots in one persistent launch.
+    The oracle runs the chunk token by token (each step appending its
+    key/value) and the decode columns as one step on the cache before the
+    launch."""
+    cfg = m.cfg
+    toks = synth.make_tokens(chunk + len(dec_slots), cfg.vocab, seed=seed).numpy()
     slots = np.array([0] * chunk + dec_slots, dtype=np.int32)
     pos = np.array([p0 + i for i in range(chunk)] + dec_pos, dtype=np.int32)
-    kv_before = synth.bf16_bits(small.kv)
+    kv_before = synth.bf16_bits(m.kv)
     n = len(toks)
-    lg = torch.full((n, cfg.vocab), float("nan"), device=small.dev)
-    small.plan.decode_step_slots(torch.from_numpy(toks.astype(np.int32)).to(small.dev),
-                                 torch.from_numpy(pos).to(small.dev),
-                                 torch.from_numpy(slots).to(small.dev), small.kv, lg)
-    rc = small.plan.status()
+    lg = torch.full((n, cfg.vocab), float("nan"), device=m.dev)
+    m.plan.decode_step_slots(torch.from_numpy(toks.astype(np.int32)).to(m.dev),
+                             torch.from_numpy(pos).to(m.dev),
+                             torch.from_numpy(slots).to(m.dev), m.kv, lg)
+    rc = m.plan.status()
     assert rc == mk.MK_OK, mk.lib().mk_status_string(rc)
     got = lg.cpu().numpy()
-    w = synth.LazyBits(small.w)
+    w = synth.LazyBits(m.w)
     # the chunk, token by token, on slot 0's cache
     kv0 = kv_before[:, :, 0:1].copy()
     for i in range(chunk):
@@ -223,18 +221,39 @@ def test_prompt_chunk_mixed_with_decode(small):
         vb = torch.from_numpy(np.ascontiguousarray(vnew[:, 0])).to(torch.bfloat16).view(torch.int16).numpy()
         kv0[:, 0, 0, :, p0 + i, :] = kb.view(kv0.dtype)
         kv0[:, 1, 0, :, p0 + i, :] = vb.view(kv0.dtype)
-    after = oracle.widen_bf16(synth.bf16_bits(small.kv))
+    after = oracle.widen_bf16(synth.bf16_bits(m.kv))
     np.testing.assert_allclose(after[:, :, 0, :, p0:p0 + chunk], oracle.widen_bf16(kv0)[:, :, 0, :, p0:p0 + chunk],
                                rtol=2.0 ** -6, atol=2e-2)
-    # the decode columns: one step of slots 1..5 (sequence b in slot b)
-    kvd = kv_before[:, :, 1:6].copy()
+    # the decode columns: one step of their slots (sequence b in slot b)
+    lo, hi = dec_slots[0], dec_slots[-1] + 1
+    assert dec_slots == list(range(lo, hi))
+    kvd = kv_before[:, :, lo:hi].copy()
     ref, _, _ = oracle.decode_step(cfg, w, toks[chunk:], dec_pos, kvd)
     _rows_close(got[chunk:], ref)
+
+
+def test_prompt_chunk_mixed_with_decode(small):
+    """A 6-token prompt chunk of slot 0 with decode tokens of slots 1..5."""
+    _chunk_with_decode(small, 150, 6, [1, 2, 3, 4, 5], [10, 299, 0, 77, 128], seed=91)
     # a slot outside the plan latches a bounds error
     small.plan.reset()
     bad = torch.tensor([0, 12], dtype=torch.int32, device=small.dev)
+    lg = torch.empty((2, small.cfg.vocab), device=small.dev)
     small.plan.decode_step_slots(torch.tensor([1, 2], dtype=torch.int32, device=small.dev),
                                  torch.tensor([5, 6], dtype=torch.int32, device=small.dev), bad,
-                                 small.kv, lg[:2])
+                                 small.kv, lg)
     assert small.plan.status() == mk.MK_ERR_BOUNDS
     small.plan.reset()
+
+
+def test_prompt_chunk_crossing_a_key_block():
+    """A chunk at positions 510..515: for its last token (516 keys, the last
+    split from key 387) the chunk's first rows lie in the split's first
+    128-key block and its own row in the next, so the block holding rows this
+    step writes is not the block holding the column's own row; both must be
+    streamed only after the projection wrote them."""
+    m = BModel(BD_SMALL, max_batch=12, max_ctx=600, seed=7)
+    try:
+        _chunk_with_decode(m, 510, 6, [1, 2, 3], [599, 3, 300], seed=92)
+    finally:
+        m.close()

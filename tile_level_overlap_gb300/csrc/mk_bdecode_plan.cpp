@@ -108,10 +108,35 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   const uint32_t gu_per_c = c.ffn <= BD_KC ? bp.n_gu_m : (uint32_t)(BD_KC / (BD_M / 2));
   // O / down row tiles (128 hidden features each) per 1024-feature chunk
   const uint32_t h_per_c = c.hidden <= BD_KC ? bp.n_down_m : (uint32_t)(BD_KC / BD_M);
+  // QKV row tiles per kv group: at head_dim 128 every 128-row tile holds one
+  // head (q, k or v) of one group, and an attention group waits on just its
+  // rep + 2 tiles; at head_dim 64 a k or v tile spans two groups, and every
+  // group waits on the whole projection
+  const bool qkv_by_group = c.head_dim == BD_M;
+  const uint32_t ng = qkv_by_group ? (uint32_t)nkv : 1u;
+  const uint32_t qkv_per_g = qkv_by_group ? (uint32_t)rep + 2u : bp.n_qkv_m;
+  const uint32_t mq = (uint32_t)(qd / BD_M), mk = (uint32_t)(kd / BD_M);
+  auto qkv_group = [&](uint32_t m) -> uint32_t {
+    if (!qkv_by_group) return 0;
+    if (m < mq) return m / (uint32_t)rep;
+    return m < mq + mk ? m - mq : m - mq - mk;
+  };
+  // emission order of the QKV row tiles: group by group (its q heads, its k,
+  // its v), so the first groups' attention can start first
+  std::vector<uint32_t> qkv_order;
+  if (qkv_by_group) {
+    for (uint32_t g = 0; g < (uint32_t)nkv; ++g) {
+      for (uint32_t r = 0; r < (uint32_t)rep; ++r) qkv_order.push_back(g * rep + r);
+      qkv_order.push_back(mq + g);
+      qkv_order.push_back(mq + mk + g);
+    }
+  } else {
+    for (uint32_t m = 0; m < bp.n_qkv_m; ++m) qkv_order.push_back(m);
+  }
   BdBars& b = bp.bl;
   b.norm1 = 0;
-  b.qkv = b.norm1 + L;
-  b.attn = b.qkv + L;                      // [L][n_kv]
+  b.qkv = b.norm1 + L;                     // [L][ng]
+  b.attn = b.qkv + L * ng;                 // [L][n_kv]
   b.o = b.attn + L * nkv;                  // [L][c_h]
   b.norm2 = b.o + L * bp.c_h;
   b.gu = b.norm2 + L;                      // [L][c_f]
@@ -131,9 +156,10 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
     uint32_t bar, target;
     uint16_t n;
   };
-  auto gemm = [&](uint8_t op, int l, uint32_t nm, uint32_t nc, auto&& wait, auto&& rel) {
+  auto gemm_rows = [&](uint8_t op, int l, const std::vector<uint32_t>& rows, uint32_t nc, auto&& wait,
+                       auto&& rel) {
     const uint32_t s = begin();
-    for (uint32_t m = 0; m < nm; ++m)
+    for (uint32_t m : rows)
       for (uint32_t ch = 0; ch < nc; ++ch) {
         Instr in = bd_make(op, l, m, ch);
         const Wait w = wait(ch);
@@ -142,6 +168,11 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
         q.push_back(in);
       }
     end(s);
+  };
+  auto gemm = [&](uint8_t op, int l, uint32_t nm, uint32_t nc, auto&& wait, auto&& rel) {
+    std::vector<uint32_t> rows(nm);
+    for (uint32_t m = 0; m < nm; ++m) rows[m] = m;
+    gemm_rows(op, l, rows, nc, wait, rel);
   };
   auto all = [](uint32_t bar, uint32_t target) { return [=](uint32_t) { return Wait{bar, target, 1}; }; };
   auto one = [](uint32_t bar) { return [=](uint32_t) { return bar; }; };
@@ -159,11 +190,12 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   // later norm is folded into the O / down epilogues (see mk_bdecode.h)
   norm(BD_NORM1, 0, NO_BAR, 0, b.norm1);
   for (int l = 0; l < L; ++l) {
-    if (l == 0) gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h, all(b.norm1, (uint32_t)bp.n_rg), one(b.qkv + l));
+    auto qkv_rel = [&](uint32_t m) { return b.qkv + l * ng + qkv_group(m); };
+    if (l == 0)
+      gemm_rows(BD_QKV, l, qkv_order, bp.c_h, all(b.norm1, (uint32_t)bp.n_rg), qkv_rel);
     else
-      gemm(BD_QKV, l, bp.n_qkv_m, bp.c_h,
-           [&](uint32_t ch) { return Wait{b.down + (l - 1) * bp.c_h + ch, h_per_c, 1}; },
-           one(b.qkv + l));
+      gemm_rows(BD_QKV, l, qkv_order, bp.c_h,
+                [&](uint32_t ch) { return Wait{b.down + (l - 1) * bp.c_h + ch, h_per_c, 1}; }, qkv_rel);
     {
       // kv group by kv group (every sequence of a group, then the next
       // group): the first groups finish first, and the O chunks that read
@@ -173,7 +205,7 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
         for (int bb = 0; bb < max_batch; ++bb)
           for (int sp = 0; sp < bp.nsplit; ++sp) {
             Instr in = bd_make(BD_ATTN, l, (uint32_t)bb, (uint32_t)g, (uint16_t)sp);
-            bd_wait(in, b.qkv + l, bp.n_qkv_m);
+            bd_wait(in, b.qkv + l * ng + (qkv_by_group ? (uint32_t)g : 0u), qkv_per_g);
             in.rel_bar = b.attn + l * nkv + g;
             q.push_back(in);
           }
