@@ -111,6 +111,8 @@ KERNEL_SOURCES = {
     "mk_interpreter": ("mk_kernel.cuh", "mk_device.cuh", "mk_internal.h", "mk_plan.h", "mk_plan.cpp",
                        "mk_variants.h", "mk_k_generic.cu", "mk_k_h1_f4_d64_r4.cu",
                        "mk_k_h2_f7_d128_r4.cu", "mk_k_h2_f6_d128_r4.cu"),
+    "mk_bdecode_kernel": ("mk_bdecode_kernel.cu", "mk_bdecode.h", "mk_bdecode_plan.cpp", "mk_device.cuh",
+                          "mk_internal.h", "mk_tc.cuh", "mk_plan.h"),
 }
 
 
@@ -543,7 +545,8 @@ def run_ours(args):
         plan.close()
         del w, kv
         torch.cuda.empty_cache()
-        batched = {name: batched_leg(name, dev, stream, timed, args) for name in BATCHED_LEGS}
+        batched = {name: batched_leg(name, dev, stream, timed, args)
+                   for name in BATCHED_LEGS if not args.batched_leg or name in args.batched_leg}
 
     if rank != 0:
         return 0
@@ -621,6 +624,10 @@ def batched_leg(name, dev, stream, timed, args):
     from tile_level_overlap_gb300 import mk, synth
 
     cfg, batch, pos_list, metric, desc, _ = workload(name)
+    if args.batched_layers:
+        # profiling case only: the same step on fewer layers
+        cfg = cfg.replace(n_layers=args.batched_layers)
+        desc = f"{desc}, first {args.batched_layers} layers (profiling case)"
     max_ctx = max(pos_list) + 1
     w = synth.make_weights(cfg, device=dev)
     kv = synth.make_kv_cache(cfg, batch, max_ctx, device=dev)
@@ -701,7 +708,8 @@ def batched_leg(name, dev, stream, timed, args):
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": achieved / peaks["hbm_gbs"], "peak_kind": kind,
                         "kernel": "mk_bdecode_kernel" if plan.stats().decode_path == 1 else "mk_interpreter",
-                        "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+                        "algorithmic_bytes_per_launch": nbytes,
+                        "traffic": None if args.batched_layers else recorded_traffic("mk_bdecode_kernel", name)},
            "per_op_graph_ms_per_step": ms_graph, "speedup_persistent_vs_graph": ms_graph / ms,
            "mixed_chunk": {"decode_columns": batch - half, "chunk_tokens": half, "ms_per_step": ms_mixed,
                            "tokens_per_s": batch / (ms_mixed / 1e3)},
@@ -726,6 +734,10 @@ def main():
     ap.add_argument("--no-batched", action="store_true",
                     help="skip the batch-8 and batch-32 tensor-core decode legs")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3-8b")
+    ap.add_argument("--batched-layers", type=int, default=0,
+                    help="run the batched legs on their first N layers (an ncu profiling case)")
+    ap.add_argument("--batched-leg", action="append", choices=BATCHED_LEGS,
+                    help="run only this batched leg (repeatable; default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
