@@ -63,6 +63,7 @@ struct BdPlan {
   int rep = 0, qkv_rows = 0, n_rg = 0;
   uint32_t n_qkv_m = 0, n_o_m = 0, n_gu_m = 0, n_down_m = 0, n_lm_m = 0;  // row tiles
   uint32_t c_h = 0, c_q = 0, c_f = 0;  // K chunks for K = H, n_q*d, F
+  uint32_t c_g = 0;  // K chunks of the gate/up projection (2048 columns each where H allows)
   BdBars bl{};
   std::vector<Instr> queue;                                // topological
   std::vector<std::pair<uint32_t, uint32_t>> perop;        // (first, count) per launch
@@ -77,7 +78,7 @@ enum BdGlobalMap { TMB_LM = 0, TMB_HN = 1, TMB_AO = 2, TMB_ACT = 3, TMB_KV = 4, 
 struct BdParams {
   int L, H, nq, nkv, d, F, V, qk_norm, rep, qkv_rows, max_ctx, max_batch, nb, n_rg, nsplit;
   float eps;
-  uint32_t n_qkv_m, n_o_m, n_gu_m, n_down_m, n_lm_m, c_h, c_q, c_f;
+  uint32_t n_qkv_m, n_o_m, n_gu_m, n_down_m, n_lm_m, c_h, c_q, c_f, c_g;
   const uint16_t* embed;
   const uint16_t* final_norm;
   const LayerW* layers;     // device array [L]

@@ -187,7 +187,7 @@ __device__ __forceinline__ BdGemm bd_gemm(const BdParams& P, const Instr& in) {
       break;
     case BD_GU:
       g.K = P.H;
-      g.chunks = (int)P.c_h;
+      g.chunks = (int)P.c_g;
       g.x_map = gmap(P, TMB_HN);
       g.a_map = l * BD_TM_PER_LAYER + TMB_WG;
       g.a_row = m * (BD_M / 2);
@@ -216,7 +216,7 @@ __device__ __forceinline__ BdGemm bd_gemm(const BdParams& P, const Instr& in) {
   const bool rb = in.op == BD_QKV || in.op == BD_GU;
   g.pslot = (rb ? P.part_b : 0u) + (uint32_t)(m * g.chunks);
   g.arr = (rb ? P.arrive_b : 0u) + (uint32_t)m;
-  const int kc = g.chunks == 1 ? g.K : (g.K < BD_KC ? g.K : BD_KC);
+  const int kc = g.K / g.chunks;  // 1024 columns (2048 for gate/up where H allows), or all of K
   g.k0 = c * kc;
   g.nk = kc / BD_BK;
   return g;

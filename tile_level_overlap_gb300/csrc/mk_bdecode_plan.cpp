@@ -100,6 +100,10 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   bp.c_h = chunks(c.hidden);
   bp.c_q = chunks(qd);
   bp.c_f = chunks(c.ffn);
+  // gate/up reads the whole hidden row for each of its 224 (Llama-3-8B) row
+  // tiles: 2048-column chunks halve its tile count (448 tiles, about three
+  // rounds over the SMs) and the per-tile overhead
+  bp.c_g = (c.hidden > BD_KC && c.hidden % (2 * BD_KC) == 0) ? (uint32_t)(c.hidden / (2 * BD_KC)) : bp.c_h;
 
   const int L = c.n_layers, nkv = c.n_kv_heads;
   // kv groups per 1024-column chunk of the attention output, gate/up row
@@ -220,8 +224,11 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
          [&](uint32_t m) { return b.o + l * bp.c_h + m / h_per_c; });
     // gate/up chunk ch: the O row tiles of its 1024 hidden features; row
     // tile m writes SwiGLU columns [64 m, 64 m + 64)
-    gemm(BD_GU, l, bp.n_gu_m, bp.c_h,
-         [&](uint32_t ch) { return Wait{b.o + l * bp.c_h + ch, h_per_c, 1}; },
+    gemm(BD_GU, l, bp.n_gu_m, bp.c_g,
+         [&](uint32_t ch) {
+           const uint32_t r = bp.c_h / bp.c_g;  // 1024-feature O chunks per gate/up chunk
+           return Wait{b.o + l * bp.c_h + ch * r, h_per_c, (uint16_t)r};
+         },
          [&](uint32_t m) { return b.gu + l * bp.c_f + m / gu_per_c; });
     // down chunk ch: the gate/up row tiles of its 1024 SwiGLU columns
     gemm(BD_DOWN, l, bp.n_down_m, bp.c_f,
@@ -244,7 +251,8 @@ int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string*
   std::map<uint64_t, uint32_t> arrived;
   auto group_size = [&](const Instr& in) -> uint32_t {
     switch (in.op) {
-      case BD_QKV: case BD_GU: return bp.c_h;
+      case BD_QKV: return bp.c_h;
+      case BD_GU: return bp.c_g;
       case BD_O: return bp.c_q;
       case BD_DOWN: return bp.c_f;
       case BD_ATTN: return (uint32_t)bp.nsplit;
@@ -307,7 +315,8 @@ void random_order_bdecode(const BdPlan& bp, uint64_t seed, std::vector<Instr>* o
   std::map<uint64_t, uint32_t> arrived;
   auto group_size = [&](const Instr& in) -> uint32_t {
     switch (in.op) {
-      case BD_QKV: case BD_GU: return bp.c_h;
+      case BD_QKV: return bp.c_h;
+      case BD_GU: return bp.c_g;
       case BD_O: return bp.c_q;
       case BD_DOWN: return bp.c_f;
       case BD_ATTN: return (uint32_t)bp.nsplit;
