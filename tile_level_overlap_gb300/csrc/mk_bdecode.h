@@ -64,6 +64,7 @@ struct BdPlan {
   uint32_t n_qkv_m = 0, n_o_m = 0, n_gu_m = 0, n_down_m = 0, n_lm_m = 0;  // row tiles
   uint32_t c_h = 0, c_q = 0, c_f = 0;  // K chunks for K = H, n_q*d, F
   uint32_t c_g = 0;  // K chunks of the gate/up projection (2048 columns each where H allows)
+  uint32_t c_k = 0;  // K chunks of the QKV projection (512 columns each where H allows)
   BdBars bl{};
   std::vector<Instr> queue;                                // topological
   std::vector<std::pair<uint32_t, uint32_t>> perop;        // (first, count) per launch
@@ -78,7 +79,7 @@ enum BdGlobalMap { TMB_LM = 0, TMB_HN = 1, TMB_AO = 2, TMB_ACT = 3, TMB_KV = 4, 
 struct BdParams {
   int L, H, nq, nkv, d, F, V, qk_norm, rep, qkv_rows, max_ctx, max_batch, nb, n_rg, nsplit;
   float eps;
-  uint32_t n_qkv_m, n_o_m, n_gu_m, n_down_m, n_lm_m, c_h, c_q, c_f, c_g;
+  uint32_t n_qkv_m, n_o_m, n_gu_m, n_down_m, n_lm_m, c_h, c_q, c_f, c_g, c_k;
   const uint16_t* embed;
   const uint16_t* final_norm;
   const LayerW* layers;     // device array [L]

@@ -104,6 +104,9 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   // tiles: 2048-column chunks halve its tile count (448 tiles, about three
   // rounds over the SMs) and the per-tile overhead
   bp.c_g = (c.hidden > BD_KC && c.hidden % (2 * BD_KC) == 0) ? (uint32_t)(c.hidden / (2 * BD_KC)) : bp.c_h;
+  // QKV's 48 (Llama-3-8B) row tiles: 512-column chunks give 384 tiles, about
+  // two and a half rounds, instead of 192 (one round and a quarter)
+  bp.c_k = c.hidden > BD_KC ? (uint32_t)(c.hidden / (BD_KC / 2)) : bp.c_h;
 
   const int L = c.n_layers, nkv = c.n_kv_heads;
   // kv groups per 1024-column chunk of the attention output, gate/up row
@@ -196,10 +199,14 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   for (int l = 0; l < L; ++l) {
     auto qkv_rel = [&](uint32_t m) { return b.qkv + l * ng + qkv_group(m); };
     if (l == 0)
-      gemm_rows(BD_QKV, l, qkv_order, bp.c_h, all(b.norm1, (uint32_t)bp.n_rg), qkv_rel);
+      gemm_rows(BD_QKV, l, qkv_order, bp.c_k, all(b.norm1, (uint32_t)bp.n_rg), qkv_rel);
     else
-      gemm_rows(BD_QKV, l, qkv_order, bp.c_h,
-                [&](uint32_t ch) { return Wait{b.down + (l - 1) * bp.c_h + ch, h_per_c, 1}; }, qkv_rel);
+      gemm_rows(BD_QKV, l, qkv_order, bp.c_k,
+                [&](uint32_t ch) {
+                  // the 1024-feature down chunk that holds this chunk's columns
+                  return Wait{b.down + (l - 1) * bp.c_h + ch * bp.c_h / bp.c_k, h_per_c, 1};
+                },
+                qkv_rel);
     {
       // kv group by kv group (every sequence of a group, then the next
       // group): the first groups finish first, and the O chunks that read
@@ -251,7 +258,7 @@ int simulate_bdecode(const BdPlan& bp, const std::vector<Instr>& q, std::string*
   std::map<uint64_t, uint32_t> arrived;
   auto group_size = [&](const Instr& in) -> uint32_t {
     switch (in.op) {
-      case BD_QKV: return bp.c_h;
+      case BD_QKV: return bp.c_k;
       case BD_GU: return bp.c_g;
       case BD_O: return bp.c_q;
       case BD_DOWN: return bp.c_f;
@@ -315,7 +322,7 @@ void random_order_bdecode(const BdPlan& bp, uint64_t seed, std::vector<Instr>* o
   std::map<uint64_t, uint32_t> arrived;
   auto group_size = [&](const Instr& in) -> uint32_t {
     switch (in.op) {
-      case BD_QKV: return bp.c_h;
+      case BD_QKV: return bp.c_k;
       case BD_GU: return bp.c_g;
       case BD_O: return bp.c_q;
       case BD_DOWN: return bp.c_f;

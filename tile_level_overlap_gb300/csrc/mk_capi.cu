@@ -140,7 +140,7 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   // split-K partials and arrival counters in two regions: O and down in the
   // first, QKV and gate/up in the second (neighbouring operators overlap)
   const size_t pairs_a = std::max((size_t)bp.n_o_m * bp.c_q, (size_t)bp.n_down_m * bp.c_f);
-  const size_t pairs_b = std::max((size_t)bp.n_qkv_m * bp.c_h, (size_t)bp.n_gu_m * bp.c_g);
+  const size_t pairs_b = std::max((size_t)bp.n_qkv_m * bp.c_k, (size_t)bp.n_gu_m * bp.c_g);
   const uint32_t m_a = std::max(bp.n_o_m, bp.n_down_m), m_b = std::max(bp.n_qkv_m, bp.n_gu_m);
   const int n_maps = L * BD_TM_PER_LAYER + TMB_COUNT;
   Bump bm;
@@ -197,7 +197,7 @@ int bd_init(mk_plan* p, const mk_weight_ptrs* w) {
   k.qk_norm = c.qk_norm; k.rep = bp.rep; k.qkv_rows = bp.qkv_rows; k.max_ctx = bp.max_ctx;
   k.max_batch = bp.max_batch; k.nb = NB; k.n_rg = bp.n_rg; k.nsplit = bp.nsplit; k.eps = c.rms_eps;
   k.n_qkv_m = bp.n_qkv_m; k.n_o_m = bp.n_o_m; k.n_gu_m = bp.n_gu_m; k.n_down_m = bp.n_down_m;
-  k.n_lm_m = bp.n_lm_m; k.c_h = bp.c_h; k.c_q = bp.c_q; k.c_f = bp.c_f; k.c_g = bp.c_g;
+  k.n_lm_m = bp.n_lm_m; k.c_h = bp.c_h; k.c_q = bp.c_q; k.c_f = bp.c_f; k.c_g = bp.c_g; k.c_k = bp.c_k;
   k.embed = (const uint16_t*)w->embed;
   k.final_norm = (const uint16_t*)w->final_norm;
   k.layers = p->base.layers;
