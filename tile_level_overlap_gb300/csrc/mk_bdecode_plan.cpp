@@ -181,6 +181,22 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
     for (uint32_t m = 0; m < nm; ++m) rows[m] = m;
     gemm_rows(op, l, rows, nc, wait, rel);
   };
+  // chunk by chunk (every row tile of chunk 0, then of chunk 1, ...): for an
+  // operator whose chunks become ready one after another, so that a tile
+  // popped early is one whose inputs come early, rather than a later chunk's
+  // tile that would hold its SM while it waits
+  auto gemm_by_chunk = [&](uint8_t op, int l, uint32_t nm, uint32_t nc, auto&& wait, auto&& rel) {
+    const uint32_t s = begin();
+    for (uint32_t ch = 0; ch < nc; ++ch)
+      for (uint32_t m = 0; m < nm; ++m) {
+        Instr in = bd_make(op, l, m, ch);
+        const Wait w = wait(ch);
+        bd_wait(in, w.bar, w.target, w.n);
+        in.rel_bar = rel(m);
+        q.push_back(in);
+      }
+    end(s);
+  };
   auto all = [](uint32_t bar, uint32_t target) { return [=](uint32_t) { return Wait{bar, target, 1}; }; };
   auto one = [](uint32_t bar) { return [=](uint32_t) { return bar; }; };
   auto norm = [&](uint8_t op, int l, uint32_t wbar, uint32_t wtarget, uint32_t rbar) {
@@ -224,7 +240,7 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
     }
     // O chunk ch: the kv groups of its 1024 attention-output columns, every
     // sequence of each
-    gemm(BD_O, l, bp.n_o_m, bp.c_q,
+    gemm_by_chunk(BD_O, l, bp.n_o_m, bp.c_q,
          [&](uint32_t ch) {
            return Wait{b.attn + l * nkv + ch * g_per_c, (uint32_t)max_batch, (uint16_t)g_per_c};
          },
@@ -238,7 +254,7 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
          },
          [&](uint32_t m) { return b.gu + l * bp.c_f + m / gu_per_c; });
     // down chunk ch: the gate/up row tiles of its 1024 SwiGLU columns
-    gemm(BD_DOWN, l, bp.n_down_m, bp.c_f,
+    gemm_by_chunk(BD_DOWN, l, bp.n_down_m, bp.c_f,
          [&](uint32_t ch) { return Wait{b.gu + l * bp.c_f + ch, gu_per_c, 1}; },
          [&](uint32_t m) { return b.down + l * bp.c_h + m / h_per_c; });
   }
