@@ -291,9 +291,10 @@ int mk_decode_step_slots(mk_plan *plan, const int32_t *tokens, const int32_t *po
  * mk_decode_step at position position[0] + s; step 0 reads token[0], every
  * later step the token the previous step chose: the index of the largest
  * logit (the smallest index among equal logits), computed on the device from
- * the LM-head tiles as they finish.  The queue runs n_steps times with barrier
- * generations per step; the layer-0 projection of step s + 1 waits on every
- * LM-head tile of step s.
+ * the LM-head tiles as they finish: each CTA keeps the running maximum of the
+ * LM-head tiles it finished in a step in one word of its own, and step s + 1
+ * reads the token once the CTAs' words account for every LM-head tile of
+ * step s.  The queue runs n_steps times with a tag per step.
  *   token       device int32 [1]      first input token
  *   position    device int32 [1]      tokens already cached (index of token)
  *   n_steps     1 .. 64               position[0] + n_steps <= max_ctx, else
@@ -301,9 +302,10 @@ int mk_decode_step_slots(mk_plan *plan, const int32_t *tokens, const int32_t *po
  *   out_tokens  device int32 [n_steps] out_tokens[s] = the token step s chose
  *   logits      device float [V]      the last step's logits
  * Cache slots position[0] .. position[0] + n_steps - 1 are written.  Batch-1
- * plans of the CUDA-core path with the batch-1 register kernel only (other
- * plans: MK_ERR_UNSUPPORTED); the caller's buffers follow mk_decode_step's
- * rules.  Asynchronous on `stream`. */
+ * plans of the CUDA-core path with the batch-1 register kernel and a
+ * vocabulary below 2^18 rows only (other plans: MK_ERR_UNSUPPORTED); the
+ * caller's buffers follow mk_decode_step's rules.  Asynchronous on
+ * `stream`. */
 int mk_decode_steps(mk_plan *plan, const int32_t *token, const int32_t *position, int n_steps,
                     void *kv_cache, int32_t *out_tokens, float *logits, void *stream);
 

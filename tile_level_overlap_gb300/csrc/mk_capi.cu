@@ -68,7 +68,7 @@ struct mk_plan {
   int32_t* d_pos = nullptr;
   float* d_logits = nullptr;
   uint32_t* d_ctl = nullptr;
-  uint8_t* d_msteps = nullptr;  // multi-step decode words (16 bytes per step)
+  uint8_t* d_msteps = nullptr;  // multi-step decode: one word per (step, CTA)
   KParams base{};
   int force_ctas = 0, trace = 0;
   int lm_separate = 0;  // MK_LM_SEPARATE: the LM head runs as its own kernel-per-op launch
@@ -419,7 +419,7 @@ int mk_plan_create_for_sms(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int
   const size_t o_log = bm.take(sizeof(float) * max_batch * c.vocab);
   // multi-step decode: per step the packed maximum (u64), the finished LM
   // tiles and the chosen token, cleared together before each such launch
-  const size_t o_msteps = bm.take(16 * MAX_DECODE_STEPS);
+  const size_t o_msteps = bm.take(sizeof(unsigned long long) * MAX_DECODE_STEPS * (size_t)p->max_ctas);
   p->scratch_bytes = bm.off;
   p->tagged_bytes = ds.tagged_end;
   if (cudaMalloc(&p->scratch, p->scratch_bytes) != cudaSuccess) {
@@ -604,14 +604,14 @@ int mk_decode_steps(mk_plan* p, const int32_t* token, const int32_t* position, i
   if (rc != MK_OK) return rc;
   if (!out_tokens || n_steps < 1 || n_steps > (int)MAX_DECODE_STEPS) return MK_ERR_INVALID_ARG;
   if (p->bd.on || !p->hp.fast_b1) return MK_ERR_UNSUPPORTED;
+  if (p->hp.cfg.vocab >= (1 << 18)) return MK_ERR_UNSUPPORTED;  // rows packed in 18 bits
   cudaStream_t st = (cudaStream_t)stream;
   const int ctas = p->force_ctas ? p->force_ctas : p->max_ctas;
   KParams k = step_params(p, token, position, 1, kv, logits);
   k.n_steps = (uint32_t)n_steps;
-  k.argmax = reinterpret_cast<unsigned long long*>(p->d_msteps);
-  k.lm_done = reinterpret_cast<uint32_t*>(p->d_msteps + 8 * MAX_DECODE_STEPS);
+  k.lm_slot = reinterpret_cast<unsigned long long*>(p->d_msteps);
   k.out_tokens = out_tokens;
-  MK_CUDA(cudaMemsetAsync(p->d_msteps, 0, 16 * MAX_DECODE_STEPS, st));
+  MK_CUDA(cudaMemsetAsync(p->d_msteps, 0, sizeof(unsigned long long) * (size_t)n_steps * ctas, st));
   return cuda_err(p->kv.mega_steps(k, ctas, st));
 }
 

@@ -224,8 +224,10 @@ struct KParams {
   // the LM-head tiles, the count of finished LM tiles, the chosen token.
   // n_steps = 1 and null pointers for a single step.
   uint32_t n_steps;
-  unsigned long long* argmax;  // [n_steps], zero before the launch
-  uint32_t* lm_done;           // [n_steps], zero before the launch
+  // [n_steps][gridDim.x], zero before the launch: each CTA's packed running
+  // greedy choice over the LM-head tiles it finished in that step (see
+  // lm_pack in mk_kernel.cuh)
+  unsigned long long* lm_slot;
   int32_t* out_tokens;         // [n_steps]
 };
 static_assert(sizeof(KParams) <= 4096, "kernel parameter block limit");

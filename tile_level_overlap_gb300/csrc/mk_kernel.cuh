@@ -60,7 +60,8 @@ static_assert(SmemLayout::total <= 227 * 1024, "shared memory budget");
 
 // F_STOP: set by a consumer that saw the abort word, read by the producer
 // before each pop (a shared-memory load instead of a global one).
-enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3, F_STOP = 4, F_SLOT_B = 5, F_ABORT_B = 6 };
+enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3, F_STOP = 4, F_SLOT_B = 5, F_ABORT_B = 6,
+            F_TOKEN = 7 };
 
 struct Sh {
   uint8_t* ring;
@@ -472,17 +473,90 @@ __device__ __forceinline__ float consumer_sum(float v, float* scratch) {
   return s;
 }
 
-// Token id of sequence b, validated: the caller's for step 0 of a launch, for
-// a later step of a multi-step launch the one the previous step chose (the
-// index in its packed maximum, read after its LM tiles all finished).
-__device__ __forceinline__ int token_of(const KParams& P, int b, uint32_t step = 0) {
-  int t = step == 0 ? P.tokens[b]
-                    : (int)(0xffffffffu - (uint32_t)__ldcg(P.argmax + (step - 1)));
+// Token id of sequence b from the caller, validated.
+__device__ __forceinline__ int token_of(const KParams& P, int b) {
+  int t = P.tokens[b];
   if (t < 0 || t >= P.V) {
     if (threadIdx.x == 0) set_error(P, MK_ERR_BOUNDS, (uint32_t)b);
     t = 0;
   }
   return t;
+}
+
+// ---------------------------------------------------------------- greedy choice (multi-step)
+// A logit and its vocabulary row packed so that the unsigned maximum picks the
+// largest logit and, among equal logits, the smallest row: the float's bits
+// mapped to an order-preserving word (bits 63..32), the row inverted (bits
+// 31..14, rows below 2^18), and bits 13..0 free for a count.  Each CTA's
+// finisher keeps the running maximum over the LM-head tiles it finished in a
+// step and stores it with their count as one word per (step, CTA): plain
+// stores to distinct words, no same-address atomics (8000 of those per step
+// queued on one L2 slice and slowed the LM head's weight stream).
+constexpr int LM_ROW_BITS = 18, LM_CNT_BITS = 14;
+constexpr unsigned long long LM_CNT_MASK = (1ull << LM_CNT_BITS) - 1;
+__device__ __forceinline__ unsigned long long lm_pack(float y, uint32_t row) {
+  const uint32_t u = __float_as_uint(y);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) |
+         ((unsigned long long)(((1u << LM_ROW_BITS) - 1u) - row) << LM_CNT_BITS);
+}
+__device__ __forceinline__ int lm_row(unsigned long long key) {
+  return (int)(((1u << LM_ROW_BITS) - 1u) - (uint32_t)((key >> LM_CNT_BITS) & ((1u << LM_ROW_BITS) - 1u)));
+}
+
+// The token step `step - 1` chose (all consumer threads call it): consumer
+// warp 0 polls the CTAs' words of that step until their counts add up to the
+// LM-head tile count, takes the largest packed maximum and hands the row to
+// the others through shared memory.  Validated like a caller's token.
+__device__ int ms_chosen_token(const KParams& P, const Sh& S, uint32_t step) {
+  const int t = threadIdx.x;
+  if (t < 32) {
+    const u64* w = reinterpret_cast<const u64*>(P.lm_slot) + (size_t)(step - 1) * gridDim.x;
+    const uint64_t t0 = globaltimer();
+    unsigned long long best = 0;
+    for (;;) {
+      unsigned long long m = 0;
+      uint32_t cnt = 0;
+      for (uint32_t c = (uint32_t)t; c < gridDim.x; c += 32) {
+        const unsigned long long v = ld_tagged(w + c);
+        cnt += (uint32_t)(v & LM_CNT_MASK);
+        m = (v & ~LM_CNT_MASK) > m ? (v & ~LM_CNT_MASK) : m;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        const unsigned long long om = __shfl_xor_sync(0xffffffffu, m, o);
+        m = om > m ? om : m;
+      }
+      best = m;
+      if (cnt >= P.n_lm_tiles) break;  // warp-uniform
+      // bounded: the lane-0 verdict decides for the whole warp
+      int verdict = 0;
+      if (t == 0) {
+        if (ld_volatile(&P.ctl[CTL_ABORT]) != 0u || S.flags[F_STOP] != 0u) verdict = 1;
+        else if (globaltimer() - t0 > P.wait_limit_ns) verdict = 2;
+      }
+      verdict = __shfl_sync(0xffffffffu, verdict, 0);
+      if (verdict) {
+        if (t == 0) {
+          if (verdict == 2) set_error(P, MK_ERR_TIMEOUT, 0xfffffff5u);
+          S.flags[F_STOP] = 1u;
+        }
+        break;
+      }
+      __nanosleep(32);
+    }
+    if (t == 0) {
+      int row = lm_row(best);
+      if (row < 0 || row >= P.V) {
+        if (S.flags[F_STOP] == 0u) set_error(P, MK_ERR_BOUNDS, 0u);
+        row = 0;
+      }
+      S.flags[F_TOKEN] = (uint32_t)row;
+    }
+  }
+  cbar();
+  return (int)S.flags[F_TOKEN];
 }
 
 // Activation source of a GEMV op (row-major [max_batch][K] tagged words), or
@@ -547,13 +621,10 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
   constexpr int K = M * FAST_K_UNIT;
   const u64* xs = gemv_x(P, in);
   // a later step of a multi-step launch starts from the token the previous
-  // step chose: the layer-0 projection waits until all of that step's LM-head
-  // tiles counted (their packed maximum is then final)
-  if (MS && !xs && step > 0)
-    poll_until(P, S, [&]() {
-      return (int32_t)(ld_acquire_gpu(P.lm_done + (step - 1)) - P.n_lm_tiles) >= 0;
-    }, 0xfffffff5u);
-  const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)token_of(P, 0, step) * P.H;
+  // step chose (every CTA's LM-head tiles of that step finished)
+  int tok = 0;
+  if (!xs) tok = (MS && step > 0) ? ms_chosen_token(P, S, step) : token_of(P, 0);
+  const uint16_t* emb_row = xs ? nullptr : P.embed + (size_t)tok * P.H;
   const uint16_t* gain = gemv_gain(P, in);
   uint4 gw[M];
   if (gain) {
@@ -633,11 +704,17 @@ __device__ __forceinline__ const u64* residual_src(const KParams& P, const Instr
   if (in.op == OP_DOWN) return P.resid + (size_t)(2 * l + 1) * bh + (size_t)b * P.H + row;
   return nullptr;
 }
-__device__ __forceinline__ u64 epilogue_prefetch(const KParams& P, const Instr& in, const GemvDesc& g,
-                                                 int t, uint32_t step = 0) {
-  if (in.op == OP_O && in.layer == 0 && t < g.rows * P.B) {
+template <bool MS>
+__device__ __forceinline__ u64 epilogue_prefetch(const KParams& P, const Sh& S, const Instr& in,
+                                                 const GemvDesc& g, int t, uint32_t step = 0) {
+  if (in.op == OP_O && in.layer == 0) {
+    // layer 0's residual input is the token's embedding row (all consumer
+    // threads take part when the token is a previous step's choice)
+    const int tok0 = (MS && step > 0) ? ms_chosen_token(P, S, step) : 0;
+    if (t >= g.rows * P.B) return 0ull;
     const int r = t / P.B, b = t % P.B;
-    return (u64)((uint32_t)P.embed[(size_t)token_of(P, b, step) * P.H + g.row0 + r] << 16);
+    const int tok = (MS && step > 0) ? tok0 : token_of(P, b);
+    return (u64)((uint32_t)P.embed[(size_t)tok * P.H + g.row0 + r] << 16);
   }
   const u64* src = residual_src(P, in, g, t);
   return src ? ld_tagged(src) : 0ull;
@@ -702,7 +779,7 @@ __device__ __forceinline__ void gemv_fast(const KParams& P, const Sh& S, const I
   if (P.trace && t == 0) trace_mark(P, ii, 11);
   // the residual input of the tile's outputs (O, down), loaded now so that its
   // latency hides behind the stages; the finisher takes it from the hand-off
-  const u64 pre_w = epilogue_prefetch(P, in, g, t, step);
+  const u64 pre_w = epilogue_prefetch<MS>(P, S, in, g, t, step);
   if (MS && t == 0) *hrec_step(S, hb) = step;  // the buffer is this tile's from here on
   float* redw = S.redw + hb * NW * RMAX;
   // the activations as packed (even, odd) column pairs for fma.rn.f32x2
@@ -1403,7 +1480,7 @@ __device__ void consumer(const KParams& P, const Sh& S) {
     } else {
       const GemvDesc g = gemv_desc(P, in);
       const Src src = instr_src(P, in);
-      const u64 pre_w = epilogue_prefetch(P, in, g, t);
+      const u64 pre_w = epilogue_prefetch<false>(P, S, in, g, t);
       gemv_generic(P, S, in, g, src, R, tag);
       if (P.trace && t == 0) trace_mark(P, i, 2);
       gemv_epilogue(P, S.red, in, g, epilogue_resolve(P, S, in, g, t, pre_w, tag), t, pub_tag(in, tag));
@@ -1426,34 +1503,52 @@ __device__ void consumer(const KParams& P, const Sh& S) {
   handoff_commit(S, R, hb);
 }
 
-// ---------------------------------------------------------------- greedy choice
-// A logit and its vocabulary row packed so that the unsigned maximum picks the
-// largest logit and, among equal logits, the smallest row: the float's bits
-// mapped to an order-preserving unsigned word, then the row inverted.
-__device__ __forceinline__ unsigned long long argmax_key(float y, uint32_t row) {
-  const uint32_t u = __float_as_uint(y);
-  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)o << 32) | (0xffffffffu - row);
-}
-
-// One LM-head tile of a multi-step launch (finisher warp, batch 1): fold the
-// tile's logits (lane r holds row r's in `y`) into the step's maximum, count
-// the tile; the last tile of the step stores the chosen token.  Runs before
-// the tile's logits are stored (only the launch's last step stores them), so
-// the counting atomic's release has no logits stores to wait for.
-__device__ void lm_tile_choose(const KParams& P, const GemvDesc& g, uint32_t step, int lane, float y) {
+// One LM-head tile of a multi-step launch (finisher warp, batch 1): the
+// tile's largest logit (lane r holds row r's in `y`) folded into this CTA's
+// running choice for the step, stored with the CTA's tile count.  Runs before
+// the tile's logits are stored (only the launch's last step stores them).
+__device__ __forceinline__ void lm_tile_choose(const KParams& P, const GemvDesc& g, uint32_t step, int lane,
+                                               float y, uint32_t& cur_step, unsigned long long& run) {
   unsigned long long key = 0;
-  if (lane < g.rows) key = argmax_key(y, (uint32_t)(g.row0 + lane));
+  if (lane < g.rows) key = lm_pack(y, (uint32_t)(g.row0 + lane));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
     key = other > key ? other : key;
   }
   if (lane == 0) {
-    atomicMax(P.argmax + step, key);
-    const uint32_t old = atom_add_acq_rel_gpu(P.lm_done + step, 1u);
-    if (old + 1u == P.n_lm_tiles)
-      P.out_tokens[step] = (int32_t)(0xffffffffu - (uint32_t)__ldcg(P.argmax + step));
+    if (step != cur_step) {  // a CTA meets the steps in order
+      cur_step = step;
+      run = 0;
+    }
+    const unsigned long long cnt = (run & LM_CNT_MASK) + 1;
+    const unsigned long long m = (run & ~LM_CNT_MASK) > key ? (run & ~LM_CNT_MASK) : key;
+    run = m | cnt;
+    unsigned long long* slot = P.lm_slot + (size_t)step * gridDim.x + blockIdx.x;
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(slot), "l"(run) : "memory");
+  }
+}
+
+// The tokens a multi-step launch chose, into out_tokens (the last CTA to
+// leave the launch, all its threads): every CTA's words are final by then.
+__device__ void lm_write_tokens(const KParams& P) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  for (uint32_t s = (uint32_t)w; s < P.n_steps; s += NTHREADS / 32) {
+    const unsigned long long* words = P.lm_slot + (size_t)s * gridDim.x;
+    unsigned long long m = 0;
+    for (uint32_t c = (uint32_t)lane; c < gridDim.x; c += 32) {
+      const unsigned long long v = __ldcg(words + c) & ~LM_CNT_MASK;
+      m = v > m ? v : m;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long om = __shfl_xor_sync(0xffffffffu, m, o);
+      m = om > m ? om : m;
+    }
+    if (lane == 0) {
+      const int row = lm_row(m);
+      P.out_tokens[s] = row < P.V ? row : 0;
+    }
   }
 }
 
@@ -1467,6 +1562,8 @@ template <bool MS>
 __device__ void finisher(const KParams& P, const Sh& S) {
   const int lane = threadIdx.x & 31;
   const uint32_t gen = S.flags[F_GEN];
+  uint32_t lm_step = 0xffffffffu;  // multi-step: the step of this CTA's running choice
+  unsigned long long lm_run = 0;
   for (uint32_t h = 0;; ++h) {
     const int hb = (int)(h & 1u);
     if (!mbar_wait(P, &S.hfull[hb], (h >> 1) & 1u)) break;
@@ -1491,7 +1588,7 @@ __device__ void finisher(const KParams& P, const Sh& S) {
     if (MS && in.op == OP_LM) {
       // greedy choice from the registers; the logits of steps before the
       // launch's last are not returned, so they are not stored
-      lm_tile_choose(P, g, step, lane, S.fin[lane * BMAX_CC]);
+      lm_tile_choose(P, g, step, lane, S.fin[lane * BMAX_CC], lm_step, lm_run);
       if (step + 1u == P.n_steps) gemv_epilogue(P, S.fin, in, g, pre, lane, 0u);
     } else {
       gemv_epilogue(P, S.fin, in, g, pre, lane, pub_tag(in, step_tag(P, gen, step)));
@@ -1505,6 +1602,9 @@ __device__ void finisher(const KParams& P, const Sh& S) {
       }
     }
   }
+  // this CTA's choice words are visible before the launch's last CTA reads
+  // them to write the chosen tokens
+  if (MS && lane == 0) __threadfence();
 }
 
 template <int MH, int MF, int AD, int AREP, bool MS>
@@ -1555,12 +1655,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
   if (t == 0 && P.mode == MODE_MEGA) {
     __threadfence();
     const uint32_t old = atomicAdd(&P.ctl[CTL_EXIT], 1u);
+    S.flags[F_LAST] = old == gridDim.x - 1 ? 1u : 0u;
     if (old == gridDim.x - 1) {
       // every CTA has left its loop: rewind the queue head for the next launch
       P.ctl[CTL_HEAD] = 0u;
       P.ctl[CTL_EXIT] = 0u;
       P.ctl[CTL_GEN] = S.flags[F_GEN] + (MS ? P.n_steps : 1u);
       __threadfence();
+    }
+  }
+  if (MS && P.mode == MODE_MEGA) {
+    __syncthreads();
+    if (S.flags[F_LAST]) {
+      __threadfence();
+      lm_write_tokens(P);
     }
   }
 }
