@@ -216,7 +216,7 @@ __device__ __forceinline__ BdGemm bd_gemm(const BdParams& P, const Instr& in) {
   const bool rb = in.op == BD_QKV || in.op == BD_GU;
   g.pslot = (rb ? P.part_b : 0u) + (uint32_t)(m * g.chunks);
   g.arr = (rb ? P.arrive_b : 0u) + (uint32_t)m;
-  const int kc = g.K / g.chunks;  // 1024 columns (gate/up 2048, QKV 512 where H allows), or all of K
+  const int kc = g.K / g.chunks;  // 1024 columns (gate/up 2048, QKV and O 512 where K allows), or all of K
   g.k0 = c * kc;
   g.nk = kc / BD_BK;
   return g;

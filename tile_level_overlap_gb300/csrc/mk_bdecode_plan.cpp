@@ -98,7 +98,9 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   bp.n_down_m = (uint32_t)(c.hidden / BD_M);
   bp.n_lm_m = (uint32_t)((c.vocab + BD_M - 1) / BD_M);
   bp.c_h = chunks(c.hidden);
-  bp.c_q = chunks(qd);
+  // O in 512-column chunks (one kv group of heads at rep 4, head_dim 128):
+  // each chunk waits on fewer attention groups and starts sooner
+  bp.c_q = qd > BD_KC ? (uint32_t)(qd / (BD_KC / 2)) : chunks(qd);
   bp.c_f = chunks(c.ffn);
   // gate/up reads the whole hidden row for each of its 224 (Llama-3-8B) row
   // tiles: 2048-column chunks halve its tile count (448 tiles, about three
@@ -111,7 +113,7 @@ int build_bdecode(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, 
   const int L = c.n_layers, nkv = c.n_kv_heads;
   // kv groups per 1024-column chunk of the attention output, gate/up row
   // tiles (64 SwiGLU columns each) per 1024-column chunk of the FFN
-  const uint32_t g_per_c = qd <= BD_KC ? (uint32_t)nkv : (uint32_t)(BD_KC / (rep * c.head_dim));
+  const uint32_t g_per_c = qd <= BD_KC ? (uint32_t)nkv : (uint32_t)((BD_KC / 2) / (rep * c.head_dim));
   const uint32_t gu_per_c = c.ffn <= BD_KC ? bp.n_gu_m : (uint32_t)(BD_KC / (BD_M / 2));
   // O / down row tiles (128 hidden features each) per 1024-feature chunk
   const uint32_t h_per_c = c.hidden <= BD_KC ? bp.n_down_m : (uint32_t)(BD_KC / BD_M);
