@@ -36,7 +36,7 @@ constexpr int PF_BN_GU = 128;  // gate/up features per tile (x2 matrices = N 256
 
 // Expression slot of prefill: S - a0 * PF_BM (> 0: the token block is live).
 constexpr int PXS_BLOCK_LIVE = 0;
-constexpr int PF_BLOCK_GROUP = 8;  // token blocks that share each weight tile in the queue order
+constexpr int PF_BLOCK_GROUP = 8;  // most token blocks that share each weight tile in the queue order
 constexpr int PXS_COUNT = 1;
 
 // Barrier sub-tensors, each [L][n_blocks]; normf and lm are [n_blocks].

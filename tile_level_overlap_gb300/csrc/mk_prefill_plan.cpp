@@ -86,13 +86,17 @@ int build_prefill(const mk_model_cfg& c, int max_ctx, PrefillPlan* out, std::str
   }
 
   std::vector<Instr>& q = pp.queue;
-  // GEMM tiles go group by group of PF_BLOCK_GROUP token blocks, and within a
-  // group weight tile by weight tile, so the blocks of a group read each
-  // weight tile from L2 right after the first of them brought it in.
+  // GEMM tiles go group by group of token blocks, and within a group weight
+  // tile by weight tile, so the blocks of a group read each weight tile from
+  // L2 right after the first of them brought it in.  Groups of up to
+  // PF_BLOCK_GROUP blocks, and at least two groups: the first group's blocks
+  // then run ahead into attention and the next layer while the second's are
+  // in their projections.
+  const int grp = std::max(1, std::min(PF_BLOCK_GROUP, NB / 2));
   auto grouped = [&](uint32_t nn, auto&& emit) {
-    for (int mg = 0; mg < NB; mg += PF_BLOCK_GROUP)
+    for (int mg = 0; mg < NB; mg += grp)
       for (uint32_t n = 0; n < nn; ++n)
-        for (int m = mg; m < NB && m < mg + PF_BLOCK_GROUP; ++m) emit(m, n);
+        for (int m = mg; m < NB && m < mg + grp; ++m) emit(m, n);
   };
   auto begin = [&]() { return (uint32_t)q.size(); };
   auto end = [&](uint32_t s) {
