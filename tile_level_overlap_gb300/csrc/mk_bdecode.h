@@ -50,6 +50,8 @@ constexpr int BD_KC = 1024;     // K chunk of a split-K tile
 constexpr int BD_RG = 8;        // sequences per RMSNorm instruction (one compute warp each)
 constexpr int BD_KEYS = 128;    // cached keys per attention block (K in one ring stage, V in the next)
 constexpr int BD_NSPLIT_MAX = 8;  // attention splits per (sequence, kv head), at most
+// a sequence of n keys uses min(nsplit, ceil(n / BD_SPLIT_KEYS)) of its splits
+constexpr int BD_SPLIT_KEYS = 512;
 
 // Barrier sub-tensors: one counter per layer and operator.
 struct BdBars {

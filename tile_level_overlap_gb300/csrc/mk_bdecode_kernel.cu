@@ -234,7 +234,11 @@ __device__ __forceinline__ BdAttn bd_attn(const BdParams& P, const BdSh& S, cons
   e.lo = e.hi = 0;
   if (e.live) {
     const int n = S.pos[b] + 1;
-    const int len = (n + P.nsplit - 1) / P.nsplit;
+    // splits of at least BD_SPLIT_KEYS keys (the later ones of a short
+    // sequence stay empty): a split count that depends only on the
+    // sequence's own length
+    const int nsp = min(P.nsplit, max(1, (n + BD_SPLIT_KEYS - 1) / BD_SPLIT_KEYS));
+    const int len = (n + nsp - 1) / nsp;
     e.lo = s * len < n ? s * len : n;
     e.hi = e.lo + len < n ? e.lo + len : n;
   }
