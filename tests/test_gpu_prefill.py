@@ -339,3 +339,25 @@ def test_prefill_chunks_mixed_with_decode(max_ctx):
         plan.close()
         del w
         torch.cuda.empty_cache()
+
+
+def test_prefill_chunks_rejects_bad_chunks():
+    """Chunks outside the plan are refused before any device work: a slot
+    past max_batch, a negative first position, an empty chunk, a chunk past
+    the context, a negative token offset."""
+    cfg = PF_SMALL
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(cfg, seed=12, device=dev)
+    plan = mk.Plan(cfg, w, 2, 300)
+    try:
+        kv = torch.zeros(synth.kv_cache_shape(cfg, 2, 300), dtype=torch.bfloat16, device=dev)
+        toks = torch.zeros(64, dtype=torch.int32, device=dev)
+        lg = torch.empty((1, cfg.vocab), device=dev)
+        for bad in [(2, 0, 4, 0), (0, -1, 4, 0), (0, 0, 0, 0), (0, 290, 20, 0), (0, 0, 4, -1)]:
+            with pytest.raises(mk.MkError):
+                plan.prefill_chunks(toks, [bad], kv, lg)
+        assert plan.status() == mk.MK_OK
+    finally:
+        plan.close()
+        del w
+        torch.cuda.empty_cache()

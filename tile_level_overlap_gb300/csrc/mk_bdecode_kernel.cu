@@ -32,6 +32,7 @@ constexpr int BD_STAGE = 32 * 1024;
 constexpr int BD_NSTAGE = 6;
 constexpr int BD_THREADS = 320;
 constexpr int BD_CBAR = 2;   // named barrier of the compute warps
+constexpr int BD_GBAR0 = 3;  // named barriers of the attention's two warp groups (3, 4)
 constexpr int BD_NC = 256;   // compute threads (8 warps: two per TMEM lane quarter)
 constexpr uint32_t BD_END = 0xffffffffu;
 constexpr uint32_t BD_W_BYTES = BD_M * BD_BK * 2;  // weight box(es) of a stage: 16 KB
@@ -41,8 +42,8 @@ struct BdSmem {
   static constexpr int ring = 0;
   static constexpr int scratch = ring + BD_NSTAGE * BD_STAGE;  // [128][BD_NMAX] f32
   static constexpr int qs = scratch + BD_M * BD_NMAX * 4;      // [4][128] f32
-  static constexpr int sc = qs + 4 * 128 * 4;                  // [4][BD_KEYS] f32
-  static constexpr int hs = sc + 4 * BD_KEYS * 4;              // [4] x {m, l, alpha} + inv norms [64]
+  static constexpr int sc = qs + 4 * 128 * 4;                  // [2 groups][4][BD_KEYS] f32
+  static constexpr int hs = sc + 2 * 4 * BD_KEYS * 4;          // [2 groups][16]: [4] x {m, l, alpha}; inv norms [64] from 16
   static constexpr int rinv = hs + (16 + 64) * 4;             // [BD_NMAX] 1 / rms per sequence
   static constexpr int bars = rinv + BD_NMAX * 4;
   // full[6] empty[6] ifull[8] iempty[8] accf[2] acce[2]
@@ -659,12 +660,19 @@ template <int D>
 __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr& in, const BdAttn& e,
                                   uint32_t stage_ctr, uint32_t idx) {
   const int tc = threadIdx.x - 64, lane = tc & 31, wc = tc >> 5;
+  // Two groups of four warps take the key blocks in turn (group 0 the even
+  // blocks, group 1 the odd ones), each with its own online-softmax state, so
+  // that one group's score / softmax / P V round trips overlap the other's;
+  // the two states are merged at the end in group order.
+  const int grp = wc >> 2, wg = wc & 3, tg = tc & 127;
   const int b = (int)in.a0, g = (int)in.a1, s = (int)in.a2, rep = P.rep;
   const int qd = P.nq * D;
   constexpr int DPL = D / 32;  // output columns per lane in P V
+  constexpr int KPW = BD_KEYS / 4;  // keys per warp of a group (scores and P V)
   const float scale = 1.0f / sqrtf((float)D);
-  float* sc = S.sc;  // [rep][BD_KEYS]
-  float* hs = S.hs;  // [rep] x {m, l, alpha}
+  float* sc = S.sc + grp * 4 * BD_KEYS;  // this group's [rep][BD_KEYS]
+  float* hs = S.hs + grp * 16;           // this group's [rep] x {m, l, alpha}
+  auto gbar = [&]() { named_bar(BD_GBAR0 + grp, BD_NC / 2); };
   // Scores on the tensor cores, 8 keys per m16n8k16 product: A rows r < rep
   // hold q of head r rounded to bf16, rows rep .. 2 rep - 1 the bf16 of its
   // remainder (hi + lo keeps q's float32 precision against the exact bf16
@@ -692,10 +700,10 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     af[ks][0] = hv[0] | (hv[1] << 16);
     af[ks][1] = hv[2] | (hv[3] << 16);
   }
-  if (tc < rep) {
-    hs[tc * 3 + 0] = -INFINITY;
-    hs[tc * 3 + 1] = 0.f;
-    hs[tc * 3 + 2] = 0.f;
+  if (tg < rep) {
+    hs[tg * 3 + 0] = -INFINITY;
+    hs[tg * 3 + 1] = 0.f;
+    hs[tg * 3 + 2] = 0.f;
   }
   float acc[4][DPL];
 #pragma unroll
@@ -704,19 +712,20 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     for (int k = 0; k < DPL; ++k) acc[h][k] = 0.f;
   cbar_bd();
   const int nblk = attn_blocks(e);
-  for (int j = 0; j < nblk; ++j) {
-    const int st = stage_ctr % BD_NSTAGE;
-    const int st_v = (stage_ctr + 1) % BD_NSTAGE;
-    bd_wait(P, &S.full[st], (stage_ctr / BD_NSTAGE) & 1u);
+  for (int j = grp; j < nblk; j += 2) {
+    const uint32_t cj = stage_ctr + 2u * (uint32_t)j;  // this block's K stage; V in the next
+    const int st = cj % BD_NSTAGE;
+    const int st_v = (cj + 1) % BD_NSTAGE;
+    bd_wait(P, &S.full[st], (cj / BD_NSTAGE) & 1u);
     if (j == 0 && tc == 0) bd_mark(P, idx, 9);
     const uint8_t* kt = S.ring + st * BD_STAGE;
     const uint8_t* vt = S.ring + st_v * BD_STAGE;
     const int base = e.lo + j * BD_KEYS;
-#pragma unroll
-    for (int nn = 0; nn < 2; ++nn) {
-      // keys 16 wc + 8 nn .. + 7: row gq of this product; the K block is
+#pragma unroll 2
+    for (int nn = 0; nn < KPW / 8; ++nn) {
+      // keys KPW wg + 8 nn .. + 7: row gq of this product; the K block is
       // [D / 64 halves][BD_KEYS][64] with 16-byte chunk c of key k at c ^ (k & 7)
-      const int kr = wc * 16 + nn * 8 + gq;
+      const int kr = wg * KPW + nn * 8 + gq;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int s2 = 0; s2 < KSTEPS / 2; ++s2) {
@@ -729,42 +738,42 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
       // row gq (hi) + row gq + rep (lo): lanes 4 rep apart
       const float s0 = c[0] + __shfl_xor_sync(0xffffffffu, c[0], 4 * rep);
       const float s1 = c[1] + __shfl_xor_sync(0xffffffffu, c[1], 4 * rep);
-      const int k = wc * 16 + nn * 8 + 2 * tq;
+      const int k = wg * KPW + nn * 8 + 2 * tq;
       if (gq < rep) {
         sc[gq * BD_KEYS + k] = base + k < e.hi ? s0 * scale : -INFINITY;
         sc[gq * BD_KEYS + k + 1] = base + k + 1 < e.hi ? s1 * scale : -INFINITY;
       }
     }
-    cbar_bd();
-    // online softmax: warp h owns head h
-    if (wc < rep) {
+    gbar();
+    // online softmax: warp h of the group owns head h
+    if (wg < rep) {
       float sv[BD_KEYS / 32];
 #pragma unroll
-      for (int u = 0; u < BD_KEYS / 32; ++u) sv[u] = sc[wc * BD_KEYS + lane + 32 * u];
+      for (int u = 0; u < BD_KEYS / 32; ++u) sv[u] = sc[wg * BD_KEYS + lane + 32 * u];
       float mx = sv[0];
 #pragma unroll
       for (int u = 1; u < BD_KEYS / 32; ++u) mx = fmaxf(mx, sv[u]);
       mx = warp_max(mx);
-      const float m_old = hs[wc * 3 + 0];
+      const float m_old = hs[wg * 3 + 0];
       const float m_new = fmaxf(m_old, mx);
       const float alpha = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
       float psum = 0.f;
 #pragma unroll
       for (int u = 0; u < BD_KEYS / 32; ++u) {
         const float pv = sv[u] == -INFINITY ? 0.f : expf(sv[u] - m_new);
-        sc[wc * BD_KEYS + lane + 32 * u] = pv;
+        sc[wg * BD_KEYS + lane + 32 * u] = pv;
         psum += pv;
       }
       const float ps = warp_sum(psum);
       __syncwarp();
       if (lane == 0) {
-        hs[wc * 3 + 0] = m_new;
-        hs[wc * 3 + 1] = hs[wc * 3 + 1] * alpha + ps;
-        hs[wc * 3 + 2] = alpha;
+        hs[wg * 3 + 0] = m_new;
+        hs[wg * 3 + 1] = hs[wg * 3 + 1] * alpha + ps;
+        hs[wg * 3 + 2] = alpha;
       }
     }
-    cbar_bd();
-    // P V over this warp's 16 keys (keys past the split are skipped, not
+    gbar();
+    // P V over this warp's KPW keys (keys past the split are skipped, not
     // weighted by zero: the cache rows there may hold anything)
     {
 #pragma unroll
@@ -774,10 +783,10 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
         for (int k = 0; k < DPL; ++k) acc[h][k] *= alpha;
       }
       const int col = lane * DPL, bx = col >> 6, cin = col & 63;
-      const int k0 = wc * (BD_KEYS / 8);
-      const int k1 = e.hi - base < k0 + BD_KEYS / 8 ? e.hi - base : k0 + BD_KEYS / 8;
+      const int k0 = wg * KPW;
+      const int k1 = e.hi - base < k0 + KPW ? e.hi - base : k0 + KPW;
       // the block's values are in the next stage
-      bd_wait(P, &S.full[st_v], ((stage_ctr + 1) / BD_NSTAGE) & 1u);
+      bd_wait(P, &S.full[st_v], ((cj + 1) / BD_NSTAGE) & 1u);
 #pragma unroll 4
       for (int k = k0; k < k1; ++k) {
         const uint8_t* vr = vt + bx * (BD_KEYS * 128) + k * 128 + ((((cin >> 3) ^ (k & 7))) << 4) + (cin & 7) * 2;
@@ -799,21 +808,31 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
         }
       }
     }
-    cbar_bd();  // every warp is done with the stages and the probabilities
-    if (tc == 0) {
+    gbar();  // the group is done with its stages and its probabilities
+    if (tg == 0) {
       mbar_arrive(&S.empty[st]);
       mbar_arrive(&S.empty[st_v]);
     }
-    stage_ctr += 2;
   }
+  stage_ctr += 2u * (uint32_t)nblk;
   if (tc == 0) bd_mark(P, idx, 10);
-  // add the eight warps' partial outputs (warp order), then the split's
-  // partial: o (unnormalised), max, sum per head
+  cbar_bd();
+  // merge: each group's output scaled to the split's maximum, then the eight
+  // warps' partial outputs added in warp order; the split's partial is
+  // o (unnormalised), max, sum per head
   float* red = S.scratch;  // [8 warps][4 heads][D]
 #pragma unroll
-  for (int h = 0; h < 4; ++h)
+  for (int h = 0; h < 4; ++h) {
+    float f = 0.f;
+    if (h < rep) {
+      const float m0 = S.hs[h * 3 + 0], m1 = S.hs[16 + h * 3 + 0];
+      const float M = fmaxf(m0, m1);
+      const float mg = grp == 0 ? m0 : m1;
+      f = mg == -INFINITY ? 0.f : expf(mg - M);
+    }
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) red[(wc * 4 + h) * D + lane * DPL + k] = acc[h][k];
+    for (int k = 0; k < DPL; ++k) red[(wc * 4 + h) * D + lane * DPL + k] = acc[h][k] * f;
+  }
   cbar_bd();
   float* part = P.apart + (((size_t)b * P.nkv + g) * P.nsplit + s) * rep * (D + 2);
   for (int t = tc; t < rep * D; t += BD_NC) {
@@ -824,8 +843,13 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
     part[h * (D + 2) + c] = o;
   }
   if (tc < rep) {
-    part[tc * (D + 2) + D] = hs[tc * 3 + 0];
-    part[tc * (D + 2) + D + 1] = hs[tc * 3 + 1];
+    const float m0 = S.hs[tc * 3 + 0], m1 = S.hs[16 + tc * 3 + 0];
+    const float l0 = S.hs[tc * 3 + 1], l1 = S.hs[16 + tc * 3 + 1];
+    const float M = fmaxf(m0, m1);
+    const float f0 = m0 == -INFINITY ? 0.f : expf(m0 - M);
+    const float f1 = m1 == -INFINITY ? 0.f : expf(m1 - M);
+    part[tc * (D + 2) + D] = M;
+    part[tc * (D + 2) + D + 1] = l0 * f0 + l1 * f1;
   }
   return stage_ctr;
 }
