@@ -228,6 +228,12 @@ struct BdAttn {
   int lo, hi;
   bool live;
 };
+// Splits a sequence of n keys uses: of at least BD_SPLIT_KEYS keys each, at
+// most nsplit (the later ones of a short sequence stay empty): a count that
+// depends only on the sequence's own length.
+__device__ __forceinline__ int attn_splits(const BdParams& P, int n) {
+  return min(P.nsplit, max(1, (n + BD_SPLIT_KEYS - 1) / BD_SPLIT_KEYS));
+}
 __device__ __forceinline__ BdAttn bd_attn(const BdParams& P, const BdSh& S, const Instr& in) {
   BdAttn e;
   const int b = (int)in.a0, s = (int)in.a2;
@@ -235,10 +241,7 @@ __device__ __forceinline__ BdAttn bd_attn(const BdParams& P, const BdSh& S, cons
   e.lo = e.hi = 0;
   if (e.live) {
     const int n = S.pos[b] + 1;
-    // splits of at least BD_SPLIT_KEYS keys (the later ones of a short
-    // sequence stay empty): a split count that depends only on the
-    // sequence's own length
-    const int nsp = min(P.nsplit, max(1, (n + BD_SPLIT_KEYS - 1) / BD_SPLIT_KEYS));
+    const int nsp = attn_splits(P, n);
     const int len = (n + nsp - 1) / nsp;
     e.lo = s * len < n ? s * len : n;
     e.hi = e.lo + len < n ? e.lo + len : n;
@@ -856,15 +859,15 @@ __device__ uint32_t bd_attn_split(const BdParams& P, const BdSh& S, const Instr&
 
 // Combine the splits of (b, g) in split order into the hi/lo planes of ao.
 template <int D>
-__device__ void bd_attn_combine(const BdParams& P, int b, int g) {
+__device__ void bd_attn_combine(const BdParams& P, int b, int g, int nsp) {
   const int tc = threadIdx.x - 64, rep = P.rep, qd = P.nq * D;
   const float* gp = P.apart + ((size_t)b * P.nkv + g) * P.nsplit * rep * (D + 2);
   for (int t = tc; t < rep * D; t += BD_NC) {
     const int h = t / D, c = t % D;
     float M = -INFINITY;
-    for (int s = 0; s < P.nsplit; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
+    for (int s = 0; s < nsp; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
     float Lsum = 0.f, O = 0.f;
-    for (int s = 0; s < P.nsplit; ++s) {
+    for (int s = 0; s < nsp; ++s) {
       const float* ps = gp + ((size_t)s * rep + h) * (D + 2);
       const float ms = __ldcg(ps + D);
       const float f = ms == -INFINITY ? 0.f : expf(ms - M);
@@ -958,26 +961,35 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
       if (!e.live) {
         release = in.a2 == 0;  // one release per dead (b, g) group
       } else {
-        if (tc == 0) {
-          S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
-          bd_mark(P, i, 2);
-        }
-        cbar_bd();
-        if (P.d == 128) stage_ctr = bd_attn_split<128>(P, S, in, e, stage_ctr, i);
-        else stage_ctr = bd_attn_split<64>(P, S, in, e, stage_ctr, i);
-        cbar_bd();
-        if (tc == 0) {
-          uint32_t* arr = P.arrive + P.n_arrive_gemm + (size_t)in.a0 * P.nkv + in.a1;
-          const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
-          const bool last = old == (uint32_t)(P.nsplit - 1);
-          if (last) *arr = 0u;
-          S.flags[BF_LAST] = last ? 1u : 0u;
-        }
-        cbar_bd();
-        release = S.flags[BF_LAST] != 0u;
-        if (release) {
-          if (P.d == 128) bd_attn_combine<128>(P, (int)in.a0, (int)in.a1);
-          else bd_attn_combine<64>(P, (int)in.a0, (int)in.a1);
+        // Splits s >= nsp (past the keys of a sequence whose length uses
+        // fewer splits) hold nothing and do nothing: no wait, no arrival.
+        // The arrival counter of (b, g) is shared by the layers, so only the
+        // splits that waited for this layer's queries may count on it (their
+        // wait orders them after the previous layer's combine).
+        const int nsp = attn_splits(P, S.pos[in.a0] + 1);
+        release = false;
+        if ((int)in.a2 < nsp) {
+          if (tc == 0) {
+            S.flags[BF_ABORT] = bd_wait_deps(P, in, gen, i) ? 0u : 1u;
+            bd_mark(P, i, 2);
+          }
+          cbar_bd();
+          if (P.d == 128) stage_ctr = bd_attn_split<128>(P, S, in, e, stage_ctr, i);
+          else stage_ctr = bd_attn_split<64>(P, S, in, e, stage_ctr, i);
+          cbar_bd();
+          if (tc == 0) {
+            uint32_t* arr = P.arrive + P.n_arrive_gemm + (size_t)in.a0 * P.nkv + in.a1;
+            const uint32_t old = atom_add_acq_rel_gpu(arr, 1u);
+            const bool last = old == (uint32_t)(nsp - 1);
+            if (last) *arr = 0u;
+            S.flags[BF_LAST] = last ? 1u : 0u;
+          }
+          cbar_bd();
+          release = S.flags[BF_LAST] != 0u;
+          if (release) {
+            if (P.d == 128) bd_attn_combine<128>(P, (int)in.a0, (int)in.a1, nsp);
+            else bd_attn_combine<64>(P, (int)in.a0, (int)in.a1, nsp);
+          }
         }
       }
     } else if (is_norm(in.op)) {
