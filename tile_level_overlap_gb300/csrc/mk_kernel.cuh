@@ -52,16 +52,18 @@ struct SmemLayout {
   static constexpr int islot = bars + n_mbar * 8;          // [NISLOT] x {u32 index, pad, Instr}
   static constexpr int islot_bytes = 48;
   static constexpr int hrec = islot + NISLOT * islot_bytes;  // [2] x {u32 index, pad, Instr}
-  static constexpr int flags = hrec + 2 * islot_bytes;     // [8] u32
-  static constexpr int layers = flags + 8 * 4;             // [MAX_LAYERS] LayerW
+  static constexpr int flags = hrec + 2 * islot_bytes;     // [16] u32
+  static constexpr int layers = flags + 16 * 4;             // [MAX_LAYERS] LayerW
   static constexpr int total = layers + MAX_LAYERS * (int)sizeof(LayerW);
 };
 static_assert(SmemLayout::total <= 227 * 1024, "shared memory budget");
 
 // F_STOP: set by a consumer that saw the abort word, read by the producer
 // before each pop (a shared-memory load instead of a global one).
+// F_POLL: set while the consumers poll a GEMV tile's input words; the
+// producer then keeps fewer copies in flight (PACE_POLL_STAGES).
 enum Flag { F_GEN = 0, F_ABORT = 1, F_LAST = 2, F_SLOT = 3, F_STOP = 4, F_SLOT_B = 5, F_ABORT_B = 6,
-            F_TOKEN = 7 };
+            F_TOKEN = 7, F_POLL = 8 };
 
 struct Sh {
   uint8_t* ring;
@@ -406,6 +408,18 @@ __device__ void producer(const KParams& P, const Sh& S) {
           break;
         }
         if (P.trace) blocked_ns += globaltimer() - tw;
+        {
+          // pace the stream: at most `lim` copies in flight, fewer while the
+          // consumers poll, so their reads do not queue behind a full ring
+          const uint32_t lim = S.flags[F_POLL] != 0u ? (uint32_t)PACE_POLL_STAGES : (uint32_t)PACE_STAGES;
+          if (stage_ctr >= lim) {
+            const uint32_t c2 = stage_ctr - lim;  // an earlier stage, not yet reissued
+            if (!mbar_wait(P, &S.full[c2 % NSTAGE], (c2 / NSTAGE) & 1u)) {
+              stuck = true;
+              break;
+            }
+          }
+        }
         mbar_arrive_expect_tx(&S.full[st], bytes);
         bulk_g2s(S.ring + (size_t)st * STAGE_BYTES, src.ptr[r] + (size_t)row * src.row_bytes, bytes,
                  &S.full[st], policy);
@@ -632,6 +646,7 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
     for (int j = 0; j < M; ++j) gw[j] = __ldg(reinterpret_cast<const uint4*>(gain + 8 * (t + NT * j)));
   }
   if (xs) {
+    if (t == 0) S.flags[F_POLL] = 1u;
     // every word of this thread's columns in flight at once, one tag check
     poll_until(P, S, [&]() {
       bool ok = true;
@@ -639,6 +654,7 @@ __device__ __forceinline__ void load_x_fast(const KParams& P, const Sh& S, const
       for (int j = 0; j < M; ++j) ok &= ld_tagged8(xs + 8 * (t + NT * j), tag, xr[j]);
       return ok;
     }, 0xfffffff2u);
+    if (t == 0) S.flags[F_POLL] = 0u;
   } else {
 #pragma unroll
     for (int j = 0; j < M; ++j) {
@@ -673,6 +689,7 @@ __device__ __forceinline__ void load_x_plain(const KParams& P, const Sh& S, cons
   // two halves, so that the tag halves of the words in flight do not push
   // the register-resident activations out
   constexpr int MA = (M + 1) / 2;
+  if (t == 0) S.flags[F_POLL] = 1u;
   poll_until(P, S, [&]() {
     bool ok = true;
 #pragma unroll
@@ -685,6 +702,7 @@ __device__ __forceinline__ void load_x_plain(const KParams& P, const Sh& S, cons
     for (int j = MA; j < M; ++j) ok &= ld_tagged8(xs + 8 * (t + NT * j), tag, xr[j]);
     return ok;
   }, 0xfffffff3u);
+  if (t == 0) S.flags[F_POLL] = 0u;
 }
 
 // The residual input of an O / down tile output element (thread t owns output
@@ -1630,6 +1648,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_interpreter(const __grid_const
     fence_proxy_async_smem();
     S.flags[F_GEN] = P.mode == MODE_MEGA ? ld_volatile(&P.ctl[CTL_GEN]) : 0u;
     S.flags[F_STOP] = 0u;
+    S.flags[F_POLL] = 0u;
   }
   {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(P.layers);

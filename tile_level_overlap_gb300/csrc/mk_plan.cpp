@@ -155,12 +155,14 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
 
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, F = c.ffn, nkv = c.n_kv_heads;
   if (n_sms <= 0) n_sms = DEFAULT_SMS;
-  // Rows per tile: ~128-256 KB of weights per instruction amortises the
-  // per-instruction handshakes; QKV tiles stay inside one head.
+  // Rows per tile: ~128-384 KB of weights per instruction amortises the
+  // per-instruction handshakes; QKV tiles stay inside one head.  The down
+  // projection takes the larger tiles (Llama-3-8B shape: two rounds of 14
+  // rows instead of three of 9; 2.828 -> 2.804 ms per step measured).
   hp.r_qkv = std::min(rows_for(128 << 10, (long)H * 2, RMAX), d);
   hp.r_o = rows_rounds(H, (long)qd * 2, 256 << 10, n_sms, RMAX);
   hp.r_gu = rows_rounds(F, (long)H * 4, 256 << 10, n_sms, RMAX / 2);
-  hp.r_down = rows_rounds(H, (long)F * 2, 256 << 10, n_sms, RMAX);
+  hp.r_down = rows_rounds(H, (long)F * 2, 384 << 10, n_sms, RMAX);
   hp.r_lm = rows_for(256 << 10, (long)H * 2, RMAX);
   hp.n_qkv_tiles = hp.qkv_rows / hp.r_qkv;
   hp.n_o_tiles = ceil_div(H, hp.r_o);

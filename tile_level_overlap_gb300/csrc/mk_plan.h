@@ -27,6 +27,13 @@ static_assert(8 * SPLIT_REGS_CONSUMER + 4 * SPLIT_REGS_SIDE == 12 * LAUNCH_REGS,
               "register split must add up to the launch's registers");
 constexpr int NSTAGE = 6;             // weight/KV ring stages
 constexpr int STAGE_BYTES = 32768;    // bytes per ring stage
+// Copies the producer keeps in flight (issued, not yet landed): PACE_STAGES
+// while the consumers compute, PACE_POLL_STAGES while they poll a tile's
+// input words.  A poll's read returns behind the copies its SM already has in
+// flight, so a full ring of requests (6 x 32 KB) delayed the first tile of
+// each all-to-all operator by a whole ring's worth of HBM time.
+constexpr int PACE_STAGES = 3;
+constexpr int PACE_POLL_STAGES = 2;
 constexpr int NISLOT = 8;             // instruction slots between producer and consumers
 constexpr int RMAX = 32;              // GEMV rows per tile (both matrices of a gate/up tile)
 constexpr int MAX_LAYERS = 64;        // layer pointer table kept in shared memory
