@@ -60,6 +60,16 @@ def _keys_per_split(head_dim):
     return 216 if head_dim >= 128 else 64
 
 
+def _combine_instructions(ns, rep, head_dim):
+    # extra combine instructions per (sequence, kv head) group (mk_plan.h): one
+    # slice per 20 KB of partial words at max_ctx, at most 8; with one slice
+    # the group's last split combines instead (no extra instruction)
+    if ns <= 1:
+        return 0
+    n = min(8, max(1, ns * rep * head_dim * 8 // 20480))
+    return n if n > 1 else 0
+
+
 @pytest.mark.parametrize("cfg,mb,mc", [
     (synth.TOY_1L, 1, 129), (synth.TOY_1L, 8, 129), (synth.TOY_1L, 3, 17),
     (synth.LLAMA32_1B, 1, 1025), (synth.LLAMA3_8B, 1, 4097),
@@ -81,8 +91,8 @@ def test_plan_check_valid(lib, cfg, mb, mc):
 def test_split_tiling_independent_of_max_batch(lib, cfg, mc):
     """The split-KV tiling is fixed keys per split (a model constant): the
     split count is ceil(max_ctx / KPS) whatever max_batch is, and only the
-    attention part of the queue grows with max_batch (one set of splits per
-    sequence slot)."""
+    attention part of the queue grows with max_batch (one set of splits, and
+    of combine slices when there are several splits, per sequence slot)."""
     kps = _keys_per_split(cfg.head_dim)
     counts = {}
     for mb in (1, 2, 3):
@@ -94,7 +104,9 @@ def test_split_tiling_independent_of_max_batch(lib, cfg, mc):
         counts[mb] = st.n_instr_decode
     for mb in counts:
         if mb > 1:
-            per_slot = cfg.n_layers * cfg.n_kv_heads * -(-mc // kps)
+            ns = -(-mc // kps)
+            rep = cfg.n_q_heads // cfg.n_kv_heads
+            per_slot = cfg.n_layers * cfg.n_kv_heads * (ns + _combine_instructions(ns, rep, cfg.head_dim))
             assert counts[mb] - counts[1] == (mb - 1) * per_slot
 
 

@@ -473,6 +473,7 @@ int mk_plan_create_for_sms(const mk_model_cfg* cfg, const mk_weight_ptrs* w, int
   k.attn_out = (u64*)(s + ds.o_attn);
   k.act = (u64*)(s + ds.o_act);
   k.kps = hp.kps;
+  k.comb_per = (hp.rep * c.head_dim + hp.n_comb - 1) / hp.n_comb;
   k.bars = (uint32_t*)(s + ds.o_bars);
   k.rope = (const float2*)(s + o_rope);
   k.ctl = p->d_ctl;

@@ -37,10 +37,13 @@ constexpr uint32_t NO_BAR = 0xffffffffu;
 constexpr uint8_t NO_EXPR = 0xff;
 
 // Instruction flags.
-// Decode attention: this split also combines every split of its (sequence, kv
-// head) group (the last split of the group in every topological order: it
-// waits on the others' partials).
+// Decode attention: this instruction combines the splits of its (sequence, kv
+// head) group (it follows every split of the group in every topological
+// order: it waits on their partials).  Alone, the flag marks a group's only
+// split, which combines its own partial; with IF_SLICE the instruction holds
+// no keys and combines output slice a2 (comb_per outputs each).
 constexpr uint8_t IF_COMBINE = 1;
+constexpr uint8_t IF_SLICE = 8;
 // The waited counter is cleared before every launch that runs this
 // instruction (it is not released by every launch): absolute target.
 constexpr uint8_t IF_ABS_TARGET = 2;
@@ -196,6 +199,7 @@ struct KParams {
   u64* attn_out;  // [L][max_batch][nq*d]
   u64* act;       // [L][max_batch][F]
   int kps;          // keys per attention split (a model constant)
+  int comb_per;     // outputs per combine slice (rep * d / the plan's slices, rounded up)
   uint32_t* bars;   // barrier tensor (host simulation; the kernel reads tags)
   const float2* rope;  // [max_ctx][d/2] (cos, sin)
   uint32_t* ctl;

@@ -214,6 +214,7 @@ __device__ __forceinline__ AttnExt attn_extent(const KParams& P, const Instr& in
     e.live = false;
     return e;
   }
+  if (in.flags & IF_SLICE) return e;  // a combine slice holds no keys
   e.lo = (int)x_eval(P.xw + XS_ATTN_LO * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step,
                      (int)in.a0, p0);
   e.hi = (int)x_eval(P.xw + XS_ATTN_HI * X_MAX_WORDS, in, P.B, P.S, P.positions, P.B, (int)step,
@@ -977,9 +978,11 @@ __device__ __forceinline__ float round_bf16(float x) {
 // norm is on, rotated, rounded to bf16 like every cached entry, written to the
 // cache by the split that holds slot pos).
 // Partial (max, sum, unnormalised o) per q head, stored as tagged words.  The
-// group's last split (IF_COMBINE) then polls every live split's partial and
-// combines them in split order; a split past the sequence's keys holds none
-// and does nothing unless it is that combining split.
+// group's combine instructions (IF_COMBINE | IF_SLICE, after every split in
+// the queue) then poll every live split's partial and combine them in split
+// order, each for its slice of the group's outputs; a group's only split
+// (IF_COMBINE alone) combines its own partial.  A split past the sequence's
+// keys holds none and does nothing.
 // (tracing) attention tile phase boundaries: trace words 8 (inputs loaded and
 // rotated), 9 (scores), 10 (softmax and P V), 11 (partials of the group ready,
 // combining split only)
@@ -1271,8 +1274,13 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
     // Combine the group's live splits (those holding keys: ceil((pos + 1) /
     // KPS) of them) in split order: weights f_s = exp(m_s - max_s m_s) per
     // head (staged in shared memory), o = sum_s f_s o_s / sum_s f_s l_s.  Every
-    // partial is a bounded poll on its tags.
+    // partial is a bounded poll on its tags.  A slice instruction combines
+    // outputs [o0, o1) of the group's rep * D (every slice reads all splits'
+    // max and sum, and only its own outputs' partial values).
     const int nl = (e.pos + P.kps) / P.kps;  // ceil((pos + 1) / KPS)
+    const int per = (in.flags & IF_SLICE) ? P.comb_per : rep * D;
+    const int o0 = (in.flags & IF_SLICE) ? split * per : 0;
+    const int o1 = o0 + per < rep * D ? o0 + per : rep * D;
     const u64* gp = P.part + (((size_t)l * P.max_batch + b) * P.nkv + g) * NS * rep * (D + 2);
     cbar();  // the scratch in xbuf is free (this split's own work is done)
     float* fw = S.xbuf;                 // [nl][rep] weights
@@ -1283,23 +1291,41 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
     // batch goes out once every split's (max, sum) is in, so its round trip
     // overlaps the weights' computation, and is checked afterwards.
     constexpr int NO = (REP * D + NT - 1) / NT;
-    constexpr int CB = NO <= 1 ? 16 : NO <= 2 ? 20 : 8;
+    constexpr int CB = NO <= 2 ? 20 : 8;
     float v[NO][CB];
+    // Every load of a batch is issued before any result is used: lanes past
+    // the slice or splits past nl read a valid word of the slice (clamped
+    // indices) whose value is then dropped, so no load sits behind a branch
+    // (predicated loads measured slower: the compiler no longer kept them in
+    // flight together); a warp whose outputs all lie past the slice issues
+    // none.
     auto load_batch = [&](int s0) {
       uint32_t bad = 0;
+      u64 wv[NO][CB];
 #pragma unroll
       for (int k = 0; k < NO; ++k) {
-        const int i = t + k * NT;
-        const u64* pc = gp + (size_t)(i / D) * (D + 2) + (i % D);
+        const int i = o0 + t + k * NT;
+        const int ic = i < o1 ? i : o1 - 1;
+        const u64* pc = gp + (size_t)(ic / D) * (D + 2) + (ic % D);
+        if (o0 + (t & ~31) + k * NT < o1) {  // warp-uniform
+#pragma unroll
+          for (int u = 0; u < CB; ++u) {
+            const int sc = s0 + u < nl ? s0 + u : nl - 1;
+            wv[k][u] = ld_tagged(pc + (size_t)sc * rep * (D + 2));
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < CB; ++u) wv[k][u] = 0ull;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NO; ++k) {
+        const int i = o0 + t + k * NT;
 #pragma unroll
         for (int u = 0; u < CB; ++u) {
-          if (i < rep * D && s0 + u < nl) {
-            const u64 wv = ld_tagged(pc + (size_t)(s0 + u) * rep * (D + 2));
-            v[k][u] = tag_val(wv);
-            bad |= tag_of(wv) ^ tag;
-          } else {
-            v[k][u] = 0.f;
-          }
+          const bool use = i < o1 && s0 + u < nl;
+          v[k][u] = use ? tag_val(wv[k][u]) : 0.f;
+          bad |= use ? (tag_of(wv[k][u]) ^ tag) : 0u;
         }
       }
       return bad;
@@ -1341,7 +1367,7 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
         poll_until(P, S, [&]() { return load_batch(s0) == 0u || tag == 0u; }, ii);
 #pragma unroll
       for (int k = 0; k < NO; ++k) {
-        const int h = (t + k * NT) / D;
+        const int h = (o0 + t + k * NT) / D;
 #pragma unroll
         for (int u = 0; u < CB; ++u)
           if (s0 + u < nl) O[k] = fmaf(v[k][u], fw[(s0 + u) * rep + h], O[k]);
@@ -1349,8 +1375,8 @@ __device__ __forceinline__ void attn_tile(const KParams& P, const Sh& S, const I
     }
 #pragma unroll
     for (int k = 0; k < NO; ++k) {
-      const int i = t + k * NT;
-      if (i < rep * D) {
+      const int i = o0 + t + k * NT;
+      if (i < o1) {
         const int h = i / D, c = i % D;
         st_tagged(P.attn_out + ((size_t)l * P.max_batch + b) * qd + (size_t)(g * rep + h) * D + c,
                   O[k] * linv[h], ptag);

@@ -214,6 +214,7 @@ extern "C" int mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_p
   k.attn_out = (u64*)(s + ds.o_attn);
   k.act = (u64*)(s + ds.o_act);
   k.kps = hp.kps;
+  k.comb_per = (hp.rep * c.head_dim + hp.n_comb - 1) / hp.n_comb;
   k.bars = (uint32_t*)(s + ds.o_bars);
   k.rope = (const float2*)(s + o_rope);
   k.ctl = (uint32_t*)(s + ds.o_ctl);

@@ -181,6 +181,7 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
   if (hp.kps > hp.split_max) return bad(MK_ERR_UNSUPPORTED, "keys per split above the score buffer");
   const int ns = std::max(1, (int)ceil_div(max_ctx, hp.kps));
   hp.n_splits = ns;
+  hp.n_comb = combine_slices(ns, rep, d);
   if (hp.n_splits > 0xffff || 2L * hp.n_splits * rep + rep > XBUF_FLOATS)
     return bad(MK_ERR_UNSUPPORTED, "max_ctx needs more split-KV partitions than the combine buffer holds");
 
@@ -235,39 +236,63 @@ int build_plan(const mk_model_cfg& c, int max_batch, int max_ctx, int n_sms, Hos
     }
     range_end(b0);
     b0 = range_begin();
-    // The last split of each (sequence, kv head) group also combines the
-    // group's partials: it waits on the other splits (its own inputs are
-    // ready once they are, since they waited on the same QKV tiles).  The
-    // combining splits of a layer follow all its other splits, so the
-    // kernel-per-operator runner launches them as their own operator.
+    // Split-KV attention, then the combine of each (sequence, kv head)
+    // group.  Sliced (n_comb > 1): every split is an ordinary split and
+    // n_comb combine instructions per group each wait on the group's splits
+    // and combine a slice of its outputs.  Otherwise the group's last split
+    // also combines the group (it waits on the other splits; a group's only
+    // split combines its own partial).  Each group's last split follows the
+    // layer's other splits (it holds keys only for contexts near max_ctx, and
+    // an empty split among the others would push a split that holds keys into
+    // a later round), and the combining instructions of a layer follow all its
+    // splits, so the kernel-per-operator runner launches them as their own
+    // operator.
+    const bool sliced = ns > 1 && hp.n_comb > 1;
+    const uint32_t n_comb = sliced ? (uint32_t)hp.n_comb : 1u;
+    auto split_instr = [&](int b, int g, int s) {
+      Instr in = make(OP_ATTN, l, b, g, (uint16_t)s);
+      in.x_lo = XS_ATTN_LO;
+      in.x_hi = XS_ATTN_HI;
+      const uint32_t grp = ((uint32_t)l * max_batch + b) * nkv + g;
+      if (s + 1 < ns || sliced) {
+        set_wait(in, bl.qkv + l * nkv + g, per_group);
+        in.rel_bar = bl.split + grp;
+      } else {
+        in.flags = IF_COMBINE;
+        if (ns > 1) set_wait(in, bl.split + grp, (uint32_t)(ns - 1));
+        else set_wait(in, bl.qkv + l * nkv + g, per_group);
+        in.rel_bar = bl.attn + l;
+      }
+      q.push_back(in);
+    };
     for (int b = 0; b < max_batch; ++b)
       for (int g = 0; g < nkv; ++g)
-        for (int s = 0; s + 1 < ns; ++s) {
-          Instr in = make(OP_ATTN, l, b, g, (uint16_t)s);
-          in.x_lo = XS_ATTN_LO;
-          in.x_hi = XS_ATTN_HI;
-          set_wait(in, bl.qkv + l * nkv + g, per_group);
-          in.rel_bar = bl.split + ((uint32_t)l * max_batch + b) * nkv + g;
-          q.push_back(in);
-        }
+        for (int s = 0; s + 1 < ns; ++s) split_instr(b, g, s);
+    if (sliced) {
+      for (int b = 0; b < max_batch; ++b)
+        for (int g = 0; g < nkv; ++g) split_instr(b, g, ns - 1);
+    }
     range_end(b0);
     b0 = range_begin();
     for (int b = 0; b < max_batch; ++b)
       for (int g = 0; g < nkv; ++g) {
-        Instr in = make(OP_ATTN, l, b, g, (uint16_t)(ns - 1));
-        in.x_lo = XS_ATTN_LO;
-        in.x_hi = XS_ATTN_HI;
-        in.flags = IF_COMBINE;
-        if (ns > 1) set_wait(in, bl.split + ((uint32_t)l * max_batch + b) * nkv + g, (uint32_t)(ns - 1));
-        else set_wait(in, bl.qkv + l * nkv + g, per_group);
-        in.rel_bar = bl.attn + l;
-        q.push_back(in);
+        if (!sliced) {
+          split_instr(b, g, ns - 1);
+          continue;
+        }
+        for (int c = 0; c < hp.n_comb; ++c) {
+          Instr in = make(OP_ATTN, l, b, g, (uint16_t)c);
+          in.flags = IF_COMBINE | IF_SLICE;
+          set_wait(in, bl.split + ((uint32_t)l * max_batch + b) * nkv + g, (uint32_t)ns);
+          in.rel_bar = bl.attn + l;
+          q.push_back(in);
+        }
       }
     range_end(b0);
     b0 = range_begin();
     for (int r = 0; r < H; r += hp.r_o) {
       Instr in = make(OP_O, l, r, std::min(hp.r_o, H - r));
-      set_wait(in, bl.attn + l, (uint32_t)(max_batch * nkv));
+      set_wait(in, bl.attn + l, (uint32_t)(max_batch * nkv) * n_comb);
       in.rel_bar = bl.o + l;
       q.push_back(in);
     }
