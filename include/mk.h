@@ -357,7 +357,8 @@ int mk_debug_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int
  * stages, then for GEMV tiles: last stage consumed (batch-1 tiles), finisher
  * took it (batch-1 tiles), instruction reached every consumer warp, hand-off
  * buffer free (batch-1 tiles); for attention tiles: inputs rotated, scores
- * done, softmax and P V done, split arrival counted; then consumer loop top
+ * done, partial stored, and for combining instructions every split's max and
+ * sum in; then consumer loop top
  * before the instruction was taken, and for batch-1 GEMV tiles: consumer warp
  * 7 reached the hand-off, finisher added the partial sums, consumer warp 0
  * finished the hand-off}.  Tensor-core batched
