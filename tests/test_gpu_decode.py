@@ -325,6 +325,31 @@ def test_llama3_8b_decode_full_size():
         m.close()
 
 
+@pytest.mark.parametrize("pos", [4096, 700, 0])
+def test_attention_combine_slices_all_some_and_one_split(pos):
+    """The Llama-3-8B head layout (head_dim 128, 4 q heads per kv head, 2
+    layers) with a 4097-token cache: the plan combines each group's splits
+    in slices (several combine instructions per group, queued after every
+    split).  A sequence that uses all 19 splits, 4 of them or 1 matches the
+    oracle, and the launch on 7 CTAs with a permuted queue and the
+    kernel-per-operator runner give the same bits."""
+    cfg = synth.LLAMA3_8B.replace(n_layers=2)
+    m = Model(cfg, 1, 4097, seed=9)
+    try:
+        tokens = synth.make_tokens(1, cfg.vocab, seed=pos).numpy()
+        kv_before = synth.bf16_bits(m.kv)
+        got = m.step(tokens, [pos])
+        ref, _, _ = m.oracle(tokens, [pos], kv_before)
+        _assert_rows_close(got, ref)
+        # repeating the step rewrites the same cache entries
+        m.plan.set_debug(force_ctas=7, queue_perm_seed=3)
+        np.testing.assert_array_equal(m.step(tokens, [pos]), got)
+        m.plan.set_debug()
+        np.testing.assert_array_equal(m.step(tokens, [pos], per_op=True), got)
+    finally:
+        m.close()
+
+
 def test_multi_step_greedy_decode():
     """mk_decode_steps: n greedy steps in one launch equal n single steps fed
     the argmax of each step's logits (same tile arithmetic: bit-identical
