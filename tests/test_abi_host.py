@@ -87,7 +87,8 @@ def test_plan_check_valid(lib, cfg, mb, mc):
 
 
 @pytest.mark.parametrize("cfg,mc", [(synth.TOY_1L, 129), (synth.LLAMA32_1B, 1025),
-                                    (synth.LLAMA3_8B, 4097), (synth.TOY_1L, 2000)])
+                                    (synth.LLAMA3_8B, 4097), (synth.TOY_1L, 2000),
+                                    (synth.TOY_1L, 4000)])
 def test_split_tiling_independent_of_max_batch(lib, cfg, mc):
     """The split-KV tiling is fixed keys per split (a model constant): the
     split count is ceil(max_ctx / KPS) whatever max_batch is, and only the
@@ -115,6 +116,9 @@ def test_plan_check_random_topological_orders(lib, seed):
     rc, _ = mk.plan_check(synth.LLAMA32_1B.replace(n_layers=3), 1, 1025, seed=seed)
     assert rc == mk.MK_OK
     rc, _ = mk.plan_check(synth.TOY_1L, 4, 65, seed=seed)
+    assert rc == mk.MK_OK
+    # a cache long enough for the combine in slices (63 splits, 3 slices)
+    rc, _ = mk.plan_check(synth.TOY_1L, 3, 4000, seed=seed)
     assert rc == mk.MK_OK
 
 
