@@ -325,6 +325,28 @@ def test_llama3_8b_decode_full_size():
         m.close()
 
 
+def test_toy_combine_slices_batch_ragged():
+    """A 4000-token cache on the toy shape: 63 splits per (sequence, kv
+    head), combined in 3 slices.  Three sequences of one batch using all,
+    some and one of the splits match the oracle, and the launch on 5 CTAs
+    with a permuted queue and the kernel-per-operator graph give the same
+    bits."""
+    m = Model(synth.TOY_1L, 3, 4000, seed=4)
+    try:
+        tokens = synth.make_tokens(3, m.cfg.vocab, seed=41).numpy()
+        positions = [3999, 100, 0]
+        kv_before = synth.bf16_bits(m.kv)
+        got = m.step(tokens, positions)
+        ref, _, _ = m.oracle(tokens, positions, kv_before)
+        _assert_rows_close(got, ref)
+        m.plan.set_debug(force_ctas=5, queue_perm_seed=2)
+        np.testing.assert_array_equal(m.step(tokens, positions), got)
+        m.plan.set_debug()
+        np.testing.assert_array_equal(m.step(tokens, positions, per_op=True, graph=True), got)
+    finally:
+        m.close()
+
+
 @pytest.mark.parametrize("pos", [4096, 700, 0])
 def test_attention_combine_slices_all_some_and_one_split(pos):
     """The Llama-3-8B head layout (head_dim 128, 4 q heads per kv head, 2
