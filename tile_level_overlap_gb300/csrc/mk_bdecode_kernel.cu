@@ -955,10 +955,25 @@ __device__ void bd_compute(const BdParams& P, const BdSh& S, uint32_t tbase) {
           const float* base = P.part + (size_t)gm.pslot * BD_NMAX * BD_M;
 #pragma unroll
           for (int k = 0; k < 16; ++k) y[k] = 0.f;
-          for (int c = 0; c < gm.chunks; ++c)
+          // the chunks' partials CG chunks at a time, every load of a group
+          // issued before any is added (chunk indices past the last clamped
+          // to it, their values dropped): one round trip per group instead
+          // of one per chunk; the adds stay in chunk order
+          constexpr int CG = 4;
+          for (int c0 = 0; c0 < gm.chunks; c0 += CG) {
+            float v[CG][16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              y[k] += __ldcg(base + ((size_t)c * BD_NMAX + b0 + k) * BD_M + row);
+            for (int u = 0; u < CG; ++u) {
+              const int c = c0 + u < gm.chunks ? c0 + u : gm.chunks - 1;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) v[u][k] = __ldcg(base + ((size_t)c * BD_NMAX + b0 + k) * BD_M + row);
+            }
+#pragma unroll
+            for (int u = 0; u < CG; ++u)
+              if (c0 + u < gm.chunks)
+#pragma unroll
+                for (int k = 0; k < 16; ++k) y[k] += v[u][k];
+          }
         }
       }
       if (release) bd_epilogue(P, S, in, row, b0, y);
