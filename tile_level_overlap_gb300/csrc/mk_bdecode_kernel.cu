@@ -870,10 +870,35 @@ __device__ void bd_attn_combine(const BdParams& P, int b, int g, int nsp) {
   const float* gp = P.apart + ((size_t)b * P.nkv + g) * P.nsplit * rep * (D + 2);
   for (int t = tc; t < rep * D; t += BD_NC) {
     const int h = t / D, c = t % D;
+    // the first W splits' (max, sum, o) words loaded together before any is
+    // used (split indices clamped to a valid split, whose values are
+    // dropped): one round trip instead of one per split; splits from W on
+    // follow in a loop
+    constexpr int W = 4;
+    float mv[W], lv[W], ov[W];
+#pragma unroll
+    for (int s = 0; s < W; ++s) {
+      const int sc = s < nsp ? s : nsp - 1;
+      const float* ps = gp + ((size_t)sc * rep + h) * (D + 2);
+      mv[s] = __ldcg(ps + D);
+      lv[s] = __ldcg(ps + D + 1);
+      ov[s] = __ldcg(ps + c);
+    }
     float M = -INFINITY;
-    for (int s = 0; s < nsp; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
+#pragma unroll
+    for (int s = 0; s < W; ++s)
+      if (s < nsp) M = fmaxf(M, mv[s]);
+    for (int s = W; s < nsp; ++s) M = fmaxf(M, __ldcg(gp + ((size_t)s * rep + h) * (D + 2) + D));
     float Lsum = 0.f, O = 0.f;
-    for (int s = 0; s < nsp; ++s) {
+#pragma unroll
+    for (int s = 0; s < W; ++s) {
+      if (s < nsp) {
+        const float f = mv[s] == -INFINITY ? 0.f : expf(mv[s] - M);
+        Lsum = fmaf(lv[s], f, Lsum);
+        O = fmaf(ov[s], f, O);
+      }
+    }
+    for (int s = W; s < nsp; ++s) {
       const float* ps = gp + ((size_t)s * rep + h) * (D + 2);
       const float ms = __ldcg(ps + D);
       const float f = ms == -INFINITY ? 0.f : expf(ms - M);
