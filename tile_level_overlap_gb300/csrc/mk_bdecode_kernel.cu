@@ -541,20 +541,25 @@ __device__ void bd_epilogue(const BdParams& P, const BdSh& S, const Instr& in, i
       float* dst = in.op == BD_O ? P.xa : P.xb;
       const float* res = in.op == BD_O ? P.xb : P.xa;
       float x[16];
+      // every residual input loaded before any is used (sequences past B
+      // read sequence 0's word, dropped)
+      float r[16];
+      if (in.op == BD_O && l == 0) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int b = b0 + k;
+          int tok = b < B ? S.tok[b] : 0;
+          if (tok < 0 || tok >= P.V) tok = 0;  // reported by the layer-0 norm
+          r[k] = bfw(P.embed + (size_t)tok * H, f);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) r[k] = __ldcg(res + (size_t)(b0 + k < B ? b0 + k : 0) * H + f);
+      }
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int b = b0 + k;
-        float r = 0.f;
-        if (b < B) {
-          if (in.op == BD_O && l == 0) {
-            int tok = S.tok[b];
-            if (tok < 0 || tok >= P.V) tok = 0;  // reported by the layer-0 norm
-            r = bfw(P.embed + (size_t)tok * H, f);
-          } else {
-            r = __ldcg(res + (size_t)b * H + f);
-          }
-        }
-        x[k] = b < B ? r + y[k] : 0.f;
+        x[k] = b < B ? r[k] + y[k] : 0.f;
         if (b < B) dst[(size_t)b * H + f] = x[k];
       }
       // the next norm's input: the FFN norm after O, the next layer's
